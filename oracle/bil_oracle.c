@@ -1,0 +1,354 @@
+/*
+ * Selected-token log-probability: the CPU oracle.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test-suite, the smoke check
+ * and the benchmark's CPU-baseline leg load this library.  It shares no code,
+ * header, table or constant with the CUDA library; the two meet only in the
+ * seeded input bytes they are both given.
+ *
+ * Plain, slow and in float64 throughout.  Each function states the passage of
+ * the pages it follows:
+ *
+ *  - "Batch-Invariant LogP" operator page, section "Reference Semantics":
+ *      out[row] = log_softmax(float(logits[row, :]))[target[row]]
+ *      ignored rows (target == ignore_index): out = 0, grad row = 0
+ *      a non-ignored target outside [0, V) is invalid.
+ *  - same page, section "Tensor Parallel", steps 1-6: per fixed vocab tile t a
+ *    (max m_t, sum-exp s_t) partial; all tiles merged in one fixed order as
+ *    LSE = M + log(sum_t s_t * exp(m_t - M)), M = max_t m_t; the target logit
+ *    is copied from the tile that owns it; logp = target_logit - LSE.
+ *  - same page, section "Batch-Invariance": the backward is computed per row
+ *    tile from the saved per-row LSE:  d[c] = g * (onehot(target)[c] - p[c]),
+ *    p[c] = exp(x[c] - LSE).
+ *
+ * The tile method is an exact rewrite of log-softmax in real arithmetic
+ * ("RL-Kernel x vime x AMD: Achieving Bitwise Consistency Between Training
+ * and Rollout", section "The Shared Normalization Structure of Attention and
+ * Logprob": the merged result depends only on the set of all blocks), so the
+ * forward and backward here compute the plain definition over the whole row;
+ * the tile-partial and merge entry points exist so that the GPU's split mode
+ * can be checked piece by piece.
+ *
+ * Readings taken where the pages are silent (each is listed with its reason in
+ * the design notes):
+ *  - ignored rows: lse = 0 and their logits are never read;
+ *  - out-of-range target on an active row: logp = NaN and the row is counted
+ *    as an error (the return value), nothing outside the row is read;
+ *  - a row whose entries are all -inf: LSE = -inf, logp = NaN;
+ *  - NaN anywhere in a row makes that row's LSE and logp NaN.
+ *
+ * Element types: 0 = float32, 1 = bfloat16, 2 = float16.  Every input value
+ * is widened to double exactly.
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -shared -fPIC (no -ffast-math: the order of
+ * every sum below is the order written).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+#define ORACLE_F16 2
+
+/* ---- exact widening of one stored element to double ---------------------- */
+
+static double from_bf16_bits(uint16_t h) {
+    /* bfloat16 is the upper half of an IEEE binary32 word. */
+    uint32_t w = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+static double from_f16_bits(uint16_t h) {
+    /* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -24); /* subnormal: frac * 2^-14 * 2^-10 */
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(frac + 1024), expo - 25); /* 1.frac * 2^(expo-15) */
+    }
+    return sign ? -v : v;
+}
+
+static double load(const void *base, int dtype, int64_t row, int64_t ld, int64_t col) {
+    int64_t i = row * ld + col;
+    if (dtype == ORACLE_BF16) {
+        return from_bf16_bits(((const uint16_t *)base)[i]);
+    }
+    if (dtype == ORACLE_F16) {
+        return from_f16_bits(((const uint16_t *)base)[i]);
+    }
+    return (double)((const float *)base)[i];
+}
+
+/* ---- log-sum-exp over columns [c0, c1) of one row --------------------------
+ * The definition log(sum_c exp(x_c)), evaluated with the usual shift by the
+ * maximum so that nothing overflows.  Returns the maximum in *m_out and the
+ * shifted sum sum_c exp(x_c - max) in *s_out.  A range whose entries are all
+ * -inf has max -inf and sum 0.  A NaN entry never wins the max (comparisons
+ * with NaN are false) and makes the sum NaN. */
+static void max_and_sumexp(const void *base, int dtype, int64_t row, int64_t ld,
+                           int64_t c0, int64_t c1, double *m_out, double *s_out) {
+    double m = -INFINITY;
+    for (int64_t c = c0; c < c1; ++c) {
+        double x = load(base, dtype, row, ld, c);
+        if (x > m) {
+            m = x;
+        }
+    }
+    double s = 0.0;
+    if (m != -INFINITY) {
+        for (int64_t c = c0; c < c1; ++c) {
+#ifdef BIL_ORACLE_MUTANT_SUM_SKIPS_FIRST
+            if (c == c0) continue;
+#endif
+            double x = load(base, dtype, row, ld, c);
+#ifdef BIL_ORACLE_MUTANT_NO_SHIFT_SIGN
+            s += exp(m - x);
+#else
+            s += exp(x - m);
+#endif
+        }
+    } else {
+        /* every entry is -inf (or the range is empty of finite values);
+         * a NaN entry still poisons the sum */
+        for (int64_t c = c0; c < c1; ++c) {
+            if (isnan(load(base, dtype, row, ld, c))) {
+                s = NAN;
+            }
+        }
+    }
+    *m_out = m;
+    *s_out = s;
+}
+
+static double row_lse(const void *base, int dtype, int64_t row, int64_t ld, int64_t vocab) {
+    double m, s;
+    max_and_sumexp(base, dtype, row, ld, 0, vocab, &m, &s);
+    if (m == -INFINITY && s == 0.0) {
+        return -INFINITY;
+    }
+#ifdef BIL_ORACLE_MUTANT_LSE_DROPS_MAX
+    return log(s);
+#else
+    return m + log(s);
+#endif
+}
+
+int bil_oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---- forward -----------------------------------------------------------------
+ * "Reference Semantics": logp[r] = x[r, t_r] - LSE(x[r, :]) for active rows,
+ * 0 for ignored rows.  lse[r] receives the row's LSE (0 for ignored rows).
+ * Returns the number of active rows whose target lies outside [0, vocab);
+ * those rows get logp = NaN. */
+int64_t bil_oracle_logp_fwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
+                            int64_t ld, const int64_t *target_ids, int64_t ignore_index,
+                            double *logp, double *lse) {
+    int64_t bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t t = target_ids[r];
+#ifndef BIL_ORACLE_MUTANT_IGNORE_NOT_ZEROED
+        if (t == ignore_index) {
+            logp[r] = 0.0;
+            lse[r] = 0.0;
+            continue;
+        }
+#endif
+        double L = row_lse(logits, dtype, r, ld, vocab);
+        lse[r] = L;
+        if (t < 0 || t >= vocab) {
+            logp[r] = NAN;
+            bad += 1;
+            continue;
+        }
+#if defined(BIL_ORACLE_MUTANT_TARGET_OFF_BY_ONE)
+        double xt = load(logits, dtype, r, ld, t + 1 < vocab ? t + 1 : t);
+#else
+        double xt = load(logits, dtype, r, ld, t);
+#endif
+#ifdef BIL_ORACLE_MUTANT_SIGN
+        logp[r] = L - xt;
+#else
+        logp[r] = xt - L;
+#endif
+    }
+    return bad;
+}
+
+/* ---- tile partials -------------------------------------------------------------
+ * "Tensor Parallel", steps 1-2 and 5: the vocabulary is split into fixed tiles
+ * of tile_v columns; tile t covers columns [t*tile_v, min((t+1)*tile_v, V)).
+ * For every row and every tile t in [tile_begin, tile_end):
+ *   part_max[r*ld_part + t] = max of the tile, part_sum[...] = sum exp(x - max).
+ * The target logit is copied (never summed) into target_logit[r] when the
+ * row's target lies in one of these tiles.  Ignored rows get (-inf, 0) and
+ * their logits are not read.  Columns are global column indices of the full
+ * row held in `logits`. */
+void bil_oracle_tile_partials(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
+                              int64_t ld, int64_t tile_v, int64_t tile_begin,
+                              int64_t tile_end, const int64_t *target_ids,
+                              int64_t ignore_index, double *part_max, double *part_sum,
+                              int64_t ld_part, double *target_logit) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t t_id = target_ids[r];
+        for (int64_t t = tile_begin; t < tile_end; ++t) {
+            double m = -INFINITY, s = 0.0;
+            if (t_id != ignore_index) {
+                int64_t c0 = t * tile_v;
+#ifdef BIL_ORACLE_MUTANT_TILE_IGNORES_VOCAB
+                int64_t c1 = c0 + tile_v;
+#else
+                int64_t c1 = c0 + tile_v < vocab ? c0 + tile_v : vocab;
+#endif
+                max_and_sumexp(logits, dtype, r, ld, c0, c1, &m, &s);
+                if (t_id >= c0 && t_id < c1) {
+                    target_logit[r] = load(logits, dtype, r, ld, t_id);
+                }
+            }
+            part_max[r * ld_part + t] = m;
+            part_sum[r * ld_part + t] = s;
+        }
+    }
+}
+
+/* ---- fixed-order merge -----------------------------------------------------------
+ * "Tensor Parallel", steps 4 and 6:
+ *   M = max_t m_t,  LSE = M + log(sum_{t=0..T-1} s_t * exp(m_t - M)),
+ *   logp = target_logit - LSE;  ignored rows give 0.
+ * Returns the number of active rows whose target lies outside [0, vocab)
+ * (their logp is NaN). */
+int64_t bil_oracle_merge(const double *part_max, const double *part_sum, int64_t n_rows,
+                         int64_t num_tiles, int64_t ld_part, const double *target_logit,
+                         const int64_t *target_ids, int64_t ignore_index, int64_t vocab,
+                         double *logp, double *lse) {
+    int64_t bad = 0;
+#pragma omp parallel for schedule(static) reduction(+ : bad)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t t_id = target_ids[r];
+        if (t_id == ignore_index) {
+            logp[r] = 0.0;
+            lse[r] = 0.0;
+            continue;
+        }
+        const double *m = part_max + r * ld_part;
+        const double *s = part_sum + r * ld_part;
+        double M = -INFINITY;
+        for (int64_t t = 0; t < num_tiles; ++t) {
+            if (m[t] > M) {
+                M = m[t];
+            }
+        }
+        double L;
+        if (M == -INFINITY) {
+            L = -INFINITY;
+            for (int64_t t = 0; t < num_tiles; ++t) {
+                if (isnan(s[t])) {
+                    L = NAN;
+                }
+            }
+        } else {
+            double S = 0.0;
+            for (int64_t t = 0; t < num_tiles; ++t) {
+#ifdef BIL_ORACLE_MUTANT_MERGE_TRANSPOSED
+                S += s[t] * exp(M - m[t]);
+#else
+                S += s[t] * exp(m[t] - M);
+#endif
+            }
+            L = M + log(S);
+        }
+        lse[r] = L;
+        if (t_id < 0 || t_id >= vocab) {
+            logp[r] = NAN;
+            bad += 1;
+        } else {
+            logp[r] = target_logit[r] - L;
+        }
+    }
+    return bad;
+}
+
+/* ---- backward --------------------------------------------------------------------
+ * "Batch-Invariance" (the backward reuses the per-row LSE) and "Reference
+ * Semantics" (ignored rows receive zero gradient):
+ *   dlogits[r, c] = g[r] * ([c == t_r] - exp(x[r, c] - LSE_r))
+ * LSE_r is the oracle's own float64 value, recomputed here from the row.
+ * Output is float64, row stride ld_out; columns [vocab, out_cols) of every
+ * row are written as 0.  Returns the number of active rows with an
+ * out-of-range target (their gradient row is NaN). */
+int64_t bil_oracle_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
+                            int64_t ld, const int64_t *target_ids, int64_t ignore_index,
+                            const double *grad_logp, double *dlogits, int64_t ld_out,
+                            int64_t out_cols) {
+    int64_t bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        double *d = dlogits + r * ld_out;
+        int64_t t_id = target_ids[r];
+        for (int64_t c = vocab; c < out_cols; ++c) {
+            d[c] = 0.0;
+        }
+        if (t_id == ignore_index) {
+            for (int64_t c = 0; c < vocab; ++c) {
+                d[c] = 0.0;
+            }
+            continue;
+        }
+        if (t_id < 0 || t_id >= vocab) {
+            for (int64_t c = 0; c < vocab; ++c) {
+                d[c] = NAN;
+            }
+            bad += 1;
+            continue;
+        }
+        double L = row_lse(logits, dtype, r, ld, vocab);
+        double g = grad_logp[r];
+        for (int64_t c = 0; c < vocab; ++c) {
+            double p = exp(load(logits, dtype, r, ld, c) - L);
+            double onehot = (c == t_id) ? 1.0 : 0.0;
+#if defined(BIL_ORACLE_MUTANT_BWD_SIGN)
+            d[c] = g * (p - onehot);
+#elif defined(BIL_ORACLE_MUTANT_BWD_NO_G)
+            d[c] = onehot - p;
+#else
+            d[c] = g * (onehot - p);
+#endif
+        }
+    }
+    return bad;
+}
+
+/* ---- element widening, exposed so that tests can pin it to library routines --- */
+void bil_oracle_widen(const void *src, int dtype, int64_t count, double *dst) {
+    for (int64_t i = 0; i < count; ++i) {
+#ifdef BIL_ORACLE_MUTANT_BF16_WIDEN
+        if (dtype == ORACLE_BF16) {
+            uint32_t w = (uint32_t)((const uint16_t *)src)[i] << 15;
+            float f;
+            memcpy(&f, &w, sizeof f);
+            dst[i] = f;
+            continue;
+        }
+#endif
+        dst[i] = load(src, dtype, 0, 0, i);
+    }
+}

@@ -1,0 +1,313 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each check takes the oracle build flags (``defines``) and raises AssertionError
+when the oracle disagrees with what the pages or the mathematics fix:
+
+  * brute force in 40-digit arithmetic on tiny inputs (no max shift, no tiles);
+  * the pages' own reference semantics as a library routine
+    (``torch.log_softmax(x.double()).gather`` and its autograd gradient);
+  * closed forms (uniform logits, a one-hot spike, two classes, V = 1);
+  * invariants (sum of probabilities, shift and permutation invariance, the
+    gradient's row sum, central finite differences of the forward);
+  * the tile construction: merged partials equal the whole-row value for any
+    tile size and any split of the tiles between calls.
+  * the ignore / invalid-target rules of the operator page.
+
+The same checks run against deliberately broken oracle builds in
+``test_oracle_mutants.py``; every planted mistake must fail at least one.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rows(seed, n, v, scale=2.0, dtype="float32", grid=None, ld=None):
+    """Random rows; columns past v (when ld > v) hold NaN so that reading them shows."""
+    x = wl.rng(seed, 100, v).standard_normal((n, v), dtype=np.float32) * np.float32(scale)
+    if grid is not None:  # coarse grid: shifts and +-h perturbations stay exact in float32
+        x = np.round(x * grid) / grid
+        x = x.astype(np.float32)
+    if ld is not None and ld > v:
+        x = np.concatenate([x, np.full((n, ld - v), np.nan, np.float32)], axis=1)
+    return wl.store(x, dtype)
+
+
+def _targets(seed, n, v, ignore_rows=()):
+    t = wl.rng(seed, 101, v).integers(0, v, n, dtype=np.int64)
+    for r in ignore_rows:
+        t[r] = wl.IGNORE_INDEX
+    return t
+
+
+# ----------------------------------------------------------------------------
+def check_widening(defines=()):
+    """Stored -> float64 widening equals the library conversions, for all 2^16 patterns."""
+    import torch
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.widen(bits, "bfloat16", defines=defines)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok]), "bf16 widening"
+    got = oracle.widen(bits, "float16", defines=defines)
+    ref = bits.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok]), "fp16 widening"
+    f = wl.rng(7, 1).standard_normal(1000).astype(np.float32)
+    assert np.array_equal(oracle.widen(f, "float32", defines=defines), f.astype(np.float64))
+
+
+def check_brute_force(defines=()):
+    """Forward and backward against 40-digit arithmetic: log(sum exp) with no shift."""
+    import mpmath
+    mpmath.mp.dps = 40
+    for seed, (n, v, dtype) in enumerate([(3, 1, "float32"), (4, 7, "bfloat16"), (4, 300, "float16"),
+                                          (3, 513, "float32"), (2, 4096, "bfloat16")]):
+        x = _rows(seed, n, v, dtype=dtype)
+        t = _targets(seed, n, v, ignore_rows=(1,) if n > 2 else ())
+        g = wl.rng(seed, 102).standard_normal(n)
+        logp, lse, bad = oracle.logp_fwd(x, dtype, v, t, defines=defines)
+        d, bad_b = oracle.logp_bwd(x, dtype, v, t, g, defines=defines)
+        assert bad == 0 and bad_b == 0
+        xv = oracle.widen(x, dtype)  # exact values (widening pinned separately)
+        for r in range(n):
+            if t[r] == wl.IGNORE_INDEX:
+                assert logp[r] == 0.0 and lse[r] == 0.0
+                assert np.all(d[r] == 0.0)
+                continue
+            total = mpmath.fsum(mpmath.exp(mpmath.mpf(float(c))) for c in xv[r])
+            ref_lse = mpmath.log(total)
+            ref = mpmath.mpf(float(xv[r, t[r]])) - ref_lse
+            assert abs(float(ref) - logp[r]) <= 1e-12, (seed, r, float(ref), logp[r])
+            assert abs(float(ref_lse) - lse[r]) <= 1e-12
+            for c in range(0, v, max(1, v // 64)):
+                p = mpmath.exp(mpmath.mpf(float(xv[r, c]))) / total
+                ref_d = g[r] * ((1 if c == t[r] else 0) - p)
+                assert abs(float(ref_d) - d[r, c]) <= 1e-12, (seed, r, c)
+            c = int(t[r])
+            p = mpmath.exp(mpmath.mpf(float(xv[r, c]))) / total
+            assert abs(float(g[r] * (1 - p)) - d[r, c]) <= 1e-12
+
+
+def check_library_log_softmax(defines=()):
+    """The pages' reference semantics as a library routine, in float64 on the CPU."""
+    import torch
+    for seed, (n, v, dtype) in enumerate([(16, 4096, "float32"), (8, 1000, "bfloat16"),
+                                          (8, 333, "float16"), (5, 8, "bfloat16")]):
+        x = _rows(seed + 10, n, v, scale=3.0, dtype=dtype)
+        t = _targets(seed + 10, n, v, ignore_rows=(0, n - 1))
+        g = wl.rng(seed, 103).standard_normal(n)
+        logp, lse, bad = oracle.logp_fwd(x, dtype, v, t, defines=defines)
+        d, _ = oracle.logp_bwd(x, dtype, v, t, g, defines=defines)
+        xt = torch.from_numpy(oracle.widen(x, dtype)).requires_grad_(True)
+        tt = torch.from_numpy(t)
+        active = tt != wl.IGNORE_INDEX
+        safe = torch.where(active, tt, torch.zeros_like(tt))
+        sel = torch.log_softmax(xt, dim=-1).gather(-1, safe.unsqueeze(-1)).squeeze(-1)
+        out = torch.where(active, sel, torch.zeros_like(sel))
+        (out * torch.from_numpy(g)).sum().backward()
+        assert np.abs(out.detach().numpy() - logp).max() <= 1e-12, "forward vs log_softmax"
+        assert np.abs(xt.grad.numpy() - d).max() <= 1e-12, "backward vs autograd"
+        ref_lse = torch.logsumexp(xt.detach(), dim=-1).numpy()
+        a = active.numpy()
+        assert np.abs(ref_lse[a] - lse[a]).max() <= 1e-12
+
+
+def check_closed_forms(defines=()):
+    # uniform logits: every class has probability 1/V
+    for v in (1, 300, 4096, 151936):
+        for c in (0.0, 3.5, -7.0):
+            x = np.full((1, v), c, np.float32)
+            t = np.array([v // 3], np.int64)
+            logp, lse, _ = oracle.logp_fwd(x, "float32", v, t, defines=defines)
+            assert abs(logp[0] + math.log(v)) <= 1e-12, (v, c)
+            assert abs(lse[0] - (c + math.log(v))) <= 1e-12
+    # V = 1: the only class has probability 1
+    x = np.array([[12.25], [-3.0]], np.float32)
+    logp, _, _ = oracle.logp_fwd(x, "float32", 1, np.zeros(2, np.int64), defines=defines)
+    assert np.all(logp == 0.0)
+    # one-hot spike of height h over zeros
+    v = 4096
+    for h in (0.5, 4.0, 12.0, 40.0):
+        x = np.zeros((2, v), np.float32)
+        x[:, 1234] = h
+        t = np.array([1234, 77], np.int64)
+        logp, _, _ = oracle.logp_fwd(x, "float32", v, t, defines=defines)
+        z = math.log1p((v - 1) * math.exp(-h))
+        assert abs(logp[0] + z) <= 1e-12, h
+        assert abs(logp[1] - (-h - z)) <= 1e-12, h
+    # two classes: the logistic function
+    for a, b in ((0.25, -1.5), (3.0, 3.0), (-20.0, 5.0)):
+        x = np.array([[a, b], [a, b]], np.float32)
+        logp, _, _ = oracle.logp_fwd(x, "float32", 2, np.array([0, 1], np.int64), defines=defines)
+        assert abs(logp[0] + math.log1p(math.exp(-(a - b)))) <= 1e-12
+        assert abs(logp[1] + math.log1p(math.exp(-(b - a)))) <= 1e-12
+
+
+def check_invariants(defines=()):
+    v = 513
+    x = _rows(3, 1, v, scale=3.0, grid=64)
+    # probabilities over all targets sum to one
+    xs = np.repeat(x, v, axis=0)
+    logp, _, _ = oracle.logp_fwd(xs, "float32", v, np.arange(v, dtype=np.int64), defines=defines)
+    assert abs(np.exp(logp).sum() - 1.0) <= 1e-12
+    # shift invariance (the grid keeps x + k exact in float32)
+    t = np.array([17], np.int64)
+    base, _, _ = oracle.logp_fwd(x, "float32", v, t, defines=defines)
+    for k in (-50.0, 3.5, 1e3):
+        y = (x + np.float32(k)).astype(np.float32)
+        assert np.array_equal(y - np.float32(k), x)
+        lp, _, _ = oracle.logp_fwd(y, "float32", v, t, defines=defines)
+        assert abs(lp[0] - base[0]) <= 1e-9, k
+    # permutation of the columns, with the target following its column
+    perm = wl.rng(3, 9).permutation(v)
+    lp, _, _ = oracle.logp_fwd(np.ascontiguousarray(x[:, perm]), "float32", v,
+                               np.array([int(np.flatnonzero(perm == 17)[0])], np.int64), defines=defines)
+    assert abs(lp[0] - base[0]) <= 1e-12
+    # the gradient of a row sums to g * (1 - sum p) = 0
+    g = np.array([-1.75])
+    d, _ = oracle.logp_bwd(x, "float32", v, t, g, defines=defines)
+    assert abs(d.sum()) <= 1e-12
+    # the target column follows g, every other column moves against it
+    assert d[0, 17] * g[0] > 0
+    assert np.all(np.delete(d[0], 17) * g[0] <= 0)
+
+
+def check_finite_differences(defines=()):
+    """d(g*logp)/dx_c by central differences; the grid keeps x +- h exact."""
+    v, h = 64, 2.0 ** -12
+    x = _rows(4, 1, v, scale=2.0, grid=256)
+    t = np.array([5], np.int64)
+    g = np.array([0.8125])
+    d, _ = oracle.logp_bwd(x, "float32", v, t, g, defines=defines)
+    for c in (0, 5, 31, 63):
+        xp = x.copy()
+        xm = x.copy()
+        xp[0, c] += np.float32(h)
+        xm[0, c] -= np.float32(h)
+        fp, _, _ = oracle.logp_fwd(xp, "float32", v, t, defines=defines)
+        fm, _, _ = oracle.logp_fwd(xm, "float32", v, t, defines=defines)
+        fd = g[0] * (fp[0] - fm[0]) / (2 * h)
+        assert abs(fd - d[0, c]) <= 1e-6, (c, fd, d[0, c])
+
+
+def check_tiles(defines=()):
+    """Merged tile partials equal the whole-row LSE for any tile size and split."""
+    for dtype, v, n in (("float32", 4096, 6), ("bfloat16", 1000, 5), ("float16", 777, 4)):
+        x = _rows(5, n, v, scale=3.0, dtype=dtype, ld=-(-v // 4096) * 4096 + 8)
+        t = _targets(5, n, v, ignore_rows=(2,))
+        ref_logp, ref_lse, _ = oracle.logp_fwd(x, dtype, v, t, defines=defines)
+        vals = oracle.widen(x, dtype)
+        for tile in (8, 64, 512, 4096):
+            nt = -(-v // tile)
+            for split in (1, 2, 4):
+                pm = np.full((n, nt), -np.inf)
+                ps = np.zeros((n, nt))
+                tl = np.full(n, np.nan)
+                bounds = [(k * nt) // split for k in range(split + 1)]
+                for k in reversed(range(split)):  # ranks may finish in any order
+                    oracle.tile_partials(x, dtype, v, tile, bounds[k], bounds[k + 1], t,
+                                         part_max=pm, part_sum=ps, target_logit=tl, defines=defines)
+                logp, lse, _ = oracle.merge(pm, ps, tl, t, v, defines=defines)
+                assert np.abs(logp - ref_logp).max() <= 1e-12, (dtype, tile, split)
+                assert np.abs(lse - ref_lse).max() <= 1e-12
+                for r in range(n):
+                    if t[r] == wl.IGNORE_INDEX:
+                        assert np.all(pm[r] == -np.inf) and np.all(ps[r] == 0.0)
+                        continue
+                    assert tl[r] == vals[r, t[r]]  # copied, never summed
+                    for k in range(nt):
+                        seg = vals[r, k * tile: min(v, (k + 1) * tile)]
+                        assert pm[r, k] == seg.max()
+                        assert 1.0 <= ps[r, k] <= len(seg)
+
+
+def check_contract_rules(defines=()):
+    rules = json.load(open(os.path.join(GOLDEN, "contract_rules.json")))
+    assert rules["ignore_index_default"] == wl.IGNORE_INDEX
+    v = 300
+    x = _rows(6, 4, v, scale=2.0, dtype="bfloat16")
+    # default ignore_index: -1 and V are invalid, V-1 is valid, -100 is ignored
+    t = np.array([-1, v, v - 1, -100], np.int64)
+    logp, lse, bad = oracle.logp_fwd(x, "bfloat16", v, t, defines=defines)
+    assert bad == 2 and np.isnan(logp[0]) and np.isnan(logp[1])
+    assert np.isfinite(logp[2]) and logp[2] < 0
+    assert logp[3] == 0.0 and not np.signbit(logp[3]) and lse[3] == 0.0
+    # ignore_index = -1 makes -1 an ignored row and -100 invalid
+    logp, _, bad = oracle.logp_fwd(x, "bfloat16", v, t, ignore_index=-1, defines=defines)
+    assert bad == 2 and logp[0] == 0.0 and np.isnan(logp[3])
+    # ignored rows receive an all-zero gradient, padded output columns are zero
+    d, bad = oracle.logp_bwd(x, "bfloat16", v, np.array([-100, 3, -100, 7], np.int64),
+                             np.ones(4), out_cols=v + 12, defines=defines)
+    assert bad == 0
+    assert np.all(d[0] == 0.0) and np.all(d[2] == 0.0) and np.all(d[:, v:] == 0.0)
+    assert not np.signbit(d[0]).any()
+
+
+def check_minimal_example(defines=()):
+    ex = json.load(open(os.path.join(GOLDEN, "minimal_example.json")))
+    shape = ex["logits_shape"]
+    n, v = int(np.prod(shape[:-1])), shape[-1]
+    x = _rows(8, n, v, scale=1.0, dtype="bfloat16")
+    t = _targets(8, n, v).reshape(shape[:-1])
+    for pos in ex["ignored_positions"]:
+        t[tuple(pos)] = ex["ignore_index"]
+    logp, _, bad = oracle.logp_fwd(x, "bfloat16", v, t.reshape(-1), ex["ignore_index"], defines=defines)
+    out = logp.astype(np.float32).reshape(t.shape)
+    assert bad == 0
+    assert list(out.shape) == ex["expect"]["out_shape"]
+    assert out.dtype == np.float32 and str(out.dtype) == ex["expect"]["out_dtype"]
+    assert out[0, 0] == ex["expect"]["out_at_ignored"]
+    assert np.all(out.reshape(-1)[1:] < 0)
+
+
+def check_special_values(defines=()):
+    """A row of -inf has no distribution (NaN); NaN poisons its row only."""
+    v = 40
+    x = np.zeros((3, v), np.float32)
+    x[0] = -np.inf
+    x[1, 7] = np.nan
+    x[2, :20] = -np.inf
+    t = np.array([3, 3, 30], np.int64)
+    logp, lse, _ = oracle.logp_fwd(x, "float32", v, t, defines=defines)
+    assert lse[0] == -np.inf and np.isnan(logp[0])
+    assert np.isnan(lse[1]) and np.isnan(logp[1])
+    assert abs(logp[2] + math.log(20)) <= 1e-12
+
+
+ALL_CHECKS = [check_widening, check_brute_force, check_library_log_softmax, check_closed_forms,
+              check_invariants, check_finite_differences, check_tiles, check_contract_rules,
+              check_minimal_example, check_special_values]
+
+
+def check_rounding_helpers():
+    """float64 -> bf16 rounding: ties to even at exact midpoints, nearest elsewhere,
+    and equal to the library float32 -> bf16 conversion on float32 values."""
+    import torch
+    r = wl.rng(11, 1)
+    b = r.integers(0, 0x7F7F, 20000).astype(np.uint16)  # finite positive bf16 values
+    b = np.concatenate([b, b | 0x8000]).astype(np.uint16)
+    lo = oracle.bf16_bits_to_float64(b)
+    hi = oracle.bf16_bits_to_float64(b + 1)            # next value away from zero
+    mid = (lo + hi) / 2                                 # exact in float64
+    got = oracle.round_to_bf16_bits(mid)
+    even = np.where((b & 1) == 0, b, b + 1).astype(np.uint16)
+    assert np.array_equal(got, even), "ties to even"
+    eps = np.abs(hi - lo) * 2.0 ** -20
+    assert np.array_equal(oracle.round_to_bf16_bits(mid - np.sign(mid) * eps), b)
+    assert np.array_equal(oracle.round_to_bf16_bits(mid + np.sign(mid) * eps), (b + 1).astype(np.uint16))
+    f = (r.standard_normal(100000) * np.exp(r.uniform(-80, 80, 100000))).astype(np.float32)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.round_to_bf16_bits(f.astype(np.float64)), ref)
+    tiny = np.array([2.0 ** -140, -(2.0 ** -133) * 1.5, 0.0, -0.0, 1e39, -1e39])
+    assert list(oracle.round_to_bf16_bits(tiny)) == [0x0000, 0x8002, 0x0000, 0x8000, 0x7F80, 0xFF80]
