@@ -1,0 +1,188 @@
+/*
+ * bil.h -- batch-invariant selected-token log-probability, C ABI.
+ *
+ * The operator ("Batch-Invariant LogP" operator page, opening paragraph and
+ * section "Reference Semantics"):
+ *
+ *     logp[r] = logits[r, target_ids[r]] - logsumexp(logits[r, :])   (float32)
+ *     logp[r] = 0.0 and d logits[r, :] = 0.0   when target_ids[r] == ignore_index
+ *
+ * The row's logsumexp is built the way the same page's section "Tensor
+ * Parallel" (steps 1-6) builds it: the vocabulary is cut into fixed tiles of
+ * tile_v columns; each tile gets a float32 (max m_t, sum-exp s_t) partial;
+ * all tiles are merged in one fixed order,
+ *     M = max_t m_t,   LSE = M + log(sum_{t = 0 .. T-1} s_t * exp(m_t - M)),
+ * and the target logit is copied from the tile that owns it.  Every row's
+ * result depends only on that row's logits, its target and tile_v -- never on
+ * the number of rows, the row's position, its neighbours, the row stride,
+ * the launch geometry, or on how the tiles are split between calls
+ * (section "Batch-Invariance").  The backward recomputes the softmax from
+ * the saved per-row LSE (section "Batch-Invariance", backward bullet):
+ *     dlogits[r, c] = g[r] * ([c == target_ids[r]] - exp(logits[r, c] - lse[r])).
+ *
+ * Conventions shared by every call:
+ *  - All array pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no memory and keeps no per-call state.
+ *  - Matrices are row-major.  `ld` is the row stride in elements (ld >= the
+ *    columns read).  Columns at or beyond `vocab` are never read.
+ *  - Work is queued on `stream` and the call returns without waiting, except
+ *    where `validate` is set (it then synchronises, see below).
+ *  - Every call returns a status code (BIL_OK on success).  Arguments are
+ *    checked on the host before anything is queued; a failed check queues
+ *    nothing and writes nothing.  There is no fallback path.
+ *  - Element types: BIL_F32, BIL_BF16, BIL_F16.  Targets are int64.
+ *  - Rows whose starting address is 16-byte aligned are read with bulk
+ *    asynchronous copies; other rows are read element by element.  The
+ *    results are bit-identical either way.
+ *
+ * Results are bitwise reproducible for a given tile_v, element type and
+ * library build (the arithmetic is fixed in bil_contract_id()).
+ */
+#ifndef BIL_H
+#define BIL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* An opaque CUDA stream handle (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st *bil_stream_t;
+
+/* ---- status codes ----------------------------------------------------- */
+#define BIL_OK 0
+#define BIL_E_INVALID_ARG 1   /* a size, pointer or range is out of its domain */
+#define BIL_E_DTYPE 2         /* unknown element type */
+#define BIL_E_ALIGN 3         /* a pointer is not aligned to its element size */
+#define BIL_E_TARGET_RANGE 4  /* validate=1 found an active target outside [0, vocab) */
+#define BIL_E_CUDA 5          /* a CUDA runtime call failed (launch, copy, device query) */
+#define BIL_E_UNSUPPORTED 6   /* well-formed but beyond this build's limits (see below) */
+
+/* ---- element types ---------------------------------------------------- */
+#define BIL_F32 0
+#define BIL_BF16 1
+#define BIL_F16 2
+
+/* Limits of this build: tile_v is a positive multiple of 8 with
+ * tile_v * element_size <= BIL_MAX_TILE_BYTES; the fused forward handles at
+ * most BIL_MAX_FUSED_TILES tiles per row (bil_logp_tile_partials and
+ * bil_logp_merge have no such limit). */
+#define BIL_MAX_TILE_BYTES (64 * 1024)
+#define BIL_MAX_FUSED_TILES 2048
+
+/* The arithmetic contract of this build as a printable string: the in-tile
+ * lane layout and reduction tree, the exp/log primitives, the merge order.
+ * Two builds with the same string give the same bits.  Static storage. */
+const char *bil_contract_id(void);
+
+/* Human-readable name of a status code.  Static storage. */
+const char *bil_status_string(int status);
+
+/*
+ * bil_logp_fwd -- fused forward: tile partials, fixed-order merge, target
+ * gather and combine in one pass over the logits ("Tensor Parallel", steps
+ * 1-6, with every tile on this device).
+ *
+ *  logits        [n_rows, ld] elements of type `dtype`; columns [0, vocab) are read.
+ *  dtype         BIL_F32 | BIL_BF16 | BIL_F16.
+ *  n_rows        >= 0 (0 queues nothing).
+ *  vocab         >= 1 real vocabulary columns; ld >= vocab.
+ *  target_ids    [n_rows] int64.  A row with target == ignore_index is inactive:
+ *                its logits are not read and logp = lse = +0.0.  An active row
+ *                whose target lies outside [0, vocab) gets logp = NaN (lse is
+ *                still its LSE) and nothing outside the row is read.
+ *  tile_v        vocabulary tile width (columns), see the limits above.
+ *  logp          [n_rows] float32 output.
+ *  lse           [n_rows] float32 output (the per-row LSE the backward needs),
+ *                or NULL when not wanted.
+ *  validate      0: no host synchronisation.  1: before queuing the kernel the
+ *                call copies target_ids to the host (synchronising `stream`)
+ *                and returns BIL_E_TARGET_RANGE, queuing nothing, if an active
+ *                target is outside [0, vocab) (section "Reference Semantics":
+ *                validate trades a synchronisation for a checked range).
+ */
+int bil_logp_fwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
+                 const int64_t *target_ids, int64_t ignore_index, int32_t tile_v, float *logp,
+                 float *lse, int validate, bil_stream_t stream);
+
+/*
+ * bil_logp_tile_partials -- one vocabulary shard's tile partials
+ * ("Tensor Parallel", steps 1, 2 and 5).
+ *
+ * The shard is the tile range [tile_begin, tile_end) of a vocabulary of
+ * `vocab` columns cut into tiles of tile_v columns (num_tiles =
+ * ceil(vocab / tile_v); 0 <= tile_begin < tile_end <= num_tiles).
+ *
+ *  logits        [n_rows, ld] elements whose column 0 is GLOBAL column
+ *                tile_begin * tile_v.  For a full-vocabulary buffer, pass its
+ *                base plus tile_begin * tile_v elements; for a rank's own
+ *                shard, pass the shard.  Global columns >= vocab are not read.
+ *  target_ids    [n_rows] int64 GLOBAL target columns; ignored rows as above.
+ *  part_max,
+ *  part_sum      [n_rows, ld_part] float32 (ld_part >= num_tiles).  For every row
+ *                and every tile t of the range, column t receives the tile's
+ *                max m_t and sum of exp(x - m_t).  Inactive rows receive
+ *                (-inf, 0).  Other columns are not touched, so several calls
+ *                (ranks) can fill one buffer.
+ *  target_logit  [n_rows] float32: written (a copy of the stored logit, widened
+ *                exactly) only for active rows whose target lies in the range.
+ */
+int bil_logp_tile_partials(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
+                           int64_t ld, int32_t tile_v, int32_t tile_begin, int32_t tile_end,
+                           const int64_t *target_ids, int64_t ignore_index, float *part_max,
+                           float *part_sum, int64_t ld_part, float *target_logit,
+                           bil_stream_t stream);
+
+/*
+ * bil_logp_merge -- the fixed-order merge and the combine ("Tensor Parallel",
+ * steps 4 and 6).  Bit-identical to bil_logp_fwd when the partials come from
+ * bil_logp_tile_partials with the same tile_v, however the tiles were split.
+ *
+ *  part_max, part_sum  [n_rows, ld_part] float32, columns [0, num_tiles) read.
+ *  target_logit        [n_rows] float32 (read for active rows with a valid target).
+ *  target_ids, ignore_index, vocab   as for bil_logp_fwd (vocab only decides
+ *                      which targets are valid).
+ *  logp, lse           [n_rows] float32 outputs (lse may be NULL).
+ *  validate            as for bil_logp_fwd.
+ */
+int bil_logp_merge(const float *part_max, const float *part_sum, int64_t n_rows,
+                   int32_t num_tiles, int64_t ld_part, const float *target_logit,
+                   const int64_t *target_ids, int64_t ignore_index, int64_t vocab, float *logp,
+                   float *lse, int validate, bil_stream_t stream);
+
+/*
+ * bil_logp_bwd -- fused backward from the saved LSE ("Batch-Invariance":
+ * one row tile per work unit, no cross-row reduction, no atomics; "Reference
+ * Semantics": ignored rows receive a zero gradient).
+ *
+ *  logits, dtype, n_rows, vocab, ld, target_ids, ignore_index   as for the forward.
+ *  lse           [n_rows] float32, the forward's lse output.
+ *  grad_logp     [n_rows] float32 upstream gradient g of logp.
+ *  dlogits       [n_rows, ld_out] elements of type dlogits_dtype (BIL_F32 |
+ *                BIL_BF16 | BIL_F16, rounded to nearest even).  Columns
+ *                [0, vocab) receive g * (onehot - p); columns [vocab, out_cols)
+ *                receive +0.0; columns >= out_cols are not touched.
+ *                vocab <= out_cols <= ld_out.  Inactive rows are +0.0 throughout
+ *                [0, out_cols) and their logits are not read; active rows with
+ *                an out-of-range target are NaN over [0, vocab).
+ */
+int bil_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
+                 const int64_t *target_ids, int64_t ignore_index, const float *lse,
+                 const float *grad_logp, void *dlogits, int dlogits_dtype, int64_t ld_out,
+                 int64_t out_cols, bil_stream_t stream);
+
+/*
+ * bil_watchdog_status -- every wait inside this library's kernels is
+ * bounded.  A wait that runs out sets a bit in a per-device word, and the
+ * kernel stops instead of hanging (its outputs are then incomplete).  This
+ * call reads that word for the current device into *flags (0 = no wait ever
+ * ran out) and clears it when `clear` is non-zero.  It synchronises the device.
+ */
+int bil_watchdog_status(unsigned int *flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIL_H */

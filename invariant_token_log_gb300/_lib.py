@@ -1,0 +1,76 @@
+"""ctypes declarations of the C ABI in include/bil.h.
+
+Loading fails loudly: there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+# status codes and element types, as include/bil.h defines them
+OK, E_INVALID_ARG, E_DTYPE, E_ALIGN, E_TARGET_RANGE, E_CUDA, E_UNSUPPORTED = range(7)
+F32, BF16, F16 = 0, 1, 2
+MAX_TILE_BYTES = 64 * 1024
+MAX_FUSED_TILES = 2048
+
+# every entry point the header declares: name -> (restype, argtypes)
+_i32, _i64, _p, _u = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
+SIGNATURES = {
+    "bil_contract_id": (ctypes.c_char_p, []),
+    "bil_status_string": (ctypes.c_char_p, [_i32]),
+    "bil_logp_fwd": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, ctypes.c_int32, _p, _p, _i32, _p]),
+    "bil_logp_tile_partials": (_i32, [_p, _i32, _i64, _i64, _i64, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, _p, _i64, _p, _p, _i64, _p, _p]),
+    "bil_logp_merge": (_i32, [_p, _p, _i64, ctypes.c_int32, _i64, _p, _p, _i64, _i64, _p, _p, _i32, _p]),
+    "bil_logp_bwd": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, _p, _p, _p, _i32, _i64, _i64, _p]),
+    "bil_watchdog_status": (_i32, [ctypes.POINTER(_u), _i32]),
+}
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+class BilError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.library_path()
+
+
+def load() -> ctypes.CDLL:
+    """Load libbil.so for this machine; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"the CUDA library is not built ({path} missing); run "
+                "`python -m invariant_token_log_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().bil_status_string(status).decode()
+
+
+def contract_id() -> str:
+    return load().bil_contract_id().decode()
+
+
+def check(fn: str, status: int) -> None:
+    if status != OK:
+        raise BilError(fn, status)

@@ -1,0 +1,212 @@
+"""PyTorch front end of the C ABI: argument marshalling only.
+
+PyTorch supplies device memory and the current stream; every step of the
+operator runs in the CUDA library (``libbil.so``).  Functions here check
+shapes and devices, flatten ``[*lead, V]`` logits to ``[N, V]`` row-major
+views (copying only when no such view exists), pass raw device pointers and
+the current stream, and turn status codes into exceptions.
+
+Operator: "Batch-Invariant LogP" operator page -- "Entry Point" (call shape:
+logits, target_ids, ignore_index, validate), "Tensor Contract" (shapes and
+dtypes), "Reference Semantics" (what is computed), "Tensor Parallel" (the
+tile partials and fixed-order merge), "Batch-Invariance" (backward from the
+saved per-row LSE).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+DEFAULT_TILE_V = 4096
+IGNORE_INDEX = -100
+
+_DTYPES = {torch.float32: _lib.F32, torch.bfloat16: _lib.BF16, torch.float16: _lib.F16}
+
+
+def _code(dtype: torch.dtype) -> int:
+    try:
+        return _DTYPES[dtype]
+    except KeyError:
+        raise TypeError(f"unsupported element type {dtype}; expected float32, bfloat16 or float16") from None
+
+
+def _rows2d(x: torch.Tensor) -> torch.Tensor:
+    """[*lead, V] -> [N, V] with unit column stride (a view when one exists)."""
+    v = x.shape[-1]
+    x2 = x.reshape(-1, v)
+    if x2.stride(-1) != 1 and x2.numel() > 0:
+        x2 = x2.contiguous()
+    return x2
+
+
+def _row_stride(x2: torch.Tensor) -> int:
+    return x2.stride(0) if x2.shape[0] > 1 else max(x2.stride(0), x2.shape[1])
+
+
+def _stream(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _targets1d(target_ids: torch.Tensor, lead_shape, device) -> torch.Tensor:
+    if tuple(target_ids.shape) != tuple(lead_shape):
+        raise ValueError(f"target_ids shape {tuple(target_ids.shape)} != logits leading shape {tuple(lead_shape)}")
+    if target_ids.dtype not in (torch.int64, torch.int32, torch.int16, torch.int8, torch.uint8):
+        raise TypeError("target_ids must be an integer tensor")
+    if target_ids.device != device:
+        raise ValueError("target_ids must be on the logits' device")
+    # the C ABI reads int64 targets; narrower integer types are widened here
+    return target_ids.reshape(-1).to(torch.int64).contiguous()
+
+
+def _need_cuda(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("the CUDA library needs CUDA tensors (there is no CPU path)")
+
+
+def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int = IGNORE_INDEX,
+             tile_v: int = DEFAULT_TILE_V, validate: bool = False, vocab: int | None = None,
+             out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """Selected-token log-probabilities: (logp, lse), both float32 with the targets' shape.
+
+    ``vocab`` (default: the last dimension) lets the row carry padding columns
+    that are never read (e.g. a vocabulary padded to a multiple of the tile).
+    """
+    _need_cuda(logits, target_ids)
+    lead = logits.shape[:-1]
+    x2 = _rows2d(logits)
+    n, width = x2.shape
+    v = width if vocab is None else int(vocab)
+    if not 1 <= v <= width:
+        raise ValueError(f"vocab {v} outside [1, {width}]")
+    t1 = _targets1d(target_ids, lead, logits.device)
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=logits.device)
+    if lse is None:
+        lse = torch.empty(n, dtype=torch.float32, device=logits.device)
+    lib = _lib.load()
+    with torch.cuda.device(logits.device):
+        st = lib.bil_logp_fwd(_ptr(x2), _code(x2.dtype), n, v, _row_stride(x2), _ptr(t1), int(ignore_index),
+                              int(tile_v), _ptr(out), _ptr(lse), int(bool(validate)), _stream(logits.device))
+    _lib.check("bil_logp_fwd", st)
+    return out.reshape(lead), lse.reshape(lead)
+
+
+def logp_tile_partials(logits_shard: torch.Tensor, target_ids: torch.Tensor, vocab: int, tile_v: int,
+                       tile_begin: int, tile_end: int, part_max: torch.Tensor, part_sum: torch.Tensor,
+                       target_logit: torch.Tensor, ignore_index: int = IGNORE_INDEX) -> None:
+    """Fill columns [tile_begin, tile_end) of the [N, T] partial buffers.
+
+    ``logits_shard`` is [N, >= shard columns]; its column 0 is global column
+    ``tile_begin * tile_v`` (a rank's own vocabulary shard, or a column slice
+    of the full logits)."""
+    _need_cuda(logits_shard, target_ids, part_max, part_sum, target_logit)
+    x2 = _rows2d(logits_shard)
+    n = x2.shape[0]
+    t1 = _targets1d(target_ids, (n,), logits_shard.device)
+    for name, b in (("part_max", part_max), ("part_sum", part_sum)):
+        if b.dtype != torch.float32 or b.dim() != 2 or b.shape[0] != n or b.stride(1) != 1:
+            raise ValueError(f"{name} must be a row-major float32 [N, >= num_tiles] tensor")
+    if part_max.stride(0) != part_sum.stride(0):
+        raise ValueError("part_max and part_sum must share a row stride")
+    if target_logit.dtype != torch.float32 or target_logit.numel() != n or not target_logit.is_contiguous():
+        raise ValueError("target_logit must be a contiguous float32 [N] tensor")
+    lib = _lib.load()
+    with torch.cuda.device(logits_shard.device):
+        st = lib.bil_logp_tile_partials(_ptr(x2), _code(x2.dtype), n, int(vocab), _row_stride(x2), int(tile_v),
+                                        int(tile_begin), int(tile_end), _ptr(t1), int(ignore_index),
+                                        _ptr(part_max), _ptr(part_sum), part_max.stride(0), _ptr(target_logit),
+                                        _stream(logits_shard.device))
+    _lib.check("bil_logp_tile_partials", st)
+
+
+def logp_merge(part_max: torch.Tensor, part_sum: torch.Tensor, num_tiles: int, target_logit: torch.Tensor,
+               target_ids: torch.Tensor, vocab: int, ignore_index: int = IGNORE_INDEX, validate: bool = False):
+    """Fixed-order merge of [N, T] partials: (logp, lse) float32 [N]."""
+    _need_cuda(part_max, part_sum, target_logit, target_ids)
+    n = part_max.shape[0]
+    t1 = _targets1d(target_ids, (n,), part_max.device)
+    if part_max.stride(0) != part_sum.stride(0) or part_max.stride(1) != 1 or part_sum.stride(1) != 1:
+        raise ValueError("part_max and part_sum must be row-major with one row stride")
+    out = torch.empty(n, dtype=torch.float32, device=part_max.device)
+    lse = torch.empty(n, dtype=torch.float32, device=part_max.device)
+    lib = _lib.load()
+    with torch.cuda.device(part_max.device):
+        st = lib.bil_logp_merge(_ptr(part_max), _ptr(part_sum), n, int(num_tiles), part_max.stride(0),
+                                _ptr(target_logit), _ptr(t1), int(ignore_index), int(vocab), _ptr(out), _ptr(lse),
+                                int(bool(validate)), _stream(part_max.device))
+    _lib.check("bil_logp_merge", st)
+    return out, lse
+
+
+def logp_bwd(logits: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor, grad_logp: torch.Tensor,
+             ignore_index: int = IGNORE_INDEX, dlogits_dtype: torch.dtype | None = None,
+             vocab: int | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """dlogits = g * (onehot(target) - softmax(logits)) from the saved LSE.
+
+    Returns a tensor of the logits' shape (columns past ``vocab`` are zero) in
+    ``dlogits_dtype`` (default: the logits' dtype)."""
+    _need_cuda(logits, target_ids, lse, grad_logp)
+    lead = logits.shape[:-1]
+    x2 = _rows2d(logits)
+    n, width = x2.shape
+    v = width if vocab is None else int(vocab)
+    t1 = _targets1d(target_ids, lead, logits.device)
+    lse1 = lse.reshape(-1).to(torch.float32).contiguous()
+    g1 = grad_logp.reshape(-1).to(torch.float32).contiguous()
+    if lse1.numel() != n or g1.numel() != n:
+        raise ValueError("lse and grad_logp must have the targets' shape")
+    odt = logits.dtype if dlogits_dtype is None else dlogits_dtype
+    if out is None:
+        out = torch.empty((n, width), dtype=odt, device=logits.device)
+    o2 = out.reshape(n, -1)
+    if o2.stride(-1) != 1 or o2.shape[1] < width:
+        raise ValueError("out must be row-major with at least the logits' columns")
+    lib = _lib.load()
+    with torch.cuda.device(logits.device):
+        st = lib.bil_logp_bwd(_ptr(x2), _code(x2.dtype), n, v, _row_stride(x2), _ptr(t1), int(ignore_index),
+                              _ptr(lse1), _ptr(g1), _ptr(o2), _code(o2.dtype), _row_stride(o2), width,
+                              _stream(logits.device))
+    _lib.check("bil_logp_bwd", st)
+    return out.reshape(logits.shape) if out.numel() == logits.numel() else out
+
+
+class BatchInvariantLogp(torch.autograd.Function):
+    """logp = BatchInvariantLogp.apply(logits, target_ids, ignore_index, tile_v, validate).
+
+    The forward saves the per-row LSE; the backward recomputes the softmax
+    from it.  target_ids receives no gradient."""
+
+    @staticmethod
+    def forward(ctx, logits, target_ids, ignore_index=IGNORE_INDEX, tile_v=DEFAULT_TILE_V, validate=False):
+        logp, lse = logp_fwd(logits, target_ids, ignore_index, tile_v, validate)
+        ctx.save_for_backward(logits, target_ids, lse)
+        ctx.ignore_index = ignore_index
+        ctx.mark_non_differentiable(lse)
+        return logp
+
+    @staticmethod
+    def backward(ctx, grad_logp):
+        logits, target_ids, lse = ctx.saved_tensors
+        d = logp_bwd(logits, target_ids, lse, grad_logp.contiguous(), ctx.ignore_index)
+        return d, None, None, None, None
+
+
+def batch_invariant_logp(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int = IGNORE_INDEX,
+                         validate: bool = False, tile_v: int = DEFAULT_TILE_V) -> torch.Tensor:
+    """Differentiable selected-token log-probability, float32 with the targets' shape."""
+    return BatchInvariantLogp.apply(logits, target_ids, ignore_index, tile_v, validate)
+
+
+def watchdog_status(clear: bool = True) -> int:
+    """Bits set by kernel waits that ran out on the current device (0 = none)."""
+    flags = ctypes.c_uint(0)
+    _lib.check("bil_watchdog_status", _lib.load().bil_watchdog_status(ctypes.byref(flags), int(clear)))
+    return int(flags.value)

@@ -1,0 +1,101 @@
+"""Shared helpers of the GPU tests: move seeded workloads to the device and
+compare CUDA results with the CPU oracle.
+
+Tolerances (written here once, used by every GPU test):
+  LOGP_ATOL   1e-4 absolute on float32 logp and lse against the float64 oracle.
+  DLOGITS_ATOL 1e-6 absolute per element on float32 dlogits against the
+              float64 oracle.
+  bf16/fp16 dlogits: the stored value must equal the correctly rounded
+              oracle value, or be the other neighbour of the oracle value when
+              that value lies within DLOGITS_ATOL of the rounding midpoint
+              (no 1e-6 bound can hold on a 2^-8-relative storage format, so the
+              bound applies to the value before the final rounding).
+  Partials:   m_t and the target logit exactly (both are copies or exact maxima
+              of exactly widened values); s_t within 1e-5 relative.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+LOGP_ATOL = 1e-4
+DLOGITS_ATOL = 1e-6
+PART_SUM_RTOL = 1e-5
+
+TORCH_DTYPE = {"float32": torch.float32, "bfloat16": torch.bfloat16, "float16": torch.float16}
+
+
+def device_logits(stored: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    """Stored elements (float32, or uint16 bit patterns) -> a device tensor of `dtype`."""
+    if dtype == "float32":
+        return torch.from_numpy(np.ascontiguousarray(stored)).to(device)
+    t = torch.from_numpy(np.ascontiguousarray(stored).view(np.int16)).to(device)
+    return t.view(TORCH_DTYPE[dtype])
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    """A device tensor's stored elements back on the host (uint16 bits for 16-bit types)."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def f32_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int32).numpy()
+
+
+def assert_close_abs(got: np.ndarray, ref: np.ndarray, atol: float, what: str):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    nan_ok = np.array_equal(np.isnan(got), np.isnan(ref))
+    assert nan_ok, f"{what}: NaN pattern differs"
+    fin = ~np.isnan(ref)
+    inf_ok = np.array_equal(got[fin & np.isinf(ref)], ref[fin & np.isinf(ref)])
+    assert inf_ok, f"{what}: infinities differ"
+    m = fin & np.isfinite(ref)
+    err = np.abs(got[m] - ref[m])
+    worst = float(err.max()) if err.size else 0.0
+    assert worst <= atol, f"{what}: max |err| {worst:.3g} > {atol:g} (at {np.argmax(err)})"
+    return worst
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.ldexp(1.0, (np.maximum(e, -126) - 7).astype(np.int64))
+
+
+def f16_ulp(v: np.ndarray) -> np.ndarray:
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.ldexp(1.0, (np.maximum(e, -14) - 10).astype(np.int64))
+
+
+def assert_rounded(got_bits: np.ndarray, exact: np.ndarray, dtype: str, atol: float, what: str):
+    """Low-precision gradient check: correct rounding of the exact value, up to
+    a flip between the two neighbours when the exact value is within `atol`
+    of their midpoint.  Returns the fraction of elements that were flipped."""
+    exact = np.asarray(exact, np.float64)
+    if dtype == "bfloat16":
+        rne = oracle.round_to_bf16_bits(exact)
+        gv = oracle.bf16_bits_to_float64(got_bits)
+        ulp = bf16_ulp(exact)
+    else:
+        rne = oracle.round_to_f16(exact).view(np.uint16)
+        gv = got_bits.view(np.float16).astype(np.float64)
+        ulp = f16_ulp(exact)
+    same = got_bits == rne
+    flip_ok = np.abs(gv - exact) <= ulp / 2 + atol
+    bad = ~(same | flip_ok)
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements off by more than a rounding flip, " \
+                          f"e.g. got {gv[bad][:4]} exact {exact[bad][:4]}"
+    return float((~same).mean())
+
+
+def check_watchdog():
+    import invariant_token_log_gb300 as bil
+    assert bil.watchdog_status(clear=True) == 0, "a kernel wait ran out"

@@ -1,0 +1,282 @@
+"""CUDA library vs the CPU oracle, element by element, through the C ABI.
+
+Tolerances are defined in gpu_helpers.py.  Sizes here span several tiles and a
+ragged last tile while the oracle still finishes in seconds; the full-size
+workloads are in test_gpu_full_size.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import invariant_token_log_gb300 as bil
+import oracle
+import workloads as wl
+from gpu_helpers import (DLOGITS_ATOL, LOGP_ATOL, PART_SUM_RTOL, assert_close_abs, assert_rounded,
+                         check_watchdog, device_logits, f32_bits, host_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _watchdog():
+    yield
+    check_watchdog()
+
+
+def run_fwd_bwd(w, dlogits_dtype="float32", tile_v=None, validate=False):
+    x = device_logits(w.logits, w.dtype)
+    t = torch.from_numpy(w.target_ids).cuda()
+    logp, lse = bil.logp_fwd(x, t, w.ignore_index, tile_v or w.tile_v, validate, vocab=w.vocab)
+    g = torch.from_numpy(w.grad_logp).cuda()
+    d = bil.logp_bwd(x, t, lse, g, w.ignore_index, dlogits_dtype={"float32": torch.float32,
+                     "bfloat16": torch.bfloat16, "float16": torch.float16}[dlogits_dtype], vocab=w.vocab)
+    torch.cuda.synchronize()
+    return logp, lse, d
+
+
+def oracle_fwd_bwd(w):
+    logp, lse, bad = oracle.logp_fwd(w.logits, w.dtype, w.vocab, w.target_ids, w.ignore_index)
+    d, _ = oracle.logp_bwd(w.logits, w.dtype, w.vocab, w.target_ids, w.grad_logp.astype(np.float64),
+                           w.ignore_index, out_cols=w.ld)
+    return logp, lse, d, bad
+
+
+def test_tiny_workload():
+    """N=16, V=4096 fp32, tile 512 (8 tiles), rows 3 and 11 ignored, g = 1."""
+    w = wl.tiny()
+    logp, lse, d = run_fwd_bwd(w)
+    ref_logp, ref_lse, ref_d, bad = oracle_fwd_bwd(w)
+    assert bad == 0
+    assert_close_abs(logp.cpu().numpy(), ref_logp, LOGP_ATOL, "logp")
+    assert_close_abs(lse.cpu().numpy(), ref_lse, LOGP_ATOL, "lse")
+    assert_close_abs(d.cpu().numpy(), ref_d, DLOGITS_ATOL, "dlogits")
+    ign = w.target_ids == w.ignore_index
+    # ignored rows: exactly +0.0, bit for bit
+    assert np.all(f32_bits(logp)[ign] == 0) and np.all(f32_bits(lse)[ign] == 0)
+    assert np.all(f32_bits(d)[ign] == 0)
+
+
+def test_minimal_example_autograd():
+    """The operator page's minimal example: [2, 4, 300] bf16, target[0, 0] ignored.
+
+    300 bf16 columns make 600-byte rows, which are not 16-byte aligned: this
+    also runs the element-by-element load path."""
+    import json
+    import os
+    ex = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "minimal_example.json")))
+    shape = ex["logits_shape"]
+    r = wl.rng(42, 0)
+    x32 = r.standard_normal(shape).astype(np.float32)
+    stored = wl.store(x32.reshape(-1, shape[-1]), "bfloat16")
+    target = r.integers(0, shape[-1], shape[:-1]).astype(np.int64)
+    for pos in ex["ignored_positions"]:
+        target[tuple(pos)] = ex["ignore_index"]
+    logits = device_logits(stored, "bfloat16").reshape(shape).requires_grad_(True)
+    t = torch.from_numpy(target).cuda()
+    out = bil.batch_invariant_logp(logits, t, ignore_index=ex["ignore_index"])
+    assert list(out.shape) == ex["expect"]["out_shape"]
+    assert out.dtype == torch.float32
+    assert out[0, 0].item() == ex["expect"]["out_at_ignored"]
+    out.sum().backward()
+    assert logits.grad is not None and logits.grad.dtype == torch.bfloat16
+    assert torch.all(logits.grad[0, 0] == 0)
+    ref_logp, _, _ = oracle.logp_fwd(stored, "bfloat16", shape[-1], target.reshape(-1), ex["ignore_index"])
+    assert_close_abs(out.detach().cpu().numpy().reshape(-1), ref_logp, LOGP_ATOL, "logp")
+    ref_d, _ = oracle.logp_bwd(stored, "bfloat16", shape[-1], target.reshape(-1), np.ones(8), ex["ignore_index"])
+    assert_rounded(host_bits(logits.grad.reshape(8, -1)), ref_d, "bfloat16", DLOGITS_ATOL, "dlogits")
+
+
+SHAPES = [(1, 1, 8), (3, 7, 8), (5, 300, 512), (4, 513, 512), (37, 4096, 512), (6, 4097, 4096),
+          (9, 12345, 1024), (2, 33000, 4096)]
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "float16"])
+@pytest.mark.parametrize("n,v,tile", SHAPES, ids=lambda x: str(x))
+def test_dtypes_and_ragged_shapes(dtype, n, v, tile):
+    w = wl.random_rows(seed=n * 7 + v, n_rows=n, vocab=v, dtype=dtype, scale=3.0, tile_v=tile,
+                       ignore_every=3 if n > 2 else 0)
+    logp, lse, d = run_fwd_bwd(w)
+    ref_logp, ref_lse, ref_d, bad = oracle_fwd_bwd(w)
+    assert bad == 0
+    assert_close_abs(logp.cpu().numpy(), ref_logp, LOGP_ATOL, "logp")
+    assert_close_abs(lse.cpu().numpy(), ref_lse, LOGP_ATOL, "lse")
+    assert_close_abs(d.cpu().numpy(), ref_d, DLOGITS_ATOL, "dlogits")
+
+
+@pytest.mark.parametrize("out_dtype", ["bfloat16", "float16"])
+def test_low_precision_dlogits_are_correctly_rounded(out_dtype):
+    w = wl.random_rows(seed=5, n_rows=24, vocab=20000, dtype="bfloat16", scale=3.0, tile_v=4096, ignore_every=5)
+    _, _, d = run_fwd_bwd(w, dlogits_dtype=out_dtype)
+    _, _, ref_d, _ = oracle_fwd_bwd(w)
+    frac = assert_rounded(host_bits(d), ref_d, out_dtype, DLOGITS_ATOL, "dlogits")
+    assert frac < 1e-3
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_partials_against_oracle_and_fused(dtype):
+    n, v, tile = 11, 10000, 1024
+    w = wl.random_rows(seed=11, n_rows=n, vocab=v, dtype=dtype, tile_v=tile, ignore_every=4)
+    nt = -(-v // tile)
+    x = device_logits(w.logits, dtype)
+    t = torch.from_numpy(w.target_ids).cuda()
+    pm = torch.full((n, nt), float("nan"), device="cuda")
+    ps = torch.full((n, nt), float("nan"), device="cuda")
+    tl = torch.full((n,), float("nan"), device="cuda")
+    bounds = [0, 3, 7, nt]
+    for b, e in zip(bounds[:-1], bounds[1:]):
+        bil.logp_tile_partials(x[:, b * tile:], t, v, tile, b, e, pm, ps, tl, w.ignore_index)
+    logp, lse = bil.logp_merge(pm, ps, nt, tl, t, v, w.ignore_index)
+    f_logp, f_lse = bil.logp_fwd(x, t, w.ignore_index, tile)
+    torch.cuda.synchronize()
+    assert np.array_equal(f32_bits(logp), f32_bits(f_logp))
+    assert np.array_equal(f32_bits(lse), f32_bits(f_lse))
+    rm, rs, rtl = oracle.tile_partials(w.logits, dtype, v, tile, 0, nt, w.target_ids, w.ignore_index)
+    gm, gs, gtl = pm.cpu().numpy(), ps.cpu().numpy(), tl.cpu().numpy()
+    assert np.array_equal(gm.astype(np.float64), rm), "tile maxima are exact"
+    act = w.target_ids != w.ignore_index
+    assert np.array_equal(gtl[act].astype(np.float64), rtl[act]), "target logits are copies"
+    rel = np.abs(gs[act] - rs[act]) / rs[act]
+    assert rel.max() <= PART_SUM_RTOL
+    assert np.all(gs[~act] == 0) and np.all(gm[~act] == -np.inf)
+
+
+def test_row_stride_padding_is_never_read():
+    """Pad columns hold NaN; the results equal those of the unpadded rows bit for bit."""
+    n, v = 9, 5000
+    w = wl.random_rows(seed=3, n_rows=n, vocab=v, ld=8192, dtype="bfloat16", tile_v=512, ignore_every=4)
+    x_pad = device_logits(w.logits, "bfloat16")
+    x = x_pad[:, :v].contiguous()
+    t = torch.from_numpy(w.target_ids).cuda()
+    a = bil.logp_fwd(x_pad, t, w.ignore_index, 512, vocab=v)
+    b = bil.logp_fwd(x, t, w.ignore_index, 512)
+    g = torch.from_numpy(w.grad_logp).cuda()
+    da = bil.logp_bwd(x_pad, t, a[1], g, w.ignore_index, vocab=v)
+    db = bil.logp_bwd(x, t, b[1], g, w.ignore_index)
+    torch.cuda.synchronize()
+    for p, q in zip(a, b):
+        assert np.array_equal(f32_bits(p), f32_bits(q))
+    assert np.array_equal(host_bits(da[:, :v]), host_bits(db))
+    assert np.all(host_bits(da[:, v:]) == 0)  # pad columns of the gradient: +0.0
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+def test_unaligned_rows_give_the_same_bits(dtype):
+    """A base pointer one element past a 16-byte boundary takes the element-by-element path."""
+    n, v = 7, 9000
+    w = wl.random_rows(seed=4, n_rows=n, vocab=v, ld=v + 8, dtype=dtype, tile_v=1024, ignore_every=3)
+    flat = device_logits(w.logits, dtype).reshape(-1)
+    big = torch.empty(flat.numel() + 8, dtype=flat.dtype, device="cuda")
+    big[1:1 + flat.numel()] = flat
+    x_odd = big[1:1 + flat.numel()].view(n, v + 8)
+    x = flat.view(n, v + 8)
+    assert x_odd.data_ptr() % 16 != 0 and x.data_ptr() % 16 == 0
+    t = torch.from_numpy(w.target_ids).cuda()
+    a = bil.logp_fwd(x, t, w.ignore_index, 1024, vocab=v)
+    b = bil.logp_fwd(x_odd, t, w.ignore_index, 1024, vocab=v)
+    g = torch.from_numpy(w.grad_logp).cuda()
+    da = bil.logp_bwd(x, t, a[1], g, w.ignore_index, vocab=v)
+    db = bil.logp_bwd(x_odd, t, a[1], g, w.ignore_index, vocab=v)
+    torch.cuda.synchronize()
+    for p, q in zip(a, b):
+        assert np.array_equal(f32_bits(p), f32_bits(q))
+    assert np.array_equal(host_bits(da), host_bits(db))
+
+
+def test_out_of_range_targets():
+    n, v = 6, 3000
+    w = wl.random_rows(seed=6, n_rows=n, vocab=v, dtype="bfloat16", tile_v=1024)
+    x = device_logits(w.logits, "bfloat16")
+    good = torch.from_numpy(w.target_ids).cuda()
+    bad = good.clone()
+    bad[1] = -1          # invalid with ignore_index -100
+    bad[4] = v           # one past the vocabulary
+    with pytest.raises(bil.BilError) as e:
+        bil.logp_fwd(x, bad, -100, 1024, validate=True)
+    assert e.value.status == 4
+    logp, lse = bil.logp_fwd(x, bad, -100, 1024, validate=False)
+    ref, ref_lse = bil.logp_fwd(x, good, -100, 1024)
+    torch.cuda.synchronize()
+    lp = logp.cpu().numpy()
+    assert np.isnan(lp[1]) and np.isnan(lp[4])
+    keep = [0, 2, 3, 5]
+    assert np.array_equal(f32_bits(logp)[keep], f32_bits(ref)[keep])
+    assert np.array_equal(f32_bits(lse), f32_bits(ref_lse))  # the LSE does not depend on the target
+    # ignore_index = -1 turns -1 into an ignored row
+    logp2, _ = bil.logp_fwd(x, bad, -1, 1024, validate=False)
+    assert logp2[1].item() == 0.0
+    # the merge validates the same way
+    nt = 3
+    pm = torch.empty(n, nt, device="cuda")
+    ps = torch.empty(n, nt, device="cuda")
+    tl = torch.empty(n, device="cuda")
+    bil.logp_tile_partials(x, good, v, 1024, 0, nt, pm, ps, tl)
+    with pytest.raises(bil.BilError):
+        bil.logp_merge(pm, ps, nt, tl, bad, v, validate=True)
+    # the backward of a row with an invalid target is NaN
+    g = torch.ones(n, device="cuda")
+    d = bil.logp_bwd(x, bad, lse, g, -100, dlogits_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.isnan(d[1]).all() and torch.isnan(d[4]).all() and not torch.isnan(d[0]).any()
+
+
+def test_special_values():
+    v = 600
+    x = np.zeros((4, v), np.float32)
+    x[0] = -np.inf                 # no distribution at all
+    x[1, 17] = np.nan              # NaN poisons its row only
+    x[2, :300] = -np.inf           # half the row impossible
+    x[3] = np.linspace(-5, 5, v)
+    t = np.array([3, 3, 400, 599], np.int64)
+    xd = torch.from_numpy(x).cuda()
+    logp, lse = bil.logp_fwd(xd, torch.from_numpy(t).cuda(), -100, 256)
+    ref_logp, ref_lse, _ = oracle.logp_fwd(x, "float32", v, t)
+    assert_close_abs(logp.cpu().numpy(), ref_logp, LOGP_ATOL, "logp")
+    assert_close_abs(lse.cpu().numpy(), ref_lse, LOGP_ATOL, "lse")
+
+
+def test_empty_batch_is_a_no_op():
+    x = torch.empty(0, 4096, dtype=torch.bfloat16, device="cuda")
+    t = torch.empty(0, dtype=torch.int64, device="cuda")
+    logp, lse = bil.logp_fwd(x, t)
+    assert logp.shape == (0,) and lse.shape == (0,)
+    d = bil.logp_bwd(x, t, lse, torch.empty(0, device="cuda"))
+    assert d.shape == (0, 4096)
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Canary bands around every output buffer stay untouched."""
+    n, v, tile = 13, 9999, 1024
+    w = wl.random_rows(seed=9, n_rows=n, vocab=v, dtype="bfloat16", tile_v=tile, ignore_every=4)
+    x = device_logits(w.logits, "bfloat16")
+    t = torch.from_numpy(w.target_ids).cuda()
+    guard = 64
+    canary = -12345.0
+    logp_buf = torch.full((n + 2 * guard,), canary, device="cuda")
+    lse_buf = torch.full((n + 2 * guard,), canary, device="cuda")
+    bil.logp_fwd(x, t, w.ignore_index, tile, out=logp_buf[guard:guard + n], lse=lse_buf[guard:guard + n])
+    nt = -(-v // tile)
+    ld_part = nt + 5
+    pm = torch.full((n, ld_part), canary, device="cuda")
+    ps = torch.full((n, ld_part), canary, device="cuda")
+    tl = torch.full((n + 2 * guard,), canary, device="cuda")
+    bil.logp_tile_partials(x[:, 2 * tile:], t, v, tile, 2, 6, pm, ps, tl[guard:guard + n], w.ignore_index)
+    d_buf = torch.full((n + 2, v + 40), canary, dtype=torch.float32, device="cuda")
+    d_view = d_buf[1:n + 1, :v]
+    bil.logp_bwd(x, t, lse_buf[guard:guard + n], torch.from_numpy(w.grad_logp).cuda(), w.ignore_index,
+                 dlogits_dtype=torch.float32, out=d_view)
+    torch.cuda.synchronize()
+    for buf in (logp_buf, lse_buf, tl):
+        assert torch.all(buf[:guard] == canary) and torch.all(buf[guard + n:] == canary)
+    assert torch.all(pm[:, :2] == canary) and torch.all(pm[:, 6:] == canary)
+    assert torch.all(ps[:, :2] == canary) and torch.all(ps[:, 6:] == canary)
+    assert torch.all(d_buf[0] == canary) and torch.all(d_buf[n + 1] == canary)
+    assert torch.all(d_buf[:, v:] == canary)
+
+
+def test_repeat_runs_are_bitwise_identical():
+    w = wl.random_rows(seed=12, n_rows=300, vocab=151936, dtype="bfloat16", tile_v=4096, ignore_every=7)
+    runs = [run_fwd_bwd(w, dlogits_dtype="bfloat16") for _ in range(3)]
+    for r in runs[1:]:
+        assert np.array_equal(f32_bits(r[0]), f32_bits(runs[0][0]))
+        assert np.array_equal(f32_bits(r[1]), f32_bits(runs[0][1]))
+        assert np.array_equal(host_bits(r[2]), host_bits(runs[0][2]))
