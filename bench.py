@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["bil", "reference"], default="bil")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--rows", type=int, default=16384,
+                    help="rows of the workload per GPU (smaller only for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -255,7 +257,7 @@ def run_bil(args):
     dist = init_dist(world, "nccl")
     bil.load()
 
-    w = wl.training()
+    w = wl.training(n_rows=args.rows)
     n, v = w.n_rows, w.vocab
     stored = np.ascontiguousarray(w.logits).view(np.int16)
     x_host = torch.from_numpy(stored).view(torch.bfloat16).pin_memory()

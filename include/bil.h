@@ -31,9 +31,10 @@
  *    checked on the host before anything is queued; a failed check queues
  *    nothing and writes nothing.  There is no fallback path.
  *  - Element types: BIL_F32, BIL_BF16, BIL_F16.  Targets are int64.
- *  - Rows whose starting address is 16-byte aligned are read with bulk
- *    asynchronous copies; other rows are read element by element.  The
- *    results are bit-identical either way.
+ *  - Rows whose starting address and stride are 16-byte aligned are read with
+ *    bulk asynchronous copies in whole 16-byte units (the unit holding column
+ *    vocab-1 may extend past it, never past column ld-1); other rows are read
+ *    element by element.  The results are bit-identical either way.
  *
  * Results are bitwise reproducible for a given tile_v, element type and
  * library build (the arithmetic is fixed in bil_contract_id()).
@@ -173,11 +174,27 @@ int bil_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab, i
                  int64_t out_cols, bil_stream_t stream);
 
 /*
+ * bil_stream_shape -- the pipeline shape the forward and tile-partials kernels
+ * use for a tile of tile_v elements of `dtype` (fused != 0: the fused forward
+ * with num_tiles tiles per row): the number of shared-memory stages in each
+ * block's ring, the number of consumer warps, and the block's dynamic shared
+ * memory in bytes.  Host arithmetic only; touches no device.  The stage count
+ * is always a multiple of the consumer count (each consumer warp owns its
+ * stages and meets them in fill order).
+ */
+int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, int *stages, int *consumers,
+                     int64_t *smem_bytes);
+
+/*
  * bil_watchdog_status -- every wait inside this library's kernels is
  * bounded.  A wait that runs out sets a bit in a per-device word, and the
  * kernel stops instead of hanging (its outputs are then incomplete).  This
  * call reads that word for the current device into *flags (0 = no wait ever
  * ran out) and clears it when `clear` is non-zero.  It synchronises the device.
+ * Bits: 1 a consumer's wait for a tile, 2 the producer's wait for a free
+ * stage, 4 its wait for a free row slot, 8 its wait for its own copies to
+ * land, 16 a consumer met a unit outside the launch's ranges (then stopped
+ * before using it).
  */
 int bil_watchdog_status(unsigned int *flags, int clear);
 

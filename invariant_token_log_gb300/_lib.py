@@ -26,6 +26,8 @@ SIGNATURES = {
                                       ctypes.c_int32, _p, _i64, _p, _p, _i64, _p, _p]),
     "bil_logp_merge": (_i32, [_p, _p, _i64, ctypes.c_int32, _i64, _p, _p, _i64, _i64, _p, _p, _i32, _p]),
     "bil_logp_bwd": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, _p, _p, _p, _i32, _i64, _i64, _p]),
+    "bil_stream_shape": (_i32, [_i32, ctypes.c_int32, _i64, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32),
+                                ctypes.POINTER(_i64)]),
     "bil_watchdog_status": (_i32, [ctypes.POINTER(_u), _i32]),
 }
 
@@ -69,6 +71,14 @@ def status_string(status: int) -> str:
 
 def contract_id() -> str:
     return load().bil_contract_id().decode()
+
+
+def stream_shape(dtype: int, tile_v: int, num_tiles: int, fused: bool) -> tuple[int, int, int]:
+    """(stages, consumer warps, shared-memory bytes) of the forward kernels' pipeline."""
+    st, cw, sm = _i32(0), _i32(0), _i64(0)
+    check("bil_stream_shape", load().bil_stream_shape(dtype, tile_v, num_tiles, int(fused), ctypes.byref(st),
+                                                      ctypes.byref(cw), ctypes.byref(sm)))
+    return st.value, cw.value, sm.value
 
 
 def check(fn: str, status: int) -> None:

@@ -79,56 +79,168 @@ struct Elem;
 template <>
 struct Elem<BIL_BF16> {
   static constexpr int kBytes = 2;
-  __device__ static __forceinline__ void group(const unsigned char* p, float (&x)[kGroup]) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-  }
+  static constexpr uint32_t kNegInf = 0xff80u;  // -inf bit pattern
   __device__ static __forceinline__ float one(const unsigned char* p) {
     return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
+  }
+  // the two elements of a packed word, low half first (exact widening)
+  __device__ static __forceinline__ void pair(uint32_t w, float& lo, float& hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  }
+  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
   }
 };
 
 template <>
 struct Elem<BIL_F16> {
   static constexpr int kBytes = 2;
-  __device__ static __forceinline__ void group(const unsigned char* p, float (&x)[kGroup]) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-      float2 f = __half22float2(h);
-      x[2 * i] = f.x;
-      x[2 * i + 1] = f.y;
-    }
-  }
+  static constexpr uint32_t kNegInf = 0xfc00u;
   __device__ static __forceinline__ float one(const unsigned char* p) {
     return __half2float(*reinterpret_cast<const __half*>(p));
+  }
+  __device__ static __forceinline__ void pair(uint32_t w, float& lo, float& hi) {
+    __half2 h = *reinterpret_cast<const __half2*>(&w);
+    const float2 f = __half22float2(h);
+    lo = f.x;
+    hi = f.y;
+  }
+  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
   }
 };
 
 template <>
 struct Elem<BIL_F32> {
   static constexpr int kBytes = 4;
-  __device__ static __forceinline__ void group(const unsigned char* p, float (&x)[kGroup]) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 16);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  }
+  static constexpr uint32_t kNegInf = 0xff800000u;
   __device__ static __forceinline__ float one(const unsigned char* p) {
     return *reinterpret_cast<const float*>(p);
   }
 };
 
-// One tile's float32 (max, sum-exp) partial, computed by one warp from the
-// tile's elements in shared memory.  The reduction order is fixed by the
-// element positions alone:
+// Packed float32 pairs (sm_100 family): each half is an independent IEEE
+// round-to-nearest operation, bit for bit what __fadd_rn / __fsub_rn /
+// __fmul_rn give.  A pair is held as a 64-bit word, first element low.
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ float lo_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a)); }
+__device__ __forceinline__ float hi_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a >> 32)); }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// contract_exp on both halves of a pair
+__device__ __forceinline__ uint64_t exp2_pair_of_diff(uint64_t x, uint64_t shift2) {
+  const uint64_t a = mul2(sub2(x, shift2), pk(kLog2e, kLog2e));
+  return pk(ex2_approx(lo_of(a)), ex2_approx(hi_of(a)));
+}
+
+// Per-group building blocks of the tile reduction.  A group is 8 consecutive
+// elements = kW 32-bit words (4 for 16-bit types, 8 for float32).
+template <int DT>
+struct Group {
+  static constexpr int EB = Elem<DT>::kBytes;
+  static constexpr int kW = EB * kGroup / 4;
+  static constexpr int kVec = kW / 4;  // 16-byte vectors per group
+
+  __device__ static __forceinline__ void load(const unsigned char* p, uint32_t (&w)[kW]) {
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      const uint4 q = *reinterpret_cast<const uint4*>(p + 16 * v);
+      w[4 * v] = q.x;
+      w[4 * v + 1] = q.y;
+      w[4 * v + 2] = q.z;
+      w[4 * v + 3] = q.w;
+    }
+  }
+  // elements j >= rem (past the vocabulary) become -inf: they cannot win the
+  // max and add exp(-inf) = +0 to the sum, i.e. leave it unchanged
+  __device__ static __forceinline__ void mask_tail(uint32_t (&w)[kW], int rem) {
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      if (j >= rem) {
+        if (EB == 4) {
+          w[j] = Elem<DT>::kNegInf;
+        } else if (j & 1) {
+          w[j / 2] = (w[j / 2] & 0x0000ffffu) | (Elem<DT>::kNegInf << 16);
+        } else {
+          w[j / 2] = (w[j / 2] & 0xffff0000u) | Elem<DT>::kNegInf;
+        }
+      }
+    }
+  }
+  // running max: packed pairs for 16-bit types, one float per slot for float32
+  __device__ static __forceinline__ void max_init(uint32_t (&mx)[kW]) {
+#pragma unroll
+    for (int i = 0; i < kW; ++i) mx[i] = EB == 4 ? Elem<DT>::kNegInf : (Elem<DT>::kNegInf * 0x10001u);
+  }
+  __device__ static __forceinline__ void max_acc(uint32_t (&mx)[kW], const uint32_t (&w)[kW]) {
+#pragma unroll
+    for (int i = 0; i < kW; ++i) {
+      if constexpr (EB == 4) {
+        mx[i] = __float_as_uint(fmaxf(__uint_as_float(mx[i]), __uint_as_float(w[i])));
+      } else {
+        mx[i] = Elem<DT>::max2(mx[i], w[i]);
+      }
+    }
+  }
+  __device__ static __forceinline__ float max_fin(const uint32_t (&mx)[kW]) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kW; ++i) {
+      if constexpr (EB == 4) {
+        m = fmaxf(m, __uint_as_float(mx[i]));
+      } else {
+        float lo, hi;
+        Elem<DT>::pair(mx[i], lo, hi);
+        m = fmaxf(m, fmaxf(lo, hi));
+      }
+    }
+    return m;
+  }
+  // a[k] holds the slot accumulators (a_2k, a_2k+1); adds exp(x_j - shift)
+  __device__ static __forceinline__ void sum_acc(uint64_t (&a)[4], const uint32_t (&w)[kW], uint64_t shift2) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint64_t x;
+      if constexpr (EB == 4) {
+        x = static_cast<uint64_t>(w[2 * k]) | (static_cast<uint64_t>(w[2 * k + 1]) << 32);
+      } else {
+        float lo, hi;
+        Elem<DT>::pair(w[k], lo, hi);
+        x = pk(lo, hi);
+      }
+      a[k] = add2(a[k], exp2_pair_of_diff(x, shift2));
+    }
+  }
+};
+
+// Groups lane `lane` holds of a tile of `valid` elements: g = lane + 32 i.
+__device__ __forceinline__ int lane_groups(int valid, int lane) {
+  const int groups = (valid + kGroup - 1) / kGroup;
+  return groups > lane ? (groups - lane + kLanes - 1) / kLanes : 0;
+}
+
+// One tile's float32 (max, sum-exp) partial, computed by one warp.  The
+// reduction order is fixed by the element positions alone:
 //   * element p of the tile (global column t*tile_v + p) sits in group
 //     g = p / 8 at slot j = p % 8; lane l takes groups l, l+32, l+64, ... in
 //     increasing order; `valid` elements exist (the rest are past the
@@ -139,55 +251,106 @@ struct Elem<BIL_F32> {
 //     the warp's sum is the butterfly over lanes (xor 16, 8, 4, 2, 1);
 //   * a tile whose max is -inf shifts by 0 instead, so it sums to 0 (or NaN
 //     if it holds a NaN) and its max stays -inf.
-// Nothing here depends on the row, the kernel or the launch geometry.
-template <int DT>
-__device__ __forceinline__ void tile_reduce(const unsigned char* tile, int valid, int lane,
-                                            float& m_out, float& s_out) {
-  constexpr int EB = Elem<DT>::kBytes;
-  const int full_groups = valid / kGroup;
-  const int rem = valid - full_groups * kGroup;  // elements in the ragged last group
-  float m = -INFINITY;
-  int g = lane;
-#pragma unroll 4
-  for (; g < full_groups; g += kLanes) {
-    float x[kGroup];
-    Elem<DT>::group(tile + static_cast<size_t>(g) * kGroup * EB, x);
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) m = fmaxf(m, x[j]);
-  }
-  if (rem != 0 && g == full_groups) {
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j)
-      if (j < rem) m = fmaxf(m, Elem<DT>::one(tile + (static_cast<size_t>(g) * kGroup + j) * EB));
-  }
-  m = warp_max(m);
-  const float shift = (m == -INFINITY) ? 0.0f : m;
+// Nothing here depends on the row, the kernel or the launch geometry.  Two
+// implementations follow, one reading a register copy of the lane's groups
+// (tiles of up to TileRegs::kMaxTile elements) and one reading shared memory
+// twice (larger tiles); they perform the same operations in the same order.
+__device__ __forceinline__ void finish_tile(float m, const uint64_t (&a)[4], float& m_out, float& s_out) {
+  float s = __fadd_rn(__fadd_rn(__fadd_rn(lo_of(a[0]), hi_of(a[0])), __fadd_rn(lo_of(a[1]), hi_of(a[1]))),
+                      __fadd_rn(__fadd_rn(lo_of(a[2]), hi_of(a[2])), __fadd_rn(lo_of(a[3]), hi_of(a[3]))));
+  s_out = warp_sum(s);
+  m_out = m;
+}
 
-  float a[kGroup];
+template <int DT>
+struct TileRegs {
+  static constexpr int kW = Group<DT>::kW;
+  static constexpr int kMaxGroups = 64 / kW;                     // 64 registers of tile data per lane
+  static constexpr int kMaxTile = kMaxGroups * kLanes * kGroup;  // 4096 (16-bit) / 2048 (float32)
+  uint32_t w[kMaxGroups][kW];
+};
+
+// FULL: the tile holds exactly TileRegs::kMaxTile valid elements, so every
+// lane has kMaxGroups whole groups and no test is needed per group.
+template <int DT, bool FULL>
+__device__ __forceinline__ void tile_load_regs_t(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r) {
+  constexpr int EB = Elem<DT>::kBytes;
+  const int ng = FULL ? TileRegs<DT>::kMaxGroups : lane_groups(valid, lane);
+  const int rem = valid % kGroup;
+  const int last = (valid - 1) / kGroup;  // index of the last group
 #pragma unroll
-  for (int j = 0; j < kGroup; ++j) a[j] = 0.0f;
-  g = lane;
-#pragma unroll 4
-  for (; g < full_groups; g += kLanes) {
-    float x[kGroup];
-    Elem<DT>::group(tile + static_cast<size_t>(g) * kGroup * EB, x);
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) a[j] = __fadd_rn(a[j], contract_exp(__fsub_rn(x[j], shift)));
-  }
-  if (rem != 0 && g == full_groups) {
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) {
-      if (j < rem) {
-        const float x = Elem<DT>::one(tile + (static_cast<size_t>(g) * kGroup + j) * EB);
-        a[j] = __fadd_rn(a[j], contract_exp(__fsub_rn(x, shift)));
-      }
+  for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i) {
+    if (FULL || i < ng) {
+      const int g = lane + kLanes * i;
+      Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, r.w[i]);
+      if (!FULL && rem != 0 && g == last) Group<DT>::mask_tail(r.w[i], rem);
     }
   }
-  float s = __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
-                      __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
-  s = warp_sum(s);
-  m_out = m;
-  s_out = s;
+}
+
+template <int DT, bool FULL>
+__device__ __forceinline__ void tile_reduce_regs_t(const TileRegs<DT>& r, int valid, int lane, float& m_out,
+                                                   float& s_out) {
+  const int ng = FULL ? TileRegs<DT>::kMaxGroups : lane_groups(valid, lane);
+  uint32_t mx[Group<DT>::kW];
+  Group<DT>::max_init(mx);
+#pragma unroll
+  for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i)
+    if (FULL || i < ng) Group<DT>::max_acc(mx, r.w[i]);
+  const float m = warp_max(Group<DT>::max_fin(mx));
+  const float shift = (m == -INFINITY) ? 0.0f : m;
+  const uint64_t shift2 = pk(shift, shift);
+  uint64_t a[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i)
+    if (FULL || i < ng) Group<DT>::sum_acc(a, r.w[i], shift2);
+  finish_tile(m, a, m_out, s_out);
+}
+
+template <int DT>
+__device__ __forceinline__ void tile_load_regs(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r) {
+  if (valid == TileRegs<DT>::kMaxTile) {
+    tile_load_regs_t<DT, true>(tile, valid, lane, r);
+  } else {
+    tile_load_regs_t<DT, false>(tile, valid, lane, r);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void tile_reduce_regs(const TileRegs<DT>& r, int valid, int lane, float& m_out,
+                                                 float& s_out) {
+  if (valid == TileRegs<DT>::kMaxTile) {
+    tile_reduce_regs_t<DT, true>(r, valid, lane, m_out, s_out);
+  } else {
+    tile_reduce_regs_t<DT, false>(r, valid, lane, m_out, s_out);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void tile_reduce_smem(const unsigned char* tile, int valid, int lane, float& m_out,
+                                                 float& s_out) {
+  constexpr int EB = Elem<DT>::kBytes;
+  const int groups = (valid + kGroup - 1) / kGroup;
+  const int rem = valid % kGroup;
+  uint32_t mx[Group<DT>::kW];
+  Group<DT>::max_init(mx);
+  for (int g = lane; g < groups; g += kLanes) {
+    uint32_t w[Group<DT>::kW];
+    Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, w);
+    if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
+    Group<DT>::max_acc(mx, w);
+  }
+  const float m = warp_max(Group<DT>::max_fin(mx));
+  const float shift = (m == -INFINITY) ? 0.0f : m;
+  const uint64_t shift2 = pk(shift, shift);
+  uint64_t a[4] = {0, 0, 0, 0};
+  for (int g = lane; g < groups; g += kLanes) {
+    uint32_t w[Group<DT>::kW];
+    Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, w);
+    if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
+    Group<DT>::sum_acc(a, w, shift2);
+  }
+  finish_tile(m, a, m_out, s_out);
 }
 
 // The fixed-order merge of one row's T tile partials, by one warp (all lanes
@@ -236,6 +399,7 @@ constexpr unsigned kWatchFull = 1u;      // consumer waited too long for a tile
 constexpr unsigned kWatchEmpty = 2u;     // producer waited too long for a free stage
 constexpr unsigned kWatchRowSlot = 4u;   // producer waited too long for a free row slot
 constexpr unsigned kWatchDrain = 8u;     // producer waited too long for its own copies
+constexpr unsigned kWatchProtocol = 16u; // a consumer met a unit outside the launch's ranges
 constexpr long long kWaitLimitNs = 2000000000LL;  // 2 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -264,6 +428,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase has not completed sleeps until it
+// completes or `hint_ns` pass, instead of returning at once: a waiting warp
+// then takes no issue slots from the warps doing the arithmetic.
+constexpr unsigned kSuspendHintNs = 200000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Warp-wide wait until the phase with parity `parity` has completed.  Every
 // lane polls (so every lane gets the barrier's acquire ordering) and the warp
 // leaves together.  Returns false if the wait ran out, or if another warp of
@@ -272,9 +453,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity, volati
                                           unsigned code) {
   long long start = 0;
   for (unsigned spin = 0;; ++spin) {
-    const bool done = mbar_try_wait(bar, parity);
+    const bool done = mbar_try_wait_sleep(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
-    if ((spin & 255u) == 255u) {
+    if ((spin & 15u) == 15u) {
       int stop = 0;
       if ((threadIdx.x % kLanes) == 0) {
         const long long now = global_ns();
@@ -323,6 +504,15 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
 // ---------------------------------------------------------------------------
 // The streaming forward (fused) and tile-partials kernel.
 // ---------------------------------------------------------------------------
+
+// Blocks of one producer and up to seven consumer warps, two blocks per SM:
+// 16 warps at no more than 128 registers each fill an SM's register file.
+#ifndef BIL_STREAM_MAX_CONSUMERS
+#define BIL_STREAM_MAX_CONSUMERS 7
+#endif
+constexpr int kStreamThreads = 256;
+constexpr int kMaxConsumers = BIL_STREAM_MAX_CONSUMERS < kStreamThreads / 32 - 1 ? BIL_STREAM_MAX_CONSUMERS
+                                                                                  : kStreamThreads / 32 - 1;
 
 struct StreamParams {
   const unsigned char* logits;  // column 0 = global column tile_begin * tile_v
@@ -414,7 +604,7 @@ __host__ __device__ inline size_t stream_smem_bytes(int stages, unsigned stage_b
 }
 
 template <int DT, bool FUSED, bool BULK>
-__global__ void __launch_bounds__(32 * 9) stream_kernel(const StreamParams p) {
+__global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   constexpr int EB = Elem<DT>::kBytes;
   Smem sm;
@@ -443,10 +633,9 @@ __global__ void __launch_bounds__(32 * 9) stream_kernel(const StreamParams p) {
   if (warp == 0) {
     // ---------------- producer warp ----------------
     const uint64_t policy = evict_first_policy();
-    int64_t k = 0;      // units issued
-    int64_t rows = 0;   // rows started (fused: row-slot uses)
     // The block's share of the work: whole rows (fused) or a contiguous range
-    // of (row, tile) units (partials).
+    // of (row, tile) units (partials).  Positions advance incrementally: no
+    // 64-bit division inside the loop.
     int64_t u0, u1;
     if (FUSED) {
       u0 = p.n_rows * blockIdx.x / gridDim.x * tiles_here;
@@ -456,92 +645,98 @@ __global__ void __launch_bounds__(32 * 9) stream_kernel(const StreamParams p) {
       u0 = total * blockIdx.x / gridDim.x;
       u1 = total * (blockIdx.x + 1) / gridDim.x;
     }
+    int64_t row = u0 / tiles_here;
+    int ti = static_cast<int>(u0 - row * tiles_here);  // tile within the range
+    int64_t left = u1 - u0;
+    int64_t k = 0;                 // units put in the ring
+    int stage = 0;                 // ring cursor: stage of unit k and its fill parity
+    unsigned phase = 0;
+    int slot = 0;                  // fused: row-slot cursor and its use parity
+    unsigned slot_phase = 0;
     bool ok = true;
-    int64_t cur_row = -1, cur_target = 0;
-    int cur_slot = 0;
-    for (int64_t u = u0; u < u1 && ok; ++u) {
-      const int64_t row = u / tiles_here;
-      const int tile = p.tile_begin + static_cast<int>(u - row * tiles_here);
-      if (row != cur_row) {
-        cur_row = row;
-        cur_target = p.targets[row];
-        if (cur_target == p.ignore_index) {
-          // Inactive row: its logits are never read.
-          if (FUSED) {
-            if (lane == 0) {
-              p.logp[row] = 0.0f;
-              if (p.lse != nullptr) p.lse[row] = 0.0f;
-            }
-          } else {
-            // this block's units of the row: tiles [tile, tile + n)
-            const int64_t n = min((row + 1) * tiles_here, u1) - u;
-            for (int64_t i = lane; i < n; i += kLanes) {
-              p.part_max[row * p.ld_part + tile + i] = -INFINITY;
-              p.part_sum[row * p.ld_part + tile + i] = 0.0f;
-            }
-          }
-          u = (row + 1) * tiles_here - 1;  // skip the row's remaining units
-          continue;
-        }
+    while (left > 0 && ok) {
+      const int64_t target = p.targets[row];
+      const int n = static_cast<int>(min(static_cast<int64_t>(tiles_here - ti), left));  // this row's units
+      if (target == p.ignore_index) {
+        // Inactive row: its logits are never read.
         if (FUSED) {
-          cur_slot = static_cast<int>(rows % p.row_slots);
-          const unsigned use = static_cast<unsigned>(rows / p.row_slots);
-          ok = warp_wait(&sm.row_free[cur_slot], (use & 1u) ^ 1u, abort, kWatchRowSlot);
+          if (lane == 0) {
+            p.logp[row] = 0.0f;
+            if (p.lse != nullptr) p.lse[row] = 0.0f;
+          }
+        } else {
+          for (int i = lane; i < n; i += kLanes) {
+            p.part_max[row * p.ld_part + p.tile_begin + ti + i] = -INFINITY;
+            p.part_sum[row * p.ld_part + p.tile_begin + ti + i] = 0.0f;
+          }
+        }
+      } else {
+        if (FUSED) {
+          ok = warp_wait(&sm.row_free[slot], slot_phase ^ 1u, abort, kWatchRowSlot);
           if (!ok) break;
           if (lane == 0) {
-            RowSlot& rs = sm.slots[cur_slot];
+            RowSlot& rs = sm.slots[slot];
             rs.row = row;
-            rs.target = cur_target;
+            rs.target = target;
             rs.target_logit = __int_as_float(0x7fc00000);
             rs.done = 0;
           }
-          ++rows;
         }
-      }
-      const int stage = static_cast<int>(k % S);
-      const unsigned fill = static_cast<unsigned>(k / S);
-      ok = warp_wait(&sm.empty[stage], (fill & 1u) ^ 1u, abort, kWatchEmpty);
-      if (!ok) break;
-      const int64_t col0 = static_cast<int64_t>(tile) * p.tile_v;  // global column
-      const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
-      const unsigned char* src =
-          p.logits + (row * p.ld + (col0 - static_cast<int64_t>(p.tile_begin) * p.tile_v)) * EB;
-      unsigned char* dst = sm.ring + static_cast<size_t>(stage) * p.stage_bytes;
-      if (lane == 0) {
-        UnitDesc d;
-        d.row = row;
-        d.tile = tile;
-        d.slot = cur_slot;
-        sm.desc[stage] = d;
-      }
-      if (BULK) {
-        if (lane == 0) {
-          const unsigned bytes = static_cast<unsigned>(align_up(static_cast<size_t>(valid) * EB, 16));
-          mbar_arrive_expect_tx(&sm.full[stage], bytes);
-          bulk_g2s(dst, src, bytes, &sm.full[stage], policy);
-        }
-      } else {
-        // Rows that are not 16-byte aligned: the producer warp copies the
-        // tile element by element into the same shared-memory layout.
-        for (int i = lane; i < valid; i += kLanes) {
-          if (EB == 2) {
-            reinterpret_cast<uint16_t*>(dst)[i] = reinterpret_cast<const uint16_t*>(src)[i];
+        const unsigned char* row_src = p.logits + row * p.ld * EB;
+        for (int i = 0; i < n; ++i) {
+          const int tile = p.tile_begin + ti + i;
+          ok = warp_wait(&sm.empty[stage], phase ^ 1u, abort, kWatchEmpty);
+          if (!ok) break;
+          const int64_t col0 = static_cast<int64_t>(tile) * p.tile_v;  // global column
+          const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
+          const unsigned char* src = row_src + static_cast<int64_t>(ti + i) * p.tile_v * EB;
+          unsigned char* dst = sm.ring + static_cast<size_t>(stage) * p.stage_bytes;
+          if (lane == 0) {
+            UnitDesc d;
+            d.row = row;
+            d.tile = tile;
+            d.slot = slot;
+            sm.desc[stage] = d;
+          }
+          if (BULK) {
+            if (lane == 0) {
+              const unsigned bytes = static_cast<unsigned>(align_up(static_cast<size_t>(valid) * EB, 16));
+              mbar_arrive_expect_tx(&sm.full[stage], bytes);
+              bulk_g2s(dst, src, bytes, &sm.full[stage], policy);
+            }
           } else {
-            reinterpret_cast<uint32_t*>(dst)[i] = reinterpret_cast<const uint32_t*>(src)[i];
+            // Rows that are not 16-byte aligned: the producer warp copies the
+            // tile element by element into the same shared-memory layout.
+            for (int e = lane; e < valid; e += kLanes) {
+              if (EB == 2) {
+                reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(src)[e];
+              } else {
+                reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.full[stage]);
+          }
+          __syncwarp();
+          ++k;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.full[stage]);
+        if (FUSED && ++slot == p.row_slots) {
+          slot = 0;
+          slot_phase ^= 1u;
+        }
       }
-      __syncwarp();
-      ++k;
+      left -= n;
+      ++row;
+      ti = 0;
     }
     // One end marker per consumer warp: units k, k+1, ..., k+W-1 map to
     // consumers k % W, ..., so each consumer sees exactly one.
-    for (int w = 0; w < W && ok; ++w, ++k) {
-      const int stage = static_cast<int>(k % S);
-      const unsigned fill = static_cast<unsigned>(k / S);
-      ok = warp_wait(&sm.empty[stage], (fill & 1u) ^ 1u, abort, kWatchEmpty);
+    for (int w = 0; w < W && ok; ++w) {
+      ok = warp_wait(&sm.empty[stage], phase ^ 1u, abort, kWatchEmpty);
       if (!ok) break;
       if (lane == 0) {
         UnitDesc d;
@@ -552,6 +747,11 @@ __global__ void __launch_bounds__(32 * 9) stream_kernel(const StreamParams p) {
         mbar_arrive(&sm.full[stage]);
       }
       __syncwarp();
+      ++k;
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
     // Drain: no bulk copy of ours may still be landing in shared memory when
     // the block exits (consumers that gave up leave fills unconsumed).  The
@@ -574,25 +774,52 @@ __global__ void __launch_bounds__(32 * 9) stream_kernel(const StreamParams p) {
   }
 
   // ---------------- consumer warps ----------------
+  // Consumer cw takes units cw, cw+W, cw+2W, ...: with S a multiple of W
+  // these sit in its own stages cw, cw+W, ... in fill order, and each step
+  // wraps the ring at most once.
   const int cw = warp - 1;
-  for (int64_t k = cw;; k += W) {
-    const int stage = static_cast<int>(k % S);
-    const unsigned fill = static_cast<unsigned>(k / S);
-    if (!warp_wait(&sm.full[stage], fill & 1u, abort, kWatchFull)) break;
+  int stage = cw;
+  unsigned phase = 0;
+  for (;; stage += W) {
+    if (stage >= S) {
+      stage -= S;
+      phase ^= 1u;
+    }
+    if (!warp_wait(&sm.full[stage], phase, abort, kWatchFull)) break;
     const UnitDesc d = sm.desc[stage];
     if (d.row < 0) break;
+    // A unit outside this launch's ranges can only come from a broken
+    // pipeline protocol: record it and stop rather than touch memory with it.
+    if (d.row >= p.n_rows || d.tile < p.tile_begin || d.tile >= p.tile_end ||
+        (FUSED && (d.slot < 0 || d.slot >= p.row_slots))) {
+      if (lane == 0) {
+        atomicOr(&g_watchdog, kWatchProtocol);
+        *abort = 1;
+      }
+      break;
+    }
     const unsigned char* tile = sm.ring + static_cast<size_t>(stage) * p.stage_bytes;
     const int64_t col0 = static_cast<int64_t>(d.tile) * p.tile_v;
     const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
-    float m, s;
-    tile_reduce<DT>(tile, valid, lane, m, s);
     // The target logit is copied from the tile that owns it, never summed.
     const int64_t target = FUSED ? sm.slots[d.slot].target : p.targets[d.row];
     const bool owner = target >= col0 && target < col0 + valid;
     float tl = 0.0f;
     if (owner) tl = Elem<DT>::one(tile + static_cast<size_t>(target - col0) * EB);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[stage]);  // the stage may be refilled now
+    float m, s;
+    if (p.tile_v <= TileRegs<DT>::kMaxTile) {
+      // Copy the lane's groups to registers and hand the stage back to the
+      // producer at once, so that its next fill overlaps this reduction.
+      TileRegs<DT> regs;
+      tile_load_regs<DT>(tile, valid, lane, regs);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[stage]);
+      tile_reduce_regs<DT>(regs, valid, lane, m, s);
+    } else {
+      tile_reduce_smem<DT>(tile, valid, lane, m, s);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[stage]);  // the stage may be refilled now
+    }
 
     if (!FUSED) {
       if (lane == 0) {
@@ -728,29 +955,59 @@ __device__ __forceinline__ float grad_elem(float x, float L, float g, bool is_ta
   return __fmul_rn(g, __fsub_rn(is_target ? 1.0f : 0.0f, p));
 }
 
+// A group of 8 gradient elements from its stored logits, with the same
+// operations as grad_elem in packed pairs.  `jt` is the target's slot in the
+// group, or -1 when the target lies elsewhere.
 template <int DT>
-__device__ __forceinline__ void load_group_global(const unsigned char* p, float (&x)[kGroup]) {
-  if (Elem<DT>::kBytes == 2) {
-    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ void grad_group(const uint32_t (&w)[Group<DT>::kW], uint64_t L2, uint64_t g2, float g,
+                                           int jt, float (&y)[kGroup]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (DT == BIL_BF16) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-      } else {
-        __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-        float2 f = __half22float2(h);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-      }
+  for (int k = 0; k < 4; ++k) {
+    uint64_t x;
+    if constexpr (Elem<DT>::kBytes == 4) {
+      x = static_cast<uint64_t>(w[2 * k]) | (static_cast<uint64_t>(w[2 * k + 1]) << 32);
+    } else {
+      float lo, hi;
+      Elem<DT>::pair(w[k], lo, hi);
+      x = pk(lo, hi);
     }
-  } else {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    const uint64_t p = exp2_pair_of_diff(x, L2);      // (p_2k, p_2k+1)
+    const uint64_t d = mul2(g2, sub2(0, p));          // g * (0 - p)
+    y[2 * k] = lo_of(d);
+    y[2 * k + 1] = hi_of(d);
+    if (jt >= 0) {  // the one target column of the row: g * (1 - p)
+      if (jt == 2 * k) y[2 * k] = __fmul_rn(g, __fsub_rn(1.0f, lo_of(p)));
+      if (jt == 2 * k + 1) y[2 * k + 1] = __fmul_rn(g, __fsub_rn(1.0f, hi_of(p)));
+    }
   }
+}
+
+template <int DT>
+__device__ __forceinline__ void load_group_stream(const unsigned char* p, uint32_t (&w)[Group<DT>::kW]) {
+#pragma unroll
+  for (int v = 0; v < Group<DT>::kVec; ++v) {
+    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(p) + v);
+    w[4 * v] = q.x;
+    w[4 * v + 1] = q.y;
+    w[4 * v + 2] = q.z;
+    w[4 * v + 3] = q.w;
+  }
+}
+
+struct RowMeta {
+  int64_t target;
+  float lse, g;
+};
+
+__device__ __forceinline__ RowMeta row_meta(const int64_t* targets, const float* lse, const float* grad,
+                                            int64_t row, int64_t n_rows) {
+  RowMeta m{0, 0.0f, 0.0f};
+  if (row < n_rows) {
+    m.target = targets[row];
+    m.lse = lse[row];
+    m.g = grad[row];
+  }
+  return m;
 }
 
 template <int DT, int OT, bool VEC>
@@ -761,20 +1018,27 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(
     int64_t out_cols) {
   constexpr int EB = Elem<DT>::kBytes;
   constexpr int OB = Out<OT>::kBytes;
+  // Work unit u = row * chunks + chunk, units strided by the grid; (row,
+  // chunk) advance by a precomputed quotient and remainder.
   const int64_t chunks = (out_cols + kBwdChunk - 1) / kBwdChunk;
-  const int64_t units = n_rows * chunks;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int64_t row = u / chunks;
-    const int64_t c0 = (u - row * chunks) * kBwdChunk;
+  const int64_t d_row = gridDim.x / chunks, d_chunk = gridDim.x % chunks;
+  int64_t row = blockIdx.x / chunks, chunk = blockIdx.x % chunks;
+  RowMeta meta = row_meta(targets, lse, grad, row, n_rows);
+  while (row < n_rows) {
+    int64_t next_row = row + d_row, next_chunk = chunk + d_chunk;
+    if (next_chunk >= chunks) {
+      next_chunk -= chunks;
+      ++next_row;
+    }
+    const RowMeta next = row_meta(targets, lse, grad, next_row, n_rows);  // in flight during this unit
+
+    const int64_t c0 = chunk * kBwdChunk;
     const int64_t c1 = min(c0 + kBwdChunk, out_cols);
-    const int64_t t = targets[row];
+    const int64_t t = meta.target;
     unsigned char* out = dlogits + row * ld_out * OB;
     const bool active = t != ignore_index;
     const bool valid_target = t >= 0 && t < vocab;
-    const float L = active ? lse[row] : 0.0f;
-    const float g = active ? grad[row] : 0.0f;
-    // columns [c0, min(c1, vocab)) hold gradient, [max(c0, vocab), c1) are pad
-    const int64_t v1 = min(c1, vocab);
+    const int64_t v1 = min(c1, vocab);  // [c0, v1): gradient; [max(c0, vocab), c1): pad
     if (!active || !valid_target) {
       const float fill = active ? __int_as_float(0x7fc00000) : 0.0f;
       for (int64_t c = c0 + threadIdx.x; c < v1; c += kBwdThreads) Out<OT>::store1(out + c * OB, fill);
@@ -783,30 +1047,35 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(
       // vectors, all of a thread's loads issued before any arithmetic.
       const unsigned char* in = logits + row * ld * EB;
       const int64_t gend = c0 + ((v1 - c0) / kGroup) * kGroup;
-      float x[kBwdGroupsPerThread][kGroup];
+      const uint64_t L2 = pk(meta.lse, meta.lse), g2 = pk(meta.g, meta.g);
+      uint32_t w[kBwdGroupsPerThread][Group<DT>::kW];
 #pragma unroll
       for (int i = 0; i < kBwdGroupsPerThread; ++i) {
         const int64_t c = c0 + (static_cast<int64_t>(i) * kBwdThreads + threadIdx.x) * kGroup;
-        if (c < gend) load_group_global<DT>(in + c * EB, x[i]);
+        if (c < gend) load_group_stream<DT>(in + c * EB, w[i]);
       }
 #pragma unroll
       for (int i = 0; i < kBwdGroupsPerThread; ++i) {
         const int64_t c = c0 + (static_cast<int64_t>(i) * kBwdThreads + threadIdx.x) * kGroup;
         if (c < gend) {
+          const uint64_t off = static_cast<uint64_t>(t - c);
+          const int jt = off < static_cast<uint64_t>(kGroup) ? static_cast<int>(off) : -1;
           float y[kGroup];
-#pragma unroll
-          for (int j = 0; j < kGroup; ++j) y[j] = grad_elem(x[i][j], L, g, c + j == t);
+          grad_group<DT>(w[i], L2, g2, meta.g, jt, y);
           Out<OT>::store8(out + c * OB, y);
         }
       }
       for (int64_t c = gend + threadIdx.x; c < v1; c += kBwdThreads)
-        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), L, g, c == t));
+        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta.lse, meta.g, c == t));
     } else {
       const unsigned char* in = logits + row * ld * EB;
       for (int64_t c = c0 + threadIdx.x; c < v1; c += kBwdThreads)
-        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), L, g, c == t));
+        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta.lse, meta.g, c == t));
     }
     for (int64_t c = max(c0, vocab) + threadIdx.x; c < c1; c += kBwdThreads) Out<OT>::store1(out + c * OB, 0.0f);
+    row = next_row;
+    chunk = next_chunk;
+    meta = next;
   }
 }
 
@@ -868,8 +1137,16 @@ int check_targets_host(const int64_t* targets, int64_t n, int64_t ignore_index, 
   return BIL_OK;
 }
 
-// Pipeline shape for a stage size: about 96 KB of ring per block so that two
-// blocks share an SM, at least two stages, one consumer warp per two stages.
+// Pipeline shape for a stage size: a ring of about BIL_STREAM_RING_BYTES per
+// block (two blocks share an SM), at least two stages, up to
+// kMaxConsumers consumer warps, and a stage count that is a multiple of the
+// consumer count.  The last rule is what keeps the barrier protocol sound:
+// consumer c then owns stages c, c+W, c+2W, ... and meets them in fill
+// order, so it can never wait on a stage two fills ahead of the copy that is
+// landing in it (a wait only tells the parity of a stage's fill count apart).
+#ifndef BIL_STREAM_RING_BYTES
+#define BIL_STREAM_RING_BYTES (96 * 1024)
+#endif
 struct StreamShape {
   int stages, consumers, row_slots;
   size_t smem;
@@ -877,8 +1154,9 @@ struct StreamShape {
 
 StreamShape stream_shape(unsigned stage_bytes, int num_tiles, bool fused) {
   StreamShape s;
-  s.stages = static_cast<int>(std::max<size_t>(2, std::min<size_t>(32, (96u * 1024u) / stage_bytes)));
-  s.consumers = std::max(1, std::min(8, s.stages / 2));
+  const int most = static_cast<int>(std::max<size_t>(2, std::min<size_t>(32, BIL_STREAM_RING_BYTES / stage_bytes)));
+  s.consumers = std::min(kMaxConsumers, most);
+  s.stages = (most / s.consumers) * s.consumers;
   s.row_slots = fused ? 4 : 0;
   s.smem = stream_smem_bytes(s.stages, stage_bytes, s.row_slots, num_tiles, fused, nullptr, nullptr);
   return s;
@@ -891,6 +1169,7 @@ int launch_stream_t(const StreamParams& p0, cudaStream_t stream) {
   StreamParams p = p0;
   StreamShape shape = stream_shape(p.stage_bytes, p.num_tiles, FUSED);
   if (shape.smem > static_cast<size_t>(dev.max_smem_optin)) return BIL_E_UNSUPPORTED;
+  if (shape.consumers < 1 || shape.stages % shape.consumers != 0) return BIL_E_UNSUPPORTED;
   p.stages = shape.stages;
   p.consumers = shape.consumers;
   p.row_slots = shape.row_slots;
@@ -1138,6 +1417,21 @@ int bil_logp_bwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
     default:
       return BIL_E_DTYPE;
   }
+}
+
+int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, int* stages, int* consumers,
+                     int64_t* smem_bytes) {
+  const int eb = elem_bytes(dtype);
+  if (eb == 0) return BIL_E_DTYPE;
+  if (tile_v <= 0 || tile_v % kGroup != 0 || num_tiles < 1 || stages == nullptr || consumers == nullptr ||
+      smem_bytes == nullptr)
+    return BIL_E_INVALID_ARG;
+  if (static_cast<int64_t>(tile_v) * eb > BIL_MAX_TILE_BYTES) return BIL_E_UNSUPPORTED;
+  const StreamShape shape = stream_shape(static_cast<unsigned>(tile_v * eb), static_cast<int>(num_tiles), fused != 0);
+  *stages = shape.stages;
+  *consumers = shape.consumers;
+  *smem_bytes = static_cast<int64_t>(shape.smem);
+  return BIL_OK;
 }
 
 int bil_watchdog_status(unsigned int* flags, int clear) {

@@ -166,8 +166,10 @@ def logp_bwd(logits: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor, 
     odt = logits.dtype if dlogits_dtype is None else dlogits_dtype
     if out is None:
         out = torch.empty((n, width), dtype=odt, device=logits.device)
-    o2 = out.reshape(n, -1)
-    if o2.stride(-1) != 1 or o2.shape[1] < width:
+    if n == 0:
+        return out.reshape(logits.shape) if out.numel() == 0 else out
+    o2 = out if out.dim() == 2 else out.reshape(n, -1)
+    if o2.shape[0] != n or o2.stride(-1) != 1 or o2.shape[1] < width:
         raise ValueError("out must be row-major with at least the logits' columns")
     lib = _lib.load()
     with torch.cuda.device(logits.device):
