@@ -85,6 +85,13 @@ def max_over_ranks(value: float, dist, device=None) -> float:
     return float(t.item())
 
 
+def aggregate(rows_per_rank: int, world: int, steps: int, max_total_ms: float):
+    """(ms per step, whole-job rows/s): every rank processed its own rows per
+    step, and the job took as long as its slowest rank."""
+    ms_step = max_total_ms / steps
+    return ms_step, rows_per_rank * world * steps / (max_total_ms / 1e3)
+
+
 def barrier(dist, device=None):
     if dist is not None:
         if device is not None and device.type == "cuda":
@@ -304,9 +311,8 @@ def run_bil(args):
     clocks = sampler.summary(host_t0, host_t1)
 
     total_ms = max_over_ranks(total_ms, dist, dev)
-    ms_step = total_ms / K
+    ms_step, value = aggregate(n, world, K, total_ms)
     rows_total = n * world
-    value = rows_total * K / (total_ms / 1e3)
 
     active = int((w.target_ids != w.ignore_index).sum())
     fwd_bytes = active * v * 2 + n * (8 + 4 + 4)                 # logits read; targets, logp, lse

@@ -898,8 +898,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
 // at a time.
 // ---------------------------------------------------------------------------
 
+#ifndef BIL_BWD_GROUPS
+#define BIL_BWD_GROUPS 4
+#endif
 constexpr int kBwdThreads = 256;
-constexpr int kBwdGroupsPerThread = 4;
+constexpr int kBwdGroupsPerThread = BIL_BWD_GROUPS;  // 16-byte loads a thread has in flight per unit
 constexpr int kBwdChunk = kBwdThreads * kBwdGroupsPerThread * kGroup;  // 8192 columns per work unit
 
 template <int OT>
