@@ -42,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "bil.cu")
 REFERENCE_ROWS_PER_STEP = 256
-CPU_BASELINE_ROWS = 4096
+CPU_BASELINE_ROWS = 8192
 
 
 def parse():
@@ -325,34 +325,39 @@ def run_bil(args):
     step_gbs = (fwd_bytes + bwd_bytes) / (ms_step / 1e3) / 1e9  # per GPU
 
     # ---- end to end: pinned host inputs -> device -> kernels -> host results ----
+    # Through the public API for host-resident batches (HostStreamedLogp):
+    # row chunks stream in, are computed and stream out on three CUDA streams.
     e2e = None
     if args.e2e_steps > 0:
+        del d  # the streamed path keeps its own chunk buffers
         d_host = torch.empty((n, v), dtype=torch.bfloat16).pin_memory()
         logp_host = torch.empty(n, dtype=torch.float32).pin_memory()
+        pipe = bil.HostStreamedLogp(n, v, torch.bfloat16, torch.bfloat16, chunk_rows=2048, device=dev)
 
         def e2e_step():
-            x.copy_(x_host, non_blocking=True)
-            t.copy_(t_host, non_blocking=True)
-            g.copy_(g_host, non_blocking=True)
-            step()
-            logp_host.copy_(logp, non_blocking=True)
-            d_host.copy_(d, non_blocking=True)
-        e2e_step()
+            return pipe.run(x_host, t_host, g_host, logp_host, d_host, w.ignore_index, w.tile_v)
+        for _ in range(2):
+            e2e_step()
         torch.cuda.synchronize(dev)
         barrier(dist, dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
+        launches = 0
+        marks[0].record(stream)
+        for i in range(args.e2e_steps):
+            launches += e2e_step()
+            marks[i + 1].record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+        e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), dist, dev)
+        step_ms = [round(marks[i].elapsed_time(marks[i + 1]), 2) for i in range(args.e2e_steps)]
         h2d = x_host.numel() * 2 + t_host.numel() * 8 + g_host.numel() * 4
         d2h = d_host.numel() * 2 + logp_host.numel() * 4
         e2e = {"value": rows_total * args.e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps}
-        del d_host
+               "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps,
+               "path": "HostStreamedLogp: pinned host -> 2048-row chunks over 3 streams -> pinned host",
+               "host_link_gbs": (h2d + d2h) / (e2e_ms / args.e2e_steps / 1e3) / 1e9,
+               "gpu_launches": launches, "step_ms": step_ms}
+        del pipe, d_host
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

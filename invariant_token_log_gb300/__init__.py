@@ -9,6 +9,7 @@ PyTorch front end.  Build the library with
 ``python -m invariant_token_log_gb300.build``.
 """
 from ._lib import BilError, contract_id, library_path, load  # noqa: F401
+from .host_pipeline import HostStreamedLogp  # noqa: F401
 from .logp import (  # noqa: F401
     DEFAULT_TILE_V,
     IGNORE_INDEX,
