@@ -74,14 +74,15 @@ def load(defines: tuple[str, ...] = ()) -> ctypes.CDLL:
         lib.bil_oracle_num_threads.restype = i32
         lib.bil_oracle_num_threads.argtypes = []
         lib.bil_oracle_logp_fwd.restype = i64
-        lib.bil_oracle_logp_fwd.argtypes = [vp, i32, i64, i64, i64, vp, i64, dp, dp]
+        f64 = ctypes.c_double
+        lib.bil_oracle_logp_fwd.argtypes = [vp, i32, i64, i64, i64, vp, i64, f64, dp, dp, dp]
         lib.bil_oracle_tile_partials.restype = None
         lib.bil_oracle_tile_partials.argtypes = [vp, i32, i64, i64, i64, i64, i64, i64, vp,
-                                                 i64, dp, dp, i64, dp]
+                                                 i64, f64, dp, dp, dp, i64, dp]
         lib.bil_oracle_merge.restype = i64
-        lib.bil_oracle_merge.argtypes = [dp, dp, i64, i64, i64, dp, vp, i64, i64, dp, dp]
+        lib.bil_oracle_merge.argtypes = [dp, dp, dp, i64, i64, i64, dp, vp, i64, i64, dp, dp, dp]
         lib.bil_oracle_logp_bwd.restype = i64
-        lib.bil_oracle_logp_bwd.argtypes = [vp, i32, i64, i64, i64, vp, i64, dp, dp, i64, i64]
+        lib.bil_oracle_logp_bwd.argtypes = [vp, i32, i64, i64, i64, vp, i64, f64, dp, dp, dp, i64, i64]
         lib.bil_oracle_widen.restype = None
         lib.bil_oracle_widen.argtypes = [vp, i32, i64, dp]
         _libs[defines] = lib
@@ -115,28 +116,38 @@ def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
 
 
+def _optr(a):
+    return None if a is None else _ptr(a)
+
+
 def logp_fwd(logits: np.ndarray, dtype: str, vocab: int, target_ids: np.ndarray,
-             ignore_index: int = -100, defines: tuple[str, ...] = ()):
-    """float64 (logp[N], lse[N], n_invalid_targets) for the first ``vocab`` columns."""
+             ignore_index: int = -100, defines: tuple[str, ...] = (), temperature: float = 1.0,
+             entropy: bool = False):
+    """float64 (logp[N], lse[N], n_invalid_targets), plus entropy[N] when asked,
+    for the first ``vocab`` columns divided by ``temperature``."""
     n, ld = _check_logits(logits, dtype)
     tgt = np.ascontiguousarray(target_ids, dtype=np.int64)
     assert tgt.shape == (n,)
     logp = np.empty(n, np.float64)
     lse = np.empty(n, np.float64)
+    ent = np.empty(n, np.float64) if entropy else None
     bad = load(defines).bil_oracle_logp_fwd(_ptr(logits), _code(dtype), n, vocab, ld, _ptr(tgt),
-                                            ignore_index, _ptr(logp), _ptr(lse))
-    return logp, lse, int(bad)
+                                            ignore_index, float(temperature), _ptr(logp), _ptr(lse),
+                                            _optr(ent))
+    return (logp, lse, int(bad), ent) if entropy else (logp, lse, int(bad))
 
 
 def tile_partials(logits: np.ndarray, dtype: str, vocab: int, tile_v: int, tile_begin: int,
                   tile_end: int, target_ids: np.ndarray, ignore_index: int = -100,
                   part_max: np.ndarray | None = None, part_sum: np.ndarray | None = None,
-                  target_logit: np.ndarray | None = None, defines: tuple[str, ...] = ()):
+                  target_logit: np.ndarray | None = None, defines: tuple[str, ...] = (),
+                  temperature: float = 1.0, part_ent: np.ndarray | None = None):
     """Fill float64 [N, T] (max, sumexp) partials for tiles [tile_begin, tile_end).
 
     Arrays passed in are updated in place (so that several calls can fill one
     buffer, as the tensor-parallel ranks do); missing ones are created
-    (partials -inf / 0, target_logit NaN).
+    (partials -inf / 0, target_logit NaN).  ``part_ent``, when given, receives
+    the entropy partials sum exp(z - m) * (z - m).
     """
     n, ld = _check_logits(logits, dtype)
     num_tiles = -(-vocab // tile_v)
@@ -147,41 +158,48 @@ def tile_partials(logits: np.ndarray, dtype: str, vocab: int, tile_v: int, tile_
         part_sum = np.zeros((n, num_tiles))
     if target_logit is None:
         target_logit = np.full(n, np.nan)
-    for a in (part_max, part_sum):
+    for a in (part_max, part_sum) + ((part_ent,) if part_ent is not None else ()):
         assert a.dtype == np.float64 and a.flags.c_contiguous and a.shape[0] == n
+    assert part_ent is None or part_ent.shape == part_max.shape
     load(defines).bil_oracle_tile_partials(_ptr(logits), _code(dtype), n, vocab, ld, tile_v,
                                            tile_begin, tile_end, _ptr(tgt), ignore_index,
-                                           _ptr(part_max), _ptr(part_sum), part_max.shape[1],
-                                           _ptr(target_logit))
+                                           float(temperature), _ptr(part_max), _ptr(part_sum),
+                                           _optr(part_ent), part_max.shape[1], _ptr(target_logit))
     return part_max, part_sum, target_logit
 
 
 def merge(part_max: np.ndarray, part_sum: np.ndarray, target_logit: np.ndarray,
           target_ids: np.ndarray, vocab: int, ignore_index: int = -100,
-          defines: tuple[str, ...] = ()):
-    """Fixed-order merge of float64 partials: (logp[N], lse[N], n_invalid_targets)."""
+          defines: tuple[str, ...] = (), part_ent: np.ndarray | None = None):
+    """Fixed-order merge of float64 partials: (logp[N], lse[N], n_invalid_targets),
+    plus entropy[N] when ``part_ent`` is given."""
     n, num_tiles = part_max.shape
     tgt = np.ascontiguousarray(target_ids, dtype=np.int64)
     tl = np.ascontiguousarray(target_logit, dtype=np.float64)
     logp = np.empty(n, np.float64)
     lse = np.empty(n, np.float64)
-    bad = load(defines).bil_oracle_merge(_ptr(part_max), _ptr(part_sum), n, num_tiles,
+    ent = np.empty(n, np.float64) if part_ent is not None else None
+    bad = load(defines).bil_oracle_merge(_ptr(part_max), _ptr(part_sum), _optr(part_ent), n, num_tiles,
                                          part_max.shape[1], _ptr(tl), _ptr(tgt), ignore_index,
-                                         vocab, _ptr(logp), _ptr(lse))
-    return logp, lse, int(bad)
+                                         vocab, _ptr(logp), _ptr(lse), _optr(ent))
+    return (logp, lse, int(bad), ent) if part_ent is not None else (logp, lse, int(bad))
 
 
 def logp_bwd(logits: np.ndarray, dtype: str, vocab: int, target_ids: np.ndarray,
              grad_logp: np.ndarray, ignore_index: int = -100, out_cols: int | None = None,
-             defines: tuple[str, ...] = ()):
-    """float64 dlogits [N, out_cols] and the number of invalid targets."""
+             defines: tuple[str, ...] = (), temperature: float = 1.0,
+             grad_entropy: np.ndarray | None = None):
+    """float64 dlogits [N, out_cols] of g * logp (+ gH * entropy) and the number
+    of invalid targets."""
     n, ld = _check_logits(logits, dtype)
     out_cols = vocab if out_cols is None else out_cols
     tgt = np.ascontiguousarray(target_ids, dtype=np.int64)
     g = np.ascontiguousarray(grad_logp, dtype=np.float64)
+    gh = None if grad_entropy is None else np.ascontiguousarray(grad_entropy, dtype=np.float64)
     d = np.empty((n, out_cols), np.float64)
     bad = load(defines).bil_oracle_logp_bwd(_ptr(logits), _code(dtype), n, vocab, ld, _ptr(tgt),
-                                            ignore_index, _ptr(g), _ptr(d), out_cols, out_cols)
+                                            ignore_index, float(temperature), _ptr(g), _optr(gh),
+                                            _ptr(d), out_cols, out_cols)
     return d, int(bad)
 
 

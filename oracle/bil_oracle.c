@@ -29,13 +29,24 @@
  * the tile-partial and merge entry points exist so that the GPU's split mode
  * can be checked piece by piece.
  *
+ *  - "[RFC][ROCm] End-to-end optimization of bitwise VIME R/R beyond native
+ *    P/P", section "Workstream 3: fused ROCm LM-head and linear logp": an
+ *    optional full-vocabulary entropy output, and a temperature applied to the
+ *    logits at one fixed point.  Here z = x / temperature (float64 division),
+ *    p = softmax(z), logp = z_t - LSE(z), entropy H = -sum_c p_c log p_c, and
+ *    the backward of g * logp + g_H * H with respect to x is
+ *      (1 / temperature) * (g * ([c == t] - p_c) - g_H * p_c * (z_c - LSE + H)).
+ *    (dH/dz_c = -p_c (log p_c + H) follows from H = -sum_j p_j log p_j and
+ *    dp_j/dz_c = p_j ([j == c] - p_c).)
+ *
  * Readings taken where the pages are silent (each is listed with its reason in
  * the design notes):
  *  - ignored rows: lse = 0 and their logits are never read;
  *  - out-of-range target on an active row: logp = NaN and the row is counted
  *    as an error (the return value), nothing outside the row is read;
  *  - a row whose entries are all -inf: LSE = -inf, logp = NaN;
- *  - NaN anywhere in a row makes that row's LSE and logp NaN.
+ *  - NaN anywhere in a row makes that row's LSE and logp NaN;
+ *  - ignored rows have entropy 0 and a zero gradient whatever g_H is.
  *
  * Element types: 0 = float32, 1 = bfloat16, 2 = float16.  Every input value
  * is widened to double exactly.
@@ -80,7 +91,15 @@ static double from_f16_bits(uint16_t h) {
     return sign ? -v : v;
 }
 
-static double load(const void *base, int dtype, int64_t row, int64_t ld, int64_t col) {
+/* One row of stored logits, as the softmax sees it: z_c = x_c / temperature. */
+typedef struct {
+    const void *base;
+    int dtype;
+    int64_t row, ld;
+    double temperature;
+} RowView;
+
+static double load_raw(const void *base, int dtype, int64_t row, int64_t ld, int64_t col) {
     int64_t i = row * ld + col;
     if (dtype == ORACLE_BF16) {
         return from_bf16_bits(((const uint16_t *)base)[i]);
@@ -91,50 +110,62 @@ static double load(const void *base, int dtype, int64_t row, int64_t ld, int64_t
     return (double)((const float *)base)[i];
 }
 
+static double z_at(const RowView *v, int64_t col) {
+    double x = load_raw(v->base, v->dtype, v->row, v->ld, col);
+    return v->temperature == 1.0 ? x : x / v->temperature;
+}
+
 /* ---- log-sum-exp over columns [c0, c1) of one row --------------------------
- * The definition log(sum_c exp(x_c)), evaluated with the usual shift by the
- * maximum so that nothing overflows.  Returns the maximum in *m_out and the
- * shifted sum sum_c exp(x_c - max) in *s_out.  A range whose entries are all
- * -inf has max -inf and sum 0.  A NaN entry never wins the max (comparisons
- * with NaN are false) and makes the sum NaN. */
-static void max_and_sumexp(const void *base, int dtype, int64_t row, int64_t ld,
-                           int64_t c0, int64_t c1, double *m_out, double *s_out) {
+ * The definition log(sum_c exp(z_c)), evaluated with the usual shift by the
+ * maximum so that nothing overflows.  Returns the maximum in *m_out, the
+ * shifted sum sum_c exp(z_c - max) in *s_out and, when u_out is not NULL,
+ * sum_c exp(z_c - max) * (z_c - max) in *u_out (what the entropy needs).  A
+ * range whose entries are all -inf has max -inf and sums 0.  A NaN entry never
+ * wins the max (comparisons with NaN are false) and makes the sums NaN. */
+static void max_and_sumexp(const RowView *v, int64_t c0, int64_t c1, double *m_out, double *s_out,
+                           double *u_out) {
     double m = -INFINITY;
     for (int64_t c = c0; c < c1; ++c) {
-        double x = load(base, dtype, row, ld, c);
-        if (x > m) {
-            m = x;
+        double z = z_at(v, c);
+        if (z > m) {
+            m = z;
         }
     }
-    double s = 0.0;
+    double s = 0.0, u = 0.0;
     if (m != -INFINITY) {
         for (int64_t c = c0; c < c1; ++c) {
 #ifdef BIL_ORACLE_MUTANT_SUM_SKIPS_FIRST
             if (c == c0) continue;
 #endif
-            double x = load(base, dtype, row, ld, c);
+            double d = z_at(v, c) - m;
 #ifdef BIL_ORACLE_MUTANT_NO_SHIFT_SIGN
-            s += exp(m - x);
+            double e = exp(-d);
 #else
-            s += exp(x - m);
+            double e = exp(d);
 #endif
+            s += e;
+            u += e * d;
         }
     } else {
         /* every entry is -inf (or the range is empty of finite values);
-         * a NaN entry still poisons the sum */
+         * a NaN entry still poisons the sums */
         for (int64_t c = c0; c < c1; ++c) {
-            if (isnan(load(base, dtype, row, ld, c))) {
+            if (isnan(z_at(v, c))) {
                 s = NAN;
+                u = NAN;
             }
         }
     }
     *m_out = m;
     *s_out = s;
+    if (u_out != NULL) {
+        *u_out = u;
+    }
 }
 
-static double row_lse(const void *base, int dtype, int64_t row, int64_t ld, int64_t vocab) {
+static double row_lse(const RowView *v, int64_t vocab) {
     double m, s;
-    max_and_sumexp(base, dtype, row, ld, 0, vocab, &m, &s);
+    max_and_sumexp(v, 0, vocab, &m, &s, NULL);
     if (m == -INFINITY && s == 0.0) {
         return -INFINITY;
     }
@@ -143,6 +174,26 @@ static double row_lse(const void *base, int dtype, int64_t row, int64_t ld, int6
 #else
     return m + log(s);
 #endif
+}
+
+/* Entropy of the row's distribution by its definition, -sum_c p_c log p_c
+ * with p_c = exp(z_c - L) and log p_c = z_c - L (L: the row's LSE). */
+static double row_entropy(const RowView *v, int64_t vocab, double L) {
+    double h = 0.0;
+    for (int64_t c = 0; c < vocab; ++c) {
+        double lp = z_at(v, c) - L;
+        double p = exp(lp);
+        if (p != 0.0) {
+#ifdef BIL_ORACLE_MUTANT_ENTROPY_SIGN
+            h += p * lp;
+#else
+            h -= p * lp;
+#endif
+        } else if (isnan(lp)) {
+            h = NAN;
+        }
+    }
+    return h;
 }
 
 int bil_oracle_num_threads(void) {
@@ -154,40 +205,48 @@ int bil_oracle_num_threads(void) {
 }
 
 /* ---- forward -----------------------------------------------------------------
- * "Reference Semantics": logp[r] = x[r, t_r] - LSE(x[r, :]) for active rows,
- * 0 for ignored rows.  lse[r] receives the row's LSE (0 for ignored rows).
+ * "Reference Semantics": logp[r] = z[r, t_r] - LSE(z[r, :]) for active rows,
+ * 0 for ignored rows.  lse[r] receives the row's LSE (0 for ignored rows);
+ * entropy[r] (when entropy is not NULL) the row's entropy (0 for ignored rows).
  * Returns the number of active rows whose target lies outside [0, vocab);
  * those rows get logp = NaN. */
 int64_t bil_oracle_logp_fwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
                             int64_t ld, const int64_t *target_ids, int64_t ignore_index,
-                            double *logp, double *lse) {
+                            double temperature, double *logp, double *lse, double *entropy) {
     int64_t bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
     for (int64_t r = 0; r < n_rows; ++r) {
+        RowView v = {logits, dtype, r, ld, temperature};
         int64_t t = target_ids[r];
 #ifndef BIL_ORACLE_MUTANT_IGNORE_NOT_ZEROED
         if (t == ignore_index) {
             logp[r] = 0.0;
             lse[r] = 0.0;
+            if (entropy != NULL) {
+                entropy[r] = 0.0;
+            }
             continue;
         }
 #endif
-        double L = row_lse(logits, dtype, r, ld, vocab);
+        double L = row_lse(&v, vocab);
         lse[r] = L;
+        if (entropy != NULL) {
+            entropy[r] = row_entropy(&v, vocab, L);
+        }
         if (t < 0 || t >= vocab) {
             logp[r] = NAN;
             bad += 1;
             continue;
         }
 #if defined(BIL_ORACLE_MUTANT_TARGET_OFF_BY_ONE)
-        double xt = load(logits, dtype, r, ld, t + 1 < vocab ? t + 1 : t);
+        double zt = z_at(&v, t + 1 < vocab ? t + 1 : t);
 #else
-        double xt = load(logits, dtype, r, ld, t);
+        double zt = z_at(&v, t);
 #endif
 #ifdef BIL_ORACLE_MUTANT_SIGN
-        logp[r] = L - xt;
+        logp[r] = L - zt;
 #else
-        logp[r] = xt - L;
+        logp[r] = zt - L;
 #endif
     }
     return bad;
@@ -197,21 +256,24 @@ int64_t bil_oracle_logp_fwd(const void *logits, int dtype, int64_t n_rows, int64
  * "Tensor Parallel", steps 1-2 and 5: the vocabulary is split into fixed tiles
  * of tile_v columns; tile t covers columns [t*tile_v, min((t+1)*tile_v, V)).
  * For every row and every tile t in [tile_begin, tile_end):
- *   part_max[r*ld_part + t] = max of the tile, part_sum[...] = sum exp(x - max).
- * The target logit is copied (never summed) into target_logit[r] when the
- * row's target lies in one of these tiles.  Ignored rows get (-inf, 0) and
+ *   part_max[r*ld_part + t] = max of the tile, part_sum[...] = sum exp(z - max),
+ *   part_ent[...] (when not NULL) = sum exp(z - max) * (z - max).
+ * The target logit z_t is copied (never summed) into target_logit[r] when the
+ * row's target lies in one of these tiles.  Ignored rows get (-inf, 0, 0) and
  * their logits are not read.  Columns are global column indices of the full
  * row held in `logits`. */
 void bil_oracle_tile_partials(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
                               int64_t ld, int64_t tile_v, int64_t tile_begin,
                               int64_t tile_end, const int64_t *target_ids,
-                              int64_t ignore_index, double *part_max, double *part_sum,
-                              int64_t ld_part, double *target_logit) {
+                              int64_t ignore_index, double temperature, double *part_max,
+                              double *part_sum, double *part_ent, int64_t ld_part,
+                              double *target_logit) {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = 0; r < n_rows; ++r) {
+        RowView v = {logits, dtype, r, ld, temperature};
         int64_t t_id = target_ids[r];
         for (int64_t t = tile_begin; t < tile_end; ++t) {
-            double m = -INFINITY, s = 0.0;
+            double m = -INFINITY, s = 0.0, u = 0.0;
             if (t_id != ignore_index) {
                 int64_t c0 = t * tile_v;
 #ifdef BIL_ORACLE_MUTANT_TILE_IGNORES_VOCAB
@@ -219,27 +281,34 @@ void bil_oracle_tile_partials(const void *logits, int dtype, int64_t n_rows, int
 #else
                 int64_t c1 = c0 + tile_v < vocab ? c0 + tile_v : vocab;
 #endif
-                max_and_sumexp(logits, dtype, r, ld, c0, c1, &m, &s);
+                max_and_sumexp(&v, c0, c1, &m, &s, &u);
                 if (t_id >= c0 && t_id < c1) {
-                    target_logit[r] = load(logits, dtype, r, ld, t_id);
+                    target_logit[r] = z_at(&v, t_id);
                 }
             }
             part_max[r * ld_part + t] = m;
             part_sum[r * ld_part + t] = s;
+            if (part_ent != NULL) {
+                part_ent[r * ld_part + t] = u;
+            }
         }
     }
 }
 
 /* ---- fixed-order merge -----------------------------------------------------------
  * "Tensor Parallel", steps 4 and 6:
- *   M = max_t m_t,  LSE = M + log(sum_{t=0..T-1} s_t * exp(m_t - M)),
- *   logp = target_logit - LSE;  ignored rows give 0.
+ *   M = max_t m_t,  w_t = exp(m_t - M),  S = sum_{t=0..T-1} s_t w_t,
+ *   LSE = M + log S,  logp = target_logit - LSE;  ignored rows give 0.
+ * Entropy from the same partials (an exact rewrite of -sum_c p_c log p_c: with
+ * d_c = z_c - m_t inside tile t, log p_c = d_c + (m_t - M) - log S):
+ *   H = log S - (1/S) sum_t w_t (u_t + (m_t - M) s_t).
  * Returns the number of active rows whose target lies outside [0, vocab)
  * (their logp is NaN). */
-int64_t bil_oracle_merge(const double *part_max, const double *part_sum, int64_t n_rows,
-                         int64_t num_tiles, int64_t ld_part, const double *target_logit,
-                         const int64_t *target_ids, int64_t ignore_index, int64_t vocab,
-                         double *logp, double *lse) {
+int64_t bil_oracle_merge(const double *part_max, const double *part_sum, const double *part_ent,
+                         int64_t n_rows, int64_t num_tiles, int64_t ld_part,
+                         const double *target_logit, const int64_t *target_ids,
+                         int64_t ignore_index, int64_t vocab, double *logp, double *lse,
+                         double *entropy) {
     int64_t bad = 0;
 #pragma omp parallel for schedule(static) reduction(+ : bad)
     for (int64_t r = 0; r < n_rows; ++r) {
@@ -247,6 +316,9 @@ int64_t bil_oracle_merge(const double *part_max, const double *part_sum, int64_t
         if (t_id == ignore_index) {
             logp[r] = 0.0;
             lse[r] = 0.0;
+            if (entropy != NULL) {
+                entropy[r] = 0.0;
+            }
             continue;
         }
         const double *m = part_max + r * ld_part;
@@ -257,7 +329,7 @@ int64_t bil_oracle_merge(const double *part_max, const double *part_sum, int64_t
                 M = m[t];
             }
         }
-        double L;
+        double L, H = NAN;
         if (M == -INFINITY) {
             L = -INFINITY;
             for (int64_t t = 0; t < num_tiles; ++t) {
@@ -266,17 +338,25 @@ int64_t bil_oracle_merge(const double *part_max, const double *part_sum, int64_t
                 }
             }
         } else {
-            double S = 0.0;
+            double S = 0.0, U = 0.0;
             for (int64_t t = 0; t < num_tiles; ++t) {
 #ifdef BIL_ORACLE_MUTANT_MERGE_TRANSPOSED
-                S += s[t] * exp(M - m[t]);
+                double w = exp(M - m[t]);
 #else
-                S += s[t] * exp(m[t] - M);
+                double w = exp(m[t] - M);
 #endif
+                S += s[t] * w;
+                if (part_ent != NULL) {
+                    U += w * (part_ent[r * ld_part + t] + (m[t] - M) * s[t]);
+                }
             }
             L = M + log(S);
+            H = log(S) - U / S;
         }
         lse[r] = L;
+        if (entropy != NULL) {
+            entropy[r] = H;
+        }
         if (t_id < 0 || t_id >= vocab) {
             logp[r] = NAN;
             bad += 1;
@@ -290,18 +370,22 @@ int64_t bil_oracle_merge(const double *part_max, const double *part_sum, int64_t
 /* ---- backward --------------------------------------------------------------------
  * "Batch-Invariance" (the backward reuses the per-row LSE) and "Reference
  * Semantics" (ignored rows receive zero gradient):
- *   dlogits[r, c] = g[r] * ([c == t_r] - exp(x[r, c] - LSE_r))
- * LSE_r is the oracle's own float64 value, recomputed here from the row.
- * Output is float64, row stride ld_out; columns [vocab, out_cols) of every
- * row are written as 0.  Returns the number of active rows with an
- * out-of-range target (their gradient row is NaN). */
+ *   dlogits[r, c] = (1/T) * (g[r] * ([c == t_r] - p_c) - gH[r] * p_c * (z_c - LSE + H))
+ * with p_c = exp(z_c - LSE), T the temperature; the second term only when
+ * grad_entropy is not NULL.  LSE and H are the oracle's own float64 values,
+ * recomputed here from the row.  Output is float64, row stride ld_out;
+ * columns [vocab, out_cols) of every row are written as 0.  Returns the
+ * number of active rows with an out-of-range target (their gradient row is
+ * NaN). */
 int64_t bil_oracle_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
                             int64_t ld, const int64_t *target_ids, int64_t ignore_index,
-                            const double *grad_logp, double *dlogits, int64_t ld_out,
+                            double temperature, const double *grad_logp,
+                            const double *grad_entropy, double *dlogits, int64_t ld_out,
                             int64_t out_cols) {
     int64_t bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
     for (int64_t r = 0; r < n_rows; ++r) {
+        RowView v = {logits, dtype, r, ld, temperature};
         double *d = dlogits + r * ld_out;
         int64_t t_id = target_ids[r];
         for (int64_t c = vocab; c < out_cols; ++c) {
@@ -320,18 +404,29 @@ int64_t bil_oracle_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64
             bad += 1;
             continue;
         }
-        double L = row_lse(logits, dtype, r, ld, vocab);
+        double L = row_lse(&v, vocab);
+        double H = grad_entropy != NULL ? row_entropy(&v, vocab, L) : 0.0;
         double g = grad_logp[r];
+        double gh = grad_entropy != NULL ? grad_entropy[r] : 0.0;
         for (int64_t c = 0; c < vocab; ++c) {
-            double p = exp(load(logits, dtype, r, ld, c) - L);
+            double z = z_at(&v, c);
+            double p = exp(z - L);
             double onehot = (c == t_id) ? 1.0 : 0.0;
 #if defined(BIL_ORACLE_MUTANT_BWD_SIGN)
-            d[c] = g * (p - onehot);
+            double dz = g * (p - onehot);
 #elif defined(BIL_ORACLE_MUTANT_BWD_NO_G)
-            d[c] = onehot - p;
+            double dz = onehot - p;
 #else
-            d[c] = g * (onehot - p);
+            double dz = g * (onehot - p);
 #endif
+            if (grad_entropy != NULL) {
+#ifdef BIL_ORACLE_MUTANT_BWD_ENTROPY_SIGN
+                dz += gh * p * (z - L + H);
+#else
+                dz -= gh * p * (z - L + H);
+#endif
+            }
+            d[c] = temperature == 1.0 ? dz : dz / temperature;
         }
     }
     return bad;
@@ -349,6 +444,6 @@ void bil_oracle_widen(const void *src, int dtype, int64_t count, double *dst) {
             continue;
         }
 #endif
-        dst[i] = load(src, dtype, 0, 0, i);
+        dst[i] = load_raw(src, dtype, 0, 0, i);
     }
 }

@@ -285,9 +285,129 @@ def check_special_values(defines=()):
     assert abs(logp[2] + math.log(20)) <= 1e-12
 
 
+def check_entropy(defines=()):
+    """Entropy: closed forms, the library's categorical entropy, 40-digit brute
+    force, and the partials-merge identity."""
+    import mpmath
+    import torch
+    # uniform logits: log V
+    for v in (1, 7, 4096):
+        x = np.full((1, v), 2.5, np.float32)
+        _, _, _, h = oracle.logp_fwd(x, "float32", v, np.array([0], np.int64), entropy=True, defines=defines)
+        assert abs(h[0] - math.log(v)) <= 1e-12, v
+    # one spike of height hgt over zeros
+    v, hgt = 1000, 6.0
+    x = np.zeros((1, v), np.float32)
+    x[0, 3] = hgt
+    _, _, _, h = oracle.logp_fwd(x, "float32", v, np.array([3], np.int64), entropy=True, defines=defines)
+    z = math.exp(hgt) + v - 1
+    pt, po = math.exp(hgt) / z, 1 / z
+    assert abs(h[0] + (pt * math.log(pt) + (v - 1) * po * math.log(po))) <= 1e-12
+    # two classes: the binary entropy
+    a, b = 1.25, -0.5
+    x = np.array([[a, b]], np.float32)
+    _, _, _, h = oracle.logp_fwd(x, "float32", 2, np.array([1], np.int64), entropy=True, defines=defines)
+    q = 1 / (1 + math.exp(-(a - b)))
+    assert abs(h[0] + q * math.log(q) + (1 - q) * math.log(1 - q)) <= 1e-12
+    # the library routine, all element types, ignored rows 0
+    for seed, (n, v, dtype) in enumerate([(6, 777, "float32"), (5, 1000, "bfloat16"), (4, 333, "float16")]):
+        x = _rows(seed + 30, n, v, scale=3.0, dtype=dtype)
+        t = _targets(seed + 30, n, v, ignore_rows=(1,))
+        _, _, _, h = oracle.logp_fwd(x, dtype, v, t, entropy=True, defines=defines)
+        ref = torch.distributions.Categorical(logits=torch.from_numpy(oracle.widen(x, dtype))).entropy().numpy()
+        act = t != wl.IGNORE_INDEX
+        assert np.abs(h[act] - ref[act]).max() <= 1e-12
+        assert np.all(h[~act] == 0.0)
+    # 40-digit brute force: -sum p log p with p = exp(x) / sum exp(x)
+    mpmath.mp.dps = 40
+    x = _rows(40, 2, 60, scale=2.0)
+    _, _, _, h = oracle.logp_fwd(x, "float32", 60, np.array([0, 1], np.int64), entropy=True, defines=defines)
+    for r in range(2):
+        tot = mpmath.fsum(mpmath.exp(mpmath.mpf(float(c))) for c in x[r])
+        ref = -mpmath.fsum((mpmath.exp(mpmath.mpf(float(c))) / tot) * (mpmath.mpf(float(c)) - mpmath.log(tot))
+                           for c in x[r])
+        assert abs(float(ref) - h[r]) <= 1e-12
+    # merged entropy partials equal the whole-row entropy for any tile size and split
+    for dtype, v, n in (("float32", 3000, 4), ("bfloat16", 1000, 3)):
+        x = _rows(41, n, v, scale=3.0, dtype=dtype)
+        t = _targets(41, n, v, ignore_rows=(0,))
+        _, _, _, ref = oracle.logp_fwd(x, dtype, v, t, entropy=True, defines=defines)
+        for tile in (8, 512, 4096):
+            nt = -(-v // tile)
+            for split in (1, 3):
+                pm, ps, pe = np.full((n, nt), -np.inf), np.zeros((n, nt)), np.zeros((n, nt))
+                tl = np.full(n, np.nan)
+                bnd = [(k * nt) // split for k in range(split + 1)]
+                for k in range(split):
+                    oracle.tile_partials(x, dtype, v, tile, bnd[k], bnd[k + 1], t, part_max=pm, part_sum=ps,
+                                         target_logit=tl, part_ent=pe, defines=defines)
+                _, _, _, h = oracle.merge(pm, ps, tl, t, v, part_ent=pe, defines=defines)
+                assert np.abs(h - ref).max() <= 1e-12, (dtype, tile, split)
+
+
+def check_temperature(defines=()):
+    """Temperature: dividing by a power of two is exact, so logp(x, T) must equal
+    logp(x / T, 1); arbitrary T against the library log-softmax of x / T; the
+    backward against finite differences."""
+    import torch
+    v = 513
+    x = _rows(50, 3, v, scale=3.0, grid=64)
+    t = np.array([5, 100, 512], np.int64)
+    for temp in (2.0, 0.5, 4.0):
+        y = (x / np.float32(temp)).astype(np.float32)
+        assert np.array_equal(y * np.float32(temp), x)
+        a, la, _, ha = oracle.logp_fwd(x, "float32", v, t, temperature=temp, entropy=True, defines=defines)
+        b, lb, _, hb = oracle.logp_fwd(y, "float32", v, t, entropy=True, defines=defines)
+        assert np.abs(a - b).max() <= 1e-12 and np.abs(la - lb).max() <= 1e-12 and np.abs(ha - hb).max() <= 1e-12
+    temp = 0.7
+    xt = torch.from_numpy(oracle.widen(x, "float32")) / temp
+    ref = torch.log_softmax(xt, -1).gather(-1, torch.from_numpy(t)[:, None])[:, 0].numpy()
+    got, _, _ = oracle.logp_fwd(x, "float32", v, t, temperature=temp, defines=defines)
+    assert np.abs(got - ref).max() <= 1e-12
+    # d(g logp + gh H)/dx by central differences, with a temperature
+    v, hstep = 48, 2.0 ** -12
+    x = _rows(51, 1, v, scale=2.0, grid=256)
+    t1 = np.array([7], np.int64)
+    g, gh = np.array([0.75]), np.array([-1.5])
+    d, _ = oracle.logp_bwd(x, "float32", v, t1, g, temperature=temp, grad_entropy=gh, defines=defines)
+
+    def f(xx):
+        lp, _, _, hh = oracle.logp_fwd(xx, "float32", v, t1, temperature=temp, entropy=True, defines=defines)
+        return g[0] * lp[0] + gh[0] * hh[0]
+    for c in (0, 7, 20, 47):
+        xp, xm = x.copy(), x.copy()
+        xp[0, c] += np.float32(hstep)
+        xm[0, c] -= np.float32(hstep)
+        fd = (f(xp) - f(xm)) / (2 * hstep)
+        assert abs(fd - d[0, c]) <= 1e-6, (c, fd, d[0, c])
+
+
+def check_entropy_gradient_library(defines=()):
+    """The backward with an entropy term against autograd of the library's
+    log-softmax and categorical entropy, in float64."""
+    import torch
+    for seed, (n, v, dtype, temp) in enumerate([(5, 300, "bfloat16", 1.0), (4, 1000, "float32", 0.8)]):
+        x = _rows(seed + 60, n, v, scale=3.0, dtype=dtype)
+        t = _targets(seed + 60, n, v, ignore_rows=(2,))
+        g = wl.rng(seed, 61).standard_normal(n)
+        gh = wl.rng(seed, 62).standard_normal(n)
+        d, _ = oracle.logp_bwd(x, dtype, v, t, g, temperature=temp, grad_entropy=gh, defines=defines)
+        xt = torch.from_numpy(oracle.widen(x, dtype)).requires_grad_(True)
+        z = xt / temp
+        tt = torch.from_numpy(t)
+        act = tt != wl.IGNORE_INDEX
+        sel = torch.log_softmax(z, -1).gather(-1, torch.where(act, tt, 0)[:, None])[:, 0]
+        ent = torch.distributions.Categorical(logits=z).entropy()
+        loss = (torch.where(act, sel, 0) * torch.from_numpy(g)).sum() + \
+               (torch.where(act, ent, 0) * torch.from_numpy(gh)).sum()
+        loss.backward()
+        assert np.abs(xt.grad.numpy() - d).max() <= 1e-12
+
+
 ALL_CHECKS = [check_widening, check_brute_force, check_library_log_softmax, check_closed_forms,
               check_invariants, check_finite_differences, check_tiles, check_contract_rules,
-              check_minimal_example, check_special_values]
+              check_minimal_example, check_special_values, check_entropy, check_temperature,
+              check_entropy_gradient_library]
 
 
 def check_rounding_helpers():

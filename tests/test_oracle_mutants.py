@@ -30,6 +30,8 @@ MUTANTS = [
     "BIL_ORACLE_MUTANT_BWD_SIGN",              # g * (p - onehot)
     "BIL_ORACLE_MUTANT_BWD_NO_G",              # upstream gradient dropped
     "BIL_ORACLE_MUTANT_BF16_WIDEN",            # bf16 bits shifted by 15 instead of 16
+    "BIL_ORACLE_MUTANT_ENTROPY_SIGN",          # +sum p log p
+    "BIL_ORACLE_MUTANT_BWD_ENTROPY_SIGN",      # entropy gradient term added instead of subtracted
 ]
 
 
