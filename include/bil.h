@@ -7,6 +7,13 @@
  *     logp[r] = logits[r, target_ids[r]] - logsumexp(logits[r, :])   (float32)
  *     logp[r] = 0.0 and d logits[r, :] = 0.0   when target_ids[r] == ignore_index
  *
+ * Optionally (the linear-logp operator of "[RFC][ROCm] End-to-end
+ * optimization of bitwise VIME R/R beyond native P/P", section "Workstream 3:
+ * fused ROCm LM-head and linear logp": temperature at one fixed point, and the
+ * full-vocabulary entropy) the softmax sees z = x * rcp with rcp = 1/T
+ * rounded once to float32, and the entropy H = -sum_c p_c log p_c is returned
+ * from the same pass.
+ *
  * The row's logsumexp is built the way the same page's section "Tensor
  * Parallel" (steps 1-6) builds it: the vocabulary is cut into fixed tiles of
  * tile_v columns; each tile gets a float32 (max m_t, sum-exp s_t) partial;
@@ -94,9 +101,12 @@ const char *bil_status_string(int status);
  *                whose target lies outside [0, vocab) gets logp = NaN (lse is
  *                still its LSE) and nothing outside the row is read.
  *  tile_v        vocabulary tile width (columns), see the limits above.
- *  logp          [n_rows] float32 output.
+ *  temperature   finite and > 0; 1 leaves the logits as they are (bit for bit).
+ *  logp          [n_rows] float32 output: z_t - LSE(z).
  *  lse           [n_rows] float32 output (the per-row LSE the backward needs),
  *                or NULL when not wanted.
+ *  entropy       [n_rows] float32 output (-sum p log p; +0.0 for inactive
+ *                rows), or NULL.  Computing it does not change logp or lse.
  *  validate      0: no host synchronisation.  1: before queuing the kernel the
  *                call copies target_ids to the host (synchronising `stream`)
  *                and returns BIL_E_TARGET_RANGE, queuing nothing, if an active
@@ -104,8 +114,8 @@ const char *bil_status_string(int status);
  *                validate trades a synchronisation for a checked range).
  */
 int bil_logp_fwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
-                 const int64_t *target_ids, int64_t ignore_index, int32_t tile_v, float *logp,
-                 float *lse, int validate, bil_stream_t stream);
+                 const int64_t *target_ids, int64_t ignore_index, int32_t tile_v, float temperature,
+                 float *logp, float *lse, float *entropy, int validate, bil_stream_t stream);
 
 /*
  * bil_logp_tile_partials -- one vocabulary shard's tile partials
@@ -120,20 +130,24 @@ int bil_logp_fwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab, i
  *                base plus tile_begin * tile_v elements; for a rank's own
  *                shard, pass the shard.  Global columns >= vocab are not read.
  *  target_ids    [n_rows] int64 GLOBAL target columns; ignored rows as above.
+ *  temperature   as for bil_logp_fwd.
  *  part_max,
  *  part_sum      [n_rows, ld_part] float32 (ld_part >= num_tiles).  For every row
  *                and every tile t of the range, column t receives the tile's
- *                max m_t and sum of exp(x - m_t).  Inactive rows receive
+ *                max m_t of z and sum of exp(z - m_t).  Inactive rows receive
  *                (-inf, 0).  Other columns are not touched, so several calls
  *                (ranks) can fill one buffer.
- *  target_logit  [n_rows] float32: written (a copy of the stored logit, widened
- *                exactly) only for active rows whose target lies in the range.
+ *  part_ent      [n_rows, ld_part] float32 (same row stride) receiving
+ *                sum exp(z - m_t) * (z - m_t) per tile (0 for inactive rows),
+ *                or NULL when the entropy is not wanted.
+ *  target_logit  [n_rows] float32: written (the stored logit widened exactly,
+ *                times rcp) only for active rows whose target lies in the range.
  */
 int bil_logp_tile_partials(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
                            int64_t ld, int32_t tile_v, int32_t tile_begin, int32_t tile_end,
-                           const int64_t *target_ids, int64_t ignore_index, float *part_max,
-                           float *part_sum, int64_t ld_part, float *target_logit,
-                           bil_stream_t stream);
+                           float temperature, const int64_t *target_ids, int64_t ignore_index,
+                           float *part_max, float *part_sum, float *part_ent, int64_t ld_part,
+                           float *target_logit, bil_stream_t stream);
 
 /*
  * bil_logp_merge -- the fixed-order merge and the combine ("Tensor Parallel",
@@ -141,25 +155,33 @@ int bil_logp_tile_partials(const void *logits, int dtype, int64_t n_rows, int64_
  * bil_logp_tile_partials with the same tile_v, however the tiles were split.
  *
  *  part_max, part_sum  [n_rows, ld_part] float32, columns [0, num_tiles) read.
+ *  part_ent, entropy   both NULL, or the entropy partials [n_rows, ld_part] and
+ *                      an [n_rows] float32 entropy output.
  *  target_logit        [n_rows] float32 (read for active rows with a valid target).
  *  target_ids, ignore_index, vocab   as for bil_logp_fwd (vocab only decides
  *                      which targets are valid).
  *  logp, lse           [n_rows] float32 outputs (lse may be NULL).
  *  validate            as for bil_logp_fwd.
  */
-int bil_logp_merge(const float *part_max, const float *part_sum, int64_t n_rows,
-                   int32_t num_tiles, int64_t ld_part, const float *target_logit,
+int bil_logp_merge(const float *part_max, const float *part_sum, const float *part_ent,
+                   int64_t n_rows, int32_t num_tiles, int64_t ld_part, const float *target_logit,
                    const int64_t *target_ids, int64_t ignore_index, int64_t vocab, float *logp,
-                   float *lse, int validate, bil_stream_t stream);
+                   float *lse, float *entropy, int validate, bil_stream_t stream);
 
 /*
  * bil_logp_bwd -- fused backward from the saved LSE ("Batch-Invariance":
  * one row tile per work unit, no cross-row reduction, no atomics; "Reference
- * Semantics": ignored rows receive a zero gradient).
+ * Semantics": ignored rows receive a zero gradient).  The gradient of
+ * g * logp + gh * H with respect to the stored logits x:
+ *     a = z - lse,  p = exp(a),  d = g * (onehot - p) [- gh * (p * (a + H))] [* rcp]
  *
- *  logits, dtype, n_rows, vocab, ld, target_ids, ignore_index   as for the forward.
+ *  logits, dtype, n_rows, vocab, ld, target_ids, ignore_index, temperature
+ *                as for the forward.
  *  lse           [n_rows] float32, the forward's lse output.
  *  grad_logp     [n_rows] float32 upstream gradient g of logp.
+ *  entropy,
+ *  grad_entropy  both NULL, or the forward's entropy output and the upstream
+ *                gradient gh of the entropy ([n_rows] float32 each).
  *  dlogits       [n_rows, ld_out] elements of type dlogits_dtype (BIL_F32 |
  *                BIL_BF16 | BIL_F16, rounded to nearest even).  Columns
  *                [0, vocab) receive g * (onehot - p); columns [vocab, out_cols)
@@ -169,21 +191,23 @@ int bil_logp_merge(const float *part_max, const float *part_sum, int64_t n_rows,
  *                an out-of-range target are NaN over [0, vocab).
  */
 int bil_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
-                 const int64_t *target_ids, int64_t ignore_index, const float *lse,
-                 const float *grad_logp, void *dlogits, int dlogits_dtype, int64_t ld_out,
+                 const int64_t *target_ids, int64_t ignore_index, float temperature,
+                 const float *lse, const float *grad_logp, const float *entropy,
+                 const float *grad_entropy, void *dlogits, int dlogits_dtype, int64_t ld_out,
                  int64_t out_cols, bil_stream_t stream);
 
 /*
  * bil_stream_shape -- the pipeline shape the forward and tile-partials kernels
  * use for a tile of tile_v elements of `dtype` (fused != 0: the fused forward
- * with num_tiles tiles per row): the number of shared-memory stages in each
+ * with num_tiles tiles per row; entropy != 0: with the entropy output): the
+ * number of shared-memory stages in each
  * block's ring, the number of consumer warps, and the block's dynamic shared
  * memory in bytes.  Host arithmetic only; touches no device.  The stage count
  * is always a multiple of the consumer count (each consumer warp owns its
  * stages and meets them in fill order).
  */
-int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, int *stages, int *consumers,
-                     int64_t *smem_bytes);
+int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, int entropy,
+                     int *stages, int *consumers, int64_t *smem_bytes);
 
 /*
  * bil_watchdog_status -- every wait inside this library's kernels is

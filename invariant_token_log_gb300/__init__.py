@@ -14,6 +14,7 @@ from .logp import (  # noqa: F401
     DEFAULT_TILE_V,
     IGNORE_INDEX,
     BatchInvariantLogp,
+    BatchInvariantLogpEntropy,
     batch_invariant_logp,
     logp_bwd,
     logp_fwd,

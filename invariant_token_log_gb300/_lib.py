@@ -18,16 +18,18 @@ MAX_FUSED_TILES = 2048
 
 # every entry point the header declares: name -> (restype, argtypes)
 _i32, _i64, _p, _u = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
+_f = ctypes.c_float
 SIGNATURES = {
     "bil_contract_id": (ctypes.c_char_p, []),
     "bil_status_string": (ctypes.c_char_p, [_i32]),
-    "bil_logp_fwd": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, ctypes.c_int32, _p, _p, _i32, _p]),
+    "bil_logp_fwd": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, ctypes.c_int32, _f, _p, _p, _p, _i32, _p]),
     "bil_logp_tile_partials": (_i32, [_p, _i32, _i64, _i64, _i64, ctypes.c_int32, ctypes.c_int32,
-                                      ctypes.c_int32, _p, _i64, _p, _p, _i64, _p, _p]),
-    "bil_logp_merge": (_i32, [_p, _p, _i64, ctypes.c_int32, _i64, _p, _p, _i64, _i64, _p, _p, _i32, _p]),
-    "bil_logp_bwd": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, _p, _p, _p, _i32, _i64, _i64, _p]),
-    "bil_stream_shape": (_i32, [_i32, ctypes.c_int32, _i64, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32),
-                                ctypes.POINTER(_i64)]),
+                                      ctypes.c_int32, _f, _p, _i64, _p, _p, _p, _i64, _p, _p]),
+    "bil_logp_merge": (_i32, [_p, _p, _p, _i64, ctypes.c_int32, _i64, _p, _p, _i64, _i64, _p, _p, _p, _i32, _p]),
+    "bil_logp_bwd": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, _f, _p, _p, _p, _p, _p, _i32, _i64, _i64,
+                            _p]),
+    "bil_stream_shape": (_i32, [_i32, ctypes.c_int32, _i64, _i32, _i32, ctypes.POINTER(_i32),
+                                ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
     "bil_watchdog_status": (_i32, [ctypes.POINTER(_u), _i32]),
 }
 
@@ -73,11 +75,11 @@ def contract_id() -> str:
     return load().bil_contract_id().decode()
 
 
-def stream_shape(dtype: int, tile_v: int, num_tiles: int, fused: bool) -> tuple[int, int, int]:
+def stream_shape(dtype: int, tile_v: int, num_tiles: int, fused: bool, entropy: bool = False) -> tuple[int, int, int]:
     """(stages, consumer warps, shared-memory bytes) of the forward kernels' pipeline."""
     st, cw, sm = _i32(0), _i32(0), _i64(0)
-    check("bil_stream_shape", load().bil_stream_shape(dtype, tile_v, num_tiles, int(fused), ctypes.byref(st),
-                                                      ctypes.byref(cw), ctypes.byref(sm)))
+    check("bil_stream_shape", load().bil_stream_shape(dtype, tile_v, num_tiles, int(fused), int(entropy),
+                                                      ctypes.byref(st), ctypes.byref(cw), ctypes.byref(sm)))
     return st.value, cw.value, sm.value
 
 

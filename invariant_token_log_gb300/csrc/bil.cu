@@ -36,6 +36,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 
 namespace {
 
@@ -48,6 +49,8 @@ constexpr int kGroup = 8;  // elements a lane takes at a time: 16 bytes of bf16/
 
 // log2(e) rounded to float32: exp(a) is evaluated as 2^(a * log2(e)).
 constexpr float kLog2e = 1.4426950408889634f;
+// The most negative finite float32.
+constexpr float kNegMax = -3.40282346638528859811704183484516925e38f;
 
 __device__ __forceinline__ float ex2_approx(float a) {
   float r;
@@ -147,12 +150,20 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-// contract_exp on both halves of a pair
-__device__ __forceinline__ uint64_t exp2_pair_of_diff(uint64_t x, uint64_t shift2) {
-  const uint64_t a = mul2(sub2(x, shift2), pk(kLog2e, kLog2e));
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// contract_exp on both halves of a pair of exponents
+__device__ __forceinline__ uint64_t exp2_pair(uint64_t d) {
+  const uint64_t a = mul2(d, pk(kLog2e, kLog2e));
   return pk(ex2_approx(lo_of(a)), ex2_approx(hi_of(a)));
 }
 
+// Temperature: the softmax sees z = x * rcp, rcp = 1/temperature rounded to
+// float32 on the host.  rcp = 1 leaves every value (and so every bit) as it is.
+//
 // Per-group building blocks of the tile reduction.  A group is 8 consecutive
 // elements = kW 32-bit words (4 for 16-bit types, 8 for float32).
 template <int DT>
@@ -172,7 +183,7 @@ struct Group {
     }
   }
   // elements j >= rem (past the vocabulary) become -inf: they cannot win the
-  // max and add exp(-inf) = +0 to the sum, i.e. leave it unchanged
+  // max and add exp(-inf) = +0 to the sums, i.e. leave them unchanged
   __device__ static __forceinline__ void mask_tail(uint32_t (&w)[kW], int rem) {
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
@@ -187,7 +198,8 @@ struct Group {
       }
     }
   }
-  // running max: packed pairs for 16-bit types, one float per slot for float32
+  // running max of the stored values: packed pairs for 16-bit types, one
+  // float per slot for float32
   __device__ static __forceinline__ void max_init(uint32_t (&mx)[kW]) {
 #pragma unroll
     for (int i = 0; i < kW; ++i) mx[i] = EB == 4 ? Elem<DT>::kNegInf : (Elem<DT>::kNegInf * 0x10001u);
@@ -216,19 +228,33 @@ struct Group {
     }
     return m;
   }
-  // a[k] holds the slot accumulators (a_2k, a_2k+1); adds exp(x_j - shift)
-  __device__ static __forceinline__ void sum_acc(uint64_t (&a)[4], const uint32_t (&w)[kW], uint64_t shift2) {
+  // the pair of stored values at slots (2k, 2k+1), widened exactly
+  __device__ static __forceinline__ uint64_t xpair(const uint32_t (&w)[kW], int k) {
+    if constexpr (EB == 4) {
+      return static_cast<uint64_t>(w[2 * k]) | (static_cast<uint64_t>(w[2 * k + 1]) << 32);
+    } else {
+      float lo, hi;
+      Elem<DT>::pair(w[k], lo, hi);
+      return pk(lo, hi);
+    }
+  }
+  // a[k] holds the slot accumulators (a_2k, a_2k+1) of exp(z - shift); with
+  // ENT, u[k] those of exp(z - shift) * (z - shift)
+  template <bool SCALED, bool ENT>
+  __device__ static __forceinline__ void sum_acc(uint64_t (&a)[4], uint64_t (&u)[4], const uint32_t (&w)[kW],
+                                                 uint64_t shift2, uint64_t rcp2) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      uint64_t x;
-      if constexpr (EB == 4) {
-        x = static_cast<uint64_t>(w[2 * k]) | (static_cast<uint64_t>(w[2 * k + 1]) << 32);
-      } else {
-        float lo, hi;
-        Elem<DT>::pair(w[k], lo, hi);
-        x = pk(lo, hi);
-      }
-      a[k] = add2(a[k], exp2_pair_of_diff(x, shift2));
+      uint64_t z = xpair(w, k);
+      if (SCALED) z = mul2(z, rcp2);
+      const uint64_t d = sub2(z, shift2);
+      const uint64_t e = exp2_pair(d);
+      a[k] = add2(a[k], e);
+      // p log p -> 0 as p -> 0: an element with z = -inf (or one masked past
+      // the vocabulary) has e = 0 and d = -inf; clamping d to the largest
+      // finite magnitude makes its term 0 instead of 0 * inf.  Finite d are
+      // left as they are.
+      if (ENT) u[k] = fma2(e, pk(fmaxf(lo_of(d), kNegMax), fmaxf(hi_of(d), kNegMax)), u[k]);
     }
   }
 };
@@ -239,27 +265,42 @@ __device__ __forceinline__ int lane_groups(int valid, int lane) {
   return groups > lane ? (groups - lane + kLanes - 1) / kLanes : 0;
 }
 
-// One tile's float32 (max, sum-exp) partial, computed by one warp.  The
-// reduction order is fixed by the element positions alone:
+// One tile's float32 partial, computed by one warp: the max m of z, the sum
+// s of exp(z - m) and, when asked, the entropy sum u of exp(z - m) * (z - m).
+// The reduction order is fixed by the element positions alone:
 //   * element p of the tile (global column t*tile_v + p) sits in group
 //     g = p / 8 at slot j = p % 8; lane l takes groups l, l+32, l+64, ... in
 //     increasing order; `valid` elements exist (the rest are past the
 //     vocabulary and do not take part);
-//   * max: exact, so its order does not matter (NaN never wins);
-//   * sum: lane accumulator a_j (slot j) adds exp(x - m) for its groups in
+//   * max: exact, so its order does not matter (NaN never wins); it is taken
+//     on the stored values and then scaled, which equals the max of the
+//     scaled values because x -> x * rcp (rcp > 0) rounds monotonically;
+//   * sums: lane accumulator a_j (slot j) adds exp(z - m) for its groups in
 //     increasing order; the lane's sum is ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7));
-//     the warp's sum is the butterfly over lanes (xor 16, 8, 4, 2, 1);
+//     the warp's sum is the butterfly over lanes (xor 16, 8, 4, 2, 1); the
+//     entropy sum u follows the same tree with u_j = fma(e, z - m, u_j);
 //   * a tile whose max is -inf shifts by 0 instead, so it sums to 0 (or NaN
 //     if it holds a NaN) and its max stays -inf.
 // Nothing here depends on the row, the kernel or the launch geometry.  Two
 // implementations follow, one reading a register copy of the lane's groups
 // (tiles of up to TileRegs::kMaxTile elements) and one reading shared memory
 // twice (larger tiles); they perform the same operations in the same order.
-__device__ __forceinline__ void finish_tile(float m, const uint64_t (&a)[4], float& m_out, float& s_out) {
-  float s = __fadd_rn(__fadd_rn(__fadd_rn(lo_of(a[0]), hi_of(a[0])), __fadd_rn(lo_of(a[1]), hi_of(a[1]))),
-                      __fadd_rn(__fadd_rn(lo_of(a[2]), hi_of(a[2])), __fadd_rn(lo_of(a[3]), hi_of(a[3]))));
-  s_out = warp_sum(s);
-  m_out = m;
+struct TilePartial {
+  float m, s, u;
+};
+
+__device__ __forceinline__ float tree8(const uint64_t (&a)[4]) {
+  return __fadd_rn(__fadd_rn(__fadd_rn(lo_of(a[0]), hi_of(a[0])), __fadd_rn(lo_of(a[1]), hi_of(a[1]))),
+                   __fadd_rn(__fadd_rn(lo_of(a[2]), hi_of(a[2])), __fadd_rn(lo_of(a[3]), hi_of(a[3]))));
+}
+
+template <bool ENT>
+__device__ __forceinline__ TilePartial finish_tile(float m, const uint64_t (&a)[4], const uint64_t (&u)[4]) {
+  TilePartial r;
+  r.m = m;
+  r.s = warp_sum(tree8(a));
+  r.u = ENT ? warp_sum(tree8(u)) : 0.0f;
+  return r;
 }
 
 template <int DT>
@@ -288,23 +329,23 @@ __device__ __forceinline__ void tile_load_regs_t(const unsigned char* tile, int 
   }
 }
 
-template <int DT, bool FULL>
-__device__ __forceinline__ void tile_reduce_regs_t(const TileRegs<DT>& r, int valid, int lane, float& m_out,
-                                                   float& s_out) {
+template <int DT, bool FULL, bool SCALED, bool ENT>
+__device__ __forceinline__ TilePartial tile_reduce_regs_t(const TileRegs<DT>& r, int valid, int lane, float rcp) {
   const int ng = FULL ? TileRegs<DT>::kMaxGroups : lane_groups(valid, lane);
   uint32_t mx[Group<DT>::kW];
   Group<DT>::max_init(mx);
 #pragma unroll
   for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i)
     if (FULL || i < ng) Group<DT>::max_acc(mx, r.w[i]);
-  const float m = warp_max(Group<DT>::max_fin(mx));
+  float m = warp_max(Group<DT>::max_fin(mx));
+  if (SCALED) m = __fmul_rn(m, rcp);
   const float shift = (m == -INFINITY) ? 0.0f : m;
-  const uint64_t shift2 = pk(shift, shift);
-  uint64_t a[4] = {0, 0, 0, 0};
+  const uint64_t shift2 = pk(shift, shift), rcp2 = pk(rcp, rcp);
+  uint64_t a[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i)
-    if (FULL || i < ng) Group<DT>::sum_acc(a, r.w[i], shift2);
-  finish_tile(m, a, m_out, s_out);
+    if (FULL || i < ng) Group<DT>::template sum_acc<SCALED, ENT>(a, u, r.w[i], shift2, rcp2);
+  return finish_tile<ENT>(m, a, u);
 }
 
 template <int DT>
@@ -316,19 +357,19 @@ __device__ __forceinline__ void tile_load_regs(const unsigned char* tile, int va
   }
 }
 
-template <int DT>
-__device__ __forceinline__ void tile_reduce_regs(const TileRegs<DT>& r, int valid, int lane, float& m_out,
-                                                 float& s_out) {
-  if (valid == TileRegs<DT>::kMaxTile) {
-    tile_reduce_regs_t<DT, true>(r, valid, lane, m_out, s_out);
-  } else {
-    tile_reduce_regs_t<DT, false>(r, valid, lane, m_out, s_out);
+template <int DT, bool ENT>
+__device__ __forceinline__ TilePartial tile_reduce_regs(const TileRegs<DT>& r, int valid, int lane, float rcp) {
+  const bool full = valid == TileRegs<DT>::kMaxTile;
+  if (rcp == 1.0f) {
+    return full ? tile_reduce_regs_t<DT, true, false, ENT>(r, valid, lane, rcp)
+                : tile_reduce_regs_t<DT, false, false, ENT>(r, valid, lane, rcp);
   }
+  return full ? tile_reduce_regs_t<DT, true, true, ENT>(r, valid, lane, rcp)
+              : tile_reduce_regs_t<DT, false, true, ENT>(r, valid, lane, rcp);
 }
 
-template <int DT>
-__device__ __forceinline__ void tile_reduce_smem(const unsigned char* tile, int valid, int lane, float& m_out,
-                                                 float& s_out) {
+template <int DT, bool SCALED, bool ENT>
+__device__ __forceinline__ TilePartial tile_reduce_smem_t(const unsigned char* tile, int valid, int lane, float rcp) {
   constexpr int EB = Elem<DT>::kBytes;
   const int groups = (valid + kGroup - 1) / kGroup;
   const int rem = valid % kGroup;
@@ -340,51 +381,79 @@ __device__ __forceinline__ void tile_reduce_smem(const unsigned char* tile, int 
     if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
     Group<DT>::max_acc(mx, w);
   }
-  const float m = warp_max(Group<DT>::max_fin(mx));
+  float m = warp_max(Group<DT>::max_fin(mx));
+  if (SCALED) m = __fmul_rn(m, rcp);
   const float shift = (m == -INFINITY) ? 0.0f : m;
-  const uint64_t shift2 = pk(shift, shift);
-  uint64_t a[4] = {0, 0, 0, 0};
+  const uint64_t shift2 = pk(shift, shift), rcp2 = pk(rcp, rcp);
+  uint64_t a[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
   for (int g = lane; g < groups; g += kLanes) {
     uint32_t w[Group<DT>::kW];
     Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, w);
     if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
-    Group<DT>::sum_acc(a, w, shift2);
+    Group<DT>::template sum_acc<SCALED, ENT>(a, u, w, shift2, rcp2);
   }
-  finish_tile(m, a, m_out, s_out);
+  return finish_tile<ENT>(m, a, u);
+}
+
+template <int DT, bool ENT>
+__device__ __forceinline__ TilePartial tile_reduce_smem(const unsigned char* tile, int valid, int lane, float rcp) {
+  return rcp == 1.0f ? tile_reduce_smem_t<DT, false, ENT>(tile, valid, lane, rcp)
+                     : tile_reduce_smem_t<DT, true, ENT>(tile, valid, lane, rcp);
 }
 
 // The fixed-order merge of one row's T tile partials, by one warp (all lanes
-// return the same value):
-//   M = max_t m_t;  S = fma(s_t, exp(m_t - M), S) for t = 0, 1, ..., T-1
-//   (one rounding per step, from S = 0);  LSE = M + log(S) (log: CUDA logf).
+// return the same values):
+//   M = max_t m_t;  w_t = exp(m_t - M);  S = fma(s_t, w_t, S) for t = 0, 1,
+//   ..., T-1 (one rounding per step, from S = 0);  LSE = M + log(S) (log:
+//   CUDA logf).
+// With ENT, also the entropy from the partial sums u_t (an exact rewrite of
+// -sum p log p, since log p = (z - m_t) + (m_t - M) - log S in tile t):
+//   v_t = fma(m_t - M, s_t, u_t);  U = fma(v_t, w_t, U) in the same order;
+//   H = log(S) - U / S.
 // M = -inf (no finite logit in the row) gives LSE = -inf, or NaN if a partial
-// sum is NaN.  The exponentials are computed in parallel across lanes; the
-// chain of fused multiply-adds is the same sequential chain in every lane.
-__device__ __forceinline__ float merge_lse(const float* m, const float* s, int T, int lane) {
+// sum is NaN, and H = NaN.  The exponentials are computed in parallel across
+// lanes; the chains of fused multiply-adds are the same sequential chains in
+// every lane.
+template <bool ENT>
+__device__ __forceinline__ float merge_lse(const float* m, const float* s, const float* u, int T, int lane,
+                                           float* entropy) {
   float M = -INFINITY;
   for (int t = lane; t < T; t += kLanes) M = fmaxf(M, m[t]);
   M = warp_max(M);
   if (M == -INFINITY) {
     bool nan = false;
     for (int t = lane; t < T; t += kLanes) nan |= isnan(s[t]);
+    if (ENT) *entropy = __int_as_float(0x7fc00000);
     return __any_sync(0xffffffffu, nan) ? __int_as_float(0x7fc00000) : -INFINITY;
   }
-  float S = 0.0f;
+  float S = 0.0f, U = 0.0f;
   for (int t0 = 0; t0 < T; t0 += kLanes) {
     const int t = t0 + lane;
-    float e = 0.0f, st = 0.0f;
+    float e = 0.0f, st = 0.0f, dm = 0.0f, ut = 0.0f;
     if (t < T) {
-      e = contract_exp(__fsub_rn(m[t], M));
+      dm = __fsub_rn(m[t], M);
+      e = contract_exp(dm);
       st = s[t];
+      if (ENT) {
+        ut = u[t];
+        dm = fmaxf(dm, kNegMax);  // a tile of -inf (s_t = 0) then adds 0, not -inf * 0
+      }
     }
     const int n = min(kLanes, T - t0);
     for (int j = 0; j < n; ++j) {
       const float ej = __shfl_sync(0xffffffffu, e, j);
       const float sj = __shfl_sync(0xffffffffu, st, j);
       S = __fmaf_rn(sj, ej, S);
+      if (ENT) {
+        const float dmj = __shfl_sync(0xffffffffu, dm, j);
+        const float uj = __shfl_sync(0xffffffffu, ut, j);
+        U = __fmaf_rn(__fmaf_rn(dmj, sj, uj), ej, U);
+      }
     }
   }
-  return __fadd_rn(M, logf(S));
+  const float logS = logf(S);
+  if (ENT) *entropy = __fsub_rn(logS, __fdiv_rn(U, S));
+  return __fadd_rn(M, logS);
 }
 
 // ---------------------------------------------------------------------------
@@ -520,12 +589,15 @@ struct StreamParams {
   int tile_v, tile_begin, tile_end, num_tiles;
   const int64_t* targets;
   int64_t ignore_index;
+  float rcp;  // 1 / temperature, rounded to float32 on the host
   // fused outputs
   float* logp;
   float* lse;
+  float* entropy;  // with ENT
   // partials outputs
   float* part_max;
   float* part_sum;
+  float* part_ent;  // with ENT
   int64_t ld_part;
   float* target_logit;
   // pipeline shape
@@ -561,14 +633,16 @@ struct Smem {
   RowSlot* slots;
   float* slot_m;
   float* slot_s;
+  float* slot_u;
   int* abort;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline size_t stream_smem_bytes(int stages, unsigned stage_bytes, int row_slots,
-                                                    int num_tiles, bool fused, Smem* out,
+                                                    int num_tiles, bool fused, bool ent, Smem* out,
                                                     unsigned char* base) {
+  const size_t slot_floats = fused ? static_cast<size_t>(row_slots) * num_tiles : 0;
   size_t off = 0;
   const size_t ring = off;
   off += static_cast<size_t>(stages) * stage_bytes;
@@ -584,9 +658,11 @@ __host__ __device__ inline size_t stream_smem_bytes(int stages, unsigned stage_b
   const size_t slots = off;
   off += sizeof(RowSlot) * (fused ? row_slots : 0);
   const size_t sm = off;
-  off += sizeof(float) * (fused ? static_cast<size_t>(row_slots) * num_tiles : 0);
+  off += sizeof(float) * slot_floats;
   const size_t ss = off;
-  off += sizeof(float) * (fused ? static_cast<size_t>(row_slots) * num_tiles : 0);
+  off += sizeof(float) * slot_floats;
+  const size_t su = off;
+  off += sizeof(float) * (ent ? slot_floats : 0);
   const size_t ab = off;
   off += sizeof(int);
   if (out != nullptr) {
@@ -598,17 +674,19 @@ __host__ __device__ inline size_t stream_smem_bytes(int stages, unsigned stage_b
     out->slots = reinterpret_cast<RowSlot*>(base + slots);
     out->slot_m = reinterpret_cast<float*>(base + sm);
     out->slot_s = reinterpret_cast<float*>(base + ss);
+    out->slot_u = reinterpret_cast<float*>(base + su);
     out->abort = reinterpret_cast<int*>(base + ab);
   }
   return off;
 }
 
-template <int DT, bool FUSED, bool BULK>
+// ENT: also the entropy partials (partials) or the entropy (fused).
+template <int DT, bool FUSED, bool BULK, bool ENT>
 __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   constexpr int EB = Elem<DT>::kBytes;
   Smem sm;
-  stream_smem_bytes(p.stages, p.stage_bytes, p.row_slots, p.num_tiles, FUSED, &sm, smem_raw);
+  stream_smem_bytes(p.stages, p.stage_bytes, p.row_slots, p.num_tiles, FUSED, ENT, &sm, smem_raw);
   const int warp = threadIdx.x / kLanes;
   const int lane = threadIdx.x % kLanes;
   const int S = p.stages;
@@ -663,11 +741,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
           if (lane == 0) {
             p.logp[row] = 0.0f;
             if (p.lse != nullptr) p.lse[row] = 0.0f;
+            if (ENT) p.entropy[row] = 0.0f;
           }
         } else {
           for (int i = lane; i < n; i += kLanes) {
             p.part_max[row * p.ld_part + p.tile_begin + ti + i] = -INFINITY;
             p.part_sum[row * p.ld_part + p.tile_begin + ti + i] = 0.0f;
+            if (ENT) p.part_ent[row * p.ld_part + p.tile_begin + ti + i] = 0.0f;
           }
         }
       } else {
@@ -801,12 +881,16 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
     const unsigned char* tile = sm.ring + static_cast<size_t>(stage) * p.stage_bytes;
     const int64_t col0 = static_cast<int64_t>(d.tile) * p.tile_v;
     const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
-    // The target logit is copied from the tile that owns it, never summed.
+    // The target logit is copied from the tile that owns it, never summed
+    // (scaled by the temperature exactly as the tile's values are).
     const int64_t target = FUSED ? sm.slots[d.slot].target : p.targets[d.row];
     const bool owner = target >= col0 && target < col0 + valid;
     float tl = 0.0f;
-    if (owner) tl = Elem<DT>::one(tile + static_cast<size_t>(target - col0) * EB);
-    float m, s;
+    if (owner) {
+      tl = Elem<DT>::one(tile + static_cast<size_t>(target - col0) * EB);
+      if (p.rcp != 1.0f) tl = __fmul_rn(tl, p.rcp);
+    }
+    TilePartial tp;
     if (p.tile_v <= TileRegs<DT>::kMaxTile) {
       // Copy the lane's groups to registers and hand the stage back to the
       // producer at once, so that its next fill overlaps this reduction.
@@ -814,17 +898,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
       tile_load_regs<DT>(tile, valid, lane, regs);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[stage]);
-      tile_reduce_regs<DT>(regs, valid, lane, m, s);
+      tp = tile_reduce_regs<DT, ENT>(regs, valid, lane, p.rcp);
     } else {
-      tile_reduce_smem<DT>(tile, valid, lane, m, s);
+      tp = tile_reduce_smem<DT, ENT>(tile, valid, lane, p.rcp);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[stage]);  // the stage may be refilled now
     }
 
     if (!FUSED) {
       if (lane == 0) {
-        p.part_max[d.row * p.ld_part + d.tile] = m;
-        p.part_sum[d.row * p.ld_part + d.tile] = s;
+        p.part_max[d.row * p.ld_part + d.tile] = tp.m;
+        p.part_sum[d.row * p.ld_part + d.tile] = tp.s;
+        if (ENT) p.part_ent[d.row * p.ld_part + d.tile] = tp.u;
         if (owner) p.target_logit[d.row] = tl;
       }
       continue;
@@ -832,10 +917,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
     RowSlot& rs = sm.slots[d.slot];
     float* sm_m = sm.slot_m + static_cast<size_t>(d.slot) * p.num_tiles;
     float* sm_s = sm.slot_s + static_cast<size_t>(d.slot) * p.num_tiles;
+    float* sm_u = sm.slot_u + static_cast<size_t>(d.slot) * p.num_tiles;
     int before = 0;
     if (lane == 0) {
-      sm_m[d.tile] = m;
-      sm_s[d.tile] = s;
+      sm_m[d.tile] = tp.m;
+      sm_s[d.tile] = tp.s;
+      if (ENT) sm_u[d.tile] = tp.u;
       if (owner) rs.target_logit = tl;
       __threadfence_block();
       before = atomicAdd(&rs.done, 1);
@@ -845,12 +932,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
     // This warp reduced the row's last tile: merge the row.
     __threadfence_block();
     __syncwarp();
-    const float L = merge_lse(sm_m, sm_s, p.num_tiles, lane);
+    float H = 0.0f;
+    const float L = merge_lse<ENT>(sm_m, sm_s, sm_u, p.num_tiles, lane, &H);
     if (lane == 0) {
       const int64_t row = rs.row;
       const bool valid_target = rs.target >= 0 && rs.target < p.vocab;
       p.logp[row] = valid_target ? __fsub_rn(rs.target_logit, L) : __int_as_float(0x7fc00000);
       if (p.lse != nullptr) p.lse[row] = L;
+      if (ENT) p.entropy[row] = H;
       __threadfence_block();
       mbar_arrive(&sm.row_free[d.slot]);
     }
@@ -862,13 +951,15 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
 // Merge kernel: one warp per row, the same merge_lse as the fused forward.
 // ---------------------------------------------------------------------------
 
+template <bool ENT>
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ part_max,
-                                                    const float* __restrict__ part_sum, int64_t n_rows,
+                                                    const float* __restrict__ part_sum,
+                                                    const float* __restrict__ part_ent, int64_t n_rows,
                                                     int num_tiles, int64_t ld_part,
                                                     const float* __restrict__ target_logit,
                                                     const int64_t* __restrict__ targets,
                                                     int64_t ignore_index, int64_t vocab, float* logp,
-                                                    float* lse) {
+                                                    float* lse, float* entropy) {
   const int lane = threadIdx.x % kLanes;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / kLanes);
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / kLanes) + threadIdx.x / kLanes;
@@ -878,14 +969,18 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
       if (lane == 0) {
         logp[row] = 0.0f;
         if (lse != nullptr) lse[row] = 0.0f;
+        if (ENT) entropy[row] = 0.0f;
       }
       continue;
     }
-    const float L = merge_lse(part_max + row * ld_part, part_sum + row * ld_part, num_tiles, lane);
+    float H = 0.0f;
+    const float L = merge_lse<ENT>(part_max + row * ld_part, part_sum + row * ld_part,
+                                   ENT ? part_ent + row * ld_part : nullptr, num_tiles, lane, &H);
     if (lane == 0) {
       const bool valid = t >= 0 && t < vocab;
       logp[row] = valid ? __fsub_rn(target_logit[row], L) : __int_as_float(0x7fc00000);
       if (lse != nullptr) lse[row] = L;
+      if (ENT) entropy[row] = H;
     }
   }
 }
@@ -952,35 +1047,64 @@ struct Out<BIL_F16> {
   }
 };
 
-// One element of the gradient, exactly as the formula reads.
-__device__ __forceinline__ float grad_elem(float x, float L, float g, bool is_target) {
-  const float p = contract_exp(__fsub_rn(x, L));
-  return __fmul_rn(g, __fsub_rn(is_target ? 1.0f : 0.0f, p));
+// What one row of the backward needs: its target, saved LSE, the upstream
+// gradients of logp (g) and of the entropy (gh, with the row's entropy H),
+// and the temperature's reciprocal.
+struct RowMeta {
+  int64_t target;
+  float lse, g, H, gh;
+};
+
+// One element of the gradient, exactly as the formula reads:
+//   z = x * rcp;  a = z - lse;  p = exp(a);  d = g * (onehot - p)
+//   with entropy:  d = d - gh * (p * (a + H))      (d H / d z = -p (log p + H))
+//   with a temperature:  d = d * rcp                (d z / d x = rcp)
+__device__ __forceinline__ float grad_elem(float x, const RowMeta& m, bool is_target, float rcp, bool ent) {
+  const bool scaled = rcp != 1.0f;
+  const float z = scaled ? __fmul_rn(x, rcp) : x;
+  const float a = __fsub_rn(z, m.lse);
+  const float p = contract_exp(a);
+  float d = __fmul_rn(m.g, __fsub_rn(is_target ? 1.0f : 0.0f, p));
+  // p (log p + H) -> 0 as p -> 0: a clamped to the largest finite magnitude
+  // makes the term of an -inf logit 0 instead of 0 * inf
+  if (ent) d = __fsub_rn(d, __fmul_rn(m.gh, __fmul_rn(p, __fadd_rn(fmaxf(a, kNegMax), m.H))));
+  return scaled ? __fmul_rn(d, rcp) : d;
 }
 
 // A group of 8 gradient elements from its stored logits, with the same
 // operations as grad_elem in packed pairs.  `jt` is the target's slot in the
 // group, or -1 when the target lies elsewhere.
 template <int DT>
-__device__ __forceinline__ void grad_group(const uint32_t (&w)[Group<DT>::kW], uint64_t L2, uint64_t g2, float g,
+__device__ __forceinline__ void grad_group(const uint32_t (&w)[Group<DT>::kW], const RowMeta& m, float rcp, bool ent,
                                            int jt, float (&y)[kGroup]) {
+  const bool scaled = rcp != 1.0f;
+  const uint64_t L2 = pk(m.lse, m.lse), g2 = pk(m.g, m.g), rcp2 = pk(rcp, rcp);
+  const uint64_t gh2 = pk(m.gh, m.gh), H2 = pk(m.H, m.H);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    uint64_t x;
-    if constexpr (Elem<DT>::kBytes == 4) {
-      x = static_cast<uint64_t>(w[2 * k]) | (static_cast<uint64_t>(w[2 * k + 1]) << 32);
-    } else {
-      float lo, hi;
-      Elem<DT>::pair(w[k], lo, hi);
-      x = pk(lo, hi);
+    uint64_t z = Group<DT>::xpair(w, k);
+    if (scaled) z = mul2(z, rcp2);
+    const uint64_t a = sub2(z, L2);
+    const uint64_t p = exp2_pair(a);                  // (p_2k, p_2k+1)
+    uint64_t d = mul2(g2, sub2(0, p));                // g * (0 - p)
+    if (ent) {
+      const uint64_t ac = pk(fmaxf(lo_of(a), kNegMax), fmaxf(hi_of(a), kNegMax));
+      d = sub2(d, mul2(gh2, mul2(p, add2(ac, H2))));
     }
-    const uint64_t p = exp2_pair_of_diff(x, L2);      // (p_2k, p_2k+1)
-    const uint64_t d = mul2(g2, sub2(0, p));          // g * (0 - p)
+    if (scaled) d = mul2(d, rcp2);
     y[2 * k] = lo_of(d);
     y[2 * k + 1] = hi_of(d);
-    if (jt >= 0) {  // the one target column of the row: g * (1 - p)
-      if (jt == 2 * k) y[2 * k] = __fmul_rn(g, __fsub_rn(1.0f, lo_of(p)));
-      if (jt == 2 * k + 1) y[2 * k + 1] = __fmul_rn(g, __fsub_rn(1.0f, hi_of(p)));
+    if (jt >= 0) {  // the one target column of the row: g * (1 - p), then as above
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (jt == 2 * k + h) {
+          const float ph = h ? hi_of(p) : lo_of(p);
+          const float ah = h ? hi_of(a) : lo_of(a);
+          float dt = __fmul_rn(m.g, __fsub_rn(1.0f, ph));
+          if (ent) dt = __fsub_rn(dt, __fmul_rn(m.gh, __fmul_rn(ph, __fadd_rn(fmaxf(ah, kNegMax), m.H))));
+          y[2 * k + h] = scaled ? __fmul_rn(dt, rcp) : dt;
+        }
+      }
     }
   }
 }
@@ -997,28 +1121,42 @@ __device__ __forceinline__ void load_group_stream(const unsigned char* p, uint32
   }
 }
 
-struct RowMeta {
-  int64_t target;
-  float lse, g;
+struct BwdParams {
+  const unsigned char* logits;
+  int64_t n_rows, vocab, ld;
+  const int64_t* targets;
+  int64_t ignore_index;
+  const float* lse;
+  const float* grad;
+  const float* entropy;       // with an entropy gradient: the forward's entropy
+  const float* grad_entropy;  // NULL: no entropy term
+  float rcp;
+  unsigned char* dlogits;
+  int64_t ld_out, out_cols;
 };
 
-__device__ __forceinline__ RowMeta row_meta(const int64_t* targets, const float* lse, const float* grad,
-                                            int64_t row, int64_t n_rows) {
-  RowMeta m{0, 0.0f, 0.0f};
-  if (row < n_rows) {
-    m.target = targets[row];
-    m.lse = lse[row];
-    m.g = grad[row];
+__device__ __forceinline__ RowMeta row_meta(const BwdParams& bp, int64_t row) {
+  RowMeta m{0, 0.0f, 0.0f, 0.0f, 0.0f};
+  if (row < bp.n_rows) {
+    m.target = bp.targets[row];
+    m.lse = bp.lse[row];
+    m.g = bp.grad[row];
+    if (bp.grad_entropy != nullptr) {
+      m.H = bp.entropy[row];
+      m.gh = bp.grad_entropy[row];
+    }
   }
   return m;
 }
 
 template <int DT, int OT, bool VEC>
-__global__ void __launch_bounds__(kBwdThreads) bwd_kernel(
-    const unsigned char* __restrict__ logits, int64_t n_rows, int64_t vocab, int64_t ld,
-    const int64_t* __restrict__ targets, int64_t ignore_index, const float* __restrict__ lse,
-    const float* __restrict__ grad, unsigned char* __restrict__ dlogits, int64_t ld_out,
-    int64_t out_cols) {
+__global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams bp) {
+  const unsigned char* __restrict__ logits = bp.logits;
+  const int64_t n_rows = bp.n_rows, vocab = bp.vocab, ld = bp.ld, ignore_index = bp.ignore_index;
+  unsigned char* __restrict__ dlogits = bp.dlogits;
+  const int64_t ld_out = bp.ld_out, out_cols = bp.out_cols;
+  const float rcp = bp.rcp;
+  const bool ent = bp.grad_entropy != nullptr;
   constexpr int EB = Elem<DT>::kBytes;
   constexpr int OB = Out<OT>::kBytes;
   // Work unit u = row * chunks + chunk, units strided by the grid; (row,
@@ -1026,14 +1164,14 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(
   const int64_t chunks = (out_cols + kBwdChunk - 1) / kBwdChunk;
   const int64_t d_row = gridDim.x / chunks, d_chunk = gridDim.x % chunks;
   int64_t row = blockIdx.x / chunks, chunk = blockIdx.x % chunks;
-  RowMeta meta = row_meta(targets, lse, grad, row, n_rows);
+  RowMeta meta = row_meta(bp, row);
   while (row < n_rows) {
     int64_t next_row = row + d_row, next_chunk = chunk + d_chunk;
     if (next_chunk >= chunks) {
       next_chunk -= chunks;
       ++next_row;
     }
-    const RowMeta next = row_meta(targets, lse, grad, next_row, n_rows);  // in flight during this unit
+    const RowMeta next = row_meta(bp, next_row);  // in flight during this unit
 
     const int64_t c0 = chunk * kBwdChunk;
     const int64_t c1 = min(c0 + kBwdChunk, out_cols);
@@ -1050,7 +1188,6 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(
       // vectors, all of a thread's loads issued before any arithmetic.
       const unsigned char* in = logits + row * ld * EB;
       const int64_t gend = c0 + ((v1 - c0) / kGroup) * kGroup;
-      const uint64_t L2 = pk(meta.lse, meta.lse), g2 = pk(meta.g, meta.g);
       uint32_t w[kBwdGroupsPerThread][Group<DT>::kW];
 #pragma unroll
       for (int i = 0; i < kBwdGroupsPerThread; ++i) {
@@ -1064,16 +1201,16 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(
           const uint64_t off = static_cast<uint64_t>(t - c);
           const int jt = off < static_cast<uint64_t>(kGroup) ? static_cast<int>(off) : -1;
           float y[kGroup];
-          grad_group<DT>(w[i], L2, g2, meta.g, jt, y);
+          grad_group<DT>(w[i], meta, rcp, ent, jt, y);
           Out<OT>::store8(out + c * OB, y);
         }
       }
       for (int64_t c = gend + threadIdx.x; c < v1; c += kBwdThreads)
-        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta.lse, meta.g, c == t));
+        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta, c == t, rcp, ent));
     } else {
       const unsigned char* in = logits + row * ld * EB;
       for (int64_t c = c0 + threadIdx.x; c < v1; c += kBwdThreads)
-        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta.lse, meta.g, c == t));
+        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta, c == t, rcp, ent));
     }
     for (int64_t c = max(c0, vocab) + threadIdx.x; c < c1; c += kBwdThreads) Out<OT>::store1(out + c * OB, 0.0f);
     row = next_row;
@@ -1155,28 +1292,28 @@ struct StreamShape {
   size_t smem;
 };
 
-StreamShape stream_shape(unsigned stage_bytes, int num_tiles, bool fused) {
+StreamShape stream_shape(unsigned stage_bytes, int num_tiles, bool fused, bool ent) {
   StreamShape s;
   const int most = static_cast<int>(std::max<size_t>(2, std::min<size_t>(32, BIL_STREAM_RING_BYTES / stage_bytes)));
   s.consumers = std::min(kMaxConsumers, most);
   s.stages = (most / s.consumers) * s.consumers;
   s.row_slots = fused ? 4 : 0;
-  s.smem = stream_smem_bytes(s.stages, stage_bytes, s.row_slots, num_tiles, fused, nullptr, nullptr);
+  s.smem = stream_smem_bytes(s.stages, stage_bytes, s.row_slots, num_tiles, fused, ent, nullptr, nullptr);
   return s;
 }
 
-template <int DT, bool FUSED, bool BULK>
+template <int DT, bool FUSED, bool BULK, bool ENT>
 int launch_stream_t(const StreamParams& p0, cudaStream_t stream) {
   DeviceInfo dev;
   if (int st = device_info(&dev)) return st;
   StreamParams p = p0;
-  StreamShape shape = stream_shape(p.stage_bytes, p.num_tiles, FUSED);
+  StreamShape shape = stream_shape(p.stage_bytes, p.num_tiles, FUSED, ENT);
   if (shape.smem > static_cast<size_t>(dev.max_smem_optin)) return BIL_E_UNSUPPORTED;
   if (shape.consumers < 1 || shape.stages % shape.consumers != 0) return BIL_E_UNSUPPORTED;
   p.stages = shape.stages;
   p.consumers = shape.consumers;
   p.row_slots = shape.row_slots;
-  auto kernel = stream_kernel<DT, FUSED, BULK>;
+  auto kernel = stream_kernel<DT, FUSED, BULK, ENT>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(shape.smem)) != cudaSuccess)
     return BIL_E_CUDA;
@@ -1192,19 +1329,21 @@ int launch_stream_t(const StreamParams& p0, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
+template <int DT, bool FUSED>
+int launch_stream_dt(bool bulk, bool ent, const StreamParams& p, cudaStream_t stream) {
+  if (ent) return bulk ? launch_stream_t<DT, FUSED, true, true>(p, stream) : launch_stream_t<DT, FUSED, false, true>(p, stream);
+  return bulk ? launch_stream_t<DT, FUSED, true, false>(p, stream) : launch_stream_t<DT, FUSED, false, false>(p, stream);
+}
+
 template <bool FUSED>
-int launch_stream(int dtype, const StreamParams& p, cudaStream_t stream) {
+int launch_stream(int dtype, bool ent, const StreamParams& p, cudaStream_t stream) {
   const int eb = elem_bytes(dtype);
   const bool bulk = aligned(p.logits, 16) && (p.ld * eb) % 16 == 0;
   switch (dtype) {
-    case BIL_BF16:
-      return bulk ? launch_stream_t<BIL_BF16, FUSED, true>(p, stream) : launch_stream_t<BIL_BF16, FUSED, false>(p, stream);
-    case BIL_F16:
-      return bulk ? launch_stream_t<BIL_F16, FUSED, true>(p, stream) : launch_stream_t<BIL_F16, FUSED, false>(p, stream);
-    case BIL_F32:
-      return bulk ? launch_stream_t<BIL_F32, FUSED, true>(p, stream) : launch_stream_t<BIL_F32, FUSED, false>(p, stream);
-    default:
-      return BIL_E_DTYPE;
+    case BIL_BF16: return launch_stream_dt<BIL_BF16, FUSED>(bulk, ent, p, stream);
+    case BIL_F16: return launch_stream_dt<BIL_F16, FUSED>(bulk, ent, p, stream);
+    case BIL_F32: return launch_stream_dt<BIL_F32, FUSED>(bulk, ent, p, stream);
+    default: return BIL_E_DTYPE;
   }
 }
 
@@ -1218,10 +1357,18 @@ int check_tile(int dtype, int64_t vocab, int32_t tile_v, int64_t* num_tiles) {
   return BIL_OK;
 }
 
+// The temperature's reciprocal as the kernels use it: 1/T computed in double
+// and rounded once to float32.  T must be finite and > 0.
+int temperature_rcp(float temperature, float* rcp) {
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return BIL_E_INVALID_ARG;
+  const double r = 1.0 / static_cast<double>(temperature);
+  if (!(r < 3.0e38)) return BIL_E_INVALID_ARG;
+  *rcp = static_cast<float>(r);
+  return BIL_OK;
+}
+
 template <int DT, int OT>
-int launch_bwd_t(bool vec, const unsigned char* logits, int64_t n_rows, int64_t vocab, int64_t ld,
-                 const int64_t* targets, int64_t ignore_index, const float* lse, const float* grad,
-                 unsigned char* dlogits, int64_t ld_out, int64_t out_cols, cudaStream_t stream) {
+int launch_bwd_t(bool vec, const BwdParams& bp, cudaStream_t stream) {
   DeviceInfo dev;
   if (int st = device_info(&dev)) return st;
   auto kernel = vec ? bwd_kernel<DT, OT, true> : bwd_kernel<DT, OT, false>;
@@ -1229,30 +1376,19 @@ int launch_bwd_t(bool vec, const unsigned char* logits, int64_t n_rows, int64_t 
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBwdThreads, 0) != cudaSuccess)
     return BIL_E_CUDA;
   per_sm = std::max(1, per_sm);
-  const int64_t units = n_rows * ((out_cols + kBwdChunk - 1) / kBwdChunk);
+  const int64_t units = bp.n_rows * ((bp.out_cols + kBwdChunk - 1) / kBwdChunk);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(units, static_cast<int64_t>(dev.sms) * per_sm));
-  kernel<<<static_cast<unsigned>(grid), kBwdThreads, 0, stream>>>(logits, n_rows, vocab, ld, targets, ignore_index,
-                                                                  lse, grad, dlogits, ld_out, out_cols);
+  kernel<<<static_cast<unsigned>(grid), kBwdThreads, 0, stream>>>(bp);
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
 template <int DT>
-int launch_bwd_dt(int out_dtype, bool vec, const unsigned char* logits, int64_t n_rows, int64_t vocab,
-                  int64_t ld, const int64_t* targets, int64_t ignore_index, const float* lse,
-                  const float* grad, unsigned char* dlogits, int64_t ld_out, int64_t out_cols,
-                  cudaStream_t stream) {
+int launch_bwd_dt(int out_dtype, bool vec, const BwdParams& bp, cudaStream_t stream) {
   switch (out_dtype) {
-    case BIL_F32:
-      return launch_bwd_t<DT, BIL_F32>(vec, logits, n_rows, vocab, ld, targets, ignore_index, lse, grad, dlogits,
-                                       ld_out, out_cols, stream);
-    case BIL_BF16:
-      return launch_bwd_t<DT, BIL_BF16>(vec, logits, n_rows, vocab, ld, targets, ignore_index, lse, grad,
-                                        dlogits, ld_out, out_cols, stream);
-    case BIL_F16:
-      return launch_bwd_t<DT, BIL_F16>(vec, logits, n_rows, vocab, ld, targets, ignore_index, lse, grad, dlogits,
-                                       ld_out, out_cols, stream);
-    default:
-      return BIL_E_DTYPE;
+    case BIL_F32: return launch_bwd_t<DT, BIL_F32>(vec, bp, stream);
+    case BIL_BF16: return launch_bwd_t<DT, BIL_BF16>(vec, bp, stream);
+    case BIL_F16: return launch_bwd_t<DT, BIL_F16>(vec, bp, stream);
+    default: return BIL_E_DTYPE;
   }
 }
 
@@ -1265,16 +1401,19 @@ int launch_bwd_dt(int out_dtype, bool vec, const unsigned char* logits, int64_t 
 extern "C" {
 
 const char* bil_contract_id(void) {
-  return "bil.v1"
+  return "bil.v2"
          ";tile=fixed tile_v columns, valid columns < vocab"
+         ";z=x*rn rcp, rcp=float32(1/temperature) (rcp=1: z=x)"
          ";lanes=32x8: lane l takes 8-element groups l, l+32, ... in order"
-         ";max=exact"
-         ";exp(a)=ex2.approx.ftz.f32(a*rn log2e), a=x-rn m"
+         ";max=exact, on x, then *rn rcp"
+         ";exp(a)=ex2.approx.ftz.f32(a*rn log2e), a=z-rn m"
          ";lane_sum=8 slot accumulators, ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))"
          ";warp_sum=butterfly xor 16,8,4,2,1"
-         ";merge=M=max m_t; S=fma(s_t,exp(m_t-M),S) t=0..T-1; LSE=M+rn logf(S)"
-         ";logp=x_t-rn LSE"
-         ";bwd=g*rn(onehot-rn exp(x-rn lse)), store rn";
+         ";entropy_sum=u_j=fma(e,max(a,-FLT_MAX),u_j), same trees"
+         ";merge=M=max m_t; w_t=exp(m_t-M); S=fma(s_t,w_t,S) t=0..T-1; LSE=M+rn logf(S)"
+         ";merge_entropy=U=fma(fma(max(m_t-M,-FLT_MAX),s_t,u_t),w_t,U); H=logf(S)-rn(U/rn S)"
+         ";logp=z_t-rn LSE"
+         ";bwd=a=z-lse; p=exp(a); d=g*(onehot-p) [-gh*(p*(max(a,-FLT_MAX)+H))] [*rcp], store rn";
 }
 
 const char* bil_status_string(int status) {
@@ -1291,15 +1430,18 @@ const char* bil_status_string(int status) {
 }
 
 int bil_logp_fwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
-                 const int64_t* target_ids, int64_t ignore_index, int32_t tile_v, float* logp, float* lse,
-                 int validate, bil_stream_t stream) {
+                 const int64_t* target_ids, int64_t ignore_index, int32_t tile_v, float temperature, float* logp,
+                 float* lse, float* entropy, int validate, bil_stream_t stream) {
   if (n_rows < 0 || vocab < 1 || ld < vocab) return BIL_E_INVALID_ARG;
   int64_t num_tiles = 0;
   if (int st = check_tile(dtype, vocab, tile_v, &num_tiles)) return st;
+  float rcp = 1.0f;
+  if (int st = temperature_rcp(temperature, &rcp)) return st;
   if (n_rows == 0) return BIL_OK;
   if (logits == nullptr || target_ids == nullptr || logp == nullptr) return BIL_E_INVALID_ARG;
   const int eb = elem_bytes(dtype);
-  if (!aligned(logits, eb) || !aligned(target_ids, 8) || !aligned(logp, 4) || (lse && !aligned(lse, 4)))
+  if (!aligned(logits, eb) || !aligned(target_ids, 8) || !aligned(logp, 4) || (lse && !aligned(lse, 4)) ||
+      (entropy && !aligned(entropy, 4)))
     return BIL_E_ALIGN;
   if (num_tiles > BIL_MAX_FUSED_TILES) return BIL_E_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1317,19 +1459,23 @@ int bil_logp_fwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
   p.num_tiles = static_cast<int>(num_tiles);
   p.targets = target_ids;
   p.ignore_index = ignore_index;
+  p.rcp = rcp;
   p.logp = logp;
   p.lse = lse;
+  p.entropy = entropy;
   p.stage_bytes = static_cast<unsigned>(static_cast<size_t>(tile_v) * eb);
-  return launch_stream<true>(dtype, p, s);
+  return launch_stream<true>(dtype, entropy != nullptr, p, s);
 }
 
 int bil_logp_tile_partials(const void* logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
-                           int32_t tile_v, int32_t tile_begin, int32_t tile_end, const int64_t* target_ids,
-                           int64_t ignore_index, float* part_max, float* part_sum, int64_t ld_part,
-                           float* target_logit, bil_stream_t stream) {
+                           int32_t tile_v, int32_t tile_begin, int32_t tile_end, float temperature,
+                           const int64_t* target_ids, int64_t ignore_index, float* part_max, float* part_sum,
+                           float* part_ent, int64_t ld_part, float* target_logit, bil_stream_t stream) {
   if (n_rows < 0 || vocab < 1) return BIL_E_INVALID_ARG;
   int64_t num_tiles = 0;
   if (int st = check_tile(dtype, vocab, tile_v, &num_tiles)) return st;
+  float rcp = 1.0f;
+  if (int st = temperature_rcp(temperature, &rcp)) return st;
   if (tile_begin < 0 || tile_end <= tile_begin || tile_end > num_tiles) return BIL_E_INVALID_ARG;
   if (ld_part < num_tiles) return BIL_E_INVALID_ARG;
   // The shard holds global columns [tile_begin*tile_v, min(tile_end*tile_v, vocab)).
@@ -1342,7 +1488,7 @@ int bil_logp_tile_partials(const void* logits, int dtype, int64_t n_rows, int64_
     return BIL_E_INVALID_ARG;
   const int eb = elem_bytes(dtype);
   if (!aligned(logits, eb) || !aligned(target_ids, 8) || !aligned(part_max, 4) || !aligned(part_sum, 4) ||
-      !aligned(target_logit, 4))
+      !aligned(target_logit, 4) || (part_ent && !aligned(part_ent, 4)))
     return BIL_E_ALIGN;
   StreamParams p{};
   p.logits = static_cast<const unsigned char*>(logits);
@@ -1355,24 +1501,29 @@ int bil_logp_tile_partials(const void* logits, int dtype, int64_t n_rows, int64_
   p.num_tiles = static_cast<int>(num_tiles);
   p.targets = target_ids;
   p.ignore_index = ignore_index;
+  p.rcp = rcp;
   p.part_max = part_max;
   p.part_sum = part_sum;
+  p.part_ent = part_ent;
   p.ld_part = ld_part;
   p.target_logit = target_logit;
   p.stage_bytes = static_cast<unsigned>(static_cast<size_t>(tile_v) * eb);
-  return launch_stream<false>(dtype, p, reinterpret_cast<cudaStream_t>(stream));
+  return launch_stream<false>(dtype, part_ent != nullptr, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int bil_logp_merge(const float* part_max, const float* part_sum, int64_t n_rows, int32_t num_tiles,
-                   int64_t ld_part, const float* target_logit, const int64_t* target_ids, int64_t ignore_index,
-                   int64_t vocab, float* logp, float* lse, int validate, bil_stream_t stream) {
+int bil_logp_merge(const float* part_max, const float* part_sum, const float* part_ent, int64_t n_rows,
+                   int32_t num_tiles, int64_t ld_part, const float* target_logit, const int64_t* target_ids,
+                   int64_t ignore_index, int64_t vocab, float* logp, float* lse, float* entropy, int validate,
+                   bil_stream_t stream) {
   if (n_rows < 0 || num_tiles < 1 || ld_part < num_tiles || vocab < 1) return BIL_E_INVALID_ARG;
+  if ((entropy != nullptr) != (part_ent != nullptr)) return BIL_E_INVALID_ARG;
   if (n_rows == 0) return BIL_OK;
   if (part_max == nullptr || part_sum == nullptr || target_logit == nullptr || target_ids == nullptr ||
       logp == nullptr)
     return BIL_E_INVALID_ARG;
   if (!aligned(part_max, 4) || !aligned(part_sum, 4) || !aligned(target_logit, 4) || !aligned(target_ids, 8) ||
-      !aligned(logp, 4) || (lse && !aligned(lse, 4)))
+      !aligned(logp, 4) || (lse && !aligned(lse, 4)) || (part_ent && !aligned(part_ent, 4)) ||
+      (entropy && !aligned(entropy, 4)))
     return BIL_E_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (validate) {
@@ -1384,53 +1535,70 @@ int bil_logp_merge(const float* part_max, const float* part_sum, int64_t n_rows,
   const int64_t rows_per_block = threads / kLanes;
   const int64_t grid = std::max<int64_t>(
       1, std::min<int64_t>((n_rows + rows_per_block - 1) / rows_per_block, static_cast<int64_t>(dev.sms) * 8));
-  merge_kernel<<<static_cast<unsigned>(grid), threads, 0, s>>>(part_max, part_sum, n_rows, num_tiles, ld_part,
-                                                                target_logit, target_ids, ignore_index, vocab,
-                                                                logp, lse);
+  if (entropy != nullptr) {
+    merge_kernel<true><<<static_cast<unsigned>(grid), threads, 0, s>>>(part_max, part_sum, part_ent, n_rows,
+                                                                        num_tiles, ld_part, target_logit, target_ids,
+                                                                        ignore_index, vocab, logp, lse, entropy);
+  } else {
+    merge_kernel<false><<<static_cast<unsigned>(grid), threads, 0, s>>>(part_max, part_sum, nullptr, n_rows,
+                                                                         num_tiles, ld_part, target_logit, target_ids,
+                                                                         ignore_index, vocab, logp, lse, nullptr);
+  }
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
 int bil_logp_bwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
-                 const int64_t* target_ids, int64_t ignore_index, const float* lse, const float* grad_logp,
-                 void* dlogits, int dlogits_dtype, int64_t ld_out, int64_t out_cols, bil_stream_t stream) {
+                 const int64_t* target_ids, int64_t ignore_index, float temperature, const float* lse,
+                 const float* grad_logp, const float* entropy, const float* grad_entropy, void* dlogits,
+                 int dlogits_dtype, int64_t ld_out, int64_t out_cols, bil_stream_t stream) {
   const int eb = elem_bytes(dtype);
   const int ob = elem_bytes(dlogits_dtype);
   if (eb == 0 || ob == 0) return BIL_E_DTYPE;
   if (n_rows < 0 || vocab < 1 || ld < vocab || out_cols < vocab || ld_out < out_cols) return BIL_E_INVALID_ARG;
+  float rcp = 1.0f;
+  if (int st = temperature_rcp(temperature, &rcp)) return st;
+  if ((entropy != nullptr) != (grad_entropy != nullptr)) return BIL_E_INVALID_ARG;
   if (n_rows == 0) return BIL_OK;
   if (logits == nullptr || target_ids == nullptr || lse == nullptr || grad_logp == nullptr || dlogits == nullptr)
     return BIL_E_INVALID_ARG;
   if (!aligned(logits, eb) || !aligned(target_ids, 8) || !aligned(lse, 4) || !aligned(grad_logp, 4) ||
-      !aligned(dlogits, ob))
+      !aligned(dlogits, ob) || (entropy && !aligned(entropy, 4)) || (grad_entropy && !aligned(grad_entropy, 4)))
     return BIL_E_ALIGN;
   const bool vec = aligned(logits, 16) && (ld * eb) % 16 == 0 && aligned(dlogits, 16) && (ld_out * ob) % 16 == 0;
-  const unsigned char* in = static_cast<const unsigned char*>(logits);
-  unsigned char* out = static_cast<unsigned char*>(dlogits);
+  BwdParams bp{};
+  bp.logits = static_cast<const unsigned char*>(logits);
+  bp.n_rows = n_rows;
+  bp.vocab = vocab;
+  bp.ld = ld;
+  bp.targets = target_ids;
+  bp.ignore_index = ignore_index;
+  bp.lse = lse;
+  bp.grad = grad_logp;
+  bp.entropy = entropy;
+  bp.grad_entropy = grad_entropy;
+  bp.rcp = rcp;
+  bp.dlogits = static_cast<unsigned char*>(dlogits);
+  bp.ld_out = ld_out;
+  bp.out_cols = out_cols;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (dtype) {
-    case BIL_BF16:
-      return launch_bwd_dt<BIL_BF16>(dlogits_dtype, vec, in, n_rows, vocab, ld, target_ids, ignore_index, lse,
-                                     grad_logp, out, ld_out, out_cols, s);
-    case BIL_F16:
-      return launch_bwd_dt<BIL_F16>(dlogits_dtype, vec, in, n_rows, vocab, ld, target_ids, ignore_index, lse,
-                                    grad_logp, out, ld_out, out_cols, s);
-    case BIL_F32:
-      return launch_bwd_dt<BIL_F32>(dlogits_dtype, vec, in, n_rows, vocab, ld, target_ids, ignore_index, lse,
-                                    grad_logp, out, ld_out, out_cols, s);
-    default:
-      return BIL_E_DTYPE;
+    case BIL_BF16: return launch_bwd_dt<BIL_BF16>(dlogits_dtype, vec, bp, s);
+    case BIL_F16: return launch_bwd_dt<BIL_F16>(dlogits_dtype, vec, bp, s);
+    case BIL_F32: return launch_bwd_dt<BIL_F32>(dlogits_dtype, vec, bp, s);
+    default: return BIL_E_DTYPE;
   }
 }
 
-int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, int* stages, int* consumers,
-                     int64_t* smem_bytes) {
+int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, int entropy, int* stages,
+                     int* consumers, int64_t* smem_bytes) {
   const int eb = elem_bytes(dtype);
   if (eb == 0) return BIL_E_DTYPE;
   if (tile_v <= 0 || tile_v % kGroup != 0 || num_tiles < 1 || stages == nullptr || consumers == nullptr ||
       smem_bytes == nullptr)
     return BIL_E_INVALID_ARG;
   if (static_cast<int64_t>(tile_v) * eb > BIL_MAX_TILE_BYTES) return BIL_E_UNSUPPORTED;
-  const StreamShape shape = stream_shape(static_cast<unsigned>(tile_v * eb), static_cast<int>(num_tiles), fused != 0);
+  const StreamShape shape =
+      stream_shape(static_cast<unsigned>(tile_v * eb), static_cast<int>(num_tiles), fused != 0, entropy != 0);
   *stages = shape.stages;
   *consumers = shape.consumers;
   *smem_bytes = static_cast<int64_t>(shape.smem);

@@ -73,11 +73,15 @@ def _need_cuda(*ts: torch.Tensor) -> None:
 
 def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int = IGNORE_INDEX,
              tile_v: int = DEFAULT_TILE_V, validate: bool = False, vocab: int | None = None,
-             out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
-    """Selected-token log-probabilities: (logp, lse), both float32 with the targets' shape.
+             out: torch.Tensor | None = None, lse: torch.Tensor | None = None, temperature: float = 1.0,
+             return_entropy: bool = False, entropy: torch.Tensor | None = None):
+    """Selected-token log-probabilities: (logp, lse), both float32 with the targets' shape,
+    and the row entropy as a third result when ``return_entropy`` (or ``entropy``) is given.
 
     ``vocab`` (default: the last dimension) lets the row carry padding columns
     that are never read (e.g. a vocabulary padded to a multiple of the tile).
+    ``temperature`` divides the logits before the softmax (applied as a
+    multiplication by the float32 reciprocal).
     """
     _need_cuda(logits, target_ids)
     lead = logits.shape[:-1]
@@ -91,18 +95,26 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
         out = torch.empty(n, dtype=torch.float32, device=logits.device)
     if lse is None:
         lse = torch.empty(n, dtype=torch.float32, device=logits.device)
+    want_ent = return_entropy or entropy is not None
+    if want_ent and entropy is None:
+        entropy = torch.empty(n, dtype=torch.float32, device=logits.device)
     lib = _lib.load()
     with torch.cuda.device(logits.device):
         st = lib.bil_logp_fwd(_ptr(x2), _code(x2.dtype), n, v, _row_stride(x2), _ptr(t1), int(ignore_index),
-                              int(tile_v), _ptr(out), _ptr(lse), int(bool(validate)), _stream(logits.device))
+                              int(tile_v), float(temperature), _ptr(out), _ptr(lse), _ptr(entropy if want_ent else None),
+                              int(bool(validate)), _stream(logits.device))
     _lib.check("bil_logp_fwd", st)
+    if want_ent:
+        return out.reshape(lead), lse.reshape(lead), entropy.reshape(lead)
     return out.reshape(lead), lse.reshape(lead)
 
 
 def logp_tile_partials(logits_shard: torch.Tensor, target_ids: torch.Tensor, vocab: int, tile_v: int,
                        tile_begin: int, tile_end: int, part_max: torch.Tensor, part_sum: torch.Tensor,
-                       target_logit: torch.Tensor, ignore_index: int = IGNORE_INDEX) -> None:
-    """Fill columns [tile_begin, tile_end) of the [N, T] partial buffers.
+                       target_logit: torch.Tensor, ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                       part_ent: torch.Tensor | None = None) -> None:
+    """Fill columns [tile_begin, tile_end) of the [N, T] partial buffers
+    (and of ``part_ent``, the entropy partials, when given).
 
     ``logits_shard`` is [N, >= shard columns]; its column 0 is global column
     ``tile_begin * tile_v`` (a rank's own vocabulary shard, or a column slice
@@ -111,49 +123,59 @@ def logp_tile_partials(logits_shard: torch.Tensor, target_ids: torch.Tensor, voc
     x2 = _rows2d(logits_shard)
     n = x2.shape[0]
     t1 = _targets1d(target_ids, (n,), logits_shard.device)
-    for name, b in (("part_max", part_max), ("part_sum", part_sum)):
+    bufs = (("part_max", part_max), ("part_sum", part_sum)) + ((("part_ent", part_ent),) if part_ent is not None else ())
+    for name, b in bufs:
         if b.dtype != torch.float32 or b.dim() != 2 or b.shape[0] != n or b.stride(1) != 1:
             raise ValueError(f"{name} must be a row-major float32 [N, >= num_tiles] tensor")
-    if part_max.stride(0) != part_sum.stride(0):
-        raise ValueError("part_max and part_sum must share a row stride")
+        if b.stride(0) != part_max.stride(0):
+            raise ValueError("the partial buffers must share a row stride")
     if target_logit.dtype != torch.float32 or target_logit.numel() != n or not target_logit.is_contiguous():
         raise ValueError("target_logit must be a contiguous float32 [N] tensor")
     lib = _lib.load()
     with torch.cuda.device(logits_shard.device):
         st = lib.bil_logp_tile_partials(_ptr(x2), _code(x2.dtype), n, int(vocab), _row_stride(x2), int(tile_v),
-                                        int(tile_begin), int(tile_end), _ptr(t1), int(ignore_index),
-                                        _ptr(part_max), _ptr(part_sum), part_max.stride(0), _ptr(target_logit),
-                                        _stream(logits_shard.device))
+                                        int(tile_begin), int(tile_end), float(temperature), _ptr(t1),
+                                        int(ignore_index), _ptr(part_max), _ptr(part_sum), _ptr(part_ent),
+                                        part_max.stride(0), _ptr(target_logit), _stream(logits_shard.device))
     _lib.check("bil_logp_tile_partials", st)
 
 
 def logp_merge(part_max: torch.Tensor, part_sum: torch.Tensor, num_tiles: int, target_logit: torch.Tensor,
-               target_ids: torch.Tensor, vocab: int, ignore_index: int = IGNORE_INDEX, validate: bool = False):
-    """Fixed-order merge of [N, T] partials: (logp, lse) float32 [N]."""
+               target_ids: torch.Tensor, vocab: int, ignore_index: int = IGNORE_INDEX, validate: bool = False,
+               part_ent: torch.Tensor | None = None):
+    """Fixed-order merge of [N, T] partials: (logp, lse) float32 [N], and the
+    entropy as a third result when ``part_ent`` is given."""
     _need_cuda(part_max, part_sum, target_logit, target_ids)
     n = part_max.shape[0]
     t1 = _targets1d(target_ids, (n,), part_max.device)
-    if part_max.stride(0) != part_sum.stride(0) or part_max.stride(1) != 1 or part_sum.stride(1) != 1:
-        raise ValueError("part_max and part_sum must be row-major with one row stride")
+    for b in (part_sum,) + ((part_ent,) if part_ent is not None else ()):
+        if b.stride(0) != part_max.stride(0) or b.stride(1) != 1:
+            raise ValueError("the partial buffers must be row-major with one row stride")
+    if part_max.stride(1) != 1:
+        raise ValueError("part_max must be row-major")
     out = torch.empty(n, dtype=torch.float32, device=part_max.device)
     lse = torch.empty(n, dtype=torch.float32, device=part_max.device)
+    ent = torch.empty(n, dtype=torch.float32, device=part_max.device) if part_ent is not None else None
     lib = _lib.load()
     with torch.cuda.device(part_max.device):
-        st = lib.bil_logp_merge(_ptr(part_max), _ptr(part_sum), n, int(num_tiles), part_max.stride(0),
+        st = lib.bil_logp_merge(_ptr(part_max), _ptr(part_sum), _ptr(part_ent), n, int(num_tiles), part_max.stride(0),
                                 _ptr(target_logit), _ptr(t1), int(ignore_index), int(vocab), _ptr(out), _ptr(lse),
-                                int(bool(validate)), _stream(part_max.device))
+                                _ptr(ent), int(bool(validate)), _stream(part_max.device))
     _lib.check("bil_logp_merge", st)
-    return out, lse
+    return (out, lse, ent) if ent is not None else (out, lse)
 
 
 def logp_bwd(logits: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor, grad_logp: torch.Tensor,
              ignore_index: int = IGNORE_INDEX, dlogits_dtype: torch.dtype | None = None,
-             vocab: int | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
-    """dlogits = g * (onehot(target) - softmax(logits)) from the saved LSE.
+             vocab: int | None = None, out: torch.Tensor | None = None, temperature: float = 1.0,
+             entropy: torch.Tensor | None = None, grad_entropy: torch.Tensor | None = None) -> torch.Tensor:
+    """dlogits of g * logp (+ gh * entropy) from the saved LSE (and entropy).
 
     Returns a tensor of the logits' shape (columns past ``vocab`` are zero) in
     ``dlogits_dtype`` (default: the logits' dtype)."""
     _need_cuda(logits, target_ids, lse, grad_logp)
+    if (entropy is None) != (grad_entropy is None):
+        raise ValueError("entropy and grad_entropy go together")
     lead = logits.shape[:-1]
     x2 = _rows2d(logits)
     n, width = x2.shape
@@ -161,6 +183,12 @@ def logp_bwd(logits: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor, 
     t1 = _targets1d(target_ids, lead, logits.device)
     lse1 = lse.reshape(-1).to(torch.float32).contiguous()
     g1 = grad_logp.reshape(-1).to(torch.float32).contiguous()
+    h1 = gh1 = None
+    if entropy is not None:
+        h1 = entropy.reshape(-1).to(torch.float32).contiguous()
+        gh1 = grad_entropy.reshape(-1).to(torch.float32).contiguous()
+        if h1.numel() != n or gh1.numel() != n:
+            raise ValueError("entropy and grad_entropy must have the targets' shape")
     if lse1.numel() != n or g1.numel() != n:
         raise ValueError("lse and grad_logp must have the targets' shape")
     odt = logits.dtype if dlogits_dtype is None else dlogits_dtype
@@ -174,37 +202,66 @@ def logp_bwd(logits: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor, 
     lib = _lib.load()
     with torch.cuda.device(logits.device):
         st = lib.bil_logp_bwd(_ptr(x2), _code(x2.dtype), n, v, _row_stride(x2), _ptr(t1), int(ignore_index),
-                              _ptr(lse1), _ptr(g1), _ptr(o2), _code(o2.dtype), _row_stride(o2), width,
-                              _stream(logits.device))
+                              float(temperature), _ptr(lse1), _ptr(g1), _ptr(h1), _ptr(gh1), _ptr(o2),
+                              _code(o2.dtype), _row_stride(o2), width, _stream(logits.device))
     _lib.check("bil_logp_bwd", st)
     return out.reshape(logits.shape) if out.numel() == logits.numel() else out
 
 
 class BatchInvariantLogp(torch.autograd.Function):
-    """logp = BatchInvariantLogp.apply(logits, target_ids, ignore_index, tile_v, validate).
+    """logp = BatchInvariantLogp.apply(logits, target_ids, ignore_index, tile_v, validate, temperature)
 
     The forward saves the per-row LSE; the backward recomputes the softmax
     from it.  target_ids receives no gradient."""
 
     @staticmethod
-    def forward(ctx, logits, target_ids, ignore_index=IGNORE_INDEX, tile_v=DEFAULT_TILE_V, validate=False):
-        logp, lse = logp_fwd(logits, target_ids, ignore_index, tile_v, validate)
+    def forward(ctx, logits, target_ids, ignore_index=IGNORE_INDEX, tile_v=DEFAULT_TILE_V, validate=False,
+                temperature=1.0):
+        logp, lse = logp_fwd(logits, target_ids, ignore_index, tile_v, validate, temperature=temperature)
         ctx.save_for_backward(logits, target_ids, lse)
-        ctx.ignore_index = ignore_index
-        ctx.mark_non_differentiable(lse)
+        ctx.ignore_index, ctx.temperature = ignore_index, temperature
         return logp
 
     @staticmethod
     def backward(ctx, grad_logp):
         logits, target_ids, lse = ctx.saved_tensors
-        d = logp_bwd(logits, target_ids, lse, grad_logp.contiguous(), ctx.ignore_index)
-        return d, None, None, None, None
+        d = logp_bwd(logits, target_ids, lse, grad_logp.contiguous(), ctx.ignore_index, temperature=ctx.temperature)
+        return d, None, None, None, None, None
+
+
+class BatchInvariantLogpEntropy(torch.autograd.Function):
+    """(logp, entropy) = BatchInvariantLogpEntropy.apply(logits, target_ids, ignore_index, tile_v,
+    validate, temperature): both outputs differentiable with respect to the logits."""
+
+    @staticmethod
+    def forward(ctx, logits, target_ids, ignore_index=IGNORE_INDEX, tile_v=DEFAULT_TILE_V, validate=False,
+                temperature=1.0):
+        logp, lse, ent = logp_fwd(logits, target_ids, ignore_index, tile_v, validate, temperature=temperature,
+                                  return_entropy=True)
+        ctx.save_for_backward(logits, target_ids, lse, ent)
+        ctx.ignore_index, ctx.temperature = ignore_index, temperature
+        return logp, ent
+
+    @staticmethod
+    def backward(ctx, grad_logp, grad_ent):
+        logits, target_ids, lse, ent = ctx.saved_tensors
+        if grad_logp is None:
+            grad_logp = torch.zeros_like(lse)
+        if grad_ent is None:
+            grad_ent = torch.zeros_like(ent)
+        d = logp_bwd(logits, target_ids, lse, grad_logp.contiguous(), ctx.ignore_index, temperature=ctx.temperature,
+                     entropy=ent, grad_entropy=grad_ent.contiguous())
+        return d, None, None, None, None, None
 
 
 def batch_invariant_logp(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int = IGNORE_INDEX,
-                         validate: bool = False, tile_v: int = DEFAULT_TILE_V) -> torch.Tensor:
-    """Differentiable selected-token log-probability, float32 with the targets' shape."""
-    return BatchInvariantLogp.apply(logits, target_ids, ignore_index, tile_v, validate)
+                         validate: bool = False, tile_v: int = DEFAULT_TILE_V, temperature: float = 1.0,
+                         return_entropy: bool = False):
+    """Differentiable selected-token log-probability, float32 with the targets' shape;
+    with ``return_entropy``, (logp, entropy)."""
+    if return_entropy:
+        return BatchInvariantLogpEntropy.apply(logits, target_ids, ignore_index, tile_v, validate, temperature)
+    return BatchInvariantLogp.apply(logits, target_ids, ignore_index, tile_v, validate, temperature)
 
 
 def watchdog_status(clear: bool = True) -> int:

@@ -144,7 +144,9 @@ static void max_and_sumexp(const RowView *v, int64_t c0, int64_t c1, double *m_o
             double e = exp(d);
 #endif
             s += e;
-            u += e * d;
+            if (e != 0.0) { /* p log p -> 0 as p -> 0: an -inf logit adds nothing */
+                u += e * d;
+            }
         }
     } else {
         /* every entry is -inf (or the range is empty of finite values);
@@ -346,7 +348,7 @@ int64_t bil_oracle_merge(const double *part_max, const double *part_sum, const d
                 double w = exp(m[t] - M);
 #endif
                 S += s[t] * w;
-                if (part_ent != NULL) {
+                if (part_ent != NULL && s[t] != 0.0) { /* an empty tile adds nothing */
                     U += w * (part_ent[r * ld_part + t] + (m[t] - M) * s[t]);
                 }
             }
@@ -419,7 +421,7 @@ int64_t bil_oracle_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64
 #else
             double dz = g * (onehot - p);
 #endif
-            if (grad_entropy != NULL) {
+            if (grad_entropy != NULL && p != 0.0) { /* p (log p + H) -> 0 as p -> 0 */
 #ifdef BIL_ORACLE_MUTANT_BWD_ENTROPY_SIGN
                 dz += gh * p * (z - L + H);
 #else

@@ -12,6 +12,17 @@ Tolerances (written here once, used by every GPU test):
               bound applies to the value before the final rounding).
   Partials:   m_t and the target logit exactly (both are copies or exact maxima
               of exactly widened values); s_t within 1e-5 relative.
+  ENTROPY_ATOL 1e-4 absolute on the float32 entropy: H = log S - U / S from
+              float32 sums whose relative error is ~1e-6, with |U / S| at most
+              about log V (12 at V = 151936), i.e. ~1e-5 worst case.
+  Gradient with an entropy term (entropy_grad_tol): the backward consumes the
+              forward's float32 lse and H, whose errors eps_L <= 2e-6 and
+              eps_H <= 2e-5 reach the element through p and through H:
+                d = rcp * (g (onehot - p) - gh p (a + H)),  a = z - lse
+                |err| <= 1e-6 + rcp p (|g| rho + |gh| (rho |a + H| + eps_L + eps_H))
+              with rho = eps_L + 3e-7 the relative error of p (2-ulp exp and
+              the rounding of a).  Without an entropy term and at rcp = 1 this
+              is the 1e-6 bound up to p |g| rho, and those tests use 1e-6.
 """
 from __future__ import annotations
 
@@ -22,6 +33,7 @@ import oracle
 
 LOGP_ATOL = 1e-4
 DLOGITS_ATOL = 1e-6
+ENTROPY_ATOL = 1e-4
 PART_SUM_RTOL = 1e-5
 
 TORCH_DTYPE = {"float32": torch.float32, "bfloat16": torch.bfloat16, "float16": torch.float16}
@@ -60,6 +72,31 @@ def assert_close_abs(got: np.ndarray, ref: np.ndarray, atol: float, what: str):
     err = np.abs(got[m] - ref[m])
     worst = float(err.max()) if err.size else 0.0
     assert worst <= atol, f"{what}: max |err| {worst:.3g} > {atol:g} (at {np.argmax(err)})"
+    return worst
+
+
+EPS_LSE = 2e-6
+EPS_ENTROPY = 2e-5
+
+
+def entropy_grad_tol(p: np.ndarray, a_plus_h: np.ndarray, g: np.ndarray, gh: np.ndarray, rcp: float) -> np.ndarray:
+    """Per-element bound for gradients with an entropy term (see the module docstring);
+    p, a_plus_h are [N, V] float64 from the oracle, g, gh are [N]."""
+    rho = EPS_LSE + 3e-7
+    with np.errstate(invalid="ignore"):
+        p_ah = np.where(p > 0, p * np.abs(a_plus_h), 0.0)  # p -> 0 at a = -inf
+    return 1e-6 + rcp * (np.abs(g)[:, None] * rho * p +
+                         np.abs(gh)[:, None] * (rho * p_ah + (EPS_LSE + EPS_ENTROPY) * p))
+
+
+def assert_close_elementwise(got: np.ndarray, ref: np.ndarray, tol: np.ndarray, what: str):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), f"{what}: NaN pattern differs"
+    m = np.isfinite(ref)
+    ratio = np.abs(got[m] - ref[m]) / tol[m]
+    worst = float(ratio.max()) if ratio.size else 0.0
+    assert worst <= 1.0, f"{what}: error {worst:.3g} x its bound (at {np.argmax(ratio)})"
     return worst
 
 

@@ -327,6 +327,26 @@ def check_entropy(defines=()):
         ref = -mpmath.fsum((mpmath.exp(mpmath.mpf(float(c))) / tot) * (mpmath.mpf(float(c)) - mpmath.log(tot))
                            for c in x[r])
         assert abs(float(ref) - h[r]) <= 1e-12
+    # -inf logits (a masked vocabulary slice, and one whole -inf tile) carry no
+    # probability and add nothing to the entropy or its gradient
+    v = 1024
+    x = _rows(42, 2, v, scale=2.0)
+    x[:, 100:140] = -np.inf
+    x[:, 512:768] = -np.inf
+    t2 = np.array([5, 900], np.int64)
+    _, _, _, h = oracle.logp_fwd(x, "float32", v, t2, entropy=True, defines=defines)
+    keep = np.isfinite(x[0])
+    ref = torch.distributions.Categorical(logits=torch.from_numpy(x[0][keep].astype(np.float64))).entropy().item()
+    assert np.all(np.isfinite(h)) and abs(h[0] - ref) <= 1e-12
+    pm, ps, pe = np.full((2, 4), -np.inf), np.zeros((2, 4)), np.zeros((2, 4))
+    tl = np.full(2, np.nan)
+    oracle.tile_partials(x, "float32", v, 256, 0, 4, t2, part_max=pm, part_sum=ps, target_logit=tl, part_ent=pe,
+                         defines=defines)
+    assert np.all(pm[:, 2] == -np.inf)
+    _, _, _, hm = oracle.merge(pm, ps, tl, t2, v, part_ent=pe, defines=defines)
+    assert np.abs(hm - h).max() <= 1e-12
+    d, _ = oracle.logp_bwd(x, "float32", v, t2, np.ones(2), grad_entropy=np.ones(2), defines=defines)
+    assert np.all(np.isfinite(d)) and np.all(d[:, 512:768] == 0.0)
     # merged entropy partials equal the whole-row entropy for any tile size and split
     for dtype, v, n in (("float32", 3000, 4), ("bfloat16", 1000, 3)):
         x = _rows(41, n, v, scale=3.0, dtype=dtype)

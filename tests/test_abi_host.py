@@ -53,7 +53,7 @@ def test_header_constants_match_binding():
 
 def test_contract_id_and_status_strings(lib):
     cid = _lib.contract_id()
-    assert cid.startswith("bil.v1") and "ex2.approx" in cid and "fma" in cid
+    assert cid.startswith("bil.v2") and "ex2.approx" in cid and "fma" in cid and "entropy" in cid
     for s in range(7):
         assert _lib.status_string(s) != "unknown status"
     assert _lib.status_string(99) == "unknown status"
@@ -67,11 +67,11 @@ NULL = None
 
 
 def fwd(lib, **kw):
-    a = dict(logits=FAKE, dtype=_lib.BF16, n=4, vocab=300, ld=300, tgt=FAKE, ign=-100, tile=4096, logp=FAKE,
-             lse=FAKE, validate=0, stream=NULL)
+    a = dict(logits=FAKE, dtype=_lib.BF16, n=4, vocab=300, ld=300, tgt=FAKE, ign=-100, tile=4096, temp=1.0,
+             logp=FAKE, lse=FAKE, ent=NULL, validate=0, stream=NULL)
     a.update(kw)
     return lib.bil_logp_fwd(a["logits"], a["dtype"], a["n"], a["vocab"], a["ld"], a["tgt"], a["ign"], a["tile"],
-                            a["logp"], a["lse"], a["validate"], a["stream"])
+                            a["temp"], a["logp"], a["lse"], a["ent"], a["validate"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -83,11 +83,17 @@ def fwd(lib, **kw):
     (dict(tile=12), _lib.E_INVALID_ARG),
     (dict(tile=65536), _lib.E_UNSUPPORTED),
     (dict(dtype=_lib.F32, tile=32768), _lib.E_UNSUPPORTED),
+    (dict(temp=0.0), _lib.E_INVALID_ARG),
+    (dict(temp=-1.0), _lib.E_INVALID_ARG),
+    (dict(temp=float("nan")), _lib.E_INVALID_ARG),
+    (dict(temp=float("inf")), _lib.E_INVALID_ARG),
+    (dict(temp=1e-45), _lib.E_INVALID_ARG),
     (dict(logits=NULL), _lib.E_INVALID_ARG),
     (dict(tgt=NULL), _lib.E_INVALID_ARG),
     (dict(logp=NULL), _lib.E_INVALID_ARG),
     (dict(logits=FAKE_ODD), _lib.E_ALIGN),
     (dict(tgt=ctypes.c_void_p(0x10004)), _lib.E_ALIGN),
+    (dict(ent=FAKE_ODD), _lib.E_ALIGN),
     (dict(vocab=8 * 2049, ld=8 * 2049, tile=8), _lib.E_UNSUPPORTED),
     (dict(n=0), _lib.OK),
     (dict(n=0, logits=NULL, tgt=NULL, logp=NULL), _lib.OK),
@@ -98,28 +104,44 @@ def test_fwd_rejects_bad_arguments(lib, kw, status):
 
 def test_partials_rejects_bad_ranges(lib):
     def call(**kw):
-        a = dict(n=4, vocab=10000, ld=10000, tile=4096, b=0, e=3, ldp=3)
+        a = dict(n=4, vocab=10000, ld=10000, tile=4096, b=0, e=3, ldp=3, temp=1.0, pe=NULL)
         a.update(kw)
         return lib.bil_logp_tile_partials(FAKE, _lib.BF16, a["n"], a["vocab"], a["ld"], a["tile"], a["b"], a["e"],
-                                          FAKE, -100, FAKE, FAKE, a["ldp"], FAKE, NULL)
+                                          a["temp"], FAKE, -100, FAKE, FAKE, a["pe"], a["ldp"], FAKE, NULL)
     assert call(b=-1) == _lib.E_INVALID_ARG
     assert call(b=2, e=2) == _lib.E_INVALID_ARG
     assert call(e=4) == _lib.E_INVALID_ARG          # only 3 tiles exist
     assert call(ldp=2) == _lib.E_INVALID_ARG
     assert call(b=1, e=3, ld=10000 - 4096 - 1) == _lib.E_INVALID_ARG  # shard narrower than its columns
+    assert call(temp=0.0) == _lib.E_INVALID_ARG
+    assert call(pe=FAKE_ODD) == _lib.E_ALIGN
     assert call(n=0) == _lib.OK
 
 
 def test_merge_and_bwd_reject_bad_arguments(lib):
     m = lib.bil_logp_merge
-    assert m(FAKE, FAKE, 4, 0, 1, FAKE, FAKE, -100, 10, FAKE, FAKE, 0, NULL) == _lib.E_INVALID_ARG
-    assert m(FAKE, FAKE, 4, 3, 2, FAKE, FAKE, -100, 10, FAKE, FAKE, 0, NULL) == _lib.E_INVALID_ARG
-    assert m(FAKE, NULL, 4, 3, 3, FAKE, FAKE, -100, 10, FAKE, FAKE, 0, NULL) == _lib.E_INVALID_ARG
-    assert m(FAKE_ODD, FAKE, 4, 3, 3, FAKE, FAKE, -100, 10, FAKE, FAKE, 0, NULL) == _lib.E_ALIGN
+    #   part_max part_sum part_ent n  T  ld tl    tgt   ign  V   logp  lse   ent   val stream
+    assert m(FAKE, FAKE, NULL, 4, 0, 1, FAKE, FAKE, -100, 10, FAKE, FAKE, NULL, 0, NULL) == _lib.E_INVALID_ARG
+    assert m(FAKE, FAKE, NULL, 4, 3, 2, FAKE, FAKE, -100, 10, FAKE, FAKE, NULL, 0, NULL) == _lib.E_INVALID_ARG
+    assert m(FAKE, NULL, NULL, 4, 3, 3, FAKE, FAKE, -100, 10, FAKE, FAKE, NULL, 0, NULL) == _lib.E_INVALID_ARG
+    assert m(FAKE_ODD, FAKE, NULL, 4, 3, 3, FAKE, FAKE, -100, 10, FAKE, FAKE, NULL, 0, NULL) == _lib.E_ALIGN
+    # entropy output without entropy partials, and the other way round
+    assert m(FAKE, FAKE, NULL, 4, 3, 3, FAKE, FAKE, -100, 10, FAKE, FAKE, FAKE, 0, NULL) == _lib.E_INVALID_ARG
+    assert m(FAKE, FAKE, FAKE, 4, 3, 3, FAKE, FAKE, -100, 10, FAKE, FAKE, NULL, 0, NULL) == _lib.E_INVALID_ARG
     b = lib.bil_logp_bwd
-    args = [FAKE, _lib.BF16, 4, 300, 300, FAKE, -100, FAKE, FAKE, FAKE, _lib.BF16, 300, 300, NULL]
-    assert b(*args[:10], 9, *args[11:]) == _lib.E_DTYPE
-    assert b(*args[:11], 299, 299, NULL) == _lib.E_INVALID_ARG   # fewer output columns than vocab
-    assert b(*args[:11], 300, 301, NULL) == _lib.E_INVALID_ARG   # out_cols beyond ld_out
-    assert b(*args[:9], FAKE_ODD, *args[10:]) == _lib.E_ALIGN
-    assert b(*args[:2], 0, *args[3:]) == _lib.OK
+    #       logits dtype      n  V    ld   tgt   ign  temp lse   g     ent   gent  d     odt        ldo  cols stream
+    args = [FAKE, _lib.BF16, 4, 300, 300, FAKE, -100, 1.0, FAKE, FAKE, NULL, NULL, FAKE, _lib.BF16, 300, 300, NULL]
+
+    def with_(**kw):
+        a = list(args)
+        for k, v in kw.items():
+            a[{"odt": 13, "ldo": 14, "cols": 15, "d": 12, "temp": 7, "ent": 10, "gent": 11, "n": 2}[k]] = v
+        return b(*a)
+    assert with_(odt=9) == _lib.E_DTYPE
+    assert with_(ldo=299, cols=299) == _lib.E_INVALID_ARG   # fewer output columns than vocab
+    assert with_(ldo=300, cols=301) == _lib.E_INVALID_ARG   # out_cols beyond ld_out
+    assert with_(d=FAKE_ODD) == _lib.E_ALIGN
+    assert with_(temp=-2.0) == _lib.E_INVALID_ARG
+    assert with_(ent=FAKE) == _lib.E_INVALID_ARG             # entropy without its gradient
+    assert with_(gent=FAKE) == _lib.E_INVALID_ARG
+    assert with_(n=0) == _lib.OK

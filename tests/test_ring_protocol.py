@@ -76,10 +76,10 @@ def lib():
 @pytest.mark.parametrize("dtype,tile_v", [(_lib.BF16, 4096), (_lib.BF16, 512), (_lib.F16, 1024),
                                           (_lib.F32, 512), (_lib.F32, 4096), (_lib.F32, 8192),
                                           (_lib.BF16, 32768), (_lib.F32, 16384), (_lib.BF16, 8)])
-@pytest.mark.parametrize("fused", [True, False])
-def test_library_shapes_are_sound(lib, dtype, tile_v, fused):
+@pytest.mark.parametrize("fused,entropy", [(True, False), (False, False), (True, True)])
+def test_library_shapes_are_sound(lib, dtype, tile_v, fused, entropy):
     num_tiles = -(-151936 // tile_v) if tile_v >= 64 else 2048
-    stages, consumers, smem = _lib.stream_shape(dtype, tile_v, num_tiles, fused)
+    stages, consumers, smem = _lib.stream_shape(dtype, tile_v, num_tiles, fused, entropy)
     assert 1 <= consumers <= 7 and stages >= 2 and stages % consumers == 0
     assert smem <= 227 * 1024
     for seed in range(25):
