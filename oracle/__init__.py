@@ -31,8 +31,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "bil_oracle.c")
 
 # element-type codes of the C oracle (its own; not shared with the CUDA library)
-F32, BF16, F16 = 0, 1, 2
-DTYPE_CODES = {"float32": F32, "bfloat16": BF16, "float16": F16}
+F32, BF16, F16, F64 = 0, 1, 2, 3
+DTYPE_CODES = {"float32": F32, "bfloat16": BF16, "float16": F16, "float64": F64}
 
 _lock = threading.Lock()
 _libs: dict[tuple, ctypes.CDLL] = {}
@@ -83,6 +83,8 @@ def load(defines: tuple[str, ...] = ()) -> ctypes.CDLL:
         lib.bil_oracle_merge.argtypes = [dp, dp, dp, i64, i64, i64, dp, vp, i64, i64, dp, dp, dp]
         lib.bil_oracle_logp_bwd.restype = i64
         lib.bil_oracle_logp_bwd.argtypes = [vp, i32, i64, i64, i64, vp, i64, f64, dp, dp, dp, i64, i64]
+        lib.bil_oracle_linear_logits.restype = None
+        lib.bil_oracle_linear_logits.argtypes = [vp, vp, i32, i64, i64, i64, i64, i64, dp, i64]
         lib.bil_oracle_widen.restype = None
         lib.bil_oracle_widen.argtypes = [vp, i32, i64, dp]
         _libs[defines] = lib
@@ -106,7 +108,7 @@ def _code(dtype: str) -> int:
 
 
 def _check_logits(logits: np.ndarray, dtype: str) -> tuple[int, int]:
-    want = np.float32 if dtype == "float32" else np.uint16
+    want = {"float32": np.float32, "float64": np.float64}.get(dtype, np.uint16)
     if logits.dtype != want or logits.ndim != 2 or logits.strides[1] != logits.itemsize:
         raise ValueError("oracle: logits must be a 2-D row-major array of the stored element type")
     return logits.shape[0], logits.strides[0] // logits.itemsize
@@ -201,6 +203,32 @@ def logp_bwd(logits: np.ndarray, dtype: str, vocab: int, target_ids: np.ndarray,
                                             ignore_index, float(temperature), _ptr(g), _optr(gh),
                                             _ptr(d), out_cols, out_cols)
     return d, int(bad)
+
+
+def linear_logits(hidden: np.ndarray, weight: np.ndarray, dtype: str,
+                  defines: tuple[str, ...] = ()) -> np.ndarray:
+    """float64 logits z [N, V] = hidden [N, H] . weight [V, H]^T, summed over k in order.
+
+    "[RFC][ROCm] End-to-end optimization of bitwise VIME R/R beyond native P/P",
+    section "Workstream 3: fused ROCm LM-head and linear logp": the LM-head
+    projection whose output the fused operator reduces without storing."""
+    n, ld_h = _check_logits(hidden, dtype)
+    v, ld_w = _check_logits(weight, dtype)
+    h = hidden.shape[1]
+    assert weight.shape[1] == h
+    z = np.empty((n, v), np.float64)
+    load(defines).bil_oracle_linear_logits(_ptr(hidden), _ptr(weight), _code(dtype), n, h, ld_h, v, ld_w,
+                                           _ptr(z), v)
+    return z
+
+
+def linear_logp_fwd(hidden: np.ndarray, weight: np.ndarray, dtype: str, target_ids: np.ndarray,
+                    ignore_index: int = -100, temperature: float = 1.0, entropy: bool = False,
+                    defines: tuple[str, ...] = ()):
+    """The fused LM-head + logp: the operator applied to the float64 projection.
+    Returns (logp, lse, n_invalid_targets[, entropy])."""
+    z = linear_logits(hidden, weight, dtype, defines)
+    return logp_fwd(z, "float64", z.shape[1], target_ids, ignore_index, defines, temperature, entropy)
 
 
 def widen(stored: np.ndarray, dtype: str, defines: tuple[str, ...] = ()) -> np.ndarray:

@@ -48,8 +48,16 @@
  *  - NaN anywhere in a row makes that row's LSE and logp NaN;
  *  - ignored rows have entropy 0 and a zero gradient whatever g_H is.
  *
- * Element types: 0 = float32, 1 = bfloat16, 2 = float16.  Every input value
- * is widened to double exactly.
+ * Element types: 0 = float32, 1 = bfloat16, 2 = float16, 3 = float64 (the
+ * exact products of the LM-head projection below).  Every input value is
+ * widened to double exactly.
+ *
+ *  - same RFC, same section: the fused LM-head and linear logp.  The logits are
+ *    the projection z[r, c] = sum_k hidden[r, k] * weight[c, k] of the row's
+ *    hidden state onto the LM-head rows (weight stored [vocab, hidden], one row
+ *    per token), and everything after that is the operator above applied to z.
+ *    bil_oracle_linear_logits forms z in float64, summing k = 0, 1, ... in
+ *    order; the products of two bf16/fp16 values are exact in double.
  *
  * Build: gcc -O2 -std=c11 -fopenmp -shared -fPIC (no -ffast-math: the order of
  * every sum below is the order written).
@@ -64,6 +72,7 @@
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
 #define ORACLE_F16 2
+#define ORACLE_F64 3
 
 /* ---- exact widening of one stored element to double ---------------------- */
 
@@ -106,6 +115,9 @@ static double load_raw(const void *base, int dtype, int64_t row, int64_t ld, int
     }
     if (dtype == ORACLE_F16) {
         return from_f16_bits(((const uint16_t *)base)[i]);
+    }
+    if (dtype == ORACLE_F64) {
+        return ((const double *)base)[i];
     }
     return (double)((const float *)base)[i];
 }
@@ -196,6 +208,37 @@ static double row_entropy(const RowView *v, int64_t vocab, double L) {
         }
     }
     return h;
+}
+
+/* ---- LM-head projection --------------------------------------------------------
+ * "Workstream 3: fused ROCm LM-head and linear logp": the logits of row r are
+ * z[r, c] = sum_{k=0}^{H-1} hidden[r, k] * weight[c, k], for the hidden state
+ * hidden [n_rows, H] (row stride ld_h) and the LM-head weight [vocab, H] (row
+ * stride ld_w), both of element type dtype.  z is written as float64 to
+ * [n_rows, ld_z]; the sum runs over k in increasing order. */
+void bil_oracle_linear_logits(const void *hidden, const void *weight, int dtype, int64_t n_rows,
+                              int64_t hidden_size, int64_t ld_h, int64_t vocab, int64_t ld_w,
+                              double *z, int64_t ld_z) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int64_t c = 0; c < vocab; ++c) {
+            double acc = 0.0;
+#ifdef BIL_ORACLE_MUTANT_LINEAR_DROPS_LAST_K
+            for (int64_t k = 0; k + 1 < hidden_size; ++k) {
+#else
+            for (int64_t k = 0; k < hidden_size; ++k) {
+#endif
+#ifdef BIL_ORACLE_MUTANT_LINEAR_TRANSPOSED
+                /* weight read as [H, vocab] */
+                double w = load_raw(weight, dtype, k % vocab, ld_w, c % hidden_size);
+#else
+                double w = load_raw(weight, dtype, c, ld_w, k);
+#endif
+                acc += load_raw(hidden, dtype, r, ld_h, k) * w;
+            }
+            z[r * ld_z + c] = acc;
+        }
+    }
 }
 
 int bil_oracle_num_threads(void) {

@@ -11,7 +11,9 @@ when the oracle disagrees with what the pages or the mathematics fix:
     gradient's row sum, central finite differences of the forward);
   * the tile construction: merged partials equal the whole-row value for any
     tile size and any split of the tiles between calls.
-  * the ignore / invalid-target rules of the operator page.
+  * the ignore / invalid-target rules of the operator page;
+  * the LM-head projection of the fused linear logp: 40-digit dot products,
+    the library's float64 matmul, and unit-vector weights that select columns.
 
 The same checks run against deliberately broken oracle builds in
 ``test_oracle_mutants.py``; every planted mistake must fail at least one.
@@ -424,10 +426,55 @@ def check_entropy_gradient_library(defines=()):
         assert np.abs(xt.grad.numpy() - d).max() <= 1e-12
 
 
-ALL_CHECKS = [check_widening, check_brute_force, check_library_log_softmax, check_closed_forms,
-              check_invariants, check_finite_differences, check_tiles, check_contract_rules,
-              check_minimal_example, check_special_values, check_entropy, check_temperature,
-              check_entropy_gradient_library]
+
+
+
+def check_linear(defines=()):
+    """The fused LM-head + logp ("[RFC][ROCm] End-to-end optimization of bitwise
+    VIME R/R beyond native P/P", "Workstream 3"): z = hidden . weight^T, then the
+    operator on z."""
+    import mpmath
+    import torch
+    # 40-digit brute force: dot products, log-sum-exp without a shift, entropy
+    mpmath.mp.dps = 40
+    n, h, v = 2, 24, 9
+    x = _rows(70, n, h, scale=1.0, dtype="bfloat16")
+    w = _rows(71, v, h, scale=0.5, dtype="bfloat16")
+    t = np.array([4, 8], np.int64)
+    lp, ls, bad, ent = oracle.linear_logp_fwd(x, w, "bfloat16", t, entropy=True, defines=defines)
+    xf, wf = oracle.widen(x, "bfloat16"), oracle.widen(w, "bfloat16")
+    assert bad == 0
+    for r in range(n):
+        z = [mpmath.fsum(mpmath.mpf(float(xf[r, k])) * mpmath.mpf(float(wf[c, k])) for k in range(h))
+             for c in range(v)]
+        lse = mpmath.log(mpmath.fsum(mpmath.exp(zc) for zc in z))
+        assert abs(float(z[t[r]] - lse) - lp[r]) <= 1e-12
+        assert abs(float(lse) - ls[r]) <= 1e-12
+        hh = -mpmath.fsum(mpmath.exp(zc - lse) * (zc - lse) for zc in z)
+        assert abs(float(hh) - ent[r]) <= 1e-12
+    # the library routine in float64, with a temperature, ragged sizes, ignored rows
+    for seed, (n, h, v, dtype, temp) in enumerate([(5, 64, 300, "bfloat16", 1.0), (4, 40, 257, "float16", 0.7),
+                                                    (3, 33, 129, "float32", 1.3)]):
+        x = _rows(seed + 72, n, h, scale=1.0, dtype=dtype)
+        w = _rows(seed + 73, v, h, scale=3.0 / math.sqrt(h), dtype=dtype)
+        t = _targets(seed + 72, n, v, ignore_rows=(1,))
+        lp, ls, _, ent = oracle.linear_logp_fwd(x, w, dtype, t, temperature=temp, entropy=True, defines=defines)
+        z = torch.from_numpy(oracle.widen(x, dtype)) @ torch.from_numpy(oracle.widen(w, dtype)).T / temp
+        tt = torch.from_numpy(t)
+        act = (tt != wl.IGNORE_INDEX).numpy()
+        ref = torch.log_softmax(z, -1).gather(-1, torch.where(tt == wl.IGNORE_INDEX, 0, tt)[:, None])[:, 0].numpy()
+        href = torch.distributions.Categorical(logits=z).entropy().numpy()
+        assert np.abs(lp[act] - ref[act]).max() <= 1e-12, (dtype, "logp")
+        assert np.abs(ent[act] - href[act]).max() <= 1e-12, (dtype, "entropy")
+        assert np.all(lp[~act] == 0.0)
+    # weight rows that are unit vectors select hidden columns: z = hidden[:, cols]
+    n, h = 6, 48
+    x = _rows(76, n, h, scale=3.0, dtype="bfloat16")
+    cols = wl.rng(76, 1).permutation(h)[:20]
+    w = np.zeros((20, h), np.float32)
+    w[np.arange(20), cols] = 1.0
+    z = oracle.linear_logits(x, wl.store(w, "bfloat16"), "bfloat16", defines=defines)
+    assert np.array_equal(z, oracle.widen(x, "bfloat16")[:, cols])
 
 
 def check_rounding_helpers():
@@ -451,3 +498,9 @@ def check_rounding_helpers():
     assert np.array_equal(oracle.round_to_bf16_bits(f.astype(np.float64)), ref)
     tiny = np.array([2.0 ** -140, -(2.0 ** -133) * 1.5, 0.0, -0.0, 1e39, -1e39])
     assert list(oracle.round_to_bf16_bits(tiny)) == [0x0000, 0x8002, 0x0000, 0x8000, 0x7F80, 0xFF80]
+
+
+ALL_CHECKS = [check_widening, check_brute_force, check_library_log_softmax, check_closed_forms,
+              check_invariants, check_finite_differences, check_tiles, check_contract_rules,
+              check_minimal_example, check_special_values, check_entropy, check_temperature,
+              check_entropy_gradient_library, check_linear]

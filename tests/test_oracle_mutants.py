@@ -32,6 +32,8 @@ MUTANTS = [
     "BIL_ORACLE_MUTANT_BF16_WIDEN",            # bf16 bits shifted by 15 instead of 16
     "BIL_ORACLE_MUTANT_ENTROPY_SIGN",          # +sum p log p
     "BIL_ORACLE_MUTANT_BWD_ENTROPY_SIGN",      # entropy gradient term added instead of subtracted
+    "BIL_ORACLE_MUTANT_LINEAR_TRANSPOSED",     # LM-head weight read as [H, V]
+    "BIL_ORACLE_MUTANT_LINEAR_DROPS_LAST_K",   # projection sum stops one term early
 ]
 
 

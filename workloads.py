@@ -26,6 +26,12 @@ vocabularies up to 151936, 4096-8192 rows, bf16) and its invariance contract
   decode    a bank of 256 rows, V=151936 bf16, x = 3*randn, uniform targets.
   packed    B=2 x T=8192 rows packed from sequences of uniform length 256-4096,
             right-padded with ignore_index, V=151936 bf16, x = 3*randn.
+  linear    the fused LM-head + logp ("[RFC][ROCm] End-to-end optimization of
+            bitwise VIME R/R beyond native P/P", "Workstream 3"; its target
+            model is Qwen3-8B: hidden size 4096, vocabulary 151936): hidden
+            states [N, 4096] bf16 ~ randn, LM-head weight [151936, 4096] bf16
+            ~ randn * 3/64 (so that the logits have standard deviation ~3, as
+            in the other workloads), uniform targets, 5% of rows ignored.
 
 "randn" scaled by s means a standard normal times s (s is the standard
 deviation).  Values are drawn in float32 and stored with round-to-nearest-even.
@@ -44,7 +50,8 @@ PADDED_VOCAB = 155648
 IGNORE_INDEX = -100
 BF16_NEG_INF = 0xFF80
 
-SEEDS = {"tiny": 0, "prefill": 1, "training": 2, "decode": 3, "packed": 4}
+SEEDS = {"tiny": 0, "prefill": 1, "training": 2, "decode": 3, "packed": 4, "linear": 5}
+HIDDEN = 4096
 
 
 def rng(seed: int, *key: int) -> np.random.Generator:
@@ -266,3 +273,63 @@ def random_rows(seed: int, n_rows: int, vocab: int, dtype: str = "bfloat16", sca
     g = rng(seed, 5).standard_normal(n_rows, dtype=np.float32)
     return Workload(f"random{seed}", store(x, dtype), dtype, vocab, tile_v, t, grad_logp=g,
                     dlogits_dtype="float32")
+
+
+@dataclass
+class LinearWorkload:
+    """Inputs of the fused LM-head + logp: hidden [N, H] and weight [V, H] as
+    stored bf16 bits, targets [N], upstream gradients [N]."""
+    name: str
+    hidden: np.ndarray
+    weight: np.ndarray
+    dtype: str
+    target_ids: np.ndarray
+    grad_logp: np.ndarray
+    ignore_index: int = IGNORE_INDEX
+
+    @property
+    def n_rows(self) -> int:
+        return self.hidden.shape[0]
+
+    @property
+    def vocab(self) -> int:
+        return self.weight.shape[0]
+
+    @property
+    def hidden_size(self) -> int:
+        return self.hidden.shape[1]
+
+
+def _normal_rows(seed: int, stream: int, n_rows: int, width: int, scale: float, chunks=None) -> np.ndarray:
+    out = np.zeros((n_rows, width), np.uint16)
+
+    def make(c, rows):
+        x = rng(seed, stream, c).standard_normal((rows, width), dtype=np.float32)
+        x *= np.float32(scale)
+        return f32_to_bf16_bits(x)
+    make.width = width
+    _fill_rows(out, n_rows, chunks, make)
+    return out
+
+
+def linear_hidden(n_rows: int, hidden: int = HIDDEN, seed: int = SEEDS["linear"], chunks=None) -> np.ndarray:
+    """Hidden states [n_rows, hidden], bf16 ~ randn; chunk c of 256 rows is stream (10, c)."""
+    return _normal_rows(seed, 10, n_rows, hidden, 1.0, chunks)
+
+
+def linear_weight(vocab: int = VOCAB, hidden: int = HIDDEN, seed: int = SEEDS["linear"], chunks=None) -> np.ndarray:
+    """LM-head weight [vocab, hidden], bf16 ~ randn * 3 / sqrt(hidden); chunk c of 256
+    vocabulary rows is stream (11, c)."""
+    return _normal_rows(seed, 11, vocab, hidden, 3.0 / np.sqrt(hidden), chunks)
+
+
+def linear(n_rows: int = 16384, hidden: int = HIDDEN, vocab: int = VOCAB, seed: int = SEEDS["linear"],
+           ignore_frac: float = 0.05) -> LinearWorkload:
+    """Qwen3-8B-shaped LM head over n_rows tokens (B=8 x T=2048 by default)."""
+    x = linear_hidden(n_rows, hidden, seed)
+    w = linear_weight(vocab, hidden, seed)
+    t = rng(seed, 1).integers(0, vocab, n_rows, dtype=np.int64)
+    n_ignored = int(round(ignore_frac * n_rows))
+    t[rng(seed, 3).permutation(n_rows)[:n_ignored]] = IGNORE_INDEX
+    g = rng(seed, 5).standard_normal(n_rows, dtype=np.float32)
+    return LinearWorkload(f"linear{n_rows}x{hidden}x{vocab}", x, w, "bfloat16", t, g)
