@@ -209,6 +209,87 @@ int bil_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab, i
 int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, int entropy,
                      int *stages, int *consumers, int64_t *smem_bytes);
 
+/* Vocabulary tile width of the fused LM-head + logp (its GEMM's N tile). */
+#define BIL_LINEAR_TILE_V 256
+
+/*
+ * bil_linear_logp_partials -- tile partials of the fused LM-head + logp
+ * ("[RFC][ROCm] End-to-end optimization of bitwise VIME R/R beyond native
+ * P/P", section "Workstream 3: fused ROCm LM-head and linear logp": the
+ * projection and the vocabulary statistics are one operation, and no
+ * [rows, vocabulary] logits are stored unless asked for; the statistics are
+ * those of "Tensor Parallel", steps 1, 2 and 5).
+ *
+ * The logits are the projection z[r, c] = sum_k hidden[r, k] * weight[c, k]
+ * (float32 accumulation on the tensor cores, K in increasing blocks of 64,
+ * the same order for every row and tile), times rcp as in bil_logp_fwd.  The
+ * vocabulary is cut into tiles of BIL_LINEAR_TILE_V columns (num_tiles =
+ * ceil(vocab / BIL_LINEAR_TILE_V)); this call fills tiles [tile_begin,
+ * tile_end), 0 <= tile_begin < tile_end <= num_tiles.
+ *
+ *  hidden        [n_rows, ld_hidden] hidden states, hidden_size <= ld_hidden.
+ *  weight        the LM-head rows of the shard: [shard, ld_weight] with row j
+ *                the weight of GLOBAL vocabulary column
+ *                tile_begin * BIL_LINEAR_TILE_V + j, for the shard's columns
+ *                (those below min(tile_end * BIL_LINEAR_TILE_V, vocab)).
+ *                hidden_size <= ld_weight.
+ *  dtype         BIL_BF16 or BIL_F16, for both hidden and weight.  Both base
+ *                addresses 16-byte aligned; ld_hidden and ld_weight multiples
+ *                of 8 (BIL_E_ALIGN otherwise).
+ *  vocab         the full vocabulary size (decides the tiles and which
+ *                targets are valid).
+ *  temperature, target_ids, ignore_index, part_max, part_sum, part_ent,
+ *  ld_part, target_logit
+ *                as for bil_logp_tile_partials, with tile_v = BIL_LINEAR_TILE_V.
+ *                Each tile's partial is taken by one thread over its 256
+ *                columns: eight slot sums over columns 8g + j, g in increasing
+ *                order, combined as ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)).
+ *  logits        NULL, or [n_rows, ld_logits] elements of logits_dtype
+ *                (BIL_F32, or BIL_BF16 rounded to nearest even) receiving the
+ *                shard's projection before the temperature is applied (column
+ *                0 = global column tile_begin * BIL_LINEAR_TILE_V); 16-byte
+ *                aligned base and row stride.  The partials are the same bits
+ *                whether or not the logits are stored.
+ * The hidden rows of ignored rows are read (the projection is computed per
+ * 128-row tile) but their partials are (-inf, 0, 0) as in
+ * bil_logp_tile_partials.
+ */
+int bil_linear_logp_partials(const void *hidden, const void *weight, int dtype, int64_t n_rows,
+                             int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight,
+                             int32_t tile_begin, int32_t tile_end, float temperature,
+                             const int64_t *target_ids, int64_t ignore_index, float *part_max,
+                             float *part_sum, float *part_ent, int64_t ld_part, float *target_logit,
+                             void *logits, int logits_dtype, int64_t ld_logits, bil_stream_t stream);
+
+/*
+ * bil_linear_logp_workspace_bytes -- bytes of device workspace that
+ * bil_linear_logp_fwd needs for n_rows rows over a vocabulary of `vocab`
+ * (entropy != 0: with the entropy output).  Host arithmetic only.
+ */
+int bil_linear_logp_workspace_bytes(int64_t n_rows, int64_t vocab, int entropy, int64_t *bytes);
+
+/*
+ * bil_linear_logp_fwd -- the fused LM-head + logp over the whole vocabulary:
+ * bil_linear_logp_partials over every tile into the caller's workspace, then
+ * bil_logp_merge.  logp, lse and entropy are as for bil_logp_fwd (of the
+ * projection, with BIL_LINEAR_TILE_V tiles).
+ *
+ *  workspace        device memory of at least
+ *                   bil_linear_logp_workspace_bytes(n_rows, vocab,
+ *                   entropy != NULL) bytes, 256-byte aligned, owned by the
+ *                   caller; its contents on entry do not matter and are
+ *                   scratch afterwards.  Two calls in flight at once need two
+ *                   workspaces.
+ *  validate         as for bil_logp_fwd (checked before anything is queued).
+ * Other arguments as for bil_linear_logp_partials.
+ */
+int bil_linear_logp_fwd(const void *hidden, const void *weight, int dtype, int64_t n_rows,
+                        int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight,
+                        float temperature, const int64_t *target_ids, int64_t ignore_index,
+                        float *logp, float *lse, float *entropy, void *logits, int logits_dtype,
+                        int64_t ld_logits, void *workspace, int64_t workspace_bytes, int validate,
+                        bil_stream_t stream);
+
 /*
  * bil_watchdog_status -- every wait inside this library's kernels is
  * bounded.  A wait that runs out sets a bit in a per-device word, and the
@@ -218,7 +299,10 @@ int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, in
  * Bits: 1 a consumer's wait for a tile, 2 the producer's wait for a free
  * stage, 4 its wait for a free row slot, 8 its wait for its own copies to
  * land, 16 a consumer met a unit outside the launch's ranges (then stopped
- * before using it).
+ * before using it).  The LM-head kernel: 32 the epilogue's wait for an
+ * accumulator, 64 the copy thread's wait for a free stage, 128 the MMA
+ * thread's wait for a stage or a free accumulator, 256 a wait of either for
+ * its own copies or MMAs to finish.
  */
 int bil_watchdog_status(unsigned int *flags, int clear);
 

@@ -15,6 +15,7 @@ OK, E_INVALID_ARG, E_DTYPE, E_ALIGN, E_TARGET_RANGE, E_CUDA, E_UNSUPPORTED = ran
 F32, BF16, F16 = 0, 1, 2
 MAX_TILE_BYTES = 64 * 1024
 MAX_FUSED_TILES = 2048
+LINEAR_TILE_V = 256
 
 # every entry point the header declares: name -> (restype, argtypes)
 _i32, _i64, _p, _u = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
@@ -31,6 +32,11 @@ SIGNATURES = {
     "bil_stream_shape": (_i32, [_i32, ctypes.c_int32, _i64, _i32, _i32, ctypes.POINTER(_i32),
                                 ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
     "bil_watchdog_status": (_i32, [ctypes.POINTER(_u), _i32]),
+    "bil_linear_logp_partials": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, ctypes.c_int32,
+                                        _f, _p, _i64, _p, _p, _p, _i64, _p, _p, _i32, _i64, _p]),
+    "bil_linear_logp_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_i64)]),
+    "bil_linear_logp_fwd": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p, _p, _i32,
+                                   _i64, _p, _i64, _i32, _p]),
 }
 
 _lock = threading.Lock()

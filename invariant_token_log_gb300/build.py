@@ -18,11 +18,12 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SOURCES = [os.path.join(HERE, "csrc", "bil.cu")]
-HEADERS = [os.path.join(ROOT, "include", "bil.h")]
+SOURCES = [os.path.join(HERE, "csrc", f) for f in ("bil.cu", "linear.cu")]
+HEADERS = [os.path.join(ROOT, "include", "bil.h")] + [
+    os.path.join(HERE, "csrc", f) for f in ("device_common.cuh", "internal.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "--fmad=false", "-std=c++17", "-Xcompiler", "-fPIC",
-              "-Xcompiler", "-Wall", "-shared"]
+              "-Xcompiler", "-Wall"]
 
 
 def library_path() -> str:
@@ -47,14 +48,26 @@ def up_to_date(out: str) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile each source to an object file (in parallel), then link libbil.so."""
     out = library_path()
     if not force and up_to_date(out):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
-    tmp = f"{out}.tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH_FLAGS, *NVCC_FLAGS, *(["-Xptxas", "-v"] if verbose else []), *SOURCES, "-o", tmp]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, out)
+    tag = f"tmp{os.getpid()}"
+    objs = [os.path.join(os.path.dirname(out), os.path.basename(src) + f".{tag}.o") for src in SOURCES]
+    procs = [subprocess.Popen([nvcc(), *ARCH_FLAGS, *NVCC_FLAGS, *(["-Xptxas", "-v"] if verbose else []),
+                               "-c", src, "-o", obj]) for src, obj in zip(SOURCES, objs)]
+    codes = [p.wait() for p in procs]
+    try:
+        if any(codes):
+            raise subprocess.CalledProcessError(max(codes), "nvcc")
+        tmp = f"{out}.{tag}"
+        subprocess.run([nvcc(), *ARCH_FLAGS, "-shared", *objs, "-o", tmp], check=True)
+        os.replace(tmp, out)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return out
 
 

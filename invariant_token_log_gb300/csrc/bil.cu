@@ -28,6 +28,8 @@
 // compiled with contraction off, so inlining cannot change them.
 
 #include "../../include/bil.h"
+#include "device_common.cuh"
+#include "internal.h"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -44,23 +46,7 @@ namespace {
 // The arithmetic contract.
 // ---------------------------------------------------------------------------
 
-constexpr int kLanes = 32;
 constexpr int kGroup = 8;  // elements a lane takes at a time: 16 bytes of bf16/fp16
-
-// log2(e) rounded to float32: exp(a) is evaluated as 2^(a * log2(e)).
-constexpr float kLog2e = 1.4426950408889634f;
-// The most negative finite float32.
-constexpr float kNegMax = -3.40282346638528859811704183484516925e38f;
-
-__device__ __forceinline__ float ex2_approx(float a) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
-  return r;
-}
-
-// exp(a) of the contract: one rounded multiply, then the hardware base-2
-// exponential (flushes results below 2^-126 to zero).
-__device__ __forceinline__ float contract_exp(float a) { return ex2_approx(__fmul_rn(a, kLog2e)); }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -469,87 +455,10 @@ constexpr unsigned kWatchEmpty = 2u;     // producer waited too long for a free 
 constexpr unsigned kWatchRowSlot = 4u;   // producer waited too long for a free row slot
 constexpr unsigned kWatchDrain = 8u;     // producer waited too long for its own copies
 constexpr unsigned kWatchProtocol = 16u; // a consumer met a unit outside the launch's ranges
-constexpr long long kWaitLimitNs = 2000000000LL;  // 2 s per wait
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ long long global_ns() {
-  long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// As mbar_try_wait, but a thread whose phase has not completed sleeps until it
-// completes or `hint_ns` pass, instead of returning at once: a waiting warp
-// then takes no issue slots from the warps doing the arithmetic.
-constexpr unsigned kSuspendHintNs = 200000;
-
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, unsigned parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return ok != 0;
-}
-
-// Warp-wide wait until the phase with parity `parity` has completed.  Every
-// lane polls (so every lane gets the barrier's acquire ordering) and the warp
-// leaves together.  Returns false if the wait ran out, or if another warp of
-// the block gave up (*abort set); the caller then stops.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity, volatile int* abort,
                                           unsigned code) {
-  long long start = 0;
-  for (unsigned spin = 0;; ++spin) {
-    const bool done = mbar_try_wait_sleep(bar, parity);
-    if (__all_sync(0xffffffffu, done)) return true;
-    if ((spin & 15u) == 15u) {
-      int stop = 0;
-      if ((threadIdx.x % kLanes) == 0) {
-        const long long now = global_ns();
-        if (start == 0) {
-          start = now;
-        } else if (*abort) {
-          stop = 1;
-        } else if (now - start > kWaitLimitNs) {
-          atomicOr(&g_watchdog, code);
-          *abort = 1;
-          stop = 1;
-        }
-      }
-      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
+  return warp_wait_watch(bar, parity, abort, code, &g_watchdog);
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.  Both
@@ -1394,6 +1303,25 @@ int launch_bwd_dt(int out_dtype, bool vec, const BwdParams& bp, cudaStream_t str
 
 }  // namespace
 
+namespace bil_internal {
+
+int check_targets_host(const int64_t* targets, int64_t n, int64_t ignore_index, int64_t vocab,
+                       cudaStream_t stream) {
+  return ::check_targets_host(targets, n, ignore_index, vocab, stream);
+}
+
+int temperature_rcp(float temperature, float* rcp) { return ::temperature_rcp(temperature, rcp); }
+
+int device_limits(int* sms, int* max_smem_optin) {
+  DeviceInfo dev;
+  if (int st = device_info(&dev)) return st;
+  *sms = dev.sms;
+  *max_smem_optin = dev.max_smem_optin;
+  return BIL_OK;
+}
+
+}  // namespace bil_internal
+
 // ---------------------------------------------------------------------------
 // C ABI
 // ---------------------------------------------------------------------------
@@ -1613,6 +1541,9 @@ int bil_watchdog_status(unsigned int* flags, int clear) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_watchdog, &zero, sizeof(unsigned int)) != cudaSuccess) return BIL_E_CUDA;
   }
+  unsigned int linear = 0;
+  if (int st = bil_internal::linear_watchdog(&linear, clear)) return st;
+  *flags |= linear;
   return BIL_OK;
 }
 

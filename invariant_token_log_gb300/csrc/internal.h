@@ -1,0 +1,31 @@
+// Host functions shared by the library's translation units.  They are not
+// part of the C ABI (hidden visibility: the shared library does not export
+// them).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define BIL_INTERNAL __attribute__((visibility("hidden")))
+
+namespace bil_internal {
+
+// Check active targets on the host: copies them in chunks through a stack
+// buffer (synchronises the stream).  BIL_E_TARGET_RANGE if an active target
+// lies outside [0, vocab).
+BIL_INTERNAL int check_targets_host(const int64_t* targets, int64_t n, int64_t ignore_index, int64_t vocab,
+                                    cudaStream_t stream);
+
+// rcp = 1/temperature rounded once to float32; BIL_E_INVALID_ARG unless the
+// temperature is finite and > 0 and its reciprocal is finite.
+BIL_INTERNAL int temperature_rcp(float temperature, float* rcp);
+
+// Streaming multiprocessors and opt-in shared memory per block of the current
+// device (cached per device).
+BIL_INTERNAL int device_limits(int* sms, int* max_smem_optin);
+
+// The LM-head kernels' watchdog word of the current device (see
+// bil_watchdog_status); cleared when `clear` is non-zero.
+BIL_INTERNAL int linear_watchdog(unsigned int* flags, int clear);
+
+}  // namespace bil_internal

@@ -1,0 +1,630 @@
+// Fused LM-head + selected-token log-probability ("linear logp") for sm_103a.
+//
+// Operator: "[RFC][ROCm] End-to-end optimization of bitwise VIME R/R beyond
+// native P/P", section "Workstream 3: fused ROCm LM-head and linear logp":
+// the LM-head projection z = hidden . weight^T and the vocabulary statistics
+// of the "Batch-Invariant LogP" operator ("Tensor Parallel", steps 1-6) are
+// one operation.  Each vocabulary tile's (max, sum-exp[, entropy statistic],
+// target logit) is produced from the projection's accumulator, without
+// storing the [rows, vocabulary] logits unless the caller asks for them, and
+// the tiles are then merged in the operator's one fixed order (the library's
+// merge kernel).  The C ABI is declared in include/bil.h.
+//
+// One kernel, persistent, one block per SM, warp-specialised:
+//   warp 0      TMA producer: 128-row hidden tile and 256-row weight tile per
+//               64-element K block, 128-byte swizzled, into a 4-stage ring;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16/fp16 in, fp32
+//               accumulate in tensor memory), K blocks in increasing order,
+//               four K=16 steps each; two accumulator buffers of 256 columns;
+//   warps 2-5   epilogue: thread i of the warp reading lanes [32q, 32q+32)
+//               owns row 32q+i of the tile and reduces its 256 columns from
+//               tensor memory into the tile's partial.
+// The accumulator of one tile is read while the next tile's MMAs run.
+//
+// What fixes the bits of z[r, c] is the K order (K blocks in order, four
+// K=16 steps each, from a zeroed accumulator), the same for every row and
+// every tile, and what fixes the partial is the per-thread reduction order
+// below; neither depends on the number of rows, the row's position, the
+// launch geometry or the vocabulary split, so the result is batch-invariant
+// and split-invariant like the logits path.
+
+#include "../../include/bil.h"
+#include "device_common.cuh"
+#include "internal.h"
+
+#include <cuda.h>  // CUtensorMap and its enums (types only; the encoder is fetched at run time)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+namespace {
+
+__device__ unsigned int g_watchdog_linear;
+
+constexpr unsigned kWatchAccFull = 32u;    // epilogue waited too long for an accumulator
+constexpr unsigned kWatchStageFree = 64u;  // producer waited too long for a free stage
+constexpr unsigned kWatchMma = 128u;       // MMA issuer waited too long for a stage or an accumulator
+constexpr unsigned kWatchOwnDrain = 256u;  // producer or MMA issuer waited too long for its own work
+
+constexpr int kBM = 128;      // rows per tile: one tensor-memory lane per row
+constexpr int kBN = 256;      // vocabulary columns per tile = the operator's tile width here
+constexpr int kBK = 64;       // K per stage: 64 x 16 bits = one 128-byte swizzle row
+constexpr int kUmmaK = 16;    // K of one tcgen05.mma kind::f16
+constexpr int kStages = 4;
+constexpr unsigned kStageABytes = kBM * kBK * 2;  // 16 KB
+constexpr unsigned kStageBBytes = kBN * kBK * 2;  // 32 KB
+constexpr unsigned kStageBytes = kStageABytes + kStageBBytes;
+constexpr int kAccCols = kBN;            // one 32-bit tensor-memory column per output column
+constexpr uint32_t kTmemCols = 2 * kAccCols;  // two accumulator buffers: 512 columns
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kChunk = 32;               // columns per tensor-memory load
+constexpr int kMGroup = 32;              // row tiles per raster group (L2 reuse of the weight tiles)
+
+static_assert(BIL_LINEAR_TILE_V == kBN, "the C ABI's tile width is the kernel's N tile");
+
+struct alignas(8) LinearSmem {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * size_t(kStageBytes) + sizeof(LinearSmem);
+
+struct LinearParams {
+  int64_t n_rows;
+  int64_t shard_cols;   // weight rows (vocabulary columns) of the shard
+  int tile_begin;       // global tile index of the shard's first column
+  int num_n;            // tiles of the shard
+  int num_m;            // row tiles
+  int k_blocks;         // ceil(hidden / kBK)
+  const int64_t* targets;
+  int64_t ignore_index;
+  float rcp;
+  float* part_max;
+  float* part_sum;
+  float* part_ent;
+  int64_t ld_part;
+  float* target_logit;
+  unsigned char* logits;  // NULL: not stored
+  int logits_dtype;
+  int64_t ld_logits;
+  uint32_t idesc;
+};
+
+// ---------------------------------------------------------------------------
+// tcgen05 / TMA wrappers.
+// ---------------------------------------------------------------------------
+
+// Instruction descriptor of tcgen05.mma kind::f16: D float32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9, 10-12 = 1) or fp16 (0), both K-major (bits 15, 16 =
+// 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t make_idesc(bool bf16) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor of a K-major operand stored the way a TMA
+// load with 128-byte swizzle writes it: rows of 128 bytes (64 elements of K),
+// 8-row groups 1024 bytes apart (stride byte offset), start address >> 4 in
+// bits 0-13, leading byte offset (unused for this layout) 16 bytes, the fixed
+// 0b001 in bits 46-48, swizzle mode 2 (128 bytes) in bits 61-63.  The 8-row
+// groups start on 1024-byte boundaries, so the base offset is 0; a K step
+// within the 128-byte row advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(16 >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (tensor memory) = A . B^T (+ D when accumulate != 0), one thread.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane, waited
+// for in the same statement (so no use of the registers can be scheduled
+// before the data has arrived).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[kChunk]) {
+  __syncwarp();  // the load is warp-wide (.sync.aligned): the warp must be converged
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Row tile m and vocabulary tile n (shard-local) of work unit u: groups of
+// kMGroup row tiles; within a group the row tile varies fastest, so the
+// blocks working at one time share a few weight tiles through L2.
+__device__ __forceinline__ void unit_coords(int64_t u, int num_m, int num_n, int& m, int& n) {
+  const int64_t per_group = static_cast<int64_t>(kMGroup) * num_n;
+  const int g = static_cast<int>(u / per_group);
+  const int r = static_cast<int>(u - g * per_group);
+  const int m0 = g * kMGroup;
+  const int gm = min(kMGroup, num_m - m0);
+  n = r / gm;
+  m = m0 + (r - n * gm);
+}
+
+// ---------------------------------------------------------------------------
+// The epilogue of one row of one tile: the tile partial of the operator, over
+// the tile's valid columns [0, vcols), from the float32 accumulator.
+//
+//   z_c = acc_c *rn rcp
+//   m   = max over valid c of z_c (exact)
+//   d_c = z_c -rn m (m = -inf: d_c = z_c), e_c = exp(d_c) of the contract
+//   slot accumulators a_j, j = 0..7, take e_c for c = 8g + j, g = 0, 1, ...,
+//   31 in order; s = ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)); the entropy sum
+//   u = sum e_c * max(d_c, -FLT_MAX) in the same slots and tree (one fma per
+//   column).
+//
+// This is one lane of the logits path's in-tile order with 32 groups and no
+// warp butterfly: a tile here is one thread's row.
+// ---------------------------------------------------------------------------
+
+template <bool ENT>
+__device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp, int64_t tloc, bool store,
+                                            unsigned char* out_row, int out_dtype, float& m_out, float& s_out,
+                                            float& u_out, float& tl_out) {
+  uint32_t r[kChunk];
+  float m = -INFINITY;
+  float tl = 0.0f;
+#pragma unroll 1
+  for (int c0 = 0; c0 < kBN; c0 += kChunk) {
+    tmem_ld32(taddr + c0, r);
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const float z = __fmul_rn(__uint_as_float(r[j]), rcp);
+      if (c0 + j < vcols) m = fmaxf(m, z);
+      if (c0 + j == tloc) tl = z;
+    }
+    if (store && c0 < vcols) {
+      if (out_dtype == BIL_F32) {
+        float* o = reinterpret_cast<float*>(out_row) + c0;
+        if (c0 + kChunk <= vcols) {
+#pragma unroll
+          for (int j = 0; j < kChunk; j += 4)
+            *reinterpret_cast<uint4*>(o + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j)
+            if (c0 + j < vcols) o[j] = __uint_as_float(r[j]);
+        }
+      } else {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out_row) + c0;
+        uint32_t pk[kChunk / 2];
+#pragma unroll
+        for (int j = 0; j < kChunk; j += 2) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+          pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        if (c0 + kChunk <= vcols) {
+#pragma unroll
+          for (int j = 0; j < kChunk / 2; j += 4)
+            *reinterpret_cast<uint4*>(o + 2 * j) = make_uint4(pk[j], pk[j + 1], pk[j + 2], pk[j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j)
+            if (c0 + j < vcols) o[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        }
+      }
+    }
+  }
+  const float shift = (m == -INFINITY) ? 0.0f : m;
+  float a[8], u[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    a[j] = 0.0f;
+    u[j] = 0.0f;
+  }
+#pragma unroll 1
+  for (int c0 = 0; c0 < kBN; c0 += kChunk) {
+    tmem_ld32(taddr + c0, r);
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const float d = __fsub_rn(__fmul_rn(__uint_as_float(r[j]), rcp), shift);
+      float e = contract_exp(d);
+      if (c0 + j >= vcols) e = 0.0f;  // columns past the vocabulary add nothing
+      a[j % 8] = __fadd_rn(a[j % 8], e);
+      if (ENT) u[j % 8] = __fmaf_rn(e, fmaxf(d, kNegMax), u[j % 8]);
+    }
+  }
+  s_out = __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
+                    __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
+  if (ENT)
+    u_out = __fadd_rn(__fadd_rn(__fadd_rn(u[0], u[1]), __fadd_rn(u[2], u[3])),
+                      __fadd_rn(__fadd_rn(u[4], u[5]), __fadd_rn(u[6], u[7])));
+  m_out = m;
+  tl_out = tl;
+}
+
+template <bool ENT>
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_partials_kernel(const __grid_constant__ CUtensorMap tmap_hidden,
+                           const __grid_constant__ CUtensorMap tmap_weight, const LinearParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  // Stage buffers start on a 1024-byte boundary (the 128-byte swizzle pattern
+  // repeats every 8 rows = 1024 bytes).
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  LinearSmem& sm = *reinterpret_cast<LinearSmem*>(base + kStages * size_t(kStageBytes));
+  volatile int* abort = &sm.abort;
+  const int warp = threadIdx.x / kLanes;
+  const int lane = threadIdx.x % kLanes;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], kEpiWarps);
+    }
+    mbar_init(&sm.mma_done, 1);
+    sm.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sm.tmem_base;
+
+  const int64_t total = static_cast<int64_t>(p.num_m) * p.num_n;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer ----
+      int64_t it = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        int m, n;
+        unit_coords(u, p.num_m, p.num_n, m, n);
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const int s = static_cast<int>(it % kStages);
+          const unsigned ph = static_cast<unsigned>((it / kStages) & 1);
+          if (!thread_wait_watch(&sm.empty[s], ph ^ 1u, abort, kWatchStageFree, &g_watchdog_linear, true)) {
+            ok = false;
+            break;
+          }
+          unsigned char* a_dst = base + s * size_t(kStageBytes);
+          mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+          tma_load_2d(a_dst, &tmap_hidden, kb * kBK, m * kBM, &sm.full[s]);
+          tma_load_2d(a_dst + kStageABytes, &tmap_weight, kb * kBK, n * kBN, &sm.full[s]);
+        }
+      }
+      // Wait (bounded, whatever happened) for the copies still in flight: the
+      // last min(it, kStages) fills, one per stage.
+      for (int64_t i = it > kStages ? it - kStages : 0; i < it; ++i) {
+        const int s = static_cast<int>(i % kStages);
+        if (!thread_wait_watch(&sm.full[s], static_cast<unsigned>((i / kStages) & 1), abort, kWatchOwnDrain,
+                               &g_watchdog_linear, false))
+          break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      int64_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x, ++local) {
+        const int b = local & 1;
+        const unsigned use = static_cast<unsigned>(local >> 1);
+        if (!thread_wait_watch(&sm.acc_empty[b], (use & 1u) ^ 1u, abort, kWatchMma, &g_watchdog_linear, true)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kAccCols);
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const int s = static_cast<int>(it % kStages);
+          const unsigned ph = static_cast<unsigned>((it / kStages) & 1);
+          if (!thread_wait_watch(&sm.full[s], ph, abort, kWatchMma, &g_watchdog_linear, true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(base + s * size_t(kStageBytes));
+          const uint32_t b_addr = a_addr + kStageABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            umma_f16(d_tmem, smem_desc(a_addr + k * kUmmaK * 2), smem_desc(b_addr + k * kUmmaK * 2), p.idesc,
+                     (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&sm.empty[s]);  // the stage is free once these MMAs have read it
+        }
+        if (!ok) break;
+        umma_commit(&sm.acc_full[b]);
+      }
+      // Every MMA this thread issued completes before the block frees tensor memory.
+      umma_commit(&sm.mma_done);
+      thread_wait_watch(&sm.mma_done, 0u, abort, kWatchOwnDrain, &g_watchdog_linear, false);
+    }
+  } else {
+    // ---- epilogue ----
+    const int q = warp & 3;  // this warp reads tensor-memory lanes [32q, 32q + 32)
+    const int row_in_tile = q * 32 + lane;
+    int local = 0;
+    for (int64_t u = blockIdx.x; u < total; u += gridDim.x, ++local) {
+      int m, n;
+      unit_coords(u, p.num_m, p.num_n, m, n);
+      const int b = local & 1;
+      const unsigned use = static_cast<unsigned>(local >> 1);
+      const int64_t row = static_cast<int64_t>(m) * kBM + row_in_tile;
+      const bool valid = row < p.n_rows;
+      const int64_t t = valid ? p.targets[row] : p.ignore_index;
+      const bool active = valid && t != p.ignore_index;
+      const int64_t col0 = static_cast<int64_t>(n) * kBN;  // shard-local column of the tile's column 0
+      const int vcols = static_cast<int>(p.shard_cols - col0 < kBN ? p.shard_cols - col0 : kBN);
+      const int64_t gcol0 = static_cast<int64_t>(p.tile_begin + n) * kBN;
+      const int64_t tloc = active ? t - gcol0 : -1;
+      if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * kAccCols);
+      float mt, st, ut = 0.0f, tl;
+      const bool store = valid && p.logits != nullptr;
+      unsigned char* out_row =
+          store ? p.logits + (row * p.ld_logits + col0) * (p.logits_dtype == BIL_F32 ? 4 : 2) : nullptr;
+      row_partial<ENT>(taddr, vcols, p.rcp, tloc, store, out_row, p.logits_dtype, mt, st, ut, tl);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+      if (valid) {
+        const int64_t at = row * p.ld_part + p.tile_begin + n;
+        p.part_max[at] = active ? mt : -INFINITY;
+        p.part_sum[at] = active ? st : 0.0f;
+        if (ENT) p.part_ent[at] = active ? ut : 0.0f;
+        if (tloc >= 0 && tloc < vcols) p.target_logit[row] = tl;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time (no link-time
+// dependency on the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A 2-D tensor map over a row-major [rows, cols] matrix of 16-bit elements
+// (row stride ld elements), box = box_rows x 64 elements, 128-byte swizzle;
+// reads past the matrix fill zeros.
+int make_map(CUtensorMap* map, const void* ptr, int dtype, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return BIL_E_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == BIL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BIL_OK : BIL_E_CUDA;
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+template <bool ENT>
+int launch_linear(const CUtensorMap& mh, const CUtensorMap& mw, const LinearParams& p, cudaStream_t stream) {
+  int sms = 0, smem_optin = 0;
+  if (int st = bil_internal::device_limits(&sms, &smem_optin)) return st;
+  if (static_cast<size_t>(smem_optin) < kSmemBytes) return BIL_E_UNSUPPORTED;
+  auto kernel = linear_partials_kernel<ENT>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
+      cudaSuccess)
+    return BIL_E_CUDA;
+  const int64_t total = static_cast<int64_t>(p.num_m) * p.num_n;
+  const int grid = static_cast<int>(std::min<int64_t>(total, sms));
+  kernel<<<grid, kThreads, kSmemBytes, stream>>>(mh, mw, p);
+  return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
+}
+
+// Workspace layout of bil_linear_logp_fwd: part_max, part_sum[, part_ent]
+// ([n_rows, num_tiles] float32 each), target_logit [n_rows], each block
+// starting on a 256-byte boundary.
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+struct Workspace {
+  size_t part, tl, total;
+};
+
+Workspace workspace_layout(int64_t n_rows, int64_t num_tiles, bool ent) {
+  Workspace w;
+  w.part = round256(static_cast<size_t>(n_rows) * static_cast<size_t>(num_tiles) * sizeof(float));
+  w.tl = round256(static_cast<size_t>(n_rows) * sizeof(float));
+  w.total = w.part * (ent ? 3 : 2) + w.tl;
+  return w;
+}
+
+}  // namespace
+
+namespace bil_internal {
+
+int linear_watchdog(unsigned int* flags, int clear) {
+  if (cudaMemcpyFromSymbol(flags, g_watchdog_linear, sizeof(unsigned int)) != cudaSuccess) return BIL_E_CUDA;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_watchdog_linear, &zero, sizeof(unsigned int)) != cudaSuccess) return BIL_E_CUDA;
+  }
+  return BIL_OK;
+}
+
+}  // namespace bil_internal
+
+extern "C" {
+
+int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, int64_t n_rows,
+                             int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight,
+                             int32_t tile_begin, int32_t tile_end, float temperature, const int64_t* target_ids,
+                             int64_t ignore_index, float* part_max, float* part_sum, float* part_ent,
+                             int64_t ld_part, float* target_logit, void* logits, int logits_dtype,
+                             int64_t ld_logits, bil_stream_t stream) {
+  if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
+  if (n_rows < 0 || hidden_size < 1 || vocab < 1 || ld_hidden < hidden_size || ld_weight < hidden_size)
+    return BIL_E_INVALID_ARG;
+  const int64_t num_tiles = (vocab + kBN - 1) / kBN;
+  if (num_tiles > INT32_MAX / 2) return BIL_E_UNSUPPORTED;
+  if (tile_begin < 0 || tile_begin >= tile_end || tile_end > num_tiles || ld_part < num_tiles)
+    return BIL_E_INVALID_ARG;
+  const int64_t shard_cols = std::min<int64_t>(static_cast<int64_t>(tile_end) * kBN, vocab) -
+                             static_cast<int64_t>(tile_begin) * kBN;
+  if (logits != nullptr) {
+    if (logits_dtype != BIL_F32 && logits_dtype != BIL_BF16) return BIL_E_DTYPE;
+    if (ld_logits < shard_cols) return BIL_E_INVALID_ARG;
+  }
+  float rcp = 1.0f;
+  if (int st = bil_internal::temperature_rcp(temperature, &rcp)) return st;
+  if (n_rows == 0) return BIL_OK;
+  if (hidden == nullptr || weight == nullptr || target_ids == nullptr || part_max == nullptr ||
+      part_sum == nullptr || target_logit == nullptr)
+    return BIL_E_INVALID_ARG;
+  // TMA: 16-byte aligned bases and row strides.
+  if (!aligned_to(hidden, 16) || !aligned_to(weight, 16) || (ld_hidden * 2) % 16 != 0 || (ld_weight * 2) % 16 != 0)
+    return BIL_E_ALIGN;
+  if (!aligned_to(target_ids, 8) || !aligned_to(part_max, 4) || !aligned_to(part_sum, 4) ||
+      (part_ent && !aligned_to(part_ent, 4)) || !aligned_to(target_logit, 4))
+    return BIL_E_ALIGN;
+  if (logits != nullptr) {
+    const int64_t eb = logits_dtype == BIL_F32 ? 4 : 2;
+    if (!aligned_to(logits, 16) || (ld_logits * eb) % 16 != 0) return BIL_E_ALIGN;
+  }
+  if (n_rows > (static_cast<int64_t>(INT32_MAX) - kBM) || shard_cols > INT32_MAX - kBN) return BIL_E_UNSUPPORTED;
+
+  CUtensorMap mh, mw;
+  if (int st = make_map(&mh, hidden, dtype, n_rows, hidden_size, ld_hidden, kBM)) return st;
+  if (int st = make_map(&mw, weight, dtype, shard_cols, hidden_size, ld_weight, kBN)) return st;
+
+  LinearParams p{};
+  p.n_rows = n_rows;
+  p.shard_cols = shard_cols;
+  p.tile_begin = tile_begin;
+  p.num_n = tile_end - tile_begin;
+  p.num_m = static_cast<int>((n_rows + kBM - 1) / kBM);
+  p.k_blocks = static_cast<int>((hidden_size + kBK - 1) / kBK);
+  p.targets = target_ids;
+  p.ignore_index = ignore_index;
+  p.rcp = rcp;
+  p.part_max = part_max;
+  p.part_sum = part_sum;
+  p.part_ent = part_ent;
+  p.ld_part = ld_part;
+  p.target_logit = target_logit;
+  p.logits = static_cast<unsigned char*>(logits);
+  p.logits_dtype = logits_dtype;
+  p.ld_logits = ld_logits;
+  p.idesc = make_idesc(dtype == BIL_BF16);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return part_ent != nullptr ? launch_linear<true>(mh, mw, p, s) : launch_linear<false>(mh, mw, p, s);
+}
+
+int bil_linear_logp_workspace_bytes(int64_t n_rows, int64_t vocab, int entropy, int64_t* bytes) {
+  if (n_rows < 0 || vocab < 1 || bytes == nullptr) return BIL_E_INVALID_ARG;
+  const int64_t num_tiles = (vocab + kBN - 1) / kBN;
+  *bytes = static_cast<int64_t>(workspace_layout(n_rows, num_tiles, entropy != 0).total);
+  return BIL_OK;
+}
+
+int bil_linear_logp_fwd(const void* hidden, const void* weight, int dtype, int64_t n_rows, int64_t hidden_size,
+                        int64_t ld_hidden, int64_t vocab, int64_t ld_weight, float temperature,
+                        const int64_t* target_ids, int64_t ignore_index, float* logp, float* lse, float* entropy,
+                        void* logits, int logits_dtype, int64_t ld_logits, void* workspace,
+                        int64_t workspace_bytes, int validate, bil_stream_t stream) {
+  if (n_rows < 0 || vocab < 1) return BIL_E_INVALID_ARG;
+  const int64_t num_tiles = (vocab + kBN - 1) / kBN;
+  const Workspace w = workspace_layout(n_rows, num_tiles, entropy != nullptr);
+  if (n_rows == 0) return BIL_OK;
+  if (logp == nullptr || workspace == nullptr) return BIL_E_INVALID_ARG;
+  if (workspace_bytes < static_cast<int64_t>(w.total)) return BIL_E_INVALID_ARG;
+  if (!aligned_to(workspace, 256)) return BIL_E_ALIGN;
+  if (!aligned_to(logp, 4) || (lse && !aligned_to(lse, 4)) || (entropy && !aligned_to(entropy, 4)))
+    return BIL_E_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (validate && target_ids != nullptr) {
+    if (int st = bil_internal::check_targets_host(target_ids, n_rows, ignore_index, vocab, s)) return st;
+  }
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  float* pm = reinterpret_cast<float*>(ws);
+  float* ps = reinterpret_cast<float*>(ws + w.part);
+  float* pe = entropy != nullptr ? reinterpret_cast<float*>(ws + 2 * w.part) : nullptr;
+  float* tl = reinterpret_cast<float*>(ws + w.part * (entropy != nullptr ? 3 : 2));
+  if (int st = bil_linear_logp_partials(hidden, weight, dtype, n_rows, hidden_size, ld_hidden, vocab, ld_weight, 0,
+                                        static_cast<int32_t>(num_tiles), temperature, target_ids, ignore_index, pm,
+                                        ps, pe, num_tiles, tl, logits, logits_dtype, ld_logits, stream))
+    return st;
+  return bil_logp_merge(pm, ps, pe, n_rows, static_cast<int32_t>(num_tiles), num_tiles, tl, target_ids,
+                        ignore_index, vocab, logp, lse, entropy, 0, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,140 @@
+"""PyTorch front end of the fused LM-head + logp: argument marshalling only.
+
+"[RFC][ROCm] End-to-end optimization of bitwise VIME R/R beyond native P/P",
+section "Workstream 3: fused ROCm LM-head and linear logp": the projection
+z = hidden . weight^T and the selected-token log-probability (with the
+optional lse, entropy and unscaled logits) are one operation; the logits are
+stored only when asked for, and logp / lse / entropy are the same bits either
+way.  The projection runs on the tensor cores (tcgen05) inside the CUDA
+library, followed by the operator's fixed-order merge over tiles of
+``LINEAR_TILE_V`` (256) vocabulary columns.
+
+Layouts: hidden [*lead, H] and weight [V, H] (one row per vocabulary entry,
+as an LM-head ``Linear`` stores it), both bfloat16 or both float16, rows
+16-byte aligned.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from .logp import IGNORE_INDEX, _need_cuda, _ptr, _stream
+
+LINEAR_TILE_V = _lib.LINEAR_TILE_V
+_IN_DTYPES = {torch.bfloat16: _lib.BF16, torch.float16: _lib.F16}
+_OUT_DTYPES = {torch.float32: _lib.F32, torch.bfloat16: _lib.BF16}
+
+
+def _in_code(dtype: torch.dtype) -> int:
+    try:
+        return _IN_DTYPES[dtype]
+    except KeyError:
+        raise TypeError(f"hidden and weight must be bfloat16 or float16, not {dtype}") from None
+
+
+def _matrix(x: torch.Tensor, what: str) -> torch.Tensor:
+    """[*lead, H] -> [N, H] with unit column stride and a row stride the C ABI accepts."""
+    x2 = x.reshape(-1, x.shape[-1])
+    if x2.shape[0] and (x2.stride(-1) != 1 or (x2.stride(0) * 2) % 16 or x2.data_ptr() % 16):
+        x2 = x2.contiguous()
+        if (x2.stride(0) * 2) % 16:
+            raise ValueError(f"{what}: the last dimension must be a multiple of 8 elements (16-byte rows)")
+    return x2
+
+
+def _ld(x2: torch.Tensor) -> int:
+    return x2.stride(0) if x2.shape[0] > 1 else max(x2.stride(0), x2.shape[1])
+
+
+def num_tiles(vocab: int) -> int:
+    return -(-vocab // LINEAR_TILE_V)
+
+
+def workspace_bytes(n_rows: int, vocab: int, entropy: bool = False) -> int:
+    out = ctypes.c_int64(0)
+    _lib.check("bil_linear_logp_workspace_bytes",
+               _lib.load().bil_linear_logp_workspace_bytes(n_rows, vocab, int(entropy), ctypes.byref(out)))
+    return out.value
+
+
+def linear_logp_partials(hidden: torch.Tensor, weight_shard: torch.Tensor, target_ids: torch.Tensor, vocab: int,
+                         tile_begin: int, tile_end: int, part_max: torch.Tensor, part_sum: torch.Tensor,
+                         target_logit: torch.Tensor, ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                         part_ent: torch.Tensor | None = None, logits_out: torch.Tensor | None = None) -> None:
+    """Tile partials of tiles [tile_begin, tile_end) into [N, ld_part] float32 buffers.
+
+    ``weight_shard`` row j is the LM-head row of global vocabulary column
+    ``tile_begin * LINEAR_TILE_V + j``; ``logits_out`` (optional, float32 or
+    bfloat16, [N, >= shard columns]) receives the shard's unscaled logits."""
+    _need_cuda(hidden, weight_shard, target_ids, part_max, part_sum, target_logit, part_ent, logits_out)
+    h2, w2 = _matrix(hidden, "hidden"), _matrix(weight_shard, "weight")
+    if h2.dtype != w2.dtype:
+        raise TypeError("hidden and weight must have the same element type")
+    if h2.shape[1] != w2.shape[1]:
+        raise ValueError(f"hidden size {h2.shape[1]} != weight's {w2.shape[1]}")
+    t = target_ids.reshape(-1).to(torch.int64).contiguous()
+    n = h2.shape[0]
+    if t.shape[0] != n:
+        raise ValueError("target_ids must have one entry per hidden row")
+    for buf in (part_max, part_sum) + ((part_ent,) if part_ent is not None else ()):
+        if buf.dtype != torch.float32 or buf.dim() != 2 or buf.shape[0] != n or buf.stride(1) != 1:
+            raise ValueError("partials must be [N, >= num_tiles] float32 with unit column stride")
+    if part_ent is not None and part_ent.stride(0) != part_max.stride(0):
+        raise ValueError("part_ent must have part_max's row stride")
+    ld_out, out_code = 0, _lib.F32
+    if logits_out is not None:
+        if logits_out.dtype not in _OUT_DTYPES or logits_out.dim() != 2 or logits_out.stride(1) != 1:
+            raise ValueError("logits_out must be [N, >= shard columns] float32 or bfloat16, unit column stride")
+        ld_out, out_code = logits_out.stride(0), _OUT_DTYPES[logits_out.dtype]
+    _lib.check("bil_linear_logp_partials", _lib.load().bil_linear_logp_partials(
+        _ptr(h2), _ptr(w2), _in_code(h2.dtype), n, h2.shape[1], _ld(h2), vocab, _ld(w2), tile_begin, tile_end,
+        float(temperature), _ptr(t), ignore_index, _ptr(part_max), _ptr(part_sum), _ptr(part_ent),
+        part_max.stride(0), _ptr(target_logit), _ptr(logits_out), out_code, ld_out, _stream(h2.device)))
+
+
+def linear_logp(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torch.Tensor,
+                ignore_index: int = IGNORE_INDEX, temperature: float = 1.0, return_entropy: bool = False,
+                return_logits: bool = False, logits_dtype: torch.dtype = torch.float32, validate: bool = False,
+                workspace: torch.Tensor | None = None):
+    """Fused LM-head + logp: (logp, lse[, entropy][, logits]) for hidden [*lead, H] and
+    weight [V, H]; logp/lse/entropy are float32 with the targets' shape, logits
+    [*lead, V] of ``logits_dtype`` (the projection before the temperature)."""
+    _need_cuda(hidden, weight, target_ids, workspace)
+    lead = hidden.shape[:-1]
+    if tuple(target_ids.shape) != tuple(lead):
+        raise ValueError(f"target_ids shape {tuple(target_ids.shape)} != hidden's leading shape {tuple(lead)}")
+    h2, w2 = _matrix(hidden, "hidden"), _matrix(weight, "weight")
+    if h2.dtype != w2.dtype:
+        raise TypeError("hidden and weight must have the same element type")
+    if h2.shape[1] != w2.shape[1]:
+        raise ValueError(f"hidden size {h2.shape[1]} != weight's {w2.shape[1]}")
+    n, vocab = h2.shape[0], w2.shape[0]
+    t = target_ids.reshape(-1).to(torch.int64).contiguous()
+    dev = h2.device
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    ent = torch.empty(n, dtype=torch.float32, device=dev) if return_entropy else None
+    logits = None
+    if return_logits:
+        if logits_dtype not in _OUT_DTYPES:
+            raise TypeError("logits_dtype must be float32 or bfloat16")
+        cols = -(-vocab // 8) * 8  # 16-byte rows for either output type
+        logits = torch.empty((n, cols), dtype=logits_dtype, device=dev)[:, :vocab]
+    need = workspace_bytes(n, vocab, return_entropy)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, needs {need}")
+    _lib.check("bil_linear_logp_fwd", _lib.load().bil_linear_logp_fwd(
+        _ptr(h2), _ptr(w2), _in_code(h2.dtype), n, h2.shape[1], _ld(h2), vocab, _ld(w2), float(temperature),
+        _ptr(t), ignore_index, _ptr(logp), _ptr(lse), _ptr(ent), _ptr(logits),
+        _OUT_DTYPES.get(logits_dtype, _lib.F32), logits.stride(0) if logits is not None else 0, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), int(validate), _stream(dev)))
+    out = [logp.reshape(lead), lse.reshape(lead)]
+    if return_entropy:
+        out.append(ent.reshape(lead))
+    if return_logits:
+        out.append(logits.reshape(*lead, vocab))
+    return tuple(out)

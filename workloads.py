@@ -300,36 +300,40 @@ class LinearWorkload:
         return self.hidden.shape[1]
 
 
-def _normal_rows(seed: int, stream: int, n_rows: int, width: int, scale: float, chunks=None) -> np.ndarray:
+def _normal_rows(seed: int, stream: int, n_rows: int, width: int, scale: float, chunks=None,
+                 dtype: str = "bfloat16") -> np.ndarray:
     out = np.zeros((n_rows, width), np.uint16)
 
     def make(c, rows):
         x = rng(seed, stream, c).standard_normal((rows, width), dtype=np.float32)
         x *= np.float32(scale)
-        return f32_to_bf16_bits(x)
+        return store(x, dtype)
     make.width = width
     _fill_rows(out, n_rows, chunks, make)
     return out
 
 
-def linear_hidden(n_rows: int, hidden: int = HIDDEN, seed: int = SEEDS["linear"], chunks=None) -> np.ndarray:
-    """Hidden states [n_rows, hidden], bf16 ~ randn; chunk c of 256 rows is stream (10, c)."""
-    return _normal_rows(seed, 10, n_rows, hidden, 1.0, chunks)
+def linear_hidden(n_rows: int, hidden: int = HIDDEN, seed: int = SEEDS["linear"], chunks=None,
+                  dtype: str = "bfloat16") -> np.ndarray:
+    """Hidden states [n_rows, hidden] ~ randn (bf16 or fp16 bits); chunk c of 256 rows is
+    stream (10, c)."""
+    return _normal_rows(seed, 10, n_rows, hidden, 1.0, chunks, dtype)
 
 
-def linear_weight(vocab: int = VOCAB, hidden: int = HIDDEN, seed: int = SEEDS["linear"], chunks=None) -> np.ndarray:
-    """LM-head weight [vocab, hidden], bf16 ~ randn * 3 / sqrt(hidden); chunk c of 256
-    vocabulary rows is stream (11, c)."""
-    return _normal_rows(seed, 11, vocab, hidden, 3.0 / np.sqrt(hidden), chunks)
+def linear_weight(vocab: int = VOCAB, hidden: int = HIDDEN, seed: int = SEEDS["linear"], chunks=None,
+                  dtype: str = "bfloat16") -> np.ndarray:
+    """LM-head weight [vocab, hidden] ~ randn * 3 / sqrt(hidden) (bf16 or fp16 bits); chunk c
+    of 256 vocabulary rows is stream (11, c)."""
+    return _normal_rows(seed, 11, vocab, hidden, 3.0 / np.sqrt(hidden), chunks, dtype)
 
 
 def linear(n_rows: int = 16384, hidden: int = HIDDEN, vocab: int = VOCAB, seed: int = SEEDS["linear"],
-           ignore_frac: float = 0.05) -> LinearWorkload:
+           ignore_frac: float = 0.05, dtype: str = "bfloat16") -> LinearWorkload:
     """Qwen3-8B-shaped LM head over n_rows tokens (B=8 x T=2048 by default)."""
-    x = linear_hidden(n_rows, hidden, seed)
-    w = linear_weight(vocab, hidden, seed)
+    x = linear_hidden(n_rows, hidden, seed, dtype=dtype)
+    w = linear_weight(vocab, hidden, seed, dtype=dtype)
     t = rng(seed, 1).integers(0, vocab, n_rows, dtype=np.int64)
     n_ignored = int(round(ignore_frac * n_rows))
     t[rng(seed, 3).permutation(n_rows)[:n_ignored]] = IGNORE_INDEX
     g = rng(seed, 5).standard_normal(n_rows, dtype=np.float32)
-    return LinearWorkload(f"linear{n_rows}x{hidden}x{vocab}", x, w, "bfloat16", t, g)
+    return LinearWorkload(f"linear{n_rows}x{hidden}x{vocab}", x, w, dtype, t, g)
