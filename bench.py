@@ -1,6 +1,7 @@
 """Benchmark: selected-token logp forward + backward, rows/s and HBM GB/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bil|reference]
+    python bench.py --workload linear [...]     # the fused LM-head + logp
 
 Workload (one step = the whole operator path over one batch):
   training: N=16384 rows (B=8 x T=2048), V=151936 bf16 logits ~ 3*randn, tile
@@ -16,6 +17,12 @@ host<->device copies inside the timed region.  ``roofline`` rates the
 backward kernel (two thirds of the step's bytes) against the measured HBM
 copy bandwidth.  ``cpu_baseline`` times the CPU oracle on a sample of the
 same workload.  ``--impl reference`` times the CPU oracle alone (rank 0).
+
+``--workload linear`` measures the fused LM-head + logp instead: hidden
+[16384, 4096] bf16 times a Qwen3-8B-shaped LM head [151936, 4096] bf16, with
+the tile partials taken from the tensor-core accumulator and the fixed-order
+merge (forward only).  Its roofline is the partials kernel against the
+measured dense bf16 tensor throughput.
 """
 from __future__ import annotations
 
@@ -41,6 +48,14 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "bil.cu")
+LINEAR_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "linear.cu")
+LINEAR_METRIC = "fused LM-head + logp forward rows/s and achieved TFLOP/s (% of GB300 dense bf16) at H=4096, V=151936"
+LINEAR_WORKLOAD = ("linear: N=16384 rows (B=8 x T=2048) of bf16 hidden states ~ randn, H=4096, LM-head weight "
+                   "[151936, 4096] bf16 ~ randn*3/64 (Qwen3-8B shape), uniform targets, 5% rows ignored; "
+                   "forward logp + lse, 256-column vocabulary tiles")
+LINEAR_CPU_ROWS = 32
+LINEAR_REFERENCE_ROWS = 16
+FALLBACK_BF16_TFLOPS = 1900.0
 REFERENCE_ROWS_PER_STEP = 256
 CPU_BASELINE_ROWS = 8192
 
@@ -55,6 +70,7 @@ def parse():
     ap.add_argument("--rows", type=int, default=16384,
                     help="rows of the workload per GPU (smaller only for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["training", "linear"], default="training")
     return ap.parse_args()
 
 
@@ -238,13 +254,22 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(kernel: str):
+def tensor_peak():
+    """(burst, sustained, source) dense bf16 TFLOP/s."""
+    try:
+        peaks = json.load(open(PEAKS_FILE))
+        return float(peaks["bf16_tflops"]), float(peaks["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def ncu_traffic(kernel: str, source: str = KERNEL_SOURCE):
     """DRAM bytes per launch from a committed ncu capture, if it was taken on this kernel source."""
     try:
         lines = open(TRAFFIC_FILE).read().splitlines()
     except OSError:
         return None
-    sha = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()[:16]
+    sha = hashlib.sha256(open(source, "rb").read()).hexdigest()[:16]
     for line in lines:
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
         if f.get("kernel") == kernel and f.get("source_sha") == sha and "bytes_per_launch" in f:
@@ -391,9 +416,186 @@ def run_bil(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# the fused LM-head + logp
+# ---------------------------------------------------------------------------
+
+def oracle_linear_rows_per_s(rows: int):
+    """Time the CPU oracle's LM-head projection + forward over `rows` rows."""
+    import oracle
+    import workloads as wl
+    oracle.build()
+    x = wl.linear_hidden(rows)
+    w = wl.linear_weight()
+    t = wl.rng(wl.SEEDS["linear"], 1).integers(0, w.shape[0], rows, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.linear_logp_fwd(x, w, "bfloat16", t)
+    dt = time.perf_counter() - t0
+    return rows / dt, dt, oracle.num_threads()
+
+
+def run_linear_reference(args):
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import workloads as wl
+    oracle.build()
+    rows = LINEAR_REFERENCE_ROWS
+    x = wl.linear_hidden(rows)
+    w = wl.linear_weight()
+    t = wl.rng(wl.SEEDS["linear"], 1).integers(0, w.shape[0], rows, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle.linear_logp_fwd(x, w, "bfloat16", t)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.linear_logp_fwd(x, w, "bfloat16", t)
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    print(json.dumps({
+        "impl": "reference", "metric": LINEAR_METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, host-generated)",
+        "config": {"workload": LINEAR_WORKLOAD, "rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{rows} rows of the workload per step, float64 oracle, projection + forward"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_linear(args):
+    import torch
+
+    import invariant_token_log_gb300 as bil
+    import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    bil.load()
+
+    lw = wl.linear(args.rows)
+    n, h, v = lw.n_rows, lw.hidden_size, lw.vocab
+    x_host = torch.from_numpy(lw.hidden.view(np.int16)).view(torch.bfloat16).pin_memory()
+    t_host = torch.from_numpy(lw.target_ids).pin_memory()
+    x = x_host.to(dev)
+    t = t_host.to(dev)
+    wt = torch.from_numpy(lw.weight.view(np.int16)).view(torch.bfloat16).to(dev)
+    nt = -(-v // bil.LINEAR_TILE_V)
+    pm = torch.empty((n, nt), dtype=torch.float32, device=dev)
+    ps = torch.empty((n, nt), dtype=torch.float32, device=dev)
+    tl = torch.empty(n, dtype=torch.float32, device=dev)
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bil.linear_logp_partials(x, wt, t, v, 0, nt, pm, ps, tl)
+        bil.logp_merge(pm, ps, nt, tl, t, v, out=logp, lse=lse)
+
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    host_t0 = time.time()
+    for i in range(K):
+        ev[i][0].record(stream)
+        bil.linear_logp_partials(x, wt, t, v, 0, nt, pm, ps, tl)
+        ev[i][1].record(stream)
+        bil.logp_merge(pm, ps, nt, tl, t, v, out=logp, lse=lse)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    host_t1 = time.time()
+    barrier(dist, dev)
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    part_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    merge_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    sampler.stop()
+    clocks = sampler.summary(host_t0, host_t1)
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    ms_step, value = aggregate(n, world, K, total_ms)
+    flops = 2.0 * n * h * v
+    tflops = flops / (part_ms / 1e3) / 1e12
+    burst, sustained, peak_kind = tensor_peak()
+    # the kernel is timed inside a loop of K back-to-back launches (seconds under
+    # the power cap), so the sustained figure is its denominator
+    peak = sustained
+
+    e2e = None
+    if args.e2e_steps > 0:
+        logp_host = torch.empty(n, dtype=torch.float32).pin_memory()
+        lse_host = torch.empty(n, dtype=torch.float32).pin_memory()
+        ws = torch.empty(bil.linear.workspace_bytes(n, v), dtype=torch.uint8, device=dev)
+        xd = torch.empty_like(x)
+        td = torch.empty_like(t)
+
+        def e2e_step():
+            xd.copy_(x_host, non_blocking=True)
+            td.copy_(t_host, non_blocking=True)
+            lp, ls = bil.linear_logp(xd, wt, td, workspace=ws)
+            logp_host.copy_(lp, non_blocking=True)
+            lse_host.copy_(ls, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
+        marks[0].record(stream)
+        for i in range(args.e2e_steps):
+            e2e_step()
+            marks[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), dist, dev)
+        h2d = x_host.numel() * 2 + t_host.numel() * 8
+        d2h = logp_host.numel() * 4 + lse_host.numel() * 4
+        e2e = {"value": n * world * args.e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.e2e_steps,
+               "steps": args.e2e_steps,
+               "path": "linear_logp: pinned host hidden states -> device (weight resident) -> pinned host logp, lse"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rps, dt, cores = oracle_linear_rows_per_s(LINEAR_CPU_ROWS)
+        cpu = {"value": rps, "unit": "rows/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {LINEAR_CPU_ROWS} rows of the workload, float64 projection + forward, "
+                         f"{dt:.1f} s wall"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": LINEAR_METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, host-generated)",
+            "config": {"workload": LINEAR_WORKLOAD, "rows_per_gpu": n, "hidden": h, "vocab": v,
+                       "tile_v": bil.LINEAR_TILE_V,
+                       "l2": "no flush: every pass reads the 1.25 GB LM-head weight, 9.6x the 129 MB L2",
+                       "parallelism": f"dp{world} (independent row batches per GPU, weight replicated)"},
+            "tflops": flops / (ms_step / 1e3) / 1e12,
+            "kernels": {"linear_partials": {"ms": part_ms, "tflops": tflops},
+                        "logp_merge": {"ms": merge_ms}},
+            "roofline": {"kernel": "linear_partials_kernel", "bound": "tensor", "achieved": tflops, "peak": peak,
+                         "peak_source": f"{peak_kind} sustained dense bf16 (burst {burst})", "unit": "TFLOP/s",
+                         "frac": tflops / peak, "frac_of_burst": tflops / burst,
+                         "traffic": ncu_traffic("linear_partials_kernel", LINEAR_SOURCE),
+                         "algorithmic_flops_per_launch": flops},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
+        }), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.workload == "linear":
+        run_linear_reference(args) if args.impl == "reference" else run_linear(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_bil(args)

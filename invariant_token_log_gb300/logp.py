@@ -142,9 +142,11 @@ def logp_tile_partials(logits_shard: torch.Tensor, target_ids: torch.Tensor, voc
 
 def logp_merge(part_max: torch.Tensor, part_sum: torch.Tensor, num_tiles: int, target_logit: torch.Tensor,
                target_ids: torch.Tensor, vocab: int, ignore_index: int = IGNORE_INDEX, validate: bool = False,
-               part_ent: torch.Tensor | None = None):
+               part_ent: torch.Tensor | None = None, out: torch.Tensor | None = None,
+               lse: torch.Tensor | None = None, entropy: torch.Tensor | None = None):
     """Fixed-order merge of [N, T] partials: (logp, lse) float32 [N], and the
-    entropy as a third result when ``part_ent`` is given."""
+    entropy as a third result when ``part_ent`` is given (``out``, ``lse``,
+    ``entropy``: optional preallocated float32 [N] outputs)."""
     _need_cuda(part_max, part_sum, target_logit, target_ids)
     n = part_max.shape[0]
     t1 = _targets1d(target_ids, (n,), part_max.device)
@@ -153,9 +155,14 @@ def logp_merge(part_max: torch.Tensor, part_sum: torch.Tensor, num_tiles: int, t
             raise ValueError("the partial buffers must be row-major with one row stride")
     if part_max.stride(1) != 1:
         raise ValueError("part_max must be row-major")
-    out = torch.empty(n, dtype=torch.float32, device=part_max.device)
-    lse = torch.empty(n, dtype=torch.float32, device=part_max.device)
-    ent = torch.empty(n, dtype=torch.float32, device=part_max.device) if part_ent is not None else None
+    for o in (out, lse, entropy):
+        if o is not None and (o.dtype != torch.float32 or o.numel() != n or not o.is_contiguous()):
+            raise ValueError("merge outputs must be contiguous float32 [N]")
+    out = torch.empty(n, dtype=torch.float32, device=part_max.device) if out is None else out
+    lse = torch.empty(n, dtype=torch.float32, device=part_max.device) if lse is None else lse
+    ent = None
+    if part_ent is not None:
+        ent = torch.empty(n, dtype=torch.float32, device=part_max.device) if entropy is None else entropy
     lib = _lib.load()
     with torch.cuda.device(part_max.device):
         st = lib.bil_logp_merge(_ptr(part_max), _ptr(part_sum), _ptr(part_ent), n, int(num_tiles), part_max.stride(0),
