@@ -290,6 +290,42 @@ int bil_linear_logp_fwd(const void *hidden, const void *weight, int dtype, int64
                         int64_t ld_logits, void *workspace, int64_t workspace_bytes, int validate,
                         bil_stream_t stream);
 
+/* Size of the device array that bil_linear_logp_fwd_static uses as its scratch. */
+#define BIL_LINEAR_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * bil_linear_logp_fwd_static -- bil_linear_logp_fwd without a caller
+ * workspace.  The pages have no counterpart of this entry point: it exists
+ * for callers that cannot allocate device memory per call (a C or C++ host
+ * driving this ABI directly, without a device memory pool, would otherwise
+ * pay a cudaMalloc / cudaFree pair on every call, and those synchronise the
+ * device).
+ *
+ * The scratch (tile partials and target logits) is one file-scope device
+ * array of BIL_LINEAR_STATIC_SCRATCH_BYTES bytes (8 MiB) in the library's
+ * device image; nothing is allocated or freed.  Sizes whose scratch,
+ * bil_linear_logp_workspace_bytes(n_rows, vocab, entropy != NULL), exceeds
+ * that return BIL_E_UNSUPPORTED and queue nothing (at vocab = 151936: up to
+ * 1763 rows, or 1176 with the entropy).
+ *
+ *  First call on each device: the call looks up the array's device address
+ *  (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *  first call before any stream capture on the device.
+ *  Nothing in the scratch has to start at zero: every entry the merge reads
+ *  is written earlier in the same call.
+ *  The array is shared by every call on the device: two calls whose work
+ *  overlaps in time (different streams, or different host threads without
+ *  ordering between their streams) race on it and give wrong results; order
+ *  them (one stream, or events).
+ *  The logits are not stored (use bil_linear_logp_fwd for that).
+ * Other arguments, results and errors as for bil_linear_logp_fwd.
+ */
+int bil_linear_logp_fwd_static(const void *hidden, const void *weight, int dtype, int64_t n_rows,
+                               int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight,
+                               float temperature, const int64_t *target_ids, int64_t ignore_index,
+                               float *logp, float *lse, float *entropy, int validate,
+                               bil_stream_t stream);
+
 /*
  * bil_watchdog_status -- every wait inside this library's kernels is
  * bounded.  A wait that runs out sets a bit in a per-device word, and the

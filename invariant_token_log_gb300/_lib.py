@@ -16,6 +16,7 @@ F32, BF16, F16 = 0, 1, 2
 MAX_TILE_BYTES = 64 * 1024
 MAX_FUSED_TILES = 2048
 LINEAR_TILE_V = 256
+LINEAR_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 # every entry point the header declares: name -> (restype, argtypes)
 _i32, _i64, _p, _u = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
@@ -37,6 +38,8 @@ SIGNATURES = {
     "bil_linear_logp_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_i64)]),
     "bil_linear_logp_fwd": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p, _p, _i32,
                                    _i64, _p, _i64, _i32, _p]),
+    "bil_linear_logp_fwd_static": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p, _i32,
+                                          _p]),
 }
 
 _lock = threading.Lock()

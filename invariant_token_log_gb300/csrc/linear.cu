@@ -508,6 +508,29 @@ Workspace workspace_layout(int64_t n_rows, int64_t num_tiles, bool ent) {
   return w;
 }
 
+// Device scratch of bil_linear_logp_fwd_static: one array per device image,
+// never allocated or freed at run time.
+static __device__ __align__(256) unsigned char g_linear_static_scratch[BIL_LINEAR_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxStaticDevices = 64;
+void* g_static_scratch_ptr[kMaxStaticDevices];
+std::mutex g_static_scratch_mutex;
+
+// The array's device address on the current device, looked up once per device
+// (with that device current) and cached.
+int static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxStaticDevices) return BIL_E_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
+  if (g_static_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_linear_static_scratch) != cudaSuccess || ptr == nullptr) return BIL_E_CUDA;
+    g_static_scratch_ptr[dev] = ptr;
+  }
+  *out = g_static_scratch_ptr[dev];
+  return BIL_OK;
+}
+
 }  // namespace
 
 namespace bil_internal {
@@ -625,6 +648,22 @@ int bil_linear_logp_fwd(const void* hidden, const void* weight, int dtype, int64
     return st;
   return bil_logp_merge(pm, ps, pe, n_rows, static_cast<int32_t>(num_tiles), num_tiles, tl, target_ids,
                         ignore_index, vocab, logp, lse, entropy, 0, stream);
+}
+
+int bil_linear_logp_fwd_static(const void* hidden, const void* weight, int dtype, int64_t n_rows,
+                               int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight,
+                               float temperature, const int64_t* target_ids, int64_t ignore_index, float* logp,
+                               float* lse, float* entropy, int validate, bil_stream_t stream) {
+  if (n_rows < 0 || vocab < 1) return BIL_E_INVALID_ARG;
+  const int64_t num_tiles = (vocab + kBN - 1) / kBN;
+  const Workspace w = workspace_layout(n_rows, num_tiles, entropy != nullptr);
+  if (w.total > BIL_LINEAR_STATIC_SCRATCH_BYTES) return BIL_E_UNSUPPORTED;
+  if (n_rows == 0) return BIL_OK;
+  void* scratch = nullptr;
+  if (int st = static_scratch(&scratch)) return st;
+  return bil_linear_logp_fwd(hidden, weight, dtype, n_rows, hidden_size, ld_hidden, vocab, ld_weight, temperature,
+                             target_ids, ignore_index, logp, lse, entropy, nullptr, BIL_F32, 0, scratch,
+                             static_cast<int64_t>(BIL_LINEAR_STATIC_SCRATCH_BYTES), validate, stream);
 }
 
 }  // extern "C"
