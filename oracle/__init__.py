@@ -85,6 +85,9 @@ def load(defines: tuple[str, ...] = ()) -> ctypes.CDLL:
         lib.bil_oracle_logp_bwd.argtypes = [vp, i32, i64, i64, i64, vp, i64, f64, dp, dp, dp, i64, i64]
         lib.bil_oracle_linear_logits.restype = None
         lib.bil_oracle_linear_logits.argtypes = [vp, vp, i32, i64, i64, i64, i64, i64, dp, i64]
+        lib.bil_oracle_linear_bwd.restype = i64
+        lib.bil_oracle_linear_bwd.argtypes = [vp, vp, i32, i64, i64, i64, i64, i64, vp, i64, f64, dp, dp, dp, dp,
+                                              dp]
         lib.bil_oracle_widen.restype = None
         lib.bil_oracle_widen.argtypes = [vp, i32, i64, dp]
         _libs[defines] = lib
@@ -229,6 +232,28 @@ def linear_logp_fwd(hidden: np.ndarray, weight: np.ndarray, dtype: str, target_i
     Returns (logp, lse, n_invalid_targets[, entropy])."""
     z = linear_logits(hidden, weight, dtype, defines)
     return logp_fwd(z, "float64", z.shape[1], target_ids, ignore_index, defines, temperature, entropy)
+
+
+def linear_logp_bwd(hidden: np.ndarray, weight: np.ndarray, dtype: str, target_ids: np.ndarray,
+                    grad_logp: np.ndarray, ignore_index: int = -100, temperature: float = 1.0,
+                    grad_entropy: np.ndarray | None = None, defines: tuple[str, ...] = ()):
+    """float64 (dhidden [N, H], dweight [V, H], dZ [N, V], n_invalid_targets): the
+    gradient of g * logp (+ gH * entropy) of the fused LM-head + logp."""
+    n, ld_h = _check_logits(hidden, dtype)
+    v, ld_w = _check_logits(weight, dtype)
+    h = hidden.shape[1]
+    tgt = np.ascontiguousarray(target_ids, dtype=np.int64)
+    g = np.ascontiguousarray(grad_logp, dtype=np.float64)
+    gh = None if grad_entropy is None else np.ascontiguousarray(grad_entropy, dtype=np.float64)
+    dx = np.empty((n, h), np.float64)
+    dw = np.empty((v, h), np.float64)
+    dz = np.empty((n, v), np.float64)
+    bad = load(defines).bil_oracle_linear_bwd(_ptr(hidden), _ptr(weight), _code(dtype), n, h, ld_h, v, ld_w,
+                                              _ptr(tgt), ignore_index, float(temperature), _ptr(g), _optr(gh),
+                                              _ptr(dx), _ptr(dw), _ptr(dz))
+    if bad < 0:
+        raise MemoryError("oracle: out of memory in linear_logp_bwd")
+    return dx, dw, dz, int(bad)
 
 
 def widen(stored: np.ndarray, dtype: str, defines: tuple[str, ...] = ()) -> np.ndarray:

@@ -64,6 +64,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -474,6 +475,66 @@ int64_t bil_oracle_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64
             d[c] = temperature == 1.0 ? dz : dz / temperature;
         }
     }
+    return bad;
+}
+
+/* ---- LM-head backward ----------------------------------------------------------
+ * "Workstream 3: fused ROCm LM-head and linear logp", the autograd actor path:
+ * the gradient of g * logp + g_H * H with respect to the hidden states and the
+ * LM-head weight.  dZ = d(g logp + g_H H)/dz is bil_oracle_logp_bwd applied to
+ * the float64 projection z = hidden . weight^T (bil_oracle_linear_logits), and
+ * the chain rule through z gives
+ *   dhidden[r, k] = sum_c dZ[r, c] * weight[c, k]    (c = 0, 1, ... in order)
+ *   dweight[c, k] = sum_r dZ[r, c] * hidden[r, k]    (r = 0, 1, ... in order)
+ * for dhidden [n_rows, hidden_size] and dweight [vocab, hidden_size] (both
+ * row-major, float64).  dZ is also written to dz [n_rows, vocab] when dz is not
+ * NULL.  Returns the number of active rows with an invalid target (their
+ * dZ rows, and so every gradient, are NaN), or -1 if memory ran out. */
+int64_t bil_oracle_linear_bwd(const void *hidden, const void *weight, int dtype, int64_t n_rows,
+                              int64_t hidden_size, int64_t ld_h, int64_t vocab, int64_t ld_w,
+                              const int64_t *target_ids, int64_t ignore_index, double temperature,
+                              const double *grad_logp, const double *grad_entropy,
+                              double *dhidden, double *dweight, double *dz) {
+    double *z = malloc(sizeof(double) * (size_t)(n_rows * vocab > 0 ? n_rows * vocab : 1));
+    double *d = dz != NULL ? dz : malloc(sizeof(double) * (size_t)(n_rows * vocab > 0 ? n_rows * vocab : 1));
+    if (z == NULL || d == NULL) {
+        free(z);
+        if (dz == NULL) free(d);
+        return -1;
+    }
+    bil_oracle_linear_logits(hidden, weight, dtype, n_rows, hidden_size, ld_h, vocab, ld_w, z, vocab);
+    int64_t bad = bil_oracle_logp_bwd(z, ORACLE_F64, n_rows, vocab, vocab, target_ids, ignore_index,
+                                      temperature, grad_logp, grad_entropy, d, vocab, vocab);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int64_t k = 0; k < hidden_size; ++k) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < vocab; ++c) {
+#ifdef BIL_ORACLE_MUTANT_LINEAR_BWD_DX_TRANSPOSED
+                acc += d[r * vocab + c] * load_raw(weight, dtype, k % vocab, ld_w, c % hidden_size);
+#else
+                acc += d[r * vocab + c] * load_raw(weight, dtype, c, ld_w, k);
+#endif
+            }
+            dhidden[r * hidden_size + k] = acc;
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t c = 0; c < vocab; ++c) {
+        for (int64_t k = 0; k < hidden_size; ++k) {
+            double acc = 0.0;
+            for (int64_t r = 0; r < n_rows; ++r) {
+#ifdef BIL_ORACLE_MUTANT_LINEAR_BWD_DW_ROW_SHIFT
+                acc += d[r * vocab + c] * load_raw(hidden, dtype, (r + 1) % n_rows, ld_h, k);
+#else
+                acc += d[r * vocab + c] * load_raw(hidden, dtype, r, ld_h, k);
+#endif
+            }
+            dweight[c * hidden_size + k] = acc;
+        }
+    }
+    free(z);
+    if (dz == NULL) free(d);
     return bad;
 }
 

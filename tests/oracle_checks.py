@@ -477,6 +477,64 @@ def check_linear(defines=()):
     assert np.array_equal(z, oracle.widen(x, "bfloat16")[:, cols])
 
 
+def check_linear_backward(defines=()):
+    """The fused LM-head's backward ("Workstream 3", the autograd actor path):
+    autograd of the library's float64 matmul + log-softmax + entropy, central
+    differences on float64 inputs, and the bilinear identity
+    <dX, X> = <dZ, z> = <dW, W> (z is bilinear in X and W)."""
+    import torch
+    for seed, (n, h, v, dtype, temp, ent) in enumerate([(5, 40, 300, "bfloat16", 1.0, False),
+                                                         (4, 24, 257, "float16", 0.8, True),
+                                                         (6, 16, 100, "float32", 1.3, True)]):
+        x = _rows(seed + 80, n, h, scale=1.0, dtype=dtype)
+        w = _rows(seed + 81, v, h, scale=3.0 / math.sqrt(h), dtype=dtype)
+        t = _targets(seed + 80, n, v, ignore_rows=(1,))
+        g = wl.rng(seed, 82).standard_normal(n)
+        gh = wl.rng(seed, 83).standard_normal(n) if ent else None
+        dx, dw, dz, bad = oracle.linear_logp_bwd(x, w, dtype, t, g, temperature=temp, grad_entropy=gh,
+                                                  defines=defines)
+        assert bad == 0
+        xt = torch.from_numpy(oracle.widen(x, dtype)).requires_grad_(True)
+        wt = torch.from_numpy(oracle.widen(w, dtype)).requires_grad_(True)
+        z = xt @ wt.T / temp
+        tt = torch.from_numpy(t)
+        act = tt != wl.IGNORE_INDEX
+        sel = torch.log_softmax(z, -1).gather(-1, torch.where(act, tt, 0)[:, None])[:, 0]
+        loss = (torch.where(act, sel, 0) * torch.from_numpy(g)).sum()
+        if ent:
+            hh = torch.distributions.Categorical(logits=z).entropy()
+            loss = loss + (torch.where(act, hh, 0) * torch.from_numpy(gh)).sum()
+        loss.backward()
+        assert np.abs(xt.grad.numpy() - dx).max() <= 1e-12 * max(1.0, np.abs(dx).max()), (dtype, "dhidden")
+        assert np.abs(wt.grad.numpy() - dw).max() <= 1e-12 * max(1.0, np.abs(dw).max()), (dtype, "dweight")
+        zz = oracle.linear_logits(x, w, dtype)
+        ip_x = float((dx * oracle.widen(x, dtype)).sum())
+        ip_w = float((dw * oracle.widen(w, dtype)).sum())
+        ip_z = float((dz * zz).sum())
+        assert abs(ip_x - ip_z) <= 1e-9 * max(1.0, abs(ip_z)) and abs(ip_w - ip_z) <= 1e-9 * max(1.0, abs(ip_z))
+    # central differences on float64 inputs (every x +- h is exact on this grid)
+    n, h, v, hs = 2, 8, 30, 2.0 ** -20
+    x = np.round(wl.rng(90, 1).standard_normal((n, h)) * 64) / 64
+    w = np.round(wl.rng(90, 2).standard_normal((v, h)) * 64) / 64
+    t = np.array([3, 17], np.int64)
+    g, gh = np.array([0.75, -1.25]), np.array([0.5, 2.0])
+    dx, dw, _, _ = oracle.linear_logp_bwd(x, w, "float64", t, g, temperature=0.9, grad_entropy=gh, defines=defines)
+
+    def f(xx, ww):
+        lp, _, _, hh = oracle.linear_logp_fwd(xx, ww, "float64", t, temperature=0.9, entropy=True, defines=defines)
+        return float((g * lp + gh * hh).sum())
+    for (r, k) in ((0, 0), (1, 5), (0, 7)):
+        xp, xm = x.copy(), x.copy()
+        xp[r, k] += hs
+        xm[r, k] -= hs
+        assert abs((f(xp, w) - f(xm, w)) / (2 * hs) - dx[r, k]) <= 1e-6, ("dhidden", r, k)
+    for (c, k) in ((3, 1), (17, 6), (29, 0)):
+        wp, wm = w.copy(), w.copy()
+        wp[c, k] += hs
+        wm[c, k] -= hs
+        assert abs((f(x, wp) - f(x, wm)) / (2 * hs) - dw[c, k]) <= 1e-6, ("dweight", c, k)
+
+
 def check_rounding_helpers():
     """float64 -> bf16 rounding: ties to even at exact midpoints, nearest elsewhere,
     and equal to the library float32 -> bf16 conversion on float32 values."""
@@ -503,4 +561,4 @@ def check_rounding_helpers():
 ALL_CHECKS = [check_widening, check_brute_force, check_library_log_softmax, check_closed_forms,
               check_invariants, check_finite_differences, check_tiles, check_contract_rules,
               check_minimal_example, check_special_values, check_entropy, check_temperature,
-              check_entropy_gradient_library, check_linear]
+              check_entropy_gradient_library, check_linear, check_linear_backward]

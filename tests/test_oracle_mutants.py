@@ -34,6 +34,8 @@ MUTANTS = [
     "BIL_ORACLE_MUTANT_BWD_ENTROPY_SIGN",      # entropy gradient term added instead of subtracted
     "BIL_ORACLE_MUTANT_LINEAR_TRANSPOSED",     # LM-head weight read as [H, V]
     "BIL_ORACLE_MUTANT_LINEAR_DROPS_LAST_K",   # projection sum stops one term early
+    "BIL_ORACLE_MUTANT_LINEAR_BWD_DX_TRANSPOSED",  # dhidden contracts with the weight read as [H, V]
+    "BIL_ORACLE_MUTANT_LINEAR_BWD_DW_ROW_SHIFT",   # dweight pairs dZ row r with hidden row r + 1
 ]
 
 
