@@ -290,6 +290,64 @@ int bil_linear_logp_fwd(const void *hidden, const void *weight, int dtype, int64
                         int64_t ld_logits, void *workspace, int64_t workspace_bytes, int validate,
                         bil_stream_t stream);
 
+/*
+ * bil_linear_logp_bwd -- backward of the fused LM-head + logp ("[RFC][ROCm]
+ * End-to-end optimization of bitwise VIME R/R beyond native P/P", section
+ * "Workstream 3": the autograd actor path; the backward recomputes the
+ * projection tiles from the saved LSE instead of keeping the logits).
+ *
+ * With z = hidden . weight^T (recomputed exactly as the forward computes it)
+ * and the library's backward formula per element,
+ *     dZ = (g (onehot - p) [- gh p (a + H)]) [* rcp],  a = z*rcp - lse, p = exp(a)
+ * (the bits bil_logp_bwd gives for float32 logits z), rounded to dtype:
+ *     dhidden = dZ . weight        [n_rows, hidden_size]
+ *     dweight = dZ^T . hidden      [vocab, hidden_size]
+ * both accumulated in float32 on the tensor cores in K blocks of 64 in
+ * increasing order (K = vocab for dhidden, n_rows for dweight), so a row's
+ * dhidden never depends on the other rows.
+ *
+ *  hidden, weight, dtype, n_rows, hidden_size, ld_hidden, vocab, ld_weight,
+ *  temperature, target_ids, ignore_index
+ *                as for bil_linear_logp_fwd over the whole vocabulary.
+ *  weight_t      the weight transposed, [hidden_size, ld_weight_t] (ld_weight_t
+ *                >= vocab), e.g. from bil_transpose_2d; a caller keeps it as
+ *                long as the weight does not change.
+ *  lse           [n_rows] float32, the forward's lse.
+ *  grad_logp     [n_rows] float32 upstream gradient of logp.
+ *  entropy, grad_entropy   both NULL, or the forward's entropy and its
+ *                upstream gradient ([n_rows] float32 each).
+ *  dz            [n_rows, ld_dz] (ld_dz >= vocab) of dtype: receives dZ.
+ *  dz_t          [vocab, ld_dz_t] (ld_dz_t >= n_rows) of dtype: receives dZ^T.
+ *  hidden_t      [hidden_size, ld_hidden_t] (ld_hidden_t >= n_rows) of dtype:
+ *                receives hidden^T.
+ *                (dz, dz_t and hidden_t are the backward's scratch, owned by
+ *                the caller, readable afterwards.)
+ *  dhidden       [n_rows, ld_dhidden] of dhidden_dtype (BIL_F32, or dtype
+ *                rounded to nearest even).
+ *  dweight       [vocab, ld_dweight] of dweight_dtype (the same choice).
+ * Every matrix argument needs a 16-byte aligned base and a row stride of a
+ * multiple of 16 bytes (BIL_E_ALIGN otherwise).  Inactive rows contribute
+ * zero; an active row with a target outside [0, vocab) makes its dZ row NaN
+ * (and so its dhidden row and every dweight entry it touches).  n_rows = 0
+ * sets dweight to zero.
+ */
+int bil_linear_logp_bwd(const void *hidden, const void *weight, const void *weight_t, int dtype,
+                        int64_t n_rows, int64_t hidden_size, int64_t ld_hidden, int64_t vocab,
+                        int64_t ld_weight, int64_t ld_weight_t, float temperature,
+                        const int64_t *target_ids, int64_t ignore_index, const float *lse,
+                        const float *grad_logp, const float *entropy, const float *grad_entropy,
+                        void *dz, int64_t ld_dz, void *dz_t, int64_t ld_dz_t, void *hidden_t,
+                        int64_t ld_hidden_t, void *dhidden, int dhidden_dtype, int64_t ld_dhidden,
+                        void *dweight, int dweight_dtype, int64_t ld_dweight, bil_stream_t stream);
+
+/*
+ * bil_transpose_2d -- dst[c, r] = src[r, c] for a [rows, cols] matrix of
+ * 16-bit elements (BIL_BF16 or BIL_F16); ld_src >= cols, ld_dst >= rows.
+ * Prepares the transposed LM-head weight that bil_linear_logp_bwd takes.
+ */
+int bil_transpose_2d(const void *src, int dtype, int64_t rows, int64_t cols, int64_t ld_src, void *dst,
+                     int64_t ld_dst, bil_stream_t stream);
+
 /* Size of the device array that bil_linear_logp_fwd_static uses as its scratch. */
 #define BIL_LINEAR_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
 

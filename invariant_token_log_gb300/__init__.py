@@ -10,7 +10,14 @@ PyTorch front end.  Build the library with
 """
 from ._lib import BilError, contract_id, library_path, load  # noqa: F401
 from .host_pipeline import HostStreamedLogp  # noqa: F401
-from .linear import LINEAR_TILE_V, linear_logp, linear_logp_partials  # noqa: F401
+from .linear import (  # noqa: F401
+    LINEAR_TILE_V,
+    LinearLogp,
+    batch_invariant_linear_logp,
+    linear_logp,
+    linear_logp_bwd,
+    linear_logp_partials,
+)
 from .logp import (  # noqa: F401
     DEFAULT_TILE_V,
     IGNORE_INDEX,

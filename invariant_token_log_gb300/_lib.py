@@ -38,6 +38,9 @@ SIGNATURES = {
     "bil_linear_logp_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_i64)]),
     "bil_linear_logp_fwd": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p, _p, _i32,
                                    _i64, _p, _i64, _i32, _p]),
+    "bil_linear_logp_bwd": (_i32, [_p, _p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p,
+                                   _p, _p, _i64, _p, _i64, _p, _i64, _p, _i32, _i64, _p, _i32, _i64, _p]),
+    "bil_transpose_2d": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, _p]),
     "bil_linear_logp_fwd_static": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p, _i32,
                                           _p]),
 }

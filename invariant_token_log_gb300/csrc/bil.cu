@@ -224,16 +224,17 @@ struct Group {
       return pk(lo, hi);
     }
   }
-  // a[k] holds the slot accumulators (a_2k, a_2k+1) of exp(z - shift); with
-  // ENT, u[k] those of exp(z - shift) * (z - shift)
+  // a[k] holds the slot accumulators (a_2k, a_2k+1) of exp(d); with ENT,
+  // u[k] those of exp(d) * d; d = x - shift, times rcp when SCALED (the
+  // multiply comes last: no packed multiply here ever feeds an add, so the
+  // code generator has nothing to contract into a fused multiply-add)
   template <bool SCALED, bool ENT>
   __device__ static __forceinline__ void sum_acc(uint64_t (&a)[4], uint64_t (&u)[4], const uint32_t (&w)[kW],
                                                  uint64_t shift2, uint64_t rcp2) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      uint64_t z = xpair(w, k);
-      if (SCALED) z = mul2(z, rcp2);
-      const uint64_t d = sub2(z, shift2);
+      uint64_t d = sub2(xpair(w, k), shift2);
+      if (SCALED) d = mul2(d, rcp2);
       const uint64_t e = exp2_pair(d);
       a[k] = add2(a[k], e);
       // p log p -> 0 as p -> 0: an element with z = -inf (or one masked past
@@ -259,12 +260,15 @@ __device__ __forceinline__ int lane_groups(int valid, int lane) {
 //     increasing order; `valid` elements exist (the rest are past the
 //     vocabulary and do not take part);
 //   * max: exact, so its order does not matter (NaN never wins); it is taken
-//     on the stored values and then scaled, which equals the max of the
-//     scaled values because x -> x * rcp (rcp > 0) rounds monotonically;
-//   * sums: lane accumulator a_j (slot j) adds exp(z - m) for its groups in
-//     increasing order; the lane's sum is ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7));
-//     the warp's sum is the butterfly over lanes (xor 16, 8, 4, 2, 1); the
-//     entropy sum u follows the same tree with u_j = fma(e, z - m, u_j);
+//     on the stored values, m_x, and the partial's max is m = m_x * rcp
+//     (the max of the scaled values, since x -> x * rcp (rcp > 0) rounds
+//     monotonically);
+//   * sums: d = (x - m_x) * rcp, each operation rounded (rcp = 1: d = x - m_x),
+//     which is z - m in real arithmetic; lane accumulator a_j (slot j) adds
+//     exp(d) for its groups in increasing order; the lane's sum is
+//     ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)); the warp's sum is the butterfly
+//     over lanes (xor 16, 8, 4, 2, 1); the entropy sum u follows the same
+//     tree with u_j = fma(exp(d), d, u_j);
 //   * a tile whose max is -inf shifts by 0 instead, so it sums to 0 (or NaN
 //     if it holds a NaN) and its max stays -inf.
 // Nothing here depends on the row, the kernel or the launch geometry.  Two
@@ -323,9 +327,9 @@ __device__ __forceinline__ TilePartial tile_reduce_regs_t(const TileRegs<DT>& r,
 #pragma unroll
   for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i)
     if (FULL || i < ng) Group<DT>::max_acc(mx, r.w[i]);
-  float m = warp_max(Group<DT>::max_fin(mx));
-  if (SCALED) m = __fmul_rn(m, rcp);
-  const float shift = (m == -INFINITY) ? 0.0f : m;
+  const float mx_all = warp_max(Group<DT>::max_fin(mx));
+  const float m = SCALED ? __fmul_rn(mx_all, rcp) : mx_all;
+  const float shift = (mx_all == -INFINITY) ? 0.0f : mx_all;  // in stored units
   const uint64_t shift2 = pk(shift, shift), rcp2 = pk(rcp, rcp);
   uint64_t a[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -367,9 +371,9 @@ __device__ __forceinline__ TilePartial tile_reduce_smem_t(const unsigned char* t
     if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
     Group<DT>::max_acc(mx, w);
   }
-  float m = warp_max(Group<DT>::max_fin(mx));
-  if (SCALED) m = __fmul_rn(m, rcp);
-  const float shift = (m == -INFINITY) ? 0.0f : m;
+  const float mx_all = warp_max(Group<DT>::max_fin(mx));
+  const float m = SCALED ? __fmul_rn(mx_all, rcp) : mx_all;
+  const float shift = (mx_all == -INFINITY) ? 0.0f : mx_all;  // in stored units
   const uint64_t shift2 = pk(shift, shift), rcp2 = pk(rcp, rcp);
   uint64_t a[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
   for (int g = lane; g < groups; g += kLanes) {
@@ -956,30 +960,6 @@ struct Out<BIL_F16> {
   }
 };
 
-// What one row of the backward needs: its target, saved LSE, the upstream
-// gradients of logp (g) and of the entropy (gh, with the row's entropy H),
-// and the temperature's reciprocal.
-struct RowMeta {
-  int64_t target;
-  float lse, g, H, gh;
-};
-
-// One element of the gradient, exactly as the formula reads:
-//   z = x * rcp;  a = z - lse;  p = exp(a);  d = g * (onehot - p)
-//   with entropy:  d = d - gh * (p * (a + H))      (d H / d z = -p (log p + H))
-//   with a temperature:  d = d * rcp                (d z / d x = rcp)
-__device__ __forceinline__ float grad_elem(float x, const RowMeta& m, bool is_target, float rcp, bool ent) {
-  const bool scaled = rcp != 1.0f;
-  const float z = scaled ? __fmul_rn(x, rcp) : x;
-  const float a = __fsub_rn(z, m.lse);
-  const float p = contract_exp(a);
-  float d = __fmul_rn(m.g, __fsub_rn(is_target ? 1.0f : 0.0f, p));
-  // p (log p + H) -> 0 as p -> 0: a clamped to the largest finite magnitude
-  // makes the term of an -inf logit 0 instead of 0 * inf
-  if (ent) d = __fsub_rn(d, __fmul_rn(m.gh, __fmul_rn(p, __fadd_rn(fmaxf(a, kNegMax), m.H))));
-  return scaled ? __fmul_rn(d, rcp) : d;
-}
-
 // A group of 8 gradient elements from its stored logits, with the same
 // operations as grad_elem in packed pairs.  `jt` is the target's slot in the
 // group, or -1 when the target lies elsewhere.
@@ -987,18 +967,22 @@ template <int DT>
 __device__ __forceinline__ void grad_group(const uint32_t (&w)[Group<DT>::kW], const RowMeta& m, float rcp, bool ent,
                                            int jt, float (&y)[kGroup]) {
   const bool scaled = rcp != 1.0f;
-  const uint64_t L2 = pk(m.lse, m.lse), g2 = pk(m.g, m.g), rcp2 = pk(rcp, rcp);
+  const uint64_t L2 = pk(m.lse, m.lse), nL2 = pk(-m.lse, -m.lse), g2 = pk(m.g, m.g), rcp2 = pk(rcp, rcp);
   const uint64_t gh2 = pk(m.gh, m.gh), H2 = pk(m.H, m.H);
+  constexpr uint64_t kSigns = 0x8000000080000000ull;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    uint64_t z = Group<DT>::xpair(w, k);
-    if (scaled) z = mul2(z, rcp2);
-    const uint64_t a = sub2(z, L2);
+    const uint64_t x = Group<DT>::xpair(w, k);
+    const uint64_t a = scaled ? fma2(x, rcp2, nL2) : sub2(x, L2);
     const uint64_t p = exp2_pair(a);                  // (p_2k, p_2k+1)
-    uint64_t d = mul2(g2, sub2(0, p));                // g * (0 - p)
+    uint64_t d;
+    uint64_t t3 = 0;
     if (ent) {
       const uint64_t ac = pk(fmaxf(lo_of(a), kNegMax), fmaxf(hi_of(a), kNegMax));
-      d = sub2(d, mul2(gh2, mul2(p, add2(ac, H2))));
+      t3 = mul2(gh2, mul2(p, add2(ac, H2)));
+      d = fma2(g2, sub2(0, p), t3 ^ kSigns);          // g * (0 - p) - t3, one rounding
+    } else {
+      d = mul2(g2, sub2(0, p));                       // g * (0 - p)
     }
     if (scaled) d = mul2(d, rcp2);
     y[2 * k] = lo_of(d);
@@ -1008,9 +992,8 @@ __device__ __forceinline__ void grad_group(const uint32_t (&w)[Group<DT>::kW], c
       for (int h = 0; h < 2; ++h) {
         if (jt == 2 * k + h) {
           const float ph = h ? hi_of(p) : lo_of(p);
-          const float ah = h ? hi_of(a) : lo_of(a);
-          float dt = __fmul_rn(m.g, __fsub_rn(1.0f, ph));
-          if (ent) dt = __fsub_rn(dt, __fmul_rn(m.gh, __fmul_rn(ph, __fadd_rn(fmaxf(ah, kNegMax), m.H))));
+          const float th = h ? hi_of(t3) : lo_of(t3);
+          const float dt = ent ? __fmaf_rn(m.g, __fsub_rn(1.0f, ph), -th) : __fmul_rn(m.g, __fsub_rn(1.0f, ph));
           y[2 * k + h] = scaled ? __fmul_rn(dt, rcp) : dt;
         }
       }
@@ -1329,19 +1312,22 @@ int device_limits(int* sms, int* max_smem_optin) {
 extern "C" {
 
 const char* bil_contract_id(void) {
-  return "bil.v2"
+  return "bil.v3"
          ";tile=fixed tile_v columns, valid columns < vocab"
-         ";z=x*rn rcp, rcp=float32(1/temperature) (rcp=1: z=x)"
+         ";rcp=float32(1/temperature) (rcp=1: no multiply)"
          ";lanes=32x8: lane l takes 8-element groups l, l+32, ... in order"
-         ";max=exact, on x, then *rn rcp"
-         ";exp(a)=ex2.approx.ftz.f32(a*rn log2e), a=z-rn m"
+         ";max=exact, on x: m_x; m_t=m_x*rn rcp"
+         ";exp(d)=ex2.approx.ftz.f32(d*rn log2e), d=(x-rn m_x)*rn rcp"
          ";lane_sum=8 slot accumulators, ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))"
          ";warp_sum=butterfly xor 16,8,4,2,1"
-         ";entropy_sum=u_j=fma(e,max(a,-FLT_MAX),u_j), same trees"
+         ";entropy_sum=u_j=fma(e,max(d,-FLT_MAX),u_j), same trees"
          ";merge=M=max m_t; w_t=exp(m_t-M); S=fma(s_t,w_t,S) t=0..T-1; LSE=M+rn logf(S)"
          ";merge_entropy=U=fma(fma(max(m_t-M,-FLT_MAX),s_t,u_t),w_t,U); H=logf(S)-rn(U/rn S)"
-         ";logp=z_t-rn LSE"
-         ";bwd=a=z-lse; p=exp(a); d=g*(onehot-p) [-gh*(p*(max(a,-FLT_MAX)+H))] [*rcp], store rn";
+         ";logp=z_t-rn LSE, z_t=x_t*rn rcp"
+         ";bwd=a=fma(x,rcp,-lse) (rcp=1: x-rn lse); p=exp(a); d=g*(onehot-p), with entropy"
+         " d=fma(g,onehot-p,-(gh*(p*(max(a,-FLT_MAX)+H)))); [*rcp]; store rn"
+         ";linear=z=fp32 tcgen05 sum over K blocks of 64 in order; tile 256, one thread per row,"
+         " 8 slots over columns 8g+j, g in order, ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))";
 }
 
 const char* bil_status_string(int status) {

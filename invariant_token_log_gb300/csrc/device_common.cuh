@@ -25,6 +25,40 @@ __device__ __forceinline__ float ex2_approx(float a) {
 // exponential (flushes results below 2^-126 to zero).
 __device__ __forceinline__ float contract_exp(float a) { return ex2_approx(__fmul_rn(a, kLog2e)); }
 
+// What one row of the backward needs: its target, saved LSE, the upstream
+// gradients of logp (g) and of the entropy (gh, with the row's entropy H),
+// and the temperature's reciprocal.
+struct RowMeta {
+  int64_t target;
+  float lse, g, H, gh;
+};
+
+// One element of the gradient:
+//   a = x * rcp - lse (one fused multiply-add; rcp = 1: x - lse);  p = exp(a)
+//   d = g * (onehot - p)
+//   with entropy:  d = g * (onehot - p) - gh * (p * (a + H)), the product with
+//                  g and the subtraction fused (d H / d z = -p (log p + H))
+//   with a temperature:  d = d * rcp                (d z / d x = rcp)
+// Every multiply whose result meets an add is an explicit fused multiply-add,
+// in this scalar form and in the packed pairs of the vectorised kernels, so
+// both produce the same bits whatever the code generator contracts.
+__device__ __forceinline__ float grad_elem(float x, const RowMeta& m, bool is_target, float rcp, bool ent) {
+  const bool scaled = rcp != 1.0f;
+  const float a = scaled ? __fmaf_rn(x, rcp, -m.lse) : __fsub_rn(x, m.lse);
+  const float p = contract_exp(a);
+  const float om = __fsub_rn(is_target ? 1.0f : 0.0f, p);
+  float d;
+  if (ent) {
+    // p (log p + H) -> 0 as p -> 0: a clamped to the largest finite magnitude
+    // makes the term of an -inf logit 0 instead of 0 * inf
+    const float t3 = __fmul_rn(m.gh, __fmul_rn(p, __fadd_rn(fmaxf(a, kNegMax), m.H)));
+    d = __fmaf_rn(m.g, om, -t3);
+  } else {
+    d = __fmul_rn(m.g, om);
+  }
+  return scaled ? __fmul_rn(d, rcp) : d;
+}
+
 // ---------------------------------------------------------------------------
 // mbarriers and bounded waits.  Every wait polls with a time limit; one that
 // runs out records a bit in the caller's watchdog word and reports failure,

@@ -79,9 +79,16 @@ struct alignas(8) LinearSmem {
 
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * size_t(kStageBytes) + sizeof(LinearSmem);
 
+// What the epilogue warps do with a finished accumulator tile.
+enum EpilogueMode {
+  kModePartials = 0,  // the operator's tile partials (and, optionally, the logits)
+  kModeGrad = 1,      // dZ = d(g logp + gh H)/dz, stored as 16-bit in [rows, vocab] and [vocab, rows]
+  kModeStore = 2,     // C = A . B^T stored as it is (float32, or rounded to 16 bits)
+};
+
 struct LinearParams {
-  int64_t n_rows;
-  int64_t shard_cols;   // weight rows (vocabulary columns) of the shard
+  int64_t n_rows;       // rows of A (valid output rows)
+  int64_t shard_cols;   // rows of B (valid output columns): weight rows of the shard in the forward
   int tile_begin;       // global tile index of the shard's first column
   int num_n;            // tiles of the shard
   int num_m;            // row tiles
@@ -98,6 +105,21 @@ struct LinearParams {
   int logits_dtype;
   int64_t ld_logits;
   uint32_t idesc;
+  int m_group;          // row tiles per raster group
+  // kModeGrad
+  const float* lse;
+  const float* grad_logp;
+  const float* entropy;        // with grad_entropy: the forward's entropy
+  const float* grad_entropy;   // NULL: no entropy term
+  int64_t vocab;               // targets outside [0, vocab) give NaN rows
+  unsigned char* dz;           // [n_rows, ld_dz] 16-bit
+  int64_t ld_dz;
+  unsigned char* dz_t;         // [shard_cols, ld_dz_t] 16-bit
+  int64_t ld_dz_t;
+  // kModeStore
+  unsigned char* out;          // [n_rows, ld_out]
+  int out_dtype;
+  int64_t ld_out;
 };
 
 // ---------------------------------------------------------------------------
@@ -172,26 +194,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[kChunk])
       : "memory");
 }
 
-// Row tile m and vocabulary tile n (shard-local) of work unit u: groups of
-// kMGroup row tiles; within a group the row tile varies fastest, so the
-// blocks working at one time share a few weight tiles through L2.
-__device__ __forceinline__ void unit_coords(int64_t u, int num_m, int num_n, int& m, int& n) {
-  const int64_t per_group = static_cast<int64_t>(kMGroup) * num_n;
+// Row tile m and column tile n of work unit u: groups of `group` row tiles;
+// within a group the row tile varies fastest, so the blocks working at one
+// time share a few B tiles (and their A tiles) through L2.
+__device__ __forceinline__ void unit_coords(int64_t u, int num_m, int num_n, int group, int& m, int& n) {
+  const int64_t per_group = static_cast<int64_t>(group) * num_n;
   const int g = static_cast<int>(u / per_group);
   const int r = static_cast<int>(u - g * per_group);
-  const int m0 = g * kMGroup;
-  const int gm = min(kMGroup, num_m - m0);
+  const int m0 = g * group;
+  const int gm = min(group, num_m - m0);
   n = r / gm;
   m = m0 + (r - n * gm);
 }
 
 // ---------------------------------------------------------------------------
 // The epilogue of one row of one tile: the tile partial of the operator, over
-// the tile's valid columns [0, vcols), from the float32 accumulator.
+// the tile's valid columns [0, vcols), from the float32 accumulator acc.
 //
-//   z_c = acc_c *rn rcp
-//   m   = max over valid c of z_c (exact)
-//   d_c = z_c -rn m (m = -inf: d_c = z_c), e_c = exp(d_c) of the contract
+//   m_acc = max over valid c of acc_c (exact);  m = m_acc *rn rcp
+//   d_c = (acc_c -rn m_acc) *rn rcp (m_acc = -inf: shift 0), e_c = exp(d_c)
+//   of the contract; the target logit is acc_t *rn rcp
 //   slot accumulators a_j, j = 0..7, take e_c for c = 8g + j, g = 0, 1, ...,
 //   31 in order; s = ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)); the entropy sum
 //   u = sum e_c * max(d_c, -FLT_MAX) in the same slots and tree (one fma per
@@ -206,16 +228,16 @@ __device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp
                                             unsigned char* out_row, int out_dtype, float& m_out, float& s_out,
                                             float& u_out, float& tl_out) {
   uint32_t r[kChunk];
-  float m = -INFINITY;
+  float mx = -INFINITY;  // max of the unscaled accumulator
   float tl = 0.0f;
 #pragma unroll 1
   for (int c0 = 0; c0 < kBN; c0 += kChunk) {
     tmem_ld32(taddr + c0, r);
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
-      const float z = __fmul_rn(__uint_as_float(r[j]), rcp);
-      if (c0 + j < vcols) m = fmaxf(m, z);
-      if (c0 + j == tloc) tl = z;
+      const float acc = __uint_as_float(r[j]);
+      if (c0 + j < vcols) mx = fmaxf(mx, acc);
+      if (c0 + j == tloc) tl = __fmul_rn(acc, rcp);
     }
     if (store && c0 < vcols) {
       if (out_dtype == BIL_F32) {
@@ -249,7 +271,8 @@ __device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp
       }
     }
   }
-  const float shift = (m == -INFINITY) ? 0.0f : m;
+  const float m = __fmul_rn(mx, rcp);
+  const float shift = (mx == -INFINITY) ? 0.0f : mx;
   float a[8], u[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -261,7 +284,7 @@ __device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp
     tmem_ld32(taddr + c0, r);
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
-      const float d = __fsub_rn(__fmul_rn(__uint_as_float(r[j]), rcp), shift);
+      const float d = __fmul_rn(__fsub_rn(__uint_as_float(r[j]), shift), rcp);
       float e = contract_exp(d);
       if (c0 + j >= vcols) e = 0.0f;  // columns past the vocabulary add nothing
       a[j % 8] = __fadd_rn(a[j % 8], e);
@@ -277,10 +300,97 @@ __device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp
   tl_out = tl;
 }
 
-template <bool ENT>
-__global__ void __launch_bounds__(kThreads, 1)
-    linear_partials_kernel(const __grid_constant__ CUtensorMap tmap_hidden,
-                           const __grid_constant__ CUtensorMap tmap_weight, const LinearParams p) {
+// float -> 16-bit storage, round to nearest even.
+template <int DT>
+__device__ __forceinline__ uint16_t to16(float v) {
+  if (DT == BIL_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+// 32 consecutive values of one row -> 16-bit elements at o[0..n), n <= 32:
+// four 16-byte stores when all 32 are in range.
+template <int DT>
+__device__ __forceinline__ void store_row16(uint16_t* o, const float (&v)[kChunk], int n) {
+  if (n >= kChunk) {
+    uint32_t pk[kChunk / 2];
+#pragma unroll
+    for (int j = 0; j < kChunk; j += 2)
+      pk[j / 2] = static_cast<uint32_t>(to16<DT>(v[j])) | (static_cast<uint32_t>(to16<DT>(v[j + 1])) << 16);
+#pragma unroll
+    for (int j = 0; j < kChunk / 2; j += 4)
+      *reinterpret_cast<uint4*>(o + 2 * j) = make_uint4(pk[j], pk[j + 1], pk[j + 2], pk[j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j)
+      if (j < n) o[j] = to16<DT>(v[j]);
+  }
+}
+
+// The gradient tile of one row: dZ[row, c] for the tile's columns, by the
+// library's backward formula (grad_elem) from the float32 accumulator, stored
+// rounded to 16 bits into dz (row-major) and dz_t (transposed; the 32 lanes of
+// a warp hold 32 consecutive rows, so each column is one 64-byte store).
+// Inactive rows are +0.0; an active row whose target is outside [0, vocab)
+// is NaN.
+template <bool ENT, int DT>
+__device__ __forceinline__ void row_grad(uint32_t taddr, int vcols, float rcp, int64_t tloc, bool valid, bool active,
+                                         bool bad_target, const RowMeta& meta, uint16_t* dz_row, uint16_t* dzt_col0,
+                                         int64_t ld_dz_t) {
+  uint32_t r[kChunk];
+  float d[kChunk];
+#pragma unroll 1
+  for (int c0 = 0; c0 < kBN; c0 += kChunk) {
+    tmem_ld32(taddr + c0, r);
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      float v = 0.0f;
+      if (active) v = grad_elem(__uint_as_float(r[j]), meta, c0 + j == tloc, rcp, ENT);
+      if (bad_target) v = __int_as_float(0x7fc00000);
+      d[j] = v;
+    }
+    if (valid && c0 < vcols) {
+      store_row16<DT>(dz_row + c0, d, vcols - c0);
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j)
+        if (c0 + j < vcols) dzt_col0[(c0 + j) * ld_dz_t] = to16<DT>(d[j]);
+    }
+  }
+}
+
+// One row of C = A . B^T as it is: float32, or rounded to 16 bits.
+template <int OT>
+__device__ __forceinline__ void row_store(uint32_t taddr, int vcols, bool valid, unsigned char* out_row) {
+  uint32_t r[kChunk];
+  float v[kChunk];
+#pragma unroll 1
+  for (int c0 = 0; c0 < kBN; c0 += kChunk) {
+    tmem_ld32(taddr + c0, r);
+    if (valid && c0 < vcols) {
+      if (OT == BIL_F32) {
+        float* o = reinterpret_cast<float*>(out_row) + c0;
+        if (c0 + kChunk <= vcols) {
+#pragma unroll
+          for (int j = 0; j < kChunk; j += 4)
+            *reinterpret_cast<uint4*>(o + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j)
+            if (c0 + j < vcols) o[j] = __uint_as_float(r[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) v[j] = __uint_as_float(r[j]);
+        store_row16<OT>(reinterpret_cast<uint16_t*>(out_row) + c0, v, vcols - c0);
+      }
+    }
+  }
+}
+
+// The GEMM C = A . B^T (A [rows, K], B [cols, K], both K-major 16-bit) with
+// one of the epilogues above.  See the file's head for the block structure.
+template <int MODE, bool ENT, int DT>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const CUtensorMap& tmap_weight,
+                                          const LinearParams& p) {
   extern __shared__ unsigned char smem_raw[];
   // Stage buffers start on a 1024-byte boundary (the 128-byte swizzle pattern
   // repeats every 8 rows = 1024 bytes).
@@ -324,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
         int m, n;
-        unit_coords(u, p.num_m, p.num_n, m, n);
+        unit_coords(u, p.num_m, p.num_n, p.m_group, m, n);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const int s = static_cast<int>(it % kStages);
           const unsigned ph = static_cast<unsigned>((it / kStages) & 1);
@@ -390,34 +500,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     int local = 0;
     for (int64_t u = blockIdx.x; u < total; u += gridDim.x, ++local) {
       int m, n;
-      unit_coords(u, p.num_m, p.num_n, m, n);
+      unit_coords(u, p.num_m, p.num_n, p.m_group, m, n);
       const int b = local & 1;
       const unsigned use = static_cast<unsigned>(local >> 1);
       const int64_t row = static_cast<int64_t>(m) * kBM + row_in_tile;
       const bool valid = row < p.n_rows;
-      const int64_t t = valid ? p.targets[row] : p.ignore_index;
-      const bool active = valid && t != p.ignore_index;
       const int64_t col0 = static_cast<int64_t>(n) * kBN;  // shard-local column of the tile's column 0
       const int vcols = static_cast<int>(p.shard_cols - col0 < kBN ? p.shard_cols - col0 : kBN);
-      const int64_t gcol0 = static_cast<int64_t>(p.tile_begin + n) * kBN;
-      const int64_t tloc = active ? t - gcol0 : -1;
-      if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
-      tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * kAccCols);
-      float mt, st, ut = 0.0f, tl;
-      const bool store = valid && p.logits != nullptr;
-      unsigned char* out_row =
-          store ? p.logits + (row * p.ld_logits + col0) * (p.logits_dtype == BIL_F32 ? 4 : 2) : nullptr;
-      row_partial<ENT>(taddr, vcols, p.rcp, tloc, store, out_row, p.logits_dtype, mt, st, ut, tl);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
-      if (valid) {
-        const int64_t at = row * p.ld_part + p.tile_begin + n;
-        p.part_max[at] = active ? mt : -INFINITY;
-        p.part_sum[at] = active ? st : 0.0f;
-        if (ENT) p.part_ent[at] = active ? ut : 0.0f;
-        if (tloc >= 0 && tloc < vcols) p.target_logit[row] = tl;
+      if constexpr (MODE == kModePartials) {
+        const int64_t t = valid ? p.targets[row] : p.ignore_index;
+        const bool active = valid && t != p.ignore_index;
+        const int64_t gcol0 = static_cast<int64_t>(p.tile_begin + n) * kBN;
+        const int64_t tloc = active ? t - gcol0 : -1;
+        if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
+        tc_fence_after();
+        float mt, st, ut = 0.0f, tl;
+        const bool store = valid && p.logits != nullptr;
+        unsigned char* out_row =
+            store ? p.logits + (row * p.ld_logits + col0) * (p.logits_dtype == BIL_F32 ? 4 : 2) : nullptr;
+        row_partial<ENT>(taddr, vcols, p.rcp, tloc, store, out_row, p.logits_dtype, mt, st, ut, tl);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+        if (valid) {
+          const int64_t at = row * p.ld_part + p.tile_begin + n;
+          p.part_max[at] = active ? mt : -INFINITY;
+          p.part_sum[at] = active ? st : 0.0f;
+          if (ENT) p.part_ent[at] = active ? ut : 0.0f;
+          if (tloc >= 0 && tloc < vcols) p.target_logit[row] = tl;
+        }
+      } else if constexpr (MODE == kModeGrad) {
+        RowMeta meta{p.ignore_index, 0.0f, 0.0f, 0.0f, 0.0f};
+        if (valid) {
+          meta.target = p.targets[row];
+          meta.lse = p.lse[row];
+          meta.g = p.grad_logp[row];
+          if (ENT) {
+            meta.H = p.entropy[row];
+            meta.gh = p.grad_entropy[row];
+          }
+        }
+        const bool active = valid && meta.target != p.ignore_index;
+        const bool bad_target = active && (meta.target < 0 || meta.target >= p.vocab);
+        const int64_t gcol0 = static_cast<int64_t>(p.tile_begin + n) * kBN;
+        const int64_t tloc = active ? meta.target - gcol0 : -1;
+        if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
+        tc_fence_after();
+        uint16_t* dz_row = valid ? reinterpret_cast<uint16_t*>(p.dz) + row * p.ld_dz + col0 : nullptr;
+        uint16_t* dzt_col0 = valid ? reinterpret_cast<uint16_t*>(p.dz_t) + col0 * p.ld_dz_t + row : nullptr;
+        row_grad<ENT, DT>(taddr, vcols, p.rcp, tloc, valid, active, bad_target, meta, dz_row, dzt_col0, p.ld_dz_t);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+      } else {
+        if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
+        tc_fence_after();
+        const int eb = DT == BIL_F32 ? 4 : 2;
+        unsigned char* out_row = valid ? p.out + (row * p.ld_out + col0) * eb : nullptr;
+        row_store<DT>(taddr, vcols, valid, out_row);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
       }
     }
   }
@@ -429,6 +573,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                  : "memory");
+  }
+}
+
+// Forward: the tile partials of hidden . weight^T.
+template <bool ENT>
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_partials_kernel(const __grid_constant__ CUtensorMap tmap_hidden,
+                           const __grid_constant__ CUtensorMap tmap_weight, const LinearParams p) {
+  gemm_body<kModePartials, ENT, 0>(tmap_hidden, tmap_weight, p);
+}
+
+// Backward, first pass: hidden . weight^T recomputed, dZ stored (16-bit DT).
+template <bool ENT, int DT>
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_grad_kernel(const __grid_constant__ CUtensorMap tmap_hidden, const __grid_constant__ CUtensorMap tmap_weight,
+                       const LinearParams p) {
+  gemm_body<kModeGrad, ENT, DT>(tmap_hidden, tmap_weight, p);
+}
+
+// Backward, the two contractions of dZ: C = A . B^T stored as OT.
+template <int OT>
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_store_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                        const LinearParams p) {
+  gemm_body<kModeStore, false, OT>(tmap_a, tmap_b, p);
+}
+
+// Out-of-place transpose of a [rows, cols] matrix of 16-bit elements
+// (dst[c, r] = src[r, c]) through a 64 x 64 shared-memory tile; consecutive
+// threads read consecutive elements of a source row and write consecutive
+// elements of a destination row.
+__global__ void __launch_bounds__(256) transpose16_kernel(const uint16_t* __restrict__ src, int64_t rows,
+                                                          int64_t cols, int64_t ld_src, uint16_t* __restrict__ dst,
+                                                          int64_t ld_dst) {
+  __shared__ uint16_t tile[64][66];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
+  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
+    const int r = i / 64, c = i % 64;
+    if (r0 + r < rows && c0 + c < cols) tile[r][c] = src[(r0 + r) * ld_src + c0 + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
+    const int c = i / 64, r = i % 64;
+    if (r0 + r < rows && c0 + c < cols) dst[(c0 + c) * ld_dst + r0 + r] = tile[r][c];
   }
 }
 
@@ -476,12 +664,14 @@ int make_map(CUtensorMap* map, const void* ptr, int dtype, int64_t rows, int64_t
 
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-template <bool ENT>
-int launch_linear(const CUtensorMap& mh, const CUtensorMap& mw, const LinearParams& p, cudaStream_t stream) {
+typedef void (*GemmKernel)(CUtensorMap, CUtensorMap, LinearParams);
+
+// One persistent block per SM (at most one per work unit).
+int launch_gemm(GemmKernel kernel, const CUtensorMap& mh, const CUtensorMap& mw, const LinearParams& p,
+                cudaStream_t stream) {
   int sms = 0, smem_optin = 0;
   if (int st = bil_internal::device_limits(&sms, &smem_optin)) return st;
   if (static_cast<size_t>(smem_optin) < kSmemBytes) return BIL_E_UNSUPPORTED;
-  auto kernel = linear_partials_kernel<ENT>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes)) !=
       cudaSuccess)
     return BIL_E_CUDA;
@@ -489,6 +679,30 @@ int launch_linear(const CUtensorMap& mh, const CUtensorMap& mw, const LinearPara
   const int grid = static_cast<int>(std::min<int64_t>(total, sms));
   kernel<<<grid, kThreads, kSmemBytes, stream>>>(mh, mw, p);
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
+}
+
+// Raster group for the store GEMMs: enough row tiles that one wave of blocks
+// covers every column tile of them (each A tile is then read from DRAM once).
+int store_group(int num_n) {
+  int sms = 0, smem = 0;
+  if (bil_internal::device_limits(&sms, &smem) != BIL_OK || sms <= 0) sms = 148;
+  return std::max(1, sms / std::max(1, num_n));
+}
+
+int launch_transpose16(const void* src, int64_t rows, int64_t cols, int64_t ld_src, void* dst, int64_t ld_dst,
+                       cudaStream_t stream) {
+  const int64_t gx = (cols + 63) / 64, gy = (rows + 63) / 64;
+  if (gx > INT32_MAX || gy > 65535) return BIL_E_UNSUPPORTED;
+  if (rows == 0 || cols == 0) return BIL_OK;
+  transpose16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(src), rows, cols, ld_src, static_cast<uint16_t*>(dst), ld_dst);
+  return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
+}
+
+// A 16-byte aligned base and a row stride of a multiple of 16 bytes (what TMA
+// and the epilogues' vector stores need).
+bool rows16(const void* p, int64_t ld, int64_t elem_bytes) {
+  return aligned_to(p, 16) && (ld * elem_bytes) % 16 == 0;
 }
 
 // Workspace layout of bil_linear_logp_fwd: part_max, part_sum[, part_ent]
@@ -608,8 +822,9 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
   p.logits_dtype = logits_dtype;
   p.ld_logits = ld_logits;
   p.idesc = make_idesc(dtype == BIL_BF16);
+  p.m_group = kMGroup;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return part_ent != nullptr ? launch_linear<true>(mh, mw, p, s) : launch_linear<false>(mh, mw, p, s);
+  return launch_gemm(part_ent != nullptr ? linear_partials_kernel<true> : linear_partials_kernel<false>, mh, mw, p, s);
 }
 
 int bil_linear_logp_workspace_bytes(int64_t n_rows, int64_t vocab, int entropy, int64_t* bytes) {
@@ -648,6 +863,138 @@ int bil_linear_logp_fwd(const void* hidden, const void* weight, int dtype, int64
     return st;
   return bil_logp_merge(pm, ps, pe, n_rows, static_cast<int32_t>(num_tiles), num_tiles, tl, target_ids,
                         ignore_index, vocab, logp, lse, entropy, 0, stream);
+}
+
+int bil_transpose_2d(const void* src, int dtype, int64_t rows, int64_t cols, int64_t ld_src, void* dst,
+                     int64_t ld_dst, bil_stream_t stream) {
+  if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
+  if (rows < 0 || cols < 0 || ld_src < cols || ld_dst < rows) return BIL_E_INVALID_ARG;
+  if (rows == 0 || cols == 0) return BIL_OK;
+  if (src == nullptr || dst == nullptr) return BIL_E_INVALID_ARG;
+  if (!aligned_to(src, 2) || !aligned_to(dst, 2)) return BIL_E_ALIGN;
+  return launch_transpose16(src, rows, cols, ld_src, dst, ld_dst, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weight_t, int dtype, int64_t n_rows,
+                        int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight, int64_t ld_weight_t,
+                        float temperature, const int64_t* target_ids, int64_t ignore_index, const float* lse,
+                        const float* grad_logp, const float* entropy, const float* grad_entropy, void* dz,
+                        int64_t ld_dz, void* dz_t, int64_t ld_dz_t, void* hidden_t, int64_t ld_hidden_t,
+                        void* dhidden, int dhidden_dtype, int64_t ld_dhidden, void* dweight, int dweight_dtype,
+                        int64_t ld_dweight, bil_stream_t stream) {
+  if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
+  for (int ot : {dhidden_dtype, dweight_dtype})
+    if (ot != BIL_F32 && ot != dtype) return BIL_E_DTYPE;
+  if (n_rows < 0 || hidden_size < 1 || vocab < 1 || ld_hidden < hidden_size || ld_weight < hidden_size ||
+      ld_weight_t < vocab || ld_dz < vocab || ld_dz_t < n_rows || ld_hidden_t < n_rows ||
+      ld_dhidden < hidden_size || ld_dweight < hidden_size)
+    return BIL_E_INVALID_ARG;
+  if ((entropy == nullptr) != (grad_entropy == nullptr)) return BIL_E_INVALID_ARG;
+  float rcp = 1.0f;
+  if (int st = bil_internal::temperature_rcp(temperature, &rcp)) return st;
+  if (weight == nullptr || weight_t == nullptr || dweight == nullptr) return BIL_E_INVALID_ARG;
+  const int64_t eo_h = dhidden_dtype == BIL_F32 ? 4 : 2, eo_w = dweight_dtype == BIL_F32 ? 4 : 2;
+  if (!rows16(weight, ld_weight, 2) || !rows16(weight_t, ld_weight_t, 2) || !rows16(dweight, ld_dweight, eo_w))
+    return BIL_E_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (n_rows == 0) {  // dweight is a sum over no rows
+    return cudaMemset2DAsync(dweight, static_cast<size_t>(ld_dweight * eo_w), 0,
+                             static_cast<size_t>(hidden_size * eo_w), static_cast<size_t>(vocab), s) == cudaSuccess
+               ? BIL_OK
+               : BIL_E_CUDA;
+  }
+  if (hidden == nullptr || target_ids == nullptr || lse == nullptr || grad_logp == nullptr || dz == nullptr ||
+      dz_t == nullptr || hidden_t == nullptr || dhidden == nullptr)
+    return BIL_E_INVALID_ARG;
+  if (!rows16(hidden, ld_hidden, 2) || !rows16(dz, ld_dz, 2) || !rows16(dz_t, ld_dz_t, 2) ||
+      !rows16(hidden_t, ld_hidden_t, 2) || !rows16(dhidden, ld_dhidden, eo_h))
+    return BIL_E_ALIGN;
+  if (!aligned_to(target_ids, 8) || !aligned_to(lse, 4) || !aligned_to(grad_logp, 4) ||
+      (entropy && (!aligned_to(entropy, 4) || !aligned_to(grad_entropy, 4))))
+    return BIL_E_ALIGN;
+  if (n_rows > INT32_MAX - kBM || vocab > INT32_MAX - kBN || hidden_size > INT32_MAX - kBN)
+    return BIL_E_UNSUPPORTED;
+  if ((n_rows + 63) / 64 > 65535) return BIL_E_UNSUPPORTED;  // the transpose's grid
+
+  // Every tensor map is encoded before anything is queued.
+  //   grad:     A = hidden [n, H],  B = weight [V, H]      (K = H)
+  //   dhidden:  A = dz [n, V],      B = weight^T [H, V]    (K = V)
+  //   dweight:  A = dz_t [V, n],    B = hidden^T [H, n]    (K = n)
+  CUtensorMap maps[6];
+  {
+    int st = make_map(&maps[0], hidden, dtype, n_rows, hidden_size, ld_hidden, kBM);
+    if (!st) st = make_map(&maps[1], weight, dtype, vocab, hidden_size, ld_weight, kBN);
+    if (!st) st = make_map(&maps[2], dz, dtype, n_rows, vocab, ld_dz, kBM);
+    if (!st) st = make_map(&maps[3], weight_t, dtype, hidden_size, vocab, ld_weight_t, kBN);
+    if (!st) st = make_map(&maps[4], dz_t, dtype, vocab, n_rows, ld_dz_t, kBM);
+    if (!st) st = make_map(&maps[5], hidden_t, dtype, hidden_size, n_rows, ld_hidden_t, kBN);
+    if (st) return st;
+  }
+
+  // 1. hidden^T [H, n_rows], the K-major B operand of dweight = dZ^T . hidden
+  if (int st = launch_transpose16(hidden, n_rows, hidden_size, ld_hidden, hidden_t, ld_hidden_t, s)) return st;
+
+  const uint32_t idesc = make_idesc(dtype == BIL_BF16);
+  // 2. dZ from the recomputed projection, stored as dz [n, V] and dz_t [V, n]
+  {
+    LinearParams p{};
+    p.n_rows = n_rows;
+    p.shard_cols = vocab;
+    p.tile_begin = 0;
+    p.num_n = static_cast<int>((vocab + kBN - 1) / kBN);
+    p.num_m = static_cast<int>((n_rows + kBM - 1) / kBM);
+    p.k_blocks = static_cast<int>((hidden_size + kBK - 1) / kBK);
+    p.targets = target_ids;
+    p.ignore_index = ignore_index;
+    p.rcp = rcp;
+    p.idesc = idesc;
+    p.m_group = kMGroup;
+    p.lse = lse;
+    p.grad_logp = grad_logp;
+    p.entropy = entropy;
+    p.grad_entropy = grad_entropy;
+    p.vocab = vocab;
+    p.dz = static_cast<unsigned char*>(dz);
+    p.ld_dz = ld_dz;
+    p.dz_t = static_cast<unsigned char*>(dz_t);
+    p.ld_dz_t = ld_dz_t;
+    const bool ent = entropy != nullptr;
+    GemmKernel k = dtype == BIL_BF16 ? (ent ? linear_grad_kernel<true, BIL_BF16> : linear_grad_kernel<false, BIL_BF16>)
+                                     : (ent ? linear_grad_kernel<true, BIL_F16> : linear_grad_kernel<false, BIL_F16>);
+    if (int st = launch_gemm(k, maps[0], maps[1], p, s)) return st;
+  }
+  // 3. dhidden = dZ . weight   (A = dz [n, V], B = weight^T [H, V], K = V)
+  // 4. dweight = dZ^T . hidden (A = dz_t [V, n], B = hidden^T [H, n], K = n)
+  struct Contraction {
+    const CUtensorMap* ma;
+    const CUtensorMap* mb;
+    int64_t a_rows, k;
+    void* out;
+    int out_dtype;
+    int64_t ld_out;
+  };
+  const Contraction cs[2] = {
+      {&maps[2], &maps[3], n_rows, vocab, dhidden, dhidden_dtype, ld_dhidden},
+      {&maps[4], &maps[5], vocab, n_rows, dweight, dweight_dtype, ld_dweight},
+  };
+  for (const Contraction& c : cs) {
+    LinearParams p{};
+    p.n_rows = c.a_rows;
+    p.shard_cols = hidden_size;
+    p.num_n = static_cast<int>((hidden_size + kBN - 1) / kBN);
+    p.num_m = static_cast<int>((c.a_rows + kBM - 1) / kBM);
+    p.k_blocks = static_cast<int>((c.k + kBK - 1) / kBK);
+    p.idesc = idesc;
+    p.m_group = store_group(p.num_n);
+    p.out = static_cast<unsigned char*>(c.out);
+    p.out_dtype = c.out_dtype;
+    p.ld_out = c.ld_out;
+    GemmKernel k = c.out_dtype == BIL_F32    ? linear_store_kernel<BIL_F32>
+                   : c.out_dtype == BIL_BF16 ? linear_store_kernel<BIL_BF16>
+                                             : linear_store_kernel<BIL_F16>;
+    if (int st = launch_gemm(k, *c.ma, *c.mb, p, s)) return st;
+  }
+  return BIL_OK;
 }
 
 int bil_linear_logp_fwd_static(const void* hidden, const void* weight, int dtype, int64_t n_rows,

@@ -138,3 +138,112 @@ def linear_logp(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torch.Te
     if return_logits:
         out.append(logits.reshape(*lead, vocab))
     return tuple(out)
+
+
+def _pad8(n: int) -> int:
+    return -(-n // 8) * 8
+
+
+def transpose(src: torch.Tensor) -> torch.Tensor:
+    """[rows, cols] -> [cols, rows] (16-bit types), in a buffer whose rows are
+    16-byte aligned (the result is a view of its first ``rows`` columns)."""
+    _need_cuda(src)
+    s2 = src if src.stride(-1) == 1 else src.contiguous()
+    rows, cols = s2.shape
+    out = torch.empty((cols, _pad8(max(rows, 1))), dtype=s2.dtype, device=s2.device)[:, :rows]
+    _lib.check("bil_transpose_2d", _lib.load().bil_transpose_2d(
+        _ptr(s2), _in_code(s2.dtype), rows, cols, _ld(s2) if rows else cols, _ptr(out), out.stride(0),
+        _stream(s2.device)))
+    return out
+
+
+_WEIGHT_T: dict = {}
+
+
+def prepared_weight_t(weight: torch.Tensor) -> torch.Tensor:
+    """The transposed LM-head weight the backward contracts with, kept while the
+    weight is unchanged (keyed by storage, shape and the tensor's version counter:
+    an in-place update of the weight prepares it again)."""
+    key = (weight.data_ptr(), tuple(weight.shape), weight.dtype, weight.device, weight._version)
+    wt = _WEIGHT_T.get("entry")
+    if wt is not None and wt[0] == key:
+        return wt[1]
+    out = transpose(weight)
+    _WEIGHT_T["entry"] = (key, out)
+    return out
+
+
+def linear_logp_bwd(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor,
+                    grad_logp: torch.Tensor, ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                    entropy: torch.Tensor | None = None, grad_entropy: torch.Tensor | None = None,
+                    weight_t: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                    return_dz: bool = False):
+    """(dhidden [*lead, H], dweight [V, H][, dZ [N, V]]) of g * logp (+ gh * entropy).
+
+    ``out_dtype`` is float32 or the inputs' type (the default)."""
+    _need_cuda(hidden, weight, target_ids, lse, grad_logp, entropy, grad_entropy, weight_t)
+    lead = hidden.shape[:-1]
+    h2, w2 = _matrix(hidden, "hidden"), _matrix(weight, "weight")
+    if h2.dtype != w2.dtype or h2.shape[1] != w2.shape[1]:
+        raise ValueError("hidden and weight must share the element type and the hidden size")
+    n, hs = h2.shape
+    v = w2.shape[0]
+    dev = h2.device
+    t = target_ids.reshape(-1).to(torch.int64).contiguous()
+    if (entropy is None) != (grad_entropy is None):
+        raise ValueError("entropy and grad_entropy come together")
+    f32 = [x.reshape(-1).float().contiguous() if x is not None else None
+           for x in (lse, grad_logp, entropy, grad_entropy)]
+    wt = prepared_weight_t(w2) if weight_t is None else weight_t
+    out_dtype = h2.dtype if out_dtype is None else out_dtype
+    if out_dtype not in (torch.float32, h2.dtype):
+        raise TypeError("out_dtype must be float32 or the inputs' type")
+    dz = torch.empty((n, _pad8(v)), dtype=h2.dtype, device=dev)[:, :v]
+    dz_t = torch.empty((v, _pad8(max(n, 1))), dtype=h2.dtype, device=dev)[:, :n]
+    h_t = torch.empty((hs, _pad8(max(n, 1))), dtype=h2.dtype, device=dev)[:, :n]
+    dh = torch.empty((n, _pad8(hs)), dtype=out_dtype, device=dev)[:, :hs]
+    dw = torch.empty((v, _pad8(hs)), dtype=out_dtype, device=dev)[:, :hs]
+    oc = _lib.F32 if out_dtype == torch.float32 else _in_code(out_dtype)
+    _lib.check("bil_linear_logp_bwd", _lib.load().bil_linear_logp_bwd(
+        _ptr(h2), _ptr(w2), _ptr(wt), _in_code(h2.dtype), n, hs, _ld(h2), v, _ld(w2), wt.stride(0),
+        float(temperature), _ptr(t), ignore_index, _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), _ptr(f32[3]),
+        _ptr(dz), dz.stride(0), _ptr(dz_t), dz_t.stride(0), _ptr(h_t), h_t.stride(0),
+        _ptr(dh), oc, dh.stride(0), _ptr(dw), oc, dw.stride(0), _stream(dev)))
+    out = (dh.reshape(*lead, hs), dw)
+    return out + (dz,) if return_dz else out
+
+
+class LinearLogp(torch.autograd.Function):
+    """Fused LM-head + logp with the autograd actor path: the forward keeps only
+    lse (and the entropy); the backward recomputes the projection tiles."""
+
+    @staticmethod
+    def forward(ctx, hidden, weight, target_ids, ignore_index, temperature, return_entropy):
+        res = linear_logp(hidden, weight, target_ids, ignore_index, temperature, return_entropy)
+        ctx.save_for_backward(hidden, weight, target_ids, *res[1:])
+        ctx.ignore_index, ctx.temperature, ctx.return_entropy = ignore_index, temperature, return_entropy
+        ctx.mark_non_differentiable(res[1])
+        return res
+
+    @staticmethod
+    def backward(ctx, grad_logp, grad_lse, *rest):
+        hidden, weight, target_ids, lse, *ent = ctx.saved_tensors
+        g = torch.zeros_like(lse) if grad_logp is None else grad_logp
+        entropy = grad_entropy = None
+        if ctx.return_entropy and rest and rest[0] is not None:
+            entropy, grad_entropy = ent[0], rest[0]
+        need_h, need_w = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        if not (need_h or need_w):
+            return None, None, None, None, None, None
+        dh, dw = linear_logp_bwd(hidden, weight, target_ids, lse, g, ctx.ignore_index, ctx.temperature,
+                                 entropy, grad_entropy)
+        return dh if need_h else None, dw if need_w else None, None, None, None, None
+
+
+def batch_invariant_linear_logp(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torch.Tensor,
+                                ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                                return_entropy: bool = False):
+    """Differentiable fused LM-head + logp: logp (and the entropy when asked) with
+    gradients for hidden and weight."""
+    res = LinearLogp.apply(hidden, weight, target_ids, ignore_index, temperature, return_entropy)
+    return (res[0], res[2]) if return_entropy else res[0]

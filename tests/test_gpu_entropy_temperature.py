@@ -178,3 +178,36 @@ def test_entropy_with_negative_infinite_logits():
     ww = wl.Workload("neginf", x, "float32", v, tile, t)
     tol = oracle_grad_bound(ww, 1.0, np.ones(n), np.ones(n))
     assert_close_elementwise(d.cpu().numpy(), ref, tol, "dlogits")
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+@pytest.mark.parametrize("temperature", [1.0, 0.7])
+def test_unaligned_rows_same_bits_with_temperature_and_entropy(dtype, temperature):
+    """Rows one element past a 16-byte boundary take the element-by-element
+    paths (forward copy, scalar backward); aligned rows the packed vector
+    paths.  With a temperature and the entropy term, every output bit must
+    still agree: the packed and scalar forms perform the same rounded and
+    fused operations."""
+    n, v = 9, 9000
+    w = wl.random_rows(seed=44, n_rows=n, vocab=v, ld=v + 8, dtype=dtype, tile_v=1024, ignore_every=4)
+    flat = device_logits(w.logits, dtype).reshape(-1)
+    big = torch.empty(flat.numel() + 8, dtype=flat.dtype, device="cuda")
+    big[1:1 + flat.numel()] = flat
+    x_odd = big[1:1 + flat.numel()].view(n, v + 8)
+    x = flat.view(n, v + 8)
+    assert x_odd.data_ptr() % 16 != 0 and x.data_ptr() % 16 == 0
+    t = torch.from_numpy(w.target_ids).cuda()
+    g = torch.from_numpy(w.grad_logp).cuda()
+    gh = torch.from_numpy(wl.rng(44, 7).standard_normal(n).astype(np.float32)).cuda()
+    a = bil.logp_fwd(x, t, w.ignore_index, 1024, vocab=v, temperature=temperature, return_entropy=True)
+    b = bil.logp_fwd(x_odd, t, w.ignore_index, 1024, vocab=v, temperature=temperature, return_entropy=True)
+    for p, q in zip(a, b):
+        assert np.array_equal(f32_bits(p), f32_bits(q))
+    for od in (torch.float32, torch.bfloat16):
+        da = bil.logp_bwd(x, t, a[1], g, w.ignore_index, vocab=v, temperature=temperature, entropy=a[2],
+                          grad_entropy=gh, dlogits_dtype=od)
+        db = bil.logp_bwd(x_odd, t, a[1], g, w.ignore_index, vocab=v, temperature=temperature, entropy=a[2],
+                          grad_entropy=gh, dlogits_dtype=od)
+        torch.cuda.synchronize()
+        assert torch.equal(da.view(torch.int16 if od == torch.bfloat16 else torch.int32),
+                           db.view(torch.int16 if od == torch.bfloat16 else torch.int32)), od
