@@ -21,8 +21,10 @@ same workload.  ``--impl reference`` times the CPU oracle alone (rank 0).
 ``--workload linear`` measures the fused LM-head + logp instead: hidden
 [16384, 4096] bf16 times a Qwen3-8B-shaped LM head [151936, 4096] bf16, with
 the tile partials taken from the tensor-core accumulator and the fixed-order
-merge (forward only).  Its roofline is the partials kernel against the
-measured dense bf16 tensor throughput.
+merge, then the backward (dZ from the recomputed projection, dhidden and
+dweight): four tensor-core GEMMs of 2*N*H*V flops each per step.  Its
+roofline is the forward partials kernel against the measured dense bf16
+tensor throughput; the backward is reported as a whole.
 """
 from __future__ import annotations
 
@@ -49,12 +51,14 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "bil.cu")
 LINEAR_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "linear.cu")
-LINEAR_METRIC = "fused LM-head + logp forward rows/s and achieved TFLOP/s (% of GB300 dense bf16) at H=4096, V=151936"
+LINEAR_METRIC = ("fused LM-head + logp fwd+bwd rows/s and achieved TFLOP/s (% of GB300 dense bf16) at H=4096, "
+                 "V=151936")
 LINEAR_WORKLOAD = ("linear: N=16384 rows (B=8 x T=2048) of bf16 hidden states ~ randn, H=4096, LM-head weight "
-                   "[151936, 4096] bf16 ~ randn*3/64 (Qwen3-8B shape), uniform targets, 5% rows ignored; "
-                   "forward logp + lse, 256-column vocabulary tiles")
-LINEAR_CPU_ROWS = 32
-LINEAR_REFERENCE_ROWS = 16
+                   "[151936, 4096] bf16 ~ randn*3/64 (Qwen3-8B shape), uniform targets, 5% rows ignored, "
+                   "g ~ N(0,1); forward logp + lse (256-column vocabulary tiles), then the backward: dhidden and "
+                   "dweight in bf16 from the recomputed projection")
+LINEAR_CPU_ROWS = 8
+LINEAR_REFERENCE_ROWS = 8
 FALLBACK_BF16_TFLOPS = 1900.0
 REFERENCE_ROWS_PER_STEP = 256
 CPU_BASELINE_ROWS = 8192
@@ -420,16 +424,23 @@ def run_bil(args):
 # the fused LM-head + logp
 # ---------------------------------------------------------------------------
 
+def _linear_oracle_step(x, w, t, g):
+    import oracle
+    oracle.linear_logp_fwd(x, w, "bfloat16", t)
+    oracle.linear_logp_bwd(x, w, "bfloat16", t, g)
+
+
 def oracle_linear_rows_per_s(rows: int):
-    """Time the CPU oracle's LM-head projection + forward over `rows` rows."""
+    """Time the CPU oracle's LM-head projection, forward and backward over `rows` rows."""
     import oracle
     import workloads as wl
     oracle.build()
     x = wl.linear_hidden(rows)
     w = wl.linear_weight()
     t = wl.rng(wl.SEEDS["linear"], 1).integers(0, w.shape[0], rows, dtype=np.int64)
+    g = wl.rng(wl.SEEDS["linear"], 5).standard_normal(rows)
     t0 = time.perf_counter()
-    oracle.linear_logp_fwd(x, w, "bfloat16", t)
+    _linear_oracle_step(x, w, t, g)
     dt = time.perf_counter() - t0
     return rows / dt, dt, oracle.num_threads()
 
@@ -445,11 +456,12 @@ def run_linear_reference(args):
     x = wl.linear_hidden(rows)
     w = wl.linear_weight()
     t = wl.rng(wl.SEEDS["linear"], 1).integers(0, w.shape[0], rows, dtype=np.int64)
+    g = wl.rng(wl.SEEDS["linear"], 5).standard_normal(rows)
     for _ in range(args.warmup):
-        oracle.linear_logp_fwd(x, w, "bfloat16", t)
+        _linear_oracle_step(x, w, t, g)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.linear_logp_fwd(x, w, "bfloat16", t)
+        _linear_oracle_step(x, w, t, g)
     dt = time.perf_counter() - t0
     value = rows * args.steps / dt
     print(json.dumps({
@@ -459,7 +471,8 @@ def run_linear_reference(args):
         "data": "synthetic (seeded, host-generated)",
         "config": {"workload": LINEAR_WORKLOAD, "rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": f"{rows} rows of the workload per step, float64 oracle, projection + forward"},
+                         "sample": f"{rows} rows of the workload per step, float64 oracle, projection, forward "
+                                   "and backward"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -480,8 +493,10 @@ def run_linear(args):
     n, h, v = lw.n_rows, lw.hidden_size, lw.vocab
     x_host = torch.from_numpy(lw.hidden.view(np.int16)).view(torch.bfloat16).pin_memory()
     t_host = torch.from_numpy(lw.target_ids).pin_memory()
+    g_host = torch.from_numpy(lw.grad_logp).pin_memory()
     x = x_host.to(dev)
     t = t_host.to(dev)
+    g = g_host.to(dev)
     wt = torch.from_numpy(lw.weight.view(np.int16)).view(torch.bfloat16).to(dev)
     nt = -(-v // bil.LINEAR_TILE_V)
     pm = torch.empty((n, nt), dtype=torch.float32, device=dev)
@@ -490,10 +505,12 @@ def run_linear(args):
     logp = torch.empty(n, dtype=torch.float32, device=dev)
     lse = torch.empty(n, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    w_t = bil.linear.prepared_weight_t(wt)  # the prepared [H, V] weight, kept while the weight is unchanged
 
     def step():
         bil.linear_logp_partials(x, wt, t, v, 0, nt, pm, ps, tl)
         bil.logp_merge(pm, ps, nt, tl, t, v, out=logp, lse=lse)
+        bil.linear_logp_bwd(x, wt, t, lse, g, weight_t=w_t)
 
     props = torch.cuda.get_device_properties(dev)
     sampler = ClockSampler(str(getattr(props, "uuid", "")))
@@ -504,8 +521,7 @@ def run_linear(args):
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     host_t0 = time.time()
     for i in range(K):
         ev[i][0].record(stream)
@@ -513,17 +529,24 @@ def run_linear(args):
         ev[i][1].record(stream)
         bil.logp_merge(pm, ps, nt, tl, t, v, out=logp, lse=lse)
         ev[i][2].record(stream)
+        bil.linear_logp_bwd(x, wt, t, lse, g, weight_t=w_t)
+        ev[i][3].record(stream)
     torch.cuda.synchronize(dev)
     host_t1 = time.time()
     barrier(dist, dev)
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    total_ms = ev[0][0].elapsed_time(ev[-1][3])
     part_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     merge_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    # the backward's scratch: dZ and dZ^T (bf16), hidden^T, plus the prepared W^T
+    scratch = 2 * n * v * 2 + h * n * 2
+    prepared = h * v * 2
     sampler.stop()
     clocks = sampler.summary(host_t0, host_t1)
     total_ms = max_over_ranks(total_ms, dist, dev)
     ms_step, value = aggregate(n, world, K, total_ms)
-    flops = 2.0 * n * h * v
+    flops = 2.0 * n * h * v           # one projection-sized GEMM
+    step_flops = 4 * flops            # forward, recomputation, dhidden, dweight
     tflops = flops / (part_ms / 1e3) / 1e12
     burst, sustained, peak_kind = tensor_peak()
     # the kernel is timed inside a loop of K back-to-back launches (seconds under
@@ -537,11 +560,14 @@ def run_linear(args):
         ws = torch.empty(bil.linear.workspace_bytes(n, v), dtype=torch.uint8, device=dev)
         xd = torch.empty_like(x)
         td = torch.empty_like(t)
+        gd = torch.empty_like(g)
 
         def e2e_step():
             xd.copy_(x_host, non_blocking=True)
             td.copy_(t_host, non_blocking=True)
+            gd.copy_(g_host, non_blocking=True)
             lp, ls = bil.linear_logp(xd, wt, td, workspace=ws)
+            bil.linear_logp_bwd(xd, wt, td, ls, gd, weight_t=w_t)
             logp_host.copy_(lp, non_blocking=True)
             lse_host.copy_(ls, non_blocking=True)
         for _ in range(2):
@@ -555,19 +581,20 @@ def run_linear(args):
             marks[i + 1].record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), dist, dev)
-        h2d = x_host.numel() * 2 + t_host.numel() * 8
+        h2d = x_host.numel() * 2 + t_host.numel() * 8 + g_host.numel() * 4
         d2h = logp_host.numel() * 4 + lse_host.numel() * 4
         e2e = {"value": n * world * args.e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.e2e_steps,
                "steps": args.e2e_steps,
-               "path": "linear_logp: pinned host hidden states -> device (weight resident) -> pinned host logp, lse"}
+               "path": "linear_logp + linear_logp_bwd: pinned host hidden states, targets, g -> device (weight "
+                       "resident; dhidden and dweight stay on the device for the optimizer) -> pinned host logp, lse"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rps, dt, cores = oracle_linear_rows_per_s(LINEAR_CPU_ROWS)
         cpu = {"value": rps, "unit": "rows/s", "cores": cores, "kind": "oracle",
-               "sample": f"first {LINEAR_CPU_ROWS} rows of the workload, float64 projection + forward, "
-                         f"{dt:.1f} s wall"}
+               "sample": f"first {LINEAR_CPU_ROWS} rows of the workload, float64 projection, forward and "
+                         f"backward, {dt:.1f} s wall"}
     if rank == 0:
         print(json.dumps({
             "metric": LINEAR_METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
@@ -577,15 +604,18 @@ def run_linear(args):
                        "tile_v": bil.LINEAR_TILE_V,
                        "l2": "no flush: every pass reads the 1.25 GB LM-head weight, 9.6x the 129 MB L2",
                        "parallelism": f"dp{world} (independent row batches per GPU, weight replicated)"},
-            "tflops": flops / (ms_step / 1e3) / 1e12,
+            "tflops": step_flops / (ms_step / 1e3) / 1e12,
             "kernels": {"linear_partials": {"ms": part_ms, "tflops": tflops},
-                        "logp_merge": {"ms": merge_ms}},
+                        "logp_merge": {"ms": merge_ms},
+                        "linear_logp_bwd": {"ms": bwd_ms, "tflops": 3 * flops / (bwd_ms / 1e3) / 1e12,
+                                            "launches": 4, "scratch_bytes": scratch,
+                                            "prepared_weight_t_bytes": prepared}},
             "roofline": {"kernel": "linear_partials_kernel", "bound": "tensor", "achieved": tflops, "peak": peak,
                          "peak_source": f"{peak_kind} sustained dense bf16 (burst {burst})", "unit": "TFLOP/s",
                          "frac": tflops / peak, "frac_of_burst": tflops / burst,
                          "traffic": ncu_traffic("linear_partials_kernel", LINEAR_SOURCE),
                          "algorithmic_flops_per_launch": flops},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 6 * K, "clocks": clocks,
         }), flush=True)
     if dist is not None:
         dist.destroy_process_group()
