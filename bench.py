@@ -75,6 +75,8 @@ def parse():
                     help="rows of the workload per GPU (smaller only for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["training", "linear"], default="training")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the secondary measurements (entropy with a temperature, decode latency)")
     return ap.parse_args()
 
 
@@ -281,6 +283,71 @@ def ncu_traffic(kernel: str, source: str = KERNEL_SOURCE):
     return None
 
 
+def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_bytes, stream, dev):
+    """The entropy output with a temperature of 0.7 (forward with the entropy, backward with an
+    entropy gradient) on the same batch, and the forward's latency on decode-sized batches (the
+    first N rows).  Outside the timed region of the headline value."""
+    import torch
+
+    gh = torch.from_numpy(np.random.default_rng(7).standard_normal(n).astype(np.float32)).to(dev)
+    ent = torch.empty(n, dtype=torch.float32, device=dev)
+
+    def step_ent():
+        bil.logp_fwd(x, t, w.ignore_index, w.tile_v, out=logp, lse=lse, temperature=0.7, entropy=ent)
+        bil.logp_bwd(x, t, lse, g, w.ignore_index, out=d, temperature=0.7, entropy=ent, grad_entropy=gh)
+    for _ in range(3):
+        step_ent()
+    KV = 20
+    evv = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KV)]
+    for i in range(KV):
+        evv[i][0].record(stream)
+        bil.logp_fwd(x, t, w.ignore_index, w.tile_v, out=logp, lse=lse, temperature=0.7, entropy=ent)
+        evv[i][1].record(stream)
+        bil.logp_bwd(x, t, lse, g, w.ignore_index, out=d, temperature=0.7, entropy=ent, grad_entropy=gh)
+        evv[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    ef = statistics.mean(e[0].elapsed_time(e[1]) for e in evv)
+    eb = statistics.mean(e[1].elapsed_time(e[2]) for e in evv)
+    variants = {"entropy_temperature_0.7": {
+        "fwd_ms": ef, "fwd_gbs": (fwd_bytes + 4 * n) / (ef / 1e3) / 1e9,
+        "bwd_ms": eb, "bwd_gbs": (bwd_bytes + 8 * n) / (eb / 1e3) / 1e9, "steps": KV}}
+    # decode-sized batches: device time per forward call on the first N rows,
+    # from a CUDA graph of 20 calls (so the host's per-call cost does not count),
+    # and the same 20 calls issued one by one from Python (host-bound)
+    lat, eager = {}, {}
+    for nd in (1, 2, 3, 7, 64, 256):
+        xs, ts = x[:nd], t[:nd]
+        for _ in range(5):
+            bil.logp_fwd(xs, ts, w.ignore_index, w.tile_v)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            bil.logp_fwd(xs, ts, w.ignore_index, w.tile_v)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        eager[str(nd)] = round(e0.elapsed_time(e1) / 20 * 1e3, 2)
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+                for _ in range(20):
+                    bil.logp_fwd(xs, ts, w.ignore_index, w.tile_v)
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for _ in range(5):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            lat[str(nd)] = round(e0.elapsed_time(e1) / 100 * 1e3, 2)
+            del graph
+        except RuntimeError as exc:  # no graph: report the host-bound figure only
+            lat[str(nd)] = f"unavailable: {str(exc).splitlines()[0][:80]}"
+    variants["decode_fwd_us_per_call_graph"] = lat
+    variants["decode_fwd_us_per_call_python"] = eager
+    return variants
+
+
 def run_bil(args):
     import torch
 
@@ -353,6 +420,11 @@ def run_bil(args):
     fwd_gbs = fwd_bytes / (fwd_avg / 1e3) / 1e9
     step_gbs = (fwd_bytes + bwd_bytes) / (ms_step / 1e3) / 1e9  # per GPU
 
+    # ---- secondary measurements (outside the timed region of `value`) ----
+    variants = None
+    if not args.no_variants:
+        variants = secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_bytes, stream, dev)
+
     # ---- end to end: pinned host inputs -> device -> kernels -> host results ----
     # Through the public API for host-resident batches (HostStreamedLogp):
     # row chunks stream in, are computed and stream out on three CUDA streams.
@@ -414,6 +486,7 @@ def run_bil(args):
                          "frac": bwd_gbs / peak, "traffic": ncu_traffic("bwd_kernel"),
                          "algorithmic_bytes_per_launch": bwd_bytes},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
+            "variants": variants,
         }
         print(json.dumps(out), flush=True)
     if dist is not None:
