@@ -315,7 +315,7 @@ def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_byte
     # from a CUDA graph of 20 calls (so the host's per-call cost does not count),
     # and the same 20 calls issued one by one from Python (host-bound)
     lat, eager = {}, {}
-    for nd in (1, 2, 3, 7, 64, 256):
+    for nd in (1, 2, 3, 7, 64, 128, 256):
         xs, ts = x[:nd], t[:nd]
         for _ in range(5):
             bil.logp_fwd(xs, ts, w.ignore_index, w.tile_v)

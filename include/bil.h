@@ -42,6 +42,10 @@
  *    bulk asynchronous copies in whole 16-byte units (the unit holding column
  *    vocab-1 may extend past it, never past column ld-1); other rows are read
  *    element by element.  The results are bit-identical either way.
+ *  - bil_logp_fwd on at most 128 rows of a 16-bit type (aligned rows, tiles of
+ *    at most 4096) shares each row among a cluster of 8 blocks instead of
+ *    streaming it through one block; the results are bit-identical to the
+ *    streaming path.
  *
  * Results are bitwise reproducible for a given tile_v, element type and
  * library build (the arithmetic is fixed in bil_contract_id()).

@@ -861,6 +861,106 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
 }
 
 // ---------------------------------------------------------------------------
+// Small-batch forward: one row per thread-block cluster.
+//
+// With a handful of rows the streaming forward has one block per row, and one
+// SM streams the whole row.  Here a cluster of kSplitCtas blocks (on as many
+// SMs) shares each row: warp w of cluster rank c takes tiles c*kSplitWarps + w,
+// then + kSplitCtas*kSplitWarps, ...; each reduces its tile straight from
+// global memory with tile_load_regs / tile_reduce_regs (the same functions,
+// and so the same bits, as the streaming forward) and writes the partial into
+// the cluster's rank-0 block through distributed shared memory.  After one
+// cluster barrier the rank-0 block merges the row with merge_lse.  The bits
+// are those of the streaming forward; only the work split differs.  Used for
+// 16-bit types whose rows are 16-byte aligned, with tiles of at most
+// TileRegs::kMaxTile elements: a group of 8 elements is then one 16-byte unit
+// inside the row (the unit holding column vocab-1 ends before column ld).
+// ---------------------------------------------------------------------------
+
+constexpr int kSplitCtas = 8;   // blocks per cluster (the portable maximum)
+constexpr int kSplitWarps = 5;  // 40 warps per row: a 151936-column row in 4096-column tiles is 38 tiles
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of `p` (a shared variable of this block) in the
+// block of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Every thread of every block of the cluster arrives; the release / acquire
+// pair makes the distributed shared-memory stores before it visible after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int DT, bool ENT>
+__global__ void __launch_bounds__(kSplitWarps * kLanes) split_row_kernel(const StreamParams p) {
+  constexpr int EB = Elem<DT>::kBytes;
+  __shared__ float sm_m[BIL_MAX_FUSED_TILES];
+  __shared__ float sm_s[BIL_MAX_FUSED_TILES];
+  __shared__ float sm_u[ENT ? BIL_MAX_FUSED_TILES : 1];
+  __shared__ float sm_tl;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t row = static_cast<int64_t>(blockIdx.x) / kSplitCtas;  // a cluster is kSplitCtas consecutive blocks
+  const int warp = threadIdx.x / kLanes;
+  const int lane = threadIdx.x % kLanes;
+  const int64_t target = row < p.n_rows ? p.targets[row] : p.ignore_index;
+  const bool active = row < p.n_rows && target != p.ignore_index;
+  if (rank == 0 && threadIdx.x == 0) sm_tl = __int_as_float(0x7fc00000);
+  cluster_sync_all();  // rank 0's initial value is in place before any block writes into it
+  if (active) {
+    const unsigned char* row_src = p.logits + row * p.ld * EB;
+    for (int t = static_cast<int>(rank) * kSplitWarps + warp; t < p.num_tiles; t += kSplitCtas * kSplitWarps) {
+      const int64_t col0 = static_cast<int64_t>(t) * p.tile_v;
+      const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
+      const unsigned char* tile = row_src + col0 * EB;
+      TileRegs<DT> regs;
+      tile_load_regs<DT>(tile, valid, lane, regs);
+      const TilePartial tp = tile_reduce_regs<DT, ENT>(regs, valid, lane, p.rcp);
+      if (lane == 0) {
+        st_cluster(cluster_addr(&sm_m[t], 0), tp.m);
+        st_cluster(cluster_addr(&sm_s[t], 0), tp.s);
+        if (ENT) st_cluster(cluster_addr(&sm_u[t], 0), tp.u);
+        if (target >= col0 && target < col0 + valid) {
+          float tl = Elem<DT>::one(tile + (target - col0) * EB);
+          if (p.rcp != 1.0f) tl = __fmul_rn(tl, p.rcp);
+          st_cluster(cluster_addr(&sm_tl, 0), tl);
+        }
+      }
+    }
+  }
+  cluster_sync_all();
+  if (rank != 0 || warp != 0 || row >= p.n_rows) return;
+  if (!active) {
+    if (lane == 0) {
+      p.logp[row] = 0.0f;
+      if (p.lse != nullptr) p.lse[row] = 0.0f;
+      if (ENT) p.entropy[row] = 0.0f;
+    }
+    return;
+  }
+  float H = 0.0f;
+  const float L = merge_lse<ENT>(sm_m, sm_s, sm_u, p.num_tiles, lane, &H);
+  if (lane == 0) {
+    const bool valid_target = target >= 0 && target < p.vocab;
+    p.logp[row] = valid_target ? __fsub_rn(sm_tl, L) : __int_as_float(0x7fc00000);
+    if (p.lse != nullptr) p.lse[row] = L;
+    if (ENT) p.entropy[row] = H;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Merge kernel: one warp per row, the same merge_lse as the fused forward.
 // ---------------------------------------------------------------------------
 
@@ -1239,6 +1339,45 @@ int launch_stream(int dtype, bool ent, const StreamParams& p, cudaStream_t strea
   }
 }
 
+// Rows at or below which the forward takes the cluster path (one row per
+// cluster of kSplitCtas blocks) when it applies.
+#ifndef BIL_SPLIT_MAX_ROWS
+#define BIL_SPLIT_MAX_ROWS 128
+#endif
+
+template <int DT, bool ENT>
+int launch_split_t(const StreamParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_rows * kSplitCtas), 1, 1);
+  cfg.blockDim = dim3(kSplitWarps * kLanes, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSplitCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, split_row_kernel<DT, ENT>, p) != cudaSuccess) return BIL_E_CUDA;
+  return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
+}
+
+// Whether the fused forward of these rows takes the cluster path.
+bool use_split(int dtype, const StreamParams& p) {
+  const int eb = elem_bytes(dtype);
+  return eb == 2 && p.n_rows >= 1 && p.n_rows <= BIL_SPLIT_MAX_ROWS && p.tile_v <= 4096 &&
+         p.num_tiles <= BIL_MAX_FUSED_TILES && aligned(p.logits, 16) && (p.ld * eb) % 16 == 0;
+}
+
+int launch_split(int dtype, bool ent, const StreamParams& p, cudaStream_t stream) {
+  switch (dtype) {
+    case BIL_BF16: return ent ? launch_split_t<BIL_BF16, true>(p, stream) : launch_split_t<BIL_BF16, false>(p, stream);
+    case BIL_F16: return ent ? launch_split_t<BIL_F16, true>(p, stream) : launch_split_t<BIL_F16, false>(p, stream);
+    default: return BIL_E_DTYPE;
+  }
+}
+
 int check_tile(int dtype, int64_t vocab, int32_t tile_v, int64_t* num_tiles) {
   const int eb = elem_bytes(dtype);
   if (eb == 0) return BIL_E_DTYPE;
@@ -1378,6 +1517,7 @@ int bil_logp_fwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
   p.lse = lse;
   p.entropy = entropy;
   p.stage_bytes = static_cast<unsigned>(static_cast<size_t>(tile_v) * eb);
+  if (use_split(dtype, p)) return launch_split(dtype, entropy != nullptr, p, s);
   return launch_stream<true>(dtype, entropy != nullptr, p, s);
 }
 

@@ -139,3 +139,33 @@ def test_packed_sequences_alone_match_the_packed_batch(packed):
     assert np.all(f32_bits(logp)[pad] == 0)
     pad_rows = torch.from_numpy(np.flatnonzero(pad)).cuda()
     assert not torch.any(d.index_select(0, pad_rows).view(torch.int16) != 0)  # +0.0 bit patterns
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.8])
+def test_small_batches_take_the_cluster_path_with_the_same_bits(bank, temperature):
+    """Up to 128 rows (16-bit, 16-byte aligned rows, tiles of at most 4096), the
+    forward shares each row among a cluster of blocks instead of streaming it
+    through one; the bits must not change: every row of a small batch (1, 5,
+    128 rows; 129 takes the streaming path) equals that row in the full
+    256-row batch, with the entropy, ignored rows and an out-of-range target
+    among them."""
+    w = bank
+    x = device_logits(w.logits, w.dtype)
+    t = torch.from_numpy(w.target_ids).cuda()
+    t[7] = -100
+    t[12] = w.vocab + 3  # invalid: NaN logp, lse still computed
+    ref = bil.logp_fwd(x, t, -100, w.tile_v, temperature=temperature, return_entropy=True)
+    torch.cuda.synchronize()
+    refb = [f32_bits(r) for r in ref]
+    r = wl.rng(11, 3)
+    for n in (1, 5, 128, 129):
+        for draw in range(3):
+            idx = r.permutation(256)[:n]
+            if draw == 0:
+                idx[: min(n, 2)] = [7, 12][: min(n, 2)]
+            sel = torch.from_numpy(idx).cuda()
+            got = bil.logp_fwd(x.index_select(0, sel), t.index_select(0, sel), -100, w.tile_v,
+                               temperature=temperature, return_entropy=True)
+            torch.cuda.synchronize()
+            for g, rb in zip(got, refb):
+                assert np.array_equal(f32_bits(g), rb[idx]), (n, draw)
