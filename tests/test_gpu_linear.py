@@ -231,3 +231,35 @@ def test_argument_errors_queue_nothing():
     with pytest.raises(bil.BilError) as e:  # target out of range with validate
         bil.linear_logp(x, w, torch.full((4,), 300, dtype=torch.int64, device="cuda"), validate=True)
     assert e.value.status == 4
+
+
+@pytest.mark.parametrize("n,h,v", [(1, 64, 300), (5, 8, 100), (130, 24, 256), (3, 4096, 40)])
+def test_small_and_ragged_shapes(n, h, v):
+    """A vocabulary inside one tile, a hidden size below one K block (the TMA
+    box reads zeros past it), a single row."""
+    x, w, t = make_case(n, h, v, seed=n * 7 + v, ignore_every=0)
+    xd, wd, td = to_dev(x, w, t, "bfloat16")
+    logp, lse, ent = bil.linear_logp(xd, wd, td, return_entropy=True)
+    torch.cuda.synchronize()
+    rl, rs, _, rh = oracle.linear_logp_fwd(x, w, "bfloat16", t, entropy=True)
+    assert_close_abs(logp.cpu().numpy(), rl, LOGP_ATOL, "logp")
+    assert_close_abs(lse.cpu().numpy(), rs, LOGP_ATOL, "lse")
+    assert_close_abs(ent.cpu().numpy(), rh, ENTROPY_ATOL, "entropy")
+
+
+def test_empty_batch_and_invalid_targets():
+    x, w, t = make_case(6, 64, 500, seed=3, ignore_every=0)
+    xd, wd, td = to_dev(x, w, t, "bfloat16")
+    lp, ls = bil.linear_logp(xd[:0], wd, td[:0])
+    assert lp.numel() == 0 and ls.numel() == 0
+    bad = td.clone()
+    bad[2] = 500        # one past the vocabulary
+    bad[4] = -1         # negative, not the ignore index
+    lp, ls = bil.linear_logp(xd, wd, bad)
+    ref, rls = bil.linear_logp(xd, wd, td)
+    torch.cuda.synchronize()
+    lpn = lp.cpu().numpy()
+    assert np.isnan(lpn[2]) and np.isnan(lpn[4])
+    keep = [0, 1, 3, 5]
+    assert np.array_equal(f32_bits(lp)[keep], f32_bits(ref)[keep])
+    assert np.array_equal(f32_bits(ls), f32_bits(rls))  # lse never depends on the target

@@ -205,3 +205,25 @@ def test_full_size_sampled_rows_and_the_bilinear_identity():
     wmax = float(wl.bf16_bits_to_f32(np.array([(lw.weight & np.uint16(0x7FFF)).max()], np.uint16))[0])
     bound = (2.0 ** -8 + 151936 / 4 * 2.0 ** -24) * 2 * np.abs(lw.grad_logp[idx])[:, None] * wmax * 2 + 1e-6
     assert np.all(np.abs(got - rdx) <= bound)
+
+
+def test_backward_edges():
+    """No rows: dweight is zero.  An active row with an out-of-range target makes
+    its dZ row NaN (and so its dhidden row); ignored rows are exactly zero."""
+    n, h, v = 6, 64, 300
+    x, w, t, g, _ = make_case(n, h, v, seed=8, ignore_every=0)
+    xd, wd, td = device_logits(x, "bfloat16"), device_logits(w, "bfloat16"), torch.from_numpy(t).cuda()
+    gd = torch.from_numpy(g).cuda()
+    lse = bil.linear_logp(xd, wd, td)[1]
+    dh0, dw0 = bil.linear_logp_bwd(xd[:0], wd, td[:0], lse[:0], gd[:0], out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert dh0.numel() == 0 and torch.count_nonzero(dw0).item() == 0
+    bad = td.clone()
+    bad[1] = v + 5
+    bad[3] = -100
+    dh, dw, dz = bil.linear_logp_bwd(xd, wd, bad, lse, gd, out_dtype=torch.float32, return_dz=True)
+    torch.cuda.synchronize()
+    dzf = dz.float().cpu().numpy()
+    assert np.all(np.isnan(dzf[1])) and np.all(np.isnan(dh.cpu().numpy()[1]))
+    assert np.all(dzf[3] == 0) and not np.isnan(dzf[[0, 2, 4, 5]]).any()
+    assert np.all(np.isnan(dw.cpu().numpy()))  # every dweight entry sums over row 1
