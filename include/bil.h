@@ -311,24 +311,30 @@ int bil_linear_logp_fwd(const void *hidden, const void *weight, int dtype, int64
  * dhidden never depends on the other rows.
  *
  *  hidden, weight, dtype, n_rows, hidden_size, ld_hidden, vocab, ld_weight,
- *  temperature, target_ids, ignore_index
- *                as for bil_linear_logp_fwd over the whole vocabulary.
- *  weight_t      the weight transposed, [hidden_size, ld_weight_t] (ld_weight_t
- *                >= vocab), e.g. from bil_transpose_2d; a caller keeps it as
- *                long as the weight does not change.
+ *  tile_begin, tile_end, temperature, target_ids, ignore_index
+ *                as for bil_linear_logp_partials: `weight` holds the shard's
+ *                rows, the global vocabulary columns [tile_begin * 256,
+ *                min(tile_end * 256, vocab)) -- "cols" below; the whole
+ *                vocabulary is tile_begin = 0, tile_end = ceil(vocab / 256).
+ *                With a shard, dhidden is the shard's part of the sum over
+ *                the vocabulary (the ranks' parts add up to it; see
+ *                bil_sum_f32) and dweight holds the shard's rows.
+ *  weight_t      the shard's weight transposed, [hidden_size, ld_weight_t]
+ *                (ld_weight_t >= cols), e.g. from bil_transpose_2d; a caller
+ *                keeps it as long as the weight does not change.
  *  lse           [n_rows] float32, the forward's lse.
  *  grad_logp     [n_rows] float32 upstream gradient of logp.
  *  entropy, grad_entropy   both NULL, or the forward's entropy and its
  *                upstream gradient ([n_rows] float32 each).
- *  dz            [n_rows, ld_dz] (ld_dz >= vocab) of dtype: receives dZ.
- *  dz_t          [vocab, ld_dz_t] (ld_dz_t >= n_rows) of dtype: receives dZ^T.
+ *  dz            [n_rows, ld_dz] (ld_dz >= cols) of dtype: receives dZ.
+ *  dz_t          [cols, ld_dz_t] (ld_dz_t >= n_rows) of dtype: receives dZ^T.
  *  hidden_t      [hidden_size, ld_hidden_t] (ld_hidden_t >= n_rows) of dtype:
  *                receives hidden^T.
  *                (dz, dz_t and hidden_t are the backward's scratch, owned by
  *                the caller, readable afterwards.)
  *  dhidden       [n_rows, ld_dhidden] of dhidden_dtype (BIL_F32, or dtype
  *                rounded to nearest even).
- *  dweight       [vocab, ld_dweight] of dweight_dtype (the same choice).
+ *  dweight       [cols, ld_dweight] of dweight_dtype (the same choice).
  * Every matrix argument needs a 16-byte aligned base and a row stride of a
  * multiple of 16 bytes (BIL_E_ALIGN otherwise).  Inactive rows contribute
  * zero; an active row with a target outside [0, vocab) makes its dZ row NaN
@@ -337,12 +343,22 @@ int bil_linear_logp_fwd(const void *hidden, const void *weight, int dtype, int64
  */
 int bil_linear_logp_bwd(const void *hidden, const void *weight, const void *weight_t, int dtype,
                         int64_t n_rows, int64_t hidden_size, int64_t ld_hidden, int64_t vocab,
-                        int64_t ld_weight, int64_t ld_weight_t, float temperature,
+                        int64_t ld_weight, int64_t ld_weight_t, int32_t tile_begin, int32_t tile_end,
+                        float temperature,
                         const int64_t *target_ids, int64_t ignore_index, const float *lse,
                         const float *grad_logp, const float *entropy, const float *grad_entropy,
                         void *dz, int64_t ld_dz, void *dz_t, int64_t ld_dz_t, void *hidden_t,
                         int64_t ld_hidden_t, void *dhidden, int dhidden_dtype, int64_t ld_dhidden,
                         void *dweight, int dweight_dtype, int64_t ld_dweight, bil_stream_t stream);
+
+/*
+ * bil_sum_f32 -- dst[i] = ((srcs[0][i] + srcs[1][i]) + srcs[2][i]) + ... for
+ * i < n: float32 sums in the order of `srcs` (1 <= count <= 16; `srcs` is a
+ * host array of device pointers; dst may be one of the sources).  Adds the
+ * tensor-parallel ranks' parts of dhidden in rank order, so that every rank
+ * holds the same bits.
+ */
+int bil_sum_f32(const float *const *srcs, int count, int64_t n, float *dst, bil_stream_t stream);
 
 /*
  * bil_transpose_2d -- dst[c, r] = src[r, c] for a [rows, cols] matrix of

@@ -600,6 +600,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   gemm_body<kModeStore, false, OT>(tmap_a, tmap_b, p);
 }
 
+// dst[i] = ((src_0[i] + src_1[i]) + src_2[i]) + ... , sources in order.
+constexpr int kMaxSumSources = 16;
+struct SumSources {
+  const float* src[kMaxSumSources];
+};
+
+__global__ void __launch_bounds__(256) sum_f32_kernel(SumSources s, int count, int64_t n, float* __restrict__ dst) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float acc = s.src[0][i];
+    for (int k = 1; k < count; ++k) acc = __fadd_rn(acc, s.src[k][i]);
+    dst[i] = acc;
+  }
+}
+
 // Out-of-place transpose of a [rows, cols] matrix of 16-bit elements
 // (dst[c, r] = src[r, c]) through a 64 x 64 shared-memory tile; consecutive
 // threads read consecutive elements of a source row and write consecutive
@@ -865,6 +880,23 @@ int bil_linear_logp_fwd(const void* hidden, const void* weight, int dtype, int64
                         ignore_index, vocab, logp, lse, entropy, 0, stream);
 }
 
+int bil_sum_f32(const float* const* srcs, int count, int64_t n, float* dst, bil_stream_t stream) {
+  if (srcs == nullptr || count < 1 || count > kMaxSumSources || n < 0 || dst == nullptr) return BIL_E_INVALID_ARG;
+  SumSources s{};
+  for (int k = 0; k < count; ++k) {
+    if (srcs[k] == nullptr) return BIL_E_INVALID_ARG;
+    if (!aligned_to(srcs[k], 4)) return BIL_E_ALIGN;
+    s.src[k] = srcs[k];
+  }
+  if (!aligned_to(dst, 4)) return BIL_E_ALIGN;
+  if (n == 0) return BIL_OK;
+  int sms = 0, smem = 0;
+  if (int st = bil_internal::device_limits(&sms, &smem)) return st;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(sms) * 8));
+  sum_f32_kernel<<<static_cast<unsigned>(grid), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(s, count, n, dst);
+  return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
+}
+
 int bil_transpose_2d(const void* src, int dtype, int64_t rows, int64_t cols, int64_t ld_src, void* dst,
                      int64_t ld_dst, bil_stream_t stream) {
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
@@ -877,7 +909,7 @@ int bil_transpose_2d(const void* src, int dtype, int64_t rows, int64_t cols, int
 
 int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weight_t, int dtype, int64_t n_rows,
                         int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight, int64_t ld_weight_t,
-                        float temperature, const int64_t* target_ids, int64_t ignore_index, const float* lse,
+                        int32_t tile_begin, int32_t tile_end, float temperature, const int64_t* target_ids, int64_t ignore_index, const float* lse,
                         const float* grad_logp, const float* entropy, const float* grad_entropy, void* dz,
                         int64_t ld_dz, void* dz_t, int64_t ld_dz_t, void* hidden_t, int64_t ld_hidden_t,
                         void* dhidden, int dhidden_dtype, int64_t ld_dhidden, void* dweight, int dweight_dtype,
@@ -885,8 +917,15 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   for (int ot : {dhidden_dtype, dweight_dtype})
     if (ot != BIL_F32 && ot != dtype) return BIL_E_DTYPE;
-  if (n_rows < 0 || hidden_size < 1 || vocab < 1 || ld_hidden < hidden_size || ld_weight < hidden_size ||
-      ld_weight_t < vocab || ld_dz < vocab || ld_dz_t < n_rows || ld_hidden_t < n_rows ||
+  if (vocab < 1) return BIL_E_INVALID_ARG;
+  const int64_t num_tiles = (vocab + kBN - 1) / kBN;
+  if (num_tiles > INT32_MAX / 2) return BIL_E_UNSUPPORTED;
+  if (tile_begin < 0 || tile_begin >= tile_end || tile_end > num_tiles) return BIL_E_INVALID_ARG;
+  // the shard: global vocabulary columns [tile_begin * 256, min(tile_end * 256, vocab))
+  const int64_t cols = std::min<int64_t>(static_cast<int64_t>(tile_end) * kBN, vocab) -
+                       static_cast<int64_t>(tile_begin) * kBN;
+  if (n_rows < 0 || hidden_size < 1 || ld_hidden < hidden_size || ld_weight < hidden_size ||
+      ld_weight_t < cols || ld_dz < cols || ld_dz_t < n_rows || ld_hidden_t < n_rows ||
       ld_dhidden < hidden_size || ld_dweight < hidden_size)
     return BIL_E_INVALID_ARG;
   if ((entropy == nullptr) != (grad_entropy == nullptr)) return BIL_E_INVALID_ARG;
@@ -899,7 +938,7 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (n_rows == 0) {  // dweight is a sum over no rows
     return cudaMemset2DAsync(dweight, static_cast<size_t>(ld_dweight * eo_w), 0,
-                             static_cast<size_t>(hidden_size * eo_w), static_cast<size_t>(vocab), s) == cudaSuccess
+                             static_cast<size_t>(hidden_size * eo_w), static_cast<size_t>(cols), s) == cudaSuccess
                ? BIL_OK
                : BIL_E_CUDA;
   }
@@ -912,7 +951,7 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
   if (!aligned_to(target_ids, 8) || !aligned_to(lse, 4) || !aligned_to(grad_logp, 4) ||
       (entropy && (!aligned_to(entropy, 4) || !aligned_to(grad_entropy, 4))))
     return BIL_E_ALIGN;
-  if (n_rows > INT32_MAX - kBM || vocab > INT32_MAX - kBN || hidden_size > INT32_MAX - kBN)
+  if (n_rows > INT32_MAX - kBM || cols > INT32_MAX - kBN || hidden_size > INT32_MAX - kBN)
     return BIL_E_UNSUPPORTED;
   if ((n_rows + 63) / 64 > 65535) return BIL_E_UNSUPPORTED;  // the transpose's grid
 
@@ -923,10 +962,10 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
   CUtensorMap maps[6];
   {
     int st = make_map(&maps[0], hidden, dtype, n_rows, hidden_size, ld_hidden, kBM);
-    if (!st) st = make_map(&maps[1], weight, dtype, vocab, hidden_size, ld_weight, kBN);
-    if (!st) st = make_map(&maps[2], dz, dtype, n_rows, vocab, ld_dz, kBM);
-    if (!st) st = make_map(&maps[3], weight_t, dtype, hidden_size, vocab, ld_weight_t, kBN);
-    if (!st) st = make_map(&maps[4], dz_t, dtype, vocab, n_rows, ld_dz_t, kBM);
+    if (!st) st = make_map(&maps[1], weight, dtype, cols, hidden_size, ld_weight, kBN);
+    if (!st) st = make_map(&maps[2], dz, dtype, n_rows, cols, ld_dz, kBM);
+    if (!st) st = make_map(&maps[3], weight_t, dtype, hidden_size, cols, ld_weight_t, kBN);
+    if (!st) st = make_map(&maps[4], dz_t, dtype, cols, n_rows, ld_dz_t, kBM);
     if (!st) st = make_map(&maps[5], hidden_t, dtype, hidden_size, n_rows, ld_hidden_t, kBN);
     if (st) return st;
   }
@@ -939,9 +978,9 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
   {
     LinearParams p{};
     p.n_rows = n_rows;
-    p.shard_cols = vocab;
-    p.tile_begin = 0;
-    p.num_n = static_cast<int>((vocab + kBN - 1) / kBN);
+    p.shard_cols = cols;
+    p.tile_begin = tile_begin;
+    p.num_n = tile_end - tile_begin;
     p.num_m = static_cast<int>((n_rows + kBM - 1) / kBM);
     p.k_blocks = static_cast<int>((hidden_size + kBK - 1) / kBK);
     p.targets = target_ids;
@@ -974,8 +1013,8 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
     int64_t ld_out;
   };
   const Contraction cs[2] = {
-      {&maps[2], &maps[3], n_rows, vocab, dhidden, dhidden_dtype, ld_dhidden},
-      {&maps[4], &maps[5], vocab, n_rows, dweight, dweight_dtype, ld_dweight},
+      {&maps[2], &maps[3], n_rows, cols, dhidden, dhidden_dtype, ld_dhidden},
+      {&maps[4], &maps[5], cols, n_rows, dweight, dweight_dtype, ld_dweight},
   };
   for (const Contraction& c : cs) {
     LinearParams p{};

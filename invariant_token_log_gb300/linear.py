@@ -177,17 +177,27 @@ def linear_logp_bwd(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torc
                     grad_logp: torch.Tensor, ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
                     entropy: torch.Tensor | None = None, grad_entropy: torch.Tensor | None = None,
                     weight_t: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
-                    return_dz: bool = False):
-    """(dhidden [*lead, H], dweight [V, H][, dZ [N, V]]) of g * logp (+ gh * entropy).
+                    return_dz: bool = False, vocab: int | None = None, tile_begin: int = 0,
+                    tile_end: int | None = None):
+    """(dhidden [*lead, H], dweight [cols, H][, dZ [N, cols]]) of g * logp (+ gh * entropy).
 
-    ``out_dtype`` is float32 or the inputs' type (the default)."""
+    ``weight`` holds the LM-head rows of global vocabulary columns
+    [tile_begin * 256, min(tile_end * 256, vocab)) ("cols"; by default the
+    whole vocabulary, vocab = weight rows).  With a shard, dhidden is the
+    shard's part of the sum over the vocabulary.  ``out_dtype`` is float32 or
+    the inputs' type (the default)."""
     _need_cuda(hidden, weight, target_ids, lse, grad_logp, entropy, grad_entropy, weight_t)
     lead = hidden.shape[:-1]
     h2, w2 = _matrix(hidden, "hidden"), _matrix(weight, "weight")
     if h2.dtype != w2.dtype or h2.shape[1] != w2.shape[1]:
         raise ValueError("hidden and weight must share the element type and the hidden size")
     n, hs = h2.shape
-    v = w2.shape[0]
+    vocab = w2.shape[0] if vocab is None else vocab
+    tile_end = num_tiles(vocab) if tile_end is None else tile_end
+    v = min(tile_end * LINEAR_TILE_V, vocab) - tile_begin * LINEAR_TILE_V  # the shard's columns
+    if v <= 0 or w2.shape[0] < v:
+        raise ValueError(f"the weight holds {w2.shape[0]} rows; tiles [{tile_begin}, {tile_end}) need {v}")
+    w2 = w2[:v]
     dev = h2.device
     t = target_ids.reshape(-1).to(torch.int64).contiguous()
     if (entropy is None) != (grad_entropy is None):
@@ -205,8 +215,8 @@ def linear_logp_bwd(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torc
     dw = torch.empty((v, _pad8(hs)), dtype=out_dtype, device=dev)[:, :hs]
     oc = _lib.F32 if out_dtype == torch.float32 else _in_code(out_dtype)
     _lib.check("bil_linear_logp_bwd", _lib.load().bil_linear_logp_bwd(
-        _ptr(h2), _ptr(w2), _ptr(wt), _in_code(h2.dtype), n, hs, _ld(h2), v, _ld(w2), wt.stride(0),
-        float(temperature), _ptr(t), ignore_index, _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), _ptr(f32[3]),
+        _ptr(h2), _ptr(w2), _ptr(wt), _in_code(h2.dtype), n, hs, _ld(h2), vocab, _ld(w2), wt.stride(0),
+        tile_begin, tile_end, float(temperature), _ptr(t), ignore_index, _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), _ptr(f32[3]),
         _ptr(dz), dz.stride(0), _ptr(dz_t), dz_t.stride(0), _ptr(h_t), h_t.stride(0),
         _ptr(dh), oc, dh.stride(0), _ptr(dw), oc, dw.stride(0), _stream(dev)))
     out = (dh.reshape(*lead, hs), dw)
@@ -247,3 +257,15 @@ def batch_invariant_linear_logp(hidden: torch.Tensor, weight: torch.Tensor, targ
     gradients for hidden and weight."""
     res = LinearLogp.apply(hidden, weight, target_ids, ignore_index, temperature, return_entropy)
     return (res[0], res[2]) if return_entropy else res[0]
+
+
+def sum_f32(parts: list[torch.Tensor], out: torch.Tensor | None = None) -> torch.Tensor:
+    """((parts[0] + parts[1]) + parts[2]) + ... elementwise in float32, in list order."""
+    _need_cuda(*parts)
+    ps = [p.contiguous() for p in parts]
+    if any(p.dtype != torch.float32 or p.shape != ps[0].shape for p in ps):
+        raise ValueError("sum_f32 takes float32 tensors of one shape")
+    out = torch.empty_like(ps[0]) if out is None else out
+    arr = (ctypes.c_void_p * len(ps))(*[p.data_ptr() for p in ps])
+    _lib.check("bil_sum_f32", _lib.load().bil_sum_f32(arr, len(ps), ps[0].numel(), _ptr(out), _stream(ps[0].device)))
+    return out

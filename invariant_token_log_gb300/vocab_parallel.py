@@ -20,6 +20,7 @@ from __future__ import annotations
 import torch
 import torch.distributed as dist
 
+from .linear import LINEAR_TILE_V, linear_logp_bwd, linear_logp_partials, sum_f32
 from .logp import DEFAULT_TILE_V, IGNORE_INDEX, logp_merge, logp_tile_partials
 
 
@@ -82,30 +83,84 @@ def vocab_parallel_logp(local_logits: torch.Tensor, target_ids: torch.Tensor, vo
     logp_fwd on the unsplit rows with the same tile_v."""
     num_tiles = -(-vocab // tile_v)
     n = target_ids.numel()
-    t_local = tile_end - tile_begin
     dev = local_logits.device
     # 1-2. this rank's tile partials (columns [tile_begin, tile_end) of [N, num_tiles])
-    width = num_tiles
-    pm = torch.empty((n, width), dtype=torch.float32, device=dev)
+    pm = torch.empty((n, num_tiles), dtype=torch.float32, device=dev)
     ps = torch.empty_like(pm)
     pe = torch.empty_like(pm) if return_entropy else None
     tl = torch.full((n,), float("nan"), dtype=torch.float32, device=dev)
     logp_tile_partials(local_logits, target_ids, vocab, tile_v, tile_begin, tile_end, pm, ps, tl, ignore_index,
                        temperature=temperature, part_ent=pe)
-    # 3. all_gather: bytes only.  Blocks are padded to the longest range so that
-    # every rank sends the same shape.
+    return _exchange_and_merge(pm, ps, pe, tl, tile_begin, tile_end, num_tiles, tile_v, target_ids, vocab, group,
+                               ignore_index)
+
+
+def _exchange_and_merge(pm, ps, pe, tl, tile_begin, tile_end, num_tiles, tile_v, target_ids, vocab, group,
+                        ignore_index):
+    """Steps 3-6 of "Tensor Parallel": all_gather this rank's partials (bytes
+    only; blocks padded to the longest range so that every rank sends one
+    shape), place every block at its tile columns, take the target logit from
+    its owner and merge all tiles in the fixed order."""
+    n = pm.shape[0]
+    t_local = tile_end - tile_begin
     ranges = tile_ranges(group, tile_begin, tile_end)
     pad = max(e - b for b, e in ranges)
-    mine = torch.zeros((3 if return_entropy else 2, n, pad), dtype=torch.float32, device=dev)
+    mine = torch.zeros((3 if pe is not None else 2, n, pad), dtype=torch.float32, device=pm.device)
     mine[0, :, :t_local] = pm[:, tile_begin:tile_end]
     mine[1, :, :t_local] = ps[:, tile_begin:tile_end]
-    if return_entropy:
+    if pe is not None:
         mine[2, :, :t_local] = pe[:, tile_begin:tile_end]
     blocks = _gather(mine, group)
     tls = _gather(tl, group)
-    # 4-6. the same fixed-order merge on every rank; the target logit from its owner
     full_m = assemble([blk[0] for blk in blocks], ranges, num_tiles).contiguous()
     full_s = assemble([blk[1] for blk in blocks], ranges, num_tiles).contiguous()
-    full_e = assemble([blk[2] for blk in blocks], ranges, num_tiles).contiguous() if return_entropy else None
+    full_e = assemble([blk[2] for blk in blocks], ranges, num_tiles).contiguous() if pe is not None else None
     tl_owner = owner_target_logit(tls, ranges, target_ids, tile_v, ignore_index).contiguous()
     return logp_merge(full_m, full_s, num_tiles, tl_owner, target_ids, vocab, ignore_index, part_ent=full_e)
+
+
+def vocab_parallel_linear_logp(hidden: torch.Tensor, weight_shard: torch.Tensor, target_ids: torch.Tensor,
+                               vocab: int, tile_begin: int, tile_end: int, group=None,
+                               ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                               return_entropy: bool = False):
+    """The fused LM-head + logp with the LM head split by vocabulary tiles across
+    the ranks of `group` ("[RFC][ROCm] End-to-end optimization of bitwise VIME
+    R/R beyond native P/P", "Workstream 3": merge vocabulary tiles and TP ranks
+    with an explicit fixed tree).
+
+    hidden        [N, H] the same on every rank.
+    weight_shard  this rank's LM-head rows: global vocabulary columns
+                  [tile_begin * 256, min(tile_end * 256, vocab)).
+    Every rank returns (logp, lse[, entropy]), bit for bit those of
+    linear_logp on the whole LM head."""
+    num_tiles = -(-vocab // LINEAR_TILE_V)
+    n = target_ids.numel()
+    dev = hidden.device
+    pm = torch.empty((n, num_tiles), dtype=torch.float32, device=dev)
+    ps = torch.empty_like(pm)
+    pe = torch.empty_like(pm) if return_entropy else None
+    tl = torch.full((n,), float("nan"), dtype=torch.float32, device=dev)
+    linear_logp_partials(hidden, weight_shard, target_ids, vocab, tile_begin, tile_end, pm, ps, tl, ignore_index,
+                         temperature=temperature, part_ent=pe)
+    return _exchange_and_merge(pm, ps, pe, tl, tile_begin, tile_end, num_tiles, LINEAR_TILE_V, target_ids, vocab,
+                               group, ignore_index)
+
+
+def vocab_parallel_linear_logp_bwd(hidden: torch.Tensor, weight_shard: torch.Tensor, target_ids: torch.Tensor,
+                                   lse: torch.Tensor, grad_logp: torch.Tensor, vocab: int, tile_begin: int,
+                                   tile_end: int, group=None, ignore_index: int = IGNORE_INDEX,
+                                   temperature: float = 1.0, entropy: torch.Tensor | None = None,
+                                   grad_entropy: torch.Tensor | None = None, weight_t: torch.Tensor | None = None):
+    """Backward of vocab_parallel_linear_logp: (dhidden [N, H], dweight_shard).
+
+    Each rank computes its shard's dZ, its dweight rows (bit for bit the
+    single-device rows: the sum runs over the batch, not the vocabulary) and
+    its part of dhidden = dZ . W; the parts are all-gathered (bytes only) and
+    added in rank order by bil_sum_f32, so every rank holds the same dhidden
+    (not the single-device bits: the sum over the vocabulary is split at the
+    shard boundaries)."""
+    dh, dw = linear_logp_bwd(hidden, weight_shard, target_ids, lse, grad_logp, ignore_index, temperature, entropy,
+                             grad_entropy, weight_t=weight_t, out_dtype=torch.float32, vocab=vocab,
+                             tile_begin=tile_begin, tile_end=tile_end)
+    parts = _gather(dh.contiguous(), group)
+    return sum_f32(parts), dw
