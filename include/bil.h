@@ -416,9 +416,18 @@ int bil_linear_logp_fwd_static(const void *hidden, const void *weight, int dtype
  * before using it).  The LM-head kernel: 32 the epilogue's wait for an
  * accumulator, 64 the copy thread's wait for a free stage, 128 the MMA
  * thread's wait for a stage or a free accumulator, 256 a wait of either for
- * its own copies or MMAs to finish.
+ * its own copies or MMAs to finish.  512: bil_watchdog_selftest.
  */
 int bil_watchdog_status(unsigned int *flags, int clear);
+
+/*
+ * bil_watchdog_selftest -- queues one warp that waits, with the kernels'
+ * bounded wait, on a barrier that nothing ever arrives at.  After the wait
+ * limit (2 s) it sets bit 512 of the watchdog word and returns: the device
+ * stays usable and bil_watchdog_status reports the bit.  For tests of the
+ * failure detection; it takes the wait limit to run.
+ */
+int bil_watchdog_selftest(bil_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -33,6 +33,7 @@ SIGNATURES = {
     "bil_stream_shape": (_i32, [_i32, ctypes.c_int32, _i64, _i32, _i32, ctypes.POINTER(_i32),
                                 ctypes.POINTER(_i32), ctypes.POINTER(_i64)]),
     "bil_watchdog_status": (_i32, [ctypes.POINTER(_u), _i32]),
+    "bil_watchdog_selftest": (_i32, [_p]),
     "bil_linear_logp_partials": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, ctypes.c_int32,
                                         _f, _p, _i64, _p, _p, _p, _i64, _p, _p, _i32, _i64, _p]),
     "bil_linear_logp_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_i64)]),

@@ -459,6 +459,7 @@ constexpr unsigned kWatchEmpty = 2u;     // producer waited too long for a free 
 constexpr unsigned kWatchRowSlot = 4u;   // producer waited too long for a free row slot
 constexpr unsigned kWatchDrain = 8u;     // producer waited too long for its own copies
 constexpr unsigned kWatchProtocol = 16u; // a consumer met a unit outside the launch's ranges
+constexpr unsigned kWatchSelfTest = 512u; // the self-test's wait on a barrier nothing arrives at
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity, volatile int* abort,
                                           unsigned code) {
@@ -958,6 +959,20 @@ __global__ void __launch_bounds__(kSplitWarps * kLanes) split_row_kernel(const S
     if (p.lse != nullptr) p.lse[row] = L;
     if (ENT) p.entropy[row] = H;
   }
+}
+
+// One warp waits, with the kernels' own bounded wait, on an mbarrier that no
+// thread and no copy ever arrives at.  The wait runs out after its limit, sets
+// kWatchSelfTest in the watchdog word and returns; nothing faults or hangs.
+__global__ void __launch_bounds__(kLanes) watchdog_selftest_kernel() {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort = 0;
+  }
+  __syncthreads();
+  warp_wait(&bar, 0u, &abort, kWatchSelfTest);
 }
 
 // ---------------------------------------------------------------------------
@@ -1657,6 +1672,11 @@ int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, in
   *consumers = shape.consumers;
   *smem_bytes = static_cast<int64_t>(shape.smem);
   return BIL_OK;
+}
+
+int bil_watchdog_selftest(bil_stream_t stream) {
+  watchdog_selftest_kernel<<<1, kLanes, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
+  return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
 int bil_watchdog_status(unsigned int* flags, int clear) {

@@ -280,3 +280,31 @@ def test_repeat_runs_are_bitwise_identical():
         assert np.array_equal(f32_bits(r[0]), f32_bits(runs[0][0]))
         assert np.array_equal(f32_bits(r[1]), f32_bits(runs[0][1]))
         assert np.array_equal(host_bits(r[2]), host_bits(runs[0][2]))
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_device_stays_usable():
+    """Failure detection without a fault: a warp waits (bounded, as every wait in
+    the kernels is) on a barrier nothing arrives at; after the 2 s limit the
+    watchdog word holds its bit, the call returns, and the next forward gives
+    the same bits as before."""
+    import ctypes
+    import time
+
+    from invariant_token_log_gb300 import _lib
+    w = wl.random_rows(seed=9, n_rows=4, vocab=5000, dtype="bfloat16", tile_v=1024)
+    x = device_logits(w.logits, w.dtype)
+    t = torch.from_numpy(w.target_ids).cuda()
+    before = bil.logp_fwd(x, t, w.ignore_index, 1024)
+    torch.cuda.synchronize()
+    assert bil.watchdog_status(clear=True) == 0
+    t0 = time.time()
+    assert _lib.load().bil_watchdog_selftest(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+    torch.cuda.synchronize()
+    waited = time.time() - t0
+    assert bil.watchdog_status(clear=True) == 512
+    assert 1.5 <= waited <= 30.0, waited
+    after = bil.logp_fwd(x, t, w.ignore_index, 1024)
+    torch.cuda.synchronize()
+    assert bil.watchdog_status(clear=True) == 0
+    for a, b in zip(before, after):
+        assert np.array_equal(f32_bits(a), f32_bits(b))
