@@ -20,7 +20,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SOURCES = [os.path.join(HERE, "csrc", f) for f in ("bil.cu", "linear.cu")]
 HEADERS = [os.path.join(ROOT, "include", "bil.h")] + [
-    os.path.join(HERE, "csrc", f) for f in ("device_common.cuh", "internal.h")]
+    os.path.join(HERE, "csrc", f) for f in ("device_common.cuh", "logp_device.cuh", "internal.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "--fmad=false", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall"]

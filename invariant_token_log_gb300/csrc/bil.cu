@@ -1,4 +1,5 @@
-// Batch-invariant selected-token log-probability for sm_103a (GB300).
+// Batch-invariant selected-token log-probability for sm_103a (GB300): host side
+// of the logits path and its kernels' launches.
 //
 // Operator: "Batch-Invariant LogP" operator page, sections "Reference
 // Semantics" (what is computed), "Tensor Parallel" steps 1-6 (the fixed-tile
@@ -6,12 +7,15 @@
 // (one row's result depends on that row only; the backward recomputes the
 // softmax from the saved per-row LSE).  The C ABI is declared in include/bil.h.
 //
-// Kernels
+// Kernels (device code in logp_device.cuh)
 //   stream_kernel<FUSED=true>   forward: every tile of a row -> shared-memory
 //                               partials -> fixed-order merge -> logp, lse.
 //   stream_kernel<FUSED=false>  partials of a tile range -> [N, ld_part] buffers.
+//   split_row_kernel            forward of up to 128 rows, one row per cluster.
 //   merge_kernel                fixed-order merge of [N, T] partials -> logp, lse.
 //   bwd_kernel                  dlogits = g * (onehot - exp(x - lse)).
+// The single-pass forward-backward is in fwdbwd.cu, the fused LM-head in
+// linear.cu.
 //
 // The forward streams each row exactly once.  A producer warp moves whole
 // tiles HBM -> shared memory with 1-D bulk asynchronous copies
@@ -20,12 +24,13 @@
 // so no tensor cores are used: the forward is bound by HBM bandwidth, with
 // the exponential unit second.
 //
-// The arithmetic contract (what makes the bits reproducible) lives in
-// tile_reduce() and merge_lse() and nowhere else: every kernel that produces
-// a tile partial or an LSE calls them, so the fused and the split paths give
-// identical bits by construction.  All floating-point operations that matter
-// are written with explicit round-to-nearest intrinsics, and the file is
-// compiled with contraction off, so inlining cannot change them.
+// The arithmetic contract (what makes the bits reproducible) lives in the
+// tile reduction, merge_lse and the gradient formula of logp_device.cuh and
+// nowhere else: every kernel that produces a tile partial, an LSE or a
+// gradient calls them, so all paths give identical bits by construction.
+// All floating-point operations that matter are written with explicit
+// round-to-nearest or fused intrinsics, and the files are compiled with
+// contraction off.
 
 #include "../../include/bil.h"
 #include "device_common.cuh"
@@ -40,1192 +45,9 @@
 #include <algorithm>
 #include <cmath>
 
+#include "logp_device.cuh"
+
 namespace {
-
-// ---------------------------------------------------------------------------
-// The arithmetic contract.
-// ---------------------------------------------------------------------------
-
-constexpr int kGroup = 8;  // elements a lane takes at a time: 16 bytes of bf16/fp16
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-// Butterfly sum: every lane ends with the same value, because a + b == b + a
-// bitwise at every level.
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-template <int DT>
-struct Elem;
-
-template <>
-struct Elem<BIL_BF16> {
-  static constexpr int kBytes = 2;
-  static constexpr uint32_t kNegInf = 0xff80u;  // -inf bit pattern
-  __device__ static __forceinline__ float one(const unsigned char* p) {
-    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
-  }
-  // the two elements of a packed word, low half first (exact widening)
-  __device__ static __forceinline__ void pair(uint32_t w, float& lo, float& hi) {
-    lo = __uint_as_float(w << 16);
-    hi = __uint_as_float(w & 0xffff0000u);
-  }
-  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-  }
-};
-
-template <>
-struct Elem<BIL_F16> {
-  static constexpr int kBytes = 2;
-  static constexpr uint32_t kNegInf = 0xfc00u;
-  __device__ static __forceinline__ float one(const unsigned char* p) {
-    return __half2float(*reinterpret_cast<const __half*>(p));
-  }
-  __device__ static __forceinline__ void pair(uint32_t w, float& lo, float& hi) {
-    __half2 h = *reinterpret_cast<const __half2*>(&w);
-    const float2 f = __half22float2(h);
-    lo = f.x;
-    hi = f.y;
-  }
-  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-  }
-};
-
-template <>
-struct Elem<BIL_F32> {
-  static constexpr int kBytes = 4;
-  static constexpr uint32_t kNegInf = 0xff800000u;
-  __device__ static __forceinline__ float one(const unsigned char* p) {
-    return *reinterpret_cast<const float*>(p);
-  }
-};
-
-// Packed float32 pairs (sm_100 family): each half is an independent IEEE
-// round-to-nearest operation, bit for bit what __fadd_rn / __fsub_rn /
-// __fmul_rn give.  A pair is held as a 64-bit word, first element low.
-__device__ __forceinline__ uint64_t pk(float lo, float hi) {
-  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
-}
-__device__ __forceinline__ float lo_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a)); }
-__device__ __forceinline__ float hi_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a >> 32)); }
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-// contract_exp on both halves of a pair of exponents
-__device__ __forceinline__ uint64_t exp2_pair(uint64_t d) {
-  const uint64_t a = mul2(d, pk(kLog2e, kLog2e));
-  return pk(ex2_approx(lo_of(a)), ex2_approx(hi_of(a)));
-}
-
-// Temperature: the softmax sees z = x * rcp, rcp = 1/temperature rounded to
-// float32 on the host.  rcp = 1 leaves every value (and so every bit) as it is.
-//
-// Per-group building blocks of the tile reduction.  A group is 8 consecutive
-// elements = kW 32-bit words (4 for 16-bit types, 8 for float32).
-template <int DT>
-struct Group {
-  static constexpr int EB = Elem<DT>::kBytes;
-  static constexpr int kW = EB * kGroup / 4;
-  static constexpr int kVec = kW / 4;  // 16-byte vectors per group
-
-  __device__ static __forceinline__ void load(const unsigned char* p, uint32_t (&w)[kW]) {
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-      const uint4 q = *reinterpret_cast<const uint4*>(p + 16 * v);
-      w[4 * v] = q.x;
-      w[4 * v + 1] = q.y;
-      w[4 * v + 2] = q.z;
-      w[4 * v + 3] = q.w;
-    }
-  }
-  // elements j >= rem (past the vocabulary) become -inf: they cannot win the
-  // max and add exp(-inf) = +0 to the sums, i.e. leave them unchanged
-  __device__ static __forceinline__ void mask_tail(uint32_t (&w)[kW], int rem) {
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) {
-      if (j >= rem) {
-        if (EB == 4) {
-          w[j] = Elem<DT>::kNegInf;
-        } else if (j & 1) {
-          w[j / 2] = (w[j / 2] & 0x0000ffffu) | (Elem<DT>::kNegInf << 16);
-        } else {
-          w[j / 2] = (w[j / 2] & 0xffff0000u) | Elem<DT>::kNegInf;
-        }
-      }
-    }
-  }
-  // running max of the stored values: packed pairs for 16-bit types, one
-  // float per slot for float32
-  __device__ static __forceinline__ void max_init(uint32_t (&mx)[kW]) {
-#pragma unroll
-    for (int i = 0; i < kW; ++i) mx[i] = EB == 4 ? Elem<DT>::kNegInf : (Elem<DT>::kNegInf * 0x10001u);
-  }
-  __device__ static __forceinline__ void max_acc(uint32_t (&mx)[kW], const uint32_t (&w)[kW]) {
-#pragma unroll
-    for (int i = 0; i < kW; ++i) {
-      if constexpr (EB == 4) {
-        mx[i] = __float_as_uint(fmaxf(__uint_as_float(mx[i]), __uint_as_float(w[i])));
-      } else {
-        mx[i] = Elem<DT>::max2(mx[i], w[i]);
-      }
-    }
-  }
-  __device__ static __forceinline__ float max_fin(const uint32_t (&mx)[kW]) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kW; ++i) {
-      if constexpr (EB == 4) {
-        m = fmaxf(m, __uint_as_float(mx[i]));
-      } else {
-        float lo, hi;
-        Elem<DT>::pair(mx[i], lo, hi);
-        m = fmaxf(m, fmaxf(lo, hi));
-      }
-    }
-    return m;
-  }
-  // the pair of stored values at slots (2k, 2k+1), widened exactly
-  __device__ static __forceinline__ uint64_t xpair(const uint32_t (&w)[kW], int k) {
-    if constexpr (EB == 4) {
-      return static_cast<uint64_t>(w[2 * k]) | (static_cast<uint64_t>(w[2 * k + 1]) << 32);
-    } else {
-      float lo, hi;
-      Elem<DT>::pair(w[k], lo, hi);
-      return pk(lo, hi);
-    }
-  }
-  // a[k] holds the slot accumulators (a_2k, a_2k+1) of exp(d); with ENT,
-  // u[k] those of exp(d) * d; d = x - shift, times rcp when SCALED (the
-  // multiply comes last: no packed multiply here ever feeds an add, so the
-  // code generator has nothing to contract into a fused multiply-add)
-  template <bool SCALED, bool ENT>
-  __device__ static __forceinline__ void sum_acc(uint64_t (&a)[4], uint64_t (&u)[4], const uint32_t (&w)[kW],
-                                                 uint64_t shift2, uint64_t rcp2) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint64_t d = sub2(xpair(w, k), shift2);
-      if (SCALED) d = mul2(d, rcp2);
-      const uint64_t e = exp2_pair(d);
-      a[k] = add2(a[k], e);
-      // p log p -> 0 as p -> 0: an element with z = -inf (or one masked past
-      // the vocabulary) has e = 0 and d = -inf; clamping d to the largest
-      // finite magnitude makes its term 0 instead of 0 * inf.  Finite d are
-      // left as they are.
-      if (ENT) u[k] = fma2(e, pk(fmaxf(lo_of(d), kNegMax), fmaxf(hi_of(d), kNegMax)), u[k]);
-    }
-  }
-};
-
-// Groups lane `lane` holds of a tile of `valid` elements: g = lane + 32 i.
-__device__ __forceinline__ int lane_groups(int valid, int lane) {
-  const int groups = (valid + kGroup - 1) / kGroup;
-  return groups > lane ? (groups - lane + kLanes - 1) / kLanes : 0;
-}
-
-// One tile's float32 partial, computed by one warp: the max m of z, the sum
-// s of exp(z - m) and, when asked, the entropy sum u of exp(z - m) * (z - m).
-// The reduction order is fixed by the element positions alone:
-//   * element p of the tile (global column t*tile_v + p) sits in group
-//     g = p / 8 at slot j = p % 8; lane l takes groups l, l+32, l+64, ... in
-//     increasing order; `valid` elements exist (the rest are past the
-//     vocabulary and do not take part);
-//   * max: exact, so its order does not matter (NaN never wins); it is taken
-//     on the stored values, m_x, and the partial's max is m = m_x * rcp
-//     (the max of the scaled values, since x -> x * rcp (rcp > 0) rounds
-//     monotonically);
-//   * sums: d = (x - m_x) * rcp, each operation rounded (rcp = 1: d = x - m_x),
-//     which is z - m in real arithmetic; lane accumulator a_j (slot j) adds
-//     exp(d) for its groups in increasing order; the lane's sum is
-//     ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)); the warp's sum is the butterfly
-//     over lanes (xor 16, 8, 4, 2, 1); the entropy sum u follows the same
-//     tree with u_j = fma(exp(d), d, u_j);
-//   * a tile whose max is -inf shifts by 0 instead, so it sums to 0 (or NaN
-//     if it holds a NaN) and its max stays -inf.
-// Nothing here depends on the row, the kernel or the launch geometry.  Two
-// implementations follow, one reading a register copy of the lane's groups
-// (tiles of up to TileRegs::kMaxTile elements) and one reading shared memory
-// twice (larger tiles); they perform the same operations in the same order.
-struct TilePartial {
-  float m, s, u;
-};
-
-__device__ __forceinline__ float tree8(const uint64_t (&a)[4]) {
-  return __fadd_rn(__fadd_rn(__fadd_rn(lo_of(a[0]), hi_of(a[0])), __fadd_rn(lo_of(a[1]), hi_of(a[1]))),
-                   __fadd_rn(__fadd_rn(lo_of(a[2]), hi_of(a[2])), __fadd_rn(lo_of(a[3]), hi_of(a[3]))));
-}
-
-template <bool ENT>
-__device__ __forceinline__ TilePartial finish_tile(float m, const uint64_t (&a)[4], const uint64_t (&u)[4]) {
-  TilePartial r;
-  r.m = m;
-  r.s = warp_sum(tree8(a));
-  r.u = ENT ? warp_sum(tree8(u)) : 0.0f;
-  return r;
-}
-
-template <int DT>
-struct TileRegs {
-  static constexpr int kW = Group<DT>::kW;
-  static constexpr int kMaxGroups = 64 / kW;                     // 64 registers of tile data per lane
-  static constexpr int kMaxTile = kMaxGroups * kLanes * kGroup;  // 4096 (16-bit) / 2048 (float32)
-  uint32_t w[kMaxGroups][kW];
-};
-
-// FULL: the tile holds exactly TileRegs::kMaxTile valid elements, so every
-// lane has kMaxGroups whole groups and no test is needed per group.
-template <int DT, bool FULL>
-__device__ __forceinline__ void tile_load_regs_t(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r) {
-  constexpr int EB = Elem<DT>::kBytes;
-  const int ng = FULL ? TileRegs<DT>::kMaxGroups : lane_groups(valid, lane);
-  const int rem = valid % kGroup;
-  const int last = (valid - 1) / kGroup;  // index of the last group
-#pragma unroll
-  for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i) {
-    if (FULL || i < ng) {
-      const int g = lane + kLanes * i;
-      Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, r.w[i]);
-      if (!FULL && rem != 0 && g == last) Group<DT>::mask_tail(r.w[i], rem);
-    }
-  }
-}
-
-template <int DT, bool FULL, bool SCALED, bool ENT>
-__device__ __forceinline__ TilePartial tile_reduce_regs_t(const TileRegs<DT>& r, int valid, int lane, float rcp) {
-  const int ng = FULL ? TileRegs<DT>::kMaxGroups : lane_groups(valid, lane);
-  uint32_t mx[Group<DT>::kW];
-  Group<DT>::max_init(mx);
-#pragma unroll
-  for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i)
-    if (FULL || i < ng) Group<DT>::max_acc(mx, r.w[i]);
-  const float mx_all = warp_max(Group<DT>::max_fin(mx));
-  const float m = SCALED ? __fmul_rn(mx_all, rcp) : mx_all;
-  const float shift = (mx_all == -INFINITY) ? 0.0f : mx_all;  // in stored units
-  const uint64_t shift2 = pk(shift, shift), rcp2 = pk(rcp, rcp);
-  uint64_t a[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
-#pragma unroll
-  for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i)
-    if (FULL || i < ng) Group<DT>::template sum_acc<SCALED, ENT>(a, u, r.w[i], shift2, rcp2);
-  return finish_tile<ENT>(m, a, u);
-}
-
-template <int DT>
-__device__ __forceinline__ void tile_load_regs(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r) {
-  if (valid == TileRegs<DT>::kMaxTile) {
-    tile_load_regs_t<DT, true>(tile, valid, lane, r);
-  } else {
-    tile_load_regs_t<DT, false>(tile, valid, lane, r);
-  }
-}
-
-template <int DT, bool ENT>
-__device__ __forceinline__ TilePartial tile_reduce_regs(const TileRegs<DT>& r, int valid, int lane, float rcp) {
-  const bool full = valid == TileRegs<DT>::kMaxTile;
-  if (rcp == 1.0f) {
-    return full ? tile_reduce_regs_t<DT, true, false, ENT>(r, valid, lane, rcp)
-                : tile_reduce_regs_t<DT, false, false, ENT>(r, valid, lane, rcp);
-  }
-  return full ? tile_reduce_regs_t<DT, true, true, ENT>(r, valid, lane, rcp)
-              : tile_reduce_regs_t<DT, false, true, ENT>(r, valid, lane, rcp);
-}
-
-template <int DT, bool SCALED, bool ENT>
-__device__ __forceinline__ TilePartial tile_reduce_smem_t(const unsigned char* tile, int valid, int lane, float rcp) {
-  constexpr int EB = Elem<DT>::kBytes;
-  const int groups = (valid + kGroup - 1) / kGroup;
-  const int rem = valid % kGroup;
-  uint32_t mx[Group<DT>::kW];
-  Group<DT>::max_init(mx);
-  for (int g = lane; g < groups; g += kLanes) {
-    uint32_t w[Group<DT>::kW];
-    Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, w);
-    if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
-    Group<DT>::max_acc(mx, w);
-  }
-  const float mx_all = warp_max(Group<DT>::max_fin(mx));
-  const float m = SCALED ? __fmul_rn(mx_all, rcp) : mx_all;
-  const float shift = (mx_all == -INFINITY) ? 0.0f : mx_all;  // in stored units
-  const uint64_t shift2 = pk(shift, shift), rcp2 = pk(rcp, rcp);
-  uint64_t a[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
-  for (int g = lane; g < groups; g += kLanes) {
-    uint32_t w[Group<DT>::kW];
-    Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, w);
-    if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
-    Group<DT>::template sum_acc<SCALED, ENT>(a, u, w, shift2, rcp2);
-  }
-  return finish_tile<ENT>(m, a, u);
-}
-
-template <int DT, bool ENT>
-__device__ __forceinline__ TilePartial tile_reduce_smem(const unsigned char* tile, int valid, int lane, float rcp) {
-  return rcp == 1.0f ? tile_reduce_smem_t<DT, false, ENT>(tile, valid, lane, rcp)
-                     : tile_reduce_smem_t<DT, true, ENT>(tile, valid, lane, rcp);
-}
-
-// The fixed-order merge of one row's T tile partials, by one warp (all lanes
-// return the same values):
-//   M = max_t m_t;  w_t = exp(m_t - M);  S = fma(s_t, w_t, S) for t = 0, 1,
-//   ..., T-1 (one rounding per step, from S = 0);  LSE = M + log(S) (log:
-//   CUDA logf).
-// With ENT, also the entropy from the partial sums u_t (an exact rewrite of
-// -sum p log p, since log p = (z - m_t) + (m_t - M) - log S in tile t):
-//   v_t = fma(m_t - M, s_t, u_t);  U = fma(v_t, w_t, U) in the same order;
-//   H = log(S) - U / S.
-// M = -inf (no finite logit in the row) gives LSE = -inf, or NaN if a partial
-// sum is NaN, and H = NaN.  The exponentials are computed in parallel across
-// lanes; the chains of fused multiply-adds are the same sequential chains in
-// every lane.
-template <bool ENT>
-__device__ __forceinline__ float merge_lse(const float* m, const float* s, const float* u, int T, int lane,
-                                           float* entropy) {
-  float M = -INFINITY;
-  for (int t = lane; t < T; t += kLanes) M = fmaxf(M, m[t]);
-  M = warp_max(M);
-  if (M == -INFINITY) {
-    bool nan = false;
-    for (int t = lane; t < T; t += kLanes) nan |= isnan(s[t]);
-    if (ENT) *entropy = __int_as_float(0x7fc00000);
-    return __any_sync(0xffffffffu, nan) ? __int_as_float(0x7fc00000) : -INFINITY;
-  }
-  float S = 0.0f, U = 0.0f;
-  for (int t0 = 0; t0 < T; t0 += kLanes) {
-    const int t = t0 + lane;
-    float e = 0.0f, st = 0.0f, dm = 0.0f, ut = 0.0f;
-    if (t < T) {
-      dm = __fsub_rn(m[t], M);
-      e = contract_exp(dm);
-      st = s[t];
-      if (ENT) {
-        ut = u[t];
-        dm = fmaxf(dm, kNegMax);  // a tile of -inf (s_t = 0) then adds 0, not -inf * 0
-      }
-    }
-    const int n = min(kLanes, T - t0);
-    for (int j = 0; j < n; ++j) {
-      const float ej = __shfl_sync(0xffffffffu, e, j);
-      const float sj = __shfl_sync(0xffffffffu, st, j);
-      S = __fmaf_rn(sj, ej, S);
-      if (ENT) {
-        const float dmj = __shfl_sync(0xffffffffu, dm, j);
-        const float uj = __shfl_sync(0xffffffffu, ut, j);
-        U = __fmaf_rn(__fmaf_rn(dmj, sj, uj), ej, U);
-      }
-    }
-  }
-  const float logS = logf(S);
-  if (ENT) *entropy = __fsub_rn(logS, __fdiv_rn(U, S));
-  return __fadd_rn(M, logS);
-}
-
-// ---------------------------------------------------------------------------
-// Bounded waits.  Every wait polls a bounded number of times; one that runs
-// out records a bit in g_watchdog and reports failure so that the kernel can
-// stop instead of hanging.
-// ---------------------------------------------------------------------------
-
-__device__ unsigned int g_watchdog;
-
-constexpr unsigned kWatchFull = 1u;      // consumer waited too long for a tile
-constexpr unsigned kWatchEmpty = 2u;     // producer waited too long for a free stage
-constexpr unsigned kWatchRowSlot = 4u;   // producer waited too long for a free row slot
-constexpr unsigned kWatchDrain = 8u;     // producer waited too long for its own copies
-constexpr unsigned kWatchProtocol = 16u; // a consumer met a unit outside the launch's ranges
-constexpr unsigned kWatchSelfTest = 512u; // the self-test's wait on a barrier nothing arrives at
-
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity, volatile int* abort,
-                                          unsigned code) {
-  return warp_wait_watch(bar, parity, abort, code, &g_watchdog);
-}
-
-// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.  Both
-// addresses 16-byte aligned, bytes a multiple of 16.  The logits are read
-// once, so the copy asks L2 to evict them first.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-// ---------------------------------------------------------------------------
-// The streaming forward (fused) and tile-partials kernel.
-// ---------------------------------------------------------------------------
-
-// Blocks of one producer and up to seven consumer warps, two blocks per SM:
-// 16 warps at no more than 128 registers each fill an SM's register file.
-#ifndef BIL_STREAM_MAX_CONSUMERS
-#define BIL_STREAM_MAX_CONSUMERS 7
-#endif
-constexpr int kStreamThreads = 256;
-constexpr int kMaxConsumers = BIL_STREAM_MAX_CONSUMERS < kStreamThreads / 32 - 1 ? BIL_STREAM_MAX_CONSUMERS
-                                                                                  : kStreamThreads / 32 - 1;
-
-struct StreamParams {
-  const unsigned char* logits;  // column 0 = global column tile_begin * tile_v
-  int64_t n_rows, vocab, ld;    // ld in elements
-  int tile_v, tile_begin, tile_end, num_tiles;
-  const int64_t* targets;
-  int64_t ignore_index;
-  float rcp;  // 1 / temperature, rounded to float32 on the host
-  // fused outputs
-  float* logp;
-  float* lse;
-  float* entropy;  // with ENT
-  // partials outputs
-  float* part_max;
-  float* part_sum;
-  float* part_ent;  // with ENT
-  int64_t ld_part;
-  float* target_logit;
-  // pipeline shape
-  int stages, consumers, row_slots;
-  unsigned stage_bytes;
-};
-
-struct UnitDesc {
-  int64_t row;   // -1: no more units for this consumer
-  int32_t tile;  // global tile index
-  int32_t slot;  // fused: row slot
-};
-
-struct RowSlot {
-  int64_t row;
-  int64_t target;
-  float target_logit;
-  int done;  // tiles reduced so far
-};
-
-// Shared-memory layout (dynamic):
-//   [stages * stage_bytes]      tile ring, 128-byte aligned stages
-//   [stages] uint64 full, [stages] uint64 empty, [row_slots] uint64 row_free
-//   [stages] UnitDesc
-//   [row_slots] RowSlot, then [row_slots][num_tiles] float m, [row_slots][num_tiles] float s
-//   int abort
-struct Smem {
-  unsigned char* ring;
-  uint64_t* full;
-  uint64_t* empty;
-  uint64_t* row_free;
-  UnitDesc* desc;
-  RowSlot* slots;
-  float* slot_m;
-  float* slot_s;
-  float* slot_u;
-  int* abort;
-};
-
-__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-__host__ __device__ inline size_t stream_smem_bytes(int stages, unsigned stage_bytes, int row_slots,
-                                                    int num_tiles, bool fused, bool ent, Smem* out,
-                                                    unsigned char* base) {
-  const size_t slot_floats = fused ? static_cast<size_t>(row_slots) * num_tiles : 0;
-  size_t off = 0;
-  const size_t ring = off;
-  off += static_cast<size_t>(stages) * stage_bytes;
-  off = align_up(off, 8);
-  const size_t full = off;
-  off += sizeof(uint64_t) * stages;
-  const size_t empty = off;
-  off += sizeof(uint64_t) * stages;
-  const size_t row_free = off;
-  off += sizeof(uint64_t) * (fused ? row_slots : 0);
-  const size_t desc = off;
-  off += sizeof(UnitDesc) * stages;
-  const size_t slots = off;
-  off += sizeof(RowSlot) * (fused ? row_slots : 0);
-  const size_t sm = off;
-  off += sizeof(float) * slot_floats;
-  const size_t ss = off;
-  off += sizeof(float) * slot_floats;
-  const size_t su = off;
-  off += sizeof(float) * (ent ? slot_floats : 0);
-  const size_t ab = off;
-  off += sizeof(int);
-  if (out != nullptr) {
-    out->ring = base + ring;
-    out->full = reinterpret_cast<uint64_t*>(base + full);
-    out->empty = reinterpret_cast<uint64_t*>(base + empty);
-    out->row_free = reinterpret_cast<uint64_t*>(base + row_free);
-    out->desc = reinterpret_cast<UnitDesc*>(base + desc);
-    out->slots = reinterpret_cast<RowSlot*>(base + slots);
-    out->slot_m = reinterpret_cast<float*>(base + sm);
-    out->slot_s = reinterpret_cast<float*>(base + ss);
-    out->slot_u = reinterpret_cast<float*>(base + su);
-    out->abort = reinterpret_cast<int*>(base + ab);
-  }
-  return off;
-}
-
-// ENT: also the entropy partials (partials) or the entropy (fused).
-template <int DT, bool FUSED, bool BULK, bool ENT>
-__global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  constexpr int EB = Elem<DT>::kBytes;
-  Smem sm;
-  stream_smem_bytes(p.stages, p.stage_bytes, p.row_slots, p.num_tiles, FUSED, ENT, &sm, smem_raw);
-  const int warp = threadIdx.x / kLanes;
-  const int lane = threadIdx.x % kLanes;
-  const int S = p.stages;
-  const int W = p.consumers;
-  volatile int* abort = sm.abort;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
-    }
-    if (FUSED) {
-      for (int r = 0; r < p.row_slots; ++r) mbar_init(&sm.row_free[r], 1);
-    }
-    *abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-
-  const int tiles_here = p.tile_end - p.tile_begin;
-
-  if (warp == 0) {
-    // ---------------- producer warp ----------------
-    const uint64_t policy = evict_first_policy();
-    // The block's share of the work: whole rows (fused) or a contiguous range
-    // of (row, tile) units (partials).  Positions advance incrementally: no
-    // 64-bit division inside the loop.
-    int64_t u0, u1;
-    if (FUSED) {
-      u0 = p.n_rows * blockIdx.x / gridDim.x * tiles_here;
-      u1 = p.n_rows * (blockIdx.x + 1) / gridDim.x * tiles_here;
-    } else {
-      const int64_t total = p.n_rows * tiles_here;
-      u0 = total * blockIdx.x / gridDim.x;
-      u1 = total * (blockIdx.x + 1) / gridDim.x;
-    }
-    int64_t row = u0 / tiles_here;
-    int ti = static_cast<int>(u0 - row * tiles_here);  // tile within the range
-    int64_t left = u1 - u0;
-    int64_t k = 0;                 // units put in the ring
-    int stage = 0;                 // ring cursor: stage of unit k and its fill parity
-    unsigned phase = 0;
-    int slot = 0;                  // fused: row-slot cursor and its use parity
-    unsigned slot_phase = 0;
-    bool ok = true;
-    while (left > 0 && ok) {
-      const int64_t target = p.targets[row];
-      const int n = static_cast<int>(min(static_cast<int64_t>(tiles_here - ti), left));  // this row's units
-      if (target == p.ignore_index) {
-        // Inactive row: its logits are never read.
-        if (FUSED) {
-          if (lane == 0) {
-            p.logp[row] = 0.0f;
-            if (p.lse != nullptr) p.lse[row] = 0.0f;
-            if (ENT) p.entropy[row] = 0.0f;
-          }
-        } else {
-          for (int i = lane; i < n; i += kLanes) {
-            p.part_max[row * p.ld_part + p.tile_begin + ti + i] = -INFINITY;
-            p.part_sum[row * p.ld_part + p.tile_begin + ti + i] = 0.0f;
-            if (ENT) p.part_ent[row * p.ld_part + p.tile_begin + ti + i] = 0.0f;
-          }
-        }
-      } else {
-        if (FUSED) {
-          ok = warp_wait(&sm.row_free[slot], slot_phase ^ 1u, abort, kWatchRowSlot);
-          if (!ok) break;
-          if (lane == 0) {
-            RowSlot& rs = sm.slots[slot];
-            rs.row = row;
-            rs.target = target;
-            rs.target_logit = __int_as_float(0x7fc00000);
-            rs.done = 0;
-          }
-        }
-        const unsigned char* row_src = p.logits + row * p.ld * EB;
-        for (int i = 0; i < n; ++i) {
-          const int tile = p.tile_begin + ti + i;
-          ok = warp_wait(&sm.empty[stage], phase ^ 1u, abort, kWatchEmpty);
-          if (!ok) break;
-          const int64_t col0 = static_cast<int64_t>(tile) * p.tile_v;  // global column
-          const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
-          const unsigned char* src = row_src + static_cast<int64_t>(ti + i) * p.tile_v * EB;
-          unsigned char* dst = sm.ring + static_cast<size_t>(stage) * p.stage_bytes;
-          if (lane == 0) {
-            UnitDesc d;
-            d.row = row;
-            d.tile = tile;
-            d.slot = slot;
-            sm.desc[stage] = d;
-          }
-          if (BULK) {
-            if (lane == 0) {
-              const unsigned bytes = static_cast<unsigned>(align_up(static_cast<size_t>(valid) * EB, 16));
-              mbar_arrive_expect_tx(&sm.full[stage], bytes);
-              bulk_g2s(dst, src, bytes, &sm.full[stage], policy);
-            }
-          } else {
-            // Rows that are not 16-byte aligned: the producer warp copies the
-            // tile element by element into the same shared-memory layout.
-            for (int e = lane; e < valid; e += kLanes) {
-              if (EB == 2) {
-                reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(src)[e];
-              } else {
-                reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
-              }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.full[stage]);
-          }
-          __syncwarp();
-          ++k;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (FUSED && ++slot == p.row_slots) {
-          slot = 0;
-          slot_phase ^= 1u;
-        }
-      }
-      left -= n;
-      ++row;
-      ti = 0;
-    }
-    // One end marker per consumer warp: units k, k+1, ..., k+W-1 map to
-    // consumers k % W, ..., so each consumer sees exactly one.
-    for (int w = 0; w < W && ok; ++w) {
-      ok = warp_wait(&sm.empty[stage], phase ^ 1u, abort, kWatchEmpty);
-      if (!ok) break;
-      if (lane == 0) {
-        UnitDesc d;
-        d.row = -1;
-        d.tile = 0;
-        d.slot = 0;
-        sm.desc[stage] = d;
-        mbar_arrive(&sm.full[stage]);
-      }
-      __syncwarp();
-      ++k;
-      if (++stage == S) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-    // Drain: no bulk copy of ours may still be landing in shared memory when
-    // the block exits (consumers that gave up leave fills unconsumed).  The
-    // latest fill of every used stage must have completed; normally they all
-    // have and this costs one poll per stage.
-    if (BULK && lane == 0) {
-      for (int s = 0; s < S && s < k; ++s) {
-        const int64_t last = ((k - 1 - s) / S) * S + s;  // latest unit issued into stage s
-        const unsigned fill = static_cast<unsigned>(last / S);
-        const long long start = global_ns();
-        while (!mbar_try_wait(&sm.full[s], fill & 1u)) {
-          if (global_ns() - start > kWaitLimitNs) {
-            atomicOr(&g_watchdog, kWatchDrain);
-            break;
-          }
-        }
-      }
-    }
-    return;
-  }
-
-  // ---------------- consumer warps ----------------
-  // Consumer cw takes units cw, cw+W, cw+2W, ...: with S a multiple of W
-  // these sit in its own stages cw, cw+W, ... in fill order, and each step
-  // wraps the ring at most once.
-  const int cw = warp - 1;
-  int stage = cw;
-  unsigned phase = 0;
-  for (;; stage += W) {
-    if (stage >= S) {
-      stage -= S;
-      phase ^= 1u;
-    }
-    if (!warp_wait(&sm.full[stage], phase, abort, kWatchFull)) break;
-    const UnitDesc d = sm.desc[stage];
-    if (d.row < 0) break;
-    // A unit outside this launch's ranges can only come from a broken
-    // pipeline protocol: record it and stop rather than touch memory with it.
-    if (d.row >= p.n_rows || d.tile < p.tile_begin || d.tile >= p.tile_end ||
-        (FUSED && (d.slot < 0 || d.slot >= p.row_slots))) {
-      if (lane == 0) {
-        atomicOr(&g_watchdog, kWatchProtocol);
-        *abort = 1;
-      }
-      break;
-    }
-    const unsigned char* tile = sm.ring + static_cast<size_t>(stage) * p.stage_bytes;
-    const int64_t col0 = static_cast<int64_t>(d.tile) * p.tile_v;
-    const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
-    // The target logit is copied from the tile that owns it, never summed
-    // (scaled by the temperature exactly as the tile's values are).
-    const int64_t target = FUSED ? sm.slots[d.slot].target : p.targets[d.row];
-    const bool owner = target >= col0 && target < col0 + valid;
-    float tl = 0.0f;
-    if (owner) {
-      tl = Elem<DT>::one(tile + static_cast<size_t>(target - col0) * EB);
-      if (p.rcp != 1.0f) tl = __fmul_rn(tl, p.rcp);
-    }
-    TilePartial tp;
-    if (p.tile_v <= TileRegs<DT>::kMaxTile) {
-      // Copy the lane's groups to registers and hand the stage back to the
-      // producer at once, so that its next fill overlaps this reduction.
-      TileRegs<DT> regs;
-      tile_load_regs<DT>(tile, valid, lane, regs);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[stage]);
-      tp = tile_reduce_regs<DT, ENT>(regs, valid, lane, p.rcp);
-    } else {
-      tp = tile_reduce_smem<DT, ENT>(tile, valid, lane, p.rcp);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[stage]);  // the stage may be refilled now
-    }
-
-    if (!FUSED) {
-      if (lane == 0) {
-        p.part_max[d.row * p.ld_part + d.tile] = tp.m;
-        p.part_sum[d.row * p.ld_part + d.tile] = tp.s;
-        if (ENT) p.part_ent[d.row * p.ld_part + d.tile] = tp.u;
-        if (owner) p.target_logit[d.row] = tl;
-      }
-      continue;
-    }
-    RowSlot& rs = sm.slots[d.slot];
-    float* sm_m = sm.slot_m + static_cast<size_t>(d.slot) * p.num_tiles;
-    float* sm_s = sm.slot_s + static_cast<size_t>(d.slot) * p.num_tiles;
-    float* sm_u = sm.slot_u + static_cast<size_t>(d.slot) * p.num_tiles;
-    int before = 0;
-    if (lane == 0) {
-      sm_m[d.tile] = tp.m;
-      sm_s[d.tile] = tp.s;
-      if (ENT) sm_u[d.tile] = tp.u;
-      if (owner) rs.target_logit = tl;
-      __threadfence_block();
-      before = atomicAdd(&rs.done, 1);
-    }
-    before = __shfl_sync(0xffffffffu, before, 0);
-    if (before != p.num_tiles - 1) continue;
-    // This warp reduced the row's last tile: merge the row.
-    __threadfence_block();
-    __syncwarp();
-    float H = 0.0f;
-    const float L = merge_lse<ENT>(sm_m, sm_s, sm_u, p.num_tiles, lane, &H);
-    if (lane == 0) {
-      const int64_t row = rs.row;
-      const bool valid_target = rs.target >= 0 && rs.target < p.vocab;
-      p.logp[row] = valid_target ? __fsub_rn(rs.target_logit, L) : __int_as_float(0x7fc00000);
-      if (p.lse != nullptr) p.lse[row] = L;
-      if (ENT) p.entropy[row] = H;
-      __threadfence_block();
-      mbar_arrive(&sm.row_free[d.slot]);
-    }
-    __syncwarp();
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Small-batch forward: one row per thread-block cluster.
-//
-// With a handful of rows the streaming forward has one block per row, and one
-// SM streams the whole row.  Here a cluster of kSplitCtas blocks (on as many
-// SMs) shares each row: warp w of cluster rank c takes tiles c*kSplitWarps + w,
-// then + kSplitCtas*kSplitWarps, ...; each reduces its tile straight from
-// global memory with tile_load_regs / tile_reduce_regs (the same functions,
-// and so the same bits, as the streaming forward) and writes the partial into
-// the cluster's rank-0 block through distributed shared memory.  After one
-// cluster barrier the rank-0 block merges the row with merge_lse.  The bits
-// are those of the streaming forward; only the work split differs.  Used for
-// 16-bit types whose rows are 16-byte aligned, with tiles of at most
-// TileRegs::kMaxTile elements: a group of 8 elements is then one 16-byte unit
-// inside the row (the unit holding column vocab-1 ends before column ld).
-// ---------------------------------------------------------------------------
-
-constexpr int kSplitCtas = 8;   // blocks per cluster (the portable maximum)
-constexpr int kSplitWarps = 5;  // 40 warps per row: a 151936-column row in 4096-column tiles is 38 tiles
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// The shared::cluster address of `p` (a shared variable of this block) in the
-// block of cluster rank `rank`.
-__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void st_cluster(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-// Every thread of every block of the cluster arrives; the release / acquire
-// pair makes the distributed shared-memory stores before it visible after it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-template <int DT, bool ENT>
-__global__ void __launch_bounds__(kSplitWarps * kLanes) split_row_kernel(const StreamParams p) {
-  constexpr int EB = Elem<DT>::kBytes;
-  __shared__ float sm_m[BIL_MAX_FUSED_TILES];
-  __shared__ float sm_s[BIL_MAX_FUSED_TILES];
-  __shared__ float sm_u[ENT ? BIL_MAX_FUSED_TILES : 1];
-  __shared__ float sm_tl;
-  const uint32_t rank = cluster_ctarank();
-  const int64_t row = static_cast<int64_t>(blockIdx.x) / kSplitCtas;  // a cluster is kSplitCtas consecutive blocks
-  const int warp = threadIdx.x / kLanes;
-  const int lane = threadIdx.x % kLanes;
-  const int64_t target = row < p.n_rows ? p.targets[row] : p.ignore_index;
-  const bool active = row < p.n_rows && target != p.ignore_index;
-  if (rank == 0 && threadIdx.x == 0) sm_tl = __int_as_float(0x7fc00000);
-  cluster_sync_all();  // rank 0's initial value is in place before any block writes into it
-  if (active) {
-    const unsigned char* row_src = p.logits + row * p.ld * EB;
-    for (int t = static_cast<int>(rank) * kSplitWarps + warp; t < p.num_tiles; t += kSplitCtas * kSplitWarps) {
-      const int64_t col0 = static_cast<int64_t>(t) * p.tile_v;
-      const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
-      const unsigned char* tile = row_src + col0 * EB;
-      TileRegs<DT> regs;
-      tile_load_regs<DT>(tile, valid, lane, regs);
-      const TilePartial tp = tile_reduce_regs<DT, ENT>(regs, valid, lane, p.rcp);
-      if (lane == 0) {
-        st_cluster(cluster_addr(&sm_m[t], 0), tp.m);
-        st_cluster(cluster_addr(&sm_s[t], 0), tp.s);
-        if (ENT) st_cluster(cluster_addr(&sm_u[t], 0), tp.u);
-        if (target >= col0 && target < col0 + valid) {
-          float tl = Elem<DT>::one(tile + (target - col0) * EB);
-          if (p.rcp != 1.0f) tl = __fmul_rn(tl, p.rcp);
-          st_cluster(cluster_addr(&sm_tl, 0), tl);
-        }
-      }
-    }
-  }
-  cluster_sync_all();
-  if (rank != 0 || warp != 0 || row >= p.n_rows) return;
-  if (!active) {
-    if (lane == 0) {
-      p.logp[row] = 0.0f;
-      if (p.lse != nullptr) p.lse[row] = 0.0f;
-      if (ENT) p.entropy[row] = 0.0f;
-    }
-    return;
-  }
-  float H = 0.0f;
-  const float L = merge_lse<ENT>(sm_m, sm_s, sm_u, p.num_tiles, lane, &H);
-  if (lane == 0) {
-    const bool valid_target = target >= 0 && target < p.vocab;
-    p.logp[row] = valid_target ? __fsub_rn(sm_tl, L) : __int_as_float(0x7fc00000);
-    if (p.lse != nullptr) p.lse[row] = L;
-    if (ENT) p.entropy[row] = H;
-  }
-}
-
-// One warp waits, with the kernels' own bounded wait, on an mbarrier that no
-// thread and no copy ever arrives at.  The wait runs out after its limit, sets
-// kWatchSelfTest in the watchdog word and returns; nothing faults or hangs.
-__global__ void __launch_bounds__(kLanes) watchdog_selftest_kernel() {
-  __shared__ uint64_t bar;
-  __shared__ int abort;
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    abort = 0;
-  }
-  __syncthreads();
-  warp_wait(&bar, 0u, &abort, kWatchSelfTest);
-}
-
-// ---------------------------------------------------------------------------
-// Merge kernel: one warp per row, the same merge_lse as the fused forward.
-// ---------------------------------------------------------------------------
-
-template <bool ENT>
-__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ part_max,
-                                                    const float* __restrict__ part_sum,
-                                                    const float* __restrict__ part_ent, int64_t n_rows,
-                                                    int num_tiles, int64_t ld_part,
-                                                    const float* __restrict__ target_logit,
-                                                    const int64_t* __restrict__ targets,
-                                                    int64_t ignore_index, int64_t vocab, float* logp,
-                                                    float* lse, float* entropy) {
-  const int lane = threadIdx.x % kLanes;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / kLanes);
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / kLanes) + threadIdx.x / kLanes;
-       row < n_rows; row += warps) {
-    const int64_t t = targets[row];
-    if (t == ignore_index) {
-      if (lane == 0) {
-        logp[row] = 0.0f;
-        if (lse != nullptr) lse[row] = 0.0f;
-        if (ENT) entropy[row] = 0.0f;
-      }
-      continue;
-    }
-    float H = 0.0f;
-    const float L = merge_lse<ENT>(part_max + row * ld_part, part_sum + row * ld_part,
-                                   ENT ? part_ent + row * ld_part : nullptr, num_tiles, lane, &H);
-    if (lane == 0) {
-      const bool valid = t >= 0 && t < vocab;
-      logp[row] = valid ? __fsub_rn(target_logit[row], L) : __int_as_float(0x7fc00000);
-      if (lse != nullptr) lse[row] = L;
-      if (ENT) entropy[row] = H;
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Backward: dlogits[r, c] = g[r] * ([c == t_r] - exp(x[r, c] - lse[r])).
-// Work unit: (row, chunk of kBwdChunk columns), spread over a persistent grid.
-// Purely elementwise given lse and g, so the bits cannot depend on the unit
-// size, the grid, or whether a row is read in 16-byte vectors or one element
-// at a time.
-// ---------------------------------------------------------------------------
-
-#ifndef BIL_BWD_GROUPS
-#define BIL_BWD_GROUPS 4
-#endif
-constexpr int kBwdThreads = 256;
-constexpr int kBwdGroupsPerThread = BIL_BWD_GROUPS;  // 16-byte loads a thread has in flight per unit
-constexpr int kBwdChunk = kBwdThreads * kBwdGroupsPerThread * kGroup;  // 8192 columns per work unit
-
-template <int OT>
-struct Out;
-template <>
-struct Out<BIL_F32> {
-  static constexpr int kBytes = 4;
-  __device__ static __forceinline__ void store8(unsigned char* p, const float (&v)[kGroup]) {
-    float4* q = reinterpret_cast<float4*>(p);
-    __stcs(q, make_float4(v[0], v[1], v[2], v[3]));
-    __stcs(q + 1, make_float4(v[4], v[5], v[6], v[7]));
-  }
-  __device__ static __forceinline__ void store1(unsigned char* p, float v) {
-    *reinterpret_cast<float*>(p) = v;
-  }
-};
-template <>
-struct Out<BIL_BF16> {
-  static constexpr int kBytes = 2;
-  __device__ static __forceinline__ void store8(unsigned char* p, const float (&v)[kGroup]) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    __stcs(reinterpret_cast<uint4*>(p), make_uint4(w[0], w[1], w[2], w[3]));
-  }
-  __device__ static __forceinline__ void store1(unsigned char* p, float v) {
-    *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
-  }
-};
-template <>
-struct Out<BIL_F16> {
-  static constexpr int kBytes = 2;
-  __device__ static __forceinline__ void store8(unsigned char* p, const float (&v)[kGroup]) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    __stcs(reinterpret_cast<uint4*>(p), make_uint4(w[0], w[1], w[2], w[3]));
-  }
-  __device__ static __forceinline__ void store1(unsigned char* p, float v) {
-    *reinterpret_cast<__half*>(p) = __float2half_rn(v);
-  }
-};
-
-// A group of 8 gradient elements from its stored logits, with the same
-// operations as grad_elem in packed pairs.  `jt` is the target's slot in the
-// group, or -1 when the target lies elsewhere.
-template <int DT>
-__device__ __forceinline__ void grad_group(const uint32_t (&w)[Group<DT>::kW], const RowMeta& m, float rcp, bool ent,
-                                           int jt, float (&y)[kGroup]) {
-  const bool scaled = rcp != 1.0f;
-  const uint64_t L2 = pk(m.lse, m.lse), nL2 = pk(-m.lse, -m.lse), g2 = pk(m.g, m.g), rcp2 = pk(rcp, rcp);
-  const uint64_t gh2 = pk(m.gh, m.gh), H2 = pk(m.H, m.H);
-  constexpr uint64_t kSigns = 0x8000000080000000ull;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint64_t x = Group<DT>::xpair(w, k);
-    const uint64_t a = scaled ? fma2(x, rcp2, nL2) : sub2(x, L2);
-    const uint64_t p = exp2_pair(a);                  // (p_2k, p_2k+1)
-    uint64_t d;
-    uint64_t t3 = 0;
-    if (ent) {
-      const uint64_t ac = pk(fmaxf(lo_of(a), kNegMax), fmaxf(hi_of(a), kNegMax));
-      t3 = mul2(gh2, mul2(p, add2(ac, H2)));
-      d = fma2(g2, sub2(0, p), t3 ^ kSigns);          // g * (0 - p) - t3, one rounding
-    } else {
-      d = mul2(g2, sub2(0, p));                       // g * (0 - p)
-    }
-    if (scaled) d = mul2(d, rcp2);
-    y[2 * k] = lo_of(d);
-    y[2 * k + 1] = hi_of(d);
-    if (jt >= 0) {  // the one target column of the row: g * (1 - p), then as above
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (jt == 2 * k + h) {
-          const float ph = h ? hi_of(p) : lo_of(p);
-          const float th = h ? hi_of(t3) : lo_of(t3);
-          const float dt = ent ? __fmaf_rn(m.g, __fsub_rn(1.0f, ph), -th) : __fmul_rn(m.g, __fsub_rn(1.0f, ph));
-          y[2 * k + h] = scaled ? __fmul_rn(dt, rcp) : dt;
-        }
-      }
-    }
-  }
-}
-
-template <int DT>
-__device__ __forceinline__ void load_group_stream(const unsigned char* p, uint32_t (&w)[Group<DT>::kW]) {
-#pragma unroll
-  for (int v = 0; v < Group<DT>::kVec; ++v) {
-    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(p) + v);
-    w[4 * v] = q.x;
-    w[4 * v + 1] = q.y;
-    w[4 * v + 2] = q.z;
-    w[4 * v + 3] = q.w;
-  }
-}
-
-struct BwdParams {
-  const unsigned char* logits;
-  int64_t n_rows, vocab, ld;
-  const int64_t* targets;
-  int64_t ignore_index;
-  const float* lse;
-  const float* grad;
-  const float* entropy;       // with an entropy gradient: the forward's entropy
-  const float* grad_entropy;  // NULL: no entropy term
-  float rcp;
-  unsigned char* dlogits;
-  int64_t ld_out, out_cols;
-};
-
-__device__ __forceinline__ RowMeta row_meta(const BwdParams& bp, int64_t row) {
-  RowMeta m{0, 0.0f, 0.0f, 0.0f, 0.0f};
-  if (row < bp.n_rows) {
-    m.target = bp.targets[row];
-    m.lse = bp.lse[row];
-    m.g = bp.grad[row];
-    if (bp.grad_entropy != nullptr) {
-      m.H = bp.entropy[row];
-      m.gh = bp.grad_entropy[row];
-    }
-  }
-  return m;
-}
-
-template <int DT, int OT, bool VEC>
-__global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams bp) {
-  const unsigned char* __restrict__ logits = bp.logits;
-  const int64_t n_rows = bp.n_rows, vocab = bp.vocab, ld = bp.ld, ignore_index = bp.ignore_index;
-  unsigned char* __restrict__ dlogits = bp.dlogits;
-  const int64_t ld_out = bp.ld_out, out_cols = bp.out_cols;
-  const float rcp = bp.rcp;
-  const bool ent = bp.grad_entropy != nullptr;
-  constexpr int EB = Elem<DT>::kBytes;
-  constexpr int OB = Out<OT>::kBytes;
-  // Work unit u = row * chunks + chunk, units strided by the grid; (row,
-  // chunk) advance by a precomputed quotient and remainder.
-  const int64_t chunks = (out_cols + kBwdChunk - 1) / kBwdChunk;
-  const int64_t d_row = gridDim.x / chunks, d_chunk = gridDim.x % chunks;
-  int64_t row = blockIdx.x / chunks, chunk = blockIdx.x % chunks;
-  RowMeta meta = row_meta(bp, row);
-  while (row < n_rows) {
-    int64_t next_row = row + d_row, next_chunk = chunk + d_chunk;
-    if (next_chunk >= chunks) {
-      next_chunk -= chunks;
-      ++next_row;
-    }
-    const RowMeta next = row_meta(bp, next_row);  // in flight during this unit
-
-    const int64_t c0 = chunk * kBwdChunk;
-    const int64_t c1 = min(c0 + kBwdChunk, out_cols);
-    const int64_t t = meta.target;
-    unsigned char* out = dlogits + row * ld_out * OB;
-    const bool active = t != ignore_index;
-    const bool valid_target = t >= 0 && t < vocab;
-    const int64_t v1 = min(c1, vocab);  // [c0, v1): gradient; [max(c0, vocab), c1): pad
-    if (!active || !valid_target) {
-      const float fill = active ? __int_as_float(0x7fc00000) : 0.0f;
-      for (int64_t c = c0 + threadIdx.x; c < v1; c += kBwdThreads) Out<OT>::store1(out + c * OB, fill);
-    } else if (VEC) {
-      // c0 is a multiple of 8; groups fully inside [c0, v1) go by 16-byte
-      // vectors, all of a thread's loads issued before any arithmetic.
-      const unsigned char* in = logits + row * ld * EB;
-      const int64_t gend = c0 + ((v1 - c0) / kGroup) * kGroup;
-      uint32_t w[kBwdGroupsPerThread][Group<DT>::kW];
-#pragma unroll
-      for (int i = 0; i < kBwdGroupsPerThread; ++i) {
-        const int64_t c = c0 + (static_cast<int64_t>(i) * kBwdThreads + threadIdx.x) * kGroup;
-        if (c < gend) load_group_stream<DT>(in + c * EB, w[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < kBwdGroupsPerThread; ++i) {
-        const int64_t c = c0 + (static_cast<int64_t>(i) * kBwdThreads + threadIdx.x) * kGroup;
-        if (c < gend) {
-          const uint64_t off = static_cast<uint64_t>(t - c);
-          const int jt = off < static_cast<uint64_t>(kGroup) ? static_cast<int>(off) : -1;
-          float y[kGroup];
-          grad_group<DT>(w[i], meta, rcp, ent, jt, y);
-          Out<OT>::store8(out + c * OB, y);
-        }
-      }
-      for (int64_t c = gend + threadIdx.x; c < v1; c += kBwdThreads)
-        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta, c == t, rcp, ent));
-    } else {
-      const unsigned char* in = logits + row * ld * EB;
-      for (int64_t c = c0 + threadIdx.x; c < v1; c += kBwdThreads)
-        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta, c == t, rcp, ent));
-    }
-    for (int64_t c = max(c0, vocab) + threadIdx.x; c < c1; c += kBwdThreads) Out<OT>::store1(out + c * OB, 0.0f);
-    row = next_row;
-    chunk = next_chunk;
-    meta = next;
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
@@ -1448,6 +270,12 @@ int check_targets_host(const int64_t* targets, int64_t n, int64_t ignore_index, 
 }
 
 int temperature_rcp(float temperature, float* rcp) { return ::temperature_rcp(temperature, rcp); }
+
+int elem_bytes(int dtype) { return ::elem_bytes(dtype); }
+
+int check_tile(int dtype, int64_t vocab, int32_t tile_v, int64_t* num_tiles) {
+  return ::check_tile(dtype, vocab, tile_v, num_tiles);
+}
 
 int device_limits(int* sms, int* max_smem_optin) {
   DeviceInfo dev;

@@ -24,6 +24,13 @@ BIL_INTERNAL int temperature_rcp(float temperature, float* rcp);
 // device (cached per device).
 BIL_INTERNAL int device_limits(int* sms, int* max_smem_optin);
 
+// Bytes of one element of a BIL_* type (0 for an unknown type).
+BIL_INTERNAL int elem_bytes(int dtype);
+
+// num_tiles = ceil(vocab / tile_v) after checking tile_v (a positive multiple
+// of 8 of at most BIL_MAX_TILE_BYTES bytes) and the element type.
+BIL_INTERNAL int check_tile(int dtype, int64_t vocab, int32_t tile_v, int64_t* num_tiles);
+
 // The LM-head kernels' watchdog word of the current device (see
 // bil_watchdog_status); cleared when `clear` is non-zero.
 BIL_INTERNAL int linear_watchdog(unsigned int* flags, int clear);
