@@ -49,7 +49,7 @@ WORKLOAD = ("training: N=16384 rows (B=8 x T=2048), V=151936 bf16 logits ~ 3*ran
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
-KERNEL_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "bil.cu")
+KERNEL_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "logp_device.cuh")
 LINEAR_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "linear.cu")
 LINEAR_METRIC = ("fused LM-head + logp fwd+bwd rows/s and achieved TFLOP/s (% of GB300 dense bf16) at H=4096, "
                  "V=151936")

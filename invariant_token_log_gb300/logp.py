@@ -276,4 +276,3 @@ def watchdog_status(clear: bool = True) -> int:
     flags = ctypes.c_uint(0)
     _lib.check("bil_watchdog_status", _lib.load().bil_watchdog_status(ctypes.byref(flags), int(clear)))
     return int(flags.value)
-
