@@ -10,16 +10,27 @@
 // the tiles are then merged in the operator's one fixed order (the library's
 // merge kernel).  The C ABI is declared in include/bil.h.
 //
-// One kernel, persistent, one block per SM, warp-specialised:
-//   warp 0      TMA producer: 128-row hidden tile and 256-row weight tile per
-//               64-element K block, 128-byte swizzled, into a 4-stage ring;
+// One GEMM body C = A . B^T (both operands K-major, 16-bit), persistent, one
+// block per SM, warp-specialised:
+//   warp 0      TMA producer: 128-row A tile and 256-row B tile per 64-element
+//               K block, 128-byte swizzled, into a 4-stage ring;
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16/fp16 in, fp32
 //               accumulate in tensor memory), K blocks in increasing order,
 //               four K=16 steps each; two accumulator buffers of 256 columns;
 //   warps 2-5   epilogue: thread i of the warp reading lanes [32q, 32q+32)
-//               owns row 32q+i of the tile and reduces its 256 columns from
-//               tensor memory into the tile's partial.
-// The accumulator of one tile is read while the next tile's MMAs run.
+//               owns row 32q+i of the tile and reads its 256 columns from
+//               tensor memory.
+// The accumulator of one tile is read while the next tile's MMAs run.  Three
+// epilogues make three kernels:
+//   linear_partials_kernel   forward: A = hidden, B = weight; the tile's
+//                            partial of the operator (and, optionally, the
+//                            logits);
+//   linear_grad_kernel       backward: the same projection recomputed; dZ by
+//                            the logits path's gradient formula, stored as
+//                            [rows, vocab] and [vocab, rows];
+//   linear_store_kernel      backward: dhidden = dZ . W (B = the prepared W^T)
+//                            and dweight = dZ^T . hidden (B = hidden^T),
+//                            stored as they are.
 //
 // What fixes the bits of z[r, c] is the K order (K blocks in order, four
 // K=16 steps each, from a zeroed accumulator), the same for every row and
