@@ -206,9 +206,10 @@ int bil_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64_t vocab, i
  * with num_tiles tiles per row; entropy != 0: with the entropy output): the
  * number of shared-memory stages in each
  * block's ring, the number of consumer warps, and the block's dynamic shared
- * memory in bytes.  Host arithmetic only; touches no device.  The stage count
- * is always a multiple of the consumer count (each consumer warp owns its
- * stages and meets them in fill order).
+ * memory in bytes, for rows whose tiles start on 16-byte boundaries (when
+ * they do not, each stage holds 128 bytes more).  Host arithmetic only;
+ * touches no device.  The stage count is always a multiple of the consumer
+ * count (each consumer warp owns its stages and meets them in fill order).
  */
 int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, int entropy,
                      int *stages, int *consumers, int64_t *smem_bytes);

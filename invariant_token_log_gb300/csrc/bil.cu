@@ -14,13 +14,14 @@
 //   split_row_kernel            forward of up to 128 rows, one row per cluster.
 //   merge_kernel                fixed-order merge of [N, T] partials -> logp, lse.
 //   bwd_kernel                  dlogits = g * (onehot - exp(x - lse)).
-// The single-pass forward-backward is in fwdbwd.cu, the fused LM-head in
-// linear.cu.
+// The fused LM-head is in linear.cu.
 //
 // The forward streams each row exactly once.  A producer warp moves whole
 // tiles HBM -> shared memory with 1-D bulk asynchronous copies
 // (cp.async.bulk, completion counted on an mbarrier) into a ring of stages;
-// consumer warps reduce one tile each.  Nothing on this path is a contraction,
+// consumer warps reduce one tile each.  Rows that do not start on a 16-byte
+// boundary are copied from the boundary below each tile, and the consumers
+// shift the tile's words back into place as they read them.  Nothing on this path is a contraction,
 // so no tensor cores are used: the forward is bound by HBM bandwidth, with
 // the exponential unit second.
 //
@@ -131,7 +132,7 @@ StreamShape stream_shape(unsigned stage_bytes, int num_tiles, bool fused, bool e
   return s;
 }
 
-template <int DT, bool FUSED, bool BULK, bool ENT>
+template <int DT, bool FUSED, bool ALIGNED, bool ENT>
 int launch_stream_t(const StreamParams& p0, cudaStream_t stream) {
   DeviceInfo dev;
   if (int st = device_info(&dev)) return st;
@@ -142,7 +143,7 @@ int launch_stream_t(const StreamParams& p0, cudaStream_t stream) {
   p.stages = shape.stages;
   p.consumers = shape.consumers;
   p.row_slots = shape.row_slots;
-  auto kernel = stream_kernel<DT, FUSED, BULK, ENT>;
+  auto kernel = stream_kernel<DT, FUSED, ALIGNED, ENT>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(shape.smem)) != cudaSuccess)
     return BIL_E_CUDA;
@@ -159,19 +160,26 @@ int launch_stream_t(const StreamParams& p0, cudaStream_t stream) {
 }
 
 template <int DT, bool FUSED>
-int launch_stream_dt(bool bulk, bool ent, const StreamParams& p, cudaStream_t stream) {
-  if (ent) return bulk ? launch_stream_t<DT, FUSED, true, true>(p, stream) : launch_stream_t<DT, FUSED, false, true>(p, stream);
-  return bulk ? launch_stream_t<DT, FUSED, true, false>(p, stream) : launch_stream_t<DT, FUSED, false, false>(p, stream);
+int launch_stream_dt(bool aligned_rows, bool ent, const StreamParams& p, cudaStream_t stream) {
+  if (ent)
+    return aligned_rows ? launch_stream_t<DT, FUSED, true, true>(p, stream)
+                        : launch_stream_t<DT, FUSED, false, true>(p, stream);
+  return aligned_rows ? launch_stream_t<DT, FUSED, true, false>(p, stream)
+                      : launch_stream_t<DT, FUSED, false, false>(p, stream);
 }
 
 template <bool FUSED>
-int launch_stream(int dtype, bool ent, const StreamParams& p, cudaStream_t stream) {
+int launch_stream(int dtype, bool ent, const StreamParams& p0, cudaStream_t stream) {
   const int eb = elem_bytes(dtype);
-  const bool bulk = aligned(p.logits, 16) && (p.ld * eb) % 16 == 0;
+  // Every tile starts 16-byte aligned, or the copies start up to 15 bytes
+  // early and a stage holds 128 bytes more than the tile.
+  const bool aligned_rows = aligned(p0.logits, 16) && (p0.ld * eb) % 16 == 0;
+  StreamParams p = p0;
+  p.stage_bytes = static_cast<unsigned>(static_cast<size_t>(p.tile_v) * eb + (aligned_rows ? 0 : 128));
   switch (dtype) {
-    case BIL_BF16: return launch_stream_dt<BIL_BF16, FUSED>(bulk, ent, p, stream);
-    case BIL_F16: return launch_stream_dt<BIL_F16, FUSED>(bulk, ent, p, stream);
-    case BIL_F32: return launch_stream_dt<BIL_F32, FUSED>(bulk, ent, p, stream);
+    case BIL_BF16: return launch_stream_dt<BIL_BF16, FUSED>(aligned_rows, ent, p, stream);
+    case BIL_F16: return launch_stream_dt<BIL_F16, FUSED>(aligned_rows, ent, p, stream);
+    case BIL_F32: return launch_stream_dt<BIL_F32, FUSED>(aligned_rows, ent, p, stream);
     default: return BIL_E_DTYPE;
   }
 }
@@ -359,7 +367,6 @@ int bil_logp_fwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
   p.logp = logp;
   p.lse = lse;
   p.entropy = entropy;
-  p.stage_bytes = static_cast<unsigned>(static_cast<size_t>(tile_v) * eb);
   if (use_split(dtype, p)) return launch_split(dtype, entropy != nullptr, p, s);
   return launch_stream<true>(dtype, entropy != nullptr, p, s);
 }
@@ -404,7 +411,6 @@ int bil_logp_tile_partials(const void* logits, int dtype, int64_t n_rows, int64_
   p.part_ent = part_ent;
   p.ld_part = ld_part;
   p.target_logit = target_logit;
-  p.stage_bytes = static_cast<unsigned>(static_cast<size_t>(tile_v) * eb);
   return launch_stream<false>(dtype, part_ent != nullptr, p, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -143,6 +143,25 @@ struct Group {
       w[4 * v + 3] = q.w;
     }
   }
+  // The group whose first element sits `off` bytes past the 16-byte aligned
+  // address p (0 <= off < 16, a multiple of the element size): the kVec + 1
+  // aligned vectors from p are read whole and the group's words taken out of
+  // them, WOFF = off / 4 words in and then sh = 8 * (off % 4) bits down.
+  // The words are those `load` reads from a 16-byte aligned copy of the group.
+  template <int WOFF>
+  __device__ static __forceinline__ void load_shifted(const unsigned char* p, unsigned sh, uint32_t (&w)[kW]) {
+    uint32_t v[4 * (kVec + 1)];
+#pragma unroll
+    for (int q = 0; q <= kVec; ++q) {
+      const uint4 x = *reinterpret_cast<const uint4*>(p + 16 * q);
+      v[4 * q] = x.x;
+      v[4 * q + 1] = x.y;
+      v[4 * q + 2] = x.z;
+      v[4 * q + 3] = x.w;
+    }
+#pragma unroll
+    for (int j = 0; j < kW; ++j) w[j] = __funnelshift_r(v[j + WOFF], v[j + WOFF + 1], sh);
+  }
   // elements j >= rem (past the vocabulary) become -inf: they cannot win the
   // max and add exp(-inf) = +0 to the sums, i.e. leave them unchanged
   __device__ static __forceinline__ void mask_tail(uint32_t (&w)[kW], int rem) {
@@ -276,11 +295,28 @@ struct TileRegs {
   uint32_t w[kMaxGroups][kW];
 };
 
+// Group g of a tile held in memory from `tile` on.  WOFF < 0: the tile starts
+// at `tile`, which is 16-byte aligned.  WOFF >= 0: `tile` is the 16-byte
+// boundary below the tile's first element, which sits off = 4 * WOFF + sh / 8
+// bytes past it (the memory from `tile` up to the 16-byte boundary after the
+// group must be readable; bytes outside the tile only reach masked slots).
+template <int DT, int WOFF>
+__device__ __forceinline__ void load_group(const unsigned char* tile, int g, unsigned sh,
+                                           uint32_t (&w)[Group<DT>::kW]) {
+  const unsigned char* p = tile + static_cast<size_t>(g) * kGroup * Elem<DT>::kBytes;
+  if constexpr (WOFF < 0) {
+    Group<DT>::load(p, w);
+  } else {
+    Group<DT>::template load_shifted<WOFF>(p, sh, w);
+  }
+}
+
 // FULL: the tile holds exactly TileRegs::kMaxTile valid elements, so every
-// lane has kMaxGroups whole groups and no test is needed per group.
-template <int DT, bool FULL>
-__device__ __forceinline__ void tile_load_regs_t(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r) {
-  constexpr int EB = Elem<DT>::kBytes;
+// lane has kMaxGroups whole groups and no test is needed per group.  WOFF, sh:
+// as for load_group.
+template <int DT, bool FULL, int WOFF = -1>
+__device__ __forceinline__ void tile_load_regs_t(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r,
+                                                 unsigned sh = 0) {
   const int ng = FULL ? TileRegs<DT>::kMaxGroups : lane_groups(valid, lane);
   const int rem = valid % kGroup;
   const int last = (valid - 1) / kGroup;  // index of the last group
@@ -288,7 +324,7 @@ __device__ __forceinline__ void tile_load_regs_t(const unsigned char* tile, int 
   for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i) {
     if (FULL || i < ng) {
       const int g = lane + kLanes * i;
-      Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, r.w[i]);
+      load_group<DT, WOFF>(tile, g, sh, r.w[i]);
       if (!FULL && rem != 0 && g == last) Group<DT>::mask_tail(r.w[i], rem);
     }
   }
@@ -313,12 +349,28 @@ __device__ __forceinline__ TilePartial tile_reduce_regs_t(const TileRegs<DT>& r,
   return finish_tile<ENT>(m, a, u);
 }
 
-template <int DT>
-__device__ __forceinline__ void tile_load_regs(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r) {
+template <int DT, int WOFF>
+__device__ __forceinline__ void tile_load_regs_w(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r,
+                                                 unsigned sh) {
   if (valid == TileRegs<DT>::kMaxTile) {
-    tile_load_regs_t<DT, true>(tile, valid, lane, r);
+    tile_load_regs_t<DT, true, WOFF>(tile, valid, lane, r, sh);
   } else {
-    tile_load_regs_t<DT, false>(tile, valid, lane, r);
+    tile_load_regs_t<DT, false, WOFF>(tile, valid, lane, r, sh);
+  }
+}
+
+// The lane's groups of a tile whose first element sits `off` bytes past the
+// 16-byte aligned address `tile` (SHIFTED = false: off is 0).
+template <int DT, bool SHIFTED = false>
+__device__ __forceinline__ void tile_load_regs(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r,
+                                               unsigned off = 0) {
+  const unsigned sh = 8u * (off & 3u);
+  if (!SHIFTED || off == 0) return tile_load_regs_w<DT, -1>(tile, valid, lane, r, 0);
+  switch (off >> 2) {
+    case 0: return tile_load_regs_w<DT, 0>(tile, valid, lane, r, sh);
+    case 1: return tile_load_regs_w<DT, 1>(tile, valid, lane, r, sh);
+    case 2: return tile_load_regs_w<DT, 2>(tile, valid, lane, r, sh);
+    default: return tile_load_regs_w<DT, 3>(tile, valid, lane, r, sh);
   }
 }
 
@@ -333,16 +385,16 @@ __device__ __forceinline__ TilePartial tile_reduce_regs(const TileRegs<DT>& r, i
               : tile_reduce_regs_t<DT, false, true, ENT>(r, valid, lane, rcp);
 }
 
-template <int DT, bool SCALED, bool ENT>
-__device__ __forceinline__ TilePartial tile_reduce_smem_t(const unsigned char* tile, int valid, int lane, float rcp) {
-  constexpr int EB = Elem<DT>::kBytes;
+template <int DT, bool SCALED, bool ENT, int WOFF>
+__device__ __forceinline__ TilePartial tile_reduce_smem_t(const unsigned char* tile, int valid, int lane, float rcp,
+                                                          unsigned sh) {
   const int groups = (valid + kGroup - 1) / kGroup;
   const int rem = valid % kGroup;
   uint32_t mx[Group<DT>::kW];
   Group<DT>::max_init(mx);
   for (int g = lane; g < groups; g += kLanes) {
     uint32_t w[Group<DT>::kW];
-    Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, w);
+    load_group<DT, WOFF>(tile, g, sh, w);
     if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
     Group<DT>::max_acc(mx, w);
   }
@@ -353,17 +405,32 @@ __device__ __forceinline__ TilePartial tile_reduce_smem_t(const unsigned char* t
   uint64_t a[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
   for (int g = lane; g < groups; g += kLanes) {
     uint32_t w[Group<DT>::kW];
-    Group<DT>::load(tile + static_cast<size_t>(g) * kGroup * EB, w);
+    load_group<DT, WOFF>(tile, g, sh, w);
     if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
     Group<DT>::template sum_acc<SCALED, ENT>(a, u, w, shift2, rcp2);
   }
   return finish_tile<ENT>(m, a, u);
 }
 
-template <int DT, bool ENT>
-__device__ __forceinline__ TilePartial tile_reduce_smem(const unsigned char* tile, int valid, int lane, float rcp) {
-  return rcp == 1.0f ? tile_reduce_smem_t<DT, false, ENT>(tile, valid, lane, rcp)
-                     : tile_reduce_smem_t<DT, true, ENT>(tile, valid, lane, rcp);
+template <int DT, bool ENT, int WOFF>
+__device__ __forceinline__ TilePartial tile_reduce_smem_w(const unsigned char* tile, int valid, int lane, float rcp,
+                                                          unsigned sh) {
+  return rcp == 1.0f ? tile_reduce_smem_t<DT, false, ENT, WOFF>(tile, valid, lane, rcp, sh)
+                     : tile_reduce_smem_t<DT, true, ENT, WOFF>(tile, valid, lane, rcp, sh);
+}
+
+// off, SHIFTED: as for tile_load_regs.
+template <int DT, bool ENT, bool SHIFTED = false>
+__device__ __forceinline__ TilePartial tile_reduce_smem(const unsigned char* tile, int valid, int lane, float rcp,
+                                                        unsigned off = 0) {
+  const unsigned sh = 8u * (off & 3u);
+  if (!SHIFTED || off == 0) return tile_reduce_smem_w<DT, ENT, -1>(tile, valid, lane, rcp, 0);
+  switch (off >> 2) {
+    case 0: return tile_reduce_smem_w<DT, ENT, 0>(tile, valid, lane, rcp, sh);
+    case 1: return tile_reduce_smem_w<DT, ENT, 1>(tile, valid, lane, rcp, sh);
+    case 2: return tile_reduce_smem_w<DT, ENT, 2>(tile, valid, lane, rcp, sh);
+    default: return tile_reduce_smem_w<DT, ENT, 3>(tile, valid, lane, rcp, sh);
+  }
 }
 
 // The fixed-order merge of one row's T tile partials, by one warp (all lanes
@@ -570,7 +637,7 @@ __host__ __device__ inline size_t stream_smem_bytes(int stages, unsigned stage_b
 }
 
 // ENT: also the entropy partials (partials) or the entropy (fused).
-template <int DT, bool FUSED, bool BULK, bool ENT>
+template <int DT, bool FUSED, bool ALIGNED, bool ENT>
 __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   constexpr int EB = Elem<DT>::kBytes;
@@ -659,6 +726,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
           const int64_t col0 = static_cast<int64_t>(tile) * p.tile_v;  // global column
           const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
           const unsigned char* src = row_src + static_cast<int64_t>(ti + i) * p.tile_v * EB;
+          const unsigned off = ALIGNED ? 0u : static_cast<unsigned>(reinterpret_cast<uintptr_t>(src) & 15u);
           unsigned char* dst = sm.ring + static_cast<size_t>(stage) * p.stage_bytes;
           if (lane == 0) {
             UnitDesc d;
@@ -667,24 +735,15 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
             d.slot = slot;
             sm.desc[stage] = d;
           }
-          if (BULK) {
-            if (lane == 0) {
-              const unsigned bytes = static_cast<unsigned>(align_up(static_cast<size_t>(valid) * EB, 16));
-              mbar_arrive_expect_tx(&sm.full[stage], bytes);
-              bulk_g2s(dst, src, bytes, &sm.full[stage], policy);
-            }
-          } else {
-            // Rows that are not 16-byte aligned: the producer warp copies the
-            // tile element by element into the same shared-memory layout.
-            for (int e = lane; e < valid; e += kLanes) {
-              if (EB == 2) {
-                reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(src)[e];
-              } else {
-                reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
-              }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.full[stage]);
+          // One bulk copy of the 16-byte aligned span that covers the tile: it
+          // starts off bytes before the tile's first element (rows that are
+          // not 16-byte aligned) and every 16 bytes of it hold an element of
+          // the tile, so it reads no page the tile does not touch.  The stage
+          // holds tile_v elements plus 128 bytes when rows are not aligned.
+          if (lane == 0) {
+            const unsigned bytes = static_cast<unsigned>(align_up(off + static_cast<size_t>(valid) * EB, 16));
+            mbar_arrive_expect_tx(&sm.full[stage], bytes);
+            bulk_g2s(dst, src - off, bytes, &sm.full[stage], policy);
           }
           __syncwarp();
           ++k;
@@ -726,7 +785,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
     // the block exits (consumers that gave up leave fills unconsumed).  The
     // latest fill of every used stage must have completed; normally they all
     // have and this costs one poll per stage.
-    if (BULK && lane == 0) {
+    if (lane == 0) {
       for (int s = 0; s < S && s < k; ++s) {
         const int64_t last = ((k - 1 - s) / S) * S + s;  // latest unit issued into stage s
         const unsigned fill = static_cast<unsigned>(last / S);
@@ -770,13 +829,19 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
     const unsigned char* tile = sm.ring + static_cast<size_t>(stage) * p.stage_bytes;
     const int64_t col0 = static_cast<int64_t>(d.tile) * p.tile_v;
     const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
+    // where the producer's copy put the tile's first element (its source address mod 16)
+    const unsigned off =
+        ALIGNED ? 0u
+                : static_cast<unsigned>((reinterpret_cast<uintptr_t>(p.logits) +
+                                         static_cast<uint64_t>(d.row) * p.ld * EB +
+                                         static_cast<uint64_t>(d.tile - p.tile_begin) * p.tile_v * EB) & 15u);
     // The target logit is copied from the tile that owns it, never summed
     // (scaled by the temperature exactly as the tile's values are).
     const int64_t target = FUSED ? sm.slots[d.slot].target : p.targets[d.row];
     const bool owner = target >= col0 && target < col0 + valid;
     float tl = 0.0f;
     if (owner) {
-      tl = Elem<DT>::one(tile + static_cast<size_t>(target - col0) * EB);
+      tl = Elem<DT>::one(tile + off + static_cast<size_t>(target - col0) * EB);
       if (p.rcp != 1.0f) tl = __fmul_rn(tl, p.rcp);
     }
     TilePartial tp;
@@ -784,12 +849,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
       // Copy the lane's groups to registers and hand the stage back to the
       // producer at once, so that its next fill overlaps this reduction.
       TileRegs<DT> regs;
-      tile_load_regs<DT>(tile, valid, lane, regs);
+      tile_load_regs<DT, !ALIGNED>(tile, valid, lane, regs, off);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[stage]);
       tp = tile_reduce_regs<DT, ENT>(regs, valid, lane, p.rcp);
     } else {
-      tp = tile_reduce_smem<DT, ENT>(tile, valid, lane, p.rcp);
+      tp = tile_reduce_smem<DT, ENT, !ALIGNED>(tile, valid, lane, p.rcp, off);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[stage]);  // the stage may be refilled now
     }
