@@ -106,3 +106,37 @@ def test_unaligned_rows_match_the_oracle():
     torch.cuda.synchronize()
     assert_close_abs(logp.cpu().numpy(), ref_logp, LOGP_ATOL, "logp")
     assert_close_abs(lse.cpu().numpy(), ref_lse, LOGP_ATOL, "lse")
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shift", [0, 3])
+def test_unaligned_backward_gives_the_aligned_bits(dtype, out_dtype, shift):
+    """The backward on rows with an odd pitch and a shifted base, writing
+    output rows at another odd pitch and offset than the input's (so the two
+    start at different offsets), two pad columns past the vocabulary, with a
+    temperature and the entropy term."""
+    n = 29
+    w = wl.random_rows(seed=64, n_rows=n, vocab=VOCAB, ld=VOCAB + 2, dtype=dtype, tile_v=4096, ignore_every=5)
+    x = _place(device_logits(w.logits, dtype), shift)
+    width = x.shape[1]
+    xa = _aligned_copy(x)[:, :width]
+    t = torch.from_numpy(w.target_ids).cuda()
+    g = torch.from_numpy(w.grad_logp).cuda()
+    gh = torch.from_numpy(wl.rng(64, 7).standard_normal(n).astype(np.float32)).cuda()
+    _, lse, ent = bil.logp_fwd(xa, t, w.ignore_index, 4096, vocab=VOCAB, temperature=0.7, return_entropy=True)
+    ob = torch.empty((), dtype=out_dtype).element_size()
+    pitch_a = -(-width * ob // 16) * 16 // ob + 8
+    buf_a = torch.full((n, pitch_a), 9.0, dtype=out_dtype, device="cuda")
+    pitch_u = width + 2
+    assert (pitch_u * ob) % 16 != 0
+    buf_u = torch.full((n * pitch_u + 8,), 9.0, dtype=out_dtype, device="cuda")
+    out_u = buf_u[1:1 + n * pitch_u].view(n, pitch_u)
+    for rows, out in ((xa, buf_a[:, :width]), (x, out_u[:, :width])):
+        bil.logp_bwd(rows, t, lse, g, w.ignore_index, vocab=VOCAB, out=out, temperature=0.7, entropy=ent,
+                     grad_entropy=gh)
+    torch.cuda.synchronize()
+    view = torch.int16 if out_dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(buf_a[:, :width].view(view), out_u[:, :width].view(view))
+    assert torch.all(buf_a[:, width:] == 9.0) and torch.all(out_u[:, width:] == 9.0)
+    assert buf_u[0] == 9.0 and torch.all(buf_u[1 + n * pitch_u:] == 9.0)
