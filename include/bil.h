@@ -38,10 +38,15 @@
  *    checked on the host before anything is queued; a failed check queues
  *    nothing and writes nothing.  There is no fallback path.
  *  - Element types: BIL_F32, BIL_BF16, BIL_F16.  Targets are int64.
- *  - Rows whose starting address and stride are 16-byte aligned are read with
- *    bulk asynchronous copies in whole 16-byte units (the unit holding column
- *    vocab-1 may extend past it, never past column ld-1); other rows are read
- *    element by element.  The results are bit-identical either way.
+ *  - The forward and the tile partials read logits with bulk asynchronous
+ *    copies in whole 16-byte aligned units: from the unit that holds a tile's
+ *    first element to the unit that holds its last.  Where rows start on
+ *    16-byte boundaries (base address and stride) nothing outside the row's
+ *    ld columns is read; elsewhere a read may take up to 15 bytes before a
+ *    row's column 0 or past its column vocab-1, always within a 16-byte unit
+ *    that holds an element of the row.  Those bytes never reach a result.
+ *    The backward reads rows that are not 16-byte aligned element by element.
+ *    The results are bit-identical for every alignment.
  *  - bil_logp_fwd on at most 128 rows of a 16-bit type (aligned rows, tiles of
  *    at most 4096) shares each row among a cluster of 8 blocks instead of
  *    streaming it through one block; the results are bit-identical to the

@@ -183,11 +183,11 @@ def test_entropy_with_negative_infinite_logits():
 @pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
 @pytest.mark.parametrize("temperature", [1.0, 0.7])
 def test_unaligned_rows_same_bits_with_temperature_and_entropy(dtype, temperature):
-    """Rows one element past a 16-byte boundary take the element-by-element
-    paths (forward copy, scalar backward); aligned rows the packed vector
-    paths.  With a temperature and the entropy term, every output bit must
-    still agree: the packed and scalar forms perform the same rounded and
-    fused operations."""
+    """Rows one element past a 16-byte boundary take the forward's shifted
+    reads and the scalar backward; aligned rows the plain reads and the packed
+    vector backward.  With a temperature and the entropy term, every output
+    bit must still agree: the packed and scalar forms perform the same rounded
+    and fused operations."""
     n, v = 9, 9000
     w = wl.random_rows(seed=44, n_rows=n, vocab=v, ld=v + 8, dtype=dtype, tile_v=1024, ignore_every=4)
     flat = device_logits(w.logits, dtype).reshape(-1)

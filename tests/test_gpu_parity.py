@@ -60,7 +60,8 @@ def test_minimal_example_autograd():
     """The operator page's minimal example: [2, 4, 300] bf16, target[0, 0] ignored.
 
     300 bf16 columns make 600-byte rows, which are not 16-byte aligned: this
-    also runs the element-by-element load path."""
+    also runs the shifted reads of the forward and the element-by-element
+    backward."""
     import json
     import os
     ex = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "minimal_example.json")))
@@ -161,7 +162,8 @@ def test_row_stride_padding_is_never_read():
 
 @pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
 def test_unaligned_rows_give_the_same_bits(dtype):
-    """A base pointer one element past a 16-byte boundary takes the element-by-element path."""
+    """A base pointer one element past a 16-byte boundary: the forward's shifted
+    reads and the element-by-element backward give the aligned bits."""
     n, v = 7, 9000
     w = wl.random_rows(seed=4, n_rows=n, vocab=v, ld=v + 8, dtype=dtype, tile_v=1024, ignore_every=3)
     flat = device_logits(w.logits, dtype).reshape(-1)
