@@ -47,10 +47,10 @@
  *    that holds an element of the row.  Those bytes never reach a result.
  *    The backward reads rows that are not 16-byte aligned element by element.
  *    The results are bit-identical for every alignment.
- *  - bil_logp_fwd on at most 128 rows of a 16-bit type (aligned rows, tiles of
- *    at most 4096) shares each row among a cluster of 8 blocks instead of
- *    streaming it through one block; the results are bit-identical to the
- *    streaming path.
+ *  - bil_logp_fwd on at most 128 rows of a 16-bit type (16 rows when rows
+ *    do not start on 16-byte boundaries; tiles of at most 4096) shares each
+ *    row among a cluster of 8 blocks instead of streaming it through one
+ *    block; the results are bit-identical to the streaming path.
  *
  * Results are bitwise reproducible for a given tile_v, element type and
  * library build (the arithmetic is fixed in bil_contract_id()).

@@ -64,6 +64,12 @@ int elem_bytes(int dtype) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Whether every one of n_rows rows of ld elements of elem_bytes bytes from p
+// starts on a 16-byte boundary (a single row's stride is never used).
+bool rows_aligned16(const void* p, int64_t n_rows, int64_t ld, int elem_bytes) {
+  return aligned(p, 16) && (n_rows <= 1 || (ld * elem_bytes) % 16 == 0);
+}
+
 struct DeviceInfo {
   int sms = 0;
   int max_smem_optin = 0;
@@ -173,7 +179,7 @@ int launch_stream(int dtype, bool ent, const StreamParams& p0, cudaStream_t stre
   const int eb = elem_bytes(dtype);
   // Every tile starts 16-byte aligned, or the copies start up to 15 bytes
   // early and a stage holds 128 bytes more than the tile.
-  const bool aligned_rows = aligned(p0.logits, 16) && (p0.ld * eb) % 16 == 0;
+  const bool aligned_rows = rows_aligned16(p0.logits, p0.n_rows, p0.ld, eb);
   StreamParams p = p0;
   p.stage_bytes = static_cast<unsigned>(static_cast<size_t>(p.tile_v) * eb + (aligned_rows ? 0 : 128));
   switch (dtype) {
@@ -185,12 +191,18 @@ int launch_stream(int dtype, bool ent, const StreamParams& p0, cudaStream_t stre
 }
 
 // Rows at or below which the forward takes the cluster path (one row per
-// cluster of kSplitCtas blocks) when it applies.
+// cluster of kSplitCtas blocks) when it applies.  Rows off 16-byte
+// boundaries cost the cluster path two 16-byte loads per group, and it beats
+// the streaming path only for fewer rows (measured on 50257- and
+// 151935-column rows: the crossover lies between 7 and 64 rows for the first).
 #ifndef BIL_SPLIT_MAX_ROWS
 #define BIL_SPLIT_MAX_ROWS 128
 #endif
+#ifndef BIL_SPLIT_MAX_ROWS_UNALIGNED
+#define BIL_SPLIT_MAX_ROWS_UNALIGNED 16
+#endif
 
-template <int DT, bool ENT>
+template <int DT, bool ENT, bool ALIGNED>
 int launch_split_t(const StreamParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.n_rows * kSplitCtas), 1, 1);
@@ -204,21 +216,27 @@ int launch_split_t(const StreamParams& p, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, split_row_kernel<DT, ENT>, p) != cudaSuccess) return BIL_E_CUDA;
+  if (cudaLaunchKernelEx(&cfg, split_row_kernel<DT, ENT, ALIGNED>, p) != cudaSuccess) return BIL_E_CUDA;
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
 // Whether the fused forward of these rows takes the cluster path.
 bool use_split(int dtype, const StreamParams& p) {
   const int eb = elem_bytes(dtype);
-  return eb == 2 && p.n_rows >= 1 && p.n_rows <= BIL_SPLIT_MAX_ROWS && p.tile_v <= 4096 &&
-         p.num_tiles <= BIL_MAX_FUSED_TILES && aligned(p.logits, 16) && (p.ld * eb) % 16 == 0;
+  const int64_t most = rows_aligned16(p.logits, p.n_rows, p.ld, eb) ? BIL_SPLIT_MAX_ROWS : BIL_SPLIT_MAX_ROWS_UNALIGNED;
+  return eb == 2 && p.n_rows >= 1 && p.n_rows <= most && p.tile_v <= 4096 && p.num_tiles <= BIL_MAX_FUSED_TILES;
+}
+
+template <int DT, bool ENT>
+int launch_split_dt(const StreamParams& p, cudaStream_t stream) {
+  return rows_aligned16(p.logits, p.n_rows, p.ld, elem_bytes(DT)) ? launch_split_t<DT, ENT, true>(p, stream)
+                                                                   : launch_split_t<DT, ENT, false>(p, stream);
 }
 
 int launch_split(int dtype, bool ent, const StreamParams& p, cudaStream_t stream) {
   switch (dtype) {
-    case BIL_BF16: return ent ? launch_split_t<BIL_BF16, true>(p, stream) : launch_split_t<BIL_BF16, false>(p, stream);
-    case BIL_F16: return ent ? launch_split_t<BIL_F16, true>(p, stream) : launch_split_t<BIL_F16, false>(p, stream);
+    case BIL_BF16: return ent ? launch_split_dt<BIL_BF16, true>(p, stream) : launch_split_dt<BIL_BF16, false>(p, stream);
+    case BIL_F16: return ent ? launch_split_dt<BIL_F16, true>(p, stream) : launch_split_dt<BIL_F16, false>(p, stream);
     default: return BIL_E_DTYPE;
   }
 }
@@ -467,7 +485,7 @@ int bil_logp_bwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
   if (!aligned(logits, eb) || !aligned(target_ids, 8) || !aligned(lse, 4) || !aligned(grad_logp, 4) ||
       !aligned(dlogits, ob) || (entropy && !aligned(entropy, 4)) || (grad_entropy && !aligned(grad_entropy, 4)))
     return BIL_E_ALIGN;
-  const bool vec = aligned(logits, 16) && (ld * eb) % 16 == 0 && aligned(dlogits, 16) && (ld_out * ob) % 16 == 0;
+  const bool vec = rows_aligned16(logits, n_rows, ld, eb) && rows_aligned16(dlogits, n_rows, ld_out, ob);
   BwdParams bp{};
   bp.logits = static_cast<const unsigned char*>(logits);
   bp.n_rows = n_rows;

@@ -148,12 +148,15 @@ struct Group {
   // aligned vectors from p are read whole and the group's words taken out of
   // them, WOFF = off / 4 words in and then sh = 8 * (off % 4) bits down.
   // The words are those `load` reads from a 16-byte aligned copy of the group.
+  // Only the first nvec vectors are read (the rest count as zero): a partial
+  // group in global memory reads only the vectors that hold its elements.
   template <int WOFF>
-  __device__ static __forceinline__ void load_shifted(const unsigned char* p, unsigned sh, uint32_t (&w)[kW]) {
+  __device__ static __forceinline__ void load_shifted(const unsigned char* p, unsigned sh, uint32_t (&w)[kW],
+                                                      int nvec = kVec + 1) {
     uint32_t v[4 * (kVec + 1)];
 #pragma unroll
     for (int q = 0; q <= kVec; ++q) {
-      const uint4 x = *reinterpret_cast<const uint4*>(p + 16 * q);
+      const uint4 x = q < nvec ? *reinterpret_cast<const uint4*>(p + 16 * q) : make_uint4(0u, 0u, 0u, 0u);
       v[4 * q] = x.x;
       v[4 * q + 1] = x.y;
       v[4 * q + 2] = x.z;
@@ -300,21 +303,24 @@ struct TileRegs {
 // boundary below the tile's first element, which sits off = 4 * WOFF + sh / 8
 // bytes past it (the memory from `tile` up to the 16-byte boundary after the
 // group must be readable; bytes outside the tile only reach masked slots).
+// nvec: as for Group::load_shifted (WOFF >= 0 only).
 template <int DT, int WOFF>
 __device__ __forceinline__ void load_group(const unsigned char* tile, int g, unsigned sh,
-                                           uint32_t (&w)[Group<DT>::kW]) {
+                                           uint32_t (&w)[Group<DT>::kW], int nvec = Group<DT>::kVec + 1) {
   const unsigned char* p = tile + static_cast<size_t>(g) * kGroup * Elem<DT>::kBytes;
   if constexpr (WOFF < 0) {
     Group<DT>::load(p, w);
   } else {
-    Group<DT>::template load_shifted<WOFF>(p, sh, w);
+    Group<DT>::template load_shifted<WOFF>(p, sh, w, nvec);
   }
 }
 
 // FULL: the tile holds exactly TileRegs::kMaxTile valid elements, so every
 // lane has kMaxGroups whole groups and no test is needed per group.  WOFF, sh:
-// as for load_group.
-template <int DT, bool FULL, int WOFF = -1>
+// as for load_group.  EXACT (WOFF >= 0): a partial last group reads only the
+// 16-byte vectors that hold its elements (for tiles in global memory, where
+// the next vector may lie past the row's storage).
+template <int DT, bool FULL, int WOFF = -1, bool EXACT = false>
 __device__ __forceinline__ void tile_load_regs_t(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r,
                                                  unsigned sh = 0) {
   const int ng = FULL ? TileRegs<DT>::kMaxGroups : lane_groups(valid, lane);
@@ -324,7 +330,12 @@ __device__ __forceinline__ void tile_load_regs_t(const unsigned char* tile, int 
   for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i) {
     if (FULL || i < ng) {
       const int g = lane + kLanes * i;
-      load_group<DT, WOFF>(tile, g, sh, r.w[i]);
+      int nvec = Group<DT>::kVec + 1;
+      if (EXACT && WOFF >= 0 && !FULL && rem != 0 && g == last) {
+        const int off = 4 * (WOFF < 0 ? 0 : WOFF) + static_cast<int>(sh / 8);
+        nvec = (off + rem * Elem<DT>::kBytes + 15) / 16;
+      }
+      load_group<DT, WOFF>(tile, g, sh, r.w[i], nvec);
       if (!FULL && rem != 0 && g == last) Group<DT>::mask_tail(r.w[i], rem);
     }
   }
@@ -349,28 +360,29 @@ __device__ __forceinline__ TilePartial tile_reduce_regs_t(const TileRegs<DT>& r,
   return finish_tile<ENT>(m, a, u);
 }
 
-template <int DT, int WOFF>
+template <int DT, int WOFF, bool EXACT>
 __device__ __forceinline__ void tile_load_regs_w(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r,
                                                  unsigned sh) {
   if (valid == TileRegs<DT>::kMaxTile) {
-    tile_load_regs_t<DT, true, WOFF>(tile, valid, lane, r, sh);
+    tile_load_regs_t<DT, true, WOFF, EXACT>(tile, valid, lane, r, sh);
   } else {
-    tile_load_regs_t<DT, false, WOFF>(tile, valid, lane, r, sh);
+    tile_load_regs_t<DT, false, WOFF, EXACT>(tile, valid, lane, r, sh);
   }
 }
 
 // The lane's groups of a tile whose first element sits `off` bytes past the
-// 16-byte aligned address `tile` (SHIFTED = false: off is 0).
-template <int DT, bool SHIFTED = false>
+// 16-byte aligned address `tile` (SHIFTED = false: off is 0).  EXACT: as for
+// tile_load_regs_t.
+template <int DT, bool SHIFTED = false, bool EXACT = false>
 __device__ __forceinline__ void tile_load_regs(const unsigned char* tile, int valid, int lane, TileRegs<DT>& r,
                                                unsigned off = 0) {
   const unsigned sh = 8u * (off & 3u);
-  if (!SHIFTED || off == 0) return tile_load_regs_w<DT, -1>(tile, valid, lane, r, 0);
+  if (!SHIFTED || off == 0) return tile_load_regs_w<DT, -1, EXACT>(tile, valid, lane, r, 0);
   switch (off >> 2) {
-    case 0: return tile_load_regs_w<DT, 0>(tile, valid, lane, r, sh);
-    case 1: return tile_load_regs_w<DT, 1>(tile, valid, lane, r, sh);
-    case 2: return tile_load_regs_w<DT, 2>(tile, valid, lane, r, sh);
-    default: return tile_load_regs_w<DT, 3>(tile, valid, lane, r, sh);
+    case 0: return tile_load_regs_w<DT, 0, EXACT>(tile, valid, lane, r, sh);
+    case 1: return tile_load_regs_w<DT, 1, EXACT>(tile, valid, lane, r, sh);
+    case 2: return tile_load_regs_w<DT, 2, EXACT>(tile, valid, lane, r, sh);
+    default: return tile_load_regs_w<DT, 3, EXACT>(tile, valid, lane, r, sh);
   }
 }
 
@@ -913,9 +925,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
 // the cluster's rank-0 block through distributed shared memory.  After one
 // cluster barrier the rank-0 block merges the row with merge_lse.  The bits
 // are those of the streaming forward; only the work split differs.  Used for
-// 16-bit types whose rows are 16-byte aligned, with tiles of at most
-// TileRegs::kMaxTile elements: a group of 8 elements is then one 16-byte unit
-// inside the row (the unit holding column vocab-1 ends before column ld).
+// 16-bit types with tiles of at most TileRegs::kMaxTile elements.  ALIGNED
+// (rows start on 16-byte boundaries): a group of 8 elements is one 16-byte
+// unit inside the row.  Otherwise a group is read as the two 16-byte units
+// that hold it and shifted into place, and a partial last group reads only the
+// units that hold its elements: no read leaves the 16-byte units that hold
+// the row's elements.
 // ---------------------------------------------------------------------------
 
 constexpr int kSplitCtas = 8;   // blocks per cluster (the portable maximum)
@@ -945,7 +960,7 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int DT, bool ENT>
+template <int DT, bool ENT, bool ALIGNED>
 __global__ void __launch_bounds__(kSplitWarps * kLanes) split_row_kernel(const StreamParams p) {
   constexpr int EB = Elem<DT>::kBytes;
   __shared__ float sm_m[BIL_MAX_FUSED_TILES];
@@ -967,7 +982,14 @@ __global__ void __launch_bounds__(kSplitWarps * kLanes) split_row_kernel(const S
       const int valid = static_cast<int>(min(static_cast<int64_t>(p.tile_v), p.vocab - col0));
       const unsigned char* tile = row_src + col0 * EB;
       TileRegs<DT> regs;
-      tile_load_regs<DT>(tile, valid, lane, regs);
+      if (ALIGNED) {
+        tile_load_regs<DT>(tile, valid, lane, regs);
+      } else {
+        // 16-byte loads from the boundary below the tile, shifted into place;
+        // every load holds an element of the tile
+        const unsigned off = static_cast<unsigned>(reinterpret_cast<uintptr_t>(tile) & 15u);
+        tile_load_regs<DT, true, true>(tile - off, valid, lane, regs, off);
+      }
       const TilePartial tp = tile_reduce_regs<DT, ENT>(regs, valid, lane, p.rcp);
       if (lane == 0) {
         st_cluster(cluster_addr(&sm_m[t], 0), tp.m);

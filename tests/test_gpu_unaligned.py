@@ -140,3 +140,30 @@ def test_unaligned_backward_gives_the_aligned_bits(dtype, out_dtype, shift):
     assert torch.equal(buf_a[:, :width].view(view), out_u[:, :width].view(view))
     assert torch.all(buf_a[:, width:] == 9.0) and torch.all(out_u[:, width:] == 9.0)
     assert buf_u[0] == 9.0 and torch.all(buf_u[1 + n * pitch_u:] == 9.0)
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+@pytest.mark.parametrize("vocab", [50257, 50263, 151935])
+@pytest.mark.parametrize("n", [1, 5, 16, 17, 128, 129])
+@pytest.mark.parametrize("tile_v", [1024, 4096])
+def test_small_unaligned_batches_give_the_aligned_bits(dtype, vocab, n, tile_v):
+    """Up to 16 rows of a 16-bit type off 16-byte boundaries (128 aligned)
+    take the cluster path, which reads its tiles straight from global memory:
+    such rows are read as the 16-byte units that hold them and shifted, and a
+    partial last group reads only the units that hold its elements.  With
+    vocab 50257 the last group holds one element, with 50263 seven.  A single
+    row counts as aligned whenever its base is (its stride is never used).
+    The other sizes cross the path boundaries on either side."""
+    w = wl.random_rows(seed=65, n_rows=n, vocab=vocab, dtype=dtype, tile_v=tile_v, ignore_every=3)
+    t = torch.from_numpy(w.target_ids).cuda()
+    for shift in (0, 1, 7):
+        x = _place(device_logits(w.logits, dtype), shift)
+        xa = _aligned_copy(x)
+        for temperature, ent in ((1.0, False), (0.7, True)):
+            a = bil.logp_fwd(xa, t, w.ignore_index, tile_v, vocab=vocab, temperature=temperature,
+                             return_entropy=ent)
+            b = bil.logp_fwd(x, t, w.ignore_index, tile_v, vocab=vocab, temperature=temperature,
+                             return_entropy=ent)
+            torch.cuda.synchronize()
+            for p, q in zip(a, b):
+                assert np.array_equal(f32_bits(p), f32_bits(q)), (shift, temperature, ent)
