@@ -44,6 +44,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "logp_device.cuh"
@@ -75,22 +76,30 @@ struct DeviceInfo {
   int max_smem_optin = 0;
 };
 
+// Per-device attributes, queried once per device and shared by every host
+// thread: the shared-memory limit is stored first and the SM count published
+// after it with release order, so a thread that reads a non-zero SM count
+// (acquire) also sees the limit.  Threads that race to fill an entry store the
+// same values.
 constexpr int kMaxDevices = 64;
-DeviceInfo g_devices[kMaxDevices];
+std::atomic<int> g_device_sms[kMaxDevices];
+std::atomic<int> g_device_smem[kMaxDevices];
 
 int device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BIL_E_CUDA;
-  DeviceInfo& d = g_devices[dev];
-  if (d.sms == 0) {
-    int sms = 0, smem = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BIL_E_CUDA;
+  int sms = g_device_sms[dev].load(std::memory_order_acquire);
+  if (sms == 0) {
+    int smem = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return BIL_E_CUDA;
     if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return BIL_E_CUDA;
-    d.max_smem_optin = smem;
-    d.sms = sms;  // written last: a non-zero sms marks the entry complete
+    g_device_smem[dev].store(smem, std::memory_order_relaxed);
+    g_device_sms[dev].store(sms, std::memory_order_release);
   }
-  *out = d;
+  out->sms = sms;
+  out->max_smem_optin = g_device_smem[dev].load(std::memory_order_relaxed);
   return BIL_OK;
 }
 
