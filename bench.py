@@ -70,7 +70,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["bil", "reference"], default="bil")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--rows", type=int, default=16384,
                     help="rows of the workload per GPU (smaller only for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -270,6 +270,19 @@ int temperature_rcp(float temperature, float* rcp) {
   return BIL_OK;
 }
 
+// Resident warps per SM for the vectorised backward without the entropy
+// term.  Its loop is a bare stream (load, a few operations, store), and more
+// resident warps than this oversubscribe the memory system: on GB300 the
+// 16-bit training backward (16384 x 151936) took 1.61 ms with the 40 warps
+// that fit and 1.52 ms with 32; 24 warps took 1.68 ms.  The entropy term's
+// extra arithmetic per element wants every warp that fits (1.55 ms with 40,
+// 1.60 ms with 32), and so does the element-by-element path for rows off
+// 16-byte boundaries (its scalar loads need the warps to keep bytes in
+// flight).
+#ifndef BIL_BWD_PLAIN_WARPS_PER_SM
+#define BIL_BWD_PLAIN_WARPS_PER_SM 32
+#endif
+
 template <int DT, int OT>
 int launch_bwd_t(bool vec, const BwdParams& bp, cudaStream_t stream) {
   DeviceInfo dev;
@@ -278,6 +291,7 @@ int launch_bwd_t(bool vec, const BwdParams& bp, cudaStream_t stream) {
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBwdThreads, 0) != cudaSuccess)
     return BIL_E_CUDA;
+  if (vec && bp.grad_entropy == nullptr) per_sm = std::min(per_sm, BIL_BWD_PLAIN_WARPS_PER_SM / (kBwdThreads / kLanes));
   per_sm = std::max(1, per_sm);
   const int64_t units = bp.n_rows * ((bp.out_cols + kBwdChunk - 1) / kBwdChunk);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(units, static_cast<int64_t>(dev.sms) * per_sm));

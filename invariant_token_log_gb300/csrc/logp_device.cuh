@@ -1137,44 +1137,32 @@ struct Out<BIL_F16> {
   }
 };
 
-// A group of 8 gradient elements from its stored logits, with the same
-// operations as grad_elem in packed pairs.  `jt` is the target's slot in the
-// group, or -1 when the target lies elsewhere.
+// A group of 8 gradient elements from its stored logits, none of them the
+// row's target column, with the same operations as grad_elem in packed pairs.
 template <int DT>
 __device__ __forceinline__ void grad_group(const uint32_t (&w)[Group<DT>::kW], const RowMeta& m, float rcp, bool ent,
-                                           int jt, float (&y)[kGroup]) {
+                                           float (&y)[kGroup]) {
   const bool scaled = rcp != 1.0f;
   const uint64_t L2 = pk(m.lse, m.lse), nL2 = pk(-m.lse, -m.lse), g2 = pk(m.g, m.g), rcp2 = pk(rcp, rcp);
-  const uint64_t gh2 = pk(m.gh, m.gh), H2 = pk(m.H, m.H);
-  constexpr uint64_t kSigns = 0x8000000080000000ull;
+  const uint64_t ngh2 = pk(-m.gh, -m.gh), H2 = pk(m.H, m.H);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint64_t x = Group<DT>::xpair(w, k);
     const uint64_t a = scaled ? fma2(x, rcp2, nL2) : sub2(x, L2);
     const uint64_t p = exp2_pair(a);                  // (p_2k, p_2k+1)
     uint64_t d;
-    uint64_t t3 = 0;
     if (ent) {
       const uint64_t ac = pk(fmaxf(lo_of(a), kNegMax), fmaxf(hi_of(a), kNegMax));
-      t3 = mul2(gh2, mul2(p, add2(ac, H2)));
-      d = fma2(g2, sub2(0, p), t3 ^ kSigns);          // g * (0 - p) - t3, one rounding
+      // -t3 = (-gh) * (p * (a + H)) is exactly -(gh * (p * (a + H))): rounding
+      // to nearest is symmetric in the sign
+      const uint64_t nt3 = mul2(ngh2, mul2(p, add2(ac, H2)));
+      d = fma2(g2, sub2(0, p), nt3);                  // g * (0 - p) - t3, one rounding
     } else {
       d = mul2(g2, sub2(0, p));                       // g * (0 - p)
     }
     if (scaled) d = mul2(d, rcp2);
     y[2 * k] = lo_of(d);
     y[2 * k + 1] = hi_of(d);
-    if (jt >= 0) {  // the one target column of the row: g * (1 - p), then as above
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (jt == 2 * k + h) {
-          const float ph = h ? hi_of(p) : lo_of(p);
-          const float th = h ? hi_of(t3) : lo_of(t3);
-          const float dt = ent ? __fmaf_rn(m.g, __fsub_rn(1.0f, ph), -th) : __fmul_rn(m.g, __fsub_rn(1.0f, ph));
-          y[2 * k + h] = scaled ? __fmul_rn(dt, rcp) : dt;
-        }
-      }
-    }
   }
 }
 
@@ -1267,11 +1255,14 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams bp) {
       for (int i = 0; i < kBwdGroupsPerThread; ++i) {
         const int64_t c = c0 + (static_cast<int64_t>(i) * kBwdThreads + threadIdx.x) * kGroup;
         if (c < gend) {
-          const uint64_t off = static_cast<uint64_t>(t - c);
-          const int jt = off < static_cast<uint64_t>(kGroup) ? static_cast<int>(off) : -1;
           float y[kGroup];
-          grad_group<DT>(w[i], meta, rcp, ent, jt, y);
+          grad_group<DT>(w[i], meta, rcp, ent, y);
           Out<OT>::store8(out + c * OB, y);
+          // The row's target column, if it is in this group: g * (1 - p) and
+          // the rest, stored over the group's value (same thread, same address:
+          // this store lands last).
+          if (static_cast<uint64_t>(t - c) < static_cast<uint64_t>(kGroup))
+            Out<OT>::store1(out + t * OB, grad_elem(Elem<DT>::one(in + t * EB), meta, true, rcp, ent));
         }
       }
       for (int64_t c = gend + threadIdx.x; c < v1; c += kBwdThreads)
