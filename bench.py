@@ -345,7 +345,43 @@ def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_byte
             lat[str(nd)] = f"unavailable: {str(exc).splitlines()[0][:80]}"
     variants["decode_fwd_us_per_call_graph"] = lat
     variants["decode_fwd_us_per_call_python"] = eager
+    variants["prefill_fwd"] = prefill_measurement(bil, stream, dev)
     return variants
+
+
+def prefill_measurement(bil, stream, dev):
+    """Forward of the prefill batch: 4096 rows (B=4, T=1024) of V=151936 bf16 logits at a
+    padded pitch of 155648 columns (-inf pads, never read), 5% of the rows ignored (their
+    logits are not read either).  Device time per call over 20 calls after 3 warm-up calls,
+    CUDA events on the launching stream; bytes are counted for the active rows, and also for
+    all rows to compare with figures quoted on N * V."""
+    import torch
+
+    import workloads as wl
+
+    w = wl.prefill()
+    x = torch.from_numpy(np.ascontiguousarray(w.logits).view(np.int16)).view(torch.bfloat16).to(dev)
+    t = torch.from_numpy(w.target_ids).to(dev)
+    n, v = w.n_rows, w.vocab
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        bil.logp_fwd(x, t, w.ignore_index, w.tile_v, vocab=v, out=logp, lse=lse)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    e0.record(stream)
+    for _ in range(reps):
+        bil.logp_fwd(x, t, w.ignore_index, w.tile_v, vocab=v, out=logp, lse=lse)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / reps
+    active = int((w.target_ids != w.ignore_index).sum())
+    peak, _ = hbm_peak()
+    gbs_active = (active * v * 2 + n * 16) / (ms / 1e3) / 1e9
+    return {"ms": ms, "rows_per_s": n / (ms / 1e3), "rows": n, "active_rows": active, "ld": int(x.shape[1]),
+            "gbs": gbs_active, "frac": gbs_active / peak,
+            "gbs_on_all_rows": n * v * 2 / (ms / 1e3) / 1e9}
 
 
 def run_bil(args):
