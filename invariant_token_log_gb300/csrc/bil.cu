@@ -46,6 +46,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <utility>
 
 #include "logp_device.cuh"
 
@@ -122,6 +123,35 @@ int check_targets_host(const int64_t* targets, int64_t n, int64_t ignore_index, 
   return BIL_OK;
 }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream finishes (its launch latency hides
+// behind that kernel's tail); each kernel of this file waits for its
+// predecessor with griddep_wait() before touching global memory.  cluster > 1:
+// thread-block clusters of that many blocks along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int64_t grid, int block, size_t smem, cudaStream_t stream,
+                       int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Pipeline shape for a stage size: a ring of about BIL_STREAM_RING_BYTES per
 // block (two blocks share an SM), at least two stages, up to
 // kMaxConsumers consumer warps, and a stage count that is a multiple of the
@@ -170,7 +200,7 @@ int launch_stream_t(const StreamParams& p0, cudaStream_t stream) {
   const int64_t tiles_here = p.tile_end - p.tile_begin;
   const int64_t work = FUSED ? p.n_rows : p.n_rows * tiles_here;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(work, static_cast<int64_t>(dev.sms) * per_sm));
-  kernel<<<static_cast<unsigned>(grid), threads, shape.smem, stream>>>(p);
+  if (launch_pdl(kernel, grid, threads, shape.smem, stream, 1, p) != cudaSuccess) return BIL_E_CUDA;
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
@@ -213,19 +243,9 @@ int launch_stream(int dtype, bool ent, const StreamParams& p0, cudaStream_t stre
 
 template <int DT, bool ENT, bool ALIGNED>
 int launch_split_t(const StreamParams& p, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.n_rows * kSplitCtas), 1, 1);
-  cfg.blockDim = dim3(kSplitWarps * kLanes, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kSplitCtas;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, split_row_kernel<DT, ENT, ALIGNED>, p) != cudaSuccess) return BIL_E_CUDA;
+  if (launch_pdl(split_row_kernel<DT, ENT, ALIGNED>, p.n_rows * kSplitCtas, kSplitWarps * kLanes, 0, stream,
+                 kSplitCtas, p) != cudaSuccess)
+    return BIL_E_CUDA;
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
@@ -295,7 +315,7 @@ int launch_bwd_t(bool vec, const BwdParams& bp, cudaStream_t stream) {
   per_sm = std::max(1, per_sm);
   const int64_t units = bp.n_rows * ((bp.out_cols + kBwdChunk - 1) / kBwdChunk);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(units, static_cast<int64_t>(dev.sms) * per_sm));
-  kernel<<<static_cast<unsigned>(grid), kBwdThreads, 0, stream>>>(bp);
+  if (launch_pdl(kernel, grid, kBwdThreads, 0, stream, 1, bp) != cudaSuccess) return BIL_E_CUDA;
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
@@ -479,15 +499,14 @@ int bil_logp_merge(const float* part_max, const float* part_sum, const float* pa
   const int64_t rows_per_block = threads / kLanes;
   const int64_t grid = std::max<int64_t>(
       1, std::min<int64_t>((n_rows + rows_per_block - 1) / rows_per_block, static_cast<int64_t>(dev.sms) * 8));
-  if (entropy != nullptr) {
-    merge_kernel<true><<<static_cast<unsigned>(grid), threads, 0, s>>>(part_max, part_sum, part_ent, n_rows,
-                                                                        num_tiles, ld_part, target_logit, target_ids,
-                                                                        ignore_index, vocab, logp, lse, entropy);
-  } else {
-    merge_kernel<false><<<static_cast<unsigned>(grid), threads, 0, s>>>(part_max, part_sum, nullptr, n_rows,
-                                                                         num_tiles, ld_part, target_logit, target_ids,
-                                                                         ignore_index, vocab, logp, lse, nullptr);
-  }
+  const cudaError_t e =
+      entropy != nullptr
+          ? launch_pdl(merge_kernel<true>, grid, threads, 0, s, 1, part_max, part_sum, part_ent, n_rows, num_tiles,
+                       ld_part, target_logit, target_ids, ignore_index, vocab, logp, lse, entropy)
+          : launch_pdl(merge_kernel<false>, grid, threads, 0, s, 1, part_max, part_sum, static_cast<const float*>(nullptr),
+                       n_rows, num_tiles, ld_part, target_logit, target_ids, ignore_index, vocab, logp, lse,
+                       static_cast<float*>(nullptr));
+  if (e != cudaSuccess) return BIL_E_CUDA;
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 

@@ -21,6 +21,16 @@ __device__ __forceinline__ float ex2_approx(float a) {
   return r;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may be scheduled while the kernel before it in the stream is
+// still finishing.  griddep_wait() returns once that kernel has completed and
+// its memory operations are visible, so every thread calls it before its
+// first access to global memory; griddep_launch_dependents() lets the next
+// kernel in the stream be scheduled early in turn.  Without the launch
+// attribute both return at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // exp(a) of the contract: one rounded multiply, then the hardware base-2
 // exponential (flushes results below 2^-126 to zero).
 __device__ __forceinline__ float contract_exp(float a) { return ex2_approx(__fmul_rn(a, kLog2e)); }

@@ -673,6 +673,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  griddep_wait();  // the barriers above are shared memory; from here on global memory is read
+  griddep_launch_dependents();
 
   const int tiles_here = p.tile_end - p.tile_begin;
 
@@ -967,6 +969,8 @@ __global__ void __launch_bounds__(kSplitWarps * kLanes) split_row_kernel(const S
   __shared__ float sm_s[BIL_MAX_FUSED_TILES];
   __shared__ float sm_u[ENT ? BIL_MAX_FUSED_TILES : 1];
   __shared__ float sm_tl;
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t rank = cluster_ctarank();
   const int64_t row = static_cast<int64_t>(blockIdx.x) / kSplitCtas;  // a cluster is kSplitCtas consecutive blocks
   const int warp = threadIdx.x / kLanes;
@@ -1050,6 +1054,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
                                                     const int64_t* __restrict__ targets,
                                                     int64_t ignore_index, int64_t vocab, float* logp,
                                                     float* lse, float* entropy) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x % kLanes;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / kLanes);
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / kLanes) + threadIdx.x / kLanes;
@@ -1208,6 +1214,8 @@ __device__ __forceinline__ RowMeta row_meta(const BwdParams& bp, int64_t row) {
 
 template <int DT, int OT, bool VEC>
 __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams bp) {
+  griddep_wait();
+  griddep_launch_dependents();
   const unsigned char* __restrict__ logits = bp.logits;
   const int64_t n_rows = bp.n_rows, vocab = bp.vocab, ld = bp.ld, ignore_index = bp.ignore_index;
   unsigned char* __restrict__ dlogits = bp.dlogits;
