@@ -495,7 +495,7 @@ int bil_logp_merge(const float* part_max, const float* part_sum, const float* pa
   }
   DeviceInfo dev;
   if (int st = device_info(&dev)) return st;
-  const int threads = 256;
+  const int threads = 256;  // merge_kernel's shared scratch has one slot per warp of 256 threads
   const int64_t rows_per_block = threads / kLanes;
   const int64_t grid = std::max<int64_t>(
       1, std::min<int64_t>((n_rows + rows_per_block - 1) / rows_per_block, static_cast<int64_t>(dev.sms) * 8));
