@@ -116,6 +116,8 @@ struct LinearParams {
   int logits_dtype;
   int64_t ld_logits;
   uint32_t idesc;
+  unsigned a_box_bytes;  // bytes one A copy brings: its box's rows (kBM, or fewer for a batch of
+                         // fewer rows) x kBK 16-bit columns
   int m_group;          // row tiles per raster group
   // kModeGrad
   const float* lse;
@@ -454,7 +456,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
             break;
           }
           unsigned char* a_dst = base + s * size_t(kStageBytes);
-          mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+          mbar_arrive_expect_tx(&sm.full[s], p.a_box_bytes + kStageBBytes);
           tma_load_2d(a_dst, &tmap_hidden, kb * kBK, m * kBM, &sm.full[s]);
           tma_load_2d(a_dst + kStageABytes, &tmap_weight, kb * kBK, n * kBN, &sm.full[s]);
         }
@@ -825,8 +827,14 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
   }
   if (n_rows > (static_cast<int64_t>(INT32_MAX) - kBM) || shard_cols > INT32_MAX - kBN) return BIL_E_UNSUPPORTED;
 
+  // A batch of fewer than kBM rows is copied with a box of exactly its rows:
+  // no part of the box lies outside the hidden states (measured: copies of a
+  // 128-row box mostly past the end slowed the weight stream by up to 35% at
+  // 1-12 rows).  The stage's other rows keep stale bytes; the tensor cores
+  // turn them into accumulator rows of their own, which no thread stores.
+  const int a_rows = static_cast<int>(n_rows < kBM ? n_rows : kBM);
   CUtensorMap mh, mw;
-  if (int st = make_map(&mh, hidden, dtype, n_rows, hidden_size, ld_hidden, kBM)) return st;
+  if (int st = make_map(&mh, hidden, dtype, n_rows, hidden_size, ld_hidden, a_rows)) return st;
   if (int st = make_map(&mw, weight, dtype, shard_cols, hidden_size, ld_weight, kBN)) return st;
 
   LinearParams p{};
@@ -848,6 +856,7 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
   p.logits_dtype = logits_dtype;
   p.ld_logits = ld_logits;
   p.idesc = make_idesc(dtype == BIL_BF16);
+  p.a_box_bytes = static_cast<unsigned>(a_rows) * kBK * 2;
   p.m_group = kMGroup;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return launch_gemm(part_ent != nullptr ? linear_partials_kernel<true> : linear_partials_kernel<false>, mh, mw, p, s);
@@ -998,6 +1007,7 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
     p.ignore_index = ignore_index;
     p.rcp = rcp;
     p.idesc = idesc;
+    p.a_box_bytes = kStageABytes;  // A maps of these GEMMs use kBM-row boxes
     p.m_group = kMGroup;
     p.lse = lse;
     p.grad_logp = grad_logp;
@@ -1035,6 +1045,7 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
     p.num_m = static_cast<int>((c.a_rows + kBM - 1) / kBM);
     p.k_blocks = static_cast<int>((c.k + kBK - 1) / kBK);
     p.idesc = idesc;
+    p.a_box_bytes = kStageABytes;  // A maps of these GEMMs use kBM-row boxes
     p.m_group = store_group(p.num_n);
     p.out = static_cast<unsigned char*>(c.out);
     p.out_dtype = c.out_dtype;
