@@ -303,28 +303,34 @@ int temperature_rcp(float temperature, float* rcp) {
 #define BIL_BWD_PLAIN_WARPS_PER_SM 32
 #endif
 
+// rows: a BwdRows value.  The rows that go by 16-byte vectors (aligned, or
+// input and output at shared offsets) take the warp cap below.
 template <int DT, int OT>
-int launch_bwd_t(bool vec, const BwdParams& bp, cudaStream_t stream) {
+int launch_bwd_t(int rows, const BwdParams& bp, cudaStream_t stream) {
   DeviceInfo dev;
   if (int st = device_info(&dev)) return st;
-  auto kernel = vec ? bwd_kernel<DT, OT, true> : bwd_kernel<DT, OT, false>;
+  auto kernel = rows == kBwdAligned         ? bwd_kernel<DT, OT, kBwdAligned>
+                : rows == kBwdSharedOffsets ? bwd_kernel<DT, OT, kBwdSharedOffsets>
+                                            : bwd_kernel<DT, OT, kBwdScalar>;
+  const bool streamed = rows != kBwdScalar;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBwdThreads, 0) != cudaSuccess)
     return BIL_E_CUDA;
-  if (vec && bp.grad_entropy == nullptr) per_sm = std::min(per_sm, BIL_BWD_PLAIN_WARPS_PER_SM / (kBwdThreads / kLanes));
+  if (streamed && bp.grad_entropy == nullptr)
+    per_sm = std::min(per_sm, BIL_BWD_PLAIN_WARPS_PER_SM / (kBwdThreads / kLanes));
   per_sm = std::max(1, per_sm);
   const int64_t units = bp.n_rows * ((bp.out_cols + kBwdChunk - 1) / kBwdChunk);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(units, static_cast<int64_t>(dev.sms) * per_sm));
-  if (launch_pdl(kernel, grid, kBwdThreads, 0, stream, 1, bp) != cudaSuccess) return BIL_E_CUDA;
+  kernel<<<static_cast<unsigned>(grid), kBwdThreads, 0, stream>>>(bp);
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
 template <int DT>
-int launch_bwd_dt(int out_dtype, bool vec, const BwdParams& bp, cudaStream_t stream) {
+int launch_bwd_dt(int out_dtype, int rows, const BwdParams& bp, cudaStream_t stream) {
   switch (out_dtype) {
-    case BIL_F32: return launch_bwd_t<DT, BIL_F32>(vec, bp, stream);
-    case BIL_BF16: return launch_bwd_t<DT, BIL_BF16>(vec, bp, stream);
-    case BIL_F16: return launch_bwd_t<DT, BIL_F16>(vec, bp, stream);
+    case BIL_F32: return launch_bwd_t<DT, BIL_F32>(rows, bp, stream);
+    case BIL_BF16: return launch_bwd_t<DT, BIL_BF16>(rows, bp, stream);
+    case BIL_F16: return launch_bwd_t<DT, BIL_F16>(rows, bp, stream);
     default: return BIL_E_DTYPE;
   }
 }
@@ -528,6 +534,11 @@ int bil_logp_bwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
       !aligned(dlogits, ob) || (entropy && !aligned(entropy, 4)) || (grad_entropy && !aligned(grad_entropy, 4)))
     return BIL_E_ALIGN;
   const bool vec = rows_aligned16(logits, n_rows, ld, eb) && rows_aligned16(dlogits, n_rows, ld_out, ob);
+  // input and output rows at the same offset from a 16-byte boundary, row after row
+  const bool shared_offsets =
+      eb == ob && (reinterpret_cast<uintptr_t>(logits) - reinterpret_cast<uintptr_t>(dlogits)) % 16 == 0 &&
+      (n_rows <= 1 || ((ld - ld_out) * eb) % 16 == 0);
+  const int rows = vec ? kBwdAligned : shared_offsets ? kBwdSharedOffsets : kBwdScalar;
   BwdParams bp{};
   bp.logits = static_cast<const unsigned char*>(logits);
   bp.n_rows = n_rows;
@@ -545,9 +556,9 @@ int bil_logp_bwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
   bp.out_cols = out_cols;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (dtype) {
-    case BIL_BF16: return launch_bwd_dt<BIL_BF16>(dlogits_dtype, vec, bp, s);
-    case BIL_F16: return launch_bwd_dt<BIL_F16>(dlogits_dtype, vec, bp, s);
-    case BIL_F32: return launch_bwd_dt<BIL_F32>(dlogits_dtype, vec, bp, s);
+    case BIL_BF16: return launch_bwd_dt<BIL_BF16>(dlogits_dtype, rows, bp, s);
+    case BIL_F16: return launch_bwd_dt<BIL_F16>(dlogits_dtype, rows, bp, s);
+    case BIL_F32: return launch_bwd_dt<BIL_F32>(dlogits_dtype, rows, bp, s);
     default: return BIL_E_DTYPE;
   }
 }

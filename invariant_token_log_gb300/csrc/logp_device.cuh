@@ -1289,10 +1289,16 @@ __device__ __forceinline__ RowMeta row_meta(const BwdParams& bp, int64_t row) {
   return m;
 }
 
-template <int DT, int OT, bool VEC>
+// How the backward reads and writes its rows.
+enum BwdRows {
+  kBwdAligned = 0,        // every input and output row starts on a 16-byte boundary
+  kBwdSharedOffsets = 1,  // input and output rows share their offset from one: groups from the first
+                          // column where both are aligned, the few columns around them one by one
+  kBwdScalar = 2,         // element by element
+};
+
+template <int DT, int OT, int ROWS>
 __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams bp) {
-  griddep_wait();
-  griddep_launch_dependents();
   const unsigned char* __restrict__ logits = bp.logits;
   const int64_t n_rows = bp.n_rows, vocab = bp.vocab, ld = bp.ld, ignore_index = bp.ignore_index;
   unsigned char* __restrict__ dlogits = bp.dlogits;
@@ -1325,20 +1331,50 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams bp) {
     if (!active || !valid_target) {
       const float fill = active ? __int_as_float(0x7fc00000) : 0.0f;
       for (int64_t c = c0 + threadIdx.x; c < v1; c += kBwdThreads) Out<OT>::store1(out + c * OB, fill);
-    } else if (VEC) {
-      // c0 is a multiple of 8; groups fully inside [c0, v1) go by 16-byte
-      // vectors, all of a thread's loads issued before any arithmetic.
+    } else if (ROWS == kBwdScalar) {
       const unsigned char* in = logits + row * ld * EB;
-      const int64_t gend = c0 + ((v1 - c0) / kGroup) * kGroup;
+      for (int64_t c = c0 + threadIdx.x; c < v1; c += kBwdThreads)
+        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta, c == t, rcp, ent));
+    } else {
+      // Groups of 8 columns go by 16-byte vectors from the first column cg at
+      // which the input and the output are both 16-byte aligned: c0 itself
+      // when every row is aligned; otherwise the first such column of
+      // [c0, c0 + 8), if there is one (the rows of a contiguous [N, V] input
+      // and output share their offsets, whatever V).  All of a thread's loads
+      // are issued before any arithmetic.  The columns before cg and after the
+      // last whole group go one by one, with the same operations.
+      const unsigned char* in = logits + row * ld * EB;
+      int64_t cg = c0;
+      if (ROWS == kBwdSharedOffsets) {
+        cg = v1;
+        for (int k = 0; k < kGroup; ++k) {
+          const int64_t c = c0 + k;
+          const uintptr_t a = reinterpret_cast<uintptr_t>(in + c * EB) | reinterpret_cast<uintptr_t>(out + c * OB);
+          if (c < v1 && (a & 15u) == 0) {
+            cg = c;
+            break;
+          }
+        }
+      }
+      const int64_t gend = cg + ((v1 - cg) / kGroup) * kGroup;
+      // With shared offsets fewer than 8 columns precede cg and fewer than 8
+      // follow gend in every unit, so a thread has at most one of each; they
+      // are read with the groups rather than after them, so that no warp waits
+      // for memory twice more per unit.  (Aligned rows have a tail only at the
+      // end of a row whose length is not a multiple of 8.)
+      const int64_t ch = c0 + threadIdx.x, ct = gend + threadIdx.x;
+      const bool head = ROWS == kBwdSharedOffsets && ch < cg, tail = ROWS == kBwdSharedOffsets && ct < v1;
+      const float xh = head ? Elem<DT>::one(in + ch * EB) : 0.0f;
+      const float xt = tail ? Elem<DT>::one(in + ct * EB) : 0.0f;
       uint32_t w[kBwdGroupsPerThread][Group<DT>::kW];
 #pragma unroll
       for (int i = 0; i < kBwdGroupsPerThread; ++i) {
-        const int64_t c = c0 + (static_cast<int64_t>(i) * kBwdThreads + threadIdx.x) * kGroup;
+        const int64_t c = cg + (static_cast<int64_t>(i) * kBwdThreads + threadIdx.x) * kGroup;
         if (c < gend) load_group_stream<DT>(in + c * EB, w[i]);
       }
 #pragma unroll
       for (int i = 0; i < kBwdGroupsPerThread; ++i) {
-        const int64_t c = c0 + (static_cast<int64_t>(i) * kBwdThreads + threadIdx.x) * kGroup;
+        const int64_t c = cg + (static_cast<int64_t>(i) * kBwdThreads + threadIdx.x) * kGroup;
         if (c < gend) {
           float y[kGroup];
           grad_group<DT>(w[i], meta, rcp, ent, y);
@@ -1350,12 +1386,12 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams bp) {
             Out<OT>::store1(out + t * OB, grad_elem(Elem<DT>::one(in + t * EB), meta, true, rcp, ent));
         }
       }
-      for (int64_t c = gend + threadIdx.x; c < v1; c += kBwdThreads)
-        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta, c == t, rcp, ent));
-    } else {
-      const unsigned char* in = logits + row * ld * EB;
-      for (int64_t c = c0 + threadIdx.x; c < v1; c += kBwdThreads)
-        Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta, c == t, rcp, ent));
+      if (head) Out<OT>::store1(out + ch * OB, grad_elem(xh, meta, ch == t, rcp, ent));
+      if (tail) Out<OT>::store1(out + ct * OB, grad_elem(xt, meta, ct == t, rcp, ent));
+      if (ROWS == kBwdAligned) {
+        for (int64_t c = gend + threadIdx.x; c < v1; c += kBwdThreads)
+          Out<OT>::store1(out + c * OB, grad_elem(Elem<DT>::one(in + c * EB), meta, c == t, rcp, ent));
+      }
     }
     for (int64_t c = max(c0, vocab) + threadIdx.x; c < c1; c += kBwdThreads) Out<OT>::store1(out + c * OB, 0.0f);
     row = next_row;
