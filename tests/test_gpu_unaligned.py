@@ -167,3 +167,32 @@ def test_small_unaligned_batches_give_the_aligned_bits(dtype, vocab, n, tile_v):
             torch.cuda.synchronize()
             for p, q in zip(a, b):
                 assert np.array_equal(f32_bits(p), f32_bits(q)), (shift, temperature, ent)
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16", "float32"])
+@pytest.mark.parametrize("shift", [0, 3])
+def test_backward_with_shared_offsets_gives_the_aligned_bits(dtype, shift):
+    """Contiguous [N, V] logits and an output of the same layout at an odd V:
+    input and output rows share their offsets from a 16-byte boundary (every
+    offset occurs), so the backward's groups start at the first column where
+    both are aligned and the few columns around them go one by one.  Bits must
+    equal those of an aligned copy, with and without a temperature and the
+    entropy term."""
+    n = 33
+    w = wl.random_rows(seed=66, n_rows=n, vocab=VOCAB, dtype=dtype, tile_v=4096, ignore_every=5)
+    x = _place(device_logits(w.logits, dtype), shift)
+    out = _place(torch.full_like(x, 9.0), shift)
+    assert (x.data_ptr() - out.data_ptr()) % 16 == 0 and (x.stride(0) * x.element_size()) % 16 != 0
+    xa = _aligned_copy(x)
+    t = torch.from_numpy(w.target_ids).cuda()
+    g = torch.from_numpy(w.grad_logp).cuda()
+    gh = torch.from_numpy(wl.rng(66, 7).standard_normal(n).astype(np.float32)).cuda()
+    view = torch.int16 if x.element_size() == 2 else torch.int32
+    for temperature, ent in ((1.0, False), (0.7, True)):
+        _, lse, h = bil.logp_fwd(xa, t, w.ignore_index, 4096, vocab=VOCAB, temperature=temperature,
+                                 return_entropy=True)
+        kw = dict(temperature=temperature, entropy=h, grad_entropy=gh) if ent else dict(temperature=temperature)
+        da = bil.logp_bwd(xa, t, lse, g, w.ignore_index, vocab=VOCAB, **kw)
+        bil.logp_bwd(x, t, lse, g, w.ignore_index, vocab=VOCAB, out=out, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(da[:, :VOCAB].view(view), out.view(view)), (temperature, ent)
