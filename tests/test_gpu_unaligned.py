@@ -171,15 +171,16 @@ def test_small_unaligned_batches_give_the_aligned_bits(dtype, vocab, n, tile_v):
 
 @pytest.mark.parametrize("dtype", ["bfloat16", "float16", "float32"])
 @pytest.mark.parametrize("shift", [0, 3])
-def test_backward_with_shared_offsets_gives_the_aligned_bits(dtype, shift):
-    """Contiguous [N, V] logits and an output of the same layout at an odd V:
-    input and output rows share their offsets from a 16-byte boundary (every
-    offset occurs), so the backward's groups start at the first column where
-    both are aligned and the few columns around them go one by one.  Bits must
-    equal those of an aligned copy, with and without a temperature and the
-    entropy term."""
+@pytest.mark.parametrize("pad", [0, 5])
+def test_backward_with_shared_offsets_gives_the_aligned_bits(dtype, shift, pad):
+    """Contiguous [N, V + pad] logits and an output of the same layout at an
+    odd pitch: input and output rows share their offsets from a 16-byte
+    boundary (every offset occurs), so the backward's groups start at the first
+    column where both are aligned and the few columns around them go one by
+    one.  Bits must equal those of an aligned copy, with and without a
+    temperature and the entropy term; the pad columns get +0.0."""
     n = 33
-    w = wl.random_rows(seed=66, n_rows=n, vocab=VOCAB, dtype=dtype, tile_v=4096, ignore_every=5)
+    w = wl.random_rows(seed=66, n_rows=n, vocab=VOCAB, ld=VOCAB + pad, dtype=dtype, tile_v=4096, ignore_every=5)
     x = _place(device_logits(w.logits, dtype), shift)
     out = _place(torch.full_like(x, 9.0), shift)
     assert (x.data_ptr() - out.data_ptr()) % 16 == 0 and (x.stride(0) * x.element_size()) % 16 != 0
@@ -195,4 +196,5 @@ def test_backward_with_shared_offsets_gives_the_aligned_bits(dtype, shift):
         da = bil.logp_bwd(xa, t, lse, g, w.ignore_index, vocab=VOCAB, **kw)
         bil.logp_bwd(x, t, lse, g, w.ignore_index, vocab=VOCAB, out=out, **kw)
         torch.cuda.synchronize()
-        assert torch.equal(da[:, :VOCAB].view(view), out.view(view)), (temperature, ent)
+        assert torch.equal(da[:, :VOCAB].view(view), out[:, :VOCAB].view(view)), (temperature, ent)
+        assert torch.all(out[:, VOCAB:].view(view) == 0)
