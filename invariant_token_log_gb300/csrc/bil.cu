@@ -11,9 +11,11 @@
 //   stream_kernel<FUSED=true>   forward: every tile of a row -> shared-memory
 //                               partials -> fixed-order merge -> logp, lse.
 //   stream_kernel<FUSED=false>  partials of a tile range -> [N, ld_part] buffers.
-//   split_row_kernel            forward of up to 128 rows, one row per cluster.
+//   split_row_kernel            forward of up to 128 rows (16 off 16-byte
+//                               boundaries), one row per cluster.
 //   merge_kernel                fixed-order merge of [N, T] partials -> logp, lse.
-//   bwd_kernel                  dlogits = g * (onehot - exp(x - lse)).
+//   bwd_kernel                  dlogits = g * (onehot - exp(x - lse)); rows aligned,
+//                               at offsets shared by input and output, or scalar.
 // The fused LM-head is in linear.cu.
 //
 // The forward streams each row exactly once.  A producer warp moves whole
@@ -21,9 +23,9 @@
 // (cp.async.bulk, completion counted on an mbarrier) into a ring of stages;
 // consumer warps reduce one tile each.  Rows that do not start on a 16-byte
 // boundary are copied from the boundary below each tile, and the consumers
-// shift the tile's words back into place as they read them.  Nothing on this path is a contraction,
-// so no tensor cores are used: the forward is bound by HBM bandwidth, with
-// the exponential unit second.
+// shift the tile's words back into place as they read them.  Nothing on this
+// path is a contraction, so no tensor cores are used: the forward is bound by
+// HBM bandwidth, with the exponential unit second.
 //
 // The arithmetic contract (what makes the bits reproducible) lives in the
 // tile reduction, merge_lse and the gradient formula of logp_device.cuh and
@@ -125,8 +127,10 @@ int check_targets_host(const int64_t* targets, int64_t n, int64_t ignore_index, 
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel in the stream finishes (its launch latency hides
-// behind that kernel's tail); each kernel of this file waits for its
-// predecessor with griddep_wait() before touching global memory.  cluster > 1:
+// behind that kernel's tail).  Only kernels that wait for their predecessor
+// with griddep_wait() before touching global memory are launched this way:
+// the forward's stream, cluster and merge kernels.  (The backward is not: the
+// wait made its element-by-element loads twice as slow.)  cluster > 1:
 // thread-block clusters of that many blocks along x.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), int64_t grid, int block, size_t smem, cudaStream_t stream,
