@@ -45,8 +45,12 @@
  *    ld columns is read; elsewhere a read may take up to 15 bytes before a
  *    row's column 0 or past its column vocab-1, always within a 16-byte unit
  *    that holds an element of the row.  Those bytes never reach a result.
- *    The backward reads rows that are not 16-byte aligned element by element.
- *    The results are bit-identical for every alignment.
+ *    The backward reads and writes by 16-byte units where the input and the
+ *    output rows are both aligned, or from the first column where both are
+ *    (rows of an input and an output that share their offsets, such as two
+ *    contiguous [N, V] buffers), and element by element otherwise; it never
+ *    touches bytes outside the rows' elements.  The results are bit-identical
+ *    for every alignment.
  *  - bil_logp_fwd on at most 128 rows of a 16-bit type (16 rows when rows
  *    do not start on 16-byte boundaries; tiles of at most 4096) shares each
  *    row among a cluster of 8 blocks instead of streaming it through one
