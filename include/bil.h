@@ -78,21 +78,21 @@ typedef struct CUstream_st *bil_stream_t;
 #define BIL_E_ALIGN 3         /* a pointer is not aligned to its element size */
 #define BIL_E_TARGET_RANGE 4  /* validate=1 found an active target outside [0, vocab) */
 #define BIL_E_CUDA 5          /* a CUDA runtime call failed (launch, copy, device query) */
-#define BIL_E_UNSUPPORTED 6   /* well-formed but beyond this build's limits (see below) */
+#define BIL_E_UNSUPPORTED 6   /* well-formed but beyond this library's limits (see below) */
 
 /* ---- element types ---------------------------------------------------- */
 #define BIL_F32 0
 #define BIL_BF16 1
 #define BIL_F16 2
 
-/* Limits of this build: tile_v is a positive multiple of 8 with
+/* Limits of the library: tile_v is a positive multiple of 8 with
  * tile_v * element_size <= BIL_MAX_TILE_BYTES; the fused forward handles at
  * most BIL_MAX_FUSED_TILES tiles per row (bil_logp_tile_partials and
  * bil_logp_merge have no such limit). */
 #define BIL_MAX_TILE_BYTES (64 * 1024)
 #define BIL_MAX_FUSED_TILES 2048
 
-/* The arithmetic contract of this build as a printable string: the in-tile
+/* The library's arithmetic contract as a printable string: the in-tile
  * lane layout and reduction tree, the exp/log primitives, the merge order.
  * Two builds with the same string give the same bits.  Static storage. */
 const char *bil_contract_id(void);

@@ -399,7 +399,7 @@ const char* bil_status_string(int status) {
     case BIL_E_ALIGN: return "pointer not aligned to its element size";
     case BIL_E_TARGET_RANGE: return "active target outside [0, vocab)";
     case BIL_E_CUDA: return "CUDA runtime error";
-    case BIL_E_UNSUPPORTED: return "beyond this build's limits";
+    case BIL_E_UNSUPPORTED: return "beyond the library's limits";
     default: return "unknown status";
   }
 }
