@@ -92,6 +92,14 @@ typedef struct CUstream_st *bil_stream_t;
 #define BIL_MAX_TILE_BYTES (64 * 1024)
 #define BIL_MAX_FUSED_TILES 2048
 
+/* Every strided buffer a call reads or writes (logits, dlogits, the partials
+ * and, for the LM-head calls, each operand and result) must span at most
+ * BIL_MAX_EXTENT_BYTES: rows x row pitch x element size, 2^48 bytes, more than
+ * any device holds.  A larger extent, or a vocabulary above it, returns
+ * BIL_E_UNSUPPORTED before any CUDA call, so that no offset a kernel forms
+ * can overflow 64 bits. */
+#define BIL_MAX_EXTENT_BYTES ((int64_t)1 << 48)
+
 /* The library's arithmetic contract as a printable string: the in-tile
  * lane layout and reduction tree, the exp/log primitives, the merge order.
  * Two builds with the same string give the same bits.  Static storage. */

@@ -15,6 +15,7 @@ OK, E_INVALID_ARG, E_DTYPE, E_ALIGN, E_TARGET_RANGE, E_CUDA, E_UNSUPPORTED = ran
 F32, BF16, F16 = 0, 1, 2
 MAX_TILE_BYTES = 64 * 1024
 MAX_FUSED_TILES = 2048
+MAX_EXTENT_BYTES = 1 << 48
 LINEAR_TILE_V = 256
 LINEAR_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
 

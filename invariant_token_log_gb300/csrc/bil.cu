@@ -274,11 +274,17 @@ int launch_split(int dtype, bool ent, const StreamParams& p, cudaStream_t stream
   }
 }
 
+// rows x pitch x eb <= BIL_MAX_EXTENT_BYTES, without forming the product.
+bool extent_ok(int64_t rows, int64_t pitch, int64_t eb) {
+  return rows <= 0 || pitch <= BIL_MAX_EXTENT_BYTES / eb / rows;
+}
+
 int check_tile(int dtype, int64_t vocab, int32_t tile_v, int64_t* num_tiles) {
   const int eb = elem_bytes(dtype);
   if (eb == 0) return BIL_E_DTYPE;
   if (tile_v <= 0 || tile_v % kGroup != 0) return BIL_E_INVALID_ARG;
   if (static_cast<int64_t>(tile_v) * eb > BIL_MAX_TILE_BYTES) return BIL_E_UNSUPPORTED;
+  if (vocab > BIL_MAX_EXTENT_BYTES) return BIL_E_UNSUPPORTED;
   *num_tiles = (vocab + tile_v - 1) / tile_v;
   if (*num_tiles > INT32_MAX) return BIL_E_UNSUPPORTED;
   return BIL_OK;
@@ -352,6 +358,8 @@ int temperature_rcp(float temperature, float* rcp) { return ::temperature_rcp(te
 
 int elem_bytes(int dtype) { return ::elem_bytes(dtype); }
 
+bool extent_ok(int64_t rows, int64_t pitch, int64_t eb) { return ::extent_ok(rows, pitch, eb); }
+
 int check_tile(int dtype, int64_t vocab, int32_t tile_v, int64_t* num_tiles) {
   return ::check_tile(dtype, vocab, tile_v, num_tiles);
 }
@@ -410,6 +418,7 @@ int bil_logp_fwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
   if (n_rows < 0 || vocab < 1 || ld < vocab) return BIL_E_INVALID_ARG;
   int64_t num_tiles = 0;
   if (int st = check_tile(dtype, vocab, tile_v, &num_tiles)) return st;
+  if (!extent_ok(n_rows, ld, elem_bytes(dtype))) return BIL_E_UNSUPPORTED;
   float rcp = 1.0f;
   if (int st = temperature_rcp(temperature, &rcp)) return st;
   if (n_rows == 0) return BIL_OK;
@@ -457,6 +466,7 @@ int bil_logp_tile_partials(const void* logits, int dtype, int64_t n_rows, int64_
   const int64_t shard_cols = std::min<int64_t>(static_cast<int64_t>(tile_end) * tile_v, vocab) -
                              static_cast<int64_t>(tile_begin) * tile_v;
   if (ld < shard_cols) return BIL_E_INVALID_ARG;
+  if (!extent_ok(n_rows, ld, elem_bytes(dtype)) || !extent_ok(n_rows, ld_part, 4)) return BIL_E_UNSUPPORTED;
   if (n_rows == 0) return BIL_OK;
   if (logits == nullptr || target_ids == nullptr || part_max == nullptr || part_sum == nullptr ||
       target_logit == nullptr)
@@ -491,6 +501,7 @@ int bil_logp_merge(const float* part_max, const float* part_sum, const float* pa
                    bil_stream_t stream) {
   if (n_rows < 0 || num_tiles < 1 || ld_part < num_tiles || vocab < 1) return BIL_E_INVALID_ARG;
   if ((entropy != nullptr) != (part_ent != nullptr)) return BIL_E_INVALID_ARG;
+  if (!extent_ok(n_rows, ld_part, 4)) return BIL_E_UNSUPPORTED;
   if (n_rows == 0) return BIL_OK;
   if (part_max == nullptr || part_sum == nullptr || target_logit == nullptr || target_ids == nullptr ||
       logp == nullptr)
@@ -528,6 +539,7 @@ int bil_logp_bwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
   const int ob = elem_bytes(dlogits_dtype);
   if (eb == 0 || ob == 0) return BIL_E_DTYPE;
   if (n_rows < 0 || vocab < 1 || ld < vocab || out_cols < vocab || ld_out < out_cols) return BIL_E_INVALID_ARG;
+  if (!extent_ok(n_rows, ld, eb) || !extent_ok(n_rows, ld_out, ob)) return BIL_E_UNSUPPORTED;
   float rcp = 1.0f;
   if (int st = temperature_rcp(temperature, &rcp)) return st;
   if ((entropy != nullptr) != (grad_entropy != nullptr)) return BIL_E_INVALID_ARG;

@@ -31,6 +31,10 @@ BIL_INTERNAL int elem_bytes(int dtype);
 // of 8 of at most BIL_MAX_TILE_BYTES bytes) and the element type.
 BIL_INTERNAL int check_tile(int dtype, int64_t vocab, int32_t tile_v, int64_t* num_tiles);
 
+// rows x pitch x eb within BIL_MAX_EXTENT_BYTES (rows <= 0: nothing spanned).
+// pitch and eb are positive.
+BIL_INTERNAL bool extent_ok(int64_t rows, int64_t pitch, int64_t eb);
+
 // The LM-head kernels' watchdog word of the current device (see
 // bil_watchdog_status); cleared when `clear` is non-zero.
 BIL_INTERNAL int linear_watchdog(unsigned int* flags, int clear);

@@ -750,6 +750,12 @@ Workspace workspace_layout(int64_t n_rows, int64_t num_tiles, bool ent) {
   return w;
 }
 
+// The vocabulary and the [n_rows, num_tiles] partials within the extent limit,
+// so that workspace_layout's sizes cannot overflow.
+bool workspace_fits(int64_t n_rows, int64_t vocab) {
+  return vocab <= BIL_MAX_EXTENT_BYTES && bil_internal::extent_ok(n_rows, (vocab + kBN - 1) / kBN, 4);
+}
+
 // Device scratch of bil_linear_logp_fwd_static: one array per device image,
 // never allocated or freed at run time.
 static __device__ __align__(256) unsigned char g_linear_static_scratch[BIL_LINEAR_STATIC_SCRATCH_BYTES];
@@ -799,6 +805,7 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   if (n_rows < 0 || hidden_size < 1 || vocab < 1 || ld_hidden < hidden_size || ld_weight < hidden_size)
     return BIL_E_INVALID_ARG;
+  if (vocab > BIL_MAX_EXTENT_BYTES) return BIL_E_UNSUPPORTED;
   const int64_t num_tiles = (vocab + kBN - 1) / kBN;
   if (num_tiles > INT32_MAX / 2) return BIL_E_UNSUPPORTED;
   if (tile_begin < 0 || tile_begin >= tile_end || tile_end > num_tiles || ld_part < num_tiles)
@@ -809,6 +816,10 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
     if (logits_dtype != BIL_F32 && logits_dtype != BIL_BF16) return BIL_E_DTYPE;
     if (ld_logits < shard_cols) return BIL_E_INVALID_ARG;
   }
+  if (!bil_internal::extent_ok(n_rows, ld_hidden, 2) || !bil_internal::extent_ok(shard_cols, ld_weight, 2) ||
+      !bil_internal::extent_ok(n_rows, ld_part, 4) ||
+      (logits != nullptr && !bil_internal::extent_ok(n_rows, ld_logits, logits_dtype == BIL_F32 ? 4 : 2)))
+    return BIL_E_UNSUPPORTED;
   float rcp = 1.0f;
   if (int st = bil_internal::temperature_rcp(temperature, &rcp)) return st;
   if (n_rows == 0) return BIL_OK;
@@ -864,6 +875,7 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
 
 int bil_linear_logp_workspace_bytes(int64_t n_rows, int64_t vocab, int entropy, int64_t* bytes) {
   if (n_rows < 0 || vocab < 1 || bytes == nullptr) return BIL_E_INVALID_ARG;
+  if (!workspace_fits(n_rows, vocab)) return BIL_E_UNSUPPORTED;
   const int64_t num_tiles = (vocab + kBN - 1) / kBN;
   *bytes = static_cast<int64_t>(workspace_layout(n_rows, num_tiles, entropy != 0).total);
   return BIL_OK;
@@ -875,6 +887,7 @@ int bil_linear_logp_fwd(const void* hidden, const void* weight, int dtype, int64
                         void* logits, int logits_dtype, int64_t ld_logits, void* workspace,
                         int64_t workspace_bytes, int validate, bil_stream_t stream) {
   if (n_rows < 0 || vocab < 1) return BIL_E_INVALID_ARG;
+  if (!workspace_fits(n_rows, vocab)) return BIL_E_UNSUPPORTED;
   const int64_t num_tiles = (vocab + kBN - 1) / kBN;
   const Workspace w = workspace_layout(n_rows, num_tiles, entropy != nullptr);
   if (n_rows == 0) return BIL_OK;
@@ -922,6 +935,8 @@ int bil_transpose_2d(const void* src, int dtype, int64_t rows, int64_t cols, int
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   if (rows < 0 || cols < 0 || ld_src < cols || ld_dst < rows) return BIL_E_INVALID_ARG;
   if (rows == 0 || cols == 0) return BIL_OK;
+  if (!bil_internal::extent_ok(rows, ld_src, 2) || !bil_internal::extent_ok(cols, ld_dst, 2))
+    return BIL_E_UNSUPPORTED;
   if (src == nullptr || dst == nullptr) return BIL_E_INVALID_ARG;
   if (!aligned_to(src, 2) || !aligned_to(dst, 2)) return BIL_E_ALIGN;
   return launch_transpose16(src, rows, cols, ld_src, dst, ld_dst, reinterpret_cast<cudaStream_t>(stream));
@@ -938,6 +953,7 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
   for (int ot : {dhidden_dtype, dweight_dtype})
     if (ot != BIL_F32 && ot != dtype) return BIL_E_DTYPE;
   if (vocab < 1) return BIL_E_INVALID_ARG;
+  if (vocab > BIL_MAX_EXTENT_BYTES) return BIL_E_UNSUPPORTED;
   const int64_t num_tiles = (vocab + kBN - 1) / kBN;
   if (num_tiles > INT32_MAX / 2) return BIL_E_UNSUPPORTED;
   if (tile_begin < 0 || tile_begin >= tile_end || tile_end > num_tiles) return BIL_E_INVALID_ARG;
@@ -949,6 +965,15 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
       ld_dhidden < hidden_size || ld_dweight < hidden_size)
     return BIL_E_INVALID_ARG;
   if ((entropy == nullptr) != (grad_entropy == nullptr)) return BIL_E_INVALID_ARG;
+  {
+    using bil_internal::extent_ok;
+    const int64_t eh = dhidden_dtype == BIL_F32 ? 4 : 2, ew = dweight_dtype == BIL_F32 ? 4 : 2;
+    if (!extent_ok(n_rows, ld_hidden, 2) || !extent_ok(cols, ld_weight, 2) ||
+        !extent_ok(hidden_size, ld_weight_t, 2) || !extent_ok(n_rows, ld_dz, 2) || !extent_ok(cols, ld_dz_t, 2) ||
+        !extent_ok(hidden_size, ld_hidden_t, 2) || !extent_ok(n_rows, ld_dhidden, eh) ||
+        !extent_ok(cols, ld_dweight, ew))
+      return BIL_E_UNSUPPORTED;
+  }
   float rcp = 1.0f;
   if (int st = bil_internal::temperature_rcp(temperature, &rcp)) return st;
   if (weight == nullptr || weight_t == nullptr || dweight == nullptr) return BIL_E_INVALID_ARG;
@@ -1063,6 +1088,7 @@ int bil_linear_logp_fwd_static(const void* hidden, const void* weight, int dtype
                                float temperature, const int64_t* target_ids, int64_t ignore_index, float* logp,
                                float* lse, float* entropy, int validate, bil_stream_t stream) {
   if (n_rows < 0 || vocab < 1) return BIL_E_INVALID_ARG;
+  if (!workspace_fits(n_rows, vocab)) return BIL_E_UNSUPPORTED;
   const int64_t num_tiles = (vocab + kBN - 1) / kBN;
   const Workspace w = workspace_layout(n_rows, num_tiles, entropy != nullptr);
   if (w.total > BIL_LINEAR_STATIC_SCRATCH_BYTES) return BIL_E_UNSUPPORTED;

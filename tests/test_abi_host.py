@@ -49,6 +49,8 @@ def test_header_constants_match_binding():
     assert (int(consts["BIL_F32"]), int(consts["BIL_BF16"]), int(consts["BIL_F16"])) == (_lib.F32, _lib.BF16, _lib.F16)
     assert eval(consts["BIL_MAX_TILE_BYTES"]) == _lib.MAX_TILE_BYTES
     assert int(consts["BIL_MAX_FUSED_TILES"]) == _lib.MAX_FUSED_TILES
+    assert re.search(r"#define BIL_MAX_EXTENT_BYTES \(\(int64_t\)1 << 48\)", text)
+    assert _lib.MAX_EXTENT_BYTES == 2 ** 48
 
 
 def test_contract_id_and_status_strings(lib):
@@ -95,6 +97,13 @@ def fwd(lib, **kw):
     (dict(tgt=ctypes.c_void_p(0x10004)), _lib.E_ALIGN),
     (dict(ent=FAKE_ODD), _lib.E_ALIGN),
     (dict(vocab=8 * 2049, ld=8 * 2049, tile=8), _lib.E_UNSUPPORTED),
+    # rows x pitch x element size above 2^48 bytes; exactly 2^48 passes the extent check
+    (dict(n=2 ** 20, vocab=300, ld=2 ** 27 + 8), _lib.E_UNSUPPORTED),
+    (dict(n=2 ** 40, vocab=300, ld=304), _lib.E_UNSUPPORTED),
+    (dict(n=2 ** 62, vocab=300, ld=300), _lib.E_UNSUPPORTED),
+    (dict(n=2 ** 20, vocab=300, ld=2 ** 27, logits=NULL), _lib.E_INVALID_ARG),
+    (dict(vocab=2 ** 48 + 1, ld=2 ** 48 + 1), _lib.E_UNSUPPORTED),
+    (dict(vocab=2 ** 63 - 1, ld=2 ** 63 - 1), _lib.E_UNSUPPORTED),
     (dict(n=0), _lib.OK),
     (dict(n=0, logits=NULL, tgt=NULL, logp=NULL), _lib.OK),
 ])
@@ -116,6 +125,9 @@ def test_partials_rejects_bad_ranges(lib):
     assert call(temp=0.0) == _lib.E_INVALID_ARG
     assert call(pe=FAKE_ODD) == _lib.E_ALIGN
     assert call(n=0) == _lib.OK
+    assert call(n=2 ** 40) == _lib.E_UNSUPPORTED                       # logits extent above 2^48 bytes
+    assert call(n=2 ** 20, ldp=2 ** 26 + 1) == _lib.E_UNSUPPORTED      # partials extent above 2^48 bytes
+    assert call(vocab=2 ** 63 - 1, e=1, ld=4096) == _lib.E_UNSUPPORTED  # ceil(vocab / tile) cannot overflow
 
 
 def test_merge_and_bwd_reject_bad_arguments(lib):
@@ -145,3 +157,48 @@ def test_merge_and_bwd_reject_bad_arguments(lib):
     assert with_(ent=FAKE) == _lib.E_INVALID_ARG             # entropy without its gradient
     assert with_(gent=FAKE) == _lib.E_INVALID_ARG
     assert with_(n=0) == _lib.OK
+    assert with_(n=2 ** 40) == _lib.E_UNSUPPORTED                          # input extent above 2^48 bytes
+    assert with_(odt=_lib.F32, n=2 ** 20, ldo=2 ** 26 + 4) == _lib.E_UNSUPPORTED  # output extent
+    assert m(FAKE, FAKE, NULL, 2 ** 40, 3, 2 ** 7, FAKE, FAKE, -100, 10, FAKE, FAKE, NULL, 0, NULL) == \
+        _lib.E_UNSUPPORTED
+
+
+def test_lm_head_calls_reject_extents_above_the_limit(lib):
+    """The LM-head entries refuse buffers spanning more than 2^48 bytes, and
+    vocabularies above it, on the host; these calls would otherwise reach a
+    launch (a CUDA error without a GPU)."""
+    big = _lib.MAX_EXTENT_BYTES
+    out = ctypes.c_int64(0)
+    ws = lib.bil_linear_logp_workspace_bytes
+    assert ws(4, 1000, 0, ctypes.byref(out)) == _lib.OK
+    part = -(-4 * 4 * 4 // 256) * 256       # [4 rows, 4 tiles of 256] float32, 256-byte aligned
+    assert out.value == 2 * part + 256
+    assert ws(2 ** 40, 151936, 0, ctypes.byref(out)) == _lib.E_UNSUPPORTED
+    assert ws(4, 2 ** 63 - 1, 1, ctypes.byref(out)) == _lib.E_UNSUPPORTED
+    assert ws(-1, 1000, 0, ctypes.byref(out)) == _lib.E_INVALID_ARG
+
+    def partials(**kw):
+        a = dict(n=4, ld_h=64, vocab=1000, ld_w=64, te=4, ldp=4, logits=NULL, ldl=0)
+        a.update(kw)
+        return lib.bil_linear_logp_partials(FAKE, FAKE, _lib.BF16, a["n"], 64, a["ld_h"], a["vocab"], a["ld_w"], 0,
+                                            a["te"], 1.0, FAKE, -100, FAKE, FAKE, NULL, a["ldp"], FAKE, a["logits"],
+                                            _lib.F32, a["ldl"], NULL)
+    assert partials(n=2 ** 20, ld_h=2 ** 30) == _lib.E_UNSUPPORTED                 # hidden: 2^51 bytes
+    assert partials(ld_w=2 ** 40) == _lib.E_UNSUPPORTED                            # 1000 weight rows
+    assert partials(n=2 ** 20, ldp=2 ** 27) == _lib.E_UNSUPPORTED                  # partials: 2^49 bytes
+    assert partials(n=2 ** 20, logits=FAKE, ldl=2 ** 28) == _lib.E_UNSUPPORTED     # logits: 2^50 bytes
+    assert partials(vocab=2 ** 63 - 1) == _lib.E_UNSUPPORTED
+    assert partials(vocab=big + 1) == _lib.E_UNSUPPORTED
+
+    assert lib.bil_transpose_2d(FAKE, _lib.BF16, 2 ** 20, 8, 2 ** 28, FAKE, 2 ** 20, NULL) == _lib.E_UNSUPPORTED
+    assert lib.bil_transpose_2d(FAKE, _lib.BF16, 8, 2 ** 20, 2 ** 20, FAKE, 2 ** 47, NULL) == _lib.E_UNSUPPORTED
+
+    def bwd(**kw):
+        a = dict(n=4, vocab=1000, ld_dz=1000, ld_dzt=8, ld_ht=8, ld_dw=64)
+        a.update(kw)
+        return lib.bil_linear_logp_bwd(FAKE, FAKE, FAKE, _lib.BF16, a["n"], 64, 64, a["vocab"], 64, 1000, 0, 4, 1.0,
+                                       FAKE, -100, FAKE, FAKE, NULL, NULL, FAKE, a["ld_dz"], FAKE, a["ld_dzt"], FAKE,
+                                       a["ld_ht"], FAKE, _lib.F32, 64, FAKE, _lib.F32, a["ld_dw"], NULL)
+    assert bwd(n=2 ** 20, ld_dz=2 ** 28, ld_dzt=2 ** 20, ld_ht=2 ** 20) == _lib.E_UNSUPPORTED  # dZ: 2^49 bytes
+    assert bwd(ld_dw=2 ** 40) == _lib.E_UNSUPPORTED                                           # dweight
+    assert bwd(vocab=2 ** 63 - 1) == _lib.E_UNSUPPORTED
