@@ -125,7 +125,11 @@ static double load_raw(const void *base, int dtype, int64_t row, int64_t ld, int
 
 static double z_at(const RowView *v, int64_t col) {
     double x = load_raw(v->base, v->dtype, v->row, v->ld, col);
+#ifdef BIL_ORACLE_MUTANT_TEMPERATURE_MULTIPLIES
+    return v->temperature == 1.0 ? x : x * v->temperature;
+#else
     return v->temperature == 1.0 ? x : x / v->temperature;
+#endif
 }
 
 /* ---- log-sum-exp over columns [c0, c1) of one row --------------------------
@@ -329,7 +333,11 @@ void bil_oracle_tile_partials(const void *logits, int dtype, int64_t n_rows, int
 #endif
                 max_and_sumexp(&v, c0, c1, &m, &s, &u);
                 if (t_id >= c0 && t_id < c1) {
+#ifdef BIL_ORACLE_MUTANT_TARGET_LOGIT_UNSCALED
+                    target_logit[r] = load_raw(v.base, v.dtype, v.row, v.ld, t_id);
+#else
                     target_logit[r] = z_at(&v, t_id);
+#endif
                 }
             }
             part_max[r * ld_part + t] = m;
@@ -393,7 +401,11 @@ int64_t bil_oracle_merge(const double *part_max, const double *part_sum, const d
 #endif
                 S += s[t] * w;
                 if (part_ent != NULL && s[t] != 0.0) { /* an empty tile adds nothing */
+#ifdef BIL_ORACLE_MUTANT_MERGE_ENTROPY_DROPS_SHIFT
+                    U += w * part_ent[r * ld_part + t];
+#else
                     U += w * (part_ent[r * ld_part + t] + (m[t] - M) * s[t]);
+#endif
                 }
             }
             L = M + log(S);
@@ -472,7 +484,11 @@ int64_t bil_oracle_logp_bwd(const void *logits, int dtype, int64_t n_rows, int64
                 dz -= gh * p * (z - L + H);
 #endif
             }
+#ifdef BIL_ORACLE_MUTANT_BWD_TEMPERATURE_DROPPED
+            d[c] = dz;
+#else
             d[c] = temperature == 1.0 ? dz : dz / temperature;
+#endif
         }
     }
     return bad;

@@ -232,6 +232,42 @@ def check_tiles(defines=()):
                         seg = vals[r, k * tile: min(v, (k + 1) * tile)]
                         assert pm[r, k] == seg.max()
                         assert 1.0 <= ps[r, k] <= len(seg)
+    check_tiles_with_temperature(defines)
+
+
+def check_tiles_with_temperature(defines=()):
+    """Tile partials at a temperature T, split and merged, against the library
+    log-softmax of x / T ("Reference Semantics" with the logits divided by T
+    before the softmax); the copied target logit is x_t / T, and the tile
+    maxima are the stored maxima divided by T."""
+    import torch
+    v, n, tile = 1000, 5, 64
+    x = _rows(6, n, v, scale=3.0, dtype="bfloat16")
+    t = _targets(6, n, v, ignore_rows=(1,))
+    vals = oracle.widen(x, "bfloat16")
+    active = t != wl.IGNORE_INDEX
+    nt = -(-v // tile)
+    for temp in (0.7, 2.0):
+        ref_all = torch.log_softmax(torch.from_numpy(vals) / temp, -1)
+        ref_lse = torch.logsumexp(torch.from_numpy(vals) / temp, -1).numpy()
+        for split in (1, 3):
+            pm = np.full((n, nt), -np.inf)
+            ps = np.zeros((n, nt))
+            tl = np.full(n, np.nan)
+            bounds = [(k * nt) // split for k in range(split + 1)]
+            for k in reversed(range(split)):
+                oracle.tile_partials(x, "bfloat16", v, tile, bounds[k], bounds[k + 1], t, part_max=pm, part_sum=ps,
+                                     target_logit=tl, temperature=temp, defines=defines)
+            logp, lse, _ = oracle.merge(pm, ps, tl, t, v, defines=defines)
+            for r in range(n):
+                if not active[r]:
+                    assert logp[r] == 0.0 and lse[r] == 0.0
+                    continue
+                assert abs(logp[r] - float(ref_all[r, t[r]])) <= 1e-12, (temp, split, r)
+                assert abs(lse[r] - ref_lse[r]) <= 1e-12 * max(1.0, abs(ref_lse[r]))
+                assert tl[r] == vals[r, t[r]] / temp
+                for k in range(nt):
+                    assert pm[r, k] == vals[r, k * tile: min(v, (k + 1) * tile)].max() / temp
 
 
 def check_contract_rules(defines=()):

@@ -36,6 +36,10 @@ MUTANTS = [
     "BIL_ORACLE_MUTANT_LINEAR_DROPS_LAST_K",   # projection sum stops one term early
     "BIL_ORACLE_MUTANT_LINEAR_BWD_DX_TRANSPOSED",  # dhidden contracts with the weight read as [H, V]
     "BIL_ORACLE_MUTANT_LINEAR_BWD_DW_ROW_SHIFT",   # dweight pairs dZ row r with hidden row r + 1
+    "BIL_ORACLE_MUTANT_TEMPERATURE_MULTIPLIES",    # z = x * T instead of x / T
+    "BIL_ORACLE_MUTANT_TARGET_LOGIT_UNSCALED",     # the partials' target logit skips the temperature
+    "BIL_ORACLE_MUTANT_MERGE_ENTROPY_DROPS_SHIFT", # the entropy merge drops the (m_t - M) s_t term
+    "BIL_ORACLE_MUTANT_BWD_TEMPERATURE_DROPPED",   # the backward's final 1/T factor is dropped
 ]
 
 
