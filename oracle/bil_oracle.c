@@ -162,18 +162,24 @@ static void max_and_sumexp(const RowView *v, int64_t c0, int64_t c1, double *m_o
 #endif
             s += e;
             if (e != 0.0) { /* p log p -> 0 as p -> 0: an -inf logit adds nothing */
+#ifdef BIL_ORACLE_MUTANT_PART_ENT_UNWEIGHTED
+                u += d;
+#else
                 u += e * d;
+#endif
             }
         }
     } else {
         /* every entry is -inf (or the range is empty of finite values);
          * a NaN entry still poisons the sums */
+#ifndef BIL_ORACLE_MUTANT_NAN_NOT_PROPAGATED
         for (int64_t c = c0; c < c1; ++c) {
             if (isnan(z_at(v, c))) {
                 s = NAN;
                 u = NAN;
             }
         }
+#endif
     }
     *m_out = m;
     *s_out = s;
@@ -283,7 +289,11 @@ int64_t bil_oracle_logp_fwd(const void *logits, int dtype, int64_t n_rows, int64
         if (entropy != NULL) {
             entropy[r] = row_entropy(&v, vocab, L);
         }
+#ifdef BIL_ORACLE_MUTANT_RANGE_ALLOWS_VOCAB
+        if (t < 0 || t > vocab) {
+#else
         if (t < 0 || t >= vocab) {
+#endif
             logp[r] = NAN;
             bad += 1;
             continue;

@@ -290,6 +290,38 @@ def check_contract_rules(defines=()):
     assert bad == 0
     assert np.all(d[0] == 0.0) and np.all(d[2] == 0.0) and np.all(d[:, v:] == 0.0)
     assert not np.signbit(d[0]).any()
+    check_nan_and_infinite_rows(defines)
+
+
+def check_nan_and_infinite_rows(defines=()):
+    """NaN and all -inf rows (a reading: the pages are silent) behave as the
+    library's logsumexp and log-softmax do: a NaN anywhere in the row, even
+    among -inf logits, gives NaN; an all -inf row gives lse = -inf and a NaN
+    logp.  The whole-row forward and merged tile partials (the NaN in a tile of
+    -inf) agree."""
+    import torch
+    v, tile = 64, 16
+    x = np.tile(np.float32(0.5) * np.arange(v, dtype=np.float32), (4, 1))
+    x[0, 10] = np.nan                       # NaN among finite logits
+    x[1, :] = -np.inf                       # every logit -inf
+    x[2, :] = -np.inf
+    x[2, 40] = np.nan                       # NaN among -inf logits
+    t = np.full(4, 3, np.int64)
+    xt = torch.from_numpy(x.astype(np.float64))
+    ref_lse = torch.logsumexp(xt, -1).numpy()
+    ref_logp = torch.log_softmax(xt, -1)[:, 3].numpy()
+    assert np.isnan(ref_lse[0]) and ref_lse[1] == -np.inf and np.isnan(ref_lse[2])
+    logp, lse, bad = oracle.logp_fwd(x, "float32", v, t, defines=defines)
+    nt = v // tile
+    pm, ps, tl = oracle.tile_partials(x, "float32", v, tile, 0, nt, t, defines=defines)
+    mlogp, mlse, mbad = oracle.merge(pm, ps, tl, t, v, defines=defines)
+    assert bad == 0 and mbad == 0
+    for got_logp, got_lse in ((logp, lse), (mlogp, mlse)):
+        for r in range(3):
+            assert np.isnan(got_logp[r]), r
+            assert np.isnan(got_lse[r]) if np.isnan(ref_lse[r]) else got_lse[r] == ref_lse[r], r
+        assert abs(got_logp[3] - ref_logp[3]) <= 1e-12 and abs(got_lse[3] - ref_lse[3]) <= 1e-12
+    assert np.isnan(ps[2, 40 // tile]) and pm[2, 40 // tile] == -np.inf   # the tile holding the NaN
 
 
 def check_minimal_example(defines=()):

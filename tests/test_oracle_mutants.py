@@ -40,6 +40,9 @@ MUTANTS = [
     "BIL_ORACLE_MUTANT_TARGET_LOGIT_UNSCALED",     # the partials' target logit skips the temperature
     "BIL_ORACLE_MUTANT_MERGE_ENTROPY_DROPS_SHIFT", # the entropy merge drops the (m_t - M) s_t term
     "BIL_ORACLE_MUTANT_BWD_TEMPERATURE_DROPPED",   # the backward's final 1/T factor is dropped
+    "BIL_ORACLE_MUTANT_PART_ENT_UNWEIGHTED",       # the entropy partial sums (z - m) without exp(z - m)
+    "BIL_ORACLE_MUTANT_NAN_NOT_PROPAGATED",        # a NaN among -inf logits is dropped
+    "BIL_ORACLE_MUTANT_RANGE_ALLOWS_VOCAB",        # target == vocab taken as valid
 ]
 
 
