@@ -223,12 +223,14 @@ def test_out_of_range_targets():
 
 def test_special_values():
     v = 600
-    x = np.zeros((4, v), np.float32)
+    x = np.zeros((5, v), np.float32)
     x[0] = -np.inf                 # no distribution at all
     x[1, 17] = np.nan              # NaN poisons its row only
     x[2, :300] = -np.inf           # half the row impossible
     x[3] = np.linspace(-5, 5, v)
-    t = np.array([3, 3, 400, 599], np.int64)
+    x[4] = -np.inf
+    x[4, 450] = np.nan             # a NaN in a tile of -inf (max -inf) still poisons the row
+    t = np.array([3, 3, 400, 599, 3], np.int64)
     xd = torch.from_numpy(x).cuda()
     logp, lse = bil.logp_fwd(xd, torch.from_numpy(t).cuda(), -100, 256)
     ref_logp, ref_lse, _ = oracle.logp_fwd(x, "float32", v, t)
