@@ -202,3 +202,40 @@ def test_lm_head_calls_reject_extents_above_the_limit(lib):
     assert bwd(n=2 ** 20, ld_dz=2 ** 28, ld_dzt=2 ** 20, ld_ht=2 ** 20) == _lib.E_UNSUPPORTED  # dZ: 2^49 bytes
     assert bwd(ld_dw=2 ** 40) == _lib.E_UNSUPPORTED                                           # dweight
     assert bwd(vocab=2 ** 63 - 1) == _lib.E_UNSUPPORTED
+
+
+def test_sum_transpose_and_stream_shape_check_their_arguments(lib):
+    srcs = (ctypes.c_void_p * 17)(*([0x10000] * 17))
+    s = lib.bil_sum_f32
+    assert s(srcs, 0, 8, FAKE, NULL) == _lib.E_INVALID_ARG          # no sources
+    assert s(srcs, 17, 8, FAKE, NULL) == _lib.E_INVALID_ARG         # more than 16 sources
+    assert s(srcs, 2, -1, FAKE, NULL) == _lib.E_INVALID_ARG
+    assert s(srcs, 2, 8, NULL, NULL) == _lib.E_INVALID_ARG
+    assert s(None, 2, 8, FAKE, NULL) == _lib.E_INVALID_ARG
+    holes = (ctypes.c_void_p * 2)(0x10000, None)
+    assert s(holes, 2, 8, FAKE, NULL) == _lib.E_INVALID_ARG         # a null source
+    odd = (ctypes.c_void_p * 2)(0x10000, 0x10002)
+    assert s(odd, 2, 8, FAKE, NULL) == _lib.E_ALIGN
+    assert s(srcs, 2, 8, ctypes.c_void_p(0x10001), NULL) == _lib.E_ALIGN
+    assert s(srcs, 16, 0, FAKE, NULL) == _lib.OK                    # nothing to add
+
+    t = lib.bil_transpose_2d
+    assert t(FAKE, _lib.F32, 4, 4, 4, FAKE, 4, NULL) == _lib.E_DTYPE  # 16-bit elements only
+    assert t(FAKE, _lib.BF16, 4, 5, 4, FAKE, 4, NULL) == _lib.E_INVALID_ARG   # ld_src < cols
+    assert t(FAKE, _lib.BF16, 5, 4, 4, FAKE, 4, NULL) == _lib.E_INVALID_ARG   # ld_dst < rows
+    assert t(FAKE, _lib.BF16, 4, 4, 4, FAKE_ODD, 4, NULL) == _lib.E_ALIGN
+    assert t(NULL, _lib.F16, 4, 4, 4, FAKE, 4, NULL) == _lib.E_INVALID_ARG
+    assert t(NULL, _lib.F16, 0, 4, 4, NULL, 4, NULL) == _lib.OK        # empty
+
+    st, co, sm = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int64(0)
+    shape = lib.bil_stream_shape
+    assert shape(_lib.BF16, 4096, 38, 1, 0, ctypes.byref(st), ctypes.byref(co), ctypes.byref(sm)) == _lib.OK
+    assert st.value >= 2 and co.value >= 1 and st.value % co.value == 0 and sm.value > 0
+    assert shape(9, 4096, 38, 1, 0, ctypes.byref(st), ctypes.byref(co), ctypes.byref(sm)) == _lib.E_DTYPE
+    assert shape(_lib.BF16, 12, 38, 1, 0, ctypes.byref(st), ctypes.byref(co), ctypes.byref(sm)) == \
+        _lib.E_INVALID_ARG
+    assert shape(_lib.BF16, 4096, 0, 1, 0, ctypes.byref(st), ctypes.byref(co), ctypes.byref(sm)) == \
+        _lib.E_INVALID_ARG
+    assert shape(_lib.F32, 32768, 38, 1, 0, ctypes.byref(st), ctypes.byref(co), ctypes.byref(sm)) == \
+        _lib.E_UNSUPPORTED
+    assert shape(_lib.BF16, 4096, 38, 1, 0, None, ctypes.byref(co), ctypes.byref(sm)) == _lib.E_INVALID_ARG
