@@ -183,6 +183,24 @@ def test_lm_head_calls_reject_extents_above_the_limit(lib):
         return lib.bil_linear_logp_partials(FAKE, FAKE, _lib.BF16, a["n"], 64, a["ld_h"], a["vocab"], a["ld_w"], 0,
                                             a["te"], 1.0, FAKE, -100, FAKE, FAKE, NULL, a["ldp"], FAKE, a["logits"],
                                             _lib.F32, a["ldl"], NULL)
+    # the plain argument checks
+    def partials_dt(dtype, **kw):
+        a = dict(n=4, h=64, ld_h=64, vocab=1000, ld_w=64, tb=0, te=4, ldp=4, hidden=FAKE, logits=NULL,
+                 ldt=_lib.F32, ldl=0)
+        a.update(kw)
+        return lib.bil_linear_logp_partials(a["hidden"], FAKE, dtype, a["n"], a["h"], a["ld_h"], a["vocab"],
+                                            a["ld_w"], a["tb"], a["te"], 1.0, FAKE, -100, FAKE, FAKE, NULL, a["ldp"],
+                                            FAKE, a["logits"], a["ldt"], a["ldl"], NULL)
+    assert partials_dt(_lib.F32) == _lib.E_DTYPE                       # 16-bit operands only
+    assert partials_dt(_lib.BF16, ld_h=63) == _lib.E_INVALID_ARG       # ld_hidden < hidden_size
+    assert partials_dt(_lib.BF16, te=5) == _lib.E_INVALID_ARG          # 1000 columns are 4 tiles of 256
+    assert partials_dt(_lib.BF16, tb=2, te=2) == _lib.E_INVALID_ARG
+    assert partials_dt(_lib.BF16, ldp=3) == _lib.E_INVALID_ARG
+    assert partials_dt(_lib.BF16, logits=FAKE, ldt=_lib.F16, ldl=1000) == _lib.E_DTYPE
+    assert partials_dt(_lib.BF16, logits=FAKE, ldl=999) == _lib.E_INVALID_ARG
+    assert partials_dt(_lib.BF16, hidden=ctypes.c_void_p(0x10008)) == _lib.E_ALIGN   # TMA: 16-byte base
+    assert partials_dt(_lib.BF16, h=60, ld_h=60) == _lib.E_ALIGN        # TMA: 16-byte row stride
+    assert partials_dt(_lib.F16, n=0) == _lib.OK
     assert partials(n=2 ** 20, ld_h=2 ** 30) == _lib.E_UNSUPPORTED                 # hidden: 2^51 bytes
     assert partials(ld_w=2 ** 40) == _lib.E_UNSUPPORTED                            # 1000 weight rows
     assert partials(n=2 ** 20, ldp=2 ** 27) == _lib.E_UNSUPPORTED                  # partials: 2^49 bytes
