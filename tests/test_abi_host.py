@@ -217,6 +217,26 @@ def test_lm_head_calls_reject_extents_above_the_limit(lib):
         return lib.bil_linear_logp_bwd(FAKE, FAKE, FAKE, _lib.BF16, a["n"], 64, 64, a["vocab"], 64, 1000, 0, 4, 1.0,
                                        FAKE, -100, FAKE, FAKE, NULL, NULL, FAKE, a["ld_dz"], FAKE, a["ld_dzt"], FAKE,
                                        a["ld_ht"], FAKE, _lib.F32, 64, FAKE, _lib.F32, a["ld_dw"], NULL)
+    def bwd_args(**kw):
+        a = dict(dtype=_lib.BF16, n=4, vocab=1000, ld_wt=1000, te=4, ent=NULL, gent=NULL, ld_dz=1000, ld_dzt=8,
+                 ld_ht=8, dh_t=_lib.F32, dw_t=_lib.F32, weight=FAKE, dweight=FAKE, dz=FAKE)
+        a.update(kw)
+        return lib.bil_linear_logp_bwd(FAKE, a["weight"], FAKE, a["dtype"], a["n"], 64, 64, a["vocab"], 64,
+                                       a["ld_wt"], 0, a["te"], 1.0, FAKE, -100, FAKE, FAKE, a["ent"], a["gent"],
+                                       a["dz"], a["ld_dz"], FAKE, a["ld_dzt"], FAKE, a["ld_ht"], FAKE, a["dh_t"], 64,
+                                       a["dweight"], a["dw_t"], 64, NULL)
+    assert bwd_args(dtype=_lib.F32) == _lib.E_DTYPE
+    assert bwd_args(dh_t=_lib.F16) == _lib.E_DTYPE             # outputs: float32 or the input type
+    assert bwd_args(dw_t=_lib.F16) == _lib.E_DTYPE
+    assert bwd_args(te=5) == _lib.E_INVALID_ARG                # beyond the 4 tiles of 1000 columns
+    assert bwd_args(ld_wt=999) == _lib.E_INVALID_ARG           # W^T narrower than the shard
+    assert bwd_args(ld_dz=999) == _lib.E_INVALID_ARG
+    assert bwd_args(ld_dzt=3) == _lib.E_INVALID_ARG            # dZ^T narrower than the rows
+    assert bwd_args(ld_ht=3) == _lib.E_INVALID_ARG
+    assert bwd_args(ent=FAKE) == _lib.E_INVALID_ARG            # entropy without its gradient
+    assert bwd_args(weight=NULL) == _lib.E_INVALID_ARG
+    assert bwd_args(weight=ctypes.c_void_p(0x10008)) == _lib.E_ALIGN
+    assert bwd_args(dz=NULL) == _lib.E_INVALID_ARG
     assert bwd(n=2 ** 20, ld_dz=2 ** 28, ld_dzt=2 ** 20, ld_ht=2 ** 20) == _lib.E_UNSUPPORTED  # dZ: 2^49 bytes
     assert bwd(ld_dw=2 ** 40) == _lib.E_UNSUPPORTED                                           # dweight
     assert bwd(vocab=2 ** 63 - 1) == _lib.E_UNSUPPORTED
