@@ -278,6 +278,8 @@ def ncu_traffic(kernel: str, source: str = KERNEL_SOURCE):
         return None
     sha = hashlib.sha256(open(source, "rb").read()).hexdigest()[:16]
     for line in lines:
+        if line.lstrip().startswith("#"):
+            continue
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
         if f.get("kernel") == kernel and f.get("source_sha") == sha and "bytes_per_launch" in f:
             return float(f["bytes_per_launch"])
