@@ -57,3 +57,28 @@ def test_package_never_imports_the_oracle():
             assert not name.split(".")[0] == "oracle", f"{path} imports {name}"
         text = open(path).read()
         assert "bil_oracle" not in text, path
+
+
+def test_bench_imports_the_oracle_only_in_its_cpu_legs():
+    """bench.py may run the oracle only for the CPU baseline and the reference
+    arm; the timed CUDA path never imports it."""
+    allowed = {"oracle_rows_per_s", "run_reference", "_linear_oracle_step", "oracle_linear_rows_per_s",
+               "run_linear_reference"}
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    for node in tree.body:
+        assert "oracle" not in set(_imports_of(node)), "bench.py imports the oracle at module level"
+    found = set()
+    for fn in ast.walk(tree):
+        if isinstance(fn, ast.FunctionDef):
+            for node in ast.walk(fn):
+                if "oracle" in set(_imports_of(node)):
+                    found.add(fn.name)
+    assert found and found <= allowed, found - allowed
+
+
+def _imports_of(node):
+    if isinstance(node, ast.Import):
+        return [a.name.split(".")[0] for a in node.names]
+    if isinstance(node, ast.ImportFrom):
+        return [(node.module or "").split(".")[0]]
+    return []
