@@ -49,10 +49,13 @@ def _ld(x2: torch.Tensor) -> int:
 
 
 def num_tiles(vocab: int) -> int:
+    """Vocabulary tiles of the fused LM-head: ceil(vocab / 256), the GEMM's N tile."""
     return -(-vocab // LINEAR_TILE_V)
 
 
 def workspace_bytes(n_rows: int, vocab: int, entropy: bool = False) -> int:
+    """Device scratch bytes bil_linear_logp_fwd needs for n_rows rows: the [n_rows, num_tiles]
+    float32 partials (max, sum-exp and, with the entropy, its sums) and the target logits."""
     out = ctypes.c_int64(0)
     _lib.check("bil_linear_logp_workspace_bytes",
                _lib.load().bil_linear_logp_workspace_bytes(n_rows, vocab, int(entropy), ctypes.byref(out)))
