@@ -95,7 +95,7 @@ def _watchdog():
 def test_a_c_program_gets_the_bindings_bits(tmp_path):
     gcc = shutil.which("gcc")
     if gcc is None:
-        pytest.skip("no C compiler")
+        pytest.fail("no C compiler: gcc builds the oracle too, so it must be on PATH")
     _lib.load()
     libdir = os.path.dirname(_lib.library_path())
     cudalib = os.path.join(CUDA, "lib64")
