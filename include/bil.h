@@ -405,8 +405,11 @@ int bil_transpose_2d(const void *src, int dtype, int64_t rows, int64_t cols, int
  * 1763 rows, or 1176 with the entropy).
  *
  *  First call on each device: the call looks up the array's device address
- *  (cudaGetSymbolAddress, with that device current) and keeps it; make that
- *  first call before any stream capture on the device.
+ *  (cudaGetSymbolAddress, with that device current) and keeps it together
+ *  with the context it was found in; make that first call before any stream
+ *  capture on the device.  A later call under another context on the same
+ *  device (after cudaDeviceReset, or a context the caller made current with
+ *  the driver API) looks the address up again, so it is a first call too.
  *  Nothing in the scratch has to start at zero: every entry the merge reads
  *  is written earlier in the same call.
  *  The array is shared by every call on the device: two calls whose work
@@ -446,6 +449,22 @@ int bil_watchdog_status(unsigned int *flags, int clear);
  * failure detection; it takes the wait limit to run.
  */
 int bil_watchdog_selftest(bil_stream_t stream);
+
+/*
+ * bil_probe_exp_rate -- a measurement helper, not part of the operator: it
+ * measures the exponential unit, the second bound of the logits path after
+ * HBM bandwidth ("Batch-Invariant LogP", "Batch-Invariance": one exponential
+ * per element in every pass).  Queues `blocks` blocks of 256 threads; every
+ * thread evaluates 8 independent chains of `iters` ex2.approx.ftz.f32 (the
+ * instruction of the contract's exp).  Block b writes records[3b] = the SM it
+ * ran on, records[3b+1] and records[3b+2] = that SM's clock64 counter before
+ * and after its loop; so ex2 results per clock on an SM are its blocks' 2048 *
+ * iters results over the span of its counters.  `sink` (one float) and
+ * `records` (3 * blocks int64) are device memory owned by the caller; the
+ * float is written only if a result were negative, which cannot happen.
+ * Asynchronous on `stream`.
+ */
+int bil_probe_exp_rate(int32_t blocks, int32_t iters, float *sink, int64_t *records, bil_stream_t stream);
 
 #ifdef __cplusplus
 }

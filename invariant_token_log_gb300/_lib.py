@@ -45,6 +45,7 @@ SIGNATURES = {
                                    _i32, _i64, _p, _i32, _i64, _p]),
     "bil_sum_f32": (_i32, [ctypes.POINTER(ctypes.c_void_p), _i32, _i64, _p, _p]),
     "bil_transpose_2d": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, _p]),
+    "bil_probe_exp_rate": (_i32, [ctypes.c_int32, ctypes.c_int32, _p, _p, _p]),
     "bil_linear_logp_fwd_static": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p, _i32,
                                           _p]),
 }
@@ -66,6 +67,9 @@ def library_path() -> str:
 def load() -> ctypes.CDLL:
     """Load libbil.so for this machine; raise if it has not been built."""
     global _lib
+    lib = _lib
+    if lib is not None:  # loaded: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is not None:
             return _lib

@@ -62,7 +62,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if any(codes):
             raise subprocess.CalledProcessError(max(codes), "nvcc")
         tmp = f"{out}.{tag}"
-        subprocess.run([nvcc(), *ARCH_FLAGS, "-shared", *objs, "-o", tmp], check=True)
+        subprocess.run([nvcc(), *ARCH_FLAGS, "-shared", *objs, "-ldl", "-o", tmp], check=True)
         os.replace(tmp, out)
     finally:
         for obj in objs:

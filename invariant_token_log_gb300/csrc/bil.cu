@@ -345,6 +345,43 @@ int launch_bwd_dt(int out_dtype, int rows, const BwdParams& bp, cudaStream_t str
   }
 }
 
+// ---------------------------------------------------------------------------
+// Measurement: the throughput of the exponential unit, the logits path's
+// second bound after HBM (one ex2.approx per element in every pass).  Each
+// thread runs 8 independent chains x <- 2^(-x) of the contract's ex2.approx
+// (x stays in [0.5, 1]); thread 0 of each block records the block's SM and
+// that SM's cycle counter before and after the loop.
+// ---------------------------------------------------------------------------
+
+constexpr int kExpRateThreads = 256;
+constexpr int kExpRateChains = 8;
+
+__global__ void __launch_bounds__(kExpRateThreads) exp_rate_kernel(int iters, float* sink, long long* rec) {
+  float x[kExpRateChains];
+#pragma unroll
+  for (int j = 0; j < kExpRateChains; ++j) x[j] = 0.5f + 0.0625f * j + 1e-7f * threadIdx.x;
+  __syncthreads();
+  const long long t0 = clock64();
+#pragma unroll 1
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < kExpRateChains; ++j) x[j] = ex2_approx(-x[j]);
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float s = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kExpRateChains; ++j) s += x[j];
+  if (s < 0.0f) sink[0] = s;  // never true (every x is positive): keeps the chains live
+  if (threadIdx.x == 0) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    rec[3 * blockIdx.x] = smid;
+    rec[3 * blockIdx.x + 1] = t0;
+    rec[3 * blockIdx.x + 2] = t1;
+  }
+}
+
 }  // namespace
 
 namespace bil_internal {
@@ -415,6 +452,7 @@ const char* bil_status_string(int status) {
 int bil_logp_fwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
                  const int64_t* target_ids, int64_t ignore_index, int32_t tile_v, float temperature, float* logp,
                  float* lse, float* entropy, int validate, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_logp_fwd");
   if (n_rows < 0 || vocab < 1 || ld < vocab) return BIL_E_INVALID_ARG;
   int64_t num_tiles = 0;
   if (int st = check_tile(dtype, vocab, tile_v, &num_tiles)) return st;
@@ -455,6 +493,7 @@ int bil_logp_tile_partials(const void* logits, int dtype, int64_t n_rows, int64_
                            int32_t tile_v, int32_t tile_begin, int32_t tile_end, float temperature,
                            const int64_t* target_ids, int64_t ignore_index, float* part_max, float* part_sum,
                            float* part_ent, int64_t ld_part, float* target_logit, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_logp_tile_partials");
   if (n_rows < 0 || vocab < 1) return BIL_E_INVALID_ARG;
   int64_t num_tiles = 0;
   if (int st = check_tile(dtype, vocab, tile_v, &num_tiles)) return st;
@@ -499,6 +538,7 @@ int bil_logp_merge(const float* part_max, const float* part_sum, const float* pa
                    int32_t num_tiles, int64_t ld_part, const float* target_logit, const int64_t* target_ids,
                    int64_t ignore_index, int64_t vocab, float* logp, float* lse, float* entropy, int validate,
                    bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_logp_merge");
   if (n_rows < 0 || num_tiles < 1 || ld_part < num_tiles || vocab < 1) return BIL_E_INVALID_ARG;
   if ((entropy != nullptr) != (part_ent != nullptr)) return BIL_E_INVALID_ARG;
   if (!extent_ok(n_rows, ld_part, 4)) return BIL_E_UNSUPPORTED;
@@ -535,6 +575,7 @@ int bil_logp_bwd(const void* logits, int dtype, int64_t n_rows, int64_t vocab, i
                  const int64_t* target_ids, int64_t ignore_index, float temperature, const float* lse,
                  const float* grad_logp, const float* entropy, const float* grad_entropy, void* dlogits,
                  int dlogits_dtype, int64_t ld_out, int64_t out_cols, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_logp_bwd");
   const int eb = elem_bytes(dtype);
   const int ob = elem_bytes(dlogits_dtype);
   if (eb == 0 || ob == 0) return BIL_E_DTYPE;
@@ -596,11 +637,22 @@ int bil_stream_shape(int dtype, int32_t tile_v, int64_t num_tiles, int fused, in
 }
 
 int bil_watchdog_selftest(bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_watchdog_selftest");
   watchdog_selftest_kernel<<<1, kLanes, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
+int bil_probe_exp_rate(int32_t blocks, int32_t iters, float* sink, int64_t* records, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_probe_exp_rate");
+  if (blocks < 1 || iters < 1 || sink == nullptr || records == nullptr) return BIL_E_INVALID_ARG;
+  if (!aligned(sink, 4) || !aligned(records, 8)) return BIL_E_ALIGN;
+  exp_rate_kernel<<<static_cast<unsigned>(blocks), kExpRateThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      iters, sink, reinterpret_cast<long long*>(records));
+  return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
+}
+
 int bil_watchdog_status(unsigned int* flags, int clear) {
+  bil_internal::NvtxRange nvtx_range("bil_watchdog_status");
   if (flags == nullptr) return BIL_E_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return BIL_E_CUDA;
   if (cudaMemcpyFromSymbol(flags, g_watchdog, sizeof(unsigned int)) != cudaSuccess) return BIL_E_CUDA;

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>  // header-only NVTX v3: ranges cost a pointer test unless a profiler is attached
 #include <stdint.h>
 
 #define BIL_INTERNAL __attribute__((visibility("hidden")))
@@ -34,6 +35,17 @@ BIL_INTERNAL int check_tile(int dtype, int64_t vocab, int32_t tile_v, int64_t* n
 // rows x pitch x eb within BIL_MAX_EXTENT_BYTES (rows <= 0: nothing spanned).
 // pitch and eb are positive.
 BIL_INTERNAL bool extent_ok(int64_t rows, int64_t pitch, int64_t eb);
+
+// A named NVTX range over the rest of the enclosing scope.  Every C-ABI entry
+// point that queues work opens one named after itself, so that a profiler's
+// timeline attributes host time and the kernels launched inside it to the call.
+class BIL_INTERNAL NvtxRange {
+ public:
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // The LM-head kernels' watchdog word of the current device (see
 // bil_watchdog_status); cleared when `clear` is non-zero.

@@ -761,21 +761,52 @@ bool workspace_fits(int64_t n_rows, int64_t vocab) {
 static __device__ __align__(256) unsigned char g_linear_static_scratch[BIL_LINEAR_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxStaticDevices = 64;
-void* g_static_scratch_ptr[kMaxStaticDevices];
+struct StaticScratch {
+  CUcontext ctx;  // the context the address was looked up in
+  void* ptr;
+};
+StaticScratch g_static_scratch[kMaxStaticDevices];
 std::mutex g_static_scratch_mutex;
 
-// The array's device address on the current device, looked up once per device
-// (with that device current) and cached.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// cuCtxGetCurrent, fetched from the driver at run time like the encoder.
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// The array's device address on the current device.  It is looked up (with
+// that device current) on the first call in each context and cached with the
+// context it belongs to: the address is a property of the module as loaded
+// into one context, so after a device reset, or under another context made
+// current on the same device, the next call looks it up again rather than
+// reuse an address that no longer maps the array.
 int static_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxStaticDevices) return BIL_E_CUDA;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (get_ctx == nullptr) return BIL_E_CUDA;
+  CUcontext ctx = nullptr;  // stays null on a thread where the runtime has made no context current yet
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return BIL_E_CUDA;
   std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
-  if (g_static_scratch_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
+  StaticScratch& e = g_static_scratch[dev];
+  if (ctx == nullptr || e.ptr == nullptr || e.ctx != ctx) {
+    void* ptr = nullptr;  // the lookup also makes the device's primary context current if none is
     if (cudaGetSymbolAddress(&ptr, g_linear_static_scratch) != cudaSuccess || ptr == nullptr) return BIL_E_CUDA;
-    g_static_scratch_ptr[dev] = ptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return BIL_E_CUDA;
+    e.ctx = ctx;
+    e.ptr = ptr;
   }
-  *out = g_static_scratch_ptr[dev];
+  *out = e.ptr;
   return BIL_OK;
 }
 
@@ -802,6 +833,7 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
                              int64_t ignore_index, float* part_max, float* part_sum, float* part_ent,
                              int64_t ld_part, float* target_logit, void* logits, int logits_dtype,
                              int64_t ld_logits, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_linear_logp_partials");
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   if (n_rows < 0 || hidden_size < 1 || vocab < 1 || ld_hidden < hidden_size || ld_weight < hidden_size)
     return BIL_E_INVALID_ARG;
@@ -886,6 +918,7 @@ int bil_linear_logp_fwd(const void* hidden, const void* weight, int dtype, int64
                         const int64_t* target_ids, int64_t ignore_index, float* logp, float* lse, float* entropy,
                         void* logits, int logits_dtype, int64_t ld_logits, void* workspace,
                         int64_t workspace_bytes, int validate, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_linear_logp_fwd");
   if (n_rows < 0 || vocab < 1) return BIL_E_INVALID_ARG;
   if (!workspace_fits(n_rows, vocab)) return BIL_E_UNSUPPORTED;
   const int64_t num_tiles = (vocab + kBN - 1) / kBN;
@@ -914,6 +947,7 @@ int bil_linear_logp_fwd(const void* hidden, const void* weight, int dtype, int64
 }
 
 int bil_sum_f32(const float* const* srcs, int count, int64_t n, float* dst, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_sum_f32");
   if (srcs == nullptr || count < 1 || count > kMaxSumSources || n < 0 || dst == nullptr) return BIL_E_INVALID_ARG;
   SumSources s{};
   for (int k = 0; k < count; ++k) {
@@ -932,6 +966,7 @@ int bil_sum_f32(const float* const* srcs, int count, int64_t n, float* dst, bil_
 
 int bil_transpose_2d(const void* src, int dtype, int64_t rows, int64_t cols, int64_t ld_src, void* dst,
                      int64_t ld_dst, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_transpose_2d");
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   if (rows < 0 || cols < 0 || ld_src < cols || ld_dst < rows) return BIL_E_INVALID_ARG;
   if (rows == 0 || cols == 0) return BIL_OK;
@@ -949,6 +984,7 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
                         int64_t ld_dz, void* dz_t, int64_t ld_dz_t, void* hidden_t, int64_t ld_hidden_t,
                         void* dhidden, int dhidden_dtype, int64_t ld_dhidden, void* dweight, int dweight_dtype,
                         int64_t ld_dweight, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_linear_logp_bwd");
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   for (int ot : {dhidden_dtype, dweight_dtype})
     if (ot != BIL_F32 && ot != dtype) return BIL_E_DTYPE;
@@ -1087,6 +1123,7 @@ int bil_linear_logp_fwd_static(const void* hidden, const void* weight, int dtype
                                int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight,
                                float temperature, const int64_t* target_ids, int64_t ignore_index, float* logp,
                                float* lse, float* entropy, int validate, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_linear_logp_fwd_static");
   if (n_rows < 0 || vocab < 1) return BIL_E_INVALID_ARG;
   if (!workspace_fits(n_rows, vocab)) return BIL_E_UNSUPPORTED;
   const int64_t num_tiles = (vocab + kBN - 1) / kBN;

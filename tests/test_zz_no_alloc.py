@@ -108,3 +108,46 @@ def test_static_scratch_matches_the_workspace_entry_point():
             for a, b in zip(outs, ref):
                 assert np.array_equal(_bits(a), _bits(b)), (rep, xd.shape[0], ent)
     assert bil.watchdog_status() == 0
+
+
+@pytest.mark.gpu
+def test_static_calls_allocate_nothing():
+    """After a first call (which looks up the array's address), further calls
+    leave both the CUDA allocator's and the device's free memory unchanged."""
+    lib = _lib.load()
+    wd = torch.from_numpy(wl.linear_weight(V, H, seed=35).view(np.int16)).cuda().view(torch.bfloat16)
+    xd, td = _inputs(300, 36)
+    outs = _outputs(300, True)
+    _static(lib, xd, wd, td, outs)
+    torch.cuda.synchronize()
+    torch_before = torch.cuda.memory_allocated()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        _static(lib, xd, wd, td, outs)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == torch_before
+    assert free_after == free_before, (free_before, free_after)
+    assert bil.watchdog_status() == 0
+
+
+@pytest.mark.gpu
+def test_static_validate_reports_an_out_of_range_target():
+    """validate=1 checks the targets on the host before anything is queued: an
+    active target at the vocabulary size gives BIL_E_TARGET_RANGE and leaves
+    the outputs untouched."""
+    lib = _lib.load()
+    wd = torch.from_numpy(wl.linear_weight(V, H, seed=37).view(np.int16)).cuda().view(torch.bfloat16)
+    xd, td = _inputs(40, 38)
+    td[11] = V
+    outs = _outputs(40, False)
+    st = lib.bil_linear_logp_fwd_static(_p(xd), _p(wd), _lib.BF16, 40, H, H, V, H, 1.0, _p(td), -100,
+                                        _p(outs[0]), _p(outs[1]), None, 1, _stream())
+    assert st == _lib.E_TARGET_RANGE
+    torch.cuda.synchronize()
+    assert all(torch.isnan(o).all() for o in outs)
+    td[11] = 3
+    _static(lib, xd, wd, td, outs)
+    torch.cuda.synchronize()
+    assert not any(torch.isnan(o).any() for o in outs)
+    assert bil.watchdog_status() == 0
