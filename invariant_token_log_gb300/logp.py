@@ -35,6 +35,8 @@ def _code(dtype: torch.dtype) -> int:
 
 def _rows2d(x: torch.Tensor) -> torch.Tensor:
     """[*lead, V] -> [N, V] with unit column stride (a view when one exists)."""
+    if x.dim() == 2 and x.stride(-1) == 1:
+        return x
     v = x.shape[-1]
     x2 = x.reshape(-1, v)
     if x2.stride(-1) != 1 and x2.numel() > 0:
@@ -46,23 +48,58 @@ def _row_stride(x2: torch.Tensor) -> int:
     return x2.stride(0) if x2.shape[0] > 1 else max(x2.stride(0), x2.shape[1])
 
 
+# The current stream's raw handle of a device, by index.  The private accessor
+# skips building a torch.cuda.Stream object on every call; the public route is
+# the fallback should a PyTorch build lack it.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(index: int) -> int:
+    if _raw_stream is not None:
+        return _raw_stream(index)
+    return torch.cuda.current_stream(index).cuda_stream
+
+
 def _stream(device: torch.device) -> ctypes.c_void_p:
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    return ctypes.c_void_p(_stream_handle(device.index))
 
 
 def _ptr(t: torch.Tensor | None):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
+
+
+def _on_device(index: int, fn, *args):
+    """fn(*args) with device `index` current (switching only when it is not)."""
+    if torch.cuda.current_device() == index:
+        return fn(*args)
+    with torch.cuda.device(index):
+        return fn(*args)
+
+
+_NARROW_INTS = (torch.int32, torch.int16, torch.int8, torch.uint8)
 
 
 def _targets1d(target_ids: torch.Tensor, lead_shape, device) -> torch.Tensor:
-    if tuple(target_ids.shape) != tuple(lead_shape):
-        raise ValueError(f"target_ids shape {tuple(target_ids.shape)} != logits leading shape {tuple(lead_shape)}")
-    if target_ids.dtype not in (torch.int64, torch.int32, torch.int16, torch.int8, torch.uint8):
-        raise TypeError("target_ids must be an integer tensor")
+    if target_ids.shape != lead_shape:
+        if tuple(target_ids.shape) != tuple(lead_shape):
+            raise ValueError(f"target_ids shape {tuple(target_ids.shape)} != logits leading shape {tuple(lead_shape)}")
     if target_ids.device != device:
         raise ValueError("target_ids must be on the logits' device")
+    if target_ids.dtype is torch.int64:
+        if target_ids.dim() == 1 and target_ids.is_contiguous():
+            return target_ids
+        return target_ids.reshape(-1).contiguous()
+    if target_ids.dtype not in _NARROW_INTS:
+        raise TypeError("target_ids must be an integer tensor")
     # the C ABI reads int64 targets; narrower integer types are widened here
     return target_ids.reshape(-1).to(torch.int64).contiguous()
+
+
+def _f32_1d(t: torch.Tensor) -> torch.Tensor:
+    """A contiguous float32 [N] view of a per-row tensor (converted only when it is not one)."""
+    if t.dtype is torch.float32 and t.dim() == 1 and t.is_contiguous():
+        return t
+    return t.reshape(-1).to(torch.float32).contiguous()
 
 
 def _need_cuda(*ts: torch.Tensor) -> None:
@@ -90,23 +127,27 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
     v = width if vocab is None else int(vocab)
     if not 1 <= v <= width:
         raise ValueError(f"vocab {v} outside [1, {width}]")
-    t1 = _targets1d(target_ids, lead, logits.device)
+    device = logits.device
+    t1 = _targets1d(target_ids, lead, device)
     if out is None:
-        out = torch.empty(n, dtype=torch.float32, device=logits.device)
+        out = torch.empty(n, dtype=torch.float32, device=device)
     if lse is None:
-        lse = torch.empty(n, dtype=torch.float32, device=logits.device)
+        lse = torch.empty(n, dtype=torch.float32, device=device)
     want_ent = return_entropy or entropy is not None
     if want_ent and entropy is None:
-        entropy = torch.empty(n, dtype=torch.float32, device=logits.device)
-    lib = _lib.load()
-    with torch.cuda.device(logits.device):
-        st = lib.bil_logp_fwd(_ptr(x2), _code(x2.dtype), n, v, _row_stride(x2), _ptr(t1), int(ignore_index),
-                              int(tile_v), float(temperature), _ptr(out), _ptr(lse), _ptr(entropy if want_ent else None),
-                              int(bool(validate)), _stream(logits.device))
-    _lib.check("bil_logp_fwd", st)
-    if want_ent:
-        return out.reshape(lead), lse.reshape(lead), entropy.reshape(lead)
-    return out.reshape(lead), lse.reshape(lead)
+        entropy = torch.empty(n, dtype=torch.float32, device=device)
+    index = device.index
+    st = _on_device(index, _lib.load().bil_logp_fwd, x2.data_ptr(), _code(x2.dtype), n, v, _row_stride(x2),
+                    t1.data_ptr(), int(ignore_index), int(tile_v), float(temperature), out.data_ptr(),
+                    lse.data_ptr(), entropy.data_ptr() if want_ent else None, 1 if validate else 0,
+                    _stream_handle(index))
+    if st:
+        _lib.check("bil_logp_fwd", st)
+    if len(lead) != 1:
+        out, lse = out.reshape(lead), lse.reshape(lead)
+        if want_ent:
+            entropy = entropy.reshape(lead)
+    return (out, lse, entropy) if want_ent else (out, lse)
 
 
 def logp_tile_partials(logits_shard: torch.Tensor, target_ids: torch.Tensor, vocab: int, tile_v: int,
@@ -131,13 +172,13 @@ def logp_tile_partials(logits_shard: torch.Tensor, target_ids: torch.Tensor, voc
             raise ValueError("the partial buffers must share a row stride")
     if target_logit.dtype != torch.float32 or target_logit.numel() != n or not target_logit.is_contiguous():
         raise ValueError("target_logit must be a contiguous float32 [N] tensor")
-    lib = _lib.load()
-    with torch.cuda.device(logits_shard.device):
-        st = lib.bil_logp_tile_partials(_ptr(x2), _code(x2.dtype), n, int(vocab), _row_stride(x2), int(tile_v),
-                                        int(tile_begin), int(tile_end), float(temperature), _ptr(t1),
-                                        int(ignore_index), _ptr(part_max), _ptr(part_sum), _ptr(part_ent),
-                                        part_max.stride(0), _ptr(target_logit), _stream(logits_shard.device))
-    _lib.check("bil_logp_tile_partials", st)
+    index = logits_shard.device.index
+    st = _on_device(index, _lib.load().bil_logp_tile_partials, x2.data_ptr(), _code(x2.dtype), n, int(vocab),
+                    _row_stride(x2), int(tile_v), int(tile_begin), int(tile_end), float(temperature),
+                    t1.data_ptr(), int(ignore_index), part_max.data_ptr(), part_sum.data_ptr(), _ptr(part_ent),
+                    part_max.stride(0), target_logit.data_ptr(), _stream_handle(index))
+    if st:
+        _lib.check("bil_logp_tile_partials", st)
 
 
 def logp_merge(part_max: torch.Tensor, part_sum: torch.Tensor, num_tiles: int, target_logit: torch.Tensor,
@@ -163,12 +204,13 @@ def logp_merge(part_max: torch.Tensor, part_sum: torch.Tensor, num_tiles: int, t
     ent = None
     if part_ent is not None:
         ent = torch.empty(n, dtype=torch.float32, device=part_max.device) if entropy is None else entropy
-    lib = _lib.load()
-    with torch.cuda.device(part_max.device):
-        st = lib.bil_logp_merge(_ptr(part_max), _ptr(part_sum), _ptr(part_ent), n, int(num_tiles), part_max.stride(0),
-                                _ptr(target_logit), _ptr(t1), int(ignore_index), int(vocab), _ptr(out), _ptr(lse),
-                                _ptr(ent), int(bool(validate)), _stream(part_max.device))
-    _lib.check("bil_logp_merge", st)
+    index = part_max.device.index
+    st = _on_device(index, _lib.load().bil_logp_merge, part_max.data_ptr(), part_sum.data_ptr(), _ptr(part_ent), n,
+                    int(num_tiles), part_max.stride(0), target_logit.data_ptr(), t1.data_ptr(), int(ignore_index),
+                    int(vocab), out.data_ptr(), lse.data_ptr(), _ptr(ent), 1 if validate else 0,
+                    _stream_handle(index))
+    if st:
+        _lib.check("bil_logp_merge", st)
     return (out, lse, ent) if ent is not None else (out, lse)
 
 
@@ -188,12 +230,12 @@ def logp_bwd(logits: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor, 
     n, width = x2.shape
     v = width if vocab is None else int(vocab)
     t1 = _targets1d(target_ids, lead, logits.device)
-    lse1 = lse.reshape(-1).to(torch.float32).contiguous()
-    g1 = grad_logp.reshape(-1).to(torch.float32).contiguous()
+    lse1 = _f32_1d(lse)
+    g1 = _f32_1d(grad_logp)
     h1 = gh1 = None
     if entropy is not None:
-        h1 = entropy.reshape(-1).to(torch.float32).contiguous()
-        gh1 = grad_entropy.reshape(-1).to(torch.float32).contiguous()
+        h1 = _f32_1d(entropy)
+        gh1 = _f32_1d(grad_entropy)
         if h1.numel() != n or gh1.numel() != n:
             raise ValueError("entropy and grad_entropy must have the targets' shape")
     if lse1.numel() != n or g1.numel() != n:
@@ -206,12 +248,12 @@ def logp_bwd(logits: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor, 
     o2 = out if out.dim() == 2 else out.reshape(n, -1)
     if o2.shape[0] != n or o2.stride(-1) != 1 or o2.shape[1] < width:
         raise ValueError("out must be row-major with at least the logits' columns")
-    lib = _lib.load()
-    with torch.cuda.device(logits.device):
-        st = lib.bil_logp_bwd(_ptr(x2), _code(x2.dtype), n, v, _row_stride(x2), _ptr(t1), int(ignore_index),
-                              float(temperature), _ptr(lse1), _ptr(g1), _ptr(h1), _ptr(gh1), _ptr(o2),
-                              _code(o2.dtype), _row_stride(o2), width, _stream(logits.device))
-    _lib.check("bil_logp_bwd", st)
+    index = logits.device.index
+    st = _on_device(index, _lib.load().bil_logp_bwd, x2.data_ptr(), _code(x2.dtype), n, v, _row_stride(x2),
+                    t1.data_ptr(), int(ignore_index), float(temperature), lse1.data_ptr(), g1.data_ptr(), _ptr(h1),
+                    _ptr(gh1), o2.data_ptr(), _code(o2.dtype), _row_stride(o2), width, _stream_handle(index))
+    if st:
+        _lib.check("bil_logp_bwd", st)
     return out.reshape(logits.shape) if out.numel() == logits.numel() else out
 
 
