@@ -49,6 +49,7 @@ WORKLOAD = ("training: N=16384 rows (B=8 x T=2048), V=151936 bf16 logits ~ 3*ran
             "targets 70% top-5 / 30% uniform, g ~ N(0,1) fp32, forward + backward, bf16 dlogits")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300's nominal HBM3e bandwidth, the denominator the 75% target is stated against
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 KERNEL_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "logp_device.cuh")
 LINEAR_SOURCE = os.path.join(ROOT, "invariant_token_log_gb300", "csrc", "linear.cu")
@@ -61,8 +62,11 @@ LINEAR_WORKLOAD = ("linear: N=16384 rows (B=8 x T=2048) of bf16 hidden states ~ 
 LINEAR_CPU_ROWS = 8
 LINEAR_REFERENCE_ROWS = 8
 FALLBACK_BF16_TFLOPS = 1900.0
-REFERENCE_ROWS_PER_STEP = 256
-CPU_BASELINE_ROWS = 8192
+# the reference arm runs the whole batch each step while (steps + warm-up) x batch
+# stays within this many rows (about a minute of the oracle on 16 host cores),
+# and an equal share of it per step beyond
+REFERENCE_ROW_BUDGET = 25 * 16384
+CPU_BASELINE_ROWS = 16384
 
 
 def parse():
@@ -195,13 +199,15 @@ class ClockSampler:
 # the CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_rows_per_s(rows: int, passes: int = 1):
-    """Time the CPU oracle's forward + backward over `rows` rows of the workload."""
+def oracle_rows_per_s(rows: int, passes: int = 1, w=None):
+    """Time the CPU oracle's forward + backward over the first `rows` rows of the
+    workload (`w`, the generated training workload, or generated here)."""
     import oracle
     import workloads as wl
     oracle.build()
-    chunks = list(range(-(-rows // wl.CHUNK_ROWS)))
-    w = wl.training(n_rows=rows, chunks=chunks)
+    if w is None:
+        chunks = list(range(-(-rows // wl.CHUNK_ROWS)))
+        w = wl.training(n_rows=rows, chunks=chunks)
     g = w.grad_logp.astype(np.float64)
     batch = 256
     t0 = time.perf_counter()
@@ -222,13 +228,19 @@ def run_reference(args):
     import oracle
     import workloads as wl
     oracle.build()
-    rows = REFERENCE_ROWS_PER_STEP
-    w = wl.training(n_rows=rows, chunks=[0])
+    n = args.rows
+    per_step = REFERENCE_ROW_BUDGET // max(1, args.steps + args.warmup)
+    rows = max(wl.CHUNK_ROWS, min(n, per_step // wl.CHUNK_ROWS * wl.CHUNK_ROWS))
+    w = wl.training(n_rows=rows, chunks=list(range(-(-rows // wl.CHUNK_ROWS))))
     g = w.grad_logp.astype(np.float64)
+    batch = 256
 
     def step():
-        oracle.logp_fwd(w.logits, w.dtype, w.vocab, w.target_ids, w.ignore_index)
-        oracle.logp_bwd(w.logits, w.dtype, w.vocab, w.target_ids, g, w.ignore_index)
+        for r0 in range(0, rows, batch):
+            r1 = min(rows, r0 + batch)
+            x = w.logits[r0:r1]
+            oracle.logp_fwd(x, w.dtype, w.vocab, w.target_ids[r0:r1], w.ignore_index)
+            oracle.logp_bwd(x, w.dtype, w.vocab, w.target_ids[r0:r1], g[r0:r1], w.ignore_index)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -236,13 +248,14 @@ def run_reference(args):
         step()
     dt = time.perf_counter() - t0
     value = rows * args.steps / dt
-    sample = f"{rows} rows of the workload per step, float64 oracle, forward + backward"
+    what = "all" if rows == n else "the first"
+    sample = f"{what} {rows} of the {n} rows of the workload per step, float64 oracle, forward + backward"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, host-generated)",
-        "config": {"workload": WORKLOAD, "rows_per_step": rows},
+        "config": training_config(n, args.gpus), "rows_per_step": rows,
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -270,8 +283,13 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def ncu_traffic(kernel: str, source: str = KERNEL_SOURCE):
-    """DRAM bytes per launch from a committed ncu capture, if it was taken on this kernel source."""
+def ncu_traffic(kernel: str, source: str = KERNEL_SOURCE, active_rows: int | None = None):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on this kernel source.
+
+    A record with ``bytes_per_row`` comes from a capture of a smaller batch than the
+    benchmark's (the traffic of these kernels grows in proportion to the rows they
+    process); it is scaled to ``active_rows``.  A record with ``bytes_per_launch``
+    was taken on the benchmark's own batch."""
     try:
         lines = open(TRAFFIC_FILE).read().splitlines()
     except OSError:
@@ -281,9 +299,99 @@ def ncu_traffic(kernel: str, source: str = KERNEL_SOURCE):
         if line.lstrip().startswith("#"):
             continue
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-        if f.get("kernel") == kernel and f.get("source_sha") == sha and "bytes_per_launch" in f:
+        if f.get("kernel") != kernel or f.get("source_sha") != sha:
+            continue
+        if "bytes_per_row" in f and active_rows is not None:
+            return float(f["bytes_per_row"]) * active_rows
+        if "bytes_per_launch" in f:
             return float(f["bytes_per_launch"])
     return None
+
+
+def exp_rate_probe(dev, sms: int):
+    """Results per clock per SM of ex2.approx, the exponential the kernels use
+    (bil_probe_exp_rate: 8 blocks of 256 threads per SM, 8 independent chains per
+    thread); median, min and max over the SMs, from each SM's own cycle counter."""
+    import ctypes
+
+    import torch
+
+    from invariant_token_log_gb300 import _lib
+    lib = _lib.load()
+    blocks = 8 * sms
+    rec = torch.zeros(3 * blocks, dtype=torch.int64, device=dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    iters = 4096
+    for it in (256, iters):  # a short warm-up launch, then the measured one
+        _lib.check("bil_probe_exp_rate", lib.bil_probe_exp_rate(blocks, it, sink.data_ptr(), rec.data_ptr(), stream))
+    torch.cuda.synchronize(dev)
+    r = rec.cpu().numpy().reshape(blocks, 3)
+    per_sm = {}
+    for smid, t0, t1 in r:
+        lo, hi, k = per_sm.get(int(smid), (t0, t1, 0))
+        per_sm[int(smid)] = (min(lo, t0), max(hi, t1), k + 1)
+    rates = sorted(k * 256 * 8 * iters / float(hi - lo) for lo, hi, k in per_sm.values())
+    return {"ex2_per_clk_per_sm": statistics.median(rates), "min": rates[0], "max": rates[-1],
+            "sms": len(rates), "blocks": blocks, "iters": iters,
+            "how": "bil_probe_exp_rate: 256-thread blocks, 8 per SM, 8 independent ex2.approx chains per thread; "
+                   "results / span of the SM's clock64"}
+
+
+def exp_secondary(variants, n, v, fwd_ms, bwd_ms, clocks):
+    """The exponential unit as the second roofline of the logits path: one ex2 per
+    element in the forward and in the backward.  demand_frac = exps per second
+    needed at the measured time / (probe rate x SMs x median SM clock)."""
+    if not variants or "sfu_exp" not in variants or not clocks.get("sm_mhz"):
+        return None
+    pr = variants["sfu_exp"]
+    cap = pr["ex2_per_clk_per_sm"] * pr["sms"] * clocks["sm_mhz"] * 1e6  # ex2 per second
+    out = {"bound": "sfu", "unit": "ex2/clk/SM", "peak": pr["ex2_per_clk_per_sm"], "sm_mhz": clocks["sm_mhz"],
+           "fwd_demand_frac": n * v / (fwd_ms / 1e3) / cap, "bwd_demand_frac": n * v / (bwd_ms / 1e3) / cap}
+    ent = variants.get("entropy_temperature_0.7")
+    if ent:
+        out["entropy_fwd_demand_frac"] = n * v / (ent["fwd_ms"] / 1e3) / cap
+    return out
+
+
+def host_link_probe(x_host, x_dev, out_host, dev, rows_per_copy: int = 4096, reps: int = 3):
+    """Pinned host <-> device copy rates over the links the end-to-end figure
+    crosses: host to device alone, device to host alone, and both at once (on two
+    streams), each of `rows_per_copy` rows of the logits per copy."""
+    import torch
+    r = min(rows_per_copy, x_host.shape[0] // 2)
+    src_h, dst_d = x_host[:r], torch.empty_like(x_dev[:r])
+    src_d, dst_h = x_dev[r:2 * r], out_host[r:2 * r]
+    nbytes = src_h.numel() * src_h.element_size()
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        return time.perf_counter() - t0
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            dst_d.copy_(src_h, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            dst_h.copy_(src_d, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+    h2d()
+    d2h()
+    t_h2d, t_d2h, t_both = timed(h2d), timed(d2h), timed(both)
+    del dst_d
+    return {"h2d_gbs": reps * nbytes / t_h2d / 1e9, "d2h_gbs": reps * nbytes / t_d2h / 1e9,
+            "both_gbs": 2 * reps * nbytes / t_both / 1e9, "bytes_per_copy": nbytes, "reps": reps,
+            "how": "pinned host <-> device tensor copies on their own streams, host wall clock around "
+                   "synchronised batches"}
 
 
 def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_bytes, stream, dev):
@@ -349,6 +457,7 @@ def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_byte
     variants["decode_fwd_us_per_call_graph"] = lat
     variants["decode_fwd_us_per_call_python"] = eager
     variants["prefill_fwd"] = prefill_measurement(bil, stream, dev)
+    variants["sfu_exp"] = exp_rate_probe(dev, torch.cuda.get_device_properties(dev).multi_processor_count)
     return variants
 
 
@@ -385,6 +494,14 @@ def prefill_measurement(bil, stream, dev):
     return {"ms": ms, "rows_per_s": n / (ms / 1e3), "rows": n, "active_rows": active, "ld": int(x.shape[1]),
             "gbs": gbs_active, "frac": gbs_active / peak,
             "gbs_on_all_rows": n * v * 2 / (ms / 1e3) / 1e9}
+
+
+def training_config(rows_per_gpu: int, world: int) -> dict:
+    """The workload's `config`, the same on the CUDA arm and the reference arm."""
+    return {"workload": WORKLOAD, "rows_per_gpu": rows_per_gpu, "vocab": 151936, "tile_v": 4096,
+            "storage": "bf16 logits, bf16 dlogits, fp32 logp/lse",
+            "l2": "no flush: every pass reads 4.98 GB of logits, 38x the 129 MB L2",
+            "parallelism": f"dp{world} (independent row batches per GPU)"}
 
 
 def run_bil(args):
@@ -502,34 +619,40 @@ def run_bil(args):
                "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps,
                "path": "HostStreamedLogp: pinned host -> 2048-row chunks over 3 streams -> pinned host",
                "host_link_gbs": (h2d + d2h) / (e2e_ms / args.e2e_steps / 1e3) / 1e9,
-               "gpu_launches": launches, "step_ms": step_ms}
+               "gpu_launches": launches, "step_ms": step_ms,
+               "host_link_probe": host_link_probe(x_host, x, d_host, dev)}
         del pipe, d_host
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        rps, dt, cores = oracle_rows_per_s(CPU_BASELINE_ROWS)
+        rows_cpu = min(n, CPU_BASELINE_ROWS)
+        rps, dt, cores = oracle_rows_per_s(rows_cpu, w=w)
+        what = "all" if rows_cpu == n else "the first"
         cpu = {"value": rps, "unit": "rows/s", "cores": cores, "kind": "oracle",
-               "sample": f"first {CPU_BASELINE_ROWS} rows of the workload, forward + backward, float64 "
-                         f"oracle, {dt:.1f} s wall"}
+               "sample": f"{what} {rows_cpu} rows of the workload, forward + backward, float64 oracle, "
+                         f"{dt:.1f} s wall"}
 
     if rank == 0:
         out = {
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, host-generated)",
-            "config": {"workload": WORKLOAD, "rows_per_gpu": n, "vocab": v, "tile_v": w.tile_v,
-                       "storage": "bf16 logits, bf16 dlogits, fp32 logp/lse",
-                       "l2": "no flush: every pass reads 4.98 GB of logits, 38x the 129 MB L2",
-                       "parallelism": f"dp{world} (independent row batches per GPU)"},
-            "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
+            "config": training_config(n, world),
+            "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak, "hbm_frac_of": f"{peak_kind} HBM copy bandwidth",
+            "hbm_frac_nominal": step_gbs / NOMINAL_HBM_GBS,
             "kernels": {
-                "logp_fwd": {"ms": fwd_avg, "gbs": fwd_gbs, "bytes": fwd_bytes, "frac": fwd_gbs / peak},
-                "logp_bwd": {"ms": bwd_avg, "gbs": bwd_gbs, "bytes": bwd_bytes, "frac": bwd_gbs / peak},
+                "logp_fwd": {"ms": fwd_avg, "gbs": fwd_gbs, "bytes": fwd_bytes, "frac": fwd_gbs / peak,
+                             "frac_nominal": fwd_gbs / NOMINAL_HBM_GBS},
+                "logp_bwd": {"ms": bwd_avg, "gbs": bwd_gbs, "bytes": bwd_bytes, "frac": bwd_gbs / peak,
+                             "frac_nominal": bwd_gbs / NOMINAL_HBM_GBS},
             },
             "roofline": {"kernel": "bwd_kernel (logp_bwd)", "bound": "hbm", "achieved": bwd_gbs, "peak": peak,
                          "peak_source": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
-                         "frac": bwd_gbs / peak, "traffic": ncu_traffic("bwd_kernel"),
-                         "algorithmic_bytes_per_launch": bwd_bytes},
+                         "frac": bwd_gbs / peak, "frac_nominal": bwd_gbs / NOMINAL_HBM_GBS,
+                         "nominal_peak": NOMINAL_HBM_GBS,
+                         "traffic": ncu_traffic("bwd_kernel", active_rows=active),
+                         "algorithmic_bytes_per_launch": bwd_bytes,
+                         "secondary": exp_secondary(variants, n, v, fwd_avg, bwd_avg, clocks)},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clocks,
             "variants": variants,
         }
