@@ -23,6 +23,14 @@ Tolerances (written here once, used by every GPU test):
               with rho = eps_L + 3e-7 the relative error of p (2-ulp exp and
               the rounding of a).  Without an entropy term and at rcp = 1 this
               is the 1e-6 bound up to p |g| rho, and those tests use 1e-6.
+  float32 dlogits where |g| p is not small (dlogits_tol): the element's error
+              is about |g| p times the relative error of p, and that relative
+              error is rho_row = half an ulp of the row's float32 lse (4.8e-7
+              for 8 <= lse < 16, 9.5e-7 for 16 <= lse < 32) + the forward's own
+              error (about 4e-7: a 2-ulp exp in every sum term and the log) +
+              the backward's 2-ulp exp (2.4e-7): at most 1.7e-6 for lse < 32.
+              So the flat 1e-6 holds where |g| p <= 1/2 (FLAT_GP); beyond it
+              the bound is 1e-6 + |g| p rho with rho = 2.3e-6 (as above).
 """
 from __future__ import annotations
 
@@ -87,6 +95,42 @@ def entropy_grad_tol(p: np.ndarray, a_plus_h: np.ndarray, g: np.ndarray, gh: np.
         p_ah = np.where(p > 0, p * np.abs(a_plus_h), 0.0)  # p -> 0 at a = -inf
     return 1e-6 + rcp * (np.abs(g)[:, None] * rho * p +
                          np.abs(gh)[:, None] * (rho * p_ah + (EPS_LSE + EPS_ENTROPY) * p))
+
+
+FLAT_GP = 0.5
+RHO_P = EPS_LSE + 3e-7
+
+
+def dlogits_tol(p: np.ndarray, g: np.ndarray, lse: np.ndarray):
+    """(per-element bound, |g| p) for float32 dlogits without an entropy term: the
+    flat DLOGITS_ATOL where |g| p <= FLAT_GP, DLOGITS_ATOL + |g| p RHO_P beyond
+    (see the module docstring; derived for rows whose lse is below 32)."""
+    assert np.all(np.abs(lse[np.isfinite(lse)]) < 32.0), "the bound is derived for |lse| < 32"
+    gp = np.abs(np.asarray(g, np.float64))[:, None] * p
+    return np.where(gp <= FLAT_GP, DLOGITS_ATOL, DLOGITS_ATOL + gp * RHO_P), gp
+
+
+def check_dlogits_split(got: np.ndarray, ref: np.ndarray, gp: np.ndarray, what: str) -> dict:
+    """Assert the flat 1e-6 where |g| p <= FLAT_GP and the derived bound beyond;
+    return the worst error found in each region (printed for the record)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), f"{what}: NaN pattern differs"
+    fin = np.isfinite(ref)
+    err = np.where(fin, np.abs(got - ref), 0.0)
+    flat = fin & (gp <= FLAT_GP)
+    beyond = fin & (gp > FLAT_GP)
+    out = {"n_flat": int(flat.sum()), "worst_flat": float(err[flat].max()) if flat.any() else 0.0,
+           "n_beyond": int(beyond.sum()), "worst_beyond": float(err[beyond].max()) if beyond.any() else 0.0,
+           "max_gp": float(gp[fin].max()) if fin.any() else 0.0}
+    if beyond.any():
+        ratio = err[beyond] / (DLOGITS_ATOL + gp[beyond] * RHO_P)
+        out["worst_beyond_ratio"] = float(ratio.max())
+        out["gp_at_worst_beyond"] = float(gp[beyond][np.argmax(err[beyond])])
+    print(f"DLOGITS-BOUND {what}: {out}")
+    assert out["worst_flat"] <= DLOGITS_ATOL, f"{what}: {out}"
+    assert out.get("worst_beyond_ratio", 0.0) <= 1.0, f"{what}: {out}"
+    return out
 
 
 def assert_close_elementwise(got: np.ndarray, ref: np.ndarray, tol: np.ndarray, what: str):

@@ -11,8 +11,8 @@ import torch
 import invariant_token_log_gb300 as bil
 import oracle
 import workloads as wl
-from gpu_helpers import (DLOGITS_ATOL, LOGP_ATOL, PART_SUM_RTOL, assert_close_abs, assert_close_elementwise,
-                         assert_rounded, check_watchdog, device_logits, entropy_grad_tol, f32_bits, host_bits)
+from gpu_helpers import (DLOGITS_ATOL, LOGP_ATOL, PART_SUM_RTOL, assert_close_abs, assert_rounded,
+                         check_dlogits_split, check_watchdog, device_logits, dlogits_tol, f32_bits, host_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -320,11 +320,11 @@ def test_common_vocabulary_widths(v, n):
     """Vocabulary widths of common LM heads, contiguous bf16 rows: multiples of
     8 and odd widths (rows then start at every offset from a 16-byte boundary),
     up to 63 tiles of 4096.  9 rows take the cluster forward, 40 the streaming
-    one.  The gradients use the per-element bound 1e-6 + |g| rho p derived from
-    the forward's float32 error (here g ~ N(0, 1) and, with as few as 32000
-    columns, p reaches ~0.5, so |g| p is not below 1 as on the fixed
-    workloads): float32 within it, bf16 (whose rows share the input's
-    offsets) correctly rounded up to it."""
+    one.  Here g ~ N(0, 1) and, with as few as 32000 columns, p reaches ~0.8,
+    so |g| p is not always small as on the fixed workloads: float32 gradients
+    meet the flat 1e-6 where |g| p <= 1/2 and the bound derived from the
+    forward's float32 error beyond (gpu_helpers.dlogits_tol); bf16 gradients
+    (rows at the input's offsets) are correctly rounded up to the same bound."""
     w = wl.random_rows(seed=v % 997 + n, n_rows=n, vocab=v, dtype="bfloat16", scale=3.0, tile_v=4096, ignore_every=4)
     logp, lse, d = run_fwd_bwd(w)
     ref_logp, ref_lse, ref_d, bad = oracle_fwd_bwd(w)
@@ -333,7 +333,7 @@ def test_common_vocabulary_widths(v, n):
     assert_close_abs(lse.cpu().numpy(), ref_lse, LOGP_ATOL, "lse")
     active = (w.target_ids != w.ignore_index)[:, None]
     p = np.where(active, np.exp(oracle.widen(w.logits, w.dtype)[:, :v] - ref_lse[:, None]), 0.0)
-    tol = entropy_grad_tol(p, np.zeros_like(p), w.grad_logp.astype(np.float64), np.zeros(n), 1.0)
-    assert_close_elementwise(d.cpu().numpy(), ref_d, tol, "dlogits")
+    tol, gp = dlogits_tol(p, w.grad_logp, ref_lse)
+    check_dlogits_split(d.cpu().numpy(), ref_d, gp, f"V={v} N={n} float32")
     _, _, d16 = run_fwd_bwd(w, dlogits_dtype="bfloat16")
     assert_rounded(host_bits(d16), ref_d, "bfloat16", tol, "dlogits")
