@@ -68,9 +68,12 @@ def _ptr(t: torch.Tensor | None):
     return None if t is None else t.data_ptr()
 
 
+_get_device = getattr(torch._C, "_cuda_getDevice", None) or torch.cuda.current_device
+
+
 def _on_device(index: int, fn, *args):
     """fn(*args) with device `index` current (switching only when it is not)."""
-    if torch.cuda.current_device() == index:
+    if _get_device() == index:
         return fn(*args)
     with torch.cuda.device(index):
         return fn(*args)
@@ -120,14 +123,44 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
     ``temperature`` divides the logits before the softmax (applied as a
     multiplication by the float32 reciprocal).
     """
-    _need_cuda(logits, target_ids)
-    lead = logits.shape[:-1]
-    x2 = _rows2d(logits)
-    n, width = x2.shape
+    if not (logits.is_cuda and target_ids.is_cuda):
+        _need_cuda(logits, target_ids)
+    shape = logits.shape
+    tshape = target_ids.shape
+    if (len(shape) == 2 and len(tshape) == 1 and tshape[0] == shape[0] and vocab is None and out is None
+            and lse is None and not (return_entropy or entropy is not None) and logits.is_contiguous()
+            and target_ids.dtype is torch.int64 and target_ids.is_contiguous()):
+        # The common call, [N, V] row-major logits and int64 [N] targets with the
+        # outputs allocated here, without the general path's reshaping: the
+        # per-call host time is what bounds small (decode-sized) batches.
+        n, width = shape
+        index = logits.get_device()
+        if target_ids.get_device() != index:
+            raise ValueError("target_ids must be on the logits' device")
+        out = torch.empty(n, dtype=torch.float32, device=index)
+        lse = torch.empty(n, dtype=torch.float32, device=index)
+        fn = _lib.load().bil_logp_fwd
+        args = (logits.data_ptr(), _code(logits.dtype), n, width, width, target_ids.data_ptr(), int(ignore_index),
+                int(tile_v), float(temperature), out.data_ptr(), lse.data_ptr(), None, 1 if validate else 0,
+                _stream_handle(index))
+        st = fn(*args) if _get_device() == index else _on_device(index, fn, *args)
+        if st:
+            _lib.check("bil_logp_fwd", st)
+        return out, lse
+    if len(shape) == 2 and logits.is_contiguous():
+        x2, lead = logits, shape[:1]
+        n, width = shape
+        ld = width
+    else:
+        lead = shape[:-1]
+        x2 = _rows2d(logits)
+        n, width = x2.shape
+        ld = _row_stride(x2)
     v = width if vocab is None else int(vocab)
     if not 1 <= v <= width:
         raise ValueError(f"vocab {v} outside [1, {width}]")
     device = logits.device
+    index = device.index
     t1 = _targets1d(target_ids, lead, device)
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=device)
@@ -136,8 +169,7 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
     want_ent = return_entropy or entropy is not None
     if want_ent and entropy is None:
         entropy = torch.empty(n, dtype=torch.float32, device=device)
-    index = device.index
-    st = _on_device(index, _lib.load().bil_logp_fwd, x2.data_ptr(), _code(x2.dtype), n, v, _row_stride(x2),
+    st = _on_device(index, _lib.load().bil_logp_fwd, x2.data_ptr(), _code(x2.dtype), n, v, ld,
                     t1.data_ptr(), int(ignore_index), int(tile_v), float(temperature), out.data_ptr(),
                     lse.data_ptr(), entropy.data_ptr() if want_ent else None, 1 if validate else 0,
                     _stream_handle(index))
