@@ -370,6 +370,36 @@ int bil_linear_logp_bwd(const void *hidden, const void *weight, const void *weig
                         void *dweight, int dweight_dtype, int64_t ld_dweight, bil_stream_t stream);
 
 /*
+ * bil_linear_logp_grad -- the first step of bil_linear_logp_bwd alone: dZ of
+ * the shard's columns from the recomputed projection, written to dz
+ * [n_rows, ld_dz] and dz_t [cols, ld_dz_t] (the same bits as there).
+ * Arguments, layouts and errors as for bil_linear_logp_bwd; nothing else is
+ * written.  Together with bil_transpose_2d and bil_linear_gemm_nt it lets a
+ * caller queue (and time) the backward's steps one by one.
+ */
+int bil_linear_logp_grad(const void *hidden, const void *weight, int dtype, int64_t n_rows,
+                         int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight,
+                         int32_t tile_begin, int32_t tile_end, float temperature,
+                         const int64_t *target_ids, int64_t ignore_index, const float *lse,
+                         const float *grad_logp, const float *entropy, const float *grad_entropy,
+                         void *dz, int64_t ld_dz, void *dz_t, int64_t ld_dz_t, bil_stream_t stream);
+
+/*
+ * bil_linear_gemm_nt -- C = A . B^T on the tensor cores, the contraction
+ * bil_linear_logp_bwd uses for dhidden (A = dZ, B = weight^T) and dweight
+ * (A = dZ^T, B = hidden^T).  A [m, k] and B [n, k] are row-major (K-major)
+ * matrices of dtype (BIL_BF16 or BIL_F16; row strides lda, ldb >= k
+ * elements); C [m, ldc] (ldc >= n) receives C[i, j] = sum_k A[i, k] B[j, k]
+ * accumulated in float32 in K blocks of 64 in increasing order, stored as
+ * c_dtype (BIL_F32, or dtype rounded to nearest even).  Row i of C depends on
+ * row i of A and on B only.  16-byte aligned bases and row strides of a
+ * multiple of 16 bytes (BIL_E_ALIGN otherwise); k >= 1; m = 0 or n = 0 queue
+ * nothing.  Device pointers owned by the caller; asynchronous on `stream`.
+ */
+int bil_linear_gemm_nt(const void *a, const void *b, int dtype, int64_t m, int64_t n, int64_t k,
+                       int64_t lda, int64_t ldb, void *c, int c_dtype, int64_t ldc, bil_stream_t stream);
+
+/*
  * bil_sum_f32 -- dst[i] = ((srcs[0][i] + srcs[1][i]) + srcs[2][i]) + ... for
  * i < n: float32 sums in the order of `srcs` (1 <= count <= 16; `srcs` is a
  * host array of device pointers; dst may be one of the sources).  Adds the

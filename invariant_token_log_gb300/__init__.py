@@ -14,8 +14,10 @@ from .linear import (  # noqa: F401
     LINEAR_TILE_V,
     LinearLogp,
     batch_invariant_linear_logp,
+    gemm_nt,
     linear_logp,
     linear_logp_bwd,
+    linear_logp_grad,
     linear_logp_partials,
 )
 from .logp import (  # noqa: F401

@@ -43,6 +43,9 @@ SIGNATURES = {
     "bil_linear_logp_bwd": (_i32, [_p, _p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32,
                                    ctypes.c_int32, _f, _p, _i64, _p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p,
                                    _i32, _i64, _p, _i32, _i64, _p]),
+    "bil_linear_logp_grad": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, ctypes.c_int32,
+                                    _f, _p, _i64, _p, _p, _p, _p, _p, _i64, _p, _i64, _p]),
+    "bil_linear_gemm_nt": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _p, _i32, _i64, _p]),
     "bil_sum_f32": (_i32, [ctypes.POINTER(ctypes.c_void_p), _i32, _i64, _p, _p]),
     "bil_transpose_2d": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, _p]),
     "bil_probe_exp_rate": (_i32, [ctypes.c_int32, ctypes.c_int32, _p, _p, _p]),

@@ -50,6 +50,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 namespace {
@@ -72,7 +73,8 @@ constexpr unsigned kStageBytes = kStageABytes + kStageBBytes;
 constexpr int kAccCols = kBN;            // one 32-bit tensor-memory column per output column
 constexpr uint32_t kTmemCols = 2 * kAccCols;  // two accumulator buffers: 512 columns
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kSyncWarp = 2 + kEpiWarps;  // the store GEMMs' lockstep (see lockstep_service)
+constexpr int kThreads = 32 * (kSyncWarp + 1);
 constexpr int kChunk = 32;               // columns per tensor-memory load
 constexpr int kMGroup = 32;              // row tiles per raster group (L2 reuse of the weight tiles)
 
@@ -86,6 +88,11 @@ struct alignas(8) LinearSmem {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
+  // lockstep of the store GEMMs: the copy thread's position (K blocks issued),
+  // the position it may issue up to, and whether it has issued everything
+  uint32_t sync_pos;
+  uint32_t sync_allowed;
+  int sync_done;
 };
 
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * size_t(kStageBytes) + sizeof(LinearSmem);
@@ -133,6 +140,7 @@ struct LinearParams {
   unsigned char* out;          // [n_rows, ld_out]
   int out_dtype;
   int64_t ld_out;
+  unsigned sync_tag;           // non-zero: the copy threads keep in step (see lockstep_service)
 };
 
 // ---------------------------------------------------------------------------
@@ -399,6 +407,106 @@ __device__ __forceinline__ void row_store(uint32_t taddr, int vcols, bool valid,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Soft lockstep of the store GEMMs' copy threads.  Their K is long (the
+// vocabulary for dhidden), and the blocks of one wave read the same A and B
+// tiles at the same K position: when they drift apart by more K blocks than
+// L2 holds for the wave, the tiles they share come from DRAM again for every
+// block that reads them late (45 GB of DRAM reads for dhidden's 5 GB of dZ
+// and 1.2 GB of W^T at 16384 x 151936 x 4096, against 27 GB in step).
+//
+// A service warp per block (kSyncWarp) publishes, every few microseconds,
+// how many K blocks its copy thread has issued (in a 128-byte line of its
+// own), reads every block's position,
+// and tells its copy thread in shared memory how far it may go: kSyncLead K
+// blocks past the slowest block of the same launch.  The copy thread only
+// reads that bound, so the polling stays off its path.  Positions are tagged
+// with a per-launch number, so stale entries of other launches count for
+// nothing; a block that has issued all its copies publishes the largest
+// position.  Every wait is bounded: the copy thread waits at most kSyncWaitNs
+// for the bound to move and otherwise stops keeping step for the rest of the
+// launch; the service warp stops when its copy thread is done or has not
+// moved for the wait limit.  None of this touches what is computed: a tile's
+// copies, MMAs and K order do not depend on it.
+// ---------------------------------------------------------------------------
+
+#ifndef BIL_STORE_LOCKSTEP
+#define BIL_STORE_LOCKSTEP 1
+#endif
+
+constexpr int kSyncLead = 64;
+constexpr int kSyncMinKBlocks = 1024;      // the shortest K (in blocks of kBK) that keeps step
+constexpr int kSyncMaxBlocks = 1024;
+constexpr long long kSyncWaitNs = 50000;   // 50 us
+constexpr unsigned kSyncPollNs = 4000;     // the service warp's pause between two updates
+constexpr uint32_t kSyncDone = 0xffffffffu;
+constexpr int kSyncSlotWords = 16;         // one 128-byte line per block: no two blocks write one line
+
+__device__ unsigned long long g_sync_pos[kSyncMaxBlocks * kSyncSlotWords];
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* a, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void lockstep_publish(unsigned tag, uint32_t pos) {
+  st_relaxed_u64(&g_sync_pos[blockIdx.x * kSyncSlotWords], (static_cast<unsigned long long>(tag) << 32) | pos);
+}
+
+// The service warp's loop (all 32 lanes).
+__device__ __forceinline__ void lockstep_service(unsigned tag, LinearSmem& sm, volatile int* abort, int lane) {
+  volatile uint32_t* pos_p = &sm.sync_pos;
+  volatile uint32_t* allowed_p = &sm.sync_allowed;
+  volatile int* done_p = &sm.sync_done;
+  uint32_t last = kSyncDone;
+  long long last_move = 0;
+  for (;;) {
+    const uint32_t pos = __shfl_sync(0xffffffffu, *pos_p, 0);
+    const int stop = __shfl_sync(0xffffffffu, (*done_p != 0 || *abort != 0) ? 1 : 0, 0);
+    if (stop) break;
+    if (lane == 0) lockstep_publish(tag, pos);
+    uint32_t slowest = kSyncDone;
+    for (int b = lane; b < static_cast<int>(gridDim.x); b += kLanes) {
+      const unsigned long long v = ld_relaxed_u64(&g_sync_pos[b * kSyncSlotWords]);
+      if (static_cast<unsigned>(v >> 32) == tag) slowest = min(slowest, static_cast<uint32_t>(v));
+    }
+    slowest = __reduce_min_sync(0xffffffffu, slowest);
+    if (lane == 0) *allowed_p = slowest == kSyncDone ? kSyncDone : slowest + static_cast<uint32_t>(kSyncLead);
+    const long long now = __shfl_sync(0xffffffffu, global_ns(), 0);
+    if (pos != last) {
+      last = pos;
+      last_move = now;
+    } else if (now - last_move > kWaitLimitNs) {
+      break;  // the copy thread has stopped moving: leave it unbounded
+    }
+    __nanosleep(kSyncPollNs);
+  }
+  if (lane == 0) {
+    *allowed_p = kSyncDone;
+    lockstep_publish(tag, kSyncDone);  // never wait for this block again
+  }
+}
+
+// The copy thread's side: publish the position, and wait (at most
+// kSyncWaitNs) until it is within the bound.  Returns false when the wait ran
+// out (the caller then stops keeping step).
+__device__ __forceinline__ bool lockstep_gate(LinearSmem& sm, uint32_t pos) {
+  volatile uint32_t* allowed_p = &sm.sync_allowed;
+  *reinterpret_cast<volatile uint32_t*>(&sm.sync_pos) = pos;
+  if (pos <= *allowed_p) return true;
+  const long long start = global_ns();
+  while (pos > *allowed_p) {
+    if (global_ns() - start > kSyncWaitNs) return false;
+    __nanosleep(200);
+  }
+  return true;
+}
+
 // The GEMM C = A . B^T (A [rows, K], B [cols, K], both K-major 16-bit) with
 // one of the epilogues above.  See the file's head for the block structure.
 template <int MODE, bool ENT, int DT>
@@ -425,6 +533,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
     }
     mbar_init(&sm.mma_done, 1);
     sm.abort = 0;
+    sm.sync_pos = 0;
+    sm.sync_allowed = kSyncLead;
+    sm.sync_done = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -440,15 +551,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
 
   const int64_t total = static_cast<int64_t>(p.num_m) * p.num_n;
 
+  const bool lockstep = MODE == kModeStore && p.sync_tag != 0u;
   if (warp == 0) {
     if (lane == 0) {
       // ---- producer ----
+      bool sync_on = lockstep;
       int64_t it = 0;
       bool ok = true;
       for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x) {
         int m, n;
         unit_coords(u, p.num_m, p.num_n, p.m_group, m, n);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          if (sync_on) sync_on = lockstep_gate(sm, static_cast<uint32_t>(it));
           const int s = static_cast<int>(it % kStages);
           const unsigned ph = static_cast<unsigned>((it / kStages) & 1);
           if (!thread_wait_watch(&sm.empty[s], ph ^ 1u, abort, kWatchStageFree, &g_watchdog_linear, true)) {
@@ -461,6 +575,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
           tma_load_2d(a_dst + kStageABytes, &tmap_weight, kb * kBK, n * kBN, &sm.full[s]);
         }
       }
+      if (lockstep) *reinterpret_cast<volatile int*>(&sm.sync_done) = 1;
       // Wait (bounded, whatever happened) for the copies still in flight: the
       // last min(it, kStages) fills, one per stage.
       for (int64_t i = it > kStages ? it - kStages : 0; i < it; ++i) {
@@ -506,6 +621,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
       umma_commit(&sm.mma_done);
       thread_wait_watch(&sm.mma_done, 0u, abort, kWatchOwnDrain, &g_watchdog_linear, false);
     }
+  } else if (warp == kSyncWarp) {
+    if (lockstep) lockstep_service(p.sync_tag, sm, abort, lane);
   } else {
     // ---- epilogue ----
     const int q = warp & 3;  // this warp reads tensor-memory lanes [32q, 32q + 32)
@@ -810,6 +927,123 @@ int static_scratch(void** out) {
   return BIL_OK;
 }
 
+// The next per-launch tag of the store GEMMs' lockstep (never 0).
+unsigned next_sync_tag() {
+  static std::atomic<unsigned> counter{0};
+  unsigned t = 0;
+  while (t == 0) t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  return t;
+}
+
+// C [a_rows, n_cols] = A . B^T over K = k with the store epilogue, rastered in
+// groups of row tiles that one wave covers with every column tile, the copy
+// threads in lockstep when every block's position fits the tag's 32 bits.
+int launch_store(const CUtensorMap& ma, const CUtensorMap& mb, int64_t a_rows, int64_t n_cols, int64_t k,
+                 uint32_t idesc, void* out, int out_dtype, int64_t ld_out, cudaStream_t s) {
+  LinearParams p{};
+  p.n_rows = a_rows;
+  p.shard_cols = n_cols;
+  p.num_n = static_cast<int>((n_cols + kBN - 1) / kBN);
+  p.num_m = static_cast<int>((a_rows + kBM - 1) / kBM);
+  p.k_blocks = static_cast<int>((k + kBK - 1) / kBK);
+  p.idesc = idesc;
+  p.a_box_bytes = kStageABytes;  // A maps of these GEMMs use kBM-row boxes
+  p.m_group = store_group(p.num_n);
+  p.out = static_cast<unsigned char*>(out);
+  p.out_dtype = out_dtype;
+  p.ld_out = ld_out;
+  int sms = 0, smem = 0;
+  if (int st = bil_internal::device_limits(&sms, &smem)) return st;
+  const int64_t total = static_cast<int64_t>(p.num_m) * p.num_n;
+  const int64_t grid = std::min<int64_t>(total, sms);
+  const int64_t iters = (total + grid - 1) / grid * p.k_blocks;  // K blocks one block issues
+  // Only units of a long K drift apart far enough to matter (measured on 16384 x 151936 x 4096: dhidden,
+  // K = 151936, read 46 GB of DRAM alone and 27 GB in step, 5% faster; dweight, K = 16384, read 26 GB
+  // either way and was 1% slower in step).
+  p.sync_tag = BIL_STORE_LOCKSTEP && p.k_blocks >= kSyncMinKBlocks && grid <= kSyncMaxBlocks &&
+                       iters + kSyncLead < INT32_MAX
+                   ? next_sync_tag()
+                   : 0u;
+  GemmKernel kern = out_dtype == BIL_F32    ? linear_store_kernel<BIL_F32>
+                    : out_dtype == BIL_BF16 ? linear_store_kernel<BIL_BF16>
+                                            : linear_store_kernel<BIL_F16>;
+  return launch_gemm(kern, ma, mb, p, s);
+}
+
+// dZ of the shard's columns from the recomputed projection (maps: hidden with
+// kBM-row boxes, weight with kBN-row boxes), stored as dz and dz_t.
+int launch_grad(const CUtensorMap& mh, const CUtensorMap& mw, int dtype, int64_t n_rows, int64_t hidden_size,
+                int64_t cols, int32_t tile_begin, int32_t tile_end, float rcp, const int64_t* targets,
+                int64_t ignore_index, const float* lse, const float* grad_logp, const float* entropy,
+                const float* grad_entropy, int64_t vocab, void* dz, int64_t ld_dz, void* dz_t, int64_t ld_dz_t,
+                cudaStream_t s) {
+  LinearParams p{};
+  p.n_rows = n_rows;
+  p.shard_cols = cols;
+  p.tile_begin = tile_begin;
+  p.num_n = tile_end - tile_begin;
+  p.num_m = static_cast<int>((n_rows + kBM - 1) / kBM);
+  p.k_blocks = static_cast<int>((hidden_size + kBK - 1) / kBK);
+  p.targets = targets;
+  p.ignore_index = ignore_index;
+  p.rcp = rcp;
+  p.idesc = make_idesc(dtype == BIL_BF16);
+  p.a_box_bytes = kStageABytes;
+  p.m_group = kMGroup;
+  p.lse = lse;
+  p.grad_logp = grad_logp;
+  p.entropy = entropy;
+  p.grad_entropy = grad_entropy;
+  p.vocab = vocab;
+  p.dz = static_cast<unsigned char*>(dz);
+  p.ld_dz = ld_dz;
+  p.dz_t = static_cast<unsigned char*>(dz_t);
+  p.ld_dz_t = ld_dz_t;
+  const bool ent = entropy != nullptr;
+  GemmKernel k = dtype == BIL_BF16 ? (ent ? linear_grad_kernel<true, BIL_BF16> : linear_grad_kernel<false, BIL_BF16>)
+                                   : (ent ? linear_grad_kernel<true, BIL_F16> : linear_grad_kernel<false, BIL_F16>);
+  return launch_gemm(k, mh, mw, p, s);
+}
+
+// Host-side checks of the gradient pass's arguments (those bil_linear_logp_bwd
+// and bil_linear_logp_grad share); *cols = the shard's vocabulary columns.
+int check_grad_args(const void* hidden, const void* weight, int64_t n_rows, int64_t hidden_size, int64_t ld_hidden,
+                    int64_t vocab, int64_t ld_weight, int32_t tile_begin, int32_t tile_end, const int64_t* targets,
+                    const float* lse, const float* grad_logp, const float* entropy, const float* grad_entropy,
+                    const void* dz, int64_t ld_dz, const void* dz_t, int64_t ld_dz_t, int64_t* cols_out) {
+  if (vocab < 1) return BIL_E_INVALID_ARG;
+  if (vocab > BIL_MAX_EXTENT_BYTES) return BIL_E_UNSUPPORTED;
+  const int64_t num_tiles = (vocab + kBN - 1) / kBN;
+  if (num_tiles > INT32_MAX / 2) return BIL_E_UNSUPPORTED;
+  if (tile_begin < 0 || tile_begin >= tile_end || tile_end > num_tiles) return BIL_E_INVALID_ARG;
+  // the shard: global vocabulary columns [tile_begin * 256, min(tile_end * 256, vocab))
+  const int64_t cols = std::min<int64_t>(static_cast<int64_t>(tile_end) * kBN, vocab) -
+                       static_cast<int64_t>(tile_begin) * kBN;
+  if (n_rows < 0 || hidden_size < 1 || ld_hidden < hidden_size || ld_weight < hidden_size || ld_dz < cols ||
+      ld_dz_t < n_rows)
+    return BIL_E_INVALID_ARG;
+  if ((entropy == nullptr) != (grad_entropy == nullptr)) return BIL_E_INVALID_ARG;
+  {
+    using bil_internal::extent_ok;
+    if (!extent_ok(n_rows, ld_hidden, 2) || !extent_ok(cols, ld_weight, 2) || !extent_ok(n_rows, ld_dz, 2) ||
+        !extent_ok(cols, ld_dz_t, 2))
+      return BIL_E_UNSUPPORTED;
+  }
+  if (weight == nullptr) return BIL_E_INVALID_ARG;
+  if (!rows16(weight, ld_weight, 2)) return BIL_E_ALIGN;
+  *cols_out = cols;
+  if (n_rows == 0) return BIL_OK;
+  if (hidden == nullptr || targets == nullptr || lse == nullptr || grad_logp == nullptr || dz == nullptr ||
+      dz_t == nullptr)
+    return BIL_E_INVALID_ARG;
+  if (!rows16(hidden, ld_hidden, 2) || !rows16(dz, ld_dz, 2) || !rows16(dz_t, ld_dz_t, 2)) return BIL_E_ALIGN;
+  if (!aligned_to(targets, 8) || !aligned_to(lse, 4) || !aligned_to(grad_logp, 4) ||
+      (entropy && (!aligned_to(entropy, 4) || !aligned_to(grad_entropy, 4))))
+    return BIL_E_ALIGN;
+  if (n_rows > INT32_MAX - kBM || cols > INT32_MAX - kBN || hidden_size > INT32_MAX - kBN) return BIL_E_UNSUPPORTED;
+  return BIL_OK;
+}
+
 }  // namespace
 
 namespace bil_internal {
@@ -979,43 +1213,33 @@ int bil_transpose_2d(const void* src, int dtype, int64_t rows, int64_t cols, int
 
 int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weight_t, int dtype, int64_t n_rows,
                         int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight, int64_t ld_weight_t,
-                        int32_t tile_begin, int32_t tile_end, float temperature, const int64_t* target_ids, int64_t ignore_index, const float* lse,
-                        const float* grad_logp, const float* entropy, const float* grad_entropy, void* dz,
-                        int64_t ld_dz, void* dz_t, int64_t ld_dz_t, void* hidden_t, int64_t ld_hidden_t,
-                        void* dhidden, int dhidden_dtype, int64_t ld_dhidden, void* dweight, int dweight_dtype,
-                        int64_t ld_dweight, bil_stream_t stream) {
+                        int32_t tile_begin, int32_t tile_end, float temperature, const int64_t* target_ids,
+                        int64_t ignore_index, const float* lse, const float* grad_logp, const float* entropy,
+                        const float* grad_entropy, void* dz, int64_t ld_dz, void* dz_t, int64_t ld_dz_t,
+                        void* hidden_t, int64_t ld_hidden_t, void* dhidden, int dhidden_dtype, int64_t ld_dhidden,
+                        void* dweight, int dweight_dtype, int64_t ld_dweight, bil_stream_t stream) {
   bil_internal::NvtxRange nvtx_range("bil_linear_logp_bwd");
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   for (int ot : {dhidden_dtype, dweight_dtype})
     if (ot != BIL_F32 && ot != dtype) return BIL_E_DTYPE;
-  if (vocab < 1) return BIL_E_INVALID_ARG;
-  if (vocab > BIL_MAX_EXTENT_BYTES) return BIL_E_UNSUPPORTED;
-  const int64_t num_tiles = (vocab + kBN - 1) / kBN;
-  if (num_tiles > INT32_MAX / 2) return BIL_E_UNSUPPORTED;
-  if (tile_begin < 0 || tile_begin >= tile_end || tile_end > num_tiles) return BIL_E_INVALID_ARG;
-  // the shard: global vocabulary columns [tile_begin * 256, min(tile_end * 256, vocab))
-  const int64_t cols = std::min<int64_t>(static_cast<int64_t>(tile_end) * kBN, vocab) -
-                       static_cast<int64_t>(tile_begin) * kBN;
-  if (n_rows < 0 || hidden_size < 1 || ld_hidden < hidden_size || ld_weight < hidden_size ||
-      ld_weight_t < cols || ld_dz < cols || ld_dz_t < n_rows || ld_hidden_t < n_rows ||
-      ld_dhidden < hidden_size || ld_dweight < hidden_size)
+  int64_t cols = 0;
+  if (int st = check_grad_args(hidden, weight, n_rows, hidden_size, ld_hidden, vocab, ld_weight, tile_begin, tile_end,
+                               target_ids, lse, grad_logp, entropy, grad_entropy, dz, ld_dz, dz_t, ld_dz_t, &cols))
+    return st;
+  if (ld_weight_t < cols || ld_hidden_t < n_rows || ld_dhidden < hidden_size || ld_dweight < hidden_size)
     return BIL_E_INVALID_ARG;
-  if ((entropy == nullptr) != (grad_entropy == nullptr)) return BIL_E_INVALID_ARG;
   {
     using bil_internal::extent_ok;
     const int64_t eh = dhidden_dtype == BIL_F32 ? 4 : 2, ew = dweight_dtype == BIL_F32 ? 4 : 2;
-    if (!extent_ok(n_rows, ld_hidden, 2) || !extent_ok(cols, ld_weight, 2) ||
-        !extent_ok(hidden_size, ld_weight_t, 2) || !extent_ok(n_rows, ld_dz, 2) || !extent_ok(cols, ld_dz_t, 2) ||
-        !extent_ok(hidden_size, ld_hidden_t, 2) || !extent_ok(n_rows, ld_dhidden, eh) ||
-        !extent_ok(cols, ld_dweight, ew))
+    if (!extent_ok(hidden_size, ld_weight_t, 2) || !extent_ok(hidden_size, ld_hidden_t, 2) ||
+        !extent_ok(n_rows, ld_dhidden, eh) || !extent_ok(cols, ld_dweight, ew))
       return BIL_E_UNSUPPORTED;
   }
   float rcp = 1.0f;
   if (int st = bil_internal::temperature_rcp(temperature, &rcp)) return st;
-  if (weight == nullptr || weight_t == nullptr || dweight == nullptr) return BIL_E_INVALID_ARG;
+  if (weight_t == nullptr || dweight == nullptr) return BIL_E_INVALID_ARG;
   const int64_t eo_h = dhidden_dtype == BIL_F32 ? 4 : 2, eo_w = dweight_dtype == BIL_F32 ? 4 : 2;
-  if (!rows16(weight, ld_weight, 2) || !rows16(weight_t, ld_weight_t, 2) || !rows16(dweight, ld_dweight, eo_w))
-    return BIL_E_ALIGN;
+  if (!rows16(weight_t, ld_weight_t, 2) || !rows16(dweight, ld_dweight, eo_w)) return BIL_E_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (n_rows == 0) {  // dweight is a sum over no rows
     return cudaMemset2DAsync(dweight, static_cast<size_t>(ld_dweight * eo_w), 0,
@@ -1023,17 +1247,8 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
                ? BIL_OK
                : BIL_E_CUDA;
   }
-  if (hidden == nullptr || target_ids == nullptr || lse == nullptr || grad_logp == nullptr || dz == nullptr ||
-      dz_t == nullptr || hidden_t == nullptr || dhidden == nullptr)
-    return BIL_E_INVALID_ARG;
-  if (!rows16(hidden, ld_hidden, 2) || !rows16(dz, ld_dz, 2) || !rows16(dz_t, ld_dz_t, 2) ||
-      !rows16(hidden_t, ld_hidden_t, 2) || !rows16(dhidden, ld_dhidden, eo_h))
-    return BIL_E_ALIGN;
-  if (!aligned_to(target_ids, 8) || !aligned_to(lse, 4) || !aligned_to(grad_logp, 4) ||
-      (entropy && (!aligned_to(entropy, 4) || !aligned_to(grad_entropy, 4))))
-    return BIL_E_ALIGN;
-  if (n_rows > INT32_MAX - kBM || cols > INT32_MAX - kBN || hidden_size > INT32_MAX - kBN)
-    return BIL_E_UNSUPPORTED;
+  if (hidden_t == nullptr || dhidden == nullptr) return BIL_E_INVALID_ARG;
+  if (!rows16(hidden_t, ld_hidden_t, 2) || !rows16(dhidden, ld_dhidden, eo_h)) return BIL_E_ALIGN;
   if ((n_rows + 63) / 64 > 65535) return BIL_E_UNSUPPORTED;  // the transpose's grid
 
   // Every tensor map is encoded before anything is queued.
@@ -1050,73 +1265,61 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
     if (!st) st = make_map(&maps[5], hidden_t, dtype, hidden_size, n_rows, ld_hidden_t, kBN);
     if (st) return st;
   }
-
+  const uint32_t idesc = make_idesc(dtype == BIL_BF16);
   // 1. hidden^T [H, n_rows], the K-major B operand of dweight = dZ^T . hidden
   if (int st = launch_transpose16(hidden, n_rows, hidden_size, ld_hidden, hidden_t, ld_hidden_t, s)) return st;
-
-  const uint32_t idesc = make_idesc(dtype == BIL_BF16);
   // 2. dZ from the recomputed projection, stored as dz [n, V] and dz_t [V, n]
-  {
-    LinearParams p{};
-    p.n_rows = n_rows;
-    p.shard_cols = cols;
-    p.tile_begin = tile_begin;
-    p.num_n = tile_end - tile_begin;
-    p.num_m = static_cast<int>((n_rows + kBM - 1) / kBM);
-    p.k_blocks = static_cast<int>((hidden_size + kBK - 1) / kBK);
-    p.targets = target_ids;
-    p.ignore_index = ignore_index;
-    p.rcp = rcp;
-    p.idesc = idesc;
-    p.a_box_bytes = kStageABytes;  // A maps of these GEMMs use kBM-row boxes
-    p.m_group = kMGroup;
-    p.lse = lse;
-    p.grad_logp = grad_logp;
-    p.entropy = entropy;
-    p.grad_entropy = grad_entropy;
-    p.vocab = vocab;
-    p.dz = static_cast<unsigned char*>(dz);
-    p.ld_dz = ld_dz;
-    p.dz_t = static_cast<unsigned char*>(dz_t);
-    p.ld_dz_t = ld_dz_t;
-    const bool ent = entropy != nullptr;
-    GemmKernel k = dtype == BIL_BF16 ? (ent ? linear_grad_kernel<true, BIL_BF16> : linear_grad_kernel<false, BIL_BF16>)
-                                     : (ent ? linear_grad_kernel<true, BIL_F16> : linear_grad_kernel<false, BIL_F16>);
-    if (int st = launch_gemm(k, maps[0], maps[1], p, s)) return st;
-  }
+  if (int st = launch_grad(maps[0], maps[1], dtype, n_rows, hidden_size, cols, tile_begin, tile_end, rcp, target_ids,
+                           ignore_index, lse, grad_logp, entropy, grad_entropy, vocab, dz, ld_dz, dz_t, ld_dz_t, s))
+    return st;
   // 3. dhidden = dZ . weight   (A = dz [n, V], B = weight^T [H, V], K = V)
+  if (int st = launch_store(maps[2], maps[3], n_rows, hidden_size, cols, idesc, dhidden, dhidden_dtype, ld_dhidden, s))
+    return st;
   // 4. dweight = dZ^T . hidden (A = dz_t [V, n], B = hidden^T [H, n], K = n)
-  struct Contraction {
-    const CUtensorMap* ma;
-    const CUtensorMap* mb;
-    int64_t a_rows, k;
-    void* out;
-    int out_dtype;
-    int64_t ld_out;
-  };
-  const Contraction cs[2] = {
-      {&maps[2], &maps[3], n_rows, cols, dhidden, dhidden_dtype, ld_dhidden},
-      {&maps[4], &maps[5], cols, n_rows, dweight, dweight_dtype, ld_dweight},
-  };
-  for (const Contraction& c : cs) {
-    LinearParams p{};
-    p.n_rows = c.a_rows;
-    p.shard_cols = hidden_size;
-    p.num_n = static_cast<int>((hidden_size + kBN - 1) / kBN);
-    p.num_m = static_cast<int>((c.a_rows + kBM - 1) / kBM);
-    p.k_blocks = static_cast<int>((c.k + kBK - 1) / kBK);
-    p.idesc = idesc;
-    p.a_box_bytes = kStageABytes;  // A maps of these GEMMs use kBM-row boxes
-    p.m_group = store_group(p.num_n);
-    p.out = static_cast<unsigned char*>(c.out);
-    p.out_dtype = c.out_dtype;
-    p.ld_out = c.ld_out;
-    GemmKernel k = c.out_dtype == BIL_F32    ? linear_store_kernel<BIL_F32>
-                   : c.out_dtype == BIL_BF16 ? linear_store_kernel<BIL_BF16>
-                                             : linear_store_kernel<BIL_F16>;
-    if (int st = launch_gemm(k, *c.ma, *c.mb, p, s)) return st;
-  }
-  return BIL_OK;
+  return launch_store(maps[4], maps[5], cols, hidden_size, n_rows, idesc, dweight, dweight_dtype, ld_dweight, s);
+}
+
+int bil_linear_logp_grad(const void* hidden, const void* weight, int dtype, int64_t n_rows, int64_t hidden_size,
+                         int64_t ld_hidden, int64_t vocab, int64_t ld_weight, int32_t tile_begin, int32_t tile_end,
+                         float temperature, const int64_t* target_ids, int64_t ignore_index, const float* lse,
+                         const float* grad_logp, const float* entropy, const float* grad_entropy, void* dz,
+                         int64_t ld_dz, void* dz_t, int64_t ld_dz_t, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_linear_logp_grad");
+  if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
+  int64_t cols = 0;
+  if (int st = check_grad_args(hidden, weight, n_rows, hidden_size, ld_hidden, vocab, ld_weight, tile_begin, tile_end,
+                               target_ids, lse, grad_logp, entropy, grad_entropy, dz, ld_dz, dz_t, ld_dz_t, &cols))
+    return st;
+  float rcp = 1.0f;
+  if (int st = bil_internal::temperature_rcp(temperature, &rcp)) return st;
+  if (n_rows == 0) return BIL_OK;
+  CUtensorMap mh, mw;
+  if (int st = make_map(&mh, hidden, dtype, n_rows, hidden_size, ld_hidden, kBM)) return st;
+  if (int st = make_map(&mw, weight, dtype, cols, hidden_size, ld_weight, kBN)) return st;
+  return launch_grad(mh, mw, dtype, n_rows, hidden_size, cols, tile_begin, tile_end, rcp, target_ids, ignore_index, lse,
+                     grad_logp, entropy, grad_entropy, vocab, dz, ld_dz, dz_t, ld_dz_t,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bil_linear_gemm_nt(const void* a, const void* b, int dtype, int64_t m, int64_t n, int64_t k, int64_t lda,
+                       int64_t ldb, void* c, int c_dtype, int64_t ldc, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_linear_gemm_nt");
+  if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
+  if (c_dtype != BIL_F32 && c_dtype != dtype) return BIL_E_DTYPE;
+  if (m < 0 || n < 0 || k < 1 || lda < k || ldb < k || ldc < n) return BIL_E_INVALID_ARG;
+  const int64_t ec = c_dtype == BIL_F32 ? 4 : 2;
+  if (!bil_internal::extent_ok(m, lda, 2) || !bil_internal::extent_ok(n, ldb, 2) ||
+      !bil_internal::extent_ok(m, ldc, ec))
+    return BIL_E_UNSUPPORTED;
+  if (m == 0 || n == 0) return BIL_OK;
+  if (a == nullptr || b == nullptr || c == nullptr) return BIL_E_INVALID_ARG;
+  if (!rows16(a, lda, 2) || !rows16(b, ldb, 2) || !rows16(c, ldc, ec)) return BIL_E_ALIGN;
+  if (m > INT32_MAX - kBM || n > INT32_MAX - kBN || k > INT32_MAX - kBK) return BIL_E_UNSUPPORTED;
+  CUtensorMap ma, mb;
+  if (int st = make_map(&ma, a, dtype, m, k, lda, kBM)) return st;
+  if (int st = make_map(&mb, b, dtype, n, k, ldb, kBN)) return st;
+  return launch_store(ma, mb, m, n, k, make_idesc(dtype == BIL_BF16), c, c_dtype, ldc,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 int bil_linear_logp_fwd_static(const void* hidden, const void* weight, int dtype, int64_t n_rows,

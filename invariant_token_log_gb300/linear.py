@@ -226,6 +226,53 @@ def linear_logp_bwd(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torc
     return out + (dz,) if return_dz else out
 
 
+def linear_logp_grad(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor,
+                     grad_logp: torch.Tensor, ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                     entropy: torch.Tensor | None = None, grad_entropy: torch.Tensor | None = None):
+    """(dZ [N, V], dZ^T [V, N]) of g * logp (+ gh * entropy) over the whole vocabulary
+    (V = weight rows): the first step of ``linear_logp_bwd`` alone, the same bits."""
+    _need_cuda(hidden, weight, target_ids, lse, grad_logp, entropy, grad_entropy)
+    h2, w2 = _matrix(hidden, "hidden"), _matrix(weight, "weight")
+    if h2.dtype != w2.dtype or h2.shape[1] != w2.shape[1]:
+        raise ValueError("hidden and weight must share the element type and the hidden size")
+    if (entropy is None) != (grad_entropy is None):
+        raise ValueError("entropy and grad_entropy come together")
+    n, hs = h2.shape
+    v = w2.shape[0]
+    dev = h2.device
+    t = target_ids.reshape(-1).to(torch.int64).contiguous()
+    f32 = [x.reshape(-1).float().contiguous() if x is not None else None
+           for x in (lse, grad_logp, entropy, grad_entropy)]
+    dz = torch.empty((n, _pad8(v)), dtype=h2.dtype, device=dev)[:, :v]
+    dz_t = torch.empty((v, _pad8(max(n, 1))), dtype=h2.dtype, device=dev)[:, :n]
+    _lib.check("bil_linear_logp_grad", _lib.load().bil_linear_logp_grad(
+        _ptr(h2), _ptr(w2), _in_code(h2.dtype), n, hs, _ld(h2), v, _ld(w2), 0, num_tiles(v), float(temperature),
+        _ptr(t), ignore_index, _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), _ptr(f32[3]), _ptr(dz), dz.stride(0),
+        _ptr(dz_t), dz_t.stride(0), _stream(dev)))
+    return dz, dz_t
+
+
+def gemm_nt(a: torch.Tensor, b: torch.Tensor, out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    """C = a . b^T for a [m, k] and b [n, k] (both bfloat16 or both float16, rows
+    16-byte aligned) on the tensor cores, float32 accumulation over K blocks of 64
+    in order: the backward's dhidden and dweight contraction.  C is float32 or the
+    inputs' type."""
+    _need_cuda(a, b)
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1] or a.dtype != b.dtype:
+        raise ValueError("gemm_nt takes a [m, k] and b [n, k] of one 16-bit type")
+    if out_dtype not in (torch.float32, a.dtype):
+        raise TypeError("out_dtype must be float32 or the inputs' type")
+    a2, b2 = _matrix(a, "a"), _matrix(b, "b")
+    m, k = a2.shape
+    n = b2.shape[0]
+    c = torch.empty((m, _pad8(n)), dtype=out_dtype, device=a2.device)[:, :n]
+    oc = _lib.F32 if out_dtype == torch.float32 else _in_code(out_dtype)
+    _lib.check("bil_linear_gemm_nt", _lib.load().bil_linear_gemm_nt(
+        _ptr(a2), _ptr(b2), _in_code(a2.dtype), m, n, k, _ld(a2), _ld(b2), _ptr(c), oc, c.stride(0),
+        _stream(a2.device)))
+    return c
+
+
 class LinearLogp(torch.autograd.Function):
     """Fused LM-head + logp with the autograd actor path: the forward keeps only
     lse (and the entropy); the backward recomputes the projection tiles."""

@@ -242,6 +242,44 @@ def test_lm_head_calls_reject_extents_above_the_limit(lib):
     assert bwd(vocab=2 ** 63 - 1) == _lib.E_UNSUPPORTED
 
 
+def test_gemm_nt_and_grad_check_their_arguments(lib):
+    g = lib.bil_linear_gemm_nt
+    ok = dict(a=FAKE, b=FAKE, dt=_lib.BF16, m=4, n=8, k=64, lda=64, ldb=64, c=FAKE, ct=_lib.F32, ldc=8)
+
+    def gemm(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return g(a["a"], a["b"], a["dt"], a["m"], a["n"], a["k"], a["lda"], a["ldb"], a["c"], a["ct"], a["ldc"], NULL)
+    assert gemm(dt=_lib.F32) == _lib.E_DTYPE                     # 16-bit operands only
+    assert gemm(ct=_lib.F16) == _lib.E_DTYPE                     # C: float32 or the operands' type
+    assert gemm(k=0) == _lib.E_INVALID_ARG
+    assert gemm(lda=63) == _lib.E_INVALID_ARG
+    assert gemm(ldb=63) == _lib.E_INVALID_ARG
+    assert gemm(ldc=7) == _lib.E_INVALID_ARG
+    assert gemm(m=-1) == _lib.E_INVALID_ARG
+    assert gemm(m=0, a=NULL, c=NULL) == _lib.OK                  # nothing to compute
+    assert gemm(a=NULL) == _lib.E_INVALID_ARG
+    assert gemm(a=ctypes.c_void_p(0x10008)) == _lib.E_ALIGN      # TMA: 16-byte base
+    assert gemm(k=60, lda=60, ldb=64) == _lib.E_ALIGN            # TMA: 16-byte row stride
+    assert gemm(ct=_lib.BF16, ldc=12) == _lib.E_ALIGN            # 16-byte rows of C
+    assert gemm(m=2 ** 20, lda=2 ** 28) == _lib.E_UNSUPPORTED     # A: 2^49 bytes
+
+    def grad(**kw):
+        a = dict(dt=_lib.BF16, n=4, vocab=1000, te=4, ld_dz=1000, ld_dzt=8, dz=FAKE, temp=1.0)
+        a.update(kw)
+        return lib.bil_linear_logp_grad(FAKE, FAKE, a["dt"], a["n"], 64, 64, a["vocab"], 64, 0, a["te"], a["temp"],
+                                        FAKE, -100, FAKE, FAKE, NULL, NULL, a["dz"], a["ld_dz"], FAKE, a["ld_dzt"],
+                                        NULL)
+    assert grad(dt=_lib.F32) == _lib.E_DTYPE
+    assert grad(te=5) == _lib.E_INVALID_ARG
+    assert grad(ld_dz=999) == _lib.E_INVALID_ARG
+    assert grad(ld_dzt=3) == _lib.E_INVALID_ARG
+    assert grad(dz=NULL) == _lib.E_INVALID_ARG
+    assert grad(temp=0.0) == _lib.E_INVALID_ARG
+    assert grad(n=0, dz=NULL) == _lib.OK
+    assert grad(n=2 ** 20, ld_dz=2 ** 28, ld_dzt=2 ** 20) == _lib.E_UNSUPPORTED
+
+
 def test_sum_transpose_and_stream_shape_check_their_arguments(lib):
     srcs = (ctypes.c_void_p * 17)(*([0x10000] * 17))
     s = lib.bil_sum_f32

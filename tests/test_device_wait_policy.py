@@ -69,3 +69,19 @@ def test_kernels_wait_only_through_bounded_paths():
             continue
         text = "\n".join(_code(path))
         assert "mbarrier.try_wait" not in text and "mbarrier.test_wait" not in text, path
+
+
+def test_every_sleeping_spin_is_bounded():
+    """Every loop that sleeps between polls of memory another thread or block
+    writes (the store GEMMs' lockstep) tests a time limit in its body."""
+    sleeps = 0
+    for path in SOURCES:
+        lines = _code(path)
+        for i, line in enumerate(lines):
+            if "__nanosleep(" not in line or re.search(r"__device__", line):
+                continue
+            sleeps += 1
+            start = max(j for j in range(i + 1) if re.search(r"\b__(device|global)__\b", lines[j]))
+            body = "\n".join(lines[start:i + 1])  # the enclosing function up to the sleep
+            assert "kSyncWaitNs" in body or "kWaitLimitNs" in body, f"{path}:{i + 1}: a sleeping spin without a limit"
+    assert sleeps >= 2

@@ -1,0 +1,106 @@
+"""The fused LM-head backward's steps as separate calls, and its store GEMM.
+
+bil_linear_logp_bwd is a transpose of the hidden states, the gradient pass
+(dZ from the recomputed projection) and two store GEMMs C = A . B^T.  Queued
+one by one through bil_transpose_2d, bil_linear_logp_grad and
+bil_linear_gemm_nt they must give the same bits; the store GEMM alone must
+match the oracle's float64 product; and store GEMMs running at once on two
+streams (whose copy threads keep in step through one shared position table)
+must give the bits they give one at a time.
+
+"[RFC][ROCm] End-to-end optimization of bitwise VIME R/R beyond native P/P",
+section "Workstream 3" (the autograd actor path: fixed-order contractions).
+"""
+import numpy as np
+import pytest
+import torch
+
+import invariant_token_log_gb300 as bil
+import oracle
+import workloads as wl
+from gpu_helpers import check_watchdog, device_logits, f32_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _watchdog():
+    yield
+    check_watchdog()
+
+
+def _dev(stored, dtype):
+    return device_logits(stored, dtype)
+
+
+@pytest.mark.parametrize("dtype,temp,entropy", [("bfloat16", 1.0, False), ("float16", 0.7, True)])
+def test_backward_steps_one_by_one_give_the_backwards_bits(dtype, temp, entropy):
+    n, h, v = 300, 256, 1000
+    x = wl.linear_hidden(n, h, seed=41, dtype=dtype)
+    w = wl.linear_weight(v, h, seed=41, dtype=dtype)
+    t = wl.rng(41, 1, n, v).integers(0, v, n, dtype=np.int64)
+    t[::6] = wl.IGNORE_INDEX
+    xd, wd, td = _dev(x, dtype), _dev(w, dtype), torch.from_numpy(t).cuda()
+    res = bil.linear_logp(xd, wd, td, temperature=temp, return_entropy=entropy)
+    lse = res[1]
+    ent = res[2] if entropy else None
+    g = torch.from_numpy(wl.rng(41, 2).standard_normal(n).astype(np.float32)).cuda()
+    gh = torch.from_numpy(wl.rng(41, 3).standard_normal(n).astype(np.float32)).cuda() if entropy else None
+    dh, dw, dz = bil.linear_logp_bwd(xd, wd, td, lse, g, temperature=temp, entropy=ent, grad_entropy=gh,
+                                     out_dtype=torch.float32, return_dz=True)
+    dz2, dz_t2 = bil.linear_logp_grad(xd, wd, td, lse, g, temperature=temp, entropy=ent, grad_entropy=gh)
+    w_t = bil.linear.transpose(wd)
+    x_t = bil.linear.transpose(xd)
+    dh2 = bil.gemm_nt(dz2, w_t)
+    dw2 = bil.gemm_nt(dz_t2, x_t)
+    torch.cuda.synchronize()
+    assert torch.equal(dz.contiguous().view(torch.int16), dz2.contiguous().view(torch.int16))
+    assert torch.equal(dz_t2.t().contiguous().view(torch.int16), dz2.contiguous().view(torch.int16))
+    assert np.array_equal(f32_bits(dh), f32_bits(dh2))
+    assert np.array_equal(f32_bits(dw), f32_bits(dw2))
+
+
+@pytest.mark.parametrize("m,n,k,dtype", [(333, 520, 1000, "bfloat16"), (128, 256, 64, "float16"),
+                                         (1, 8, 8, "bfloat16")])
+def test_gemm_nt_against_the_oracle(m, n, k, dtype):
+    """C = A . B^T against the oracle's float64 product of the same stored
+    elements: |dC| <= 2^-20 * sum_k |a b| + 1e-6 (products of two 16-bit values
+    are exact in float32; only the accumulation rounds), and a 16-bit C is the
+    float32 value rounded (2^-8 or 2^-11 relative more)."""
+    a = wl.linear_hidden(m, k, seed=43, dtype=dtype)
+    b = wl.linear_weight(n, k, seed=44, dtype=dtype)
+    ref = oracle.linear_logits(a, b, dtype)
+    bound = (np.abs(oracle.widen(a, dtype)) @ np.abs(oracle.widen(b, dtype)).T) * 2.0 ** -20 + 1e-6
+    ad, bd = _dev(a, dtype), _dev(b, dtype)
+    c = bil.gemm_nt(ad, bd)
+    c16 = bil.gemm_nt(ad, bd, out_dtype=ad.dtype)
+    torch.cuda.synchronize()
+    err = np.abs(c.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), float((err / bound).max())
+    u = 2.0 ** -8 if dtype == "bfloat16" else 2.0 ** -11
+    err16 = np.abs(c16.float().cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err16 <= bound * (1 + u) + u * np.abs(ref) + 2.0 ** -24), float((err16 / (bound + u * np.abs(ref))).max())
+
+
+def test_store_gemms_at_once_on_two_streams_keep_their_bits():
+    """Two store GEMMs of several waves each (512 work units for 152 SMs) run at
+    the same time on two streams; each must give the bits it gives alone."""
+    m, n, k = 4096, 4096, 4096
+    a1 = _dev(wl.linear_hidden(m, k, seed=45), "bfloat16")
+    b1 = _dev(wl.linear_weight(n, k, seed=46), "bfloat16")
+    a2 = _dev(wl.linear_hidden(m, k, seed=47), "bfloat16")
+    b2 = _dev(wl.linear_weight(n, k, seed=48), "bfloat16")
+    ref1, ref2 = bil.gemm_nt(a1, b1), bil.gemm_nt(a2, b2)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            c1 = bil.gemm_nt(a1, b1)
+        with torch.cuda.stream(s2):
+            c2 = bil.gemm_nt(a2, b2)
+        outs.append((c1, c2))
+    torch.cuda.synchronize()
+    for c1, c2 in outs:
+        assert np.array_equal(f32_bits(c1), f32_bits(ref1))
+        assert np.array_equal(f32_bits(c2), f32_bits(ref2))
