@@ -418,15 +418,16 @@ int device_limits(int* sms, int* max_smem_optin) {
 extern "C" {
 
 const char* bil_contract_id(void) {
-  return "bil.v3"
+  return "bil.v4"
          ";tile=fixed tile_v columns, valid columns < vocab"
          ";rcp=float32(1/temperature) (rcp=1: no multiply)"
          ";lanes=32x8: lane l takes 8-element groups l, l+32, ... in order"
          ";max=exact, on x: m_x; m_t=m_x*rn rcp"
-         ";exp(d)=ex2.approx.ftz.f32(d*rn log2e), d=(x-rn m_x)*rn rcp"
+         ";tile_term=e=ex2.approx.ftz.f32(t), t=(x-rn m_x)*rn c, c=rcp*rn log2e"
+         ";exp(a)=ex2.approx.ftz.f32(a*rn log2e) (merge, backward)"
          ";lane_sum=8 slot accumulators, ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))"
          ";warp_sum=butterfly xor 16,8,4,2,1"
-         ";entropy_sum=u_j=fma(e,max(d,-FLT_MAX),u_j), same trees"
+         ";entropy_sum=u_j=fma(e,max(t,-FLT_MAX),u_j), same trees; u_t=sum*rn ln2"
          ";merge=M=max m_t; w_t=exp(m_t-M); S=fma(s_t,w_t,S) t=0..T-1; LSE=M+rn logf(S)"
          ";merge_entropy=U=fma(fma(max(m_t-M,-FLT_MAX),s_t,u_t),w_t,U); H=logf(S)-rn(U/rn S)"
          ";logp=z_t-rn LSE, z_t=x_t*rn rcp"

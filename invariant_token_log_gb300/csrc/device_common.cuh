@@ -12,6 +12,7 @@ constexpr int kLanes = 32;
 
 // log2(e) rounded to float32: exp(a) is evaluated as 2^(a * log2(e)).
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.693147180559945309f;  // ln 2 rounded to float32: the tile entropy sum's unit
 // The most negative finite float32.
 constexpr float kNegMax = -3.40282346638528859811704183484516925e38f;
 

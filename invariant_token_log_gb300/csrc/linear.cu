@@ -233,12 +233,13 @@ __device__ __forceinline__ void unit_coords(int64_t u, int num_m, int num_n, int
 // the tile's valid columns [0, vcols), from the float32 accumulator acc.
 //
 //   m_acc = max over valid c of acc_c (exact);  m = m_acc *rn rcp
-//   d_c = (acc_c -rn m_acc) *rn rcp (m_acc = -inf: shift 0), e_c = exp(d_c)
-//   of the contract; the target logit is acc_t *rn rcp
+//   t_c = (acc_c -rn m_acc) *rn c, c = rcp *rn log2e (m_acc = -inf: shift 0),
+//   e_c = 2^t_c (ex2.approx), as the logits path's tile terms; the target
+//   logit is acc_t *rn rcp
 //   slot accumulators a_j, j = 0..7, take e_c for c = 8g + j, g = 0, 1, ...,
 //   31 in order; s = ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)); the entropy sum
-//   u = sum e_c * max(d_c, -FLT_MAX) in the same slots and tree (one fma per
-//   column).
+//   u = ln2 *rn (sum e_c * max(t_c, -FLT_MAX) in the same slots and tree, one
+//   fma per column).
 //
 // This is one lane of the logits path's in-tile order with 32 groups and no
 // warp butterfly: a tile here is one thread's row.
@@ -294,6 +295,7 @@ __device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp
   }
   const float m = __fmul_rn(mx, rcp);
   const float shift = (mx == -INFINITY) ? 0.0f : mx;
+  const float c = __fmul_rn(rcp, kLog2e);  // rcp = 1: log2e
   float a[8], u[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -305,18 +307,19 @@ __device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp
     tmem_ld32(taddr + c0, r);
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
-      const float d = __fmul_rn(__fsub_rn(__uint_as_float(r[j]), shift), rcp);
-      float e = contract_exp(d);
+      const float t = __fmul_rn(__fsub_rn(__uint_as_float(r[j]), shift), c);
+      float e = ex2_approx(t);
       if (c0 + j >= vcols) e = 0.0f;  // columns past the vocabulary add nothing
       a[j % 8] = __fadd_rn(a[j % 8], e);
-      if (ENT) u[j % 8] = __fmaf_rn(e, fmaxf(d, kNegMax), u[j % 8]);
+      if (ENT) u[j % 8] = __fmaf_rn(e, fmaxf(t, kNegMax), u[j % 8]);
     }
   }
   s_out = __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
                     __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
   if (ENT)
-    u_out = __fadd_rn(__fadd_rn(__fadd_rn(u[0], u[1]), __fadd_rn(u[2], u[3])),
-                      __fadd_rn(__fadd_rn(u[4], u[5]), __fadd_rn(u[6], u[7])));
+    u_out = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(u[0], u[1]), __fadd_rn(u[2], u[3])),
+                                __fadd_rn(__fadd_rn(u[4], u[5]), __fadd_rn(u[6], u[7]))),
+                      kLn2);
   m_out = m;
   tl_out = tl;
 }

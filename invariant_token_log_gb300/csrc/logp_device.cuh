@@ -221,24 +221,28 @@ struct Group {
       return pk(lo, hi);
     }
   }
-  // a[k] holds the slot accumulators (a_2k, a_2k+1) of exp(d); with ENT,
-  // u[k] those of exp(d) * d; d = x - shift, times rcp when SCALED (the
-  // multiply comes last: no packed multiply here ever feeds an add, so the
-  // code generator has nothing to contract into a fused multiply-add)
-  template <bool SCALED, bool ENT>
+  // a[k] holds the slot accumulators (a_2k, a_2k+1) of e = 2^t for the tile
+  // term t = (x - shift) * c, c = rcp * log2e rounded once (rcp = 1: c =
+  // log2e, so t is the exponent exp(x - shift) of the contract takes); with
+  // ENT, u[k] those of e * t.  The multiply comes last: no packed multiply
+  // here ever feeds an add, so the code generator has nothing to contract
+  // into a fused multiply-add.
+  //
+  // p log p -> 0 as p -> 0: an element with z = -inf (or one masked past the
+  // vocabulary, or whose t overflows) has e = 0 and t = -inf, and its entropy
+  // term must be 0, not 0 * inf.  CLAMP takes max(t, -FLT_MAX) for the term,
+  // which leaves every finite t as it is; without CLAMP such an element makes
+  // the sum NaN, and the caller then sums the entropy terms again with it (a
+  // NaN logit makes the sum NaN either way).  The bits are the same.
+  template <bool ENT, bool CLAMP>
   __device__ static __forceinline__ void sum_acc(uint64_t (&a)[4], uint64_t (&u)[4], const uint32_t (&w)[kW],
-                                                 uint64_t shift2, uint64_t rcp2) {
+                                                 uint64_t shift2, uint64_t c2) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      uint64_t d = sub2(xpair(w, k), shift2);
-      if (SCALED) d = mul2(d, rcp2);
-      const uint64_t e = exp2_pair(d);
+      const uint64_t t = mul2(sub2(xpair(w, k), shift2), c2);
+      const uint64_t e = pk(ex2_approx(lo_of(t)), ex2_approx(hi_of(t)));
       a[k] = add2(a[k], e);
-      // p log p -> 0 as p -> 0: an element with z = -inf (or one masked past
-      // the vocabulary) has e = 0 and d = -inf; clamping d to the largest
-      // finite magnitude makes its term 0 instead of 0 * inf.  Finite d are
-      // left as they are.
-      if (ENT) u[k] = fma2(e, pk(fmaxf(lo_of(d), kNegMax), fmaxf(hi_of(d), kNegMax)), u[k]);
+      if (ENT) u[k] = fma2(e, CLAMP ? pk(fmaxf(lo_of(t), kNegMax), fmaxf(hi_of(t), kNegMax)) : t, u[k]);
     }
   }
 };
@@ -260,12 +264,13 @@ __device__ __forceinline__ int lane_groups(int valid, int lane) {
 //     on the stored values, m_x, and the partial's max is m = m_x * rcp
 //     (the max of the scaled values, since x -> x * rcp (rcp > 0) rounds
 //     monotonically);
-//   * sums: d = (x - m_x) * rcp, each operation rounded (rcp = 1: d = x - m_x),
-//     which is z - m in real arithmetic; lane accumulator a_j (slot j) adds
-//     exp(d) for its groups in increasing order; the lane's sum is
-//     ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)); the warp's sum is the butterfly
-//     over lanes (xor 16, 8, 4, 2, 1); the entropy sum u follows the same
-//     tree with u_j = fma(exp(d), d, u_j);
+//   * sums: t = (x - m_x) * c with c = rcp * log2e, each operation rounded
+//     (t = (z - m) log2 e in real arithmetic); lane accumulator a_j (slot j)
+//     adds e = 2^t (ex2.approx) for its groups in increasing order; the
+//     lane's sum is ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)); the warp's sum is
+//     the butterfly over lanes (xor 16, 8, 4, 2, 1); the entropy sum follows
+//     the same tree with u_j = fma(e, t, u_j), and u is that sum times ln 2
+//     (rounded once), i.e. sum e (z - m) in real arithmetic;
 //   * a tile whose max is -inf shifts by 0 instead, so it sums to 0 (or NaN
 //     if it holds a NaN) and its max stays -inf.
 // Nothing here depends on the row, the kernel or the launch geometry.  Two
@@ -286,7 +291,7 @@ __device__ __forceinline__ TilePartial finish_tile(float m, const uint64_t (&a)[
   TilePartial r;
   r.m = m;
   r.s = warp_sum(tree8(a));
-  r.u = ENT ? warp_sum(tree8(u)) : 0.0f;
+  r.u = ENT ? __fmul_rn(warp_sum(tree8(u)), kLn2) : 0.0f;
   return r;
 }
 
@@ -341,7 +346,7 @@ __device__ __forceinline__ void tile_load_regs_t(const unsigned char* tile, int 
   }
 }
 
-template <int DT, bool FULL, bool SCALED, bool ENT>
+template <int DT, bool FULL, bool ENT, bool CLAMP>
 __device__ __forceinline__ TilePartial tile_reduce_regs_t(const TileRegs<DT>& r, int valid, int lane, float rcp) {
   const int ng = FULL ? TileRegs<DT>::kMaxGroups : lane_groups(valid, lane);
   uint32_t mx[Group<DT>::kW];
@@ -350,13 +355,14 @@ __device__ __forceinline__ TilePartial tile_reduce_regs_t(const TileRegs<DT>& r,
   for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i)
     if (FULL || i < ng) Group<DT>::max_acc(mx, r.w[i]);
   const float mx_all = warp_max(Group<DT>::max_fin(mx));
-  const float m = SCALED ? __fmul_rn(mx_all, rcp) : mx_all;
+  const float m = rcp == 1.0f ? mx_all : __fmul_rn(mx_all, rcp);
   const float shift = (mx_all == -INFINITY) ? 0.0f : mx_all;  // in stored units
-  const uint64_t shift2 = pk(shift, shift), rcp2 = pk(rcp, rcp);
+  const float c = __fmul_rn(rcp, kLog2e);                     // rcp = 1: log2e exactly
+  const uint64_t shift2 = pk(shift, shift), c2 = pk(c, c);
   uint64_t a[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int i = 0; i < TileRegs<DT>::kMaxGroups; ++i)
-    if (FULL || i < ng) Group<DT>::template sum_acc<SCALED, ENT>(a, u, r.w[i], shift2, rcp2);
+    if (FULL || i < ng) Group<DT>::template sum_acc<ENT, CLAMP>(a, u, r.w[i], shift2, c2);
   return finish_tile<ENT>(m, a, u);
 }
 
@@ -386,18 +392,17 @@ __device__ __forceinline__ void tile_load_regs(const unsigned char* tile, int va
   }
 }
 
-template <int DT, bool ENT>
+// CLAMP: as for Group::sum_acc.  With ENT and CLAMP = false the entropy sum
+// comes out NaN when the tile holds an element whose term needs the clamp;
+// the caller then reloads the tile and takes its u from a CLAMP = true pass
+// (same m and s; the same u bits a clamped pass gives in one go).
+template <int DT, bool ENT, bool CLAMP = !ENT>
 __device__ __forceinline__ TilePartial tile_reduce_regs(const TileRegs<DT>& r, int valid, int lane, float rcp) {
-  const bool full = valid == TileRegs<DT>::kMaxTile;
-  if (rcp == 1.0f) {
-    return full ? tile_reduce_regs_t<DT, true, false, ENT>(r, valid, lane, rcp)
-                : tile_reduce_regs_t<DT, false, false, ENT>(r, valid, lane, rcp);
-  }
-  return full ? tile_reduce_regs_t<DT, true, true, ENT>(r, valid, lane, rcp)
-              : tile_reduce_regs_t<DT, false, true, ENT>(r, valid, lane, rcp);
+  return valid == TileRegs<DT>::kMaxTile ? tile_reduce_regs_t<DT, true, ENT, CLAMP>(r, valid, lane, rcp)
+                                         : tile_reduce_regs_t<DT, false, ENT, CLAMP>(r, valid, lane, rcp);
 }
 
-template <int DT, bool SCALED, bool ENT, int WOFF>
+template <int DT, bool ENT, int WOFF>
 __device__ __forceinline__ TilePartial tile_reduce_smem_t(const unsigned char* tile, int valid, int lane, float rcp,
                                                           unsigned sh) {
   const int groups = (valid + kGroup - 1) / kGroup;
@@ -411,24 +416,29 @@ __device__ __forceinline__ TilePartial tile_reduce_smem_t(const unsigned char* t
     Group<DT>::max_acc(mx, w);
   }
   const float mx_all = warp_max(Group<DT>::max_fin(mx));
-  const float m = SCALED ? __fmul_rn(mx_all, rcp) : mx_all;
+  const float m = rcp == 1.0f ? mx_all : __fmul_rn(mx_all, rcp);
   const float shift = (mx_all == -INFINITY) ? 0.0f : mx_all;  // in stored units
-  const uint64_t shift2 = pk(shift, shift), rcp2 = pk(rcp, rcp);
+  const float c = __fmul_rn(rcp, kLog2e);                     // rcp = 1: log2e exactly
+  const uint64_t shift2 = pk(shift, shift), c2 = pk(c, c);
   uint64_t a[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
   for (int g = lane; g < groups; g += kLanes) {
     uint32_t w[Group<DT>::kW];
     load_group<DT, WOFF>(tile, g, sh, w);
     if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
-    Group<DT>::template sum_acc<SCALED, ENT>(a, u, w, shift2, rcp2);
+    Group<DT>::template sum_acc<ENT, false>(a, u, w, shift2, c2);
   }
-  return finish_tile<ENT>(m, a, u);
-}
-
-template <int DT, bool ENT, int WOFF>
-__device__ __forceinline__ TilePartial tile_reduce_smem_w(const unsigned char* tile, int valid, int lane, float rcp,
-                                                          unsigned sh) {
-  return rcp == 1.0f ? tile_reduce_smem_t<DT, false, ENT, WOFF>(tile, valid, lane, rcp, sh)
-                     : tile_reduce_smem_t<DT, true, ENT, WOFF>(tile, valid, lane, rcp, sh);
+  TilePartial tp = finish_tile<ENT>(m, a, u);
+  if (ENT && tp.u != tp.u) {  // NaN (warp-uniform): the entropy terms again, with the clamp
+    uint64_t a2[4] = {0, 0, 0, 0}, u2[4] = {0, 0, 0, 0};
+    for (int g = lane; g < groups; g += kLanes) {
+      uint32_t w[Group<DT>::kW];
+      load_group<DT, WOFF>(tile, g, sh, w);
+      if (rem != 0 && g == groups - 1) Group<DT>::mask_tail(w, rem);
+      Group<DT>::template sum_acc<ENT, true>(a2, u2, w, shift2, c2);
+    }
+    tp.u = finish_tile<ENT>(m, a2, u2).u;
+  }
+  return tp;
 }
 
 // off, SHIFTED: as for tile_load_regs.
@@ -436,12 +446,12 @@ template <int DT, bool ENT, bool SHIFTED = false>
 __device__ __forceinline__ TilePartial tile_reduce_smem(const unsigned char* tile, int valid, int lane, float rcp,
                                                         unsigned off = 0) {
   const unsigned sh = 8u * (off & 3u);
-  if (!SHIFTED || off == 0) return tile_reduce_smem_w<DT, ENT, -1>(tile, valid, lane, rcp, 0);
+  if (!SHIFTED || off == 0) return tile_reduce_smem_t<DT, ENT, -1>(tile, valid, lane, rcp, 0);
   switch (off >> 2) {
-    case 0: return tile_reduce_smem_w<DT, ENT, 0>(tile, valid, lane, rcp, sh);
-    case 1: return tile_reduce_smem_w<DT, ENT, 1>(tile, valid, lane, rcp, sh);
-    case 2: return tile_reduce_smem_w<DT, ENT, 2>(tile, valid, lane, rcp, sh);
-    default: return tile_reduce_smem_w<DT, ENT, 3>(tile, valid, lane, rcp, sh);
+    case 0: return tile_reduce_smem_t<DT, ENT, 0>(tile, valid, lane, rcp, sh);
+    case 1: return tile_reduce_smem_t<DT, ENT, 1>(tile, valid, lane, rcp, sh);
+    case 2: return tile_reduce_smem_t<DT, ENT, 2>(tile, valid, lane, rcp, sh);
+    default: return tile_reduce_smem_t<DT, ENT, 3>(tile, valid, lane, rcp, sh);
   }
 }
 
@@ -940,7 +950,19 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_kernel(const StreamP
       tile_load_regs<DT, !ALIGNED>(tile, valid, lane, regs, off);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[stage]);
-      tp = tile_reduce_regs<DT, ENT>(regs, valid, lane, p.rcp);
+      tp = tile_reduce_regs<DT, ENT, false>(regs, valid, lane, p.rcp);
+      if (ENT && tp.u != tp.u) {
+        // The entropy terms need the clamp (a -inf logit or a masked column)
+        // or a logit is NaN: take u from a clamped pass over the tile, read
+        // again from global memory (the stage has been handed back).
+        const unsigned char* g = p.logits + d.row * p.ld * EB + static_cast<int64_t>(d.tile - p.tile_begin) * p.tile_v * EB;
+        if (ALIGNED) {
+          tile_load_regs<DT>(g, valid, lane, regs);
+        } else {
+          tile_load_regs<DT, true, true>(g - off, valid, lane, regs, off);
+        }
+        tp.u = tile_reduce_regs<DT, ENT, true>(regs, valid, lane, p.rcp).u;
+      }
     } else {
       tp = tile_reduce_smem<DT, ENT, !ALIGNED>(tile, valid, lane, p.rcp, off);
       __syncwarp();
@@ -1068,7 +1090,16 @@ __global__ void __launch_bounds__(kSplitWarps * kLanes) split_row_kernel(const S
         const unsigned off = static_cast<unsigned>(reinterpret_cast<uintptr_t>(tile) & 15u);
         tile_load_regs<DT, true, true>(tile - off, valid, lane, regs, off);
       }
-      const TilePartial tp = tile_reduce_regs<DT, ENT>(regs, valid, lane, p.rcp);
+      TilePartial tp = tile_reduce_regs<DT, ENT, false>(regs, valid, lane, p.rcp);
+      if (ENT && tp.u != tp.u) {  // as in stream_kernel: u from a clamped pass
+        if (ALIGNED) {
+          tile_load_regs<DT>(tile, valid, lane, regs);
+        } else {
+          const unsigned off = static_cast<unsigned>(reinterpret_cast<uintptr_t>(tile) & 15u);
+          tile_load_regs<DT, true, true>(tile - off, valid, lane, regs, off);
+        }
+        tp.u = tile_reduce_regs<DT, ENT, true>(regs, valid, lane, p.rcp).u;
+      }
       if (lane == 0) {
         st_cluster(cluster_addr(&sm_m[t], 0), tp.m);
         st_cluster(cluster_addr(&sm_s[t], 0), tp.s);

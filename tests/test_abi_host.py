@@ -55,7 +55,7 @@ def test_header_constants_match_binding():
 
 def test_contract_id_and_status_strings(lib):
     cid = _lib.contract_id()
-    assert cid.startswith("bil.v3") and "ex2.approx" in cid and "fma" in cid and "entropy" in cid
+    assert cid.startswith("bil.v4") and "ex2.approx" in cid and "fma" in cid and "entropy" in cid
     for s in range(7):
         assert _lib.status_string(s) != "unknown status"
     assert _lib.status_string(99) == "unknown status"
