@@ -81,7 +81,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["training", "linear"], default="training")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the secondary measurements (entropy with a temperature, decode latency)")
+                    help="skip the secondary measurements (entropy with a temperature, decode latency, prefill, "
+                         "the exponential unit, the fused LM-head step)")
     return ap.parse_args()
 
 
@@ -458,7 +459,93 @@ def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_byte
     variants["decode_fwd_us_per_call_python"] = eager
     variants["prefill_fwd"] = prefill_measurement(bil, stream, dev)
     variants["sfu_exp"] = exp_rate_probe(dev, torch.cuda.get_device_properties(dev).multi_processor_count)
+    variants["linear"] = linear_measurement(bil, stream, dev)
     return variants
+
+
+def linear_measurement(bil, stream, dev, steps: int = 5):
+    """The fused LM-head + logp step at full size: hidden [16384, 4096] bf16 times a
+    Qwen3-8B-shaped LM head [151936, 4096] bf16 (the `--workload linear` batch).
+    Forward: tile partials from the tensor-core accumulator, then the merge.
+    Backward, queued step by step through the public calls it is made of: the
+    hidden states transposed, dZ from the recomputed projection, dhidden = dZ . W
+    and dweight = dZ^T . X.  Each step is timed with CUDA events on the
+    launching stream, `steps` steps after 2 warm-up steps, clocks sampled
+    meanwhile.  Outside the timed region of the headline value."""
+    import torch
+
+    import workloads as wl
+
+    lw = wl.linear(16384)
+    n, h, v = lw.n_rows, lw.hidden_size, lw.vocab
+    x = torch.from_numpy(lw.hidden.view(np.int16)).view(torch.bfloat16).to(dev)
+    wt = torch.from_numpy(lw.weight.view(np.int16)).view(torch.bfloat16).to(dev)
+    t = torch.from_numpy(lw.target_ids).to(dev)
+    g = torch.from_numpy(lw.grad_logp).to(dev)
+    nt = -(-v // bil.LINEAR_TILE_V)
+    pm = torch.empty((n, nt), dtype=torch.float32, device=dev)
+    ps = torch.empty((n, nt), dtype=torch.float32, device=dev)
+    tl = torch.empty(n, dtype=torch.float32, device=dev)
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    w_t = bil.linear.prepared_weight_t(wt)
+
+    def parts():
+        bil.linear_logp_partials(x, wt, t, v, 0, nt, pm, ps, tl)
+
+    def merge():
+        bil.logp_merge(pm, ps, nt, tl, t, v, out=logp, lse=lse)
+    state = {}
+
+    def transpose():
+        state["x_t"] = bil.linear.transpose(x)
+
+    def grad():
+        state["dz"], state["dz_t"] = bil.linear_logp_grad(x, wt, t, lse, g)
+
+    def dhidden():
+        state["dh"] = bil.gemm_nt(state["dz"], w_t, out_dtype=torch.bfloat16)
+
+    def dweight():
+        state["dw"] = bil.gemm_nt(state["dz_t"], state["x_t"], out_dtype=torch.bfloat16)
+    seq = [("partials", parts), ("merge", merge), ("transpose", transpose), ("grad", grad), ("dhidden", dhidden),
+           ("dweight", dweight)]
+    for _ in range(2):
+        for _, f in seq:
+            f()
+    torch.cuda.synchronize(dev)
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    sampler.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(seq) + 1)] for _ in range(steps)]
+    host_t0 = time.time()
+    for i in range(steps):
+        ev[i][0].record(stream)
+        for j, (_, f) in enumerate(seq):
+            f()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    host_t1 = time.time()
+    sampler.stop()
+    ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, (name, _) in enumerate(seq)}
+    step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in ev)
+    flops = 2.0 * n * h * v
+    _, sustained, kind = tensor_peak()
+    bwd_ms = ms["transpose"] + ms["grad"] + ms["dhidden"] + ms["dweight"]
+    out = {"workload": LINEAR_WORKLOAD, "steps": steps, "step_ms": step_ms, "rows_per_s": n / (step_ms / 1e3),
+           "tflops": 4 * flops / (step_ms / 1e3) / 1e12, "fwd_ms": ms["partials"] + ms["merge"],
+           "fwd_tflops": flops / (ms["partials"] / 1e3) / 1e12, "bwd_ms": bwd_ms,
+           "bwd_tflops": 3 * flops / (bwd_ms / 1e3) / 1e12, "peak_sustained_tflops": sustained,
+           "peak_source": f"{kind} cuBLAS bf16, sustained", "clocks": sampler.summary(host_t0, host_t1)}
+    out["bwd_frac_of_sustained"] = out["bwd_tflops"] / sustained
+    out["fwd_frac_of_sustained"] = out["fwd_tflops"] / sustained
+    for name in ("grad", "dhidden", "dweight"):
+        out[f"{name}_ms"] = ms[name]
+        out[f"{name}_tflops"] = flops / (ms[name] / 1e3) / 1e12
+    out["transpose_ms"] = ms["transpose"]
+    out["merge_ms"] = ms["merge"]
+    del state, pm, ps, x, wt, w_t
+    return out
 
 
 def prefill_measurement(bil, stream, dev):
