@@ -80,6 +80,10 @@ def parse():
                     help="rows of the workload per GPU (smaller only for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["training", "linear"], default="training")
+    ap.add_argument("--entropy", action="store_true",
+                    help="training step with the entropy output and its gradient (for profiling; not the headline)")
+    ap.add_argument("--temperature", type=float, default=1.0,
+                    help="training step at this temperature (for profiling; not the headline)")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the secondary measurements (entropy with a temperature, decode latency, prefill, "
                          "the exponential unit, the fused LM-head step)")
@@ -426,19 +430,21 @@ def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_byte
     # decode-sized batches: device time per forward call on the first N rows,
     # from a CUDA graph of 20 calls (so the host's per-call cost does not count),
     # and the same 20 calls issued one by one from Python (host-bound)
-    lat, eager = {}, {}
+    lat, eager, eager_pre = {}, {}, {}
     for nd in (1, 2, 3, 7, 64, 128, 256):
         xs, ts = x[:nd], t[:nd]
+        os_, ls_ = logp[:nd], lse[:nd]
         for _ in range(5):
             bil.logp_fwd(xs, ts, w.ignore_index, w.tile_v)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(20):
-            bil.logp_fwd(xs, ts, w.ignore_index, w.tile_v)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        eager[str(nd)] = round(e0.elapsed_time(e1) / 20 * 1e3, 2)
+        for res, kw in ((eager, {}), (eager_pre, {"out": os_, "lse": ls_})):
+            e0.record(stream)
+            for _ in range(20):
+                bil.logp_fwd(xs, ts, w.ignore_index, w.tile_v, **kw)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            res[str(nd)] = round(e0.elapsed_time(e1) / 20 * 1e3, 2)
         try:
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, capture_error_mode="thread_local"):
@@ -457,6 +463,7 @@ def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_byte
             lat[str(nd)] = f"unavailable: {str(exc).splitlines()[0][:80]}"
     variants["decode_fwd_us_per_call_graph"] = lat
     variants["decode_fwd_us_per_call_python"] = eager
+    variants["decode_fwd_us_per_call_python_preallocated"] = eager_pre
     variants["prefill_fwd"] = prefill_measurement(bil, stream, dev)
     variants["sfu_exp"] = exp_rate_probe(dev, torch.cuda.get_device_properties(dev).multi_processor_count)
     variants["linear"] = linear_measurement(bil, stream, dev)
@@ -617,9 +624,22 @@ def run_bil(args):
     d = torch.empty(n, v, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # --entropy / --temperature: the same step with the entropy output (and its
+    # gradient) and a temperature, for profiling those kernels; not the headline
+    ent = torch.empty(n, dtype=torch.float32, device=dev) if args.entropy else None
+    gh = torch.from_numpy(np.random.default_rng(7).standard_normal(n).astype(np.float32)).to(dev) \
+        if args.entropy else None
+    temp = args.temperature
+
+    def fwd():
+        bil.logp_fwd(x, t, w.ignore_index, w.tile_v, out=logp, lse=lse, temperature=temp, entropy=ent)
+
+    def bwd():
+        bil.logp_bwd(x, t, lse, g, w.ignore_index, out=d, temperature=temp, entropy=ent, grad_entropy=gh)
+
     def step():
-        bil.logp_fwd(x, t, w.ignore_index, w.tile_v, out=logp, lse=lse)
-        bil.logp_bwd(x, t, lse, g, w.ignore_index, out=d)
+        fwd()
+        bwd()
 
     props = torch.cuda.get_device_properties(dev)
     sampler = ClockSampler(str(getattr(props, "uuid", "")))
@@ -636,9 +656,9 @@ def run_bil(args):
     host_t0 = time.time()
     for i in range(K):
         ev[i][0].record(stream)
-        bil.logp_fwd(x, t, w.ignore_index, w.tile_v, out=logp, lse=lse)
+        fwd()
         ev[i][1].record(stream)
-        bil.logp_bwd(x, t, lse, g, w.ignore_index, out=d)
+        bwd()
         ev[i][2].record(stream)
     torch.cuda.synchronize(dev)
     host_t1 = time.time()
@@ -724,7 +744,8 @@ def run_bil(args):
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, host-generated)",
-            "config": training_config(n, world),
+            "config": dict(training_config(n, world), **({"entropy": True} if args.entropy else {}),
+                           **({"temperature": args.temperature} if args.temperature != 1.0 else {})),
             "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak, "hbm_frac_of": f"{peak_kind} HBM copy bandwidth",
             "hbm_frac_nominal": step_gbs / NOMINAL_HBM_GBS,
             "kernels": {
@@ -941,7 +962,7 @@ def run_linear(args):
             "roofline": {"kernel": "linear_partials_kernel", "bound": "tensor", "achieved": tflops, "peak": peak,
                          "peak_source": f"{peak_kind} sustained dense bf16 (burst {burst})", "unit": "TFLOP/s",
                          "frac": tflops / peak, "frac_of_burst": tflops / burst,
-                         "traffic": ncu_traffic("linear_partials_kernel", LINEAR_SOURCE),
+                         "traffic": ncu_traffic("linear_partials_kernel", LINEAR_SOURCE, active_rows=n),
                          "algorithmic_flops_per_launch": flops},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 6 * K, "clocks": clocks,
         }), flush=True)

@@ -105,6 +105,12 @@ def _f32_1d(t: torch.Tensor) -> torch.Tensor:
     return t.reshape(-1).to(torch.float32).contiguous()
 
 
+def _check_out(t: torch.Tensor, n: int, index: int, what: str) -> None:
+    """A caller-supplied per-row output: contiguous float32 with n elements on the device."""
+    if t.dtype is not torch.float32 or t.numel() != n or not t.is_contiguous() or t.get_device() != index:
+        raise ValueError(f"{what} must be a contiguous float32 tensor of {n} elements on the logits' device")
+
+
 def _need_cuda(*ts: torch.Tensor) -> None:
     for t in ts:
         if t is not None and not t.is_cuda:
@@ -127,18 +133,24 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
         _need_cuda(logits, target_ids)
     shape = logits.shape
     tshape = target_ids.shape
-    if (len(shape) == 2 and len(tshape) == 1 and tshape[0] == shape[0] and vocab is None and out is None
-            and lse is None and not (return_entropy or entropy is not None) and logits.is_contiguous()
+    if (len(shape) == 2 and len(tshape) == 1 and tshape[0] == shape[0] and vocab is None
+            and not (return_entropy or entropy is not None) and logits.is_contiguous()
             and target_ids.dtype is torch.int64 and target_ids.is_contiguous()):
-        # The common call, [N, V] row-major logits and int64 [N] targets with the
-        # outputs allocated here, without the general path's reshaping: the
-        # per-call host time is what bounds small (decode-sized) batches.
+        # The common call, [N, V] row-major logits and int64 [N] targets, without
+        # the general path's reshaping: the per-call host time is what bounds
+        # small (decode-sized) batches.
         n, width = shape
         index = logits.get_device()
         if target_ids.get_device() != index:
             raise ValueError("target_ids must be on the logits' device")
-        out = torch.empty(n, dtype=torch.float32, device=index)
-        lse = torch.empty(n, dtype=torch.float32, device=index)
+        if out is None:
+            out = torch.empty(n, dtype=torch.float32, device=index)
+        else:
+            _check_out(out, n, index, "out")
+        if lse is None:
+            lse = torch.empty(n, dtype=torch.float32, device=index)
+        else:
+            _check_out(lse, n, index, "lse")
         fn = _lib.load().bil_logp_fwd
         args = (logits.data_ptr(), _code(logits.dtype), n, width, width, target_ids.data_ptr(), int(ignore_index),
                 int(tile_v), float(temperature), out.data_ptr(), lse.data_ptr(), None, 1 if validate else 0,
@@ -164,11 +176,17 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
     t1 = _targets1d(target_ids, lead, device)
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=device)
+    else:
+        _check_out(out, n, index, "out")
     if lse is None:
         lse = torch.empty(n, dtype=torch.float32, device=device)
+    else:
+        _check_out(lse, n, index, "lse")
     want_ent = return_entropy or entropy is not None
     if want_ent and entropy is None:
         entropy = torch.empty(n, dtype=torch.float32, device=device)
+    elif want_ent:
+        _check_out(entropy, n, index, "entropy")
     st = _on_device(index, _lib.load().bil_logp_fwd, x2.data_ptr(), _code(x2.dtype), n, v, ld,
                     t1.data_ptr(), int(ignore_index), int(tile_v), float(temperature), out.data_ptr(),
                     lse.data_ptr(), entropy.data_ptr() if want_ent else None, 1 if validate else 0,
