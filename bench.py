@@ -75,7 +75,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["bil", "reference"], default="bil")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    # The end-to-end steps stream 10 GB per step over the host link; on the GPU machine a step now and
+    # then stalls for 100-200 ms with the host already queued far ahead (the GPU side waits), so
+    # the end-to-end figure is taken over enough steps that one such stall does not dominate it.
+    ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--rows", type=int, default=16384,
                     help="rows of the workload per GPU (smaller only for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -136,6 +139,61 @@ def barrier(dist, device=None):
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 
+class NvmlClocks:
+    """The SM clock and the clock-event reasons read through NVML (read-only queries) every
+    couple of milliseconds, so that a timed region of a few tens of milliseconds still gets
+    a dozen samples; nvidia-smi's own loop samples every 50 ms."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, uuid: str, period_s: float = 0.002):
+        import ctypes
+        self.rows, self.period, self.lib, self.handle = [], period_s, None, None
+        self.stop_flag = threading.Event()
+        self.thread = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            u = uuid if uuid.upper().startswith("GPU-") else "GPU-" + uuid
+            if lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) != 0:
+                return
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.lib, self.handle, self.ctypes = lib, h, ctypes
+        except (OSError, AttributeError):
+            self.lib = None
+
+    def start(self):
+        if self.lib is None:
+            return
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _run(self):
+        ct, lib, h = self.ctypes, self.lib, self.handle
+        clk, reasons = ct.c_uint(0), ct.c_ulonglong(0)
+        while not self.stop_flag.is_set():
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0  # 1: the SM clock domain
+            ok = ok and self.reason_fn(h, ct.byref(reasons)) == 0
+            if ok:
+                self.rows.append((time.time(), clk.value, reasons.value))
+            time.sleep(self.period)
+
+    def stop(self):
+        self.stop_flag.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        window = [(c, r) for (ts, c, r) in self.rows if t0 <= ts <= t1]
+        if len(window) < 3:
+            return None
+        reasons = sorted({name for (_, r) in window for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in window), "sm_min_mhz": min(c for c, _ in window),
+                "reasons": reasons, "samples": len(window), "scope": "timed region", "source": "NVML, every 2 ms"}
+
+
 class ClockSampler:
     FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -146,8 +204,11 @@ class ClockSampler:
         self.rows = []
         self.proc = None
         self.thread = None
+        self.nvml = NvmlClocks(self.uuid) if self.uuid else None
 
     def start(self):
+        if self.nvml is not None:
+            self.nvml.start()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"],
@@ -165,6 +226,8 @@ class ClockSampler:
                 self.rows.append((time.time(), parts))
 
     def stop(self):
+        if self.nvml is not None:
+            self.nvml.stop()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -175,6 +238,21 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float):
+        """nvidia-smi's samples in the timed region (the whole measured phase if it holds fewer
+        than three); with NVML's faster samples of the timed region, their median clock and
+        reasons lead, and nvidia-smi's figures stay under `nvidia_smi`."""
+        smi = self._smi_summary(t0, t1)
+        fast = self.nvml.summary(t0, t1) if self.nvml is not None else None
+        if fast is None:
+            return smi
+        out = dict(fast)
+        out["sm_max_mhz"] = smi.get("sm_max_mhz")
+        out["power_w_max"] = smi.get("power_w_max")
+        out["reasons"] = sorted(set(fast["reasons"]) | set(smi.get("reasons") or []))
+        out["nvidia_smi"] = smi
+        return out
+
+    def _smi_summary(self, t0: float, t1: float):
         uuids = {p[1] for (_, p) in self.rows}
         mine = [p for (_, p) in self.rows
                 if len(uuids) == 1 or (self.uuid and p[1].lower().replace("gpu-", "") == self.uuid)]
@@ -727,6 +805,7 @@ def run_bil(args):
                "path": "HostStreamedLogp: pinned host -> 2048-row chunks over 3 streams -> pinned host",
                "host_link_gbs": (h2d + d2h) / (e2e_ms / args.e2e_steps / 1e3) / 1e9,
                "gpu_launches": launches, "step_ms": step_ms,
+               "step_ms_median": statistics.median(step_ms),
                "host_link_probe": host_link_probe(x_host, x, d_host, dev)}
         del pipe, d_host
 
