@@ -82,6 +82,21 @@ def test_gemm_nt_against_the_oracle(m, n, k, dtype):
     assert np.all(err16 <= bound * (1 + u) + u * np.abs(ref) + 2.0 ** -24), float((err16 / (bound + u * np.abs(ref))).max())
 
 
+def test_gemm_nt_of_a_long_k_against_the_oracle():
+    """A K long enough (66000, ragged: 1032 blocks of 64) that the copy threads keep in step,
+    against the oracle's float64 product; the float32 accumulation's bound for K terms,
+    gamma_K * sum_k |a b| with gamma_K = K/4 * 2^-24 (one rounding per four products)."""
+    m, n, k = 130, 260, 66000
+    a = wl.linear_hidden(m, k, seed=51)
+    b = wl.linear_weight(n, k, seed=52)
+    ref = oracle.linear_logits(a, b, "bfloat16")
+    bound = (np.abs(oracle.widen(a, "bfloat16")) @ np.abs(oracle.widen(b, "bfloat16")).T) * (k / 4 * 2.0 ** -24) + 1e-6
+    c = bil.gemm_nt(_dev(a, "bfloat16"), _dev(b, "bfloat16"))
+    torch.cuda.synchronize()
+    err = np.abs(c.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), float((err / bound).max())
+
+
 def test_store_gemms_at_once_on_two_streams_keep_their_bits():
     """Two store GEMMs of several waves each (512 work units for 152 SMs) run at
     the same time on two streams; each must give the bits it gives alone."""
@@ -90,6 +105,21 @@ def test_store_gemms_at_once_on_two_streams_keep_their_bits():
     b1 = _dev(wl.linear_weight(n, k, seed=46), "bfloat16")
     a2 = _dev(wl.linear_hidden(m, k, seed=47), "bfloat16")
     b2 = _dev(wl.linear_weight(n, k, seed=48), "bfloat16")
+    _two_streams_same_bits(a1, b1, a2, b2)
+
+
+def test_store_gemms_of_long_k_at_once_on_two_streams_keep_their_bits():
+    """The same with a K of 65600 (1025 blocks of 64), where the copy threads of each GEMM keep
+    in step through the one position table the two launches share: each still gives its bits."""
+    m, n, k = 2048, 1024, 65600
+    a1 = _dev(wl.linear_hidden(m, k, seed=55), "bfloat16")
+    b1 = _dev(wl.linear_weight(n, k, seed=56), "bfloat16")
+    a2 = _dev(wl.linear_hidden(m, k, seed=57), "bfloat16")
+    b2 = _dev(wl.linear_weight(n, k, seed=58), "bfloat16")
+    _two_streams_same_bits(a1, b1, a2, b2)
+
+
+def _two_streams_same_bits(a1, b1, a2, b2):
     ref1, ref2 = bil.gemm_nt(a1, b1), bil.gemm_nt(a2, b2)
     torch.cuda.synchronize()
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
