@@ -30,7 +30,10 @@
 //                            [rows, vocab] and [vocab, rows];
 //   linear_store_kernel      backward: dhidden = dZ . W (B = the prepared W^T)
 //                            and dweight = dZ^T . hidden (B = hidden^T),
-//                            stored as they are.
+//                            stored as they are; from 256 rows on its work
+//                            unit is two 128-row A tiles sharing one B tile
+//                            (a 3-stage ring of 64 KB stages, both
+//                            accumulators in tensor memory at once).
 //
 // What fixes the bits of z[r, c] is the K order (K blocks in order, four
 // K=16 steps each, from a zeroed accumulator), the same for every row and
@@ -437,6 +440,11 @@ __device__ __forceinline__ void row_store(uint32_t taddr, int vcols, bool valid,
 #define BIL_STORE_LOCKSTEP 1
 #endif
 
+// Work units of the store GEMMs: 2 (two 128-row halves, from 256 rows on) or 1.
+#ifndef BIL_STORE_HALVES
+#define BIL_STORE_HALVES 2
+#endif
+
 constexpr int kSyncLead = 64;
 constexpr int kSyncMinKBlocks = 1024;      // the shortest K (in blocks of kBK) that keeps step
 constexpr int kSyncMaxBlocks = 1024;
@@ -512,9 +520,25 @@ __device__ __forceinline__ bool lockstep_gate(LinearSmem& sm, uint32_t pos) {
 
 // The GEMM C = A . B^T (A [rows, K], B [cols, K], both K-major 16-bit) with
 // one of the epilogues above.  See the file's head for the block structure.
-template <int MODE, bool ENT, int DT>
+//
+// HALVES = 2 (the store epilogue only): a work unit is 2 x kBM rows.  A stage
+// holds both 128-row A tiles and the B tile, and the two MMAs of a K step (one
+// per A tile, each into its own 256 accumulator columns) share the B tile, so
+// a block copies 32 KB per 128 x 256 x 64 of MMA work instead of 48 KB, and a
+// wave of blocks covers twice the rows (each B tile is read from DRAM half as
+// often).  The two accumulators fill tensor memory: one buffer, so the
+// epilogue of a unit does not overlap the next unit's MMAs, which costs little
+// when K is long.  Each output element still sums its K blocks in order, four
+// K=16 steps each: the same bits as with HALVES = 1.
+template <int MODE, bool ENT, int DT, int HALVES = 1>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const CUtensorMap& tmap_weight,
                                           const LinearParams& p) {
+  static_assert(HALVES == 1 || (HALVES == 2 && MODE == kModeStore), "two-half units are for the store epilogue");
+  constexpr unsigned kStageBytesH = HALVES * kStageABytes + kStageBBytes;
+  constexpr int kStagesH = static_cast<int>(kStages * size_t(kStageBytes) / kStageBytesH);  // 4, or 3 of 64 KB
+  static_assert(kStagesH >= 3 && kStagesH <= kStages, "the stage ring fits the shared memory of the 1-half layout");
+  constexpr int kAccBufs = HALVES == 1 ? 2 : 1;
+  constexpr int kRowsPerUnit = HALVES * kBM;
   extern __shared__ unsigned char smem_raw[];
   // Stage buffers start on a 1024-byte boundary (the 128-byte swizzle pattern
   // repeats every 8 rows = 1024 bytes).
@@ -566,24 +590,26 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
         unit_coords(u, p.num_m, p.num_n, p.m_group, m, n);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           if (sync_on) sync_on = lockstep_gate(sm, static_cast<uint32_t>(it));
-          const int s = static_cast<int>(it % kStages);
-          const unsigned ph = static_cast<unsigned>((it / kStages) & 1);
+          const int s = static_cast<int>(it % kStagesH);
+          const unsigned ph = static_cast<unsigned>((it / kStagesH) & 1);
           if (!thread_wait_watch(&sm.empty[s], ph ^ 1u, abort, kWatchStageFree, &g_watchdog_linear, true)) {
             ok = false;
             break;
           }
-          unsigned char* a_dst = base + s * size_t(kStageBytes);
-          mbar_arrive_expect_tx(&sm.full[s], p.a_box_bytes + kStageBBytes);
-          tma_load_2d(a_dst, &tmap_hidden, kb * kBK, m * kBM, &sm.full[s]);
-          tma_load_2d(a_dst + kStageABytes, &tmap_weight, kb * kBK, n * kBN, &sm.full[s]);
+          unsigned char* a_dst = base + s * size_t(kStageBytesH);
+          mbar_arrive_expect_tx(&sm.full[s], HALVES * p.a_box_bytes + kStageBBytes);
+#pragma unroll
+          for (int h = 0; h < HALVES; ++h)  // a half past the last row reads zeros
+            tma_load_2d(a_dst + h * kStageABytes, &tmap_hidden, kb * kBK, (m * HALVES + h) * kBM, &sm.full[s]);
+          tma_load_2d(a_dst + HALVES * kStageABytes, &tmap_weight, kb * kBK, n * kBN, &sm.full[s]);
         }
       }
       if (lockstep) *reinterpret_cast<volatile int*>(&sm.sync_done) = 1;
       // Wait (bounded, whatever happened) for the copies still in flight: the
-      // last min(it, kStages) fills, one per stage.
-      for (int64_t i = it > kStages ? it - kStages : 0; i < it; ++i) {
-        const int s = static_cast<int>(i % kStages);
-        if (!thread_wait_watch(&sm.full[s], static_cast<unsigned>((i / kStages) & 1), abort, kWatchOwnDrain,
+      // last min(it, kStagesH) fills, one per stage.
+      for (int64_t i = it > kStagesH ? it - kStagesH : 0; i < it; ++i) {
+        const int s = static_cast<int>(i % kStagesH);
+        if (!thread_wait_watch(&sm.full[s], static_cast<unsigned>((i / kStagesH) & 1), abort, kWatchOwnDrain,
                                &g_watchdog_linear, false))
           break;
       }
@@ -595,25 +621,27 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
       int local = 0;
       bool ok = true;
       for (int64_t u = blockIdx.x; u < total && ok; u += gridDim.x, ++local) {
-        const int b = local & 1;
-        const unsigned use = static_cast<unsigned>(local >> 1);
+        const int b = local % kAccBufs;
+        const unsigned use = static_cast<unsigned>(local / kAccBufs);
         if (!thread_wait_watch(&sm.acc_empty[b], (use & 1u) ^ 1u, abort, kWatchMma, &g_watchdog_linear, true)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kAccCols);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-          const int s = static_cast<int>(it % kStages);
-          const unsigned ph = static_cast<unsigned>((it / kStages) & 1);
+          const int s = static_cast<int>(it % kStagesH);
+          const unsigned ph = static_cast<unsigned>((it / kStagesH) & 1);
           if (!thread_wait_watch(&sm.full[s], ph, abort, kWatchMma, &g_watchdog_linear, true)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(base + s * size_t(kStageBytes));
-          const uint32_t b_addr = a_addr + kStageABytes;
+          const uint32_t a_addr = smem_u32(base + s * size_t(kStageBytesH));
+          const uint32_t b_addr = a_addr + HALVES * kStageABytes;
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
-            umma_f16(d_tmem, smem_desc(a_addr + k * kUmmaK * 2), smem_desc(b_addr + k * kUmmaK * 2), p.idesc,
-                     (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h)
+              umma_f16(d_tmem + static_cast<uint32_t>(h * kAccCols), smem_desc(a_addr + h * kStageABytes + k * kUmmaK * 2),
+                       smem_desc(b_addr + k * kUmmaK * 2), p.idesc, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit(&sm.empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -634,9 +662,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
     for (int64_t u = blockIdx.x; u < total; u += gridDim.x, ++local) {
       int m, n;
       unit_coords(u, p.num_m, p.num_n, p.m_group, m, n);
-      const int b = local & 1;
-      const unsigned use = static_cast<unsigned>(local >> 1);
-      const int64_t row = static_cast<int64_t>(m) * kBM + row_in_tile;
+      const int b = local % kAccBufs;
+      const unsigned use = static_cast<unsigned>(local / kAccBufs);
+      const int64_t row = static_cast<int64_t>(m) * kRowsPerUnit + row_in_tile;
       const bool valid = row < p.n_rows;
       const int64_t col0 = static_cast<int64_t>(n) * kBN;  // shard-local column of the tile's column 0
       const int vcols = static_cast<int>(p.shard_cols - col0 < kBN ? p.shard_cols - col0 : kBN);
@@ -690,8 +718,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
         if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
         tc_fence_after();
         const int eb = DT == BIL_F32 ? 4 : 2;
-        unsigned char* out_row = valid ? p.out + (row * p.ld_out + col0) * eb : nullptr;
-        row_store<DT>(taddr, vcols, valid, out_row);
+#pragma unroll 1
+        for (int h = 0; h < HALVES; ++h) {  // half h: rows [h kBM, (h + 1) kBM) of the unit
+          const int64_t row_h = row + h * kBM;
+          const bool valid_h = row_h < p.n_rows;
+          unsigned char* out_row = valid_h ? p.out + (row_h * p.ld_out + col0) * eb : nullptr;
+          row_store<DT>(taddr + static_cast<uint32_t>(h * kAccCols), vcols, valid_h, out_row);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
@@ -725,12 +758,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   gemm_body<kModeGrad, ENT, DT>(tmap_hidden, tmap_weight, p);
 }
 
-// Backward, the two contractions of dZ: C = A . B^T stored as OT.
-template <int OT>
+// Backward, the two contractions of dZ: C = A . B^T stored as OT, in work
+// units of HALVES x 128 rows.
+template <int OT, int HALVES>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_store_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const LinearParams p) {
-  gemm_body<kModeStore, false, OT>(tmap_a, tmap_b, p);
+  gemm_body<kModeStore, false, OT, HALVES>(tmap_a, tmap_b, p);
 }
 
 // dst[i] = ((src_0[i] + src_1[i]) + src_2[i]) + ... , sources in order.
@@ -938,16 +972,18 @@ unsigned next_sync_tag() {
   return t;
 }
 
-// C [a_rows, n_cols] = A . B^T over K = k with the store epilogue, rastered in
-// groups of row tiles that one wave covers with every column tile, the copy
-// threads in lockstep when every block's position fits the tag's 32 bits.
+// C [a_rows, n_cols] = A . B^T over K = k with the store epilogue, in units of
+// two 128-row halves from 256 rows on (one otherwise), rastered in groups of
+// row units that one wave covers with every column tile, the copy threads in
+// lockstep when every block's position fits the tag's 32 bits.
 int launch_store(const CUtensorMap& ma, const CUtensorMap& mb, int64_t a_rows, int64_t n_cols, int64_t k,
                  uint32_t idesc, void* out, int out_dtype, int64_t ld_out, cudaStream_t s) {
+  const int halves = BIL_STORE_HALVES == 2 && a_rows >= 2 * kBM ? 2 : 1;
   LinearParams p{};
   p.n_rows = a_rows;
   p.shard_cols = n_cols;
   p.num_n = static_cast<int>((n_cols + kBN - 1) / kBN);
-  p.num_m = static_cast<int>((a_rows + kBM - 1) / kBM);
+  p.num_m = static_cast<int>((a_rows + halves * kBM - 1) / (halves * kBM));
   p.k_blocks = static_cast<int>((k + kBK - 1) / kBK);
   p.idesc = idesc;
   p.a_box_bytes = kStageABytes;  // A maps of these GEMMs use kBM-row boxes
@@ -967,9 +1003,15 @@ int launch_store(const CUtensorMap& ma, const CUtensorMap& mb, int64_t a_rows, i
                        iters + kSyncLead < INT32_MAX
                    ? next_sync_tag()
                    : 0u;
-  GemmKernel kern = out_dtype == BIL_F32    ? linear_store_kernel<BIL_F32>
-                    : out_dtype == BIL_BF16 ? linear_store_kernel<BIL_BF16>
-                                            : linear_store_kernel<BIL_F16>;
+  GemmKernel kern;
+  if (halves == 2)
+    kern = out_dtype == BIL_F32    ? linear_store_kernel<BIL_F32, 2>
+           : out_dtype == BIL_BF16 ? linear_store_kernel<BIL_BF16, 2>
+                                   : linear_store_kernel<BIL_F16, 2>;
+  else
+    kern = out_dtype == BIL_F32    ? linear_store_kernel<BIL_F32, 1>
+           : out_dtype == BIL_BF16 ? linear_store_kernel<BIL_BF16, 1>
+                                   : linear_store_kernel<BIL_F16, 1>;
   return launch_gemm(kern, ma, mb, p, s);
 }
 

@@ -4,7 +4,8 @@ bil_linear_logp_bwd is a transpose of the hidden states, the gradient pass
 (dZ from the recomputed projection) and two store GEMMs C = A . B^T.  Queued
 one by one through bil_transpose_2d, bil_linear_logp_grad and
 bil_linear_gemm_nt they must give the same bits; the store GEMM alone must
-match the oracle's float64 product; and store GEMMs running at once on two
+match the oracle's float64 product, and a row's bits must not depend on the
+shape of the work unit that computed it; and store GEMMs running at once on two
 streams (whose copy threads keep in step through one shared position table)
 must give the bits they give one at a time.
 
@@ -95,6 +96,41 @@ def test_gemm_nt_of_a_long_k_against_the_oracle():
     torch.cuda.synchronize()
     err = np.abs(c.cpu().numpy().astype(np.float64) - ref)
     assert np.all(err <= bound), float((err / bound).max())
+
+
+def test_gemm_nt_of_a_long_k_in_two_half_units_against_the_oracle():
+    """The same bound with 300 rows (work units of two 128-row halves, the second unit's
+    second half past the last row) and a K of 66000, where the copy threads keep in step."""
+    m, n, k = 300, 260, 66000
+    a = wl.linear_hidden(m, k, seed=53)
+    b = wl.linear_weight(n, k, seed=54)
+    ref = oracle.linear_logits(a, b, "bfloat16")
+    bound = (np.abs(oracle.widen(a, "bfloat16")) @ np.abs(oracle.widen(b, "bfloat16")).T) * (k / 4 * 2.0 ** -24) + 1e-6
+    c = bil.gemm_nt(_dev(a, "bfloat16"), _dev(b, "bfloat16"))
+    torch.cuda.synchronize()
+    err = np.abs(c.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), float((err / bound).max())
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_store_gemm_rows_agree_across_work_unit_shapes(out_dtype):
+    """From 256 rows on the store GEMM's work unit is two 128-row A tiles sharing one B
+    tile, below that one 128-row tile.  Each element sums its K blocks in the same order
+    either way, so a row has the same bits whichever unit computed it, wherever the batch
+    starts: a 600-row A against slices of it of 200 and 100 rows (one-half units) and of
+    500 and 257 rows (two-half units at other offsets)."""
+    m, n, k = 600, 520, 5000
+    a = _dev(wl.linear_hidden(m, k, seed=61), "bfloat16")
+    b = _dev(wl.linear_weight(n, k, seed=62), "bfloat16")
+    c = bil.gemm_nt(a, b, out_dtype=out_dtype)
+    parts = {(256, 456): None, (333, 433): None, (100, 600): None, (343, 600): None}
+    for lo, hi in parts:
+        parts[(lo, hi)] = bil.gemm_nt(a[lo:hi], b, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    full = c.contiguous().view(torch.int32 if out_dtype == torch.float32 else torch.int16)
+    for (lo, hi), cp in parts.items():
+        got = cp.contiguous().view(full.dtype)
+        assert torch.equal(got, full[lo:hi]), (lo, hi)
 
 
 def test_store_gemms_at_once_on_two_streams_keep_their_bits():
