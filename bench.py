@@ -552,9 +552,9 @@ def linear_measurement(bil, stream, dev, steps: int = 5):
     """The fused LM-head + logp step at full size: hidden [16384, 4096] bf16 times a
     Qwen3-8B-shaped LM head [151936, 4096] bf16 (the `--workload linear` batch).
     Forward: tile partials from the tensor-core accumulator, then the merge.
-    Backward, queued step by step through the public calls it is made of: the
-    hidden states transposed, dZ from the recomputed projection, dhidden = dZ . W
-    and dweight = dZ^T . X.  Each step is timed with CUDA events on the
+    Backward, queued step by step through the public calls it is made of: dZ
+    from the recomputed projection, dhidden = dZ . W and dweight = dZ^T . X (the
+    products read dZ, W and X where they lie).  Each step is timed with CUDA events on the
     launching stream, `steps` steps after 2 warm-up steps, clocks sampled
     meanwhile.  Outside the timed region of the headline value."""
     import torch
@@ -573,7 +573,6 @@ def linear_measurement(bil, stream, dev, steps: int = 5):
     tl = torch.empty(n, dtype=torch.float32, device=dev)
     logp = torch.empty(n, dtype=torch.float32, device=dev)
     lse = torch.empty(n, dtype=torch.float32, device=dev)
-    w_t = bil.linear.prepared_weight_t(wt)
 
     def parts():
         bil.linear_logp_partials(x, wt, t, v, 0, nt, pm, ps, tl)
@@ -582,19 +581,15 @@ def linear_measurement(bil, stream, dev, steps: int = 5):
         bil.logp_merge(pm, ps, nt, tl, t, v, out=logp, lse=lse)
     state = {}
 
-    def transpose():
-        state["x_t"] = bil.linear.transpose(x)
-
     def grad():
-        state["dz"], state["dz_t"] = bil.linear_logp_grad(x, wt, t, lse, g)
+        state["dz"] = bil.linear_logp_grad(x, wt, t, lse, g)
 
     def dhidden():
-        state["dh"] = bil.gemm_nt(state["dz"], w_t, out_dtype=torch.bfloat16)
+        state["dh"] = bil.matmul(state["dz"], wt, out_dtype=torch.bfloat16)
 
     def dweight():
-        state["dw"] = bil.gemm_nt(state["dz_t"], state["x_t"], out_dtype=torch.bfloat16)
-    seq = [("partials", parts), ("merge", merge), ("transpose", transpose), ("grad", grad), ("dhidden", dhidden),
-           ("dweight", dweight)]
+        state["dw"] = bil.matmul(state["dz"].t(), x, out_dtype=torch.bfloat16)
+    seq = [("partials", parts), ("merge", merge), ("grad", grad), ("dhidden", dhidden), ("dweight", dweight)]
     for _ in range(2):
         for _, f in seq:
             f()
@@ -616,7 +611,7 @@ def linear_measurement(bil, stream, dev, steps: int = 5):
     step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in ev)
     flops = 2.0 * n * h * v
     _, sustained, kind = tensor_peak()
-    bwd_ms = ms["transpose"] + ms["grad"] + ms["dhidden"] + ms["dweight"]
+    bwd_ms = ms["grad"] + ms["dhidden"] + ms["dweight"]
     out = {"workload": LINEAR_WORKLOAD, "steps": steps, "step_ms": step_ms, "rows_per_s": n / (step_ms / 1e3),
            "tflops": 4 * flops / (step_ms / 1e3) / 1e12, "fwd_ms": ms["partials"] + ms["merge"],
            "fwd_tflops": flops / (ms["partials"] / 1e3) / 1e12, "bwd_ms": bwd_ms,
@@ -627,9 +622,8 @@ def linear_measurement(bil, stream, dev, steps: int = 5):
     for name in ("grad", "dhidden", "dweight"):
         out[f"{name}_ms"] = ms[name]
         out[f"{name}_tflops"] = flops / (ms[name] / 1e3) / 1e12
-    out["transpose_ms"] = ms["transpose"]
     out["merge_ms"] = ms["merge"]
-    del state, pm, ps, x, wt, w_t
+    del state, pm, ps, x, wt
     return out
 
 
@@ -933,12 +927,11 @@ def run_linear(args):
     logp = torch.empty(n, dtype=torch.float32, device=dev)
     lse = torch.empty(n, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    w_t = bil.linear.prepared_weight_t(wt)  # the prepared [H, V] weight, kept while the weight is unchanged
 
     def step():
         bil.linear_logp_partials(x, wt, t, v, 0, nt, pm, ps, tl)
         bil.logp_merge(pm, ps, nt, tl, t, v, out=logp, lse=lse)
-        bil.linear_logp_bwd(x, wt, t, lse, g, weight_t=w_t)
+        bil.linear_logp_bwd(x, wt, t, lse, g)
 
     props = torch.cuda.get_device_properties(dev)
     sampler = ClockSampler(str(getattr(props, "uuid", "")))
@@ -957,7 +950,7 @@ def run_linear(args):
         ev[i][1].record(stream)
         bil.logp_merge(pm, ps, nt, tl, t, v, out=logp, lse=lse)
         ev[i][2].record(stream)
-        bil.linear_logp_bwd(x, wt, t, lse, g, weight_t=w_t)
+        bil.linear_logp_bwd(x, wt, t, lse, g)
         ev[i][3].record(stream)
     torch.cuda.synchronize(dev)
     host_t1 = time.time()
@@ -966,9 +959,7 @@ def run_linear(args):
     part_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     merge_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
-    # the backward's scratch: dZ and dZ^T (bf16), hidden^T, plus the prepared W^T
-    scratch = 2 * n * v * 2 + h * n * 2
-    prepared = h * v * 2
+    scratch = n * v * 2  # the backward's scratch: dZ (bf16)
     sampler.stop()
     clocks = sampler.summary(host_t0, host_t1)
     total_ms = max_over_ranks(total_ms, dist, dev)
@@ -995,7 +986,7 @@ def run_linear(args):
             td.copy_(t_host, non_blocking=True)
             gd.copy_(g_host, non_blocking=True)
             lp, ls = bil.linear_logp(xd, wt, td, workspace=ws)
-            bil.linear_logp_bwd(xd, wt, td, ls, gd, weight_t=w_t)
+            bil.linear_logp_bwd(xd, wt, td, ls, gd)
             logp_host.copy_(lp, non_blocking=True)
             lse_host.copy_(ls, non_blocking=True)
         for _ in range(2):
@@ -1036,14 +1027,13 @@ def run_linear(args):
             "kernels": {"linear_partials": {"ms": part_ms, "tflops": tflops},
                         "logp_merge": {"ms": merge_ms},
                         "linear_logp_bwd": {"ms": bwd_ms, "tflops": 3 * flops / (bwd_ms / 1e3) / 1e12,
-                                            "launches": 4, "scratch_bytes": scratch,
-                                            "prepared_weight_t_bytes": prepared}},
+                                            "launches": 3, "scratch_bytes": scratch}},
             "roofline": {"kernel": "linear_partials_kernel", "bound": "tensor", "achieved": tflops, "peak": peak,
                          "peak_source": f"{peak_kind} sustained dense bf16 (burst {burst})", "unit": "TFLOP/s",
                          "frac": tflops / peak, "frac_of_burst": tflops / burst,
                          "traffic": ncu_traffic("linear_partials_kernel", LINEAR_SOURCE, active_rows=n),
                          "algorithmic_flops_per_launch": flops},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 6 * K, "clocks": clocks,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 5 * K, "clocks": clocks,
         }), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -326,7 +326,9 @@ int bil_linear_logp_fwd(const void *hidden, const void *weight, int dtype, int64
  *     dweight = dZ^T . hidden      [vocab, hidden_size]
  * both accumulated in float32 on the tensor cores in K blocks of 64 in
  * increasing order (K = vocab for dhidden, n_rows for dweight), so a row's
- * dhidden never depends on the other rows.
+ * dhidden never depends on the other rows.  Three launches: dZ into `dz`, then
+ * the two products, which read dz, weight and hidden where they lie (no
+ * transposed copies).
  *
  *  hidden, weight, dtype, n_rows, hidden_size, ld_hidden, vocab, ld_weight,
  *  tile_begin, tile_end, temperature, target_ids, ignore_index
@@ -337,19 +339,12 @@ int bil_linear_logp_fwd(const void *hidden, const void *weight, int dtype, int64
  *                With a shard, dhidden is the shard's part of the sum over
  *                the vocabulary (the ranks' parts add up to it; see
  *                bil_sum_f32) and dweight holds the shard's rows.
- *  weight_t      the shard's weight transposed, [hidden_size, ld_weight_t]
- *                (ld_weight_t >= cols), e.g. from bil_transpose_2d; a caller
- *                keeps it as long as the weight does not change.
  *  lse           [n_rows] float32, the forward's lse.
  *  grad_logp     [n_rows] float32 upstream gradient of logp.
  *  entropy, grad_entropy   both NULL, or the forward's entropy and its
  *                upstream gradient ([n_rows] float32 each).
- *  dz            [n_rows, ld_dz] (ld_dz >= cols) of dtype: receives dZ.
- *  dz_t          [cols, ld_dz_t] (ld_dz_t >= n_rows) of dtype: receives dZ^T.
- *  hidden_t      [hidden_size, ld_hidden_t] (ld_hidden_t >= n_rows) of dtype:
- *                receives hidden^T.
- *                (dz, dz_t and hidden_t are the backward's scratch, owned by
- *                the caller, readable afterwards.)
+ *  dz            [n_rows, ld_dz] (ld_dz >= cols) of dtype: receives dZ (the
+ *                backward's scratch, owned by the caller, readable afterwards).
  *  dhidden       [n_rows, ld_dhidden] of dhidden_dtype (BIL_F32, or dtype
  *                rounded to nearest even).
  *  dweight       [cols, ld_dweight] of dweight_dtype (the same choice).
@@ -359,45 +354,52 @@ int bil_linear_logp_fwd(const void *hidden, const void *weight, int dtype, int64
  * (and so its dhidden row and every dweight entry it touches).  n_rows = 0
  * sets dweight to zero.
  */
-int bil_linear_logp_bwd(const void *hidden, const void *weight, const void *weight_t, int dtype,
-                        int64_t n_rows, int64_t hidden_size, int64_t ld_hidden, int64_t vocab,
-                        int64_t ld_weight, int64_t ld_weight_t, int32_t tile_begin, int32_t tile_end,
-                        float temperature,
+int bil_linear_logp_bwd(const void *hidden, const void *weight, int dtype, int64_t n_rows,
+                        int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight,
+                        int32_t tile_begin, int32_t tile_end, float temperature,
                         const int64_t *target_ids, int64_t ignore_index, const float *lse,
                         const float *grad_logp, const float *entropy, const float *grad_entropy,
-                        void *dz, int64_t ld_dz, void *dz_t, int64_t ld_dz_t, void *hidden_t,
-                        int64_t ld_hidden_t, void *dhidden, int dhidden_dtype, int64_t ld_dhidden,
+                        void *dz, int64_t ld_dz, void *dhidden, int dhidden_dtype, int64_t ld_dhidden,
                         void *dweight, int dweight_dtype, int64_t ld_dweight, bil_stream_t stream);
 
 /*
  * bil_linear_logp_grad -- the first step of bil_linear_logp_bwd alone: dZ of
  * the shard's columns from the recomputed projection, written to dz
- * [n_rows, ld_dz] and dz_t [cols, ld_dz_t] (the same bits as there).
- * Arguments, layouts and errors as for bil_linear_logp_bwd; nothing else is
- * written.  Together with bil_transpose_2d and bil_linear_gemm_nt it lets a
- * caller queue (and time) the backward's steps one by one.
+ * [n_rows, ld_dz] (the same bits as there).  Arguments, layouts and errors as
+ * for bil_linear_logp_bwd; nothing else is written.  Together with
+ * bil_linear_gemm it lets a caller queue (and time) the backward's steps one
+ * by one: dhidden = bil_linear_gemm(dz K-major, weight MN-major), dweight =
+ * bil_linear_gemm(dz MN-major, hidden MN-major).
  */
 int bil_linear_logp_grad(const void *hidden, const void *weight, int dtype, int64_t n_rows,
                          int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight,
                          int32_t tile_begin, int32_t tile_end, float temperature,
                          const int64_t *target_ids, int64_t ignore_index, const float *lse,
                          const float *grad_logp, const float *entropy, const float *grad_entropy,
-                         void *dz, int64_t ld_dz, void *dz_t, int64_t ld_dz_t, bil_stream_t stream);
+                         void *dz, int64_t ld_dz, bil_stream_t stream);
+
+/* How bil_linear_gemm finds an operand with `rows` rows over K: */
+#define BIL_LAYOUT_K_MAJOR 0  /* stored [rows, K] row-major: element (i, k) at p[i * ld + k] */
+#define BIL_LAYOUT_MN_MAJOR 1 /* stored [K, rows] row-major: element (i, k) at p[k * ld + i] */
 
 /*
- * bil_linear_gemm_nt -- C = A . B^T on the tensor cores, the contraction
- * bil_linear_logp_bwd uses for dhidden (A = dZ, B = weight^T) and dweight
- * (A = dZ^T, B = hidden^T).  A [m, k] and B [n, k] are row-major (K-major)
- * matrices of dtype (BIL_BF16 or BIL_F16; row strides lda, ldb >= k
- * elements); C [m, ldc] (ldc >= n) receives C[i, j] = sum_k A[i, k] B[j, k]
- * accumulated in float32 in K blocks of 64 in increasing order, stored as
- * c_dtype (BIL_F32, or dtype rounded to nearest even).  Row i of C depends on
- * row i of A and on B only.  16-byte aligned bases and row strides of a
- * multiple of 16 bytes (BIL_E_ALIGN otherwise); k >= 1; m = 0 or n = 0 queue
- * nothing.  Device pointers owned by the caller; asynchronous on `stream`.
+ * bil_linear_gemm -- C = A . B^T on the tensor cores, the contraction
+ * bil_linear_logp_bwd uses for dhidden (A = dZ, B = weight read as [K, n])
+ * and dweight (A = dZ read as [K, m], B = hidden read as [K, n]).  A has m
+ * rows and B n rows over K = k, each stored as its layout says (row strides
+ * lda, ldb >= the stored row length: k for K-major, m or n for MN-major), of
+ * dtype (BIL_BF16 or BIL_F16).  C [m, ldc] (ldc >= n) receives
+ * C[i, j] = sum_k A(i, k) B(j, k) accumulated in float32 in K blocks of 64 in
+ * increasing order (the same bits for either layout), stored as c_dtype
+ * (BIL_F32, or dtype rounded to nearest even).  Row i of C depends on row i
+ * of A and on B only.  16-byte aligned bases and row strides of a multiple of
+ * 16 bytes (BIL_E_ALIGN otherwise); k >= 1; a layout other than the two
+ * above is BIL_E_INVALID_ARG; m = 0 or n = 0 queue nothing.  Device pointers
+ * owned by the caller; asynchronous on `stream`.
  */
-int bil_linear_gemm_nt(const void *a, const void *b, int dtype, int64_t m, int64_t n, int64_t k,
-                       int64_t lda, int64_t ldb, void *c, int c_dtype, int64_t ldc, bil_stream_t stream);
+int bil_linear_gemm(const void *a, int a_layout, const void *b, int b_layout, int dtype, int64_t m,
+                    int64_t n, int64_t k, int64_t lda, int64_t ldb, void *c, int c_dtype, int64_t ldc,
+                    bil_stream_t stream);
 
 /*
  * bil_sum_f32 -- dst[i] = ((srcs[0][i] + srcs[1][i]) + srcs[2][i]) + ... for
@@ -407,14 +409,6 @@ int bil_linear_gemm_nt(const void *a, const void *b, int dtype, int64_t m, int64
  * holds the same bits.
  */
 int bil_sum_f32(const float *const *srcs, int count, int64_t n, float *dst, bil_stream_t stream);
-
-/*
- * bil_transpose_2d -- dst[c, r] = src[r, c] for a [rows, cols] matrix of
- * 16-bit elements (BIL_BF16 or BIL_F16); ld_src >= cols, ld_dst >= rows.
- * Prepares the transposed LM-head weight that bil_linear_logp_bwd takes.
- */
-int bil_transpose_2d(const void *src, int dtype, int64_t rows, int64_t cols, int64_t ld_src, void *dst,
-                     int64_t ld_dst, bil_stream_t stream);
 
 /* Size of the device array that bil_linear_logp_fwd_static uses as its scratch. */
 #define BIL_LINEAR_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)

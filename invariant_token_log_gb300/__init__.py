@@ -19,6 +19,7 @@ from .linear import (  # noqa: F401
     linear_logp_bwd,
     linear_logp_grad,
     linear_logp_partials,
+    matmul,
 )
 from .logp import (  # noqa: F401
     DEFAULT_TILE_V,

@@ -18,6 +18,7 @@ MAX_FUSED_TILES = 2048
 MAX_EXTENT_BYTES = 1 << 48
 LINEAR_TILE_V = 256
 LINEAR_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
+LAYOUT_K_MAJOR, LAYOUT_MN_MAJOR = 0, 1
 
 # every entry point the header declares: name -> (restype, argtypes)
 _i32, _i64, _p, _u = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
@@ -40,14 +41,12 @@ SIGNATURES = {
     "bil_linear_logp_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_i64)]),
     "bil_linear_logp_fwd": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p, _p, _i32,
                                    _i64, _p, _i64, _i32, _p]),
-    "bil_linear_logp_bwd": (_i32, [_p, _p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32,
-                                   ctypes.c_int32, _f, _p, _i64, _p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p,
-                                   _i32, _i64, _p, _i32, _i64, _p]),
+    "bil_linear_logp_bwd": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, ctypes.c_int32,
+                                   _f, _p, _i64, _p, _p, _p, _p, _p, _i64, _p, _i32, _i64, _p, _i32, _i64, _p]),
     "bil_linear_logp_grad": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, ctypes.c_int32, ctypes.c_int32,
-                                    _f, _p, _i64, _p, _p, _p, _p, _p, _i64, _p, _i64, _p]),
-    "bil_linear_gemm_nt": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _p, _i32, _i64, _p]),
+                                    _f, _p, _i64, _p, _p, _p, _p, _p, _i64, _p]),
+    "bil_linear_gemm": (_i32, [_p, _i32, _p, _i32, _i32, _i64, _i64, _i64, _i64, _i64, _p, _i32, _i64, _p]),
     "bil_sum_f32": (_i32, [ctypes.POINTER(ctypes.c_void_p), _i32, _i64, _p, _p]),
-    "bil_transpose_2d": (_i32, [_p, _i32, _i64, _i64, _i64, _p, _i64, _p]),
     "bil_probe_exp_rate": (_i32, [ctypes.c_int32, ctypes.c_int32, _p, _p, _p]),
     "bil_linear_logp_fwd_static": (_i32, [_p, _p, _i32, _i64, _i64, _i64, _i64, _i64, _f, _p, _i64, _p, _p, _p, _i32,
                                           _p]),

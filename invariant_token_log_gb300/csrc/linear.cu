@@ -137,13 +137,12 @@ struct LinearParams {
   int64_t vocab;               // targets outside [0, vocab) give NaN rows
   unsigned char* dz;           // [n_rows, ld_dz] 16-bit
   int64_t ld_dz;
-  unsigned char* dz_t;         // [shard_cols, ld_dz_t] 16-bit
-  int64_t ld_dz_t;
   // kModeStore
   unsigned char* out;          // [n_rows, ld_out]
   int out_dtype;
   int64_t ld_out;
   unsigned sync_tag;           // non-zero: the copy threads keep in step (see lockstep_service)
+  int a_mn, b_mn;              // 1: the operand is stored [K, rows] (rows contiguous), else [rows, K]
 };
 
 // ---------------------------------------------------------------------------
@@ -151,11 +150,12 @@ struct LinearParams {
 // ---------------------------------------------------------------------------
 
 // Instruction descriptor of tcgen05.mma kind::f16: D float32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9, 10-12 = 1) or fp16 (0), both K-major (bits 15, 16 =
-// 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t make_idesc(bool bf16) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+// A and B bf16 (bits 7-9, 10-12 = 1) or fp16 (0), A and B K-major (bits 15,
+// 16 = 0) or MN-major (1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t make_idesc(bool bf16, bool a_mn = false, bool b_mn = false) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(kBN >> 3) << 17) |
+         (static_cast<uint32_t>(kBM >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor of a K-major operand stored the way a TMA
@@ -167,6 +167,21 @@ constexpr uint32_t make_idesc(bool bf16) {
 // within the 128-byte row advances the start address by 32 bytes.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
   return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(16 >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// The same for an MN-major operand (rows contiguous in memory), as TMA loads
+// with 128-byte swizzle write it in boxes of 64 rows x 64 K: each K index is
+// one 128-byte line of 64 consecutive rows, 8 K indices make a 1024-byte
+// swizzle atom (stride byte offset between the atoms along K), and the next
+// 64 rows are the next box, kMnBoxBytes further on (leading byte offset).  A
+// K step of 16 advances the start address by 16 lines = 2048 bytes, two whole
+// atoms.
+constexpr int kMnBox = 64;                                // rows (and K) per box of an MN-major operand
+constexpr uint32_t kMnBoxBytes = kMnBox * kBK * 2;        // 8 KB
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(kMnBoxBytes >> 4) << 16) |
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
          (static_cast<uint64_t>(2) << 61);
 }
@@ -355,14 +370,11 @@ __device__ __forceinline__ void store_row16(uint16_t* o, const float (&v)[kChunk
 
 // The gradient tile of one row: dZ[row, c] for the tile's columns, by the
 // library's backward formula (grad_elem) from the float32 accumulator, stored
-// rounded to 16 bits into dz (row-major) and dz_t (transposed; the 32 lanes of
-// a warp hold 32 consecutive rows, so each column is one 64-byte store).
-// Inactive rows are +0.0; an active row whose target is outside [0, vocab)
-// is NaN.
+// rounded to 16 bits into dz (row-major).  Inactive rows are +0.0; an active
+// row whose target is outside [0, vocab) is NaN.
 template <bool ENT, int DT>
 __device__ __forceinline__ void row_grad(uint32_t taddr, int vcols, float rcp, int64_t tloc, bool valid, bool active,
-                                         bool bad_target, const RowMeta& meta, uint16_t* dz_row, uint16_t* dzt_col0,
-                                         int64_t ld_dz_t) {
+                                         bool bad_target, const RowMeta& meta, uint16_t* dz_row) {
   uint32_t r[kChunk];
   float d[kChunk];
 #pragma unroll 1
@@ -375,12 +387,7 @@ __device__ __forceinline__ void row_grad(uint32_t taddr, int vcols, float rcp, i
       if (bad_target) v = __int_as_float(0x7fc00000);
       d[j] = v;
     }
-    if (valid && c0 < vcols) {
-      store_row16<DT>(dz_row + c0, d, vcols - c0);
-#pragma unroll
-      for (int j = 0; j < kChunk; ++j)
-        if (c0 + j < vcols) dzt_col0[(c0 + j) * ld_dz_t] = to16<DT>(d[j]);
-    }
+    if (valid && c0 < vcols) store_row16<DT>(dz_row + c0, d, vcols - c0);
   }
 }
 
@@ -597,11 +604,27 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
             break;
           }
           unsigned char* a_dst = base + s * size_t(kStageBytesH);
+          unsigned char* b_dst = a_dst + HALVES * kStageABytes;
           mbar_arrive_expect_tx(&sm.full[s], HALVES * p.a_box_bytes + kStageBBytes);
+          // Boxes past the last row (or K) read zeros.  A K-major operand comes
+          // in one box of 128 (A) or 256 (B) rows by 64 K, an MN-major one in
+          // boxes of 64 rows by 64 K (their coordinates: row, then K).
+          if (MODE == kModeStore && p.a_mn) {
 #pragma unroll
-          for (int h = 0; h < HALVES; ++h)  // a half past the last row reads zeros
-            tma_load_2d(a_dst + h * kStageABytes, &tmap_hidden, kb * kBK, (m * HALVES + h) * kBM, &sm.full[s]);
-          tma_load_2d(a_dst + HALVES * kStageABytes, &tmap_weight, kb * kBK, n * kBN, &sm.full[s]);
+            for (int j = 0; j < HALVES * kBM / kMnBox; ++j)
+              tma_load_2d(a_dst + j * kMnBoxBytes, &tmap_hidden, m * HALVES * kBM + j * kMnBox, kb * kBK, &sm.full[s]);
+          } else {
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h)
+              tma_load_2d(a_dst + h * kStageABytes, &tmap_hidden, kb * kBK, (m * HALVES + h) * kBM, &sm.full[s]);
+          }
+          if (MODE == kModeStore && p.b_mn) {
+#pragma unroll
+            for (int j = 0; j < kBN / kMnBox; ++j)
+              tma_load_2d(b_dst + j * kMnBoxBytes, &tmap_weight, n * kBN + j * kMnBox, kb * kBK, &sm.full[s]);
+          } else {
+            tma_load_2d(b_dst, &tmap_weight, kb * kBK, n * kBN, &sm.full[s]);
+          }
         }
       }
       if (lockstep) *reinterpret_cast<volatile int*>(&sm.sync_done) = 1;
@@ -636,12 +659,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
           tc_fence_after();
           const uint32_t a_addr = smem_u32(base + s * size_t(kStageBytesH));
           const uint32_t b_addr = a_addr + HALVES * kStageABytes;
+          const bool a_mn = MODE == kModeStore && p.a_mn, b_mn = MODE == kModeStore && p.b_mn;
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
+            // a K step: 32 bytes along a K-major line, 16 lines of an MN-major box
+            const uint64_t bdesc = b_mn ? smem_desc_mn(b_addr + k * kUmmaK * 128) : smem_desc(b_addr + k * kUmmaK * 2);
 #pragma unroll
-            for (int h = 0; h < HALVES; ++h)
-              umma_f16(d_tmem + static_cast<uint32_t>(h * kAccCols), smem_desc(a_addr + h * kStageABytes + k * kUmmaK * 2),
-                       smem_desc(b_addr + k * kUmmaK * 2), p.idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int h = 0; h < HALVES; ++h) {
+              const uint32_t ah = a_addr + h * kStageABytes;  // an MN-major half is two boxes: the same 16 KB
+              const uint64_t adesc = a_mn ? smem_desc_mn(ah + k * kUmmaK * 128) : smem_desc(ah + k * kUmmaK * 2);
+              umma_f16(d_tmem + static_cast<uint32_t>(h * kAccCols), adesc, bdesc, p.idesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(&sm.empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -709,8 +737,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
         if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
         tc_fence_after();
         uint16_t* dz_row = valid ? reinterpret_cast<uint16_t*>(p.dz) + row * p.ld_dz + col0 : nullptr;
-        uint16_t* dzt_col0 = valid ? reinterpret_cast<uint16_t*>(p.dz_t) + col0 * p.ld_dz_t + row : nullptr;
-        row_grad<ENT, DT>(taddr, vcols, p.rcp, tloc, valid, active, bad_target, meta, dz_row, dzt_col0, p.ld_dz_t);
+        row_grad<ENT, DT>(taddr, vcols, p.rcp, tloc, valid, active, bad_target, meta, dz_row);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
@@ -782,26 +809,6 @@ __global__ void __launch_bounds__(256) sum_f32_kernel(SumSources s, int count, i
   }
 }
 
-// Out-of-place transpose of a [rows, cols] matrix of 16-bit elements
-// (dst[c, r] = src[r, c]) through a 64 x 64 shared-memory tile; consecutive
-// threads read consecutive elements of a source row and write consecutive
-// elements of a destination row.
-__global__ void __launch_bounds__(256) transpose16_kernel(const uint16_t* __restrict__ src, int64_t rows,
-                                                          int64_t cols, int64_t ld_src, uint16_t* __restrict__ dst,
-                                                          int64_t ld_dst) {
-  __shared__ uint16_t tile[64][66];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
-  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
-    const int r = i / 64, c = i % 64;
-    if (r0 + r < rows && c0 + c < cols) tile[r][c] = src[(r0 + r) * ld_src + c0 + c];
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
-    const int c = i / 64, r = i % 64;
-    if (r0 + r < rows && c0 + c < cols) dst[(c0 + c) * ld_dst + r0 + r] = tile[r][c];
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
@@ -869,16 +876,6 @@ int store_group(int num_n) {
   int sms = 0, smem = 0;
   if (bil_internal::device_limits(&sms, &smem) != BIL_OK || sms <= 0) sms = 148;
   return std::max(1, sms / std::max(1, num_n));
-}
-
-int launch_transpose16(const void* src, int64_t rows, int64_t cols, int64_t ld_src, void* dst, int64_t ld_dst,
-                       cudaStream_t stream) {
-  const int64_t gx = (cols + 63) / 64, gy = (rows + 63) / 64;
-  if (gx > INT32_MAX || gy > 65535) return BIL_E_UNSUPPORTED;
-  if (rows == 0 || cols == 0) return BIL_OK;
-  transpose16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(src), rows, cols, ld_src, static_cast<uint16_t*>(dst), ld_dst);
-  return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
 // A 16-byte aligned base and a row stride of a multiple of 16 bytes (what TMA
@@ -976,8 +973,8 @@ unsigned next_sync_tag() {
 // two 128-row halves from 256 rows on (one otherwise), rastered in groups of
 // row units that one wave covers with every column tile, the copy threads in
 // lockstep when every block's position fits the tag's 32 bits.
-int launch_store(const CUtensorMap& ma, const CUtensorMap& mb, int64_t a_rows, int64_t n_cols, int64_t k,
-                 uint32_t idesc, void* out, int out_dtype, int64_t ld_out, cudaStream_t s) {
+int launch_store(const CUtensorMap& ma, const CUtensorMap& mb, int64_t a_rows, int64_t n_cols, int64_t k, bool bf16,
+                 bool a_mn, bool b_mn, void* out, int out_dtype, int64_t ld_out, cudaStream_t s) {
   const int halves = BIL_STORE_HALVES == 2 && a_rows >= 2 * kBM ? 2 : 1;
   LinearParams p{};
   p.n_rows = a_rows;
@@ -985,8 +982,10 @@ int launch_store(const CUtensorMap& ma, const CUtensorMap& mb, int64_t a_rows, i
   p.num_n = static_cast<int>((n_cols + kBN - 1) / kBN);
   p.num_m = static_cast<int>((a_rows + halves * kBM - 1) / (halves * kBM));
   p.k_blocks = static_cast<int>((k + kBK - 1) / kBK);
-  p.idesc = idesc;
-  p.a_box_bytes = kStageABytes;  // A maps of these GEMMs use kBM-row boxes
+  p.idesc = make_idesc(bf16, a_mn, b_mn);
+  p.a_box_bytes = kStageABytes;  // kBM-row boxes (K-major), or two of 64 rows (MN-major)
+  p.a_mn = a_mn ? 1 : 0;
+  p.b_mn = b_mn ? 1 : 0;
   p.m_group = store_group(p.num_n);
   p.out = static_cast<unsigned char*>(out);
   p.out_dtype = out_dtype;
@@ -1015,13 +1014,20 @@ int launch_store(const CUtensorMap& ma, const CUtensorMap& mb, int64_t a_rows, i
   return launch_gemm(kern, ma, mb, p, s);
 }
 
+// A store GEMM operand with `rows` rows (M or N) over K = k: stored [rows, k]
+// (K-major) and copied in boxes of box_rows x 64 K, or stored [k, rows] (mn:
+// MN-major) and copied in boxes of 64 rows x 64 K.
+int operand_map(CUtensorMap* map, const void* ptr, int dtype, int64_t rows, int64_t k, int64_t ld, bool mn,
+                int box_rows) {
+  return mn ? make_map(map, ptr, dtype, k, rows, ld, kMnBox) : make_map(map, ptr, dtype, rows, k, ld, box_rows);
+}
+
 // dZ of the shard's columns from the recomputed projection (maps: hidden with
-// kBM-row boxes, weight with kBN-row boxes), stored as dz and dz_t.
+// kBM-row boxes, weight with kBN-row boxes), stored as dz.
 int launch_grad(const CUtensorMap& mh, const CUtensorMap& mw, int dtype, int64_t n_rows, int64_t hidden_size,
                 int64_t cols, int32_t tile_begin, int32_t tile_end, float rcp, const int64_t* targets,
                 int64_t ignore_index, const float* lse, const float* grad_logp, const float* entropy,
-                const float* grad_entropy, int64_t vocab, void* dz, int64_t ld_dz, void* dz_t, int64_t ld_dz_t,
-                cudaStream_t s) {
+                const float* grad_entropy, int64_t vocab, void* dz, int64_t ld_dz, cudaStream_t s) {
   LinearParams p{};
   p.n_rows = n_rows;
   p.shard_cols = cols;
@@ -1042,8 +1048,6 @@ int launch_grad(const CUtensorMap& mh, const CUtensorMap& mw, int dtype, int64_t
   p.vocab = vocab;
   p.dz = static_cast<unsigned char*>(dz);
   p.ld_dz = ld_dz;
-  p.dz_t = static_cast<unsigned char*>(dz_t);
-  p.ld_dz_t = ld_dz_t;
   const bool ent = entropy != nullptr;
   GemmKernel k = dtype == BIL_BF16 ? (ent ? linear_grad_kernel<true, BIL_BF16> : linear_grad_kernel<false, BIL_BF16>)
                                    : (ent ? linear_grad_kernel<true, BIL_F16> : linear_grad_kernel<false, BIL_F16>);
@@ -1055,7 +1059,7 @@ int launch_grad(const CUtensorMap& mh, const CUtensorMap& mw, int dtype, int64_t
 int check_grad_args(const void* hidden, const void* weight, int64_t n_rows, int64_t hidden_size, int64_t ld_hidden,
                     int64_t vocab, int64_t ld_weight, int32_t tile_begin, int32_t tile_end, const int64_t* targets,
                     const float* lse, const float* grad_logp, const float* entropy, const float* grad_entropy,
-                    const void* dz, int64_t ld_dz, const void* dz_t, int64_t ld_dz_t, int64_t* cols_out) {
+                    const void* dz, int64_t ld_dz, int64_t* cols_out) {
   if (vocab < 1) return BIL_E_INVALID_ARG;
   if (vocab > BIL_MAX_EXTENT_BYTES) return BIL_E_UNSUPPORTED;
   const int64_t num_tiles = (vocab + kBN - 1) / kBN;
@@ -1064,24 +1068,21 @@ int check_grad_args(const void* hidden, const void* weight, int64_t n_rows, int6
   // the shard: global vocabulary columns [tile_begin * 256, min(tile_end * 256, vocab))
   const int64_t cols = std::min<int64_t>(static_cast<int64_t>(tile_end) * kBN, vocab) -
                        static_cast<int64_t>(tile_begin) * kBN;
-  if (n_rows < 0 || hidden_size < 1 || ld_hidden < hidden_size || ld_weight < hidden_size || ld_dz < cols ||
-      ld_dz_t < n_rows)
+  if (n_rows < 0 || hidden_size < 1 || ld_hidden < hidden_size || ld_weight < hidden_size || ld_dz < cols)
     return BIL_E_INVALID_ARG;
   if ((entropy == nullptr) != (grad_entropy == nullptr)) return BIL_E_INVALID_ARG;
   {
     using bil_internal::extent_ok;
-    if (!extent_ok(n_rows, ld_hidden, 2) || !extent_ok(cols, ld_weight, 2) || !extent_ok(n_rows, ld_dz, 2) ||
-        !extent_ok(cols, ld_dz_t, 2))
+    if (!extent_ok(n_rows, ld_hidden, 2) || !extent_ok(cols, ld_weight, 2) || !extent_ok(n_rows, ld_dz, 2))
       return BIL_E_UNSUPPORTED;
   }
   if (weight == nullptr) return BIL_E_INVALID_ARG;
   if (!rows16(weight, ld_weight, 2)) return BIL_E_ALIGN;
   *cols_out = cols;
   if (n_rows == 0) return BIL_OK;
-  if (hidden == nullptr || targets == nullptr || lse == nullptr || grad_logp == nullptr || dz == nullptr ||
-      dz_t == nullptr)
+  if (hidden == nullptr || targets == nullptr || lse == nullptr || grad_logp == nullptr || dz == nullptr)
     return BIL_E_INVALID_ARG;
-  if (!rows16(hidden, ld_hidden, 2) || !rows16(dz, ld_dz, 2) || !rows16(dz_t, ld_dz_t, 2)) return BIL_E_ALIGN;
+  if (!rows16(hidden, ld_hidden, 2) || !rows16(dz, ld_dz, 2)) return BIL_E_ALIGN;
   if (!aligned_to(targets, 8) || !aligned_to(lse, 4) || !aligned_to(grad_logp, 4) ||
       (entropy && (!aligned_to(entropy, 4) || !aligned_to(grad_entropy, 4))))
     return BIL_E_ALIGN;
@@ -1243,48 +1244,28 @@ int bil_sum_f32(const float* const* srcs, int count, int64_t n, float* dst, bil_
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
-int bil_transpose_2d(const void* src, int dtype, int64_t rows, int64_t cols, int64_t ld_src, void* dst,
-                     int64_t ld_dst, bil_stream_t stream) {
-  bil_internal::NvtxRange nvtx_range("bil_transpose_2d");
-  if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
-  if (rows < 0 || cols < 0 || ld_src < cols || ld_dst < rows) return BIL_E_INVALID_ARG;
-  if (rows == 0 || cols == 0) return BIL_OK;
-  if (!bil_internal::extent_ok(rows, ld_src, 2) || !bil_internal::extent_ok(cols, ld_dst, 2))
-    return BIL_E_UNSUPPORTED;
-  if (src == nullptr || dst == nullptr) return BIL_E_INVALID_ARG;
-  if (!aligned_to(src, 2) || !aligned_to(dst, 2)) return BIL_E_ALIGN;
-  return launch_transpose16(src, rows, cols, ld_src, dst, ld_dst, reinterpret_cast<cudaStream_t>(stream));
-}
-
-int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weight_t, int dtype, int64_t n_rows,
-                        int64_t hidden_size, int64_t ld_hidden, int64_t vocab, int64_t ld_weight, int64_t ld_weight_t,
-                        int32_t tile_begin, int32_t tile_end, float temperature, const int64_t* target_ids,
-                        int64_t ignore_index, const float* lse, const float* grad_logp, const float* entropy,
-                        const float* grad_entropy, void* dz, int64_t ld_dz, void* dz_t, int64_t ld_dz_t,
-                        void* hidden_t, int64_t ld_hidden_t, void* dhidden, int dhidden_dtype, int64_t ld_dhidden,
-                        void* dweight, int dweight_dtype, int64_t ld_dweight, bil_stream_t stream) {
+int bil_linear_logp_bwd(const void* hidden, const void* weight, int dtype, int64_t n_rows, int64_t hidden_size,
+                        int64_t ld_hidden, int64_t vocab, int64_t ld_weight, int32_t tile_begin, int32_t tile_end,
+                        float temperature, const int64_t* target_ids, int64_t ignore_index, const float* lse,
+                        const float* grad_logp, const float* entropy, const float* grad_entropy, void* dz,
+                        int64_t ld_dz, void* dhidden, int dhidden_dtype, int64_t ld_dhidden, void* dweight,
+                        int dweight_dtype, int64_t ld_dweight, bil_stream_t stream) {
   bil_internal::NvtxRange nvtx_range("bil_linear_logp_bwd");
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   for (int ot : {dhidden_dtype, dweight_dtype})
     if (ot != BIL_F32 && ot != dtype) return BIL_E_DTYPE;
   int64_t cols = 0;
   if (int st = check_grad_args(hidden, weight, n_rows, hidden_size, ld_hidden, vocab, ld_weight, tile_begin, tile_end,
-                               target_ids, lse, grad_logp, entropy, grad_entropy, dz, ld_dz, dz_t, ld_dz_t, &cols))
+                               target_ids, lse, grad_logp, entropy, grad_entropy, dz, ld_dz, &cols))
     return st;
-  if (ld_weight_t < cols || ld_hidden_t < n_rows || ld_dhidden < hidden_size || ld_dweight < hidden_size)
-    return BIL_E_INVALID_ARG;
-  {
-    using bil_internal::extent_ok;
-    const int64_t eh = dhidden_dtype == BIL_F32 ? 4 : 2, ew = dweight_dtype == BIL_F32 ? 4 : 2;
-    if (!extent_ok(hidden_size, ld_weight_t, 2) || !extent_ok(hidden_size, ld_hidden_t, 2) ||
-        !extent_ok(n_rows, ld_dhidden, eh) || !extent_ok(cols, ld_dweight, ew))
-      return BIL_E_UNSUPPORTED;
-  }
+  if (ld_dhidden < hidden_size || ld_dweight < hidden_size) return BIL_E_INVALID_ARG;
+  const int64_t eo_h = dhidden_dtype == BIL_F32 ? 4 : 2, eo_w = dweight_dtype == BIL_F32 ? 4 : 2;
+  if (!bil_internal::extent_ok(n_rows, ld_dhidden, eo_h) || !bil_internal::extent_ok(cols, ld_dweight, eo_w))
+    return BIL_E_UNSUPPORTED;
   float rcp = 1.0f;
   if (int st = bil_internal::temperature_rcp(temperature, &rcp)) return st;
-  if (weight_t == nullptr || dweight == nullptr) return BIL_E_INVALID_ARG;
-  const int64_t eo_h = dhidden_dtype == BIL_F32 ? 4 : 2, eo_w = dweight_dtype == BIL_F32 ? 4 : 2;
-  if (!rows16(weight_t, ld_weight_t, 2) || !rows16(dweight, ld_dweight, eo_w)) return BIL_E_ALIGN;
+  if (dweight == nullptr) return BIL_E_INVALID_ARG;
+  if (!rows16(dweight, ld_dweight, eo_w)) return BIL_E_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (n_rows == 0) {  // dweight is a sum over no rows
     return cudaMemset2DAsync(dweight, static_cast<size_t>(ld_dweight * eo_w), 0,
@@ -1292,48 +1273,49 @@ int bil_linear_logp_bwd(const void* hidden, const void* weight, const void* weig
                ? BIL_OK
                : BIL_E_CUDA;
   }
-  if (hidden_t == nullptr || dhidden == nullptr) return BIL_E_INVALID_ARG;
-  if (!rows16(hidden_t, ld_hidden_t, 2) || !rows16(dhidden, ld_dhidden, eo_h)) return BIL_E_ALIGN;
-  if ((n_rows + 63) / 64 > 65535) return BIL_E_UNSUPPORTED;  // the transpose's grid
+  if (dhidden == nullptr) return BIL_E_INVALID_ARG;
+  if (!rows16(dhidden, ld_dhidden, eo_h)) return BIL_E_ALIGN;
 
-  // Every tensor map is encoded before anything is queued.
-  //   grad:     A = hidden [n, H],  B = weight [V, H]      (K = H)
-  //   dhidden:  A = dz [n, V],      B = weight^T [H, V]    (K = V)
-  //   dweight:  A = dz_t [V, n],    B = hidden^T [H, n]    (K = n)
+  // Every tensor map is encoded before anything is queued.  The store GEMMs
+  // read dz, weight and hidden where they lie, as MN-major operands where
+  // their rows run along K:
+  //   grad:     A = hidden [n, H],            B = weight [V, H]             (K = H)
+  //   dhidden:  A = dz [n, V],                B = weight [V, H] as [K, H]   (K = V)
+  //   dweight:  A = dz [n, V] as [K, V],      B = hidden [n, H] as [K, H]   (K = n)
   CUtensorMap maps[6];
   {
     int st = make_map(&maps[0], hidden, dtype, n_rows, hidden_size, ld_hidden, kBM);
     if (!st) st = make_map(&maps[1], weight, dtype, cols, hidden_size, ld_weight, kBN);
-    if (!st) st = make_map(&maps[2], dz, dtype, n_rows, cols, ld_dz, kBM);
-    if (!st) st = make_map(&maps[3], weight_t, dtype, hidden_size, cols, ld_weight_t, kBN);
-    if (!st) st = make_map(&maps[4], dz_t, dtype, cols, n_rows, ld_dz_t, kBM);
-    if (!st) st = make_map(&maps[5], hidden_t, dtype, hidden_size, n_rows, ld_hidden_t, kBN);
+    if (!st) st = operand_map(&maps[2], dz, dtype, n_rows, cols, ld_dz, false, kBM);
+    if (!st) st = operand_map(&maps[3], weight, dtype, hidden_size, cols, ld_weight, true, kBN);
+    if (!st) st = operand_map(&maps[4], dz, dtype, cols, n_rows, ld_dz, true, kBM);
+    if (!st) st = operand_map(&maps[5], hidden, dtype, hidden_size, n_rows, ld_hidden, true, kBN);
     if (st) return st;
   }
-  const uint32_t idesc = make_idesc(dtype == BIL_BF16);
-  // 1. hidden^T [H, n_rows], the K-major B operand of dweight = dZ^T . hidden
-  if (int st = launch_transpose16(hidden, n_rows, hidden_size, ld_hidden, hidden_t, ld_hidden_t, s)) return st;
-  // 2. dZ from the recomputed projection, stored as dz [n, V] and dz_t [V, n]
+  const bool bf16 = dtype == BIL_BF16;
+  // 1. dZ from the recomputed projection, stored as dz [n, V]
   if (int st = launch_grad(maps[0], maps[1], dtype, n_rows, hidden_size, cols, tile_begin, tile_end, rcp, target_ids,
-                           ignore_index, lse, grad_logp, entropy, grad_entropy, vocab, dz, ld_dz, dz_t, ld_dz_t, s))
+                           ignore_index, lse, grad_logp, entropy, grad_entropy, vocab, dz, ld_dz, s))
     return st;
-  // 3. dhidden = dZ . weight   (A = dz [n, V], B = weight^T [H, V], K = V)
-  if (int st = launch_store(maps[2], maps[3], n_rows, hidden_size, cols, idesc, dhidden, dhidden_dtype, ld_dhidden, s))
+  // 2. dhidden = dZ . weight
+  if (int st = launch_store(maps[2], maps[3], n_rows, hidden_size, cols, bf16, false, true, dhidden, dhidden_dtype,
+                            ld_dhidden, s))
     return st;
-  // 4. dweight = dZ^T . hidden (A = dz_t [V, n], B = hidden^T [H, n], K = n)
-  return launch_store(maps[4], maps[5], cols, hidden_size, n_rows, idesc, dweight, dweight_dtype, ld_dweight, s);
+  // 3. dweight = dZ^T . hidden
+  return launch_store(maps[4], maps[5], cols, hidden_size, n_rows, bf16, true, true, dweight, dweight_dtype,
+                      ld_dweight, s);
 }
 
 int bil_linear_logp_grad(const void* hidden, const void* weight, int dtype, int64_t n_rows, int64_t hidden_size,
                          int64_t ld_hidden, int64_t vocab, int64_t ld_weight, int32_t tile_begin, int32_t tile_end,
                          float temperature, const int64_t* target_ids, int64_t ignore_index, const float* lse,
                          const float* grad_logp, const float* entropy, const float* grad_entropy, void* dz,
-                         int64_t ld_dz, void* dz_t, int64_t ld_dz_t, bil_stream_t stream) {
+                         int64_t ld_dz, bil_stream_t stream) {
   bil_internal::NvtxRange nvtx_range("bil_linear_logp_grad");
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   int64_t cols = 0;
   if (int st = check_grad_args(hidden, weight, n_rows, hidden_size, ld_hidden, vocab, ld_weight, tile_begin, tile_end,
-                               target_ids, lse, grad_logp, entropy, grad_entropy, dz, ld_dz, dz_t, ld_dz_t, &cols))
+                               target_ids, lse, grad_logp, entropy, grad_entropy, dz, ld_dz, &cols))
     return st;
   float rcp = 1.0f;
   if (int st = bil_internal::temperature_rcp(temperature, &rcp)) return st;
@@ -1342,28 +1324,33 @@ int bil_linear_logp_grad(const void* hidden, const void* weight, int dtype, int6
   if (int st = make_map(&mh, hidden, dtype, n_rows, hidden_size, ld_hidden, kBM)) return st;
   if (int st = make_map(&mw, weight, dtype, cols, hidden_size, ld_weight, kBN)) return st;
   return launch_grad(mh, mw, dtype, n_rows, hidden_size, cols, tile_begin, tile_end, rcp, target_ids, ignore_index, lse,
-                     grad_logp, entropy, grad_entropy, vocab, dz, ld_dz, dz_t, ld_dz_t,
-                     reinterpret_cast<cudaStream_t>(stream));
+                     grad_logp, entropy, grad_entropy, vocab, dz, ld_dz, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int bil_linear_gemm_nt(const void* a, const void* b, int dtype, int64_t m, int64_t n, int64_t k, int64_t lda,
-                       int64_t ldb, void* c, int c_dtype, int64_t ldc, bil_stream_t stream) {
-  bil_internal::NvtxRange nvtx_range("bil_linear_gemm_nt");
+int bil_linear_gemm(const void* a, int a_layout, const void* b, int b_layout, int dtype, int64_t m, int64_t n,
+                    int64_t k, int64_t lda, int64_t ldb, void* c, int c_dtype, int64_t ldc, bil_stream_t stream) {
+  bil_internal::NvtxRange nvtx_range("bil_linear_gemm");
   if (dtype != BIL_BF16 && dtype != BIL_F16) return BIL_E_DTYPE;
   if (c_dtype != BIL_F32 && c_dtype != dtype) return BIL_E_DTYPE;
-  if (m < 0 || n < 0 || k < 1 || lda < k || ldb < k || ldc < n) return BIL_E_INVALID_ARG;
+  for (int layout : {a_layout, b_layout})
+    if (layout != BIL_LAYOUT_K_MAJOR && layout != BIL_LAYOUT_MN_MAJOR) return BIL_E_INVALID_ARG;
+  const bool a_mn = a_layout == BIL_LAYOUT_MN_MAJOR, b_mn = b_layout == BIL_LAYOUT_MN_MAJOR;
+  // stored shapes: A [m, k] or [k, m], B [n, k] or [k, n]
+  const int64_t a_srows = a_mn ? k : m, a_scols = a_mn ? m : k;
+  const int64_t b_srows = b_mn ? k : n, b_scols = b_mn ? n : k;
+  if (m < 0 || n < 0 || k < 1 || lda < a_scols || ldb < b_scols || ldc < n) return BIL_E_INVALID_ARG;
   const int64_t ec = c_dtype == BIL_F32 ? 4 : 2;
-  if (!bil_internal::extent_ok(m, lda, 2) || !bil_internal::extent_ok(n, ldb, 2) ||
+  if (!bil_internal::extent_ok(a_srows, lda, 2) || !bil_internal::extent_ok(b_srows, ldb, 2) ||
       !bil_internal::extent_ok(m, ldc, ec))
     return BIL_E_UNSUPPORTED;
   if (m == 0 || n == 0) return BIL_OK;
   if (a == nullptr || b == nullptr || c == nullptr) return BIL_E_INVALID_ARG;
   if (!rows16(a, lda, 2) || !rows16(b, ldb, 2) || !rows16(c, ldc, ec)) return BIL_E_ALIGN;
-  if (m > INT32_MAX - kBM || n > INT32_MAX - kBN || k > INT32_MAX - kBK) return BIL_E_UNSUPPORTED;
+  if (m > INT32_MAX - kBN || n > INT32_MAX - kBN || k > INT32_MAX - kBK) return BIL_E_UNSUPPORTED;
   CUtensorMap ma, mb;
-  if (int st = make_map(&ma, a, dtype, m, k, lda, kBM)) return st;
-  if (int st = make_map(&mb, b, dtype, n, k, ldb, kBN)) return st;
-  return launch_store(ma, mb, m, n, k, make_idesc(dtype == BIL_BF16), c, c_dtype, ldc,
+  if (int st = operand_map(&ma, a, dtype, m, k, lda, a_mn, kBM)) return st;
+  if (int st = operand_map(&mb, b, dtype, n, k, ldb, b_mn, kBN)) return st;
+  return launch_store(ma, mb, m, n, k, dtype == BIL_BF16, a_mn, b_mn, c, c_dtype, ldc,
                       reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -147,41 +147,11 @@ def _pad8(n: int) -> int:
     return -(-n // 8) * 8
 
 
-def transpose(src: torch.Tensor) -> torch.Tensor:
-    """[rows, cols] -> [cols, rows] (16-bit types), in a buffer whose rows are
-    16-byte aligned (the result is a view of its first ``rows`` columns)."""
-    _need_cuda(src)
-    s2 = src if src.stride(-1) == 1 else src.contiguous()
-    rows, cols = s2.shape
-    out = torch.empty((cols, _pad8(max(rows, 1))), dtype=s2.dtype, device=s2.device)[:, :rows]
-    _lib.check("bil_transpose_2d", _lib.load().bil_transpose_2d(
-        _ptr(s2), _in_code(s2.dtype), rows, cols, _ld(s2) if rows else cols, _ptr(out), out.stride(0),
-        _stream(s2.device)))
-    return out
-
-
-_WEIGHT_T: dict = {}
-
-
-def prepared_weight_t(weight: torch.Tensor) -> torch.Tensor:
-    """The transposed LM-head weight the backward contracts with, kept while the
-    weight is unchanged (keyed by storage, shape and the tensor's version counter:
-    an in-place update of the weight prepares it again)."""
-    key = (weight.data_ptr(), tuple(weight.shape), weight.dtype, weight.device, weight._version)
-    wt = _WEIGHT_T.get("entry")
-    if wt is not None and wt[0] == key:
-        return wt[1]
-    out = transpose(weight)
-    _WEIGHT_T["entry"] = (key, out)
-    return out
-
-
 def linear_logp_bwd(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor,
                     grad_logp: torch.Tensor, ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
                     entropy: torch.Tensor | None = None, grad_entropy: torch.Tensor | None = None,
-                    weight_t: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
-                    return_dz: bool = False, vocab: int | None = None, tile_begin: int = 0,
-                    tile_end: int | None = None):
+                    out_dtype: torch.dtype | None = None, return_dz: bool = False, vocab: int | None = None,
+                    tile_begin: int = 0, tile_end: int | None = None):
     """(dhidden [*lead, H], dweight [cols, H][, dZ [N, cols]]) of g * logp (+ gh * entropy).
 
     ``weight`` holds the LM-head rows of global vocabulary columns
@@ -189,7 +159,7 @@ def linear_logp_bwd(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torc
     whole vocabulary, vocab = weight rows).  With a shard, dhidden is the
     shard's part of the sum over the vocabulary.  ``out_dtype`` is float32 or
     the inputs' type (the default)."""
-    _need_cuda(hidden, weight, target_ids, lse, grad_logp, entropy, grad_entropy, weight_t)
+    _need_cuda(hidden, weight, target_ids, lse, grad_logp, entropy, grad_entropy)
     lead = hidden.shape[:-1]
     h2, w2 = _matrix(hidden, "hidden"), _matrix(weight, "weight")
     if h2.dtype != w2.dtype or h2.shape[1] != w2.shape[1]:
@@ -207,30 +177,27 @@ def linear_logp_bwd(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torc
         raise ValueError("entropy and grad_entropy come together")
     f32 = [x.reshape(-1).float().contiguous() if x is not None else None
            for x in (lse, grad_logp, entropy, grad_entropy)]
-    wt = prepared_weight_t(w2) if weight_t is None else weight_t
     out_dtype = h2.dtype if out_dtype is None else out_dtype
     if out_dtype not in (torch.float32, h2.dtype):
         raise TypeError("out_dtype must be float32 or the inputs' type")
     dz = torch.empty((n, _pad8(v)), dtype=h2.dtype, device=dev)[:, :v]
-    dz_t = torch.empty((v, _pad8(max(n, 1))), dtype=h2.dtype, device=dev)[:, :n]
-    h_t = torch.empty((hs, _pad8(max(n, 1))), dtype=h2.dtype, device=dev)[:, :n]
     dh = torch.empty((n, _pad8(hs)), dtype=out_dtype, device=dev)[:, :hs]
     dw = torch.empty((v, _pad8(hs)), dtype=out_dtype, device=dev)[:, :hs]
     oc = _lib.F32 if out_dtype == torch.float32 else _in_code(out_dtype)
     _lib.check("bil_linear_logp_bwd", _lib.load().bil_linear_logp_bwd(
-        _ptr(h2), _ptr(w2), _ptr(wt), _in_code(h2.dtype), n, hs, _ld(h2), vocab, _ld(w2), wt.stride(0),
-        tile_begin, tile_end, float(temperature), _ptr(t), ignore_index, _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), _ptr(f32[3]),
-        _ptr(dz), dz.stride(0), _ptr(dz_t), dz_t.stride(0), _ptr(h_t), h_t.stride(0),
-        _ptr(dh), oc, dh.stride(0), _ptr(dw), oc, dw.stride(0), _stream(dev)))
+        _ptr(h2), _ptr(w2), _in_code(h2.dtype), n, hs, _ld(h2), vocab, _ld(w2), tile_begin, tile_end,
+        float(temperature), _ptr(t), ignore_index, _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), _ptr(f32[3]),
+        _ptr(dz), dz.stride(0), _ptr(dh), oc, dh.stride(0), _ptr(dw), oc, dw.stride(0), _stream(dev)))
     out = (dh.reshape(*lead, hs), dw)
     return out + (dz,) if return_dz else out
 
 
 def linear_logp_grad(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torch.Tensor, lse: torch.Tensor,
                      grad_logp: torch.Tensor, ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
-                     entropy: torch.Tensor | None = None, grad_entropy: torch.Tensor | None = None):
-    """(dZ [N, V], dZ^T [V, N]) of g * logp (+ gh * entropy) over the whole vocabulary
-    (V = weight rows): the first step of ``linear_logp_bwd`` alone, the same bits."""
+                     entropy: torch.Tensor | None = None, grad_entropy: torch.Tensor | None = None) -> torch.Tensor:
+    """dZ [N, V] of g * logp (+ gh * entropy) over the whole vocabulary (V =
+    weight rows): the first step of ``linear_logp_bwd`` alone, the same bits.
+    The other two are ``matmul(dz, weight)`` and ``matmul(dz.t(), hidden)``."""
     _need_cuda(hidden, weight, target_ids, lse, grad_logp, entropy, grad_entropy)
     h2, w2 = _matrix(hidden, "hidden"), _matrix(weight, "weight")
     if h2.dtype != w2.dtype or h2.shape[1] != w2.shape[1]:
@@ -244,33 +211,60 @@ def linear_logp_grad(hidden: torch.Tensor, weight: torch.Tensor, target_ids: tor
     f32 = [x.reshape(-1).float().contiguous() if x is not None else None
            for x in (lse, grad_logp, entropy, grad_entropy)]
     dz = torch.empty((n, _pad8(v)), dtype=h2.dtype, device=dev)[:, :v]
-    dz_t = torch.empty((v, _pad8(max(n, 1))), dtype=h2.dtype, device=dev)[:, :n]
     _lib.check("bil_linear_logp_grad", _lib.load().bil_linear_logp_grad(
         _ptr(h2), _ptr(w2), _in_code(h2.dtype), n, hs, _ld(h2), v, _ld(w2), 0, num_tiles(v), float(temperature),
         _ptr(t), ignore_index, _ptr(f32[0]), _ptr(f32[1]), _ptr(f32[2]), _ptr(f32[3]), _ptr(dz), dz.stride(0),
-        _ptr(dz_t), dz_t.stride(0), _stream(dev)))
-    return dz, dz_t
+        _stream(dev)))
+    return dz
+
+
+def _rows_over_k(x: torch.Tensor, k_dim: int) -> tuple[torch.Tensor, int, int]:
+    """(tensor, layout, row stride) of a 2-D operand whose dimension ``k_dim`` is K, as
+    bil_linear_gemm finds it: K-major when K is the unit-stride dimension, MN-major
+    when the other one is (a transposed view of a row-major matrix), else a
+    contiguous copy with the rows over K."""
+    r_dim = 1 - k_dim
+    rows, k = x.shape[r_dim], x.shape[k_dim]
+    for layout, unit, ld_dim, run in ((_lib.LAYOUT_K_MAJOR, k_dim, r_dim, k), (_lib.LAYOUT_MN_MAJOR, r_dim, k_dim, rows)):
+        outer = x.shape[ld_dim]
+        ld = x.stride(ld_dim) if outer > 1 else max(x.stride(ld_dim), run)
+        if (x.stride(unit) == 1 or x.shape[unit] == 1) and ld >= run and (ld * 2) % 16 == 0 and x.data_ptr() % 16 == 0:
+            return x, layout, ld
+    y = x.transpose(0, 1) if k_dim == 0 else x
+    y = torch.empty((rows, _pad8(k)), dtype=x.dtype, device=x.device)[:, :k].copy_(y)
+    return y, _lib.LAYOUT_K_MAJOR, y.stride(0)
+
+
+def matmul(a: torch.Tensor, b: torch.Tensor, out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    """C = a @ b for a [m, k] and b [k, n] (both bfloat16 or both float16) on the
+    tensor cores, float32 accumulation over K blocks of 64 in order: the
+    backward's dhidden (``matmul(dz, weight)``) and dweight (``matmul(dz.t(),
+    hidden)``) contraction.  Each operand is read where it lies when one of
+    its dimensions has unit stride (a row-major matrix or a transposed view of
+    one, 16-byte aligned rows), else from a copy.  C is float32 or the inputs'
+    type."""
+    _need_cuda(a, b)
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0] or a.dtype != b.dtype:
+        raise ValueError("matmul takes a [m, k] and b [k, n] of one 16-bit type")
+    if out_dtype not in (torch.float32, a.dtype):
+        raise TypeError("out_dtype must be float32 or the inputs' type")
+    m, k = a.shape
+    n = b.shape[1]
+    c = torch.empty((m, _pad8(n)), dtype=out_dtype, device=a.device)[:, :n]
+    if m == 0 or n == 0:
+        return c
+    a2, la, lda = _rows_over_k(a, 1)
+    b2, lb, ldb = _rows_over_k(b, 0)
+    oc = _lib.F32 if out_dtype == torch.float32 else _in_code(out_dtype)
+    _lib.check("bil_linear_gemm", _lib.load().bil_linear_gemm(
+        _ptr(a2), la, _ptr(b2), lb, _in_code(a2.dtype), m, n, k, lda, ldb, _ptr(c), oc, c.stride(0),
+        _stream(a2.device)))
+    return c
 
 
 def gemm_nt(a: torch.Tensor, b: torch.Tensor, out_dtype: torch.dtype = torch.float32) -> torch.Tensor:
-    """C = a . b^T for a [m, k] and b [n, k] (both bfloat16 or both float16, rows
-    16-byte aligned) on the tensor cores, float32 accumulation over K blocks of 64
-    in order: the backward's dhidden and dweight contraction.  C is float32 or the
-    inputs' type."""
-    _need_cuda(a, b)
-    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1] or a.dtype != b.dtype:
-        raise ValueError("gemm_nt takes a [m, k] and b [n, k] of one 16-bit type")
-    if out_dtype not in (torch.float32, a.dtype):
-        raise TypeError("out_dtype must be float32 or the inputs' type")
-    a2, b2 = _matrix(a, "a"), _matrix(b, "b")
-    m, k = a2.shape
-    n = b2.shape[0]
-    c = torch.empty((m, _pad8(n)), dtype=out_dtype, device=a2.device)[:, :n]
-    oc = _lib.F32 if out_dtype == torch.float32 else _in_code(out_dtype)
-    _lib.check("bil_linear_gemm_nt", _lib.load().bil_linear_gemm_nt(
-        _ptr(a2), _ptr(b2), _in_code(a2.dtype), m, n, k, _ld(a2), _ld(b2), _ptr(c), oc, c.stride(0),
-        _stream(a2.device)))
-    return c
+    """C = a . b^T for a [m, k] and b [n, k]: ``matmul(a, b.t())``."""
+    return matmul(a, b.t(), out_dtype)
 
 
 class LinearLogp(torch.autograd.Function):

@@ -150,7 +150,7 @@ def vocab_parallel_linear_logp_bwd(hidden: torch.Tensor, weight_shard: torch.Ten
                                    lse: torch.Tensor, grad_logp: torch.Tensor, vocab: int, tile_begin: int,
                                    tile_end: int, group=None, ignore_index: int = IGNORE_INDEX,
                                    temperature: float = 1.0, entropy: torch.Tensor | None = None,
-                                   grad_entropy: torch.Tensor | None = None, weight_t: torch.Tensor | None = None):
+                                   grad_entropy: torch.Tensor | None = None):
     """Backward of vocab_parallel_linear_logp: (dhidden [N, H], dweight_shard).
 
     Each rank computes its shard's dZ, its dweight rows (bit for bit the
@@ -160,7 +160,7 @@ def vocab_parallel_linear_logp_bwd(hidden: torch.Tensor, weight_shard: torch.Ten
     (not the single-device bits: the sum over the vocabulary is split at the
     shard boundaries)."""
     dh, dw = linear_logp_bwd(hidden, weight_shard, target_ids, lse, grad_logp, ignore_index, temperature, entropy,
-                             grad_entropy, weight_t=weight_t, out_dtype=torch.float32, vocab=vocab,
+                             grad_entropy, out_dtype=torch.float32, vocab=vocab,
                              tile_begin=tile_begin, tile_end=tile_end)
     parts = _gather(dh.contiguous(), group)
     return sum_f32(parts), dw

@@ -208,79 +208,80 @@ def test_lm_head_calls_reject_extents_above_the_limit(lib):
     assert partials(vocab=2 ** 63 - 1) == _lib.E_UNSUPPORTED
     assert partials(vocab=big + 1) == _lib.E_UNSUPPORTED
 
-    assert lib.bil_transpose_2d(FAKE, _lib.BF16, 2 ** 20, 8, 2 ** 28, FAKE, 2 ** 20, NULL) == _lib.E_UNSUPPORTED
-    assert lib.bil_transpose_2d(FAKE, _lib.BF16, 8, 2 ** 20, 2 ** 20, FAKE, 2 ** 47, NULL) == _lib.E_UNSUPPORTED
-
-    def bwd(**kw):
-        a = dict(n=4, vocab=1000, ld_dz=1000, ld_dzt=8, ld_ht=8, ld_dw=64)
-        a.update(kw)
-        return lib.bil_linear_logp_bwd(FAKE, FAKE, FAKE, _lib.BF16, a["n"], 64, 64, a["vocab"], 64, 1000, 0, 4, 1.0,
-                                       FAKE, -100, FAKE, FAKE, NULL, NULL, FAKE, a["ld_dz"], FAKE, a["ld_dzt"], FAKE,
-                                       a["ld_ht"], FAKE, _lib.F32, 64, FAKE, _lib.F32, a["ld_dw"], NULL)
     def bwd_args(**kw):
-        a = dict(dtype=_lib.BF16, n=4, vocab=1000, ld_wt=1000, te=4, ent=NULL, gent=NULL, ld_dz=1000, ld_dzt=8,
-                 ld_ht=8, dh_t=_lib.F32, dw_t=_lib.F32, weight=FAKE, dweight=FAKE, dz=FAKE)
+        a = dict(dtype=_lib.BF16, n=4, vocab=1000, te=4, ent=NULL, gent=NULL, ld_dz=1000, dh_t=_lib.F32,
+                 dw_t=_lib.F32, weight=FAKE, dweight=FAKE, dhidden=FAKE, dz=FAKE, ld_dh=64, ld_dw=64)
         a.update(kw)
-        return lib.bil_linear_logp_bwd(FAKE, a["weight"], FAKE, a["dtype"], a["n"], 64, 64, a["vocab"], 64,
-                                       a["ld_wt"], 0, a["te"], 1.0, FAKE, -100, FAKE, FAKE, a["ent"], a["gent"],
-                                       a["dz"], a["ld_dz"], FAKE, a["ld_dzt"], FAKE, a["ld_ht"], FAKE, a["dh_t"], 64,
-                                       a["dweight"], a["dw_t"], 64, NULL)
+        return lib.bil_linear_logp_bwd(FAKE, a["weight"], a["dtype"], a["n"], 64, 64, a["vocab"], 64, 0, a["te"],
+                                       1.0, FAKE, -100, FAKE, FAKE, a["ent"], a["gent"], a["dz"], a["ld_dz"],
+                                       a["dhidden"], a["dh_t"], a["ld_dh"], a["dweight"], a["dw_t"], a["ld_dw"], NULL)
     assert bwd_args(dtype=_lib.F32) == _lib.E_DTYPE
     assert bwd_args(dh_t=_lib.F16) == _lib.E_DTYPE             # outputs: float32 or the input type
     assert bwd_args(dw_t=_lib.F16) == _lib.E_DTYPE
     assert bwd_args(te=5) == _lib.E_INVALID_ARG                # beyond the 4 tiles of 1000 columns
-    assert bwd_args(ld_wt=999) == _lib.E_INVALID_ARG           # W^T narrower than the shard
-    assert bwd_args(ld_dz=999) == _lib.E_INVALID_ARG
-    assert bwd_args(ld_dzt=3) == _lib.E_INVALID_ARG            # dZ^T narrower than the rows
-    assert bwd_args(ld_ht=3) == _lib.E_INVALID_ARG
+    assert bwd_args(ld_dz=999) == _lib.E_INVALID_ARG           # dZ narrower than the shard
+    assert bwd_args(ld_dh=63) == _lib.E_INVALID_ARG
+    assert bwd_args(ld_dw=63) == _lib.E_INVALID_ARG
     assert bwd_args(ent=FAKE) == _lib.E_INVALID_ARG            # entropy without its gradient
     assert bwd_args(weight=NULL) == _lib.E_INVALID_ARG
     assert bwd_args(weight=ctypes.c_void_p(0x10008)) == _lib.E_ALIGN
     assert bwd_args(dz=NULL) == _lib.E_INVALID_ARG
-    assert bwd(n=2 ** 20, ld_dz=2 ** 28, ld_dzt=2 ** 20, ld_ht=2 ** 20) == _lib.E_UNSUPPORTED  # dZ: 2^49 bytes
-    assert bwd(ld_dw=2 ** 40) == _lib.E_UNSUPPORTED                                           # dweight
-    assert bwd(vocab=2 ** 63 - 1) == _lib.E_UNSUPPORTED
+    assert bwd_args(dhidden=NULL) == _lib.E_INVALID_ARG
+    assert bwd_args(dweight=NULL) == _lib.E_INVALID_ARG
+    assert bwd_args(dhidden=ctypes.c_void_p(0x10008)) == _lib.E_ALIGN
+    assert bwd_args(dh_t=_lib.BF16, ld_dh=68) == _lib.E_ALIGN  # 136-byte rows of a 16-bit dhidden
+    assert bwd_args(n=2 ** 20, ld_dz=2 ** 28) == _lib.E_UNSUPPORTED     # dZ: 2^49 bytes
+    assert bwd_args(n=2 ** 20, ld_dh=2 ** 28) == _lib.E_UNSUPPORTED     # dhidden: 2^50 bytes
+    assert bwd_args(ld_dw=2 ** 40) == _lib.E_UNSUPPORTED                # dweight
+    assert bwd_args(vocab=2 ** 63 - 1) == _lib.E_UNSUPPORTED
 
 
-def test_gemm_nt_and_grad_check_their_arguments(lib):
-    g = lib.bil_linear_gemm_nt
-    ok = dict(a=FAKE, b=FAKE, dt=_lib.BF16, m=4, n=8, k=64, lda=64, ldb=64, c=FAKE, ct=_lib.F32, ldc=8)
+def test_gemm_and_grad_check_their_arguments(lib):
+    g = lib.bil_linear_gemm
+    K, MN = _lib.LAYOUT_K_MAJOR, _lib.LAYOUT_MN_MAJOR
+    ok = dict(a=FAKE, la=K, b=FAKE, lb=K, dt=_lib.BF16, m=4, n=8, k=64, lda=64, ldb=64, c=FAKE, ct=_lib.F32, ldc=8)
 
     def gemm(**kw):
         a = dict(ok)
         a.update(kw)
-        return g(a["a"], a["b"], a["dt"], a["m"], a["n"], a["k"], a["lda"], a["ldb"], a["c"], a["ct"], a["ldc"], NULL)
+        return g(a["a"], a["la"], a["b"], a["lb"], a["dt"], a["m"], a["n"], a["k"], a["lda"], a["ldb"], a["c"],
+                 a["ct"], a["ldc"], NULL)
     assert gemm(dt=_lib.F32) == _lib.E_DTYPE                     # 16-bit operands only
     assert gemm(ct=_lib.F16) == _lib.E_DTYPE                     # C: float32 or the operands' type
+    assert gemm(la=2) == _lib.E_INVALID_ARG                      # a layout the header does not define
+    assert gemm(lb=-1) == _lib.E_INVALID_ARG
     assert gemm(k=0) == _lib.E_INVALID_ARG
-    assert gemm(lda=63) == _lib.E_INVALID_ARG
+    assert gemm(lda=63) == _lib.E_INVALID_ARG                    # a K-major row holds k elements
     assert gemm(ldb=63) == _lib.E_INVALID_ARG
+    assert gemm(la=MN, lda=3) == _lib.E_INVALID_ARG              # an MN-major row holds m ...
+    assert gemm(lb=MN, ldb=7) == _lib.E_INVALID_ARG              # ... or n elements
+    assert gemm(la=MN, lda=8, lb=MN, ldb=8, c=FAKE_ODD) == _lib.E_ALIGN  # [k, m], [k, n] rows pass; C's base fails
     assert gemm(ldc=7) == _lib.E_INVALID_ARG
     assert gemm(m=-1) == _lib.E_INVALID_ARG
     assert gemm(m=0, a=NULL, c=NULL) == _lib.OK                  # nothing to compute
     assert gemm(a=NULL) == _lib.E_INVALID_ARG
     assert gemm(a=ctypes.c_void_p(0x10008)) == _lib.E_ALIGN      # TMA: 16-byte base
     assert gemm(k=60, lda=60, ldb=64) == _lib.E_ALIGN            # TMA: 16-byte row stride
+    assert gemm(la=MN, lda=4) == _lib.E_ALIGN                    # 8-byte rows of an MN-major A
     assert gemm(ct=_lib.BF16, ldc=12) == _lib.E_ALIGN            # 16-byte rows of C
     assert gemm(m=2 ** 20, lda=2 ** 28) == _lib.E_UNSUPPORTED     # A: 2^49 bytes
+    assert gemm(la=MN, lb=MN, k=2 ** 20, lda=2 ** 28, ldb=8) == _lib.E_UNSUPPORTED  # A stored [k, m]: 2^49 bytes
 
     def grad(**kw):
-        a = dict(dt=_lib.BF16, n=4, vocab=1000, te=4, ld_dz=1000, ld_dzt=8, dz=FAKE, temp=1.0)
+        a = dict(dt=_lib.BF16, n=4, vocab=1000, te=4, ld_dz=1000, dz=FAKE, temp=1.0)
         a.update(kw)
         return lib.bil_linear_logp_grad(FAKE, FAKE, a["dt"], a["n"], 64, 64, a["vocab"], 64, 0, a["te"], a["temp"],
-                                        FAKE, -100, FAKE, FAKE, NULL, NULL, a["dz"], a["ld_dz"], FAKE, a["ld_dzt"],
-                                        NULL)
+                                        FAKE, -100, FAKE, FAKE, NULL, NULL, a["dz"], a["ld_dz"], NULL)
     assert grad(dt=_lib.F32) == _lib.E_DTYPE
     assert grad(te=5) == _lib.E_INVALID_ARG
     assert grad(ld_dz=999) == _lib.E_INVALID_ARG
-    assert grad(ld_dzt=3) == _lib.E_INVALID_ARG
     assert grad(dz=NULL) == _lib.E_INVALID_ARG
     assert grad(temp=0.0) == _lib.E_INVALID_ARG
     assert grad(n=0, dz=NULL) == _lib.OK
-    assert grad(n=2 ** 20, ld_dz=2 ** 28, ld_dzt=2 ** 20) == _lib.E_UNSUPPORTED
+    assert grad(n=2 ** 20, ld_dz=2 ** 28) == _lib.E_UNSUPPORTED
 
 
-def test_sum_transpose_and_stream_shape_check_their_arguments(lib):
+def test_sum_and_stream_shape_check_their_arguments(lib):
     srcs = (ctypes.c_void_p * 17)(*([0x10000] * 17))
     s = lib.bil_sum_f32
     assert s(srcs, 0, 8, FAKE, NULL) == _lib.E_INVALID_ARG          # no sources
@@ -295,13 +296,6 @@ def test_sum_transpose_and_stream_shape_check_their_arguments(lib):
     assert s(srcs, 2, 8, ctypes.c_void_p(0x10001), NULL) == _lib.E_ALIGN
     assert s(srcs, 16, 0, FAKE, NULL) == _lib.OK                    # nothing to add
 
-    t = lib.bil_transpose_2d
-    assert t(FAKE, _lib.F32, 4, 4, 4, FAKE, 4, NULL) == _lib.E_DTYPE  # 16-bit elements only
-    assert t(FAKE, _lib.BF16, 4, 5, 4, FAKE, 4, NULL) == _lib.E_INVALID_ARG   # ld_src < cols
-    assert t(FAKE, _lib.BF16, 5, 4, 4, FAKE, 4, NULL) == _lib.E_INVALID_ARG   # ld_dst < rows
-    assert t(FAKE, _lib.BF16, 4, 4, 4, FAKE_ODD, 4, NULL) == _lib.E_ALIGN
-    assert t(NULL, _lib.F16, 4, 4, 4, FAKE, 4, NULL) == _lib.E_INVALID_ARG
-    assert t(NULL, _lib.F16, 0, 4, 4, NULL, 4, NULL) == _lib.OK        # empty
 
     st, co, sm = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int64(0)
     shape = lib.bil_stream_shape

@@ -1,13 +1,14 @@
 """The fused LM-head backward's steps as separate calls, and its store GEMM.
 
-bil_linear_logp_bwd is a transpose of the hidden states, the gradient pass
-(dZ from the recomputed projection) and two store GEMMs C = A . B^T.  Queued
-one by one through bil_transpose_2d, bil_linear_logp_grad and
-bil_linear_gemm_nt they must give the same bits; the store GEMM alone must
-match the oracle's float64 product, and a row's bits must not depend on the
-shape of the work unit that computed it; and store GEMMs running at once on two
-streams (whose copy threads keep in step through one shared position table)
-must give the bits they give one at a time.
+bil_linear_logp_bwd is the gradient pass (dZ from the recomputed projection)
+and two store GEMMs C = A . B^T that read dZ, the weight and the hidden states
+where they lie (K-major or MN-major).  Queued one by one through
+bil_linear_logp_grad and bil_linear_gemm they must give the same bits; the
+store GEMM alone must match the oracle's float64 product, and a row's bits must
+depend neither on the operands' layouts nor on the shape of the work unit that
+computed it; and store GEMMs running at once on two streams (whose copy threads
+keep in step through one shared position table) must give the bits they give
+one at a time.
 
 "[RFC][ROCm] End-to-end optimization of bitwise VIME R/R beyond native P/P",
 section "Workstream 3" (the autograd actor path: fixed-order contractions).
@@ -49,16 +50,56 @@ def test_backward_steps_one_by_one_give_the_backwards_bits(dtype, temp, entropy)
     gh = torch.from_numpy(wl.rng(41, 3).standard_normal(n).astype(np.float32)).cuda() if entropy else None
     dh, dw, dz = bil.linear_logp_bwd(xd, wd, td, lse, g, temperature=temp, entropy=ent, grad_entropy=gh,
                                      out_dtype=torch.float32, return_dz=True)
-    dz2, dz_t2 = bil.linear_logp_grad(xd, wd, td, lse, g, temperature=temp, entropy=ent, grad_entropy=gh)
-    w_t = bil.linear.transpose(wd)
-    x_t = bil.linear.transpose(xd)
-    dh2 = bil.gemm_nt(dz2, w_t)
-    dw2 = bil.gemm_nt(dz_t2, x_t)
+    dz2 = bil.linear_logp_grad(xd, wd, td, lse, g, temperature=temp, entropy=ent, grad_entropy=gh)
+    dh2 = bil.matmul(dz2, wd)
+    dw2 = bil.matmul(dz2.t(), xd)
     torch.cuda.synchronize()
     assert torch.equal(dz.contiguous().view(torch.int16), dz2.contiguous().view(torch.int16))
-    assert torch.equal(dz_t2.t().contiguous().view(torch.int16), dz2.contiguous().view(torch.int16))
     assert np.array_equal(f32_bits(dh), f32_bits(dh2))
     assert np.array_equal(f32_bits(dw), f32_bits(dw2))
+
+
+def _row_major(x):
+    """A row-major copy of x whose rows are padded to 8 elements (16 bytes)."""
+    rows, cols = x.shape
+    return torch.empty((rows, -(-cols // 8) * 8), dtype=x.dtype, device=x.device)[:, :cols].copy_(x)
+
+
+def _layouts(a, b):
+    """The operands of a . b^T (a [m, k], b [n, k]) as matmul takes them, each in both
+    layouts: K-major (K the unit-stride dimension) and MN-major (a transposed view of
+    a row-major [k, rows] copy)."""
+    return {"a": {"K": a, "MN": _row_major(a.t()).t()}, "b": {"K": b.t(), "MN": _row_major(b.t())}}
+
+
+@pytest.mark.parametrize("m,n,k", [(520, 264, 1000), (136, 72, 200), (8, 8, 8), (1, 520, 64)])
+def test_matmul_gives_the_same_bits_for_every_operand_layout(m, n, k):
+    """C[i, j] sums A(i, k) B(j, k) over its K blocks in the same order whichever way
+    each operand is stored, so the four layout pairs give one set of bits."""
+    a = _dev(wl.linear_hidden(m, k, seed=71), "bfloat16")
+    b = _dev(wl.linear_weight(n, k, seed=72), "bfloat16")
+    ops = _layouts(a, b)
+    assert ops["a"]["MN"].stride(0) == 1 and ops["b"]["MN"].stride(1) == 1
+    ref = bil.gemm_nt(a, b)
+    outs = {(la, lb): bil.matmul(ops["a"][la], ops["b"][lb]) for la in ("K", "MN") for lb in ("K", "MN")}
+    torch.cuda.synchronize()
+    for key, c in outs.items():
+        assert np.array_equal(f32_bits(c), f32_bits(ref)), key
+
+
+@pytest.mark.parametrize("m,n,k", [(333, 520, 1000), (300, 260, 66000)])
+def test_matmul_of_mn_major_operands_against_the_oracle(m, n, k):
+    """Both operands MN-major, against the oracle's float64 product, with the
+    accumulation bound for K terms; K = 66000 (1032 blocks) keeps the copy threads in step."""
+    a = wl.linear_hidden(m, k, seed=73)
+    b = wl.linear_weight(n, k, seed=74)
+    ref = oracle.linear_logits(a, b, "bfloat16")
+    bound = (np.abs(oracle.widen(a, "bfloat16")) @ np.abs(oracle.widen(b, "bfloat16")).T) * (k / 4 * 2.0 ** -24) + 1e-6
+    ops = _layouts(_dev(a, "bfloat16"), _dev(b, "bfloat16"))
+    c = bil.matmul(ops["a"]["MN"], ops["b"]["MN"])
+    torch.cuda.synchronize()
+    err = np.abs(c.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), float((err / bound).max())
 
 
 @pytest.mark.parametrize("m,n,k,dtype", [(333, 520, 1000, "bfloat16"), (128, 256, 64, "float16"),
