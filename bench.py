@@ -474,7 +474,41 @@ def host_link_probe(x_host, x_dev, out_host, dev, rows_per_copy: int = 4096, rep
     return {"h2d_gbs": reps * nbytes / t_h2d / 1e9, "d2h_gbs": reps * nbytes / t_d2h / 1e9,
             "both_gbs": 2 * reps * nbytes / t_both / 1e9, "bytes_per_copy": nbytes, "reps": reps,
             "how": "pinned host <-> device tensor copies on their own streams, host wall clock around "
-                   "synchronised batches"}
+                   "synchronised batches",
+            "trace": host_link_trace(x_host, x_dev, out_host, dev)}
+
+
+def host_link_trace(x_host, x_dev, out_host, dev, iters: int = 40):
+    """The host link alone over about a second, without the library: each iteration copies the whole
+    pinned host logits to the device and the whole device logits back (the end-to-end step's bytes,
+    one copy per direction on its own stream), timed with CUDA events.  Iterations well above the
+    median show stalls of the link itself, which the end-to-end steps meet as well."""
+    import torch
+    cur = torch.cuda.current_stream(dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def it():
+        s1.wait_stream(cur)
+        s2.wait_stream(cur)
+        with torch.cuda.stream(s1):
+            x_dev.copy_(x_host, non_blocking=True)   # the same bytes the device copy already holds
+        with torch.cuda.stream(s2):
+            out_host.copy_(x_dev, non_blocking=True)
+        cur.wait_stream(s1)
+        cur.wait_stream(s2)
+    it()
+    torch.cuda.synchronize(dev)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+    marks[0].record(cur)
+    for i in range(iters):
+        it()
+        marks[i + 1].record(cur)
+    torch.cuda.synchronize(dev)
+    ms = [round(marks[i].elapsed_time(marks[i + 1]), 2) for i in range(iters)]
+    med = statistics.median(ms)
+    return {"iter_ms": ms, "median_ms": med, "mean_ms": statistics.mean(ms),
+            "stalled_iters": sum(m > 1.5 * med for m in ms),
+            "bytes_per_iter": 2 * x_host.numel() * x_host.element_size()}
 
 
 def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_bytes, stream, dev):
@@ -771,7 +805,10 @@ def run_bil(args):
         pipe = bil.HostStreamedLogp(n, v, torch.bfloat16, torch.bfloat16, chunk_rows=2048, device=dev)
 
         def e2e_step():
-            return pipe.run(x_host, t_host, g_host, logp_host, d_host, w.ignore_index, w.tile_v)
+            # the host inputs are written by the CPU once: no queued work produces them, so each
+            # step's copies in may start while the step before is still copying out
+            return pipe.run(x_host, t_host, g_host, logp_host, d_host, w.ignore_index, w.tile_v,
+                            order_inputs=False)
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize(dev)
@@ -796,7 +833,8 @@ def run_bil(args):
         e2e = {"value": rows_total * args.e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps,
-               "path": "HostStreamedLogp: pinned host -> 2048-row chunks over 3 streams -> pinned host",
+               "path": "HostStreamedLogp: pinned host -> 2048-row chunks over 3 streams -> pinned host; a "
+                       "step's copies in overlap the step before's copies out",
                "host_link_gbs": (h2d + d2h) / (e2e_ms / args.e2e_steps / 1e3) / 1e9,
                "gpu_launches": launches, "step_ms": step_ms,
                "step_ms_median": statistics.median(step_ms),

@@ -37,19 +37,31 @@ class HostStreamedLogp:
         self.s_in = torch.cuda.Stream(dev)
         self.s_comp = torch.cuda.Stream(dev)
         self.s_out = torch.cuda.Stream(dev)
+        # per chunk buffer, kept from one call to the next: its inputs have been
+        # read by the kernels (computed) and its outputs copied out (drained)
+        self._computed = [None, None]
+        self._drained = [None, None]
 
     def run(self, logits_h: torch.Tensor, target_h: torch.Tensor, grad_h: torch.Tensor, logp_h: torch.Tensor,
-            dlogits_h: torch.Tensor, ignore_index: int = IGNORE_INDEX, tile_v: int = DEFAULT_TILE_V) -> int:
+            dlogits_h: torch.Tensor, ignore_index: int = IGNORE_INDEX, tile_v: int = DEFAULT_TILE_V,
+            order_inputs: bool = True) -> int:
         """Queue the whole batch; returns the number of CUDA-library kernel launches queued.
 
-        The caller's current stream waits for the last copy out."""
+        The caller's current stream waits for the last copy out.  With
+        ``order_inputs`` (the default) the batch's copies and kernels also wait
+        for the work already queued on the caller's stream, as if they ran on
+        it.  ``order_inputs=False`` drops that wait, for host inputs that the
+        CPU wrote (no queued work produces them): the next batch's copies in
+        then overlap this batch's last copies out, and the chunk buffers are
+        guarded by the pipeline's own events."""
         n, c = self.n_rows, self.chunk
         cur = torch.cuda.current_stream(self.device)
-        for s in (self.s_in, self.s_comp, self.s_out):
-            s.wait_stream(cur)
+        if order_inputs:
+            for s in (self.s_in, self.s_comp, self.s_out):
+                s.wait_stream(cur)
         loaded = [None, None]      # event: chunk buffer b holds its inputs
-        computed = [None, None]    # event: chunk buffer b holds its outputs
-        drained = [None, None]     # event: chunk buffer b's outputs are copied out
+        computed = self._computed  # event: chunk buffer b holds its outputs
+        drained = self._drained    # event: chunk buffer b's outputs are copied out
         launches = 0
         for i, r0 in enumerate(range(0, n, c)):
             r1 = min(n, r0 + c)
