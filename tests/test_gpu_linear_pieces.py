@@ -72,12 +72,15 @@ def _layouts(a, b):
     return {"a": {"K": a, "MN": _row_major(a.t()).t()}, "b": {"K": b.t(), "MN": _row_major(b.t())}}
 
 
-@pytest.mark.parametrize("m,n,k", [(520, 264, 1000), (136, 72, 200), (8, 8, 8), (1, 520, 64)])
-def test_matmul_gives_the_same_bits_for_every_operand_layout(m, n, k):
+@pytest.mark.parametrize("m,n,k,dtype", [(520, 264, 1000, "bfloat16"), (136, 72, 200, "bfloat16"),
+                                         (8, 8, 8, "bfloat16"), (1, 520, 64, "bfloat16"), (3, 24, 40, "float16"),
+                                         (300, 136, 130, "float16")])
+def test_matmul_gives_the_same_bits_for_every_operand_layout(m, n, k, dtype):
     """C[i, j] sums A(i, k) B(j, k) over its K blocks in the same order whichever way
-    each operand is stored, so the four layout pairs give one set of bits."""
-    a = _dev(wl.linear_hidden(m, k, seed=71), "bfloat16")
-    b = _dev(wl.linear_weight(n, k, seed=72), "bfloat16")
+    each operand is stored, so the four layout pairs give one set of bits (ragged K,
+    rows fewer than a 64-row box, one-half and two-half work units)."""
+    a = _dev(wl.linear_hidden(m, k, seed=71, dtype=dtype), dtype)
+    b = _dev(wl.linear_weight(n, k, seed=72, dtype=dtype), dtype)
     ops = _layouts(a, b)
     assert ops["a"]["MN"].stride(0) == 1 and ops["b"]["MN"].stride(1) == 1
     ref = bil.gemm_nt(a, b)
