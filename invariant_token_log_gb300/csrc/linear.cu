@@ -10,8 +10,8 @@
 // the tiles are then merged in the operator's one fixed order (the library's
 // merge kernel).  The C ABI is declared in include/bil.h.
 //
-// One GEMM body C = A . B^T (both operands K-major, 16-bit), persistent, one
-// block per SM, warp-specialised:
+// One GEMM body C = A . B^T (16-bit operands), persistent, one block per SM,
+// warp-specialised:
 //   warp 0      TMA producer: 128-row A tile and 256-row B tile per 64-element
 //               K block, 128-byte swizzled, into a 4-stage ring;
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16/fp16 in, fp32
@@ -19,7 +19,8 @@
 //               four K=16 steps each; two accumulator buffers of 256 columns;
 //   warps 2-5   epilogue: thread i of the warp reading lanes [32q, 32q+32)
 //               owns row 32q+i of the tile and reads its 256 columns from
-//               tensor memory.
+//               tensor memory;
+//   warp 6      the store GEMMs' lockstep service (see lockstep_service).
 // The accumulator of one tile is read while the next tile's MMAs run.  Three
 // epilogues make three kernels:
 //   linear_partials_kernel   forward: A = hidden, B = weight; the tile's
@@ -27,13 +28,15 @@
 //                            logits);
 //   linear_grad_kernel       backward: the same projection recomputed; dZ by
 //                            the logits path's gradient formula, stored as
-//                            [rows, vocab] and [vocab, rows];
-//   linear_store_kernel      backward: dhidden = dZ . W (B = the prepared W^T)
-//                            and dweight = dZ^T . hidden (B = hidden^T),
-//                            stored as they are; from 256 rows on its work
-//                            unit is two 128-row A tiles sharing one B tile
-//                            (a 3-stage ring of 64 KB stages, both
-//                            accumulators in tensor memory at once).
+//                            [rows, vocab];
+//   linear_store_kernel      backward: dhidden = dZ . W and dweight =
+//                            dZ^T . hidden, stored as they are.  Each operand
+//                            is read where it lies, K-major ([rows, K]) or
+//                            MN-major ([K, rows], copied in 64 x 64 boxes);
+//                            from 256 rows on the work unit is two 128-row A
+//                            tiles sharing one B tile (a 3-stage ring of
+//                            64 KB stages, both accumulators in tensor memory
+//                            at once).
 //
 // What fixes the bits of z[r, c] is the K order (K blocks in order, four
 // K=16 steps each, from a zeroed accumulator), the same for every row and
@@ -452,8 +455,14 @@ __device__ __forceinline__ void row_store(uint32_t taddr, int vcols, bool valid,
 #define BIL_STORE_HALVES 2
 #endif
 
-constexpr int kSyncLead = 64;
-constexpr int kSyncMinKBlocks = 1024;      // the shortest K (in blocks of kBK) that keeps step
+#ifndef BIL_STORE_SYNC_LEAD
+#define BIL_STORE_SYNC_LEAD 64
+#endif
+#ifndef BIL_STORE_SYNC_MIN_KBLOCKS
+#define BIL_STORE_SYNC_MIN_KBLOCKS 1024
+#endif
+constexpr int kSyncLead = BIL_STORE_SYNC_LEAD;                // K blocks a copy thread may run ahead
+constexpr int kSyncMinKBlocks = BIL_STORE_SYNC_MIN_KBLOCKS;   // the shortest K (in blocks of kBK) that keeps step
 constexpr int kSyncMaxBlocks = 1024;
 constexpr long long kSyncWaitNs = 50000;   // 50 us
 constexpr unsigned kSyncPollNs = 4000;     // the service warp's pause between two updates
