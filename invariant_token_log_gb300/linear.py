@@ -253,6 +253,8 @@ def matmul(a: torch.Tensor, b: torch.Tensor, out_dtype: torch.dtype = torch.floa
     c = torch.empty((m, _pad8(n)), dtype=out_dtype, device=a.device)[:, :n]
     if m == 0 or n == 0:
         return c
+    if k == 0:
+        raise ValueError("matmul needs k >= 1 (the library computes no empty sums)")
     a2, la, lda = _rows_over_k(a, 1)
     b2, lb, ldb = _rows_over_k(b, 0)
     oc = _lib.F32 if out_dtype == torch.float32 else _in_code(out_dtype)
