@@ -183,7 +183,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 // atoms.
 constexpr int kMnBox = 64;                                // rows (and K) per box of an MN-major operand
 constexpr uint32_t kMnBoxBytes = kMnBox * kBK * 2;        // 8 KB
-static_assert(kMnBox == kBK, "make_map's box is kBK elements wide: an MN-major box's 64 rows");
 __device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr) {
   return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(kMnBoxBytes >> 4) << 16) |
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
