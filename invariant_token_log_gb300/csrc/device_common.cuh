@@ -22,6 +22,34 @@ __device__ __forceinline__ float ex2_approx(float a) {
   return r;
 }
 
+// Packed float32 pairs (sm_100 family): each half is an independent IEEE
+// round-to-nearest operation, bit for bit what __fadd_rn / __fsub_rn /
+// __fmul_rn give.  A pair is held as a 64-bit word, first element low.
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ float lo_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a)); }
+__device__ __forceinline__ float hi_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a >> 32)); }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 // Programmatic dependent launch.  A kernel launched with programmatic stream
 // serialization may be scheduled while the kernel before it in the stream is
 // still finishing.  griddep_wait() returns once that kernel has completed and

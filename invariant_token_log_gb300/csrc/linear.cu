@@ -323,16 +323,46 @@ __device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp
     a[j] = 0.0f;
     u[j] = 0.0f;
   }
+  if constexpr (ENT) {
+    // The entropy variant runs this pass on packed float32 pairs (faster there;
+    // the plain variant is as fast in the scalar form): slot pair q holds slots
+    // (2q, 2q + 1), and columns c0 + 2k, c0 + 2k + 1 go to pair k % 4 in column
+    // order, so each slot's operations are the scalar form's, in its order.
+    uint64_t a2[4] = {0, 0, 0, 0}, u2[4] = {0, 0, 0, 0};
+    const uint64_t shift2 = pk(shift, shift), c2 = pk(c, c);
 #pragma unroll 1
-  for (int c0 = 0; c0 < kBN; c0 += kChunk) {
-    tmem_ld32(taddr + c0, r);
+    for (int c0 = 0; c0 < kBN; c0 += kChunk) {
+      tmem_ld32(taddr + c0, r);
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      const float t = __fmul_rn(__fsub_rn(__uint_as_float(r[j]), shift), c);
-      float e = ex2_approx(t);
-      if (c0 + j >= vcols) e = 0.0f;  // columns past the vocabulary add nothing
-      a[j % 8] = __fadd_rn(a[j % 8], e);
-      if (ENT) u[j % 8] = __fmaf_rn(e, fmaxf(t, kNegMax), u[j % 8]);
+      for (int k = 0; k < kChunk / 2; ++k) {
+        const uint64_t x = static_cast<uint64_t>(r[2 * k]) | (static_cast<uint64_t>(r[2 * k + 1]) << 32);
+        const uint64_t t = mul2(sub2(x, shift2), c2);
+        float e0 = ex2_approx(lo_of(t)), e1 = ex2_approx(hi_of(t));
+        if (c0 + 2 * k >= vcols) e0 = 0.0f;  // columns past the vocabulary add nothing
+        if (c0 + 2 * k + 1 >= vcols) e1 = 0.0f;
+        const uint64_t e = pk(e0, e1);
+        a2[k % 4] = add2(a2[k % 4], e);
+        u2[k % 4] = fma2(e, pk(fmaxf(lo_of(t), kNegMax), fmaxf(hi_of(t), kNegMax)), u2[k % 4]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      a[2 * q] = lo_of(a2[q]);
+      a[2 * q + 1] = hi_of(a2[q]);
+      u[2 * q] = lo_of(u2[q]);
+      u[2 * q + 1] = hi_of(u2[q]);
+    }
+  } else {
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBN; c0 += kChunk) {
+      tmem_ld32(taddr + c0, r);
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        const float t = __fmul_rn(__fsub_rn(__uint_as_float(r[j]), shift), c);
+        float e = ex2_approx(t);
+        if (c0 + j >= vcols) e = 0.0f;  // columns past the vocabulary add nothing
+        a[j % 8] = __fadd_rn(a[j % 8], e);
+      }
     }
   }
   s_out = __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
