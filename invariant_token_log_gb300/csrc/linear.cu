@@ -101,7 +101,16 @@ struct alignas(8) LinearSmem {
   int sync_done;
 };
 
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * size_t(kStageBytes) + sizeof(LinearSmem);
+// The gradient pass stores dZ through shared memory with TMA (1) or with
+// per-thread vector stores (0).
+#ifndef BIL_GRAD_TMA_STORE
+#define BIL_GRAD_TMA_STORE 1
+#endif
+constexpr int kStoreBox = 32;  // rows and columns of one dZ store box: a warp's rows, one TMEM chunk
+constexpr uint32_t kStoreBoxBytes = kStoreBox * kStoreBox * 2;           // 2 KB of 16-bit elements
+constexpr size_t kStagingBytes = BIL_GRAD_TMA_STORE ? 4 * 2 * kStoreBoxBytes : 0;  // 4 warps x 2 buffers
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * size_t(kStageBytes) + sizeof(LinearSmem) +
+                              (BIL_GRAD_TMA_STORE ? 1024 + kStagingBytes : 0);
 
 // What the epilogue warps do with a finished accumulator tile.
 enum EpilogueMode {
@@ -196,6 +205,21 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
+
+// One box from shared memory to global memory (the tensor map's box; parts
+// past the matrix are not written), in this thread's current bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until at most one of this thread's bulk groups still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -424,6 +448,49 @@ __device__ __forceinline__ void row_grad(uint32_t taddr, int vcols, float rcp, i
   }
 }
 
+// The same gradient tile through shared memory: chunk by chunk (32 columns),
+// the warp's 32 rows go into one of its two 2 KB staging boxes (row-major,
+// lane i's row at 64 i bytes), and lane 0 stores the box to dz with TMA at
+// (column x0 + chunk, row y0); rows and columns past the matrix are not
+// written.  `issued` counts the warp's boxes (it picks the buffer).
+template <bool ENT, int DT>
+__device__ __forceinline__ void row_grad_tma(uint32_t taddr, int vcols, float rcp, int64_t tloc, bool active,
+                                             bool bad_target, const RowMeta& meta, unsigned char* staging,
+                                             const CUtensorMap* map, int x0, int y0, int lane, uint32_t& issued) {
+  uint32_t r[kChunk];
+  float d[kChunk];
+  const int nchunks = (vcols + kChunk - 1) / kChunk;  // chunks past the vocabulary hold no column
+#pragma unroll 1
+  for (int c0 = 0; c0 < kBN; c0 += kChunk) {
+    tmem_ld32(taddr + c0, r);
+    if (c0 / kChunk >= nchunks) continue;
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      float v = 0.0f;
+      if (active) v = grad_elem(__uint_as_float(r[j]), meta, c0 + j == tloc, rcp, ENT);
+      if (bad_target) v = __int_as_float(0x7fc00000);
+      d[j] = v;
+    }
+    unsigned char* box = staging + (issued & 1u) * kStoreBoxBytes;
+    if (lane == 0) bulk_wait_read_1();  // the store that used this buffer two boxes ago has read it
+    __syncwarp();
+    uint32_t pk16[kChunk / 2];
+#pragma unroll
+    for (int j = 0; j < kChunk; j += 2)
+      pk16[j / 2] = static_cast<uint32_t>(to16<DT>(d[j])) | (static_cast<uint32_t>(to16<DT>(d[j + 1])) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(box + lane * (kStoreBox * 2));
+#pragma unroll
+    for (int j = 0; j < kChunk / 8; ++j) dst[j] = make_uint4(pk16[4 * j], pk16[4 * j + 1], pk16[4 * j + 2], pk16[4 * j + 3]);
+    fence_proxy_async_smem();  // the writes above, before the bulk copy reads them
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, x0 + c0, y0, box);
+      bulk_commit();
+    }
+    ++issued;
+  }
+}
+
 // One row of C = A . B^T as it is: float32, or rounded to 16 bits.
 template <int OT>
 __device__ __forceinline__ void row_store(uint32_t taddr, int vcols, bool valid, unsigned char* out_row) {
@@ -578,7 +645,7 @@ __device__ __forceinline__ bool lockstep_gate(LinearSmem& sm, uint32_t pos) {
 // K=16 steps each: the same bits as with HALVES = 1.
 template <int MODE, bool ENT, int DT, int HALVES = 1>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const CUtensorMap& tmap_weight,
-                                          const LinearParams& p) {
+                                          const CUtensorMap& tmap_out, const LinearParams& p) {
   static_assert(HALVES == 1 || (HALVES == 2 && MODE == kModeStore), "two-half units are for the store epilogue");
   constexpr unsigned kStageBytesH = HALVES * kStageABytes + kStageBBytes;
   constexpr int kStagesH = static_cast<int>(kStages * size_t(kStageBytes) / kStageBytesH);  // 4, or 3 of 64 KB
@@ -726,6 +793,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
     const int q = warp & 3;  // this warp reads tensor-memory lanes [32q, 32q + 32)
     const int row_in_tile = q * 32 + lane;
     int local = 0;
+    uint32_t store_boxes = 0;  // dZ boxes this warp has handed to TMA
     for (int64_t u = blockIdx.x; u < total; u += gridDim.x, ++local) {
       int m, n;
       unit_coords(u, p.num_m, p.num_n, p.m_group, m, n);
@@ -775,8 +843,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
         const int64_t tloc = active ? meta.target - gcol0 : -1;
         if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
         tc_fence_after();
+#if BIL_GRAD_TMA_STORE
+        unsigned char* staging = reinterpret_cast<unsigned char*>(
+                                     (reinterpret_cast<uintptr_t>(&sm + 1) + 1023) & ~static_cast<uintptr_t>(1023)) +
+                                 q * 2 * kStoreBoxBytes;
+        row_grad_tma<ENT, DT>(taddr, vcols, p.rcp, tloc, active, bad_target, meta, staging, &tmap_out,
+                              static_cast<int>(col0), static_cast<int>(m * kBM + q * 32), lane, store_boxes);
+#else
         uint16_t* dz_row = valid ? reinterpret_cast<uint16_t*>(p.dz) + row * p.ld_dz + col0 : nullptr;
         row_grad<ENT, DT>(taddr, vcols, p.rcp, tloc, valid, active, bad_target, meta, dz_row);
+#endif
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
@@ -796,6 +872,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
         if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
       }
     }
+    // the staging boxes stay in use until their stores have completed
+    if (MODE == kModeGrad && BIL_GRAD_TMA_STORE && lane == 0 && store_boxes != 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -812,16 +890,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
 template <bool ENT>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_partials_kernel(const __grid_constant__ CUtensorMap tmap_hidden,
-                           const __grid_constant__ CUtensorMap tmap_weight, const LinearParams p) {
-  gemm_body<kModePartials, ENT, 0>(tmap_hidden, tmap_weight, p);
+                           const __grid_constant__ CUtensorMap tmap_weight,
+                           const __grid_constant__ CUtensorMap tmap_out, const LinearParams p) {
+  gemm_body<kModePartials, ENT, 0>(tmap_hidden, tmap_weight, tmap_out, p);
 }
 
 // Backward, first pass: hidden . weight^T recomputed, dZ stored (16-bit DT).
 template <bool ENT, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_grad_kernel(const __grid_constant__ CUtensorMap tmap_hidden, const __grid_constant__ CUtensorMap tmap_weight,
-                       const LinearParams p) {
-  gemm_body<kModeGrad, ENT, DT>(tmap_hidden, tmap_weight, p);
+                       const __grid_constant__ CUtensorMap tmap_dz, const LinearParams p) {
+  gemm_body<kModeGrad, ENT, DT>(tmap_hidden, tmap_weight, tmap_dz, p);
 }
 
 // Backward, the two contractions of dZ: C = A . B^T stored as OT, in work
@@ -829,8 +908,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int OT, int HALVES>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_store_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                        const LinearParams p) {
-  gemm_body<kModeStore, false, OT, HALVES>(tmap_a, tmap_b, p);
+                        const __grid_constant__ CUtensorMap tmap_out, const LinearParams p) {
+  gemm_body<kModeStore, false, OT, HALVES>(tmap_a, tmap_b, tmap_out, p);
 }
 
 // dst[i] = ((src_0[i] + src_1[i]) + src_2[i]) + ... , sources in order.
@@ -890,13 +969,32 @@ int make_map(CUtensorMap* map, const void* ptr, int dtype, int64_t rows, int64_t
   return r == CUDA_SUCCESS ? BIL_OK : BIL_E_CUDA;
 }
 
+// The tensor map the gradient pass stores dZ [rows, cols] (row stride ld
+// elements, 16-bit) through: boxes of kStoreBox x kStoreBox elements, no
+// swizzle (a box in shared memory is row-major, 64-byte rows).
+int make_store_map(CUtensorMap* map, void* ptr, int dtype, int64_t rows, int64_t cols, int64_t ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return BIL_E_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStoreBox), static_cast<cuuint32_t>(kStoreBox)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == BIL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = fn(map, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BIL_OK : BIL_E_CUDA;
+}
+
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-typedef void (*GemmKernel)(CUtensorMap, CUtensorMap, LinearParams);
+typedef void (*GemmKernel)(CUtensorMap, CUtensorMap, CUtensorMap, LinearParams);
 
 // One persistent block per SM (at most one per work unit).
-int launch_gemm(GemmKernel kernel, const CUtensorMap& mh, const CUtensorMap& mw, const LinearParams& p,
-                cudaStream_t stream) {
+// mo: the output's tensor map for an epilogue that stores with TMA (the
+// gradient pass's dZ), else any valid map (unused).
+int launch_gemm(GemmKernel kernel, const CUtensorMap& mh, const CUtensorMap& mw, const CUtensorMap& mo,
+                const LinearParams& p, cudaStream_t stream) {
   int sms = 0, smem_optin = 0;
   if (int st = bil_internal::device_limits(&sms, &smem_optin)) return st;
   if (static_cast<size_t>(smem_optin) < kSmemBytes) return BIL_E_UNSUPPORTED;
@@ -905,7 +1003,7 @@ int launch_gemm(GemmKernel kernel, const CUtensorMap& mh, const CUtensorMap& mw,
     return BIL_E_CUDA;
   const int64_t total = static_cast<int64_t>(p.num_m) * p.num_n;
   const int grid = static_cast<int>(std::min<int64_t>(total, sms));
-  kernel<<<grid, kThreads, kSmemBytes, stream>>>(mh, mw, p);
+  kernel<<<grid, kThreads, kSmemBytes, stream>>>(mh, mw, mo, p);
   return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
 }
 
@@ -1050,7 +1148,7 @@ int launch_store(const CUtensorMap& ma, const CUtensorMap& mb, int64_t a_rows, i
     kern = out_dtype == BIL_F32    ? linear_store_kernel<BIL_F32, 1>
            : out_dtype == BIL_BF16 ? linear_store_kernel<BIL_BF16, 1>
                                    : linear_store_kernel<BIL_F16, 1>;
-  return launch_gemm(kern, ma, mb, p, s);
+  return launch_gemm(kern, ma, mb, mb, p, s);
 }
 
 // A store GEMM operand with `rows` rows (M or N) over K = k: stored [rows, k]
@@ -1090,7 +1188,11 @@ int launch_grad(const CUtensorMap& mh, const CUtensorMap& mw, int dtype, int64_t
   const bool ent = entropy != nullptr;
   GemmKernel k = dtype == BIL_BF16 ? (ent ? linear_grad_kernel<true, BIL_BF16> : linear_grad_kernel<false, BIL_BF16>)
                                    : (ent ? linear_grad_kernel<true, BIL_F16> : linear_grad_kernel<false, BIL_F16>);
-  return launch_gemm(k, mh, mw, p, s);
+  CUtensorMap mdz = mw;
+  if (BIL_GRAD_TMA_STORE) {
+    if (int st = make_store_map(&mdz, dz, dtype, n_rows, cols, ld_dz)) return st;
+  }
+  return launch_gemm(k, mh, mw, mdz, p, s);
 }
 
 // Host-side checks of the gradient pass's arguments (those bil_linear_logp_bwd
@@ -1221,7 +1323,8 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
   p.a_box_bytes = static_cast<unsigned>(a_rows) * kBK * 2;
   p.m_group = kMGroup;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return launch_gemm(part_ent != nullptr ? linear_partials_kernel<true> : linear_partials_kernel<false>, mh, mw, p, s);
+  return launch_gemm(part_ent != nullptr ? linear_partials_kernel<true> : linear_partials_kernel<false>, mh, mw, mw,
+                     p, s);
 }
 
 int bil_linear_logp_workspace_bytes(int64_t n_rows, int64_t vocab, int entropy, int64_t* bytes) {
