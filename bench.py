@@ -657,7 +657,37 @@ def linear_measurement(bil, stream, dev, steps: int = 5):
         out[f"{name}_ms"] = ms[name]
         out[f"{name}_tflops"] = flops / (ms[name] / 1e3) / 1e12
     out["merge_ms"] = ms["merge"]
-    del state, pm, ps, x, wt
+
+    # The same step with the forward's float32 logits kept for the backward (keep_logits): dZ by the
+    # logits path's backward from them instead of a recomputing GEMM; the same bits, 4 bytes per row
+    # and vocabulary column held from the forward to the backward.
+    ws = torch.empty(bil.linear.workspace_bytes(n, v), dtype=torch.uint8, device=dev)
+
+    def fwd_keep():
+        state["lp"], state["lse"], state["logits"] = bil.linear_logp(x, wt, t, workspace=ws, return_logits=True,
+                                                                     logits_dtype=torch.float32)
+
+    def bwd_keep():
+        state["dh"], state["dw"] = bil.linear.linear_logp_bwd_from_logits(x, wt, t, state["logits"], state["lse"], g)
+    keep_seq = [("forward", fwd_keep), ("backward", bwd_keep)]
+    for _ in range(2):
+        for _, f in keep_seq:
+            f()
+    torch.cuda.synchronize(dev)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        kev[i][0].record(stream)
+        for j, (_, f) in enumerate(keep_seq):
+            f()
+            kev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    k_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in kev)
+    k_bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in kev)
+    out["keep_logits"] = {"step_ms": k_fwd + k_bwd, "rows_per_s": n / ((k_fwd + k_bwd) / 1e3), "fwd_ms": k_fwd,
+                          "bwd_ms": k_bwd, "logits_bytes": n * v * 4, "gemms": 3,
+                          "how": "linear_logp(return_logits=True, float32) + linear_logp_bwd_from_logits; the same "
+                                 "bits as the recomputing backward"}
+    del state, pm, ps, x, wt, ws
     return out
 
 

@@ -273,6 +273,28 @@ __device__ __forceinline__ void unit_coords(int64_t u, int num_m, int num_n, int
   m = m0 + (r - n * gm);
 }
 
+// A warp hands one 2 KB box (32 rows of 64 bytes: 32 16-bit or 16 float32
+// values per row) to TMA: each lane writes its row's four 16-byte words into
+// the warp's next staging buffer (two, used in turn), and lane 0 stores the
+// box at (column x, row y) of `map` once the store that used the buffer before
+// has read it.  `issued` counts the warp's boxes.
+__device__ __forceinline__ void store_box(unsigned char* staging, const CUtensorMap* map, int x, int y, int lane,
+                                          uint32_t& issued, const uint32_t (&w)[16]) {
+  unsigned char* box = staging + (issued & 1u) * kStoreBoxBytes;
+  if (lane == 0) bulk_wait_read_1();
+  __syncwarp();
+  uint4* dst = reinterpret_cast<uint4*>(box + lane * 64);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  fence_proxy_async_smem();  // the writes above, before the bulk copy reads them
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, x, y, box);
+    bulk_commit();
+  }
+  ++issued;
+}
+
 // ---------------------------------------------------------------------------
 // The epilogue of one row of one tile: the tile partial of the operator, over
 // the tile's valid columns [0, vcols), from the float32 accumulator acc.
@@ -290,10 +312,16 @@ __device__ __forceinline__ void unit_coords(int64_t u, int num_m, int num_n, int
 // warp butterfly: a tile here is one thread's row.
 // ---------------------------------------------------------------------------
 
+// With `box_map` (the logits' store map), the logits go out through the warp's
+// staging boxes with TMA (all 32 lanes of the warp call this together; `store`
+// and out_row are then unused, and rows or columns past the matrix are not
+// written); else `store` rows write them with vector stores.
 template <bool ENT>
 __device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp, int64_t tloc, bool store,
                                             unsigned char* out_row, int out_dtype, float& m_out, float& s_out,
-                                            float& u_out, float& tl_out) {
+                                            float& u_out, float& tl_out, const CUtensorMap* box_map = nullptr,
+                                            unsigned char* staging = nullptr, int box_x = 0, int box_y = 0,
+                                            int lane = 0, uint32_t* issued = nullptr) {
   uint32_t r[kChunk];
   float mx = -INFINITY;  // max of the unscaled accumulator
   float tl = 0.0f;
@@ -306,7 +334,26 @@ __device__ __forceinline__ void row_partial(uint32_t taddr, int vcols, float rcp
       if (c0 + j < vcols) mx = fmaxf(mx, acc);
       if (c0 + j == tloc) tl = __fmul_rn(acc, rcp);
     }
-    if (store && c0 < vcols) {
+    if (box_map != nullptr && c0 < vcols) {
+      if (out_dtype == BIL_F32) {  // two boxes of 16 columns
+        uint32_t w0[16], w1[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          w0[j] = r[j];
+          w1[j] = r[16 + j];
+        }
+        store_box(staging, box_map, box_x + c0, box_y, lane, *issued, w0);
+        store_box(staging, box_map, box_x + c0 + 16, box_y, lane, *issued, w1);
+      } else {
+        uint32_t pk16[kChunk / 2];
+#pragma unroll
+        for (int j = 0; j < kChunk; j += 2) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+          pk16[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        store_box(staging, box_map, box_x + c0, box_y, lane, *issued, pk16);
+      }
+    } else if (store && c0 < vcols) {
       if (out_dtype == BIL_F32) {
         float* o = reinterpret_cast<float*>(out_row) + c0;
         if (c0 + kChunk <= vcols) {
@@ -471,23 +518,11 @@ __device__ __forceinline__ void row_grad_tma(uint32_t taddr, int vcols, float rc
       if (bad_target) v = __int_as_float(0x7fc00000);
       d[j] = v;
     }
-    unsigned char* box = staging + (issued & 1u) * kStoreBoxBytes;
-    if (lane == 0) bulk_wait_read_1();  // the store that used this buffer two boxes ago has read it
-    __syncwarp();
     uint32_t pk16[kChunk / 2];
 #pragma unroll
     for (int j = 0; j < kChunk; j += 2)
       pk16[j / 2] = static_cast<uint32_t>(to16<DT>(d[j])) | (static_cast<uint32_t>(to16<DT>(d[j + 1])) << 16);
-    uint4* dst = reinterpret_cast<uint4*>(box + lane * (kStoreBox * 2));
-#pragma unroll
-    for (int j = 0; j < kChunk / 8; ++j) dst[j] = make_uint4(pk16[4 * j], pk16[4 * j + 1], pk16[4 * j + 2], pk16[4 * j + 3]);
-    fence_proxy_async_smem();  // the writes above, before the bulk copy reads them
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(map, x0 + c0, y0, box);
-      bulk_commit();
-    }
-    ++issued;
+    store_box(staging, map, x0 + c0, y0, lane, issued, pk16);
   }
 }
 
@@ -812,10 +847,22 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
         if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
         tc_fence_after();
         float mt, st, ut = 0.0f, tl;
+#if BIL_GRAD_TMA_STORE
+        if (p.logits != nullptr) {  // the logits through the warp's staging boxes with TMA
+          unsigned char* staging = reinterpret_cast<unsigned char*>(
+                                       (reinterpret_cast<uintptr_t>(&sm + 1) + 1023) & ~static_cast<uintptr_t>(1023)) +
+                                   q * 2 * kStoreBoxBytes;
+          row_partial<ENT>(taddr, vcols, p.rcp, tloc, false, nullptr, p.logits_dtype, mt, st, ut, tl, &tmap_out,
+                           staging, static_cast<int>(col0), static_cast<int>(m * kBM + q * 32), lane, &store_boxes);
+        } else {
+          row_partial<ENT>(taddr, vcols, p.rcp, tloc, false, nullptr, p.logits_dtype, mt, st, ut, tl);
+        }
+#else
         const bool store = valid && p.logits != nullptr;
         unsigned char* out_row =
             store ? p.logits + (row * p.ld_logits + col0) * (p.logits_dtype == BIL_F32 ? 4 : 2) : nullptr;
         row_partial<ENT>(taddr, vcols, p.rcp, tloc, store, out_row, p.logits_dtype, mt, st, ut, tl);
+#endif
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
@@ -873,7 +920,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
       }
     }
     // the staging boxes stay in use until their stores have completed
-    if (MODE == kModeGrad && BIL_GRAD_TMA_STORE && lane == 0 && store_boxes != 0) bulk_wait_all();
+    if (BIL_GRAD_TMA_STORE && lane == 0 && store_boxes != 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -969,18 +1016,21 @@ int make_map(CUtensorMap* map, const void* ptr, int dtype, int64_t rows, int64_t
   return r == CUDA_SUCCESS ? BIL_OK : BIL_E_CUDA;
 }
 
-// The tensor map the gradient pass stores dZ [rows, cols] (row stride ld
-// elements, 16-bit) through: boxes of kStoreBox x kStoreBox elements, no
-// swizzle (a box in shared memory is row-major, 64-byte rows).
+// The tensor map an epilogue stores a [rows, cols] output (row stride ld
+// elements) through from the warps' staging boxes: 32 rows of 64 bytes, i.e.
+// 32 columns of a 16-bit type or 16 of float32, no swizzle (a box in shared
+// memory is row-major).
 int make_store_map(CUtensorMap* map, void* ptr, int dtype, int64_t rows, int64_t cols, int64_t ld) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return BIL_E_CUDA;
+  const int eb = dtype == BIL_F32 ? 4 : 2;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStoreBox), static_cast<cuuint32_t>(kStoreBox)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * eb};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / eb), static_cast<cuuint32_t>(kStoreBox)};
   const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      dtype == BIL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = dtype == BIL_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dtype == BIL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUresult r = fn(map, dt, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? BIL_OK : BIL_E_CUDA;
@@ -1323,7 +1373,11 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
   p.a_box_bytes = static_cast<unsigned>(a_rows) * kBK * 2;
   p.m_group = kMGroup;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return launch_gemm(part_ent != nullptr ? linear_partials_kernel<true> : linear_partials_kernel<false>, mh, mw, mw,
+  CUtensorMap mo = mw;
+  if (BIL_GRAD_TMA_STORE && logits != nullptr) {
+    if (int st = make_store_map(&mo, logits, logits_dtype, n_rows, shard_cols, ld_logits)) return st;
+  }
+  return launch_gemm(part_ent != nullptr ? linear_partials_kernel<true> : linear_partials_kernel<false>, mh, mw, mo,
                      p, s);
 }
 

@@ -20,7 +20,7 @@ import ctypes
 import torch
 
 from . import _lib
-from .logp import IGNORE_INDEX, _need_cuda, _ptr, _stream
+from .logp import IGNORE_INDEX, _need_cuda, _ptr, _stream, logp_bwd
 
 LINEAR_TILE_V = _lib.LINEAR_TILE_V
 _IN_DTYPES = {torch.bfloat16: _lib.BF16, torch.float16: _lib.F16}
@@ -269,39 +269,85 @@ def gemm_nt(a: torch.Tensor, b: torch.Tensor, out_dtype: torch.dtype = torch.flo
     return matmul(a, b.t(), out_dtype)
 
 
+def linear_logp_bwd_from_logits(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torch.Tensor,
+                                logits: torch.Tensor, lse: torch.Tensor, grad_logp: torch.Tensor,
+                                ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                                entropy: torch.Tensor | None = None, grad_entropy: torch.Tensor | None = None,
+                                out_dtype: torch.dtype | None = None):
+    """(dhidden [N, H], dweight [V, H]) like ``linear_logp_bwd``, from the forward's float32
+    logits [N, V] (``linear_logp(..., return_logits=True, logits_dtype=torch.float32)``)
+    instead of recomputing the projection: dZ by the logits path's backward on the stored
+    logits, then the two products.  The same bits as ``linear_logp_bwd``; the logits cost
+    4 bytes per row and vocabulary column while they are kept."""
+    _need_cuda(hidden, weight, target_ids, logits, lse, grad_logp, entropy, grad_entropy)
+    h2, w2 = _matrix(hidden, "hidden"), _matrix(weight, "weight")
+    if logits.dtype != torch.float32 or logits.dim() != 2 or logits.shape != (h2.shape[0], w2.shape[0]):
+        raise ValueError("logits must be the forward's float32 [N, V] projection")
+    n, v = logits.shape
+    dz = torch.empty((n, _pad8(v)), dtype=h2.dtype, device=h2.device)[:, :v]
+    logp_bwd(logits, target_ids.reshape(-1), lse.reshape(-1), grad_logp.reshape(-1), ignore_index, out=dz,
+             temperature=temperature, entropy=None if entropy is None else entropy.reshape(-1),
+             grad_entropy=None if grad_entropy is None else grad_entropy.reshape(-1))
+    out_dtype = h2.dtype if out_dtype is None else out_dtype
+    return matmul(dz, w2, out_dtype), matmul(dz.t(), h2, out_dtype)
+
+
 class LinearLogp(torch.autograd.Function):
     """Fused LM-head + logp with the autograd actor path: the forward keeps only
-    lse (and the entropy); the backward recomputes the projection tiles."""
+    lse (and the entropy), and the backward recomputes the projection tiles; or,
+    with ``keep_logits``, the forward also keeps its float32 logits and the
+    backward starts from them (the same bits, one GEMM fewer, 4 bytes per row and
+    vocabulary column kept until the backward)."""
 
     @staticmethod
-    def forward(ctx, hidden, weight, target_ids, ignore_index, temperature, return_entropy):
-        res = linear_logp(hidden, weight, target_ids, ignore_index, temperature, return_entropy)
-        ctx.save_for_backward(hidden, weight, target_ids, *res[1:])
+    def forward(ctx, hidden, weight, target_ids, ignore_index, temperature, return_entropy, keep_logits=False):
+        lead = hidden.shape[:-1]
+        if keep_logits:
+            res = linear_logp(hidden.reshape(-1, hidden.shape[-1]), weight, target_ids.reshape(-1), ignore_index,
+                              temperature, return_entropy, return_logits=True, logits_dtype=torch.float32)
+            logits = res[-1]
+            res = tuple(r.reshape(lead) for r in res[:-1])
+            ctx.save_for_backward(hidden, weight, target_ids, logits, *res[1:])
+        else:
+            res = linear_logp(hidden, weight, target_ids, ignore_index, temperature, return_entropy)
+            ctx.save_for_backward(hidden, weight, target_ids, *res[1:])
         ctx.ignore_index, ctx.temperature, ctx.return_entropy = ignore_index, temperature, return_entropy
+        ctx.keep_logits = keep_logits
         ctx.mark_non_differentiable(res[1])
         return res
 
     @staticmethod
     def backward(ctx, grad_logp, grad_lse, *rest):
-        hidden, weight, target_ids, lse, *ent = ctx.saved_tensors
+        saved = list(ctx.saved_tensors)
+        hidden, weight, target_ids = saved[:3]
+        logits = saved[3] if ctx.keep_logits else None
+        lse, *ent = saved[4:] if ctx.keep_logits else saved[3:]
         g = torch.zeros_like(lse) if grad_logp is None else grad_logp
         entropy = grad_entropy = None
         if ctx.return_entropy and rest and rest[0] is not None:
             entropy, grad_entropy = ent[0], rest[0]
         need_h, need_w = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        nones = (None,) * 5
         if not (need_h or need_w):
-            return None, None, None, None, None, None
-        dh, dw = linear_logp_bwd(hidden, weight, target_ids, lse, g, ctx.ignore_index, ctx.temperature,
-                                 entropy, grad_entropy)
-        return dh if need_h else None, dw if need_w else None, None, None, None, None
+            return (None, None) + nones
+        if logits is not None:
+            dh, dw = linear_logp_bwd_from_logits(hidden, weight, target_ids, logits, lse, g, ctx.ignore_index,
+                                                 ctx.temperature, entropy, grad_entropy)
+            dh = dh.reshape(hidden.shape)
+        else:
+            dh, dw = linear_logp_bwd(hidden, weight, target_ids, lse, g, ctx.ignore_index, ctx.temperature,
+                                     entropy, grad_entropy)
+        return (dh if need_h else None, dw if need_w else None) + nones
 
 
 def batch_invariant_linear_logp(hidden: torch.Tensor, weight: torch.Tensor, target_ids: torch.Tensor,
                                 ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
-                                return_entropy: bool = False):
+                                return_entropy: bool = False, keep_logits: bool = False):
     """Differentiable fused LM-head + logp: logp (and the entropy when asked) with
-    gradients for hidden and weight."""
-    res = LinearLogp.apply(hidden, weight, target_ids, ignore_index, temperature, return_entropy)
+    gradients for hidden and weight.  ``keep_logits`` trades 4 bytes per row and
+    vocabulary column, kept from the forward to the backward, for the backward's
+    recomputation of the projection (the same bits)."""
+    res = LinearLogp.apply(hidden, weight, target_ids, ignore_index, temperature, return_entropy, keep_logits)
     return (res[0], res[2]) if return_entropy else res[0]
 
 

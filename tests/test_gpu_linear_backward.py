@@ -179,6 +179,44 @@ def test_autograd_matches_the_c_abi():
     assert torch.equal(wd.grad.view(torch.int16), dw.contiguous().view(torch.int16))
 
 
+@pytest.mark.parametrize("dtype,temp,entropy,lead", [("bfloat16", 0.9, True, (200,)), ("float16", 1.0, False, (4, 50)),
+                                                   ("bfloat16", 1.0, False, (300,))])
+def test_keeping_the_logits_gives_the_recomputing_backwards_bits(dtype, temp, entropy, lead):
+    """keep_logits: the forward keeps its float32 logits and the backward starts from them
+    (the logits path's backward for dZ, then the two products) instead of recomputing the
+    projection; the gradients have the same bits, through autograd and through the call."""
+    n = int(np.prod(lead))
+    h, v = 192, 900
+    x, w, t, g, gh = make_case(n, h, v, seed=8, entropy=True, dtype=dtype)
+    grads = []
+    for keep in (False, True):
+        xd = device_logits(x, dtype).reshape(*lead, h).requires_grad_(True)
+        wd = device_logits(w, dtype).requires_grad_(True)
+        td = torch.from_numpy(t).cuda().reshape(lead)
+        gd, ghd = torch.from_numpy(g).cuda().reshape(lead), torch.from_numpy(gh).cuda().reshape(lead)
+        if entropy:
+            logp, ent = bil.batch_invariant_linear_logp(xd, wd, td, temperature=temp, return_entropy=True,
+                                                        keep_logits=keep)
+            ((logp * gd).sum() + (ent * ghd).sum()).backward()
+        else:
+            logp = bil.batch_invariant_linear_logp(xd, wd, td, temperature=temp, keep_logits=keep)
+            (logp * gd).sum().backward()
+        grads.append((f32_bits(logp), xd.grad.contiguous().view(torch.int16).clone(),
+                      wd.grad.contiguous().view(torch.int16).clone()))
+    torch.cuda.synchronize()
+    assert np.array_equal(grads[0][0], grads[1][0])
+    assert torch.equal(grads[0][1], grads[1][1])
+    assert torch.equal(grads[0][2], grads[1][2])
+    xd, wd = device_logits(x, dtype), device_logits(w, dtype)
+    td, gd = torch.from_numpy(t).cuda(), torch.from_numpy(g).cuda()
+    lp, lse, logits = bil.linear_logp(xd, wd, td, temperature=temp, return_logits=True, logits_dtype=torch.float32)
+    dh, dw = bil.linear.linear_logp_bwd_from_logits(xd, wd, td, logits, lse, gd, temperature=temp)
+    dh2, dw2 = bil.linear_logp_bwd(xd, wd, td, lse, gd, temperature=temp)
+    torch.cuda.synchronize()
+    assert torch.equal(dh.contiguous().view(torch.int16), dh2.contiguous().view(torch.int16))
+    assert torch.equal(dw.contiguous().view(torch.int16), dw2.contiguous().view(torch.int16))
+
+
 def test_full_size_sampled_rows_and_the_bilinear_identity():
     """Qwen3-8B-shaped LM head over 16384 rows: four sampled dhidden rows against the
     oracle (a row's dhidden depends on that row only), and <dX, X> = <dW, W> for the
