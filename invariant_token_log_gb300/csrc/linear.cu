@@ -19,7 +19,9 @@
 //               four K=16 steps each; two accumulator buffers of 256 columns;
 //   warps 2-5   epilogue: thread i of the warp reading lanes [32q, 32q+32)
 //               owns row 32q+i of the tile and reads its 256 columns from
-//               tensor memory;
+//               tensor memory; a large output (dZ, the optional logits) goes
+//               out 32 rows x 64 bytes at a time through two staging boxes
+//               of the warp's own and TMA stores;
 //   warp 6      the store GEMMs' lockstep service (see lockstep_service).
 // The accumulator of one tile is read while the next tile's MMAs run.  Three
 // epilogues make three kernels:
@@ -101,16 +103,17 @@ struct alignas(8) LinearSmem {
   int sync_done;
 };
 
-// The gradient pass stores dZ through shared memory with TMA (1) or with
-// per-thread vector stores (0).
-#ifndef BIL_GRAD_TMA_STORE
-#define BIL_GRAD_TMA_STORE 1
+// The epilogues that store a large output (the gradient pass's dZ, the
+// forward's optional logits) hand it to TMA through per-warp staging boxes in
+// shared memory (1), or store it with per-thread vector stores (0).
+#ifndef BIL_EPILOGUE_TMA_STORE
+#define BIL_EPILOGUE_TMA_STORE 1
 #endif
 constexpr int kStoreBox = 32;  // rows and columns of one dZ store box: a warp's rows, one TMEM chunk
 constexpr uint32_t kStoreBoxBytes = kStoreBox * kStoreBox * 2;           // 2 KB of 16-bit elements
-constexpr size_t kStagingBytes = BIL_GRAD_TMA_STORE ? 4 * 2 * kStoreBoxBytes : 0;  // 4 warps x 2 buffers
+constexpr size_t kStagingBytes = BIL_EPILOGUE_TMA_STORE ? 4 * 2 * kStoreBoxBytes : 0;  // 4 warps x 2 buffers
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * size_t(kStageBytes) + sizeof(LinearSmem) +
-                              (BIL_GRAD_TMA_STORE ? 1024 + kStagingBytes : 0);
+                              (BIL_EPILOGUE_TMA_STORE ? 1024 + kStagingBytes : 0);
 
 // What the epilogue warps do with a finished accumulator tile.
 enum EpilogueMode {
@@ -847,7 +850,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
         if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
         tc_fence_after();
         float mt, st, ut = 0.0f, tl;
-#if BIL_GRAD_TMA_STORE
+#if BIL_EPILOGUE_TMA_STORE
         if (p.logits != nullptr) {  // the logits through the warp's staging boxes with TMA
           unsigned char* staging = reinterpret_cast<unsigned char*>(
                                        (reinterpret_cast<uintptr_t>(&sm + 1) + 1023) & ~static_cast<uintptr_t>(1023)) +
@@ -890,7 +893,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
         const int64_t tloc = active ? meta.target - gcol0 : -1;
         if (!warp_wait_watch(&sm.acc_full[b], use & 1u, abort, kWatchAccFull, &g_watchdog_linear)) break;
         tc_fence_after();
-#if BIL_GRAD_TMA_STORE
+#if BIL_EPILOGUE_TMA_STORE
         unsigned char* staging = reinterpret_cast<unsigned char*>(
                                      (reinterpret_cast<uintptr_t>(&sm + 1) + 1023) & ~static_cast<uintptr_t>(1023)) +
                                  q * 2 * kStoreBoxBytes;
@@ -920,7 +923,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmap_hidden, const 
       }
     }
     // the staging boxes stay in use until their stores have completed
-    if (BIL_GRAD_TMA_STORE && lane == 0 && store_boxes != 0) bulk_wait_all();
+    if (BIL_EPILOGUE_TMA_STORE && lane == 0 && store_boxes != 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -1239,7 +1242,7 @@ int launch_grad(const CUtensorMap& mh, const CUtensorMap& mw, int dtype, int64_t
   GemmKernel k = dtype == BIL_BF16 ? (ent ? linear_grad_kernel<true, BIL_BF16> : linear_grad_kernel<false, BIL_BF16>)
                                    : (ent ? linear_grad_kernel<true, BIL_F16> : linear_grad_kernel<false, BIL_F16>);
   CUtensorMap mdz = mw;
-  if (BIL_GRAD_TMA_STORE) {
+  if (BIL_EPILOGUE_TMA_STORE) {
     if (int st = make_store_map(&mdz, dz, dtype, n_rows, cols, ld_dz)) return st;
   }
   return launch_gemm(k, mh, mw, mdz, p, s);
@@ -1374,7 +1377,7 @@ int bil_linear_logp_partials(const void* hidden, const void* weight, int dtype, 
   p.m_group = kMGroup;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   CUtensorMap mo = mw;
-  if (BIL_GRAD_TMA_STORE && logits != nullptr) {
+  if (BIL_EPILOGUE_TMA_STORE && logits != nullptr) {
     if (int st = make_store_map(&mo, logits, logits_dtype, n_rows, shard_cols, ld_logits)) return st;
   }
   return launch_gemm(part_ent != nullptr ? linear_partials_kernel<true> : linear_partials_kernel<false>, mh, mw, mo,
