@@ -563,14 +563,15 @@ __device__ __forceinline__ void row_store(uint32_t taddr, int vcols, bool valid,
 // vocabulary for dhidden), and the blocks of one wave read the same A and B
 // tiles at the same K position: when they drift apart by more K blocks than
 // L2 holds for the wave, the tiles they share come from DRAM again for every
-// block that reads them late (45 GB of DRAM reads for dhidden's 5 GB of dZ
-// and 1.2 GB of W^T at 16384 x 151936 x 4096, against 27 GB in step).
+// block that reads them late (with one-half units at 16384 x 151936 x 4096:
+// 46 GB of DRAM reads for dhidden's 5 GB of dZ and 1.2 GB of weight, against
+// 27 GB in step).
 //
 // A service warp per block (kSyncWarp) publishes, every few microseconds,
 // how many K blocks its copy thread has issued (in a 128-byte line of its
-// own), reads every block's position,
-// and tells its copy thread in shared memory how far it may go: kSyncLead K
-// blocks past the slowest block of the same launch.  The copy thread only
+// own), reads every block's position, and tells its copy thread in shared
+// memory how far it may go: kSyncLead K blocks past the slowest block of
+// the same launch.  The copy thread only
 // reads that bound, so the polling stays off its path.  Positions are tagged
 // with a per-launch number, so stale entries of other launches count for
 // nothing; a block that has issued all its copies publishes the largest
@@ -1185,9 +1186,10 @@ int launch_store(const CUtensorMap& ma, const CUtensorMap& mb, int64_t a_rows, i
   const int64_t total = static_cast<int64_t>(p.num_m) * p.num_n;
   const int64_t grid = std::min<int64_t>(total, sms);
   const int64_t iters = (total + grid - 1) / grid * p.k_blocks;  // K blocks one block issues
-  // Only units of a long K drift apart far enough to matter (measured on 16384 x 151936 x 4096: dhidden,
-  // K = 151936, read 46 GB of DRAM alone and 27 GB in step, 5% faster; dweight, K = 16384, read 26 GB
-  // either way and was 1% slower in step).
+  // Only units of a long K drift apart far enough to matter (measured on 16384 x 151936 x 4096 with
+  // one-half units: dhidden, K = 151936, read 46 GB of DRAM alone and 27 GB in step, 5% faster; dweight,
+  // K = 16384, read 26 GB either way and was 1% slower in step; with two-half units dweight in step
+  // read the same 17.8 GB in the same time).
   p.sync_tag = BIL_STORE_LOCKSTEP && p.k_blocks >= kSyncMinKBlocks && grid <= kSyncMaxBlocks &&
                        iters + kSyncLead < INT32_MAX
                    ? next_sync_tag()
