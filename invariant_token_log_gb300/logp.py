@@ -111,6 +111,16 @@ def _check_out(t: torch.Tensor, n: int, index: int, what: str) -> None:
         raise ValueError(f"{what} must be a contiguous float32 tensor of {n} elements on the logits' device")
 
 
+# torch.device objects by CUDA index: allocating with a device object skips
+# parsing an integer into one on every call.
+_DEVICE_OBJECTS: dict = {}
+
+
+def _device_object(index: int) -> torch.device:
+    dev = _DEVICE_OBJECTS[index] = torch.device("cuda", index)
+    return dev
+
+
 def _need_cuda(*ts: torch.Tensor) -> None:
     for t in ts:
         if t is not None and not t.is_cuda:
@@ -129,7 +139,9 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
     ``temperature`` divides the logits before the softmax (applied as a
     multiplication by the float32 reciprocal).
     """
-    if not (logits.is_cuda and target_ids.is_cuda):
+    index = logits.get_device()  # -1 for a CPU tensor
+    tindex = target_ids.get_device()
+    if index < 0 or tindex < 0:
         _need_cuda(logits, target_ids)
     shape = logits.shape
     tshape = target_ids.shape
@@ -140,15 +152,16 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
         # the general path's reshaping: the per-call host time is what bounds
         # small (decode-sized) batches.
         n, width = shape
-        index = logits.get_device()
-        if target_ids.get_device() != index:
+        if tindex != index:
             raise ValueError("target_ids must be on the logits' device")
+        if out is None or lse is None:
+            dev = _DEVICE_OBJECTS.get(index) or _device_object(index)
         if out is None:
-            out = torch.empty(n, dtype=torch.float32, device=index)
+            out = torch.empty(n, dtype=torch.float32, device=dev)
         else:
             _check_out(out, n, index, "out")
         if lse is None:
-            lse = torch.empty(n, dtype=torch.float32, device=index)
+            lse = torch.empty(n, dtype=torch.float32, device=dev)
         else:
             _check_out(lse, n, index, "lse")
         fn = _lib.load().bil_logp_fwd
