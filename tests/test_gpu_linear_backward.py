@@ -245,6 +245,24 @@ def test_full_size_sampled_rows_and_the_bilinear_identity():
     assert np.all(np.abs(got - rdx) <= bound)
 
 
+def test_full_size_keeping_the_logits_gives_the_recomputing_bits():
+    """The Qwen3-8B-shaped LM head over 16384 rows: the backward from the forward's kept
+    float32 logits (9.96 GB) and the recomputing backward give the same dhidden and dweight
+    bits (the dZ bits equal, and the same two products)."""
+    lw = wl.linear(16384)
+    xd = device_logits(lw.hidden, lw.dtype)
+    wd = device_logits(lw.weight, lw.dtype)
+    td = torch.from_numpy(lw.target_ids).cuda()
+    gd = torch.from_numpy(lw.grad_logp).cuda()
+    lp, lse, logits = bil.linear_logp(xd, wd, td, return_logits=True, logits_dtype=torch.float32)
+    dh, dw = bil.linear.linear_logp_bwd_from_logits(xd, wd, td, logits, lse, gd)
+    del logits
+    dh2, dw2 = bil.linear_logp_bwd(xd, wd, td, lse, gd)
+    torch.cuda.synchronize()
+    assert torch.equal(dh.contiguous().view(torch.int16), dh2.contiguous().view(torch.int16))
+    assert torch.equal(dw.contiguous().view(torch.int16), dw2.contiguous().view(torch.int16))
+
+
 def test_backward_edges():
     """No rows: dweight is zero.  An active row with an out-of-range target makes
     its dZ row NaN (and so its dhidden row); ignored rows are exactly zero."""
