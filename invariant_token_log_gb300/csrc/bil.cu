@@ -558,6 +558,19 @@ int bil_logp_merge(const float* part_max, const float* part_sum, const float* pa
   DeviceInfo dev;
   if (int st = device_info(&dev)) return st;
   const int threads = 256;  // merge_kernel's shared scratch has one slot per warp of 256 threads
+  // A few rows of many tiles: a block per row (the same bits, the partials' loads in one round).
+  const size_t block_smem = static_cast<size_t>(num_tiles) * (entropy != nullptr ? 4 : 2) * sizeof(float);
+  if (n_rows <= static_cast<int64_t>(dev.sms) && num_tiles >= kMergeBlockMinTiles && block_smem <= 48 * 1024) {
+    const cudaError_t e =
+        entropy != nullptr
+            ? launch_pdl(merge_block_kernel<true>, n_rows, threads, block_smem, s, 1, part_max, part_sum, part_ent,
+                         n_rows, num_tiles, ld_part, target_logit, target_ids, ignore_index, vocab, logp, lse, entropy)
+            : launch_pdl(merge_block_kernel<false>, n_rows, threads, block_smem, s, 1, part_max, part_sum,
+                         static_cast<const float*>(nullptr), n_rows, num_tiles, ld_part, target_logit, target_ids,
+                         ignore_index, vocab, logp, lse, static_cast<float*>(nullptr));
+    if (e != cudaSuccess) return BIL_E_CUDA;
+    return cudaGetLastError() == cudaSuccess ? BIL_OK : BIL_E_CUDA;
+  }
   const int64_t rows_per_block = threads / kLanes;
   const int64_t grid = std::max<int64_t>(
       1, std::min<int64_t>((n_rows + rows_per_block - 1) / rows_per_block, static_cast<int64_t>(dev.sms) * 8));

@@ -443,6 +443,9 @@ __device__ __forceinline__ TilePartial tile_reduce_smem(const unsigned char* til
 // Floats of shared scratch one warp's merge_lse uses (SCRATCH): four batch
 // columns of 32.
 constexpr int kMergeScratch = 4 * kLanes;
+// bil_logp_merge gives each row a block (merge_block_kernel) from this many tiles on, for batches of
+// at most one row per SM: the warp merge pays a load's latency per batch of 32 tiles.
+constexpr int kMergeBlockMinTiles = 128;
 
 // SCRATCH selects how the sequential chain is fed; both perform the same
 // operations in the same order.  SCRATCH = true: the batch after the current
@@ -1161,7 +1164,99 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
   }
 }
 
+// The same merge with one block per row, for a few rows of many tiles (the
+// fused LM-head's decode-sized batches: 594 tiles of 256).  The block loads
+// the row's partials and takes their exponentials in parallel into shared
+// memory (`sm`: T floats each of e_t and s_t, with ENT also of the clamped
+// m_t - M and of u_t), and one thread runs merge_lse's chains over them in the
+// same order with the same operations, so the bits are the warp merge's; the
+// loads' latency is paid once instead of once per batch of 32 tiles.
+template <bool ENT>
+__global__ void __launch_bounds__(256) merge_block_kernel(const float* __restrict__ part_max,
+                                                          const float* __restrict__ part_sum,
+                                                          const float* __restrict__ part_ent, int64_t n_rows,
+                                                          int num_tiles, int64_t ld_part,
+                                                          const float* __restrict__ target_logit,
+                                                          const int64_t* __restrict__ targets,
+                                                          int64_t ignore_index, int64_t vocab, float* logp,
+                                                          float* lse, float* entropy) {
+  extern __shared__ float sm[];
+  __shared__ float red[256 / kLanes];
+  __shared__ int red_nan[256 / kLanes];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int T = num_tiles;
+  const int lane = threadIdx.x % kLanes, warp = threadIdx.x / kLanes, nwarps = blockDim.x / kLanes;
+  float* se = sm;
+  float* ss = sm + T;
+  float* sd = sm + 2 * T;
+  float* su = sm + 3 * T;
+  for (int64_t row = blockIdx.x; row < n_rows; row += gridDim.x) {
+    const int64_t t = targets[row];
+    if (t == ignore_index) {
+      if (threadIdx.x == 0) {
+        logp[row] = 0.0f;
+        if (lse != nullptr) lse[row] = 0.0f;
+        if (ENT) entropy[row] = 0.0f;
+      }
+      continue;
+    }
+    const float* m = part_max + row * ld_part;
+    const float* s = part_sum + row * ld_part;
+    float mx = -INFINITY;  // exact: any order
+    for (int i = threadIdx.x; i < T; i += blockDim.x) mx = fmaxf(mx, m[i]);
+    mx = warp_max(mx);
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    float M = red[0];
+    for (int w = 1; w < nwarps; ++w) M = fmaxf(M, red[w]);
+    float L, H = 0.0f;
+    if (M == -INFINITY) {  // no finite logit: as merge_lse
+      bool nan = false;
+      for (int i = threadIdx.x; i < T; i += blockDim.x) nan |= isnan(s[i]);
+      nan = __any_sync(0xffffffffu, nan);
+      if (lane == 0) red_nan[warp] = nan ? 1 : 0;
+      __syncthreads();
+      int any = 0;
+      for (int w = 0; w < nwarps; ++w) any |= red_nan[w];
+      L = any ? __int_as_float(0x7fc00000) : -INFINITY;
+      H = __int_as_float(0x7fc00000);
+    } else {
+      for (int i = threadIdx.x; i < T; i += blockDim.x) {
+        const float dm = __fsub_rn(m[i], M);
+        se[i] = contract_exp(dm);
+        ss[i] = s[i];
+        if (ENT) {
+          sd[i] = fmaxf(dm, kNegMax);  // a tile of -inf (s_t = 0) then adds 0, not -inf * 0
+          su[i] = part_ent[row * ld_part + i];
+        }
+      }
+      __syncthreads();
+      L = 0.0f;
+      if (threadIdx.x == 0) {
+        float S = 0.0f, U = 0.0f;
+#pragma unroll 8
+        for (int i = 0; i < T; ++i) {
+          S = __fmaf_rn(ss[i], se[i], S);
+          if (ENT) U = __fmaf_rn(__fmaf_rn(sd[i], ss[i], su[i]), se[i], U);
+        }
+        const float logS = logf(S);
+        if (ENT) H = __fsub_rn(logS, __fdiv_rn(U, S));
+        L = __fadd_rn(M, logS);
+      }
+    }
+    if (threadIdx.x == 0) {
+      const bool valid = t >= 0 && t < vocab;
+      logp[row] = valid ? __fsub_rn(target_logit[row], L) : __int_as_float(0x7fc00000);
+      if (lse != nullptr) lse[row] = L;
+      if (ENT) entropy[row] = H;
+    }
+    __syncthreads();  // the shared arrays and `red` are free for the next row
+  }
+}
+
 // ---------------------------------------------------------------------------
+// Backward: dlogits[r, c] = g[r] * ([c == t_r] - exp(x[r, c] - lse[r])).// ---------------------------------------------------------------------------
 // Backward: dlogits[r, c] = g[r] * ([c == t_r] - exp(x[r, c] - lse[r])).
 // Work unit: (row, chunk of kBwdChunk columns), spread over a persistent grid.
 // Purely elementwise given lse and g, so the bits cannot depend on the unit
