@@ -141,6 +141,31 @@ def test_partials_against_oracle_and_fused(dtype):
     assert np.all(gs[~act] == 0) and np.all(gm[~act] == -np.inf)
 
 
+@pytest.mark.parametrize("entropy", [False, True])
+def test_merges_of_many_tiles_give_the_fused_bits_in_both_forms(entropy):
+    """594 tiles of 256 per row: up to one row per SM the merge gives each row a block
+    (partials loaded and exponentiated in parallel, one thread's chain), beyond that a warp
+    per row; both give the fused forward's bits, also with the entropy and a temperature."""
+    v, tile = 151936, 256
+    nt = -(-v // tile)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for n in (1, sms, sms + 1):
+        w = wl.random_rows(seed=12, n_rows=n, vocab=v, dtype="bfloat16", tile_v=tile, ignore_every=5)
+        x = device_logits(w.logits, "bfloat16")
+        t = torch.from_numpy(w.target_ids).cuda()
+        pm = torch.empty((n, nt), device="cuda")
+        ps = torch.empty((n, nt), device="cuda")
+        pe = torch.empty((n, nt), device="cuda") if entropy else None
+        tl = torch.full((n,), float("nan"), device="cuda")
+        temp = 0.8 if entropy else 1.0
+        bil.logp_tile_partials(x, t, v, tile, 0, nt, pm, ps, tl, w.ignore_index, temperature=temp, part_ent=pe)
+        split = bil.logp_merge(pm, ps, nt, tl, t, v, w.ignore_index, part_ent=pe)
+        fused = bil.logp_fwd(x, t, w.ignore_index, tile, temperature=temp, return_entropy=entropy)
+        torch.cuda.synchronize()
+        for a, b in zip(split, fused):
+            assert np.array_equal(f32_bits(a), f32_bits(b)), n
+
+
 def test_row_stride_padding_is_never_read():
     """Pad columns hold NaN; the results equal those of the unpadded rows bit for bit."""
     n, v = 9, 5000
