@@ -542,7 +542,7 @@ def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_byte
     # decode-sized batches: device time per forward call on the first N rows,
     # from a CUDA graph of 20 calls (so the host's per-call cost does not count),
     # and the same 20 calls issued one by one from Python (host-bound)
-    lat, eager, eager_pre = {}, {}, {}
+    lat, eager, eager_pre, eager_nolse = {}, {}, {}, {}
     for nd in (1, 2, 3, 7, 64, 128, 256):
         xs, ts = x[:nd], t[:nd]
         os_, ls_ = logp[:nd], lse[:nd]
@@ -550,7 +550,7 @@ def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_byte
             bil.logp_fwd(xs, ts, w.ignore_index, w.tile_v)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for res, kw in ((eager, {}), (eager_pre, {"out": os_, "lse": ls_})):
+        for res, kw in ((eager, {}), (eager_pre, {"out": os_, "lse": ls_}), (eager_nolse, {"with_lse": False})):
             e0.record(stream)
             for _ in range(20):
                 bil.logp_fwd(xs, ts, w.ignore_index, w.tile_v, **kw)
@@ -576,6 +576,7 @@ def secondary_measurements(bil, x, t, g, w, logp, lse, d, n, fwd_bytes, bwd_byte
     variants["decode_fwd_us_per_call_graph"] = lat
     variants["decode_fwd_us_per_call_python"] = eager
     variants["decode_fwd_us_per_call_python_preallocated"] = eager_pre
+    variants["decode_fwd_us_per_call_python_logp_only"] = eager_nolse  # with_lse=False: one allocation
     variants["prefill_fwd"] = prefill_measurement(bil, stream, dev)
     variants["sfu_exp"] = exp_rate_probe(dev, torch.cuda.get_device_properties(dev).multi_processor_count)
     variants["linear"] = linear_measurement(bil, stream, dev)

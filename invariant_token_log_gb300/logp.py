@@ -130,9 +130,12 @@ def _need_cuda(*ts: torch.Tensor) -> None:
 def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int = IGNORE_INDEX,
              tile_v: int = DEFAULT_TILE_V, validate: bool = False, vocab: int | None = None,
              out: torch.Tensor | None = None, lse: torch.Tensor | None = None, temperature: float = 1.0,
-             return_entropy: bool = False, entropy: torch.Tensor | None = None):
+             return_entropy: bool = False, entropy: torch.Tensor | None = None, with_lse: bool = True):
     """Selected-token log-probabilities: (logp, lse), both float32 with the targets' shape,
     and the row entropy as a third result when ``return_entropy`` (or ``entropy``) is given.
+
+    ``with_lse=False`` (inference, no backward to come) returns ``(logp, None)``: the
+    LSE is neither allocated nor written, and logp has the same bits.
 
     ``vocab`` (default: the last dimension) lets the row carry padding columns
     that are never read (e.g. a vocabulary padded to a multiple of the tile).
@@ -154,20 +157,22 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
         n, width = shape
         if tindex != index:
             raise ValueError("target_ids must be on the logits' device")
-        if out is None or lse is None:
+        if out is None or (lse is None and with_lse):
             dev = _DEVICE_OBJECTS.get(index) or _device_object(index)
         if out is None:
             out = torch.empty(n, dtype=torch.float32, device=dev)
         else:
             _check_out(out, n, index, "out")
-        if lse is None:
+        if not with_lse:
+            lse = None
+        elif lse is None:
             lse = torch.empty(n, dtype=torch.float32, device=dev)
         else:
             _check_out(lse, n, index, "lse")
         fn = _lib.load().bil_logp_fwd
         args = (logits.data_ptr(), _code(logits.dtype), n, width, width, target_ids.data_ptr(), int(ignore_index),
-                int(tile_v), float(temperature), out.data_ptr(), lse.data_ptr(), None, 1 if validate else 0,
-                _stream_handle(index))
+                int(tile_v), float(temperature), out.data_ptr(), None if lse is None else lse.data_ptr(), None,
+                1 if validate else 0, _stream_handle(index))
         st = fn(*args) if _get_device() == index else _on_device(index, fn, *args)
         if st:
             _lib.check("bil_logp_fwd", st)
@@ -191,7 +196,9 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
         out = torch.empty(n, dtype=torch.float32, device=device)
     else:
         _check_out(out, n, index, "out")
-    if lse is None:
+    if not with_lse:
+        lse = None
+    elif lse is None:
         lse = torch.empty(n, dtype=torch.float32, device=device)
     else:
         _check_out(lse, n, index, "lse")
@@ -202,12 +209,13 @@ def logp_fwd(logits: torch.Tensor, target_ids: torch.Tensor, ignore_index: int =
         _check_out(entropy, n, index, "entropy")
     st = _on_device(index, _lib.load().bil_logp_fwd, x2.data_ptr(), _code(x2.dtype), n, v, ld,
                     t1.data_ptr(), int(ignore_index), int(tile_v), float(temperature), out.data_ptr(),
-                    lse.data_ptr(), entropy.data_ptr() if want_ent else None, 1 if validate else 0,
-                    _stream_handle(index))
+                    None if lse is None else lse.data_ptr(), entropy.data_ptr() if want_ent else None,
+                    1 if validate else 0, _stream_handle(index))
     if st:
         _lib.check("bil_logp_fwd", st)
     if len(lead) != 1:
-        out, lse = out.reshape(lead), lse.reshape(lead)
+        out = out.reshape(lead)
+        lse = None if lse is None else lse.reshape(lead)
         if want_ent:
             entropy = entropy.reshape(lead)
     return (out, lse, entropy) if want_ent else (out, lse)

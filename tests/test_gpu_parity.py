@@ -166,6 +166,24 @@ def test_merges_of_many_tiles_give_the_fused_bits_in_both_forms(entropy):
             assert np.array_equal(f32_bits(a), f32_bits(b)), n
 
 
+def test_logp_without_the_lse_has_the_same_bits():
+    """with_lse=False (inference): no LSE is written or returned, logp keeps its bits, on the
+    lean path ([N, V], int64 targets) and the general one (a leading shape, the entropy)."""
+    w = wl.random_rows(seed=13, n_rows=24, vocab=50257, dtype="bfloat16", tile_v=4096, ignore_every=5)
+    x = device_logits(w.logits, "bfloat16")
+    t = torch.from_numpy(w.target_ids).cuda()
+    ref, _ = bil.logp_fwd(x, t, w.ignore_index)
+    lp, none = bil.logp_fwd(x, t, w.ignore_index, with_lse=False)
+    ref3, _, ent3 = bil.logp_fwd(x.reshape(4, 6, -1), t.reshape(4, 6), w.ignore_index, return_entropy=True)
+    lp3, none3, e3 = bil.logp_fwd(x.reshape(4, 6, -1), t.reshape(4, 6), w.ignore_index, return_entropy=True,
+                                  with_lse=False)
+    torch.cuda.synchronize()
+    assert none is None and none3 is None
+    assert np.array_equal(f32_bits(lp), f32_bits(ref))
+    assert np.array_equal(f32_bits(lp3), f32_bits(ref3))
+    assert np.array_equal(f32_bits(e3), f32_bits(ent3))
+
+
 def test_row_stride_padding_is_never_read():
     """Pad columns hold NaN; the results equal those of the unpadded rows bit for bit."""
     n, v = 9, 5000
